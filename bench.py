@@ -1,0 +1,457 @@
+#!/usr/bin/env python3
+"""Benchmark of split-KV paged GQA decode attention on GB300.
+
+One step = one ``attn_decode`` call (split kernel with the last-CTA merge)
+over one synthetic workload.  Default workload: the sliding-window multi-row
+decode (nh16 nkv8 hd256, ctx 8192, rows at qpos 8188..8191, window 1024).
+
+Prints ONE JSON line (rank 0).  ``value`` is KV GB/s: the call's algorithmic
+bytes (in-window KV + Q + O) over the device time per call, measured with CUDA
+events around a CUDA graph of exactly ``--steps`` back-to-back calls that
+rotate over enough pool copies that every call reads its KV from HBM.
+
+``--impl reference`` times the f64 CPU oracle instead (the only other place
+this file runs it is the ``cpu_baseline`` leg).
+
+Multi-GPU (torchrun): every rank runs the same workload on its own GPU (weak
+scaling, no collective on the data path); the job's value is all ranks' bytes
+over the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from paged_gqa_decode_attn_gb300 import workloads as wl  # noqa: E402
+
+METRIC = "paged decode attention KV GB/s and fraction of GB300 HBM peak; µs/call"
+L2_BYTES = 129 * 1024 * 1024
+KERNEL_SOURCES = ["paged_gqa_decode_attn_gb300/csrc/pgqa_device.cuh",
+                  "paged_gqa_decode_attn_gb300/csrc/pgqa_launch.cuh"]
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "decode_split_kernel_traffic.json")
+
+
+# ------------------------------------------------------------------ distributed helpers
+
+def dist_env():
+    return int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")), \
+        int(os.environ.get("LOCAL_RANK", "0"))
+
+
+def init_dist(world: int):
+    if world <= 1:
+        return None
+    import torch.distributed as dist
+    os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+    dist.init_process_group("gloo")
+    return dist
+
+
+def barrier(dist):
+    if dist is not None:
+        dist.barrier()
+
+
+def max_over_ranks(dist, x: float) -> float:
+    """Max of a host float over all ranks (gloo; host-side only)."""
+    if dist is None:
+        return x
+    import torch
+    t = torch.tensor([x], dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def sum_over_ranks(dist, x: float) -> float:
+    if dist is None:
+        return x
+    import torch
+    t = torch.tensor([x], dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+# ------------------------------------------------------------------ measured peaks, traffic, clocks
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+def kernel_sources_sha() -> str:
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload: str):
+    """dram bytes per launch from the committed ncu summary, or None if it is stale or absent."""
+    try:
+        with open(TRAFFIC_FILE) as f:
+            d = json.load(f)
+    except Exception:
+        return None
+    e = d.get(workload)
+    if not e or e.get("kernel_sources_sha256_16") != kernel_sources_sha():
+        return None
+    return float(e["dram_bytes_per_launch"])
+
+
+class ClockSampler:
+    """nvidia-smi samples (SM clock, throttle reasons) while the GPU works."""
+
+    FIELDS = ["timestamp", "clocks.sm", "clocks.max.sm", "power.draw", "clocks_event_reasons.hw_slowdown",
+              "clocks_event_reasons.hw_thermal_slowdown", "clocks_event_reasons.sw_thermal_slowdown",
+              "clocks_event_reasons.sw_power_cap"]
+
+    def __init__(self, device_index: int):
+        self.proc = None
+        self.lines = []
+        try:
+            import torch
+            ident = str(torch.cuda.get_device_properties(device_index).uuid)
+            ident = ident if ident.startswith("GPU-") else "GPU-" + ident
+        except Exception:
+            ident = str(device_index)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", ident, "--query-gpu=" + ",".join(self.FIELDS), "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        rows = [ln.split(", ") for ln in out.strip().splitlines() if ln.count(",") >= len(self.FIELDS) - 1]
+        mhz, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            try:
+                mhz.append(float(r[1]))
+                mx.append(float(r[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, r[4:8]):
+                if v.strip().lower() == "active":
+                    reasons.add(n)
+        if not mhz:
+            return None
+        busy = [m for m in mhz if m > 0.5 * max(mhz)]
+        return {"sm_mhz": statistics.median(busy), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(mhz), "window": "warm-up and timed steps"}
+
+
+# ------------------------------------------------------------------ workloads
+
+def build_case(name: str):
+    if name == "sliding":
+        return wl.sliding()
+    if name == "sliding_mapped":
+        return wl.sliding(mapped=True)
+    if name == "tiny":
+        return wl.tiny()
+    if name == "long":
+        return wl.long_ctx()
+    if name == "batched":
+        return wl.batched()
+    raise SystemExit(f"unknown workload {name}")
+
+
+def nseq_of(case) -> int:
+    return len(set(int(x) for x in case.off))
+
+
+# ------------------------------------------------------------------ the CPU oracle (baseline / reference arm)
+
+def oracle_rate(case, budget_s: float, steps: int | None = None, warmup: int = 0):
+    """Time the f64 oracle on ``case`` (all host cores).  With ``steps`` set,
+    each step is a bounded sample of (row, head) pairs sized so the whole run
+    takes about ``budget_s``; otherwise whole calls repeat for ``budget_s``.
+    Returns (GB/s, seconds per step, sample description, cores, pairs per step)."""
+    import oracle
+    cores = oracle.default_threads()
+    total_pairs = case.rows * case.nh
+    all_pairs = [(r, h) for r in range(case.rows) for h in range(case.nh)]
+    t0 = time.perf_counter()
+    oracle.decode_case(case, pairs=all_pairs[:min(total_pairs, max(cores, 1))], want_f64=False)
+    t_pair = max((time.perf_counter() - t0) / min(total_pairs, max(cores, 1)), 1e-7)
+    bytes_per_pair = case.algorithmic_bytes() / total_pairs
+    if steps is None:
+        n_calls, t_tot = 0, 0.0
+        while t_tot < budget_s or n_calls == 0:
+            t0 = time.perf_counter()
+            oracle.decode_case(case, want_f64=False)
+            t_tot += time.perf_counter() - t0
+            n_calls += 1
+        per = t_tot / n_calls
+        return (case.algorithmic_bytes() / per / 1e9, per,
+                f"{n_calls} whole calls ({total_pairs} (row, head) pairs each), {t_tot:.1f} s", cores, total_pairs)
+    per_step_budget = budget_s / max(steps + warmup, 1)
+    k = int(min(total_pairs, max(1, per_step_budget / t_pair * cores)))
+    k = max(1, min(k, total_pairs))
+    cursor = 0
+
+    def one():
+        nonlocal cursor
+        sel = [all_pairs[(cursor + i) % total_pairs] for i in range(k)]
+        cursor = (cursor + k) % total_pairs
+        oracle.decode_case(case, pairs=sel, want_f64=False)
+
+    for _ in range(warmup):
+        one()
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        one()
+    el = time.perf_counter() - t0
+    per = el / steps
+    return (bytes_per_pair * k / per / 1e9, per,
+            f"{k} of {total_pairs} (row, head) pairs per step, cycling", cores, k)
+
+
+def run_reference(args, case, rank, world):
+    gbs, per, sample, cores, k = oracle_rate(case, budget_s=args.ref_budget, steps=args.steps, warmup=args.warmup)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(gbs, 4), "unit": "GB/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": per * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": config_of(args, case, None),
+        "cpu_baseline": {"value": round(gbs, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": round(gbs, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def config_of(args, case, splits):
+    c = {"workload": case.name, "nh": case.nh, "nkv": case.nkv, "hd": case.hd, "ctx": case.ctx,
+         "rows": case.rows, "window": case.window, "pool": "page map + NaN null page" if case.page_map is not None
+         else "identity", "algorithmic_bytes_per_call": case.algorithmic_bytes()}
+    if splits is not None:
+        c["splits"] = splits
+        c["merge"] = "last-CTA counters" if args.merge == "counters" else "combine kernel"
+    return c
+
+
+# ------------------------------------------------------------------ our arm
+
+def run_ours(args, case, rank, world, dist):
+    import torch
+    import paged_gqa_decode_attn_gb300 as pgqa
+
+    torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
+    dev = torch.device("cuda")
+    if rank == 0:
+        pgqa.build()
+    barrier(dist)
+    pgqa.load()
+
+    bpc = case.algorithmic_bytes()
+    splits = args.splits or pgqa.choose_splits(case.kv_len_eff(), case.rows, case.nkv, nseq_of(case))
+    # enough pool copies that consecutive reads of one copy are > 3x L2 apart
+    pool_bytes = case.k_pool.nbytes + case.v_pool.nbytes
+    copies = max(2, math.ceil(3 * L2_BYTES / max(bpc, 1)))
+    copies = min(copies, max(2, int(0.25 * torch.cuda.get_device_properties(dev).total_memory // pool_bytes)))
+
+    def i16(a):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16))
+
+    def i32(a):
+        return None if a is None else torch.from_numpy(np.ascontiguousarray(a, dtype=np.int32))
+
+    k_host, v_host = i16(case.k_pool), i16(case.v_pool)
+    ks = [k_host.to(dev) for _ in range(copies)]
+    vs = [v_host.to(dev) for _ in range(copies)]
+    q_h = i16(case.q).pin_memory()
+    bt_h, off_h, qpos_h = i32(case.block_table).pin_memory(), i32(case.off).pin_memory(), i32(case.qpos).pin_memory()
+    q, bt, off, qpos = q_h.to(dev), bt_h.to(dev), off_h.to(dev), qpos_h.to(dev)
+    kvpos = None if case.kvpos is None else i32(case.kvpos).to(dev)
+    pm = None if case.page_map is None else i32(case.page_map).to(dev)
+    part = torch.empty(max(1, pgqa.decode_part_bytes(case.rows, case.nh, splits, case.hd)) // 4 + 4,
+                       dtype=torch.float32, device=dev)
+    cnt = torch.zeros(max(1, pgqa.decode_counter_count(case.rows, case.nh, case.nkv)), dtype=torch.int32,
+                      device=dev)
+    o = torch.empty(case.rows * case.nh * case.hd, dtype=torch.int16, device=dev)
+    o_h = torch.empty_like(o, device="cpu").pin_memory()
+    counters = cnt if args.merge == "counters" else None
+    launches_per_call = 1 if (splits == 1 or counters is not None) else 2
+
+    def call(i, stream=None):
+        pgqa.attn_decode(o, part, q, ks[i % copies], vs[i % copies], bt, off, qpos, kvpos, case.rows, case.nh,
+                         case.nkv, case.hd, case.window, splits, counters, pm, stream)
+
+    # spot check against the oracle on rank 0 (a few (row, head) pairs)
+    call(0)
+    torch.cuda.synchronize()
+    spot = None
+    if rank == 0 and not args.no_check:
+        import oracle
+        got = o.cpu().numpy().view(np.uint16).reshape(case.rows, case.nh, case.hd)
+        pairs = [(r, h) for r in range(case.rows) for h in range(case.nh)][:: max(1, case.rows * case.nh // 16)]
+        _, ref = oracle.decode_case(case, pairs=pairs, want_f64=False)
+        spot = oracle.rel_rms(np.stack([got[r, h] for r, h in pairs]), ref)
+        if not spot < 1e-2:
+            raise SystemExit(f"spot check against the oracle failed: rel_rms {spot}")
+
+    sampler = ClockSampler(torch.cuda.current_device()) if not args.no_clocks else None
+
+    # warm-up (eager), then graphs of back-to-back calls for the timed steps
+    for i in range(args.warmup):
+        call(i)
+    torch.cuda.synchronize()
+    chunk = max(1, min(args.steps, args.graph_chunk))
+    graphs = {}
+
+    def graph_for(n):
+        if n not in graphs:
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                for i in range(n):
+                    call(i)
+            graphs[n] = g
+        return graphs[n]
+
+    full, rem = divmod(args.steps, chunk)
+    g_full = graph_for(chunk) if full else None
+    g_rem = graph_for(rem) if rem else None
+    # a graph replay before timing settles the graphs' first-launch cost
+    (g_full or g_rem).replay()
+    torch.cuda.synchronize()
+
+    stream = torch.cuda.current_stream()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(dist)
+    torch.cuda.synchronize()
+    ev0.record(stream)
+    for _ in range(full):
+        g_full.replay()
+    if rem:
+        g_rem.replay()
+    ev1.record(stream)
+    ev1.synchronize()
+    torch.cuda.synchronize()
+    barrier(dist)
+    el_ms = ev0.elapsed_time(ev1)
+    clocks = sampler.stop() if sampler else None
+    el_max = max_over_ranks(dist, el_ms)
+    ms_per_step = el_max / args.steps
+    total_bytes = sum_over_ranks(dist, float(bpc) * args.steps)
+    value = total_bytes / (el_max * 1e-3) / 1e9
+    kernel_us = el_ms * 1e3 / args.steps / launches_per_call
+
+    # end to end through the public API from pinned host buffers: per step
+    # H2D of q, qpos, off and the block table, the call, D2H of o
+    e2e_steps = max(1, min(args.steps, args.e2e_steps))
+    h2d = q_h.nbytes + qpos_h.nbytes + off_h.nbytes + bt_h.nbytes
+    d2h = o_h.nbytes
+    barrier(dist)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for i in range(e2e_steps):
+        q.copy_(q_h, non_blocking=True)
+        qpos.copy_(qpos_h, non_blocking=True)
+        off.copy_(off_h, non_blocking=True)
+        bt.copy_(bt_h, non_blocking=True)
+        call(i)
+        o_h.copy_(o, non_blocking=True)
+    torch.cuda.synchronize()
+    e2e_s = max_over_ranks(dist, time.perf_counter() - t0)
+    e2e_value = sum_over_ranks(dist, float(bpc) * e2e_steps) / e2e_s / 1e9
+
+    if rank != 0:
+        return 0
+    peak, peak_kind = measured_peaks()
+    achieved = bpc / (kernel_us * 1e-6) / 1e9 if launches_per_call == 1 else None
+    traffic = recorded_traffic(case.name)
+    roofline = {"bound": "hbm", "achieved": round(achieved, 2) if achieved else None, "peak": peak,
+                "unit": "GB/s", "frac": round(achieved / peak, 4) if achieved else None,
+                "traffic": traffic, "peak_kind": peak_kind, "kernel": "decode_split_kernel",
+                "algorithmic_bytes_per_launch": bpc, "launch_us": round(kernel_us, 3)}
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        gbs, per, sample, cores, _ = oracle_rate(case, budget_s=args.cpu_budget)
+        cpu = {"value": round(gbs, 4), "unit": "GB/s", "cores": cores, "kind": "oracle", "sample": sample}
+    cfg = config_of(args, case, splits)
+    cfg["l2"] = (f"rotating {copies} pool copies ({copies * pool_bytes / 1e9:.2f} GB, "
+                 f"{copies * bpc / 1e6:.0f} MB of reads per rotation > 3x L2): every step reads KV from HBM")
+    cfg["timing"] = f"CUDA events around CUDA graphs of {chunk} back-to-back calls"
+    if spot is not None:
+        cfg["spot_check_rel_rms"] = spot
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "us_per_call": round(ms_per_step * 1e3, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": cfg, "roofline": roofline, "cpu_baseline": cpu,
+        "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "steps": e2e_steps, "us_per_step": round(e2e_s / e2e_steps * 1e6, 3),
+                "resident": "k_pool and v_pool stay in HBM (the KV cache); q, qpos, off, block table come from "
+                            "pinned host memory and o goes back every step"},
+        "gpu_launches": args.steps * launches_per_call, "clocks": clocks,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="sliding",
+                    choices=["sliding", "sliding_mapped", "tiny", "long", "batched"])
+    ap.add_argument("--splits", type=int, default=0, help="override choose_splits")
+    ap.add_argument("--merge", choices=["counters", "combine"], default="counters")
+    ap.add_argument("--graph-chunk", type=int, default=2000)
+    ap.add_argument("--e2e-steps", type=int, default=2000)
+    ap.add_argument("--cpu-budget", type=float, default=10.0, help="seconds of oracle work for cpu_baseline")
+    ap.add_argument("--ref-budget", type=float, default=60.0, help="seconds of oracle work for --impl reference")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-check", action="store_true")
+    ap.add_argument("--no-clocks", action="store_true")
+    args = ap.parse_args(argv)
+    if args.steps < 1 or args.warmup < 0:
+        raise SystemExit("--steps >= 1 and --warmup >= 0")
+    rank, world, _ = dist_env()
+    if args.impl == "reference" and rank != 0:
+        return 0            # the reference arm runs on rank 0 alone
+    case = build_case(args.workload)
+    if args.impl == "reference":
+        return run_reference(args, case, rank, world)
+    dist = init_dist(world)
+    try:
+        return run_ours(args, case, rank, world, dist)
+    finally:
+        if dist is not None:
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,130 @@
+/*
+ * pgqa — split-KV paged GQA decode attention for NVIDIA GB300 (sm_103a).
+ *
+ * C ABI of libpgqa.so.  Plain pointers and sizes only; every pointer named
+ * "device" must be a CUDA device (or managed) address on the current device,
+ * every other pointer is host memory.  The caller owns all buffers.
+ *
+ * The operation is the decode attention exercised by span-02
+ * `engine/crates/kernels/tests/gpu.rs` (`attn::attn_decode`,
+ * `attn::choose_splits`, `attn::decode_part_bytes` in its `run` function, and
+ * the f64 `reference` function that defines the result):
+ *
+ *   for every query row r and head h, kv head kh = h / (nh / nkv):
+ *     lo   = window > 0 ? max(0, qpos[r] + 1 - window) : 0
+ *     hi   = kvpos ? kvpos[r] : qpos[r]
+ *     o[r,h,:] = softmax_p( q[r,h,:] . K[p,kh,:] ) @ V[p,kh,:],  p in [lo, hi]
+ *
+ * with scale 1.0 (no 1/sqrt(hd)).  KV position p of row r is slot p % 16 of
+ * physical page  phys = block_table[off[r] + p / 16]  (then
+ * phys = page_map[phys] when page_map is given).  The pools are
+ * [page][nkv][16][hd] bf16, so the (page, kv head) tile is 16*hd contiguous
+ * elements.  A row with hi < lo has no visible position and gets zeros.
+ *
+ * Status codes: every function returning int returns PGQA_OK (0) or one of
+ * the negative PGQA_ERR_* codes below; pgqa_strerror() names them.
+ */
+#ifndef PGQA_H
+#define PGQA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define PGQA_OK 0
+#define PGQA_ERR_INVALID_ARGUMENT (-1)   /* null pointer, bad size, nh % nkv != 0, ... */
+#define PGQA_ERR_UNSUPPORTED_HD (-2)     /* hd not in {64, 128, 256, 512} */
+#define PGQA_ERR_MISALIGNED (-3)         /* a pool is not 16-byte aligned */
+#define PGQA_ERR_CUDA (-4)               /* a CUDA runtime call or launch failed */
+#define PGQA_ERR_TENSOR_MAP (-5)         /* the driver refused the TMA descriptor */
+#define PGQA_ERR_DEVICE_TIMEOUT (-6)     /* a kernel gave up a bounded wait (see pgqa_device_status) */
+#define PGQA_ERR_TOO_MANY_SPLITS (-7)    /* splits > PGQA_MAX_SPLITS */
+
+#define PGQA_PAGE_TOKENS 16
+#define PGQA_MAX_SPLITS 256
+
+/*
+ * Split-KV paged decode attention (`attn::attn_decode` of the test file
+ * above; the result is its f64 `reference`).
+ *
+ * Device buffers:
+ *   o           [rows][nh][hd] bf16, written (never read).
+ *   part        scratch of at least pgqa_decode_part_bytes(rows, nh, splits, hd)
+ *               bytes; contents need no initialisation and are dead after the
+ *               call.  May be NULL when splits == 1.
+ *   q           [rows][nh][hd] bf16.
+ *   k_pool,
+ *   v_pool      [npages][nkv][16][hd] bf16, 16-byte aligned.  Only the pages
+ *               holding positions [lo, hi] of some row are read, so pages wholly
+ *               outside every row's window may point anywhere, e.g. a NaN-filled
+ *               null page.  Slots of a read page outside every row's [lo, hi]
+ *               may hold any bits (NaN included): they never reach o.
+ *   block_table int32; row r's logical page j is block_table[off[r] + j].
+ *   off         [rows] int32, per-row start in block_table.
+ *   qpos        [rows] int32, query position of each row (>= 0).
+ *   kvpos       [rows] int32 last visible KV position, or NULL for kvpos = qpos.
+ *   counters    merge counters, NULL or at least
+ *               pgqa_decode_counter_count(rows, nh, nkv) uint32 slots.  Zero
+ *               them once before first use; every successful call leaves them
+ *               zero again.  Non-NULL: the last CTA of each tile merges the
+ *               split partials.  NULL: a separate combine kernel merges them.
+ *               Both give bit-identical o.
+ *   page_map    int32 map from block-table entries to physical pages, or NULL.
+ *
+ * Host scalars: rows >= 0, nh, nkv > 0 with nh % nkv == 0, hd in
+ * {64, 128, 256, 512}, window >= 0 (0 = full causal), 1 <= splits <=
+ * PGQA_MAX_SPLITS.  The output for a given (inputs, splits) does not depend on
+ * which physical pages hold the data.
+ *
+ * stream: a cudaStream_t (NULL = the legacy default stream).  The call only
+ * enqueues work: it never synchronises and never allocates.  Calls sharing
+ * `part` or `counters` must be ordered on the GPU (same stream or events).
+ */
+int pgqa_attn_decode(void *o, void *part, const void *q, const void *k_pool, const void *v_pool,
+                     const int32_t *block_table, const int32_t *off, const int32_t *qpos,
+                     const int32_t *kvpos, int rows, int nh, int nkv, int hd, int window,
+                     int splits, uint32_t *counters, const int32_t *page_map, void *stream);
+
+/*
+ * Number of KV splits per (row, kv head) tile (`attn::choose_splits` of the
+ * test file; its body is not given there, this rule is this library's own).
+ * kv_len_eff is the visible KV length, min(ctx, window) for sliding layers.
+ * rows and nseq are the query rows and the distinct sequences among them;
+ * nkv the kv heads.  Uses the current device's SM count.  Returns >= 1.
+ */
+int pgqa_choose_splits(int kv_len_eff, int rows, int nkv, int nseq);
+
+/* pgqa_choose_splits for an explicit SM count (pure host arithmetic). */
+int pgqa_choose_splits_for(int kv_len_eff, int rows, int nkv, int nseq, int num_sms);
+
+/*
+ * Bytes of the `part` scratch (`attn::decode_part_bytes` of the test file):
+ * rows * nh * splits * (hd + 2) * 4 (f32 O, running max and sum per split).
+ */
+size_t pgqa_decode_part_bytes(int rows, int nh, int splits, int hd);
+
+/* uint32 merge-counter slots one call needs: rows * nkv * ceil((nh / nkv) / 8). */
+size_t pgqa_decode_counter_count(int rows, int nh, int nkv);
+
+/*
+ * Reads and clears the device-side error word of the current device
+ * (synchronises the device).  Returns PGQA_OK, or PGQA_ERR_DEVICE_TIMEOUT if a
+ * kernel gave up one of its bounded waits since the last read; merge counters
+ * must then be zeroed again.
+ */
+int pgqa_device_status(void);
+
+/* Static, human-readable name of a status code. */
+const char *pgqa_strerror(int status);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+int pgqa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PGQA_H */

@@ -1,0 +1,120 @@
+"""ctypes binding of libpgqa.so (include/pgqa.h).  Argument marshalling only:
+every step of the decode runs in the library's CUDA kernels.  There is no CPU
+fallback: without the built library these functions raise."""
+from __future__ import annotations
+
+import ctypes
+import os
+
+from . import build as _build
+
+PGQA_OK = 0
+PGQA_ERR_INVALID_ARGUMENT = -1
+PGQA_ERR_UNSUPPORTED_HD = -2
+PGQA_ERR_MISALIGNED = -3
+PGQA_ERR_CUDA = -4
+PGQA_ERR_TENSOR_MAP = -5
+PGQA_ERR_DEVICE_TIMEOUT = -6
+PGQA_ERR_TOO_MANY_SPLITS = -7
+PAGE_TOKENS = 16
+MAX_SPLITS = 256
+
+# name -> (restype, argtypes)
+_P, _I = ctypes.c_void_p, ctypes.c_int
+SIGNATURES = {
+    "pgqa_attn_decode": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P, _P]),
+    "pgqa_choose_splits": (_I, [_I, _I, _I, _I]),
+    "pgqa_choose_splits_for": (_I, [_I, _I, _I, _I, _I]),
+    "pgqa_decode_part_bytes": (ctypes.c_size_t, [_I, _I, _I, _I]),
+    "pgqa_decode_counter_count": (ctypes.c_size_t, [_I, _I, _I]),
+    "pgqa_device_status": (_I, []),
+    "pgqa_strerror": (ctypes.c_char_p, [_I]),
+    "pgqa_version": (_I, []),
+}
+
+
+class PgqaError(RuntimeError):
+    def __init__(self, status: int, what: str = ""):
+        self.status = status
+        super().__init__(f"{what}: {strerror(status)} ({status})" if what else f"{strerror(status)} ({status})")
+
+
+_lib = None
+
+
+def lib_path() -> str:
+    return _build.LIB
+
+
+def load() -> ctypes.CDLL:
+    """Load libpgqa.so (it must have been built: ``paged_gqa_decode_attn_gb300.build.build()``)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(_build.LIB):
+            raise ImportError(f"libpgqa.so is not built ({_build.LIB}); run paged_gqa_decode_attn_gb300.build.build()")
+        lib = ctypes.CDLL(_build.LIB)
+        for name, (res, args) in SIGNATURES.items():
+            fn = getattr(lib, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = lib
+    return _lib
+
+
+def strerror(status: int) -> str:
+    return load().pgqa_strerror(int(status)).decode()
+
+
+def _ptr(x):
+    """A device/host pointer from a torch tensor, an int address, or None."""
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    return x.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def attn_decode(o, part, q, k_pool, v_pool, block_table, off, qpos, kvpos, rows: int, nh: int, nkv: int,
+                hd: int, window: int, splits: int, counters=None, page_map=None, stream=None) -> None:
+    """Split-KV paged GQA decode attention (``pgqa_attn_decode``), enqueued on ``stream``
+    (default: torch's current stream).  Tensors are passed by device pointer;
+    bf16 buffers may be any 2-byte dtype holding bf16 bits."""
+    st = load().pgqa_attn_decode(_ptr(o), _ptr(part), _ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(block_table),
+                                 _ptr(off), _ptr(qpos), _ptr(kvpos), int(rows), int(nh), int(nkv), int(hd),
+                                 int(window), int(splits), _ptr(counters), _ptr(page_map), _stream(stream))
+    if st != PGQA_OK:
+        raise PgqaError(st, "attn_decode")
+
+
+def choose_splits(kv_len_eff: int, rows: int, nkv: int, nseq: int, num_sms: int | None = None) -> int:
+    if num_sms is None:
+        return int(load().pgqa_choose_splits(int(kv_len_eff), int(rows), int(nkv), int(nseq)))
+    return int(load().pgqa_choose_splits_for(int(kv_len_eff), int(rows), int(nkv), int(nseq), int(num_sms)))
+
+
+def decode_part_bytes(rows: int, nh: int, splits: int, hd: int) -> int:
+    return int(load().pgqa_decode_part_bytes(int(rows), int(nh), int(splits), int(hd)))
+
+
+def decode_counter_count(rows: int, nh: int, nkv: int) -> int:
+    return int(load().pgqa_decode_counter_count(int(rows), int(nh), int(nkv)))
+
+
+def device_status() -> None:
+    """Raise PgqaError if a kernel gave up a bounded wait since the last check (synchronises)."""
+    st = load().pgqa_device_status()
+    if st != PGQA_OK:
+        raise PgqaError(st, "device_status")
+
+
+def version() -> int:
+    return int(load().pgqa_version())

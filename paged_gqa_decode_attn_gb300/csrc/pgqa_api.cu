@@ -1,0 +1,310 @@
+// C ABI of libpgqa.so (declared in include/pgqa.h): argument checks, the
+// split heuristic, scratch sizing, TMA descriptors and the launches.
+//
+// The entry points mirror the calls of span-02
+// `engine/crates/kernels/tests/gpu.rs`: `attn::attn_decode`,
+// `attn::choose_splits` and `attn::decode_part_bytes` in its `run` function.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "pgqa.h"
+#include "pgqa_launch.cuh"
+
+namespace {
+
+// Device-side error word: bounded waits OR their code into it.
+__device__ unsigned int g_pgqa_error_word;
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceState {
+    bool ready = false;
+    int num_sms = 0;
+    unsigned int *err = nullptr;
+    bool attr_set[4] = {false, false, false, false};
+};
+
+std::mutex g_mutex;
+DeviceState g_dev[kMaxDevices];
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                   const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn g_encode = nullptr;
+
+int hd_index(int hd)
+{
+    switch (hd) {
+    case 64: return 0;
+    case 128: return 1;
+    case 256: return 2;
+    case 512: return 3;
+    default: return -1;
+    }
+}
+
+// Per-device set-up (SM count, error-word address).  Caller holds g_mutex.
+int device_state(DeviceState **out)
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
+        return PGQA_ERR_CUDA;
+    DeviceState &s = g_dev[dev];
+    if (!s.ready) {
+        if (cudaDeviceGetAttribute(&s.num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return PGQA_ERR_CUDA;
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_pgqa_error_word) != cudaSuccess)
+            return PGQA_ERR_CUDA;
+        s.err = static_cast<unsigned int *>(p);
+        s.ready = true;
+    }
+    *out = &s;
+    return PGQA_OK;
+}
+
+int get_encoder()
+{
+    if (g_encode)
+        return PGQA_OK;
+    void *fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || fn == nullptr)
+        return PGQA_ERR_TENSOR_MAP;
+    g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+    return PGQA_OK;
+}
+
+// 3-D view of a [pages][nkv][16][hd] bf16 pool: x = dim (hd), y = slot (16),
+// z = (page, kv head) tile index phys * nkv + kh.  The box is 64 dims x 16
+// slots of one tile (2 KiB, 128-byte swizzle).  The pool's page count is not
+// known here, so z spans the int32 coordinate range; only tiles the block
+// table names are ever addressed.
+struct MapCacheEntry {
+    const void *base = nullptr;
+    int hd = 0;
+    CUtensorMap map;
+};
+MapCacheEntry g_map_cache[128];
+unsigned g_map_next = 0;
+
+int pool_map(const void *base, int hd, CUtensorMap *out)
+{
+    for (auto &e : g_map_cache)
+        if (e.base == base && e.hd == hd) {
+            *out = e.map;
+            return PGQA_OK;
+        }
+    int st = get_encoder();
+    if (st != PGQA_OK)
+        return st;
+    CUtensorMap m;
+    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(hd), 16u, 0x7fffffffull};
+    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(hd) * 2u, static_cast<cuuint64_t>(hd) * 32u};
+    const cuuint32_t box[3] = {64u, 16u, 1u};
+    const cuuint32_t estride[3] = {1u, 1u, 1u};
+    CUresult r = g_encode(&m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box,
+                          estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS)
+        return PGQA_ERR_TENSOR_MAP;
+    MapCacheEntry &e = g_map_cache[g_map_next++ % 128];
+    e.base = base;
+    e.hd = hd;
+    e.map = m;
+    *out = m;
+    return PGQA_OK;
+}
+
+bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+}  // namespace
+
+namespace pgqa {
+int split_kernel_smem_bytes(int hd)
+{
+    switch (hd) {
+    case 64: return Smem<64>::kAlloc;
+    case 128: return Smem<128>::kAlloc;
+    case 256: return Smem<256>::kAlloc;
+    case 512: return Smem<512>::kAlloc;
+    default: return 0;
+    }
+}
+}  // namespace pgqa
+
+extern "C" {
+
+int pgqa_version(void) { return 100; }
+
+const char *pgqa_strerror(int status)
+{
+    switch (status) {
+    case PGQA_OK: return "ok";
+    case PGQA_ERR_INVALID_ARGUMENT: return "invalid argument";
+    case PGQA_ERR_UNSUPPORTED_HD: return "unsupported head dimension (64, 128, 256 or 512)";
+    case PGQA_ERR_MISALIGNED: return "buffer not 16-byte aligned";
+    case PGQA_ERR_CUDA: return "CUDA runtime error";
+    case PGQA_ERR_TENSOR_MAP: return "TMA descriptor rejected by the driver";
+    case PGQA_ERR_DEVICE_TIMEOUT: return "a kernel gave up a bounded wait";
+    case PGQA_ERR_TOO_MANY_SPLITS: return "splits above PGQA_MAX_SPLITS";
+    default: return "unknown status";
+    }
+}
+
+size_t pgqa_decode_part_bytes(int rows, int nh, int splits, int hd)
+{
+    if (rows <= 0 || nh <= 0 || splits <= 0 || hd <= 0)
+        return 0;
+    return static_cast<size_t>(rows) * nh * splits * (static_cast<size_t>(hd) + 2) * 4;
+}
+
+size_t pgqa_decode_counter_count(int rows, int nh, int nkv)
+{
+    if (rows <= 0 || nh <= 0 || nkv <= 0 || nh % nkv != 0)
+        return 0;
+    const int g = nh / nkv;
+    return static_cast<size_t>(rows) * nkv * ((g + pgqa::kQRows - 1) / pgqa::kQRows);
+}
+
+int pgqa_choose_splits_for(int kv_len_eff, int rows, int nkv, int nseq, int num_sms)
+{
+    (void)nseq;
+    if (kv_len_eff < 1)
+        kv_len_eff = 1;
+    if (rows < 1)
+        rows = 1;
+    if (nkv < 1)
+        nkv = 1;
+    if (num_sms < 1)
+        num_sms = 1;
+    const long long pages = (kv_len_eff + PGQA_PAGE_TOKENS - 1) / PGQA_PAGE_TOKENS;
+    const long long tiles = static_cast<long long>(rows) * nkv;
+    // Aim at four CTAs per SM over the whole grid, but keep at least four
+    // pages in every split so each CTA streams more than it merges.
+    long long s = (4LL * num_sms + tiles - 1) / tiles;
+    long long cap = pages / 4;
+    if (cap < 1)
+        cap = 1;
+    if (s > cap)
+        s = cap;
+    if (s > PGQA_MAX_SPLITS)
+        s = PGQA_MAX_SPLITS;
+    if (s < 1)
+        s = 1;
+    return static_cast<int>(s);
+}
+
+int pgqa_choose_splits(int kv_len_eff, int rows, int nkv, int nseq)
+{
+    int sms = 152;
+    {
+        std::lock_guard<std::mutex> lock(g_mutex);
+        DeviceState *s = nullptr;
+        if (device_state(&s) == PGQA_OK)
+            sms = s->num_sms;
+    }
+    return pgqa_choose_splits_for(kv_len_eff, rows, nkv, nseq, sms);
+}
+
+int pgqa_device_status(void)
+{
+    std::lock_guard<std::mutex> lock(g_mutex);
+    DeviceState *s = nullptr;
+    int st = device_state(&s);
+    if (st != PGQA_OK)
+        return st;
+    unsigned int word = 0;
+    if (cudaDeviceSynchronize() != cudaSuccess ||
+        cudaMemcpy(&word, s->err, sizeof word, cudaMemcpyDeviceToHost) != cudaSuccess)
+        return PGQA_ERR_CUDA;
+    if (word != 0) {
+        const unsigned int zero = 0;
+        if (cudaMemcpy(s->err, &zero, sizeof zero, cudaMemcpyHostToDevice) != cudaSuccess)
+            return PGQA_ERR_CUDA;
+        return PGQA_ERR_DEVICE_TIMEOUT;
+    }
+    return PGQA_OK;
+}
+
+int pgqa_attn_decode(void *o, void *part, const void *q, const void *k_pool, const void *v_pool,
+                     const int32_t *block_table, const int32_t *off, const int32_t *qpos, const int32_t *kvpos,
+                     int rows, int nh, int nkv, int hd, int window, int splits, uint32_t *counters,
+                     const int32_t *page_map, void *stream)
+{
+    if (rows < 0 || nh <= 0 || nkv <= 0 || nh % nkv != 0 || window < 0 || splits < 1)
+        return PGQA_ERR_INVALID_ARGUMENT;
+    const int hi = hd_index(hd);
+    if (hi < 0)
+        return PGQA_ERR_UNSUPPORTED_HD;
+    if (splits > PGQA_MAX_SPLITS)
+        return PGQA_ERR_TOO_MANY_SPLITS;
+    if (rows == 0)
+        return PGQA_OK;
+    if (!o || !q || !k_pool || !v_pool || !block_table || !off || !qpos || (splits > 1 && !part))
+        return PGQA_ERR_INVALID_ARGUMENT;
+    const int g = nh / nkv;
+    const int hsg = (g + pgqa::kQRows - 1) / pgqa::kQRows;
+    if (rows > 65535 || static_cast<long long>(nkv) * hsg > 65535)
+        return PGQA_ERR_INVALID_ARGUMENT;
+    if (!aligned(k_pool, 16) || !aligned(v_pool, 16) || !aligned(q, 16) || !aligned(o, 2) ||
+        (splits > 1 && !aligned(part, 16)))
+        return PGQA_ERR_MISALIGNED;
+
+    pgqa::LaunchArgs a;
+    pgqa::DecodeParams &p = a.p;
+    p.o = static_cast<__nv_bfloat16 *>(o);
+    p.part_o = static_cast<float *>(part);
+    p.part_ml = splits > 1 ? reinterpret_cast<float2 *>(static_cast<char *>(part) +
+                                                        static_cast<size_t>(rows) * nh * splits * hd * 4)
+                           : nullptr;
+    p.q = static_cast<const __nv_bfloat16 *>(q);
+    p.block_table = block_table;
+    p.off = off;
+    p.qpos = qpos;
+    p.kvpos = kvpos;
+    p.page_map = page_map;
+    p.counters = counters;
+    p.rows = rows;
+    p.nh = nh;
+    p.nkv = nkv;
+    p.window = window;
+    p.splits = splits;
+    p.g = g;
+    p.hsg = hsg;
+    a.stream = static_cast<cudaStream_t>(stream);
+
+    // The lock covers set-up and the (asynchronous) launch itself, so the
+    // one-time shared-memory attribute is in place before any launch.
+    std::lock_guard<std::mutex> lock(g_mutex);
+    DeviceState *s = nullptr;
+    int st = device_state(&s);
+    if (st != PGQA_OK)
+        return st;
+    CUtensorMap tk, tv;
+    if ((st = pool_map(k_pool, hd, &tk)) != PGQA_OK || (st = pool_map(v_pool, hd, &tv)) != PGQA_OK)
+        return st;
+    p.err = s->err;
+    a.tm_k = &tk;
+    a.tm_v = &tv;
+    const bool set_attr = !s->attr_set[hi];
+    cudaError_t e;
+    switch (hd) {
+    case 64: e = pgqa::launch_decode_hd64(a, set_attr); break;
+    case 128: e = pgqa::launch_decode_hd128(a, set_attr); break;
+    case 256: e = pgqa::launch_decode_hd256(a, set_attr); break;
+    default: e = pgqa::launch_decode_hd512(a, set_attr); break;
+    }
+    if (e != cudaSuccess)
+        return PGQA_ERR_CUDA;
+    s->attr_set[hi] = true;
+    return PGQA_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,6 @@
+// Split-KV decode kernels instantiated for head dimension 512.
+#include "pgqa_launch.cuh"
+
+namespace pgqa {
+cudaError_t launch_decode_hd512(const LaunchArgs &a, bool set_attr) { return launch_decode<512>(a, set_attr); }
+}  // namespace pgqa

@@ -1,0 +1,119 @@
+"""Host-side checks of libpgqa.so that need no GPU: it builds, loads, exports every
+symbol include/pgqa.h declares, sizes its scratch, picks splits, and rejects bad
+arguments before touching CUDA.  Also pins constants that the header, the
+kernels and the Python binding must agree on (a structural source test)."""
+import ctypes
+import os
+import re
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+
+import paged_gqa_decode_attn_gb300 as pgqa  # noqa: E402
+from paged_gqa_decode_attn_gb300 import _lib  # noqa: E402
+
+HEADER = os.path.join(ROOT, "include", "pgqa.h")
+DEVICE = os.path.join(ROOT, "paged_gqa_decode_attn_gb300", "csrc", "pgqa_device.cuh")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    pgqa.build()
+    return pgqa.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?[\w ]+?\*?\s*(pgqa_\w+)\s*\(", text, re.M)))
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    for n in ("pgqa_attn_decode", "pgqa_choose_splits", "pgqa_decode_part_bytes"):
+        assert n in names
+    assert set(names) <= set(_lib.SIGNATURES), "binding lacks a declared function"
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for n in declared_functions():
+        assert hasattr(lib, n), n
+        assert isinstance(getattr(lib, n), ctypes._CFuncPtr)
+
+
+def test_constants_agree_between_header_kernels_and_binding():
+    h = open(HEADER).read()
+    dev = open(DEVICE).read()
+    hdr = {k: int(v) for k, v in re.findall(r"#define (PGQA_\w+) \(?(-?\d+)\)?", h)}
+    assert hdr["PGQA_PAGE_TOKENS"] == int(re.search(r"kPage = (\d+);", dev).group(1)) == _lib.PAGE_TOKENS
+    assert hdr["PGQA_MAX_SPLITS"] == int(re.search(r"kMaxSplits = (\d+);", dev).group(1)) == _lib.MAX_SPLITS
+    for name in ("OK", "ERR_INVALID_ARGUMENT", "ERR_UNSUPPORTED_HD", "ERR_MISALIGNED", "ERR_CUDA",
+                 "ERR_TENSOR_MAP", "ERR_DEVICE_TIMEOUT", "ERR_TOO_MANY_SPLITS"):
+        assert hdr["PGQA_" + name] == getattr(_lib, "PGQA_" + name)
+
+
+def test_part_bytes_and_counter_count(lib):
+    assert pgqa.decode_part_bytes(4, 16, 9, 256) == 4 * 16 * 9 * 258 * 4
+    assert pgqa.decode_part_bytes(1, 32, 1, 512) == 32 * 514 * 4
+    assert pgqa.decode_part_bytes(0, 16, 9, 256) == 0
+    assert pgqa.decode_counter_count(4, 16, 8) == 32          # g = 2: one subgroup per kv head
+    assert pgqa.decode_counter_count(1, 32, 2) == 4           # g = 16: two subgroups of 8 heads
+    assert pgqa.decode_counter_count(2, 24, 2) == 8           # g = 12: two subgroups
+    assert pgqa.decode_counter_count(2, 10, 3) == 0           # nh % nkv != 0
+
+
+def test_choose_splits_rule(lib):
+    for kv in (1, 15, 16, 64, 1000, 1024, 4096, 32768, 1 << 20):
+        for rows in (1, 4, 16, 64):
+            for nkv in (1, 2, 4, 8, 16):
+                s = pgqa.choose_splits(kv, rows, nkv, rows, num_sms=152)
+                pages = (kv + 15) // 16
+                assert 1 <= s <= pgqa.MAX_SPLITS
+                assert s == 1 or s <= pages // 4           # at least four pages per split
+                assert s == 1 or rows * nkv * (s - 1) < 4 * 152   # no more splits than needed
+    # the named workloads (152 SMs)
+    assert pgqa.choose_splits(256, 1, 2, 1, num_sms=152) == 4
+    assert pgqa.choose_splits(1024, 4, 8, 4, num_sms=152) == 16
+    assert pgqa.choose_splits(32768, 1, 4, 1, num_sms=152) == 152
+    assert pgqa.choose_splits(4096, 64, 8, 64, num_sms=152) == 2
+    # without a device the current-device form falls back to 152 SMs
+    assert pgqa.choose_splits(32768, 1, 4, 1) >= 1
+
+
+def test_strerror_names_every_code(lib):
+    for code in range(-7, 1):
+        assert pgqa.strerror(code) != "unknown status"
+    assert pgqa.strerror(-99) == "unknown status"
+
+
+FAKE = 0x10000   # never dereferenced: validation fails first
+
+
+def call(lib, rows=1, nh=8, nkv=2, hd=128, window=0, splits=1, o=FAKE, part=FAKE, q=FAKE, k=FAKE, v=FAKE,
+         bt=FAKE, off=FAKE, qpos=FAKE):
+    return lib.pgqa_attn_decode(o, part, q, k, v, bt, off, qpos, None, rows, nh, nkv, hd, window, splits,
+                                None, None, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(rows=-1), -1), (dict(nh=0), -1), (dict(nkv=0), -1), (dict(nh=10, nkv=4), -1),
+    (dict(window=-1), -1), (dict(splits=0), -1), (dict(hd=96), -2), (dict(hd=1024), -2),
+    (dict(splits=257), -7), (dict(o=None), -1), (dict(q=None), -1), (dict(k=None), -1),
+    (dict(v=None), -1), (dict(bt=None), -1), (dict(off=None), -1), (dict(qpos=None), -1),
+    (dict(splits=2, part=None), -1), (dict(k=FAKE + 8), -3), (dict(v=FAKE + 2), -3),
+    (dict(q=FAKE + 4), -3), (dict(splits=2, part=FAKE + 4), -3), (dict(rows=70000), -1),
+])
+def test_bad_arguments_are_rejected_before_any_cuda_call(lib, kw, code):
+    assert call(lib, **kw) == code
+
+
+def test_zero_rows_is_ok_without_a_device(lib):
+    assert call(lib, rows=0, o=None, q=None) == 0
+
+
+def test_python_binding_raises_on_error(lib):
+    with pytest.raises(pgqa.PgqaError) as ei:
+        pgqa.attn_decode(FAKE, None, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None, 1, 8, 2, 96, 0, 1, stream=0)
+    assert ei.value.status == -2

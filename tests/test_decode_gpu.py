@@ -1,0 +1,216 @@
+"""GPU parity of libpgqa's split-KV paged decode attention against the f64 oracle.
+
+The three gates follow the `run` function of span-02
+``engine/crates/kernels/tests/gpu.rs``:
+  1. rel-RMS of the bf16 output against the oracle's bf16 output < 1e-2;
+  2. merge counters (last CTA merges) == separate combine kernel, bit for bit;
+  3. identity pool == permuted pool behind a page map with the NaN null page 0
+     for pages outside every row's window, bit for bit (also with the map
+     folded into the block table).
+On top of the page's gate every element is held to a bound derived from the
+arithmetic (bf16 P and output rounding, f32 score accumulation):
+|o - o_f64| <= 2^-7 (|o_f64| + max|V|).
+"""
+import os
+import sys
+
+import numpy as np
+import pytest
+
+sys.path.insert(0, os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, os.path.dirname(os.path.dirname(os.path.abspath(__file__))))
+
+import oracle  # noqa: E402
+from paged_gqa_decode_attn_gb300 import workloads as wl  # noqa: E402
+
+pytestmark = pytest.mark.gpu
+
+REL_RMS_GATE = 1e-2
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    import torch  # noqa: F401
+    import paged_gqa_decode_attn_gb300 as pgqa
+    pgqa.build()
+    pgqa.load()
+    yield
+
+
+def bits_to_f64(b):
+    return wl.bf16_to_f32(b).astype(np.float64)
+
+
+def check_parity(case, got, label=""):
+    ref64, ref16 = oracle.decode_case(case)
+    e = oracle.rel_rms(got, ref16)
+    assert e < REL_RMS_GATE, f"{label} rel_rms {e:.3e}"
+    g = bits_to_f64(got)
+    vmax = float(np.nanmax(np.abs(np.where(np.isfinite(bits_to_f64(case.v_pool)), bits_to_f64(case.v_pool), 0))))
+    bound = 2.0 ** -7 * (np.abs(ref64) + vmax)
+    bad = np.abs(g - ref64) > bound
+    assert not bad.any(), f"{label}: {int(bad.sum())} elements beyond bound, first {np.argwhere(bad)[0]}"
+    assert np.all(np.isfinite(g))
+    return e
+
+
+def full_gates(case, splits=None, mapped=True):
+    """Gates 1-3 on one case; returns the identity-pool output."""
+    from gpu_util import DevCase, first_difference
+    d = DevCase(case, splits)
+    a = d.result(counters=True)
+    check_parity(case, a, case.name)
+    b = d.result(counters=False)
+    assert np.array_equal(a, b), "merge modes differ: " + first_difference(b, a)
+    assert int(d.cnt.abs().sum().item()) == 0, "merge counters not left at zero"
+    if mapped:
+        for fold in (False, True):
+            m = wl.with_mapped_pool(case, fold_into_table=fold)
+            dm = DevCase(m, d.splits)
+            am = dm.result(counters=True)
+            assert np.array_equal(am, a), f"page map (fold={fold}) differs: " + first_difference(am, a)
+            bm = dm.result(counters=False)
+            assert np.array_equal(bm, a), f"page map (fold={fold}) combine differs: " + first_difference(bm, a)
+    return a, d
+
+
+@pytest.mark.parametrize("args", [(16, 8, 256, 1024, 1500, 5), (16, 2, 512, 0, 700, 1)],
+                         ids=["hd256_w1024_ctx1500_r5", "hd512_w0_ctx700_r1"])
+def test_page_decode_cases(args):
+    full_gates(wl.page_case(*args))
+
+
+def test_tiny_full_attention():
+    full_gates(wl.tiny())
+
+
+def test_sliding_window_multirow():
+    full_gates(wl.sliding())
+
+
+def test_long_context_32k_both_merge_modes():
+    full_gates(wl.long_ctx(), mapped=True)
+
+
+def test_batched_64_rows_shared_permuted_table():
+    full_gates(wl.batched(), mapped=False)
+
+
+SWEEP_SAMPLE = [
+    (128, 1024, 1, 0), (128, 4096, 16, 1024), (128, 65536, 4, 4096), (128, 65536, 1, 0),
+    (256, 1024, 16, 4096), (256, 4096, 4, 0), (256, 16384, 1, 1024),
+    (512, 1024, 4, 1024), (512, 4096, 1, 4096), (512, 16384, 16, 0),
+]
+
+
+@pytest.mark.parametrize("pt", SWEEP_SAMPLE, ids=lambda p: "hd%d_ctx%d_r%d_w%d" % p)
+def test_sweep_points_gaussian_peaky_permuted(pt):
+    """Gaussian Q/K/V with 5% of keys x8, served from the permuted pool with the NaN null page."""
+    c = wl.sweep(*pt, mapped=False)
+    a, d = full_gates(c, mapped=True)
+
+
+@pytest.mark.parametrize("splits", [1, 2, 3, 7, 64, 256])
+def test_any_split_count_matches_oracle(splits):
+    """More splits than pages leaves empty splits; all counts must pass the gates."""
+    c = wl.page_case(8, 2, 128, 0, 300, 3, dist="sym", seed=11)
+    full_gates(c, splits=splits)
+
+
+@pytest.mark.parametrize("hd", [64, 128, 256, 512])
+@pytest.mark.parametrize("nh,nkv", [(4, 4), (8, 1), (32, 2), (24, 2)])
+def test_head_dims_and_group_sizes(hd, nh, nkv):
+    """g = 1, 8, 16 (two head subgroups per kv head) and 12 (a partial subgroup)."""
+    c = wl.page_case(nh, nkv, hd, 0, 200, 2, dist="sym", seed=hd + nh)
+    full_gates(c, splits=3, mapped=False)
+
+
+@pytest.mark.parametrize("window,ctx,rows", [(1, 50, 3), (5000, 700, 2), (17, 33, 4), (0, 1, 1), (16, 16, 1)])
+def test_window_and_tiny_context_edges(window, ctx, rows):
+    c = wl.page_case(16, 4, 128, window, ctx, rows, dist="sym", seed=window + ctx)
+    full_gates(c, splits=4)
+
+
+def ragged_case(seed=21, nh=16, nkv=4, hd=128, window=40):
+    """Rows with distinct non-zero offsets, positions mid-page, and one empty row (kvpos < lo)."""
+    rng = wl.Lcg(seed)
+    npages = 64
+    n = npages * nkv * 16 * hd
+    k = wl.draw_bf16(rng, n, "sym")
+    v = wl.draw_bf16(rng, n, "sym")
+    rows = 5
+    q = wl.draw_bf16(rng, rows * nh * hd, "sym")
+    perm = wl.lcg_permutation(npages, seed + 1)
+    bt = np.concatenate([perm[:20], perm[20:44], perm[44:64]]).astype(np.int32)
+    off = np.array([0, 20, 44, 20, 5], dtype=np.int32)
+    qpos = np.array([300, 383, 250, 17, 100], dtype=np.int32)
+    kvpos = np.array([300, 383, 250, 19, 30], dtype=np.int32)    # row 3 sees ahead; row 4 is empty
+    return wl.Case("ragged", nh, nkv, hd, window, rows, q, k, v, bt, off, qpos, kvpos=kvpos,
+                   ctx=384, npg=npages)
+
+
+@pytest.mark.parametrize("window", [0, 40])
+def test_ragged_rows_offsets_kvpos_and_empty_row(window):
+    from gpu_util import DevCase
+    c = ragged_case(window=window)
+    for splits in (1, 5):
+        d = DevCase(c, splits)
+        a = d.result(counters=True)
+        check_parity(c, a, f"ragged w{window} s{splits}")
+        assert np.array_equal(a, d.result(counters=False))
+        if window:
+            assert np.all(a[4] == 0), "row with no visible position must be zero"
+
+
+def test_nan_outside_windows_never_reaches_output():
+    """Slots of read pages outside every row's [lo, hi] and whole unread pages hold NaN."""
+    from gpu_util import DevCase, first_difference
+    c = wl.page_case(16, 8, 256, 1024, 1500, 5, dist="sym", seed=3)
+    d = DevCase(c, 6)
+    clean = d.result()
+    poisoned_k = c.k_pool.copy().reshape(c.npg, c.nkv, 16, c.hd)
+    poisoned_v = c.v_pool.copy().reshape(c.npg, c.nkv, 16, c.hd)
+    lo_min = min(wl.window_lo(int(x), c.window) for x in c.qpos)
+    hi_max = int(c.qpos.max())
+    for pos in range(c.npg * 16):
+        if pos < lo_min or pos > hi_max:
+            poisoned_k[pos // 16, :, pos % 16, :] = wl.BF16_NAN
+            poisoned_v[pos // 16, :, pos % 16, :] = wl.BF16_NAN
+    import dataclasses
+    pc = dataclasses.replace(c, k_pool=poisoned_k.reshape(-1), v_pool=poisoned_v.reshape(-1))
+    dp = DevCase(pc, 6)
+    for counters in (True, False):
+        got = dp.result(counters=counters)
+        assert np.array_equal(got, clean), first_difference(got, clean)
+
+
+def test_repeated_calls_and_streams_are_deterministic():
+    import torch
+    from gpu_util import DevCase
+    c = wl.page_case(32, 4, 512, 0, 3000, 2, dist="sym", seed=8)
+    d = DevCase(c)
+    first = d.result()
+    for _ in range(5):
+        assert np.array_equal(d.result(), first)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        o = d.run(stream=s)
+    s.synchronize()
+    assert np.array_equal(o.cpu().numpy().view(np.uint16).reshape(first.shape), first)
+    assert int(d.cnt.abs().sum().item()) == 0
+
+
+def test_zero_rows_is_a_no_op():
+    import torch
+    import paged_gqa_decode_attn_gb300 as pgqa
+    x = torch.zeros(16, dtype=torch.int16, device="cuda")
+    pgqa.attn_decode(x, None, x, x, x, x, x, x, None, 0, 8, 2, 128, 0, 1)
+    torch.cuda.synchronize()
+    assert int(x.abs().sum().item()) == 0
+
+
+def test_device_status_clean_after_runs():
+    import paged_gqa_decode_attn_gb300 as pgqa
+    from gpu_util import DevCase
+    DevCase(wl.tiny()).result()
+    pgqa.device_status()
