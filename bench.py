@@ -279,6 +279,8 @@ def run_ours(args, case, rank, world, dist):
     pool_bytes = case.k_pool.nbytes + case.v_pool.nbytes
     copies = max(2, math.ceil(3 * L2_BYTES / max(bpc, 1)))
     copies = min(copies, max(2, int(0.25 * torch.cuda.get_device_properties(dev).total_memory // pool_bytes)))
+    if args.copies:
+        copies = args.copies
 
     def i16(a):
         return torch.from_numpy(np.ascontiguousarray(a).view(np.int16))
@@ -430,6 +432,7 @@ def main(argv=None):
     ap.add_argument("--splits", type=int, default=0, help="override choose_splits")
     ap.add_argument("--merge", choices=["counters", "combine"], default="counters")
     ap.add_argument("--graph-chunk", type=int, default=2000)
+    ap.add_argument("--copies", type=int, default=0, help="override the number of rotated pool copies")
     ap.add_argument("--e2e-steps", type=int, default=2000)
     ap.add_argument("--cpu-budget", type=float, default=10.0, help="seconds of oracle work for cpu_baseline")
     ap.add_argument("--ref-budget", type=float, default=60.0, help="seconds of oracle work for --impl reference")

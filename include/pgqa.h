@@ -37,7 +37,7 @@ extern "C" {
 #define PGQA_OK 0
 #define PGQA_ERR_INVALID_ARGUMENT (-1)   /* null pointer, bad size, nh % nkv != 0, ... */
 #define PGQA_ERR_UNSUPPORTED_HD (-2)     /* hd not in {64, 128, 256, 512} */
-#define PGQA_ERR_MISALIGNED (-3)         /* a pool is not 16-byte aligned */
+#define PGQA_ERR_MISALIGNED (-3)         /* o, part, q or a pool is not 16-byte aligned */
 #define PGQA_ERR_CUDA (-4)               /* a CUDA runtime call or launch failed */
 #define PGQA_ERR_TENSOR_MAP (-5)         /* the driver refused the TMA descriptor */
 #define PGQA_ERR_DEVICE_TIMEOUT (-6)     /* a kernel gave up a bounded wait (see pgqa_device_status) */
@@ -51,11 +51,11 @@ extern "C" {
  * above; the result is its f64 `reference`).
  *
  * Device buffers:
- *   o           [rows][nh][hd] bf16, written (never read).
+ *   o           [rows][nh][hd] bf16, written (never read), 16-byte aligned.
  *   part        scratch of at least pgqa_decode_part_bytes(rows, nh, splits, hd)
- *               bytes; contents need no initialisation and are dead after the
- *               call.  May be NULL when splits == 1.
- *   q           [rows][nh][hd] bf16.
+ *               bytes, 16-byte aligned; contents need no initialisation and are
+ *               dead after the call.  May be NULL when splits == 1.
+ *   q           [rows][nh][hd] bf16, 16-byte aligned.
  *   k_pool,
  *   v_pool      [npages][nkv][16][hd] bf16, 16-byte aligned.  Only the pages
  *               holding positions [lo, hi] of some row are read, so pages wholly
@@ -78,6 +78,11 @@ extern "C" {
  * {64, 128, 256, 512}, window >= 0 (0 = full causal), 1 <= splits <=
  * PGQA_MAX_SPLITS.  The output for a given (inputs, splits) does not depend on
  * which physical pages hold the data.
+ *
+ * Row packing: consecutive rows in groups of max(1, 8 / (nh / nkv)) that share
+ * their block-table span (equal off) and whose visible ranges pairwise
+ * overlap are served together, so their common KV is read once.  Which rows
+ * pack depends only on off, qpos, kvpos and window.
  *
  * stream: a cudaStream_t (NULL = the legacy default stream).  The call only
  * enqueues work: it never synchronises and never allocates.  Calls sharing
@@ -116,6 +121,17 @@ size_t pgqa_decode_counter_count(int rows, int nh, int nkv);
  * must then be zeroed again.
  */
 int pgqa_device_status(void);
+
+/*
+ * Debug tracing.  In a library built with PGQA_TRACE defined, every split-kernel
+ * CTA of later calls writes 16 uint64 slots (global timer, ns) at phase
+ * boundaries into device_buffer, at [cta][event] with
+ * cta = (blockIdx.z * gridDim.y + blockIdx.y) * gridDim.x + blockIdx.x, when
+ * the buffer holds the whole grid; NULL turns it off.  Returns PGQA_OK in a
+ * trace build and PGQA_ERR_INVALID_ARGUMENT (with no effect on kernels) in a
+ * normal one.
+ */
+int pgqa_trace_buffer(void *device_buffer, size_t bytes);
 
 /* Static, human-readable name of a status code. */
 const char *pgqa_strerror(int status);

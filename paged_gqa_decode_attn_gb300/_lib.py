@@ -6,7 +6,7 @@ from __future__ import annotations
 import ctypes
 import os
 
-from . import build as _build
+from . import builder as _build
 
 PGQA_OK = 0
 PGQA_ERR_INVALID_ARGUMENT = -1
@@ -30,6 +30,7 @@ SIGNATURES = {
     "pgqa_device_status": (_I, []),
     "pgqa_strerror": (ctypes.c_char_p, [_I]),
     "pgqa_version": (_I, []),
+    "pgqa_trace_buffer": (_I, [_P, ctypes.c_size_t]),
 }
 
 
@@ -43,16 +44,20 @@ _lib = None
 
 
 def lib_path() -> str:
-    return _build.LIB
+    return _build.lib_path(os.environ.get("PGQA_VARIANT", ""))
 
 
 def load() -> ctypes.CDLL:
-    """Load libpgqa.so (it must have been built: ``paged_gqa_decode_attn_gb300.build.build()``)."""
+    """Load libpgqa.so (it must have been built: ``paged_gqa_decode_attn_gb300.build.build()``).
+
+    With PGQA_VARIANT=trace in the environment the trace build is loaded instead."""
     global _lib
     if _lib is None:
-        if not os.path.exists(_build.LIB):
-            raise ImportError(f"libpgqa.so is not built ({_build.LIB}); run paged_gqa_decode_attn_gb300.build.build()")
-        lib = ctypes.CDLL(_build.LIB)
+        path = _build.lib_path(os.environ.get("PGQA_VARIANT", ""))
+        if not os.path.exists(path):
+            raise ImportError(f"{os.path.basename(path)} is not built ({path}); "
+                              "run paged_gqa_decode_attn_gb300.build.build()")
+        lib = ctypes.CDLL(path)
         for name, (res, args) in SIGNATURES.items():
             fn = getattr(lib, name)
             fn.restype = res
@@ -114,6 +119,12 @@ def device_status() -> None:
     st = load().pgqa_device_status()
     if st != PGQA_OK:
         raise PgqaError(st, "device_status")
+
+
+def trace_buffer(buf) -> bool:
+    """Point trace builds at a device buffer (torch tensor or None); False in normal builds."""
+    nbytes = 0 if buf is None else buf.numel() * buf.element_size()
+    return load().pgqa_trace_buffer(_ptr(buf), nbytes) == PGQA_OK
 
 
 def version() -> int:

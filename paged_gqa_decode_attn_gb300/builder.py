@@ -17,6 +17,12 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libpgqa.so")
+VARIANTS = {"": [], "trace": ["-DPGQA_TRACE"]}
+
+
+def lib_path(variant: str = "") -> str:
+    """The shared library of a build variant ("" = normal, "trace" = with phase timestamps)."""
+    return LIB if not variant else os.path.join(HERE, f"libpgqa_{variant}.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-I" + INCLUDE, "-I" + CSRC]
 
@@ -35,24 +41,27 @@ def _deps():
             + [os.path.abspath(__file__)])
 
 
-def stale() -> bool:
-    if not os.path.exists(LIB):
+def stale(variant: str = "") -> bool:
+    lib = lib_path(variant)
+    if not os.path.exists(lib):
         return True
-    t = os.path.getmtime(LIB)
+    t = os.path.getmtime(lib)
     return any(os.path.getmtime(d) > t for d in _deps())
 
 
-def build(force: bool = False, verbose: bool = False, ptxas_v: bool = False) -> str:
-    """Compile every CUDA source for sm_103a and link ``libpgqa.so``; returns its path."""
-    if not force and not stale():
-        return LIB
-    os.makedirs(BUILD, exist_ok=True)
+def build(force: bool = False, verbose: bool = False, ptxas_v: bool = False, variant: str = "") -> str:
+    """Compile every CUDA source for sm_103a and link ``libpgqa.so`` (or a variant); returns its path."""
+    lib = lib_path(variant)
+    if not force and not stale(variant):
+        return lib
+    bdir = os.path.join(BUILD, variant or "default")
+    os.makedirs(bdir, exist_ok=True)
     nvcc = _nvcc()
-    extra = ["-Xptxas", "-v"] if ptxas_v else []
+    extra = (["-Xptxas", "-v"] if ptxas_v else []) + VARIANTS[variant]
     procs = []
     objs = []
     for src in _sources():
-        obj = os.path.join(BUILD, os.path.splitext(os.path.basename(src))[0] + ".o")
+        obj = os.path.join(bdir, os.path.splitext(os.path.basename(src))[0] + ".o")
         objs.append(obj)
         cmd = [nvcc, *ARCH, *NVCC_FLAGS, *extra, "-c", src, "-o", obj]
         if verbose:
@@ -67,12 +76,13 @@ def build(force: bool = False, verbose: bool = False, ptxas_v: bool = False) -> 
             failed.append(src)
     if failed:
         raise RuntimeError(f"nvcc failed for {failed}")
-    tmp = LIB + f".tmp{os.getpid()}"
+    tmp = lib + f".tmp{os.getpid()}"
     subprocess.check_call([nvcc, *ARCH, "-shared", "-o", tmp, *objs])
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":
-    build(force="--force" in sys.argv, verbose="-v" in sys.argv, ptxas_v="--ptxas-v" in sys.argv)
-    print(LIB)
+    variant = "trace" if "--trace" in sys.argv else ""
+    print(build(force="--force" in sys.argv, verbose="-v" in sys.argv, ptxas_v="--ptxas-v" in sys.argv,
+                variant=variant))

@@ -30,6 +30,8 @@ struct DeviceState {
 
 std::mutex g_mutex;
 DeviceState g_dev[kMaxDevices];
+unsigned long long *g_trace = nullptr;    // trace builds: per-CTA timestamps
+size_t g_trace_bytes = 0;
 
 using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
                                    const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
@@ -143,6 +145,18 @@ extern "C" {
 
 int pgqa_version(void) { return 100; }
 
+int pgqa_trace_buffer(void *device_buffer, size_t bytes)
+{
+    std::lock_guard<std::mutex> lock(g_mutex);
+    g_trace = static_cast<unsigned long long *>(device_buffer);
+    g_trace_bytes = device_buffer ? bytes : 0;
+#ifdef PGQA_TRACE
+    return PGQA_OK;
+#else
+    return PGQA_ERR_INVALID_ARGUMENT;
+#endif
+}
+
 const char *pgqa_strerror(int status)
 {
     switch (status) {
@@ -175,21 +189,23 @@ size_t pgqa_decode_counter_count(int rows, int nh, int nkv)
 
 int pgqa_choose_splits_for(int kv_len_eff, int rows, int nkv, int nseq, int num_sms)
 {
-    (void)nseq;
     if (kv_len_eff < 1)
         kv_len_eff = 1;
     if (rows < 1)
         rows = 1;
+    if (nseq < 1 || nseq > rows)
+        nseq = rows;
     if (nkv < 1)
         nkv = 1;
     if (num_sms < 1)
         num_sms = 1;
     const long long pages = (kv_len_eff + PGQA_PAGE_TOKENS - 1) / PGQA_PAGE_TOKENS;
-    const long long tiles = static_cast<long long>(rows) * nkv;
-    // Aim at four CTAs per SM over the whole grid, but keep at least four
-    // pages in every split so each CTA streams more than it merges.
-    long long s = (4LL * num_sms + tiles - 1) / tiles;
-    long long cap = pages / 4;
+    // Rows of one sequence share CTAs (row packing), so the CTAs of one split
+    // are about nseq * nkv.  Few tiles: split until the grid is one wave of
+    // one CTA per SM.  Many tiles: about four CTAs per SM, for balance.
+    const long long tiles = static_cast<long long>(nseq) * nkv;
+    long long s = tiles < num_sms ? (num_sms + tiles - 1) / tiles : (4LL * num_sms + tiles - 1) / tiles;
+    long long cap = pages / 2;       // at least two pages per split
     if (cap < 1)
         cap = 1;
     if (s > cap)
@@ -253,7 +269,7 @@ int pgqa_attn_decode(void *o, void *part, const void *q, const void *k_pool, con
     const int hsg = (g + pgqa::kQRows - 1) / pgqa::kQRows;
     if (rows > 65535 || static_cast<long long>(nkv) * hsg > 65535)
         return PGQA_ERR_INVALID_ARGUMENT;
-    if (!aligned(k_pool, 16) || !aligned(v_pool, 16) || !aligned(q, 16) || !aligned(o, 2) ||
+    if (!aligned(k_pool, 16) || !aligned(v_pool, 16) || !aligned(q, 16) || !aligned(o, 16) ||
         (splits > 1 && !aligned(part, 16)))
         return PGQA_ERR_MISALIGNED;
 
@@ -278,6 +294,8 @@ int pgqa_attn_decode(void *o, void *part, const void *q, const void *k_pool, con
     p.splits = splits;
     p.g = g;
     p.hsg = hsg;
+    p.pack = g <= pgqa::kQRows ? pgqa::kQRows / g : 1;
+    p.trace = nullptr;
     a.stream = static_cast<cudaStream_t>(stream);
 
     // The lock covers set-up and the (asynchronous) launch itself, so the
@@ -291,6 +309,8 @@ int pgqa_attn_decode(void *o, void *part, const void *q, const void *k_pool, con
     if ((st = pool_map(k_pool, hd, &tk)) != PGQA_OK || (st = pool_map(v_pool, hd, &tv)) != PGQA_OK)
         return st;
     p.err = s->err;
+    if (g_trace && static_cast<size_t>(splits) * nkv * hsg * rows * pgqa::kTraceEvents * 8 <= g_trace_bytes)
+        p.trace = g_trace;
     a.tm_k = &tk;
     a.tm_v = &tv;
     const bool set_attr = !s->attr_set[hi];

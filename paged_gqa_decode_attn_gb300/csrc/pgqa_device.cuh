@@ -10,15 +10,19 @@
 // sum, unnormalised O); the last CTA of the tile (merge counters) or a
 // separate combine kernel merges them.
 //
-// GB300 design (see the header comment of each kernel for its roofline):
+// GB300 design:
 //  * one producer warp streams whole (page, kv head) tiles of K and V into a
 //    ring of shared-memory stages with 3-D TMA (cp.async.bulk.tensor) and the
 //    128-byte swizzle, completion counted on mbarriers;
-//  * four consumer warps each take whole pages: S = Q K^T and O^T += V^T P^T
-//    on the tensor cores (mma.sync m16n8k16 bf16 -> f32), all g = nh/nkv query
-//    heads of the kv head packed into the MMA rows so each KV byte leaves HBM
-//    once; the S accumulator fragment is, register for register, the B
-//    fragment of the PV product, so P never touches shared memory;
+//  * four consumer warps work on every page together, each owning a quarter
+//    of the head dimension: partial S = Q K^T over its quarter on the tensor
+//    cores (mma.sync m16n8k16 bf16 -> f32, all query heads of the kv head in
+//    the MMA rows so each KV byte leaves HBM once), partial sums exchanged
+//    through a small double-buffered shared array (one barrier per page),
+//    then the same online softmax in every warp and O^T += V^T P^T for its
+//    quarter.  The S accumulator fragment is, register for register, the B
+//    fragment of the PV product, so P never touches shared memory.  Pages
+//    are consumed in order, so the producer keeps the whole ring in flight;
 //  * online softmax in the log2 domain with quad shuffles; the O rescale is
 //    skipped when no running max moved;
 //  * every wait is bounded (about one second) and reports through a device
@@ -30,58 +34,83 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <climits>
+
 namespace pgqa {
 
 constexpr int kPage = 16;                 // tokens per KV page
-constexpr int kConsumerWarps = 4;
-constexpr int kThreads = (kConsumerWarps + 1) * 32;
-constexpr int kConsumerThreads = kConsumerWarps * 32;
 constexpr int kQRows = 8;                 // query rows (heads) per CTA: one MMA n-tile
 constexpr int kBoxElems = 64;             // 128-byte swizzle atom: 64 bf16 per row
 constexpr int kBoxBytes = kPage * kBoxElems * 2;   // one TMA box: 16 rows x 128 B
 constexpr int kMaxSplits = 256;
-constexpr unsigned long long kWaitLimitNs = 1000000000ull;   // bounded waits: 1 s
+constexpr long long kWaitLimitCycles = 2000000000ll;   // bounded waits: ~1 s at 2 GHz
 constexpr unsigned int kErrTimeoutFull = 1u;
 constexpr unsigned int kErrTimeoutEmpty = 2u;
 constexpr float kLog2e = 1.4426950408889634f;
+constexpr int kTraceEvents = 16;          // per-CTA timestamps of a trace build
+constexpr int kAllConsumersBarrier = 15;  // named barrier of every consumer warp
 
-// Stage-ring depth and CTAs per SM by head dimension.  The ring depth is a
-// multiple of the consumer-warp count: page i goes to warp i % 4 and stage
-// i % kStages, so every stage is only ever consumed by one warp, which waits
-// for its mbarrier phases strictly in order.  (A parity wait names the
-// current or the previous phase; a warp that waited on phase k of a stage
-// whose phase k-1 had not completed would pass at once.)
+// Per head dimension: the stage ring (about 128 KB of K/V in flight per SM
+// keeps HBM streaming at full rate), and how the consumer warps share the
+// pages.  Pages go round-robin to kGroups page groups; a group owns the ring
+// stages s with s % kGroups == its index, so it waits for their mbarrier
+// phases strictly in order.  The kWpg warps of a group split the head
+// dimension and exchange partial scores once per page.
 template <int HD>
 struct Cfg;
 template <>
-struct Cfg<64> { static constexpr int kStages = 8, kMinBlocks = 4; };
+struct Cfg<64> { static constexpr int kStages = 16, kGroups = 4, kWpg = 1, kMinBlocks = 3; };
 template <>
-struct Cfg<128> { static constexpr int kStages = 8, kMinBlocks = 3; };
+struct Cfg<128> { static constexpr int kStages = 8, kGroups = 4, kWpg = 1, kMinBlocks = 3; };
 template <>
-struct Cfg<256> { static constexpr int kStages = 4, kMinBlocks = 2; };
+struct Cfg<256> { static constexpr int kStages = 8, kGroups = 4, kWpg = 2, kMinBlocks = 1; };
 template <>
-struct Cfg<512> { static constexpr int kStages = 4, kMinBlocks = 1; };
+struct Cfg<512> { static constexpr int kStages = 6, kGroups = 2, kWpg = 4, kMinBlocks = 1; };
+
+template <int HD>
+struct Geo {
+    static constexpr int kStages = Cfg<HD>::kStages;
+    static constexpr int kGroups = Cfg<HD>::kGroups;
+    static constexpr int kWpg = Cfg<HD>::kWpg;
+    static constexpr int kConsumerWarps = kGroups * kWpg;
+    static constexpr int kConsumerThreads = kConsumerWarps * 32;
+    static constexpr int kThreads = kConsumerThreads + 32;      // + one producer warp
+    static constexpr int kDims = HD / kWpg;                     // head dims per consumer warp
+    static constexpr int kBlocks = kDims / 16;                  // 16-dim MMA blocks per consumer warp
+    static_assert(kStages % kGroups == 0, "each stage must belong to one page group");
+    static_assert(kBlocks >= 1, "at least one 16-dim block per warp");
+    static_assert((kQRows * HD / 4) % kConsumerThreads == 0, "merge: whole float4 outputs per thread");
+};
 
 template <int HD>
 struct Smem {
+    using G = Geo<HD>;
     static constexpr int kTile = kPage * HD * 2;                   // one (page, kv head) tile
     static constexpr int kStage = 2 * kTile;                       // K + V
-    static constexpr int kStagesBytes = Cfg<HD>::kStages * kStage;
-    static constexpr int kQOff = kStagesBytes;
-    static constexpr int kQBytes = kQRows * HD * 2;
-    static constexpr int kBarOff = kQOff + kQBytes;
-    static constexpr int kBarBytes = 2 * Cfg<HD>::kStages * 8;
+    static constexpr int kStagesBytes = G::kStages * kStage;
+    static constexpr int kXOff = kStagesBytes;                     // S exchange: float4 [groups][2][wpg][32]
+    static constexpr int kXBytes = G::kGroups * 2 * G::kWpg * 32 * 16;
+    static constexpr int kBarOff = kXOff + kXBytes;
+    static constexpr int kBarBytes = (2 * G::kStages + 2) * 8;      // full, empty, 2 merge barriers
     static constexpr int kMiscOff = kBarOff + kBarBytes;
     static constexpr int kTotal = kMiscOff + 16;
     static constexpr int kAlloc = kTotal + 1024;                   // slack for 1024-B alignment
-    // merge scratch, reusing the stage ring once every page is consumed
-    static constexpr int kObufStride = HD + 4;                     // floats; padded against bank conflicts
-    static constexpr int kObufBytes = kConsumerWarps * kQRows * kObufStride * 4;
-    static constexpr int kMlOff = kObufBytes;                      // float2 [warps][8]
-    static constexpr int kStatOff = kMlOff + kConsumerWarps * kQRows * 8;   // per-q weights, L
-    static_assert(kStatOff + kQRows * (kMaxSplits + 2) * 4 <= kStagesBytes, "merge scratch");
+    // merge of the page groups' results, in the stage ring once every page is
+    // consumed: O [groups][8][hd + 4] f32, (m, l) [groups][8], weights [8][groups + 2]
+    static constexpr int kObufStride = HD + 4;
+    static constexpr int kObufBytes = G::kGroups * kQRows * kObufStride * 4;
+    static constexpr int kMlOff = kObufBytes;
+    static constexpr int kStatOff = kMlOff + G::kGroups * kQRows * 8;
+    static_assert(kStatOff + kQRows * (G::kGroups + 2) * 4 <= kStagesBytes, "group merge scratch");
+    // last-CTA merge of the split partials, also in the stage ring: merge
+    // weights [8][kMaxSplits + 1], then two buffers of partial rows
+    static constexpr int kWtsBytes = kQRows * (kMaxSplits + 1) * 4;
+    static constexpr int kRowBytes = HD * 4;
+    static constexpr int kBufRows = ((kStagesBytes - kWtsBytes) / 2) / kRowBytes;
+    static constexpr int kBufOff0 = (kWtsBytes + 15) / 16 * 16;
+    static constexpr int kBufOff1 = kBufOff0 + kBufRows * kRowBytes;
+    static_assert(kBufRows >= kQRows, "merge buffers must hold one split of every query row");
     static_assert(kAlloc <= 227 * 1024, "shared memory");
-    static_assert(Cfg<HD>::kStages % kConsumerWarps == 0, "each stage must belong to one consumer warp");
 };
 
 struct DecodeParams {
@@ -96,7 +125,10 @@ struct DecodeParams {
     const int32_t *page_map; // may be null
     uint32_t *counters;      // may be null: separate combine kernel
     unsigned int *err;       // device error word
-    int rows, nh, nkv, window, splits, g, hsg;   // hsg = head subgroups of 8 per kv head
+    int rows, nh, nkv, window, splits, g;
+    int hsg;                 // head subgroups of up to 8 heads per kv head
+    int pack;                // rows per packing group (1 = no packing)
+    unsigned long long *trace;   // per-CTA timestamps (trace builds only), or null
 };
 
 // ---------------------------------------------------------------- PTX helpers
@@ -104,13 +136,6 @@ struct DecodeParams {
 __device__ __forceinline__ uint32_t smem_u32(const void *p)
 {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-
-__device__ __forceinline__ unsigned long long global_timer_ns()
-{
-    unsigned long long t;
-    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-    return t;
 }
 
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count)
@@ -147,16 +172,18 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
     return ok != 0;
 }
 
-// Waits for the phase with the given parity; gives up after kWaitLimitNs,
-// records `code` in the error word and returns false.
+// Waits for the phase with the given parity; gives up after about one second
+// (kWaitLimitCycles of the SM clock), records `code` in the error word and
+// returns false.  The bound uses the SM cycle counter, which is cheap to read
+// between polls; the nanosecond global timer is not.
 __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity, unsigned int *err,
                                                   unsigned int code)
 {
     if (mbar_try_wait(bar, parity))
         return true;
-    const unsigned long long t0 = global_timer_ns();
+    const long long t0 = clock64();
     while (!mbar_try_wait(bar, parity)) {
-        if (global_timer_ns() - t0 > kWaitLimitNs) {
+        if (clock64() - t0 > kWaitLimitCycles) {
             atomicOr(err, code);
             return false;
         }
@@ -179,14 +206,37 @@ __device__ __forceinline__ void tma_prefetch_map(const CUtensorMap *map)
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
 
+// 1-D bulk copy global -> shared (no tensor map); both addresses 16-B aligned,
+// size a multiple of 16.
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar)
+{
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+                 "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
+                 : "memory");
+}
+
+// Orders this thread's generic-proxy view of global memory before its later
+// async-proxy (bulk copy) reads of it.
+__device__ __forceinline__ void fence_proxy_async_global()
+{
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
 __device__ __forceinline__ void fence_proxy_async_smem()
 {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
-__device__ __forceinline__ void consumer_bar_sync()
+// Named barrier `id` over `threads` threads (a multiple of 32).
+template <int id, int threads>
+__device__ __forceinline__ void named_bar_sync()
 {
-    asm volatile("bar.sync 1, %0;" ::"n"(kConsumerThreads) : "memory");
+    asm volatile("bar.sync %0, %1;" ::"n"(id), "n"(threads) : "memory");
+}
+
+__device__ __forceinline__ void group_bar_sync(int id, int threads)
+{
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
 }
 
 __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2,
@@ -236,55 +286,152 @@ __device__ __forceinline__ uint32_t swz(int row, int u)
 
 // ---------------------------------------------------------------- merge
 //
-// One (row, head)'s S partials (m_s, l_s, O_s) -> o.  Shared verbatim by the
-// last-CTA merge and the combine kernel, so the two give the same bits:
+// The S split partials (m_s, l_s, O_s) of one (row, head) merge as
 //   M = max_s m_s,  w_s = (m_s == -inf) ? 0 : 2^(m_s - M),  L = sum_s w_s l_s,
-//   o[d] = bf16_rn( (sum_s w_s O_s[d]) / L ), or 0 when L == 0,
-// accumulated in split order with explicit fused multiply-adds.
+//   o[d] = bf16_rn( (sum_s w_s O_s[d]) / L ), or 0 when L == 0.
+// The last-CTA merge and the combine kernel run exactly these operations in
+// exactly this order, so they agree bit for bit:
+//  * merge_stats_warp (one warp): lane l takes splits l, l+32, ... in order,
+//    then a fixed xor-butterfly combines the lanes; every lane ends with the
+//    same bits because float max and addition are commutative;
+//  * O: one fused multiply-add per split, splits in increasing order.
 
-__device__ __forceinline__ float merge_stats(const float2 *ml, int splits, float *w)
+// Writes w[s] for s < S and returns L (in every lane).  1 <= S <= kMaxSplits.
+// All loads are issued up front (clamped to valid splits, then masked).
+__device__ __forceinline__ float merge_stats_warp(const float2 *ml, int S, float *w, int lane)
 {
+    constexpr int kPer = kMaxSplits / 32;
+    float2 v[kPer];
+#pragma unroll
+    for (int j = 0; j < kPer; ++j)
+        v[j] = __ldcg(&ml[min(lane + 32 * j, S - 1)]);
     float mx = -INFINITY;
-    for (int s = 0; s < splits; ++s)
-        mx = fmaxf(mx, __ldcg(&ml[s].x));
-    float L = 0.f;
-    for (int s = 0; s < splits; ++s) {
-        const float2 v = __ldcg(&ml[s]);
-        const float ws = (v.x == -INFINITY) ? 0.f : exp2f(v.x - mx);
-        w[s] = ws;
-        L = __fmaf_rn(ws, v.y, L);
+#pragma unroll
+    for (int j = 0; j < kPer; ++j) {
+        if (lane + 32 * j >= S)
+            v[j] = make_float2(-INFINITY, 0.f);
+        mx = fmaxf(mx, v[j].x);
     }
+#pragma unroll
+    for (int k = 16; k; k >>= 1)
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, k));
+    float L = 0.f;
+#pragma unroll
+    for (int j = 0; j < kPer; ++j) {
+        const int s = lane + 32 * j;
+        if (s < S) {
+            const float ws = (v[j].x == -INFINITY) ? 0.f : exp2f(v[j].x - mx);
+            w[s] = ws;
+            L = __fmaf_rn(ws, v[j].y, L);
+        }
+    }
+#pragma unroll
+    for (int k = 16; k; k >>= 1)
+        L = __fadd_rn(L, __shfl_xor_sync(0xffffffffu, L, k));
     return L;
 }
 
-__device__ __forceinline__ __nv_bfloat16 merge_value(const float *po, int hd, const float *w, int splits,
-                                                     float L)
+__device__ __forceinline__ void fma4(float4 &acc, float w, const float4 &v)
 {
-    float acc = 0.f;
-    for (int s = 0; s < splits; ++s)
-        acc = __fmaf_rn(w[s], __ldcg(po + static_cast<size_t>(s) * hd), acc);
+    acc.x = __fmaf_rn(w, v.x, acc.x);
+    acc.y = __fmaf_rn(w, v.y, acc.y);
+    acc.z = __fmaf_rn(w, v.z, acc.z);
+    acc.w = __fmaf_rn(w, v.w, acc.w);
+}
+
+__device__ __forceinline__ __nv_bfloat16 merge_finish(float acc, float L)
+{
     return L > 0.f ? __float2bfloat16_rn(__fdiv_rn(acc, L)) : __float2bfloat16_rn(0.f);
+}
+
+// Four merged outputs -> o (8-byte store).
+__device__ __forceinline__ void store_out4(__nv_bfloat16 *dst, const float4 &acc, float L)
+{
+    __nv_bfloat162 a, b;
+    a.x = merge_finish(acc.x, L);
+    a.y = merge_finish(acc.y, L);
+    b.x = merge_finish(acc.z, L);
+    b.y = merge_finish(acc.w, L);
+    uint2 u;
+    u.x = *reinterpret_cast<uint32_t *>(&a);
+    u.y = *reinterpret_cast<uint32_t *>(&b);
+    *reinterpret_cast<uint2 *>(dst) = u;
+}
+
+// Visible KV range [lo, hi] of row r (hi < lo: nothing visible).
+__device__ __forceinline__ void row_window(const DecodeParams &p, int r, int &lo, int &hi)
+{
+    const int qp = __ldg(p.qpos + r);
+    hi = p.kvpos ? __ldg(p.kvpos + r) : qp;
+    lo = p.window > 0 ? max(0, qp + 1 - p.window) : 0;
+}
+
+// ---------------------------------------------------------------- tracing
+//
+// A library built with PGQA_TRACE records, per CTA, the global timer (ns) at a
+// few phase boundaries into DecodeParams::trace; other builds compile the
+// hooks away.
+enum TraceEvent {
+    kTrStart = 0,        // CTA starts its work (after any packing exit)
+    kTrReady = 1,        // barriers initialised
+    kTrFirstTma = 2,     // producer issued its first copy
+    kTrFirstPage = 3,    // consumers hold the first page
+    kTrLoopDone = 4,     // every page consumed
+    kTrPartial = 5,      // output or partial written
+    kTrTicket = 6,       // merge ticket taken
+    kTrStats = 7,        // last CTA: merge weights ready
+    kTrMerged = 8,       // last CTA: output written
+    kTrFence = 9,        // last CTA: after the acquire fences
+    kTrIssued = 10,      // last CTA: first two merge batches issued
+    kTrBatch0 = 11,      // last CTA: first merge batch landed
+};
+
+__device__ __forceinline__ void trace_event(const DecodeParams &p, int ev)
+{
+#ifdef PGQA_TRACE
+    if (p.trace) {
+        unsigned long long t;
+        asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+        const size_t cta = (static_cast<size_t>(blockIdx.z) * gridDim.y + blockIdx.y) * gridDim.x + blockIdx.x;
+        p.trace[cta * kTraceEvents + ev] = t;
+    }
+#else
+    (void)p;
+    (void)ev;
+#endif
 }
 
 // ---------------------------------------------------------------- main kernel
 //
-// Grid (splits, nkv * hsg, rows); block = 4 consumer warps + 1 producer warp.
+// Grid (splits, nkv * hsg, rows); block = the consumer warps of Cfg<HD> + one
+// producer warp.  A CTA serves up to 8 query rows of the MMA: the heads of one
+// kv head (a subgroup of 8 when nh/nkv > 8) of one row, or, when `pack` > 1
+// and a group of `pack` consecutive rows shares its block-table span (equal
+// off) and has pairwise-overlapping windows, of all rows of the group: the
+// group's first CTA then serves them all and the others exit at once, so KV
+// shared by the rows leaves HBM and enters shared memory once.
 // HBM-bound: per (page, kv head) it moves 2 * 16 * hd * 2 bytes and runs
-// 3 * hd / 16 MMAs, far below the tensor pipe's rate.
+// 3 * hd / 16 MMAs, below the legacy tensor pipe's rate.
 template <int HD>
-__global__ void __launch_bounds__(kThreads, Cfg<HD>::kMinBlocks)
+__global__ void __launch_bounds__(Geo<HD>::kThreads, Cfg<HD>::kMinBlocks)
     decode_split_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                         const DecodeParams p)
 {
     using SM = Smem<HD>;
-    constexpr int NS = Cfg<HD>::kStages;
+    using GE = Geo<HD>;
+    constexpr int NS = GE::kStages;
+    constexpr int NG = GE::kGroups;
+    constexpr int WPG = GE::kWpg;
+    constexpr int NW = GE::kConsumerWarps;
+    constexpr int NT = GE::kConsumerThreads;
+    constexpr int KB = GE::kBlocks;           // 16-dim blocks per consumer warp
     constexpr int kChunks = HD / kBoxElems;   // TMA boxes per tile
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t s_base = smem_u32(smem);
-    const uint32_t s_q = s_base + SM::kQOff;
     const uint32_t s_full = s_base + SM::kBarOff;
     const uint32_t s_empty = s_full + NS * 8;
+    const uint32_t s_mbar = s_empty + NS * 8;      // two merge barriers
     int *s_misc = reinterpret_cast<int *>(smem + SM::kMiscOff);
 
     const int tid = threadIdx.x;
@@ -292,47 +439,139 @@ __global__ void __launch_bounds__(kThreads, Cfg<HD>::kMinBlocks)
     const int lane = tid & 31;
     const int split = blockIdx.x;
     const int kh = blockIdx.y / p.hsg;
-    const int hsg = blockIdx.y - kh * p.hsg;
-    const int row = blockIdx.z;
-    const int head0 = kh * p.g + hsg * kQRows;
-    const int nq = min(kQRows, p.g - hsg * kQRows);
+    const int hs = blockIdx.y - kh * p.hsg;
+    const int rz = blockIdx.z;
+    const int head0 = kh * p.g + hs * kQRows;
+    const int nh_sub = min(kQRows, p.g - hs * kQRows);
     const int S = p.splits;
 
-    // visible range of this row and this split's page-aligned share of it
-    const int qp = __ldg(p.qpos + row);
-    const int hi = p.kvpos ? __ldg(p.kvpos + row) : qp;
-    const int lo = p.window > 0 ? max(0, qp + 1 - p.window) : 0;
+    // ---- rows served: this CTA's own, or a packing group led by its first row.
+    // Lane i of every warp loads row g0 + i's metadata, so the check costs one
+    // round of (parallel) loads; the shuffles leave every thread with the same
+    // verdict, so the CTA decides uniformly.
+    int r0 = rz, nr = 1;
+    if (p.pack > 1) {
+        const int g0 = rz - rz % p.pack;
+        const int gn = min(p.pack, p.rows - g0);
+        if (gn > 1) {
+            const int li = lane < gn ? lane : 0;
+            const int off_i = __ldg(p.off + g0 + li);
+            int lo_i, hi_i;
+            row_window(p, g0 + li, lo_i, hi_i);
+            const bool live = lane < gn && hi_i >= lo_i;
+            const int off0 = __shfl_sync(0xffffffffu, off_i, 0);
+            const bool same = __all_sync(0xffffffffu, lane >= gn || off_i == off0);
+            int max_lo = live ? lo_i : INT_MIN, min_hi = live ? hi_i : INT_MAX;
+#pragma unroll
+            for (int k = 16; k; k >>= 1) {
+                max_lo = max(max_lo, __shfl_xor_sync(0xffffffffu, max_lo, k));
+                min_hi = min(min_hi, __shfl_xor_sync(0xffffffffu, min_hi, k));
+            }
+            const bool overlap = max_lo == INT_MIN ||
+                                 static_cast<long long>(max_lo) <= static_cast<long long>(min_hi) + 1;
+            if (same && overlap) {
+                if (rz != g0)
+                    return;               // served by the group's first CTA
+                r0 = g0;
+                nr = gn;
+            }
+        }
+    }
+    const int nq = nr * nh_sub;        // query rows in use (<= 8)
+    if (tid == 0)
+        trace_event(p, kTrStart);
+
+    // ---- union of the served rows' visible ranges; this split's page share
+    int lo_u = 0, hi_u = -1;
+    {
+        int lo_i = 1, hi_i = 0;
+        if (lane < nr)
+            row_window(p, r0 + lane, lo_i, hi_i);
+        const bool live = lane < nr && hi_i >= lo_i;
+        int lo_m = live ? lo_i : INT_MAX, hi_m = live ? hi_i : INT_MIN;
+#pragma unroll
+        for (int k = 16; k; k >>= 1) {
+            lo_m = min(lo_m, __shfl_xor_sync(0xffffffffu, lo_m, k));
+            hi_m = max(hi_m, __shfl_xor_sync(0xffffffffu, hi_m, k));
+        }
+        if (hi_m != INT_MIN) {
+            lo_u = lo_m;
+            hi_u = hi_m;
+        }
+    }
     int page_begin = 0, npages_mine = 0;
-    if (hi >= lo) {
-        const int p0 = lo >> 4;
-        const int np = (hi >> 4) - p0 + 1;
+    if (hi_u >= lo_u) {
+        const int p0 = lo_u >> 4;
+        const int np = (hi_u >> 4) - p0 + 1;
         page_begin = p0 + static_cast<int>((static_cast<long long>(split) * np) / S);
         npages_mine = p0 + static_cast<int>((static_cast<long long>(split + 1) * np) / S) - page_begin;
+    }
+
+    // ---- loads that need no barrier go out before the barrier set-up
+    const int32_t *tbl = nullptr;
+    int phys_first = 0;              // producer: physical page of lane's first-chunk page
+    const int gid = lane >> 2;       // MMA group: query row of S, d row of O^T
+    const int tig = lane & 3;        // thread in group
+    const int grp = warp / WPG;      // consumer: page group
+    const int wig = warp - grp * WPG;    // consumer: warp within the group
+    const int dq0 = wig * GE::kDims; // consumer: first head dim of this warp
+    uint32_t qa[KB][2];
+    int lo_g = 1, hi_g = 0;          // visible range of query row gid (empty if unused)
+    if (warp == NW) {
+        tbl = p.block_table + __ldg(p.off + r0) + page_begin;
+        if (lane < npages_mine) {
+            phys_first = __ldg(tbl + lane);
+            if (p.page_map)
+                phys_first = __ldg(p.page_map + phys_first);
+        }
+    } else {
+        // Query row r of the MMA is (row r0 + r / nh_sub, head head0 + r % nh_sub);
+        // rows >= nq are zero.  A-fragments of this warp's dims come straight
+        // from global memory into registers.
+#pragma unroll
+        for (int kb = 0; kb < KB; ++kb)
+            qa[kb][0] = qa[kb][1] = 0u;
+        if (gid < nq) {
+            const size_t rh = static_cast<size_t>(r0 + gid / nh_sub) * p.nh + head0 + gid % nh_sub;
+            const uint32_t *qg = reinterpret_cast<const uint32_t *>(p.q + rh * HD + dq0);
+#pragma unroll
+            for (int kb = 0; kb < KB; ++kb) {
+                qa[kb][0] = __ldg(qg + kb * 8 + tig);          // dims 16kb + 2tig, +1
+                qa[kb][1] = __ldg(qg + kb * 8 + 4 + tig);      // dims 16kb + 8 + 2tig, +1
+            }
+            row_window(p, r0 + gid / nh_sub, lo_g, hi_g);
+        }
     }
 
     if (tid == 0) {
         for (int s = 0; s < NS; ++s) {
             mbar_init(s_full + 8 * s, 1);
-            mbar_init(s_empty + 8 * s, 1);
+            mbar_init(s_empty + 8 * s, WPG);
         }
+        mbar_init(s_mbar, 1);
+        mbar_init(s_mbar + 8, 1);
         mbar_init_fence();
     }
     __syncthreads();
+    if (tid == 0)
+        trace_event(p, kTrReady);
 
-    if (warp == kConsumerWarps) {
+    if (warp == NW) {
         // ------------------------------------------------ producer warp
         if (lane == 0) {
             tma_prefetch_map(&tm_k);
             tma_prefetch_map(&tm_v);
         }
-        const int32_t *tbl = p.block_table + __ldg(p.off + row) + page_begin;
         bool ok = true;
         for (int c0 = 0; c0 < npages_mine && ok; c0 += 32) {
-            int phys = 0;
-            if (c0 + lane < npages_mine) {
-                phys = __ldg(tbl + c0 + lane);
-                if (p.page_map)
-                    phys = __ldg(p.page_map + phys);
+            int phys = phys_first;
+            if (c0 > 0) {
+                phys = 0;
+                if (c0 + lane < npages_mine) {
+                    phys = __ldg(tbl + c0 + lane);
+                    if (p.page_map)
+                        phys = __ldg(p.page_map + phys);
+                }
             }
             const int n = min(32, npages_mine - c0);
             for (int j = 0; j < n; ++j) {
@@ -353,6 +592,8 @@ __global__ void __launch_bounds__(kThreads, Cfg<HD>::kMinBlocks)
                             tma_load_3d(dk + c * kBoxBytes, &tm_k, bar, c * kBoxElems, 0, tile);
                             tma_load_3d(dv + c * kBoxBytes, &tm_v, bar, c * kBoxElems, 0, tile);
                         }
+                        if (i == 0)
+                            trace_event(p, kTrFirstTma);
                     }
                 }
             }
@@ -362,79 +603,73 @@ __global__ void __launch_bounds__(kThreads, Cfg<HD>::kMinBlocks)
     }
 
     // ---------------------------------------------------- consumer warps
-    // Q rows head0 .. head0+nq-1 of this row -> shared memory, swizzled by
-    // 16-byte unit (unit u of q-row r sits at u ^ r); rows >= nq are zero.
-    {
-        constexpr int kUnits = HD / 8;
-        const uint4 *qg = reinterpret_cast<const uint4 *>(p.q + (static_cast<size_t>(row) * p.nh + head0) * HD);
-        for (int idx = tid; idx < kQRows * kUnits; idx += kConsumerThreads) {
-            const int r = idx / kUnits, u = idx - r * kUnits;
-            uint4 v = make_uint4(0u, 0u, 0u, 0u);
-            if (r < nq)
-                v = __ldg(qg + r * kUnits + u);
-            *reinterpret_cast<uint4 *>(smem + SM::kQOff + r * HD * 2 + ((u ^ r) << 4)) = v;
-        }
-    }
-    consumer_bar_sync();
-
-    const int gid = lane >> 2;     // MMA group: query row of S, d row of O^T
-    const int tig = lane & 3;      // thread in group
-    const bool row_live = gid < nq;
-
-    float acc[HD / 16][4];
+    float acc[KB][4];              // O^T: dims dq0 + 16mt + {gid, gid+8}, query rows {2tig, 2tig+1}
 #pragma unroll
-    for (int mt = 0; mt < HD / 16; ++mt)
+    for (int mt = 0; mt < KB; ++mt)
         acc[mt][0] = acc[mt][1] = acc[mt][2] = acc[mt][3] = 0.f;
-    float m_run = -INFINITY;       // running max of q-row gid, log2 units
+    float m_run = -INFINITY;       // running max of query row gid, log2 units (same in the group's warps)
     float l_run = 0.f;             // this thread's share of the running sum
 
     // per-lane ldmatrix row/unit selectors
     const int lm_i = lane >> 3, lm_r = lane & 7;
     const int tok_sel = (lm_i >> 1) * 8 + lm_r;    // K/V token row addressed by this lane
     const int half_sel = lm_i & 1;                 // low / high 8 columns
+    float4 *sx = reinterpret_cast<float4 *>(smem + SM::kXOff) + grp * (2 * WPG * 32);
 
     bool ok = true;
-    for (int i = warp; i < npages_mine; i += kConsumerWarps) {
+    int jj = 0;                    // this group's page count
+    for (int i = grp; i < npages_mine; i += NG, ++jj) {
         const int st = i % NS;
         if (ok)
             ok = mbar_wait_bounded(s_full + 8 * st, (i / NS) & 1, p.err, kErrTimeoutFull);
-        if (!ok)
-            break;
+        if (i == 0 && wig == 0 && lane == 0)
+            trace_event(p, kTrFirstPage);
         const uint32_t sk = s_base + st * SM::kStage;
         const uint32_t sv = sk + SM::kTile;
         const int pos0 = (page_begin + i) * kPage;
 
-        // S = Q K^T over the page's 16 tokens: two n-tiles of 8 tokens
-        float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
+        // (partial) S = Q K^T over this warp's dims: two n-tiles of 8 tokens,
+        // even and odd 16-dim blocks in separate accumulators
+        float sa[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+        float sb[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+        if (ok) {
 #pragma unroll
-        for (int kc = 0; kc < HD / 16; kc += 2) {
-            uint32_t qa0, qa2, qb0, qb2;
-            {
-                const int u = kc * 2 + lm_i;    // 16-byte unit of the Q row
-                ldsm_x4(s_q + lm_r * HD * 2 + ((u ^ lm_r) << 4), qa0, qa2, qb0, qb2);
-            }
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                const int k16 = kc + h;
-                const int chunk = k16 >> 2;
-                const int u = (k16 & 3) * 2 + half_sel;
+            for (int kb = 0; kb < KB; ++kb) {
+                const int k16 = dq0 / 16 + kb;
                 uint32_t b0n0, b1n0, b0n1, b1n1;
-                ldsm_x4(sk + chunk * kBoxBytes + swz(tok_sel, u), b0n0, b1n0, b0n1, b1n1);
-                const uint32_t a0 = h ? qb0 : qa0, a2 = h ? qb2 : qa2;
-                mma_bf16_16816(s0, a0, 0u, a2, 0u, b0n0, b1n0);
-                mma_bf16_16816(s1, a0, 0u, a2, 0u, b0n1, b1n1);
+                ldsm_x4(sk + (k16 >> 2) * kBoxBytes + swz(tok_sel, (k16 & 3) * 2 + half_sel), b0n0, b1n0, b0n1,
+                        b1n1);
+                mma_bf16_16816(sa[kb & 1], qa[kb][0], 0u, qa[kb][1], 0u, b0n0, b1n0);
+                mma_bf16_16816(sb[kb & 1], qa[kb][0], 0u, qa[kb][1], 0u, b0n1, b1n1);
+            }
+        }
+        float4 sfull = make_float4(sa[0][0] + sa[1][0], sa[0][1] + sa[1][1], sb[0][0] + sb[1][0],
+                                   sb[0][1] + sb[1][1]);
+        if (WPG > 1) {
+            // full S = sum of the group's partials, in warp order
+            float4 *xb = sx + (jj & 1) * (WPG * 32);
+            xb[wig * 32 + lane] = sfull;
+            group_bar_sync(1 + grp, WPG * 32);
+            sfull = xb[lane];
+#pragma unroll
+            for (int w = 1; w < WPG; ++w) {
+                const float4 v = xb[w * 32 + lane];
+                sfull.x += v.x;
+                sfull.y += v.y;
+                sfull.z += v.z;
+                sfull.w += v.w;
             }
         }
 
-        // mask to [lo, hi], scale to log2 units
+        // mask to the query row's [lo, hi], scale to log2 units
         const int t0 = pos0 + 2 * tig;
         float x[4];
-        x[0] = (row_live && t0 >= lo && t0 <= hi) ? s0[0] * kLog2e : -INFINITY;
-        x[1] = (row_live && t0 + 1 >= lo && t0 + 1 <= hi) ? s0[1] * kLog2e : -INFINITY;
-        x[2] = (row_live && t0 + 8 >= lo && t0 + 8 <= hi) ? s1[0] * kLog2e : -INFINITY;
-        x[3] = (row_live && t0 + 9 >= lo && t0 + 9 <= hi) ? s1[1] * kLog2e : -INFINITY;
+        x[0] = (t0 >= lo_g && t0 <= hi_g) ? sfull.x * kLog2e : -INFINITY;
+        x[1] = (t0 + 1 >= lo_g && t0 + 1 <= hi_g) ? sfull.y * kLog2e : -INFINITY;
+        x[2] = (t0 + 8 >= lo_g && t0 + 8 <= hi_g) ? sfull.z * kLog2e : -INFINITY;
+        x[3] = (t0 + 9 >= lo_g && t0 + 9 <= hi_g) ? sfull.w * kLog2e : -INFINITY;
 
-        // online softmax for q-row gid (the 4 lanes of a group hold its 16 scores)
+        // online softmax for query row gid (the 4 lanes of a group hold its 16 scores)
         float mx = fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3]));
         mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
         mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
@@ -452,12 +687,12 @@ __global__ void __launch_bounds__(kThreads, Cfg<HD>::kMinBlocks)
         const uint32_t pb0 = pack_bf16x2(pr[0], pr[1]);   // P^T rows 2tig, 2tig+1 -> B frag
         const uint32_t pb1 = pack_bf16x2(pr[2], pr[3]);   // P^T rows 8+2tig, 9+2tig
 
-        // O^T columns are q-rows 2tig and 2tig+1: fetch their alphas
+        // O^T columns are query rows 2tig and 2tig+1: fetch their alphas
         const float al_a = __shfl_sync(0xffffffffu, alpha, (2 * tig) * 4);
         const float al_b = __shfl_sync(0xffffffffu, alpha, (2 * tig + 1) * 4);
         if (__any_sync(0xffffffffu, al_a != 1.f || al_b != 1.f)) {
 #pragma unroll
-            for (int mt = 0; mt < HD / 16; ++mt) {
+            for (int mt = 0; mt < KB; ++mt) {
                 acc[mt][0] *= al_a;
                 acc[mt][1] *= al_b;
                 acc[mt][2] *= al_a;
@@ -465,138 +700,230 @@ __global__ void __launch_bounds__(kThreads, Cfg<HD>::kMinBlocks)
             }
         }
 
-        // positions of this page outside [lo, hi] may hold any bits: zero their V rows
-        if (pos0 < lo || pos0 + kPage - 1 > hi) {
-            const int t = lane & 15;
-            if (pos0 + t < lo || pos0 + t > hi) {
-                uint8_t *vrow = smem + (sv - s_base) + t * 128;
-                for (int c = (lane >> 4); c < kChunks; c += 2) {
-                    uint4 *dst = reinterpret_cast<uint4 *>(vrow + c * kBoxBytes);
-#pragma unroll
-                    for (int u = 0; u < 8; ++u)
-                        dst[u] = make_uint4(0u, 0u, 0u, 0u);
+        // positions of this page outside every served row's range may hold any
+        // bits: zero this warp's dims of their V rows, so 0 * NaN cannot reach
+        // the accumulators
+        const bool edge = pos0 < lo_u || pos0 + kPage - 1 > hi_u;
+        if (edge && ok) {
+            constexpr int kUnits = GE::kDims / 8;     // 16-byte units of one token row this warp owns
+            for (int e = lane; e < kPage * kUnits; e += 32) {
+                const int t = e / kUnits;
+                if (pos0 + t < lo_u || pos0 + t > hi_u) {
+                    const int col = dq0 / 8 + (e - t * kUnits);   // 16-byte unit of the row
+                    *reinterpret_cast<uint4 *>(smem + (sv - s_base) + (col >> 3) * kBoxBytes + swz(t, col & 7)) =
+                        make_uint4(0u, 0u, 0u, 0u);
                 }
             }
             __syncwarp();
         }
 
-        // O^T += V^T P^T: hd/16 m-tiles of 16 dims
+        // O^T += V^T P^T over this warp's dims
+        if (ok) {
 #pragma unroll
-        for (int mt = 0; mt < HD / 16; ++mt) {
-            const int chunk = mt >> 2;
-            const int u = (mt & 3) * 2 + half_sel;
-            uint32_t a0, a1, a2, a3;
-            ldsm_x4_trans(sv + chunk * kBoxBytes + swz(tok_sel, u), a0, a1, a2, a3);
-            mma_bf16_16816(acc[mt], a0, a1, a2, a3, pb0, pb1);
+            for (int mt = 0; mt < KB; ++mt) {
+                const int m16 = dq0 / 16 + mt;
+                uint32_t a0, a1, a2, a3;
+                ldsm_x4_trans(sv + (m16 >> 2) * kBoxBytes + swz(tok_sel, (m16 & 3) * 2 + half_sel), a0, a1, a2, a3);
+                mma_bf16_16816(acc[mt], a0, a1, a2, a3, pb0, pb1);
+            }
         }
 
-        if (pos0 < lo || pos0 + kPage - 1 > hi)
+        if (edge)
             fence_proxy_async_smem();      // generic writes above vs the next TMA into this stage
         __syncwarp();
         if (lane == 0)
             mbar_arrive(s_empty + 8 * st);
     }
-
-    // ---------------------------------------------------- CTA-level merge
     l_run += __shfl_xor_sync(0xffffffffu, l_run, 1);
     l_run += __shfl_xor_sync(0xffffffffu, l_run, 2);
-    consumer_bar_sync();      // every page consumed: the stage ring is free
+    named_bar_sync<kAllConsumersBarrier, NT>();      // every page consumed: the stage ring is free
+    if (tid == 0)
+        trace_event(p, kTrLoopDone);
 
+    // ---------------------------------------------------- merge of the page groups
     float *obuf = reinterpret_cast<float *>(smem);
     float2 *mlbuf = reinterpret_cast<float2 *>(smem + SM::kMlOff);
     float *stat = reinterpret_cast<float *>(smem + SM::kStatOff);
     {
-        float *ob = obuf + warp * kQRows * SM::kObufStride;
+        float *ob = obuf + grp * kQRows * SM::kObufStride;
 #pragma unroll
-        for (int mt = 0; mt < HD / 16; ++mt) {
-            const int d = mt * 16 + gid;
+        for (int mt = 0; mt < KB; ++mt) {
+            const int d = dq0 + mt * 16 + gid;
             ob[(2 * tig) * SM::kObufStride + d] = acc[mt][0];
             ob[(2 * tig + 1) * SM::kObufStride + d] = acc[mt][1];
             ob[(2 * tig) * SM::kObufStride + d + 8] = acc[mt][2];
             ob[(2 * tig + 1) * SM::kObufStride + d + 8] = acc[mt][3];
         }
-        if (tig == 0)
-            mlbuf[warp * kQRows + gid] = make_float2(m_run, l_run);
+        if (wig == 0 && tig == 0)
+            mlbuf[grp * kQRows + gid] = make_float2(m_run, l_run);
     }
-    consumer_bar_sync();
-
-    // per q-row: weights of the 4 warps' partials, the CTA's (M, L)
+    named_bar_sync<kAllConsumersBarrier, NT>();
     if (tid < nq) {
         float mx = -INFINITY;
-        for (int w = 0; w < kConsumerWarps; ++w)
-            mx = fmaxf(mx, mlbuf[w * kQRows + tid].x);
+        for (int g = 0; g < NG; ++g)
+            mx = fmaxf(mx, mlbuf[g * kQRows + tid].x);
         float L = 0.f;
-        for (int w = 0; w < kConsumerWarps; ++w) {
-            const float2 v = mlbuf[w * kQRows + tid];
+        for (int g = 0; g < NG; ++g) {
+            const float2 v = mlbuf[g * kQRows + tid];
             const float ws = (v.x == -INFINITY) ? 0.f : exp2f(v.x - mx);
-            stat[tid * (kConsumerWarps + 2) + w] = ws;
+            stat[tid * (NG + 2) + g] = ws;
             L = __fmaf_rn(ws, v.y, L);
         }
-        stat[tid * (kConsumerWarps + 2) + kConsumerWarps] = L;
-        stat[tid * (kConsumerWarps + 2) + kConsumerWarps + 1] = mx;
-        if (S > 1)
-            p.part_ml[(static_cast<size_t>(row) * p.nh + head0 + tid) * S + split] = make_float2(mx, L);
-    }
-    consumer_bar_sync();
-
-    for (int idx = tid; idx < nq * HD; idx += kConsumerThreads) {
-        const int q = idx / HD, d = idx - q * HD;
-        const float *st = stat + q * (kConsumerWarps + 2);
-        float o = 0.f;
-#pragma unroll
-        for (int w = 0; w < kConsumerWarps; ++w)
-            o = __fmaf_rn(st[w], obuf[(w * kQRows + q) * SM::kObufStride + d], o);
-        const size_t rh = static_cast<size_t>(row) * p.nh + head0 + q;
-        if (S == 1) {
-            const float L = st[kConsumerWarps];
-            p.o[rh * HD + d] = L > 0.f ? __float2bfloat16_rn(__fdiv_rn(o, L)) : __float2bfloat16_rn(0.f);
-        } else {
-            p.part_o[(rh * S + split) * HD + d] = o;
+        stat[tid * (NG + 2) + NG] = L;
+        if (S > 1) {
+            const size_t rh = static_cast<size_t>(r0 + tid / nh_sub) * p.nh + head0 + tid % nh_sub;
+            p.part_ml[rh * S + split] = make_float2(mx, L);
         }
     }
+    named_bar_sync<kAllConsumersBarrier, NT>();
+    for (int idx = tid; idx < nq * HD; idx += NT) {
+        const int q = idx / HD, d = idx - q * HD;
+        const float *st = stat + q * (NG + 2);
+        float o = 0.f;
+#pragma unroll
+        for (int g = 0; g < NG; ++g)
+            o = __fmaf_rn(st[g], obuf[(g * kQRows + q) * SM::kObufStride + d], o);
+        const size_t rh = static_cast<size_t>(r0 + q / nh_sub) * p.nh + head0 + q % nh_sub;
+        if (S == 1)
+            p.o[rh * HD + d] = merge_finish(o, st[NG]);
+        else
+            p.part_o[(rh * S + split) * HD + d] = o;
+    }
+    if (tid == 0)
+        trace_event(p, kTrPartial);
     if (S == 1 || p.counters == nullptr)
         return;
 
     // ---------------------------------------------------- last-CTA merge
+    // This thread's generic writes to the ring precede the merge's bulk copies
+    // into it (no copy is in flight here, so the fence does not wait on one).
+    fence_proxy_async_smem();
     __threadfence();
-    consumer_bar_sync();
-    const int tile_id = (row * p.nkv + kh) * p.hsg + hsg;
+    named_bar_sync<kAllConsumersBarrier, NT>();
+    const int tile_id = (r0 * p.nkv + kh) * p.hsg + hs;
     if (tid == 0)
         s_misc[0] = static_cast<int>(atomicAdd(p.counters + tile_id, 1u));
-    consumer_bar_sync();
+    named_bar_sync<kAllConsumersBarrier, NT>();
+    if (tid == 0)
+        trace_event(p, kTrTicket);
     if (s_misc[0] != S - 1)
         return;
     __threadfence();
-    float *wts = stat;      // [nq][S + 1]
-    if (tid < nq) {
-        const size_t rh = static_cast<size_t>(row) * p.nh + head0 + tid;
-        wts[tid * (S + 1) + S] = merge_stats(p.part_ml + rh * S, S, wts + tid * (S + 1));
-    }
-    consumer_bar_sync();
-    for (int idx = tid; idx < nq * HD; idx += kConsumerThreads) {
-        const int q = idx / HD, d = idx - q * HD;
-        const size_t rh = static_cast<size_t>(row) * p.nh + head0 + q;
-        p.o[rh * HD + d] = merge_value(p.part_o + rh * S * HD + d, HD, wts + q * (S + 1), S, wts[q * (S + 1) + S]);
-    }
+    fence_proxy_async_global();      // the other CTAs' partials, now visible, feed bulk copies
     if (tid == 0)
+        trace_event(p, kTrFence);
+
+    // Partial rows (query row q, split s) stream through two shared buffers by
+    // bulk copy; batch b holds splits [b*SB, b*SB + SB) of every query row.
+    // The buffers follow the weights, which the group-merge scratch no longer
+    // needs.
+    float *wts = reinterpret_cast<float *>(smem);  // [8][kMaxSplits + 1]; entry kMaxSplits = L
+    const int SB = SM::kBufRows / nq;
+    const int nb = (S + SB - 1) / SB;
+    auto issue = [&](int b) {
+        const int s0 = b * SB, sn = min(SB, S - s0);
+        const uint32_t buf = s_base + ((b & 1) ? SM::kBufOff1 : SM::kBufOff0);
+        const uint32_t bar = s_mbar + 8 * (b & 1);
+        mbar_arrive_expect_tx(bar, static_cast<uint32_t>(nq * sn * SM::kRowBytes));
+        for (int q = 0; q < nq; ++q) {
+            const size_t rh = static_cast<size_t>(r0 + q / nh_sub) * p.nh + head0 + q % nh_sub;
+            for (int j = 0; j < sn; ++j)
+                bulk_load(buf + (q * SB + j) * SM::kRowBytes, p.part_o + (rh * S + s0 + j) * HD, SM::kRowBytes,
+                          bar);
+        }
+    };
+    if (tid == 0) {
+        issue(0);
+        if (nb > 1)
+            issue(1);
+        trace_event(p, kTrIssued);
+    }
+    for (int q = warp; q < nq; q += NW) {
+        const size_t rh = static_cast<size_t>(r0 + q / nh_sub) * p.nh + head0 + q % nh_sub;
+        const float L = merge_stats_warp(p.part_ml + rh * S, S, wts + q * (kMaxSplits + 1), lane);
+        if (lane == 0)
+            wts[q * (kMaxSplits + 1) + kMaxSplits] = L;
+    }
+    named_bar_sync<kAllConsumersBarrier, NT>();      // merge weights visible to every thread
+    if (tid == 0)
+        trace_event(p, kTrStats);
+
+    constexpr int kVec = HD / 4;                               // float4 per query row
+    constexpr int kOwn = kQRows * kVec / NT;                   // float4 outputs per thread
+    float4 oacc[kOwn];
+#pragma unroll
+    for (int k = 0; k < kOwn; ++k)
+        oacc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+    bool mok = true;
+    for (int b = 0; b < nb; ++b) {
+        if (mok)
+            mok = mbar_wait_bounded(s_mbar + 8 * (b & 1), (b >> 1) & 1, p.err, kErrTimeoutFull);
+        if (b == 0 && tid == 0)
+            trace_event(p, kTrBatch0);
+        const float *buf = reinterpret_cast<const float *>(smem + ((b & 1) ? SM::kBufOff1 : SM::kBufOff0));
+        const int s0 = b * SB, sn = min(SB, S - s0);
+        for (int j = 0; j < sn; ++j) {
+#pragma unroll
+            for (int k = 0; k < kOwn; ++k) {
+                const int e = tid + k * NT;
+                const int q = e / kVec, d4 = e - q * kVec;
+                if (q < nq)
+                    fma4(oacc[k], wts[q * (kMaxSplits + 1) + s0 + j],
+                         *reinterpret_cast<const float4 *>(buf + (q * SB + j) * HD + d4 * 4));
+            }
+        }
+        named_bar_sync<kAllConsumersBarrier, NT>();      // every thread is done with this buffer
+        if (tid == 0 && b + 2 < nb && mok)
+            issue(b + 2);
+    }
+#pragma unroll
+    for (int k = 0; k < kOwn; ++k) {
+        const int e = tid + k * NT;
+        const int q = e / kVec, d4 = e - q * kVec;
+        if (q < nq) {
+            const size_t rh = static_cast<size_t>(r0 + q / nh_sub) * p.nh + head0 + q % nh_sub;
+            store_out4(p.o + rh * HD + d4 * 4, oacc[k], wts[q * (kMaxSplits + 1) + kMaxSplits]);
+        }
+    }
+    if (tid == 0) {
         p.counters[tile_id] = 0u;      // ready for the next call, which is ordered after this kernel
+        trace_event(p, kTrMerged);
+    }
 }
 
 // ---------------------------------------------------------------- combine kernel
 //
-// One CTA per (row, head): merges the S partials with the same routine as the
-// last-CTA path.  Reads rows*nh*S*(hd+2)*4 bytes, writes rows*nh*hd*2.
+// One CTA per (row, head), one thread per 4 dims: merges the S partials with
+// the same statistics routine and the same per-element fused multiply-add
+// order as the last-CTA path.  Reads rows*nh*S*(hd+2)*4 bytes, writes
+// rows*nh*hd*2.
 template <int HD>
-__global__ void __launch_bounds__(128) decode_combine_kernel(const DecodeParams p)
+constexpr int combine_threads()
+{
+    return HD / 4 < 32 ? 32 : HD / 4;
+}
+
+template <int HD>
+__global__ void __launch_bounds__(combine_threads<HD>()) decode_combine_kernel(const DecodeParams p)
 {
     __shared__ float wts[kMaxSplits + 1];
     const size_t rh = blockIdx.x;
     const int S = p.splits;
-    if (threadIdx.x == 0)
-        wts[S] = merge_stats(p.part_ml + rh * S, S, wts);
+    if (threadIdx.x < 32) {
+        const float L = merge_stats_warp(p.part_ml + rh * S, S, wts, threadIdx.x);
+        if (threadIdx.x == 0)
+            wts[kMaxSplits] = L;
+    }
     __syncthreads();
-    for (int d = threadIdx.x; d < HD; d += blockDim.x)
-        p.o[rh * HD + d] = merge_value(p.part_o + rh * S * HD + d, HD, wts, S, wts[S]);
+    const int d4 = threadIdx.x;
+    if (d4 < HD / 4) {
+        const float4 *po = reinterpret_cast<const float4 *>(p.part_o + rh * S * HD) + d4;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 8
+        for (int s = 0; s < S; ++s)
+            fma4(acc, wts[s], __ldcg(po + static_cast<size_t>(s) * (HD / 4)));
+        store_out4(p.o + rh * HD + d4 * 4, acc, wts[kMaxSplits]);
+    }
 }
 
 }  // namespace pgqa

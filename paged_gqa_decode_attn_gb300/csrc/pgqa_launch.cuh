@@ -28,12 +28,12 @@ cudaError_t launch_decode(const LaunchArgs &a, bool set_attr)
     }
     const DecodeParams &p = a.p;
     dim3 grid(p.splits, p.nkv * p.hsg, p.rows);
-    decode_split_kernel<HD><<<grid, kThreads, Smem<HD>::kAlloc, a.stream>>>(*a.tm_k, *a.tm_v, p);
+    decode_split_kernel<HD><<<grid, Geo<HD>::kThreads, Smem<HD>::kAlloc, a.stream>>>(*a.tm_k, *a.tm_v, p);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess)
         return e;
     if (p.splits > 1 && p.counters == nullptr) {
-        decode_combine_kernel<HD><<<p.rows * p.nh, 128, 0, a.stream>>>(p);
+        decode_combine_kernel<HD><<<p.rows * p.nh, combine_threads<HD>(), 0, a.stream>>>(p);
         e = cudaGetLastError();
     }
     return e;

@@ -71,13 +71,16 @@ def test_choose_splits_rule(lib):
                 s = pgqa.choose_splits(kv, rows, nkv, rows, num_sms=152)
                 pages = (kv + 15) // 16
                 assert 1 <= s <= pgqa.MAX_SPLITS
-                assert s == 1 or s <= pages // 4           # at least four pages per split
+                assert s == 1 or s <= pages // 2           # at least two pages per split
                 assert s == 1 or rows * nkv * (s - 1) < 4 * 152   # no more splits than needed
-    # the named workloads (152 SMs)
-    assert pgqa.choose_splits(256, 1, 2, 1, num_sms=152) == 4
-    assert pgqa.choose_splits(1024, 4, 8, 4, num_sms=152) == 16
-    assert pgqa.choose_splits(32768, 1, 4, 1, num_sms=152) == 152
+    # the named workloads (152 SMs): one wave for few tiles, ~4 CTAs per SM for many
+    assert pgqa.choose_splits(256, 1, 2, 1, num_sms=152) == 8           # capped at 2 pages per split
+    assert pgqa.choose_splits(1024, 4, 8, 1, num_sms=152) == 19         # 4 rows of one sequence packed
+    assert pgqa.choose_splits(1024, 4, 8, 4, num_sms=152) == 5          # 4 independent rows
+    assert pgqa.choose_splits(32768, 1, 4, 1, num_sms=152) == 38
     assert pgqa.choose_splits(4096, 64, 8, 64, num_sms=152) == 2
+    # nseq outside [1, rows] means every row is its own sequence
+    assert pgqa.choose_splits(1024, 4, 8, 0, num_sms=152) == pgqa.choose_splits(1024, 4, 8, 4, num_sms=152)
     # without a device the current-device form falls back to 152 SMs
     assert pgqa.choose_splits(32768, 1, 4, 1) >= 1
 
@@ -103,7 +106,8 @@ def call(lib, rows=1, nh=8, nkv=2, hd=128, window=0, splits=1, o=FAKE, part=FAKE
     (dict(splits=257), -7), (dict(o=None), -1), (dict(q=None), -1), (dict(k=None), -1),
     (dict(v=None), -1), (dict(bt=None), -1), (dict(off=None), -1), (dict(qpos=None), -1),
     (dict(splits=2, part=None), -1), (dict(k=FAKE + 8), -3), (dict(v=FAKE + 2), -3),
-    (dict(q=FAKE + 4), -3), (dict(splits=2, part=FAKE + 4), -3), (dict(rows=70000), -1),
+    (dict(q=FAKE + 4), -3), (dict(o=FAKE + 8), -3), (dict(splits=2, part=FAKE + 4), -3),
+    (dict(rows=70000), -1),
 ])
 def test_bad_arguments_are_rejected_before_any_cuda_call(lib, kw, code):
     assert call(lib, **kw) == code

@@ -162,6 +162,38 @@ def test_ragged_rows_offsets_kvpos_and_empty_row(window):
             assert np.all(a[4] == 0), "row with no visible position must be zero"
 
 
+def packing_case(kind, seed=31, nh=16, nkv=8, hd=256, window=300):
+    """Four rows of one table (g = 2: groups of four rows pack when their windows overlap)."""
+    rng = wl.Lcg(seed)
+    npages = 40
+    n = npages * nkv * 16 * hd
+    k = wl.draw_bf16(rng, n, "sym")
+    v = wl.draw_bf16(rng, n, "sym")
+    rows = 4
+    q = wl.draw_bf16(rng, rows * nh * hd, "sym")
+    bt = wl.lcg_permutation(npages, seed + 1)
+    off = np.zeros(rows, dtype=np.int32)
+    if kind == "overlap":        # packed: windows [301..600] .. [330..629] overlap
+        qpos = np.array([600, 610, 620, 629], dtype=np.int32)
+    elif kind == "disjoint":     # refused: row 0's window ends before the others start
+        qpos = np.array([100, 610, 620, 629], dtype=np.int32)
+    else:                        # refused: one row has its own span
+        qpos = np.array([300, 301, 302, 303], dtype=np.int32)
+        off = np.array([0, 0, 5, 0], dtype=np.int32)
+    return wl.Case(f"pack_{kind}", nh, nkv, hd, window, rows, q, k, v, bt, off, qpos, ctx=640, npg=npages)
+
+
+@pytest.mark.parametrize("kind", ["overlap", "disjoint", "mixed_off"])
+@pytest.mark.parametrize("splits", [1, 3, 19])
+def test_row_packing_groups(kind, splits):
+    from gpu_util import DevCase
+    c = packing_case(kind)
+    d = DevCase(c, splits)
+    a = d.result(counters=True)
+    check_parity(c, a, f"{kind} s{splits}")
+    assert np.array_equal(a, d.result(counters=False))
+
+
 def test_nan_outside_windows_never_reaches_output():
     """Slots of read pages outside every row's [lo, hi] and whole unread pages hold NaN."""
     from gpu_util import DevCase, first_difference
