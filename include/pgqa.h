@@ -42,6 +42,7 @@ extern "C" {
 #define PGQA_ERR_TENSOR_MAP (-5)         /* the driver refused the TMA descriptor */
 #define PGQA_ERR_DEVICE_TIMEOUT (-6)     /* a kernel gave up a bounded wait (see pgqa_device_status) */
 #define PGQA_ERR_TOO_MANY_SPLITS (-7)    /* splits > PGQA_MAX_SPLITS */
+#define PGQA_ERR_NOALLOC_TOO_LARGE (-8)  /* call needs more scratch than pgqa_attn_decode_noalloc has */
 
 #define PGQA_PAGE_TOKENS 16
 #define PGQA_MAX_SPLITS 256
@@ -132,6 +133,35 @@ int pgqa_device_status(void);
  * normal one.
  */
 int pgqa_trace_buffer(void *device_buffer, size_t bytes);
+
+/*
+ * pgqa_attn_decode without caller scratch.  The pages describe no such entry
+ * point; this one exists for callers that cannot allocate device memory for
+ * `part` and `counters` (a plugin inside a host runtime that owns all device
+ * allocations, or a caller that must not call cudaMalloc on its path).
+ *
+ * Same arguments and result as pgqa_attn_decode with the last-CTA merge,
+ * minus part and counters: those live in one static device array of this
+ * library (PGQA_NOALLOC_MAX_COUNTERS uint32 counters followed by
+ * PGQA_NOALLOC_MAX_PART_BYTES of partials, about 8.1 MiB), which every GPU
+ * that loads the library holds until the process exits.  Calls needing more
+ * (pgqa_decode_part_bytes or pgqa_decode_counter_count above those limits)
+ * return PGQA_ERR_NOALLOC_TOO_LARGE and enqueue nothing.
+ *
+ * It allocates nothing.  Each call clears the counters it uses with
+ * cudaMemsetAsync on `stream`, then enqueues the decode there.  The first
+ * call on a device looks up the array's device address (cudaGetSymbolAddress,
+ * with that device current); make that first call before any stream capture.
+ * Every call on a device shares the one array and finds it as the previous
+ * call left it, so calls that may overlap on the GPU (different streams
+ * without ordering between them) race and must not be issued.
+ */
+#define PGQA_NOALLOC_MAX_COUNTERS 16384
+#define PGQA_NOALLOC_MAX_PART_BYTES (8 * 1024 * 1024)
+int pgqa_attn_decode_noalloc(void *o, const void *q, const void *k_pool, const void *v_pool,
+                             const int32_t *block_table, const int32_t *off, const int32_t *qpos,
+                             const int32_t *kvpos, int rows, int nh, int nkv, int hd, int window,
+                             int splits, const int32_t *page_map, void *stream);
 
 /* Static, human-readable name of a status code. */
 const char *pgqa_strerror(int status);

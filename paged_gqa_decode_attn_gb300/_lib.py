@@ -16,6 +16,9 @@ PGQA_ERR_CUDA = -4
 PGQA_ERR_TENSOR_MAP = -5
 PGQA_ERR_DEVICE_TIMEOUT = -6
 PGQA_ERR_TOO_MANY_SPLITS = -7
+PGQA_ERR_NOALLOC_TOO_LARGE = -8
+NOALLOC_MAX_COUNTERS = 16384
+NOALLOC_MAX_PART_BYTES = 8 * 1024 * 1024
 PAGE_TOKENS = 16
 MAX_SPLITS = 256
 
@@ -31,6 +34,7 @@ SIGNATURES = {
     "pgqa_strerror": (ctypes.c_char_p, [_I]),
     "pgqa_version": (_I, []),
     "pgqa_trace_buffer": (_I, [_P, ctypes.c_size_t]),
+    "pgqa_attn_decode_noalloc": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P]),
 }
 
 
@@ -98,6 +102,17 @@ def attn_decode(o, part, q, k_pool, v_pool, block_table, off, qpos, kvpos, rows:
                                  int(window), int(splits), _ptr(counters), _ptr(page_map), _stream(stream))
     if st != PGQA_OK:
         raise PgqaError(st, "attn_decode")
+
+
+def attn_decode_noalloc(o, q, k_pool, v_pool, block_table, off, qpos, kvpos, rows: int, nh: int, nkv: int,
+                        hd: int, window: int, splits: int, page_map=None, stream=None) -> None:
+    """``pgqa_attn_decode_noalloc``: the decode with its scratch in the library's
+    static device array, for callers that cannot allocate device memory."""
+    st = load().pgqa_attn_decode_noalloc(_ptr(o), _ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(block_table), _ptr(off),
+                                         _ptr(qpos), _ptr(kvpos), int(rows), int(nh), int(nkv), int(hd), int(window),
+                                         int(splits), _ptr(page_map), _stream(stream))
+    if st != PGQA_OK:
+        raise PgqaError(st, "attn_decode_noalloc")
 
 
 def choose_splits(kv_len_eff: int, rows: int, nkv: int, nseq: int, num_sms: int | None = None) -> int:

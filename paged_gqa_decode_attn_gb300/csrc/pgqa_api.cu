@@ -168,6 +168,7 @@ const char *pgqa_strerror(int status)
     case PGQA_ERR_TENSOR_MAP: return "TMA descriptor rejected by the driver";
     case PGQA_ERR_DEVICE_TIMEOUT: return "a kernel gave up a bounded wait";
     case PGQA_ERR_TOO_MANY_SPLITS: return "splits above PGQA_MAX_SPLITS";
+    case PGQA_ERR_NOALLOC_TOO_LARGE: return "call needs more scratch than the no-allocation entry point holds";
     default: return "unknown status";
     }
 }
