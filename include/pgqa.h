@@ -70,9 +70,13 @@ extern "C" {
  *   counters    merge counters, NULL or at least
  *               pgqa_decode_counter_count(rows, nh, nkv) uint32 slots.  Zero
  *               them once before first use; every successful call leaves them
- *               zero again.  Non-NULL: the last CTA of each tile merges the
- *               split partials.  NULL: a separate combine kernel merges them.
- *               Both give bit-identical o.
+ *               zero again.  Non-NULL: the split partials merge inside the
+ *               kernel -- on chip, through the distributed shared memory of a
+ *               thread-block cluster holding a tile's splits, when splits is 2,
+ *               4 or 8 and the device can co-schedule such a cluster;
+ *               otherwise in the tile's last CTA, found through the counters.
+ *               NULL: a separate combine kernel merges them.  All give
+ *               bit-identical o.
  *   page_map    int32 map from block-table entries to physical pages, or NULL.
  *
  * Host scalars: rows >= 0, nh, nkv > 0 with nh % nkv == 0, hd in
@@ -125,8 +129,9 @@ int pgqa_device_status(void);
 
 /*
  * Debug tracing.  In a library built with PGQA_TRACE defined, every split-kernel
- * CTA of later calls writes 16 uint64 slots (global timer, ns) at phase
- * boundaries into device_buffer, at [cta][event] with
+ * CTA of later calls writes 32 uint64 slots into device_buffer: the global
+ * timer (ns) at up to 16 phase boundaries in slots 0-15 and the SM cycle
+ * counter at the same moments in slots 16-31, at [cta][slot] with
  * cta = (blockIdx.z * gridDim.y + blockIdx.y) * gridDim.x + blockIdx.x, when
  * the buffer holds the whole grid; NULL turns it off.  Returns PGQA_OK in a
  * trace build and PGQA_ERR_INVALID_ARGUMENT (with no effect on kernels) in a

@@ -26,7 +26,33 @@ struct DeviceState {
     int num_sms = 0;
     unsigned int *err = nullptr;
     bool attr_set[4] = {false, false, false, false};
+    int cluster_cap[4][5] = {{-1, -1, -1, -1, -1}, {-1, -1, -1, -1, -1}, {-1, -1, -1, -1, -1},
+                             {-1, -1, -1, -1, -1}};   // [hd][log2 cluster]: resident clusters, -1 unknown
 };
+
+// Cluster size for the on-chip merge of `splits` CTAs, or 0 to merge through
+// global memory.  Caller holds g_mutex.
+int on_chip_cluster(DeviceState *s, int hi, int hd, int splits)
+{
+    int lg = -1;
+    switch (splits) {
+    case 2: lg = 1; break;
+    case 4: lg = 2; break;
+    case 8: lg = 3; break;
+    default: return 0;          // 16-CTA clusters rarely all fit beside each other
+
+    }
+    int &cap = s->cluster_cap[hi][lg];
+    if (cap < 0) {
+        switch (hd) {
+        case 64: cap = pgqa::cluster_capacity_hd64(splits); break;
+        case 128: cap = pgqa::cluster_capacity_hd128(splits); break;
+        case 256: cap = pgqa::cluster_capacity_hd256(splits); break;
+        default: cap = pgqa::cluster_capacity_hd512(splits); break;
+        }
+    }
+    return cap >= 1 ? splits : 0;
+}
 
 std::mutex g_mutex;
 DeviceState g_dev[kMaxDevices];
@@ -211,6 +237,14 @@ int pgqa_choose_splits_for(int kv_len_eff, int rows, int nkv, int nseq, int num_
         cap = 1;
     if (s > cap)
         s = cap;
+    // Up to 24 splits, take a power of two no larger than 8: 2, 4 and 8
+    // splits merge on chip, in one thread-block cluster per tile.
+    if (s <= 24) {
+        long long p2 = 1;
+        while (p2 * 2 <= s && p2 < 8)
+            p2 *= 2;
+        s = p2;
+    }
     if (s > PGQA_MAX_SPLITS)
         s = PGQA_MAX_SPLITS;
     if (s < 1)
@@ -297,6 +331,7 @@ int pgqa_attn_decode(void *o, void *part, const void *q, const void *k_pool, con
     p.hsg = hsg;
     p.pack = g <= pgqa::kQRows ? pgqa::kQRows / g : 1;
     p.trace = nullptr;
+    p.cluster = 0;
     a.stream = static_cast<cudaStream_t>(stream);
 
     // The lock covers set-up and the (asynchronous) launch itself, so the
@@ -310,6 +345,7 @@ int pgqa_attn_decode(void *o, void *part, const void *q, const void *k_pool, con
     if ((st = pool_map(k_pool, hd, &tk)) != PGQA_OK || (st = pool_map(v_pool, hd, &tv)) != PGQA_OK)
         return st;
     p.err = s->err;
+    p.cluster = counters ? on_chip_cluster(s, hi, hd, splits) : 0;
     if (g_trace && static_cast<size_t>(splits) * nkv * hsg * rows * pgqa::kTraceEvents * 8 <= g_trace_bytes)
         p.trace = g_trace;
     a.tm_k = &tk;

@@ -43,11 +43,12 @@ constexpr int kQRows = 8;                 // query rows (heads) per CTA: one MMA
 constexpr int kBoxElems = 64;             // 128-byte swizzle atom: 64 bf16 per row
 constexpr int kBoxBytes = kPage * kBoxElems * 2;   // one TMA box: 16 rows x 128 B
 constexpr int kMaxSplits = 256;
+constexpr int kMaxCluster = 8;            // largest thread-block cluster for the on-chip merge
 constexpr long long kWaitLimitCycles = 2000000000ll;   // bounded waits: ~1 s at 2 GHz
 constexpr unsigned int kErrTimeoutFull = 1u;
 constexpr unsigned int kErrTimeoutEmpty = 2u;
 constexpr float kLog2e = 1.4426950408889634f;
-constexpr int kTraceEvents = 16;          // per-CTA timestamps of a trace build
+constexpr int kTraceEvents = 32;          // per-CTA slots of a trace build: 16 events x (ns, SM cycles)
 constexpr int kAllConsumersBarrier = 15;  // named barrier of every consumer warp
 
 // Per head dimension: the stage ring (about 128 KB of K/V in flight per SM
@@ -91,7 +92,7 @@ struct Smem {
     static constexpr int kXOff = kStagesBytes;                     // S exchange: float4 [groups][2][wpg][32]
     static constexpr int kXBytes = G::kGroups * 2 * G::kWpg * 32 * 16;
     static constexpr int kBarOff = kXOff + kXBytes;
-    static constexpr int kBarBytes = (2 * G::kStages + 2) * 8;      // full, empty, 2 merge barriers
+    static constexpr int kBarBytes = 2 * G::kStages * 8;            // full, empty
     static constexpr int kMiscOff = kBarOff + kBarBytes;
     static constexpr int kTotal = kMiscOff + 16;
     static constexpr int kAlloc = kTotal + 1024;                   // slack for 1024-B alignment
@@ -102,14 +103,16 @@ struct Smem {
     static constexpr int kMlOff = kObufBytes;
     static constexpr int kStatOff = kMlOff + G::kGroups * kQRows * 8;
     static_assert(kStatOff + kQRows * (G::kGroups + 2) * 4 <= kStagesBytes, "group merge scratch");
-    // last-CTA merge of the split partials, also in the stage ring: merge
-    // weights [8][kMaxSplits + 1], then two buffers of partial rows
+    // last-CTA merge of the split partials: merge weights [8][kMaxSplits + 1],
+    // also in the stage ring
     static constexpr int kWtsBytes = kQRows * (kMaxSplits + 1) * 4;
-    static constexpr int kRowBytes = HD * 4;
-    static constexpr int kBufRows = ((kStagesBytes - kWtsBytes) / 2) / kRowBytes;
-    static constexpr int kBufOff0 = (kWtsBytes + 15) / 16 * 16;
-    static constexpr int kBufOff1 = kBufOff0 + kBufRows * kRowBytes;
-    static_assert(kBufRows >= kQRows, "merge buffers must hold one split of every query row");
+    static_assert(kWtsBytes <= kStagesBytes, "merge weights");
+    // cluster merge, after the group-merge scratch: this CTA's O [8][hd] and
+    // (M, L) [8] for its peers to read, then the merge weights [8][kMaxCluster + 1]
+    static constexpr int kCpartOff = (kStatOff + kQRows * (G::kGroups + 2) * 4 + 15) / 16 * 16;
+    static constexpr int kCmlOff = kCpartOff + kQRows * HD * 4;
+    static constexpr int kCwOff = kCmlOff + kQRows * 8;
+    static_assert(kCwOff + kQRows * (kMaxCluster + 1) * 4 <= kStagesBytes, "cluster merge scratch");
     static_assert(kAlloc <= 227 * 1024, "shared memory");
 };
 
@@ -128,6 +131,7 @@ struct DecodeParams {
     int rows, nh, nkv, window, splits, g;
     int hsg;                 // head subgroups of up to 8 heads per kv head
     int pack;                // rows per packing group (1 = no packing)
+    int cluster;             // > 1: the splits of a tile are one cluster of this size, merged on chip
     unsigned long long *trace;   // per-CTA timestamps (trace builds only), or null
 };
 
@@ -206,20 +210,43 @@ __device__ __forceinline__ void tma_prefetch_map(const CUtensorMap *map)
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
 
-// 1-D bulk copy global -> shared (no tensor map); both addresses 16-B aligned,
-// size a multiple of 16.
-__device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar)
+// Ticket: atomic add with release (this CTA's partials, ordered before by a
+// CTA barrier, become visible with it) and acquire (the other CTAs'
+// partials are visible to whoever observes the final count, and through a
+// following CTA barrier to the rest of the CTA).
+__device__ __forceinline__ unsigned int atomic_add_acq_rel(unsigned int *addr, unsigned int v)
 {
-    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
-                 "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
-                 : "memory");
+    unsigned int old;
+    asm volatile("atom.add.acq_rel.gpu.u32 %0, [%1], %2;" : "=r"(old) : "l"(addr), "r"(v) : "memory");
+    return old;
 }
 
-// Orders this thread's generic-proxy view of global memory before its later
-// async-proxy (bulk copy) reads of it.
-__device__ __forceinline__ void fence_proxy_async_global()
+// Thread-block cluster helpers (distributed shared memory).
+__device__ __forceinline__ void cluster_sync_all()
 {
-    asm volatile("fence.proxy.async.global;" ::: "memory");
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// Address of this CTA's shared location `addr` in the shared memory of cluster CTA `rank`.
+__device__ __forceinline__ uint32_t map_to_cta(uint32_t addr, int rank)
+{
+    uint32_t out;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(out) : "r"(addr), "r"(rank));
+    return out;
+}
+
+__device__ __forceinline__ float ld_dsmem_f32(uint32_t addr)
+{
+    float v;
+    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ float2 ld_dsmem_f32x2(uint32_t addr)
+{
+    float2 v;
+    asm volatile("ld.shared::cluster.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "r"(addr) : "memory");
+    return v;
 }
 
 __device__ __forceinline__ void fence_proxy_async_smem()
@@ -266,6 +293,15 @@ __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint3
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
+// Transpose of an 8x8 b16 matrix held in the warp's fragment layout (lane t
+// holds row t/4, columns 2(t%4) and 2(t%4)+1).
+__device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x)
+{
+    uint32_t y;
+    asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
+    return y;
+}
+
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
 {
     __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
@@ -298,13 +334,11 @@ __device__ __forceinline__ uint32_t swz(int row, int u)
 
 // Writes w[s] for s < S and returns L (in every lane).  1 <= S <= kMaxSplits.
 // All loads are issued up front (clamped to valid splits, then masked).
-__device__ __forceinline__ float merge_stats_warp(const float2 *ml, int S, float *w, int lane)
+// The statistics of merge_stats_warp from values already in registers: lane
+// l holds splits l, l+32, ... in v[] ((-inf, 0) beyond S).
+template <int kPer>
+__device__ __forceinline__ float merge_stats_values(float2 (&v)[kPer], int S, float *w, int lane)
 {
-    constexpr int kPer = kMaxSplits / 32;
-    float2 v[kPer];
-#pragma unroll
-    for (int j = 0; j < kPer; ++j)
-        v[j] = __ldcg(&ml[min(lane + 32 * j, S - 1)]);
     float mx = -INFINITY;
 #pragma unroll
     for (int j = 0; j < kPer; ++j) {
@@ -329,6 +363,16 @@ __device__ __forceinline__ float merge_stats_warp(const float2 *ml, int S, float
     for (int k = 16; k; k >>= 1)
         L = __fadd_rn(L, __shfl_xor_sync(0xffffffffu, L, k));
     return L;
+}
+
+__device__ __forceinline__ float merge_stats_warp(const float2 *ml, int S, float *w, int lane)
+{
+    constexpr int kPer = kMaxSplits / 32;
+    float2 v[kPer];
+#pragma unroll
+    for (int j = 0; j < kPer; ++j)
+        v[j] = __ldcg(&ml[min(lane + 32 * j, S - 1)]);
+    return merge_stats_values(v, S, w, lane);
 }
 
 __device__ __forceinline__ void fma4(float4 &acc, float w, const float4 &v)
@@ -381,23 +425,35 @@ enum TraceEvent {
     kTrTicket = 6,       // merge ticket taken
     kTrStats = 7,        // last CTA: merge weights ready
     kTrMerged = 8,       // last CTA: output written
-    kTrFence = 9,        // last CTA: after the acquire fences
-    kTrIssued = 10,      // last CTA: first two merge batches issued
-    kTrBatch0 = 11,      // last CTA: first merge batch landed
+    kTrFence = 9,        // last CTA: after the acquire fence
+    kTrGroupO = 10,      // group results in shared memory
+    kTrGroupStats = 11,  // group weights ready
 };
 
-__device__ __forceinline__ void trace_event(const DecodeParams &p, int ev)
+// Slots of a CTA's trace record: 0-15 the SM cycle counter at each event;
+// 16 the global timer (ns) at kTrStart, 17 at the CTA's last event, 18 the
+// cycles one global-timer read took.
+__device__ __forceinline__ void trace_event(const DecodeParams &p, int ev, bool last = false)
 {
 #ifdef PGQA_TRACE
     if (p.trace) {
-        unsigned long long t;
-        asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
         const size_t cta = (static_cast<size_t>(blockIdx.z) * gridDim.y + blockIdx.y) * gridDim.x + blockIdx.x;
-        p.trace[cta * kTraceEvents + ev] = t;
+        unsigned long long *rec = p.trace + cta * kTraceEvents;
+        const long long c0 = clock64();
+        rec[ev] = static_cast<unsigned long long>(c0);
+        if (ev == kTrStart || last) {
+            unsigned long long t;
+            asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+            const long long c1 = clock64();
+            rec[ev == kTrStart ? 16 : 17] = t;
+            if (ev == kTrStart)
+                rec[18] = static_cast<unsigned long long>(c1 - c0);
+        }
     }
 #else
     (void)p;
     (void)ev;
+    (void)last;
 #endif
 }
 
@@ -431,7 +487,6 @@ __global__ void __launch_bounds__(Geo<HD>::kThreads, Cfg<HD>::kMinBlocks)
     const uint32_t s_base = smem_u32(smem);
     const uint32_t s_full = s_base + SM::kBarOff;
     const uint32_t s_empty = s_full + NS * 8;
-    const uint32_t s_mbar = s_empty + NS * 8;      // two merge barriers
     int *s_misc = reinterpret_cast<int *>(smem + SM::kMiscOff);
 
     const int tid = threadIdx.x;
@@ -444,6 +499,15 @@ __global__ void __launch_bounds__(Geo<HD>::kThreads, Cfg<HD>::kMinBlocks)
     const int head0 = kh * p.g + hs * kQRows;
     const int nh_sub = min(kQRows, p.g - hs * kQRows);
     const int S = p.splits;
+
+    // Barriers first: the init fence then has no earlier load to wait for.
+    if (tid == 0) {
+        for (int s = 0; s < NS; ++s) {
+            mbar_init(s_full + 8 * s, 1);
+            mbar_init(s_empty + 8 * s, WPG);
+        }
+        mbar_init_fence();
+    }
 
     // ---- rows served: this CTA's own, or a packing group led by its first row.
     // Lane i of every warp loads row g0 + i's metadata, so the check costs one
@@ -503,8 +567,13 @@ __global__ void __launch_bounds__(Geo<HD>::kThreads, Cfg<HD>::kMinBlocks)
     if (hi_u >= lo_u) {
         const int p0 = lo_u >> 4;
         const int np = (hi_u >> 4) - p0 + 1;
-        page_begin = p0 + static_cast<int>((static_cast<long long>(split) * np) / S);
-        npages_mine = p0 + static_cast<int>((static_cast<long long>(split + 1) * np) / S) - page_begin;
+        if (np <= (1 << 22)) {       // (S + 1) * np < 2^31: 32-bit arithmetic
+            page_begin = p0 + (split * np) / S;
+            npages_mine = p0 + ((split + 1) * np) / S - page_begin;
+        } else {
+            page_begin = p0 + static_cast<int>((static_cast<long long>(split) * np) / S);
+            npages_mine = p0 + static_cast<int>((static_cast<long long>(split + 1) * np) / S) - page_begin;
+        }
     }
 
     // ---- loads that need no barrier go out before the barrier set-up
@@ -516,7 +585,8 @@ __global__ void __launch_bounds__(Geo<HD>::kThreads, Cfg<HD>::kMinBlocks)
     const int wig = warp - grp * WPG;    // consumer: warp within the group
     const int dq0 = wig * GE::kDims; // consumer: first head dim of this warp
     uint32_t qa[KB][2];
-    int lo_g = 1, hi_g = 0;          // visible range of query row gid (empty if unused)
+    int lo_a = 1, hi_a = 0;          // visible ranges of query rows 2tig and 2tig+1 (empty if unused)
+    int lo_b = 1, hi_b = 0;
     if (warp == NW) {
         tbl = p.block_table + __ldg(p.off + r0) + page_begin;
         if (lane < npages_mine) {
@@ -539,19 +609,13 @@ __global__ void __launch_bounds__(Geo<HD>::kThreads, Cfg<HD>::kMinBlocks)
                 qa[kb][0] = __ldg(qg + kb * 8 + tig);          // dims 16kb + 2tig, +1
                 qa[kb][1] = __ldg(qg + kb * 8 + 4 + tig);      // dims 16kb + 8 + 2tig, +1
             }
-            row_window(p, r0 + gid / nh_sub, lo_g, hi_g);
         }
+        if (2 * tig < nq)
+            row_window(p, r0 + (2 * tig) / nh_sub, lo_a, hi_a);
+        if (2 * tig + 1 < nq)
+            row_window(p, r0 + (2 * tig + 1) / nh_sub, lo_b, hi_b);
     }
 
-    if (tid == 0) {
-        for (int s = 0; s < NS; ++s) {
-            mbar_init(s_full + 8 * s, 1);
-            mbar_init(s_empty + 8 * s, WPG);
-        }
-        mbar_init(s_mbar, 1);
-        mbar_init(s_mbar + 8, 1);
-        mbar_init_fence();
-    }
     __syncthreads();
     if (tid == 0)
         trace_event(p, kTrReady);
@@ -599,21 +663,32 @@ __global__ void __launch_bounds__(Geo<HD>::kThreads, Cfg<HD>::kMinBlocks)
             }
             ok = __shfl_sync(0xffffffffu, ok, 0);
         }
+        if (p.cluster > 1) {         // the cluster merge's two barriers count every thread
+            cluster_sync_all();
+            cluster_sync_all();
+        }
         return;
     }
 
     // ---------------------------------------------------- consumer warps
+    // Scores are computed transposed, S^T = K Q^T: the page's 16 tokens are the
+    // MMA rows and the 8 query rows its columns, so no MMA row is padding.
+    // Lane (gid, tig) holds S^T for tokens gid and gid+8 of query rows 2tig and
+    // 2tig+1 -- the same query rows as its O^T columns, so the softmax state
+    // of those two rows lives in the lane that rescales them.
     float acc[KB][4];              // O^T: dims dq0 + 16mt + {gid, gid+8}, query rows {2tig, 2tig+1}
 #pragma unroll
     for (int mt = 0; mt < KB; ++mt)
         acc[mt][0] = acc[mt][1] = acc[mt][2] = acc[mt][3] = 0.f;
-    float m_run = -INFINITY;       // running max of query row gid, log2 units (same in the group's warps)
-    float l_run = 0.f;             // this thread's share of the running sum
+    float m_a = -INFINITY, m_b = -INFINITY;   // running max of query rows 2tig, 2tig+1 (log2 units)
+    float l_a = 0.f, l_b = 0.f;               // this lane's share of their running sums
 
     // per-lane ldmatrix row/unit selectors
     const int lm_i = lane >> 3, lm_r = lane & 7;
-    const int tok_sel = (lm_i >> 1) * 8 + lm_r;    // K/V token row addressed by this lane
-    const int half_sel = lm_i & 1;                 // low / high 8 columns
+    const int k_tok = (lm_i & 1) * 8 + lm_r;       // K as A operand: matrices (tok lo/hi) x (dims lo/hi)
+    const int k_half = lm_i >> 1;
+    const int v_tok = (lm_i >> 1) * 8 + lm_r;      // V^T as A operand via .trans: (tok lo/hi) x (dims lo/hi)
+    const int v_half = lm_i & 1;
     float4 *sx = reinterpret_cast<float4 *>(smem + SM::kXOff) + grp * (2 * WPG * 32);
 
     bool ok = true;
@@ -628,25 +703,22 @@ __global__ void __launch_bounds__(Geo<HD>::kThreads, Cfg<HD>::kMinBlocks)
         const uint32_t sv = sk + SM::kTile;
         const int pos0 = (page_begin + i) * kPage;
 
-        // (partial) S = Q K^T over this warp's dims: two n-tiles of 8 tokens,
-        // even and odd 16-dim blocks in separate accumulators
-        float sa[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-        float sb[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+        // (partial) S^T over this warp's dims, even and odd 16-dim blocks in
+        // separate accumulators
+        float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
         if (ok) {
 #pragma unroll
             for (int kb = 0; kb < KB; ++kb) {
                 const int k16 = dq0 / 16 + kb;
-                uint32_t b0n0, b1n0, b0n1, b1n1;
-                ldsm_x4(sk + (k16 >> 2) * kBoxBytes + swz(tok_sel, (k16 & 3) * 2 + half_sel), b0n0, b1n0, b0n1,
-                        b1n1);
-                mma_bf16_16816(sa[kb & 1], qa[kb][0], 0u, qa[kb][1], 0u, b0n0, b1n0);
-                mma_bf16_16816(sb[kb & 1], qa[kb][0], 0u, qa[kb][1], 0u, b0n1, b1n1);
+                uint32_t a0, a1, a2, a3;
+                ldsm_x4(sk + (k16 >> 2) * kBoxBytes + swz(k_tok, (k16 & 3) * 2 + k_half), a0, a1, a2, a3);
+                mma_bf16_16816(sc[kb & 1], a0, a1, a2, a3, qa[kb][0], qa[kb][1]);
             }
         }
-        float4 sfull = make_float4(sa[0][0] + sa[1][0], sa[0][1] + sa[1][1], sb[0][0] + sb[1][0],
-                                   sb[0][1] + sb[1][1]);
+        float4 sfull = make_float4(sc[0][0] + sc[1][0], sc[0][1] + sc[1][1], sc[0][2] + sc[1][2],
+                                   sc[0][3] + sc[1][3]);
         if (WPG > 1) {
-            // full S = sum of the group's partials, in warp order
+            // full S^T = sum of the group's partials, in warp order
             float4 *xb = sx + (jj & 1) * (WPG * 32);
             xb[wig * 32 + lane] = sfull;
             group_bar_sync(1 + grp, WPG * 32);
@@ -661,35 +733,43 @@ __global__ void __launch_bounds__(Geo<HD>::kThreads, Cfg<HD>::kMinBlocks)
             }
         }
 
-        // mask to the query row's [lo, hi], scale to log2 units
-        const int t0 = pos0 + 2 * tig;
+        // mask to each query row's [lo, hi], scale to log2 units:
+        // x0/x1 token gid, x2/x3 token gid+8; x0/x2 query row 2tig, x1/x3 row 2tig+1
+        const int ta = pos0 + gid, tb = ta + 8;
         float x[4];
-        x[0] = (t0 >= lo_g && t0 <= hi_g) ? sfull.x * kLog2e : -INFINITY;
-        x[1] = (t0 + 1 >= lo_g && t0 + 1 <= hi_g) ? sfull.y * kLog2e : -INFINITY;
-        x[2] = (t0 + 8 >= lo_g && t0 + 8 <= hi_g) ? sfull.z * kLog2e : -INFINITY;
-        x[3] = (t0 + 9 >= lo_g && t0 + 9 <= hi_g) ? sfull.w * kLog2e : -INFINITY;
+        x[0] = (ta >= lo_a && ta <= hi_a) ? sfull.x * kLog2e : -INFINITY;
+        x[1] = (ta >= lo_b && ta <= hi_b) ? sfull.y * kLog2e : -INFINITY;
+        x[2] = (tb >= lo_a && tb <= hi_a) ? sfull.z * kLog2e : -INFINITY;
+        x[3] = (tb >= lo_b && tb <= hi_b) ? sfull.w * kLog2e : -INFINITY;
 
-        // online softmax for query row gid (the 4 lanes of a group hold its 16 scores)
-        float mx = fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3]));
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-        const float m_new = fmaxf(m_run, mx);
-        float alpha = 1.f;
-        float pr[4] = {0.f, 0.f, 0.f, 0.f};
-        if (m_new != -INFINITY) {
-            alpha = exp2f(m_run - m_new);
+        // online softmax: the 8 lanes of a tig column hold a query row's 16 scores
+        float mxa = fmaxf(x[0], x[2]), mxb = fmaxf(x[1], x[3]);
 #pragma unroll
-            for (int e = 0; e < 4; ++e)
-                pr[e] = bf16_round(exp2f(x[e] - m_new));
+        for (int k = 4; k < 32; k <<= 1) {
+            mxa = fmaxf(mxa, __shfl_xor_sync(0xffffffffu, mxa, k));
+            mxb = fmaxf(mxb, __shfl_xor_sync(0xffffffffu, mxb, k));
         }
-        m_run = m_new;
-        l_run = __fmaf_rn(l_run, alpha, (pr[0] + pr[1]) + (pr[2] + pr[3]));
-        const uint32_t pb0 = pack_bf16x2(pr[0], pr[1]);   // P^T rows 2tig, 2tig+1 -> B frag
-        const uint32_t pb1 = pack_bf16x2(pr[2], pr[3]);   // P^T rows 8+2tig, 9+2tig
+        const float mna = fmaxf(m_a, mxa), mnb = fmaxf(m_b, mxb);
+        float al_a = 1.f, al_b = 1.f;
+        float pr[4] = {0.f, 0.f, 0.f, 0.f};
+        if (mna != -INFINITY) {
+            al_a = exp2f(m_a - mna);
+            pr[0] = bf16_round(exp2f(x[0] - mna));
+            pr[2] = bf16_round(exp2f(x[2] - mna));
+        }
+        if (mnb != -INFINITY) {
+            al_b = exp2f(m_b - mnb);
+            pr[1] = bf16_round(exp2f(x[1] - mnb));
+            pr[3] = bf16_round(exp2f(x[3] - mnb));
+        }
+        m_a = mna;
+        m_b = mnb;
+        l_a = __fmaf_rn(l_a, al_a, pr[0] + pr[2]);
+        l_b = __fmaf_rn(l_b, al_b, pr[1] + pr[3]);
+        // P^T as the PV B fragment: transpose the (token x query) 8x8 tiles
+        const uint32_t pb0 = movmatrix_trans(pack_bf16x2(pr[0], pr[1]));   // tokens 0-7
+        const uint32_t pb1 = movmatrix_trans(pack_bf16x2(pr[2], pr[3]));   // tokens 8-15
 
-        // O^T columns are query rows 2tig and 2tig+1: fetch their alphas
-        const float al_a = __shfl_sync(0xffffffffu, alpha, (2 * tig) * 4);
-        const float al_b = __shfl_sync(0xffffffffu, alpha, (2 * tig + 1) * 4);
         if (__any_sync(0xffffffffu, al_a != 1.f || al_b != 1.f)) {
 #pragma unroll
             for (int mt = 0; mt < KB; ++mt) {
@@ -723,7 +803,7 @@ __global__ void __launch_bounds__(Geo<HD>::kThreads, Cfg<HD>::kMinBlocks)
             for (int mt = 0; mt < KB; ++mt) {
                 const int m16 = dq0 / 16 + mt;
                 uint32_t a0, a1, a2, a3;
-                ldsm_x4_trans(sv + (m16 >> 2) * kBoxBytes + swz(tok_sel, (m16 & 3) * 2 + half_sel), a0, a1, a2, a3);
+                ldsm_x4_trans(sv + (m16 >> 2) * kBoxBytes + swz(v_tok, (m16 & 3) * 2 + v_half), a0, a1, a2, a3);
                 mma_bf16_16816(acc[mt], a0, a1, a2, a3, pb0, pb1);
             }
         }
@@ -734,8 +814,11 @@ __global__ void __launch_bounds__(Geo<HD>::kThreads, Cfg<HD>::kMinBlocks)
         if (lane == 0)
             mbar_arrive(s_empty + 8 * st);
     }
-    l_run += __shfl_xor_sync(0xffffffffu, l_run, 1);
-    l_run += __shfl_xor_sync(0xffffffffu, l_run, 2);
+#pragma unroll
+    for (int k = 4; k < 32; k <<= 1) {
+        l_a += __shfl_xor_sync(0xffffffffu, l_a, k);
+        l_b += __shfl_xor_sync(0xffffffffu, l_b, k);
+    }
     named_bar_sync<kAllConsumersBarrier, NT>();      // every page consumed: the stage ring is free
     if (tid == 0)
         trace_event(p, kTrLoopDone);
@@ -754,10 +837,14 @@ __global__ void __launch_bounds__(Geo<HD>::kThreads, Cfg<HD>::kMinBlocks)
             ob[(2 * tig) * SM::kObufStride + d + 8] = acc[mt][2];
             ob[(2 * tig + 1) * SM::kObufStride + d + 8] = acc[mt][3];
         }
-        if (wig == 0 && tig == 0)
-            mlbuf[grp * kQRows + gid] = make_float2(m_run, l_run);
+        if (wig == 0 && gid == 0) {
+            mlbuf[grp * kQRows + 2 * tig] = make_float2(m_a, l_a);
+            mlbuf[grp * kQRows + 2 * tig + 1] = make_float2(m_b, l_b);
+        }
     }
     named_bar_sync<kAllConsumersBarrier, NT>();
+    if (tid == 0)
+        trace_event(p, kTrGroupO);
     if (tid < nq) {
         float mx = -INFINITY;
         for (int g = 0; g < NG; ++g)
@@ -770,74 +857,157 @@ __global__ void __launch_bounds__(Geo<HD>::kThreads, Cfg<HD>::kMinBlocks)
             L = __fmaf_rn(ws, v.y, L);
         }
         stat[tid * (NG + 2) + NG] = L;
-        if (S > 1) {
+        stat[tid * (NG + 2) + NG + 1] = mx;
+        if (S > 1 && p.cluster <= 1) {
             const size_t rh = static_cast<size_t>(r0 + tid / nh_sub) * p.nh + head0 + tid % nh_sub;
             p.part_ml[rh * S + split] = make_float2(mx, L);
         }
     }
     named_bar_sync<kAllConsumersBarrier, NT>();
-    for (int idx = tid; idx < nq * HD; idx += NT) {
-        const int q = idx / HD, d = idx - q * HD;
-        const float *st = stat + q * (NG + 2);
-        float o = 0.f;
+    if (tid == 0)
+        trace_event(p, kTrGroupStats);
+
+    if (p.cluster > 1) {
+        // ------------------------------------------------ on-chip merge of the cluster
+        // The S = cluster splits of this tile are the CTAs of one cluster.
+        // Each leaves its (M, L) and O in its own shared memory; CTA r then
+        // merges dims [r*hd/S, (r+1)*hd/S) of every query row from all of
+        // them over distributed shared memory, with the same operations in
+        // the same order as the combine kernel.
+        float *cpart = reinterpret_cast<float *>(smem + SM::kCpartOff);
+        float2 *cml = reinterpret_cast<float2 *>(smem + SM::kCmlOff);
+        float *cw = reinterpret_cast<float *>(smem + SM::kCwOff);
 #pragma unroll
-        for (int g = 0; g < NG; ++g)
-            o = __fmaf_rn(st[g], obuf[(g * kQRows + q) * SM::kObufStride + d], o);
-        const size_t rh = static_cast<size_t>(r0 + q / nh_sub) * p.nh + head0 + q % nh_sub;
-        if (S == 1)
-            p.o[rh * HD + d] = merge_finish(o, st[NG]);
-        else
-            p.part_o[(rh * S + split) * HD + d] = o;
+        for (int q = 0; q < kQRows; ++q) {
+            if (q < nq) {
+                const float *st = stat + q * (NG + 2);
+#pragma unroll
+                for (int d = tid; d < HD; d += NT) {
+                    float o = 0.f;
+#pragma unroll
+                    for (int g = 0; g < NG; ++g)
+                        o = __fmaf_rn(st[g], obuf[(g * kQRows + q) * SM::kObufStride + d], o);
+                    cpart[q * HD + d] = o;
+                }
+            }
+        }
+        if (tid < nq)
+            cml[tid] = make_float2(stat[tid * (NG + 2) + NG + 1], stat[tid * (NG + 2) + NG]);
+        cluster_sync_all();          // every CTA's partial is in its shared memory
+        if (tid == 0)
+            trace_event(p, kTrTicket);
+        const int C = p.cluster;
+        for (int q = warp; q < nq; q += NW) {
+            float2 v[1];
+            v[0] = lane < C ? ld_dsmem_f32x2(map_to_cta(smem_u32(&cml[q]), lane)) : make_float2(-INFINITY, 0.f);
+            const float L = merge_stats_values(v, C, cw + q * (kMaxCluster + 1), lane);
+            if (lane == 0)
+                cw[q * (kMaxCluster + 1) + kMaxCluster] = L;
+        }
+        named_bar_sync<kAllConsumersBarrier, NT>();
+        const int slice = HD / C;
+        const int d0 = split * slice;
+        for (int e = tid; e < nq * slice; e += NT) {
+            const int q = e / slice, d = d0 + (e - q * slice);
+            const uint32_t la = smem_u32(&cpart[q * HD + d]);
+            float vj[kMaxCluster];
+#pragma unroll
+            for (int j = 0; j < kMaxCluster; ++j)
+                vj[j] = j < C ? ld_dsmem_f32(map_to_cta(la, j)) : 0.f;
+            const float *w = cw + q * (kMaxCluster + 1);
+            float acc = 0.f;
+#pragma unroll
+            for (int j = 0; j < kMaxCluster; ++j)
+                if (j < C)
+                    acc = __fmaf_rn(w[j], vj[j], acc);
+            const size_t rh = static_cast<size_t>(r0 + q / nh_sub) * p.nh + head0 + q % nh_sub;
+            p.o[rh * HD + d] = merge_finish(acc, w[kMaxCluster]);
+        }
+        if (tid == 0)
+            trace_event(p, kTrMerged, true);
+        cluster_sync_all();          // peers may still be reading this CTA's shared memory
+        return;
+    }
+#pragma unroll
+    for (int q = 0; q < kQRows; ++q) {
+        if (q < nq) {
+            const float *st = stat + q * (NG + 2);
+            const size_t rh = static_cast<size_t>(r0 + q / nh_sub) * p.nh + head0 + q % nh_sub;
+#pragma unroll
+            for (int d = tid; d < HD; d += NT) {
+                float o = 0.f;
+#pragma unroll
+                for (int g = 0; g < NG; ++g)
+                    o = __fmaf_rn(st[g], obuf[(g * kQRows + q) * SM::kObufStride + d], o);
+                if (S == 1)
+                    p.o[rh * HD + d] = merge_finish(o, st[NG]);
+                else
+                    p.part_o[(rh * S + split) * HD + d] = o;
+            }
+        }
     }
     if (tid == 0)
-        trace_event(p, kTrPartial);
+        trace_event(p, kTrPartial, S == 1 || p.counters == nullptr);
     if (S == 1 || p.counters == nullptr)
         return;
 
     // ---------------------------------------------------- last-CTA merge
-    // This thread's generic writes to the ring precede the merge's bulk copies
-    // into it (no copy is in flight here, so the fence does not wait on one).
-    fence_proxy_async_smem();
-    __threadfence();
+    // The barrier orders every thread's partial stores before thread 0's
+    // acquire-release ticket; the last CTA's threads see all partials after
+    // the second barrier.
     named_bar_sync<kAllConsumersBarrier, NT>();
     const int tile_id = (r0 * p.nkv + kh) * p.hsg + hs;
     if (tid == 0)
-        s_misc[0] = static_cast<int>(atomicAdd(p.counters + tile_id, 1u));
+        s_misc[0] = static_cast<int>(atomic_add_acq_rel(p.counters + tile_id, 1u));
     named_bar_sync<kAllConsumersBarrier, NT>();
     if (tid == 0)
-        trace_event(p, kTrTicket);
+        trace_event(p, kTrTicket, s_misc[0] != S - 1);
     if (s_misc[0] != S - 1)
         return;
-    __threadfence();
-    fence_proxy_async_global();      // the other CTAs' partials, now visible, feed bulk copies
-    if (tid == 0)
-        trace_event(p, kTrFence);
 
-    // Partial rows (query row q, split s) stream through two shared buffers by
-    // bulk copy; batch b holds splits [b*SB, b*SB + SB) of every query row.
-    // The buffers follow the weights, which the group-merge scratch no longer
-    // needs.
-    float *wts = reinterpret_cast<float *>(smem);  // [8][kMaxSplits + 1]; entry kMaxSplits = L
-    const int SB = SM::kBufRows / nq;
-    const int nb = (S + SB - 1) / SB;
-    auto issue = [&](int b) {
-        const int s0 = b * SB, sn = min(SB, S - s0);
-        const uint32_t buf = s_base + ((b & 1) ? SM::kBufOff1 : SM::kBufOff0);
-        const uint32_t bar = s_mbar + 8 * (b & 1);
-        mbar_arrive_expect_tx(bar, static_cast<uint32_t>(nq * sn * SM::kRowBytes));
-        for (int q = 0; q < nq; ++q) {
-            const size_t rh = static_cast<size_t>(r0 + q / nh_sub) * p.nh + head0 + q % nh_sub;
-            for (int j = 0; j < sn; ++j)
-                bulk_load(buf + (q * SB + j) * SM::kRowBytes, p.part_o + (rh * S + s0 + j) * HD, SM::kRowBytes,
-                          bar);
-        }
-    };
-    if (tid == 0) {
-        issue(0);
-        if (nb > 1)
-            issue(1);
-        trace_event(p, kTrIssued);
+    // Each thread owns kOwn float4 outputs (query row q, dims 4*d4..+3) and
+    // streams the splits' partial rows through registers: kUnroll splits per
+    // chunk, the next chunk's loads in flight while the current one is
+    // accumulated, fused multiply-adds in split order.  The first chunk's
+    // loads go out before the weights are computed.
+    constexpr int kVec = HD / 4;                               // float4 per query row
+    constexpr int kOwn = kQRows * kVec / NT;                   // float4 outputs per thread
+    constexpr int kUnroll = 8 / kOwn > 0 ? 8 / kOwn : 1;
+    float4 oacc[kOwn];
+    const float4 *src[kOwn];
+    int qown[kOwn];
+#pragma unroll
+    for (int k = 0; k < kOwn; ++k) {
+        const int e = tid + k * NT;
+        const int q = e / kVec, d4 = e - q * kVec;
+        qown[k] = q;
+        oacc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+        const int qc = min(q, nq - 1);
+        const size_t rh = static_cast<size_t>(r0 + qc / nh_sub) * p.nh + head0 + qc % nh_sub;
+        src[k] = reinterpret_cast<const float4 *>(p.part_o + rh * S * HD) + d4;
     }
+    float4 va[kUnroll][kOwn], vb[kUnroll][kOwn];
+    auto load_chunk = [&](float4 (&v)[kUnroll][kOwn], int s0) {
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u)
+#pragma unroll
+            for (int k = 0; k < kOwn; ++k)
+                v[u][k] = (s0 + u < S && qown[k] < nq) ? __ldcg(src[k] + static_cast<size_t>(s0 + u) * kVec)
+                                                       : make_float4(0.f, 0.f, 0.f, 0.f);
+    };
+    auto add_chunk = [&](const float4 (&v)[kUnroll][kOwn], int s0, const float *w) {
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u)
+            if (s0 + u < S) {
+#pragma unroll
+                for (int k = 0; k < kOwn; ++k)
+                    if (qown[k] < nq)
+                        fma4(oacc[k], w[qown[k] * (kMaxSplits + 1) + s0 + u], v[u][k]);
+            }
+    };
+    load_chunk(va, 0);
+
+    float *wts = reinterpret_cast<float *>(smem);  // [8][kMaxSplits + 1]; entry kMaxSplits = L
     for (int q = warp; q < nq; q += NW) {
         const size_t rh = static_cast<size_t>(r0 + q / nh_sub) * p.nh + head0 + q % nh_sub;
         const float L = merge_stats_warp(p.part_ml + rh * S, S, wts + q * (kMaxSplits + 1), lane);
@@ -848,33 +1018,14 @@ __global__ void __launch_bounds__(Geo<HD>::kThreads, Cfg<HD>::kMinBlocks)
     if (tid == 0)
         trace_event(p, kTrStats);
 
-    constexpr int kVec = HD / 4;                               // float4 per query row
-    constexpr int kOwn = kQRows * kVec / NT;                   // float4 outputs per thread
-    float4 oacc[kOwn];
-#pragma unroll
-    for (int k = 0; k < kOwn; ++k)
-        oacc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
-    bool mok = true;
-    for (int b = 0; b < nb; ++b) {
-        if (mok)
-            mok = mbar_wait_bounded(s_mbar + 8 * (b & 1), (b >> 1) & 1, p.err, kErrTimeoutFull);
-        if (b == 0 && tid == 0)
-            trace_event(p, kTrBatch0);
-        const float *buf = reinterpret_cast<const float *>(smem + ((b & 1) ? SM::kBufOff1 : SM::kBufOff0));
-        const int s0 = b * SB, sn = min(SB, S - s0);
-        for (int j = 0; j < sn; ++j) {
-#pragma unroll
-            for (int k = 0; k < kOwn; ++k) {
-                const int e = tid + k * NT;
-                const int q = e / kVec, d4 = e - q * kVec;
-                if (q < nq)
-                    fma4(oacc[k], wts[q * (kMaxSplits + 1) + s0 + j],
-                         *reinterpret_cast<const float4 *>(buf + (q * SB + j) * HD + d4 * 4));
-            }
-        }
-        named_bar_sync<kAllConsumersBarrier, NT>();      // every thread is done with this buffer
-        if (tid == 0 && b + 2 < nb && mok)
-            issue(b + 2);
+    for (int s0 = 0; s0 < S; s0 += 2 * kUnroll) {
+        if (s0 + kUnroll < S)
+            load_chunk(vb, s0 + kUnroll);
+        add_chunk(va, s0, wts);
+        if (s0 + 2 * kUnroll < S)
+            load_chunk(va, s0 + 2 * kUnroll);
+        if (s0 + kUnroll < S)
+            add_chunk(vb, s0 + kUnroll, wts);
     }
 #pragma unroll
     for (int k = 0; k < kOwn; ++k) {
@@ -887,7 +1038,7 @@ __global__ void __launch_bounds__(Geo<HD>::kThreads, Cfg<HD>::kMinBlocks)
     }
     if (tid == 0) {
         p.counters[tile_id] = 0u;      // ready for the next call, which is ordered after this kernel
-        trace_event(p, kTrMerged);
+        trace_event(p, kTrMerged, true);
     }
 }
 

@@ -3,4 +3,5 @@
 
 namespace pgqa {
 cudaError_t launch_decode_hd512(const LaunchArgs &a, bool set_attr) { return launch_decode<512>(a, set_attr); }
+int cluster_capacity_hd512(int cluster) { return cluster_capacity<512>(cluster); }
 }  // namespace pgqa

@@ -3,4 +3,5 @@
 
 namespace pgqa {
 cudaError_t launch_decode_hd64(const LaunchArgs &a, bool set_attr) { return launch_decode<64>(a, set_attr); }
+int cluster_capacity_hd64(int cluster) { return cluster_capacity<64>(cluster); }
 }  // namespace pgqa

@@ -75,10 +75,15 @@ def test_choose_splits_rule(lib):
                 assert s == 1 or rows * nkv * (s - 1) < 4 * 152   # no more splits than needed
     # the named workloads (152 SMs): one wave for few tiles, ~4 CTAs per SM for many
     assert pgqa.choose_splits(256, 1, 2, 1, num_sms=152) == 8           # capped at 2 pages per split
-    assert pgqa.choose_splits(1024, 4, 8, 1, num_sms=152) == 19         # 4 rows of one sequence packed
-    assert pgqa.choose_splits(1024, 4, 8, 4, num_sms=152) == 5          # 4 independent rows
+    assert pgqa.choose_splits(1024, 4, 8, 1, num_sms=152) == 8          # 4 rows of one sequence packed; 19 -> 8
+    assert pgqa.choose_splits(1024, 4, 8, 4, num_sms=152) == 4          # 4 independent rows; 5 -> 4
     assert pgqa.choose_splits(32768, 1, 4, 1, num_sms=152) == 38
     assert pgqa.choose_splits(4096, 64, 8, 64, num_sms=152) == 2
+    # up to 24 the count is a power of two of at most 8 (on-chip merge), above it is not rounded
+    for kv in (256, 1024, 4096, 1 << 16):
+        for tiles in range(1, 160):
+            s = pgqa.choose_splits(kv, tiles, 1, tiles, num_sms=152)
+            assert s > 24 or (s in (1, 2, 4, 8))
     # nseq outside [1, rows] means every row is its own sequence
     assert pgqa.choose_splits(1024, 4, 8, 0, num_sms=152) == pgqa.choose_splits(1024, 4, 8, 4, num_sms=152)
     # without a device the current-device form falls back to 152 SMs
