@@ -109,44 +109,65 @@ int get_encoder()
     return PGQA_OK;
 }
 
-// 3-D view of a [pages][nkv][16][hd] bf16 pool: x = dim (hd), y = slot (16),
-// z = (page, kv head) tile index phys * nkv + kh.  The box is 64 dims x 16
-// slots of one tile (2 KiB, 128-byte swizzle).  The pool's page count is not
-// known here, so z spans the int32 coordinate range; only tiles the block
-// table names are ever addressed.
+// TMA descriptors of a [pages][nkv][16][hd] bf16 pool.  The pool's page
+// count is not known here, so the tile dimension spans the int32 coordinate
+// range; only tiles the block table names are ever addressed.  Preferred is
+// a 4-D view (64 dims, 16 slots, hd/64 dim chunks, tile = phys*nkv + kh)
+// whose single box is a whole (page, kv head) tile -- one TMA per tile, laid
+// out in shared memory as [chunk][slot][64] under the 128-byte swizzle.  If
+// the driver refuses that stride order, a 3-D view (dims, slots, tiles) with
+// 64-dim boxes gives the same shared-memory layout in hd/64 copies.
 struct MapCacheEntry {
     const void *base = nullptr;
     int hd = 0;
+    int whole = 0;
     CUtensorMap map;
 };
 MapCacheEntry g_map_cache[128];
 unsigned g_map_next = 0;
 
-int pool_map(const void *base, int hd, CUtensorMap *out)
+int pool_map(const void *base, int hd, CUtensorMap *out, int *whole)
 {
     for (auto &e : g_map_cache)
         if (e.base == base && e.hd == hd) {
             *out = e.map;
+            *whole = e.whole;
             return PGQA_OK;
         }
     int st = get_encoder();
     if (st != PGQA_OK)
         return st;
     CUtensorMap m;
-    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(hd), 16u, 0x7fffffffull};
-    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(hd) * 2u, static_cast<cuuint64_t>(hd) * 32u};
-    const cuuint32_t box[3] = {64u, 16u, 1u};
-    const cuuint32_t estride[3] = {1u, 1u, 1u};
-    CUresult r = g_encode(&m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box,
-                          estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    if (r != CUDA_SUCCESS)
-        return PGQA_ERR_TENSOR_MAP;
+    int w = 1;
+    {
+        const cuuint64_t dims[4] = {64u, 16u, static_cast<cuuint64_t>(hd / 64), 0x7fffffffull};
+        const cuuint64_t strides[3] = {static_cast<cuuint64_t>(hd) * 2u, 128u, static_cast<cuuint64_t>(hd) * 32u};
+        const cuuint32_t box[4] = {64u, 16u, static_cast<cuuint32_t>(hd / 64), 1u};
+        const cuuint32_t estride[4] = {1u, 1u, 1u, 1u};
+        CUresult r = g_encode(&m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(base), dims, strides, box,
+                              estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        if (r != CUDA_SUCCESS)
+            w = 0;
+    }
+    if (!w) {
+        const cuuint64_t dims[3] = {static_cast<cuuint64_t>(hd), 16u, 0x7fffffffull};
+        const cuuint64_t strides[2] = {static_cast<cuuint64_t>(hd) * 2u, static_cast<cuuint64_t>(hd) * 32u};
+        const cuuint32_t box[3] = {64u, 16u, 1u};
+        const cuuint32_t estride[3] = {1u, 1u, 1u};
+        CUresult r = g_encode(&m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box,
+                              estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        if (r != CUDA_SUCCESS)
+            return PGQA_ERR_TENSOR_MAP;
+    }
     MapCacheEntry &e = g_map_cache[g_map_next++ % 128];
     e.base = base;
     e.hd = hd;
+    e.whole = w;
     e.map = m;
     *out = m;
+    *whole = w;
     return PGQA_OK;
 }
 
@@ -332,6 +353,7 @@ int pgqa_attn_decode(void *o, void *part, const void *q, const void *k_pool, con
     p.pack = g <= pgqa::kQRows ? pgqa::kQRows / g : 1;
     p.trace = nullptr;
     p.cluster = 0;
+    p.whole_tile_box = 0;
     a.stream = static_cast<cudaStream_t>(stream);
 
     // The lock covers set-up and the (asynchronous) launch itself, so the
@@ -342,8 +364,12 @@ int pgqa_attn_decode(void *o, void *part, const void *q, const void *k_pool, con
     if (st != PGQA_OK)
         return st;
     CUtensorMap tk, tv;
-    if ((st = pool_map(k_pool, hd, &tk)) != PGQA_OK || (st = pool_map(v_pool, hd, &tv)) != PGQA_OK)
+    int whole_k = 0, whole_v = 0;
+    if ((st = pool_map(k_pool, hd, &tk, &whole_k)) != PGQA_OK || (st = pool_map(v_pool, hd, &tv, &whole_v)) != PGQA_OK)
         return st;
+    if (whole_k != whole_v)
+        return PGQA_ERR_TENSOR_MAP;
+    p.whole_tile_box = whole_k;
     p.err = s->err;
     p.cluster = counters ? on_chip_cluster(s, hi, hd, splits) : 0;
     if (g_trace && static_cast<size_t>(splits) * nkv * hsg * rows * pgqa::kTraceEvents * 8 <= g_trace_bytes)

@@ -132,6 +132,7 @@ struct DecodeParams {
     int hsg;                 // head subgroups of up to 8 heads per kv head
     int pack;                // rows per packing group (1 = no packing)
     int cluster;             // > 1: the splits of a tile are one cluster of this size, merged on chip
+    int whole_tile_box;      // 1: one 4-D TMA box per (page, kv head) tile; 0: hd/64 3-D boxes
     unsigned long long *trace;   // per-CTA timestamps (trace builds only), or null
 };
 
@@ -205,6 +206,16 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map
         : "memory");
 }
 
+__device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap *map, uint32_t bar, int x, int y,
+                                            int z, int w)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4, %5, %6}], [%2];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y), "r"(z), "r"(w)
+        : "memory");
+}
+
 __device__ __forceinline__ void tma_prefetch_map(const CUtensorMap *map)
 {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
@@ -247,6 +258,19 @@ __device__ __forceinline__ float2 ld_dsmem_f32x2(uint32_t addr)
     float2 v;
     asm volatile("ld.shared::cluster.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "r"(addr) : "memory");
     return v;
+}
+
+// Programmatic dependent launch: wait until the grids this one depends on
+// have completed with their memory visible; then allow the next grid in the
+// stream to start launching (it runs the same wait before touching memory).
+__device__ __forceinline__ void grid_dependency_wait()
+{
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+__device__ __forceinline__ void grid_launch_dependents()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
 __device__ __forceinline__ void fence_proxy_async_smem()
@@ -432,7 +456,7 @@ enum TraceEvent {
 
 // Slots of a CTA's trace record: 0-15 the SM cycle counter at each event;
 // 16 the global timer (ns) at kTrStart, 17 at the CTA's last event, 18 the
-// cycles one global-timer read took.
+// cycles one global-timer read took, 19 whether whole-tile TMA boxes were used.
 __device__ __forceinline__ void trace_event(const DecodeParams &p, int ev, bool last = false)
 {
 #ifdef PGQA_TRACE
@@ -446,8 +470,10 @@ __device__ __forceinline__ void trace_event(const DecodeParams &p, int ev, bool 
             asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
             const long long c1 = clock64();
             rec[ev == kTrStart ? 16 : 17] = t;
-            if (ev == kTrStart)
+            if (ev == kTrStart) {
                 rec[18] = static_cast<unsigned long long>(c1 - c0);
+                rec[19] = static_cast<unsigned long long>(p.whole_tile_box);
+            }
         }
     }
 #else
@@ -508,51 +534,55 @@ __global__ void __launch_bounds__(Geo<HD>::kThreads, Cfg<HD>::kMinBlocks)
         }
         mbar_init_fence();
     }
+    // Nothing above touched global memory: wait here for the previous kernel
+    // in the stream (inputs may be its outputs), then let the next one launch.
+    grid_dependency_wait();
+    grid_launch_dependents();
 
     // ---- rows served: this CTA's own, or a packing group led by its first row.
-    // Lane i of every warp loads row g0 + i's metadata, so the check costs one
-    // round of (parallel) loads; the shuffles leave every thread with the same
-    // verdict, so the CTA decides uniformly.
+    // One round of metadata loads: lane i of every warp loads row g0 + i of
+    // the packing group (just row rz without packing).  Everything else --
+    // the packing verdict, the union range, off of the first served row and
+    // each query row's window -- comes from shuffles, identical in every warp,
+    // so the CTA decides uniformly.
+    const int g0 = p.pack > 1 ? rz - rz % p.pack : rz;
+    const int gn = p.pack > 1 ? min(p.pack, p.rows - g0) : 1;
+    int off_i = 0, lo_i = 1, hi_i = 0;
+    if (lane < gn) {
+        off_i = __ldg(p.off + g0 + lane);
+        row_window(p, g0 + lane, lo_i, hi_i);
+    }
     int r0 = rz, nr = 1;
-    if (p.pack > 1) {
-        const int g0 = rz - rz % p.pack;
-        const int gn = min(p.pack, p.rows - g0);
-        if (gn > 1) {
-            const int li = lane < gn ? lane : 0;
-            const int off_i = __ldg(p.off + g0 + li);
-            int lo_i, hi_i;
-            row_window(p, g0 + li, lo_i, hi_i);
-            const bool live = lane < gn && hi_i >= lo_i;
-            const int off0 = __shfl_sync(0xffffffffu, off_i, 0);
-            const bool same = __all_sync(0xffffffffu, lane >= gn || off_i == off0);
-            int max_lo = live ? lo_i : INT_MIN, min_hi = live ? hi_i : INT_MAX;
+    if (gn > 1) {
+        const bool live = lane < gn && hi_i >= lo_i;
+        const int off0 = __shfl_sync(0xffffffffu, off_i, 0);
+        const bool same = __all_sync(0xffffffffu, lane >= gn || off_i == off0);
+        int max_lo = live ? lo_i : INT_MIN, min_hi = live ? hi_i : INT_MAX;
 #pragma unroll
-            for (int k = 16; k; k >>= 1) {
-                max_lo = max(max_lo, __shfl_xor_sync(0xffffffffu, max_lo, k));
-                min_hi = min(min_hi, __shfl_xor_sync(0xffffffffu, min_hi, k));
-            }
-            const bool overlap = max_lo == INT_MIN ||
-                                 static_cast<long long>(max_lo) <= static_cast<long long>(min_hi) + 1;
-            if (same && overlap) {
-                if (rz != g0)
-                    return;               // served by the group's first CTA
-                r0 = g0;
-                nr = gn;
-            }
+        for (int k = 16; k; k >>= 1) {
+            max_lo = max(max_lo, __shfl_xor_sync(0xffffffffu, max_lo, k));
+            min_hi = min(min_hi, __shfl_xor_sync(0xffffffffu, min_hi, k));
+        }
+        const bool overlap = max_lo == INT_MIN ||
+                             static_cast<long long>(max_lo) <= static_cast<long long>(min_hi) + 1;
+        if (same && overlap) {
+            if (rz != g0)
+                return;               // served by the group's first CTA
+            r0 = g0;
+            nr = gn;
         }
     }
     const int nq = nr * nh_sub;        // query rows in use (<= 8)
+    const int lb = r0 - g0;            // metadata lane of the first served row
+    const int off_r0 = __shfl_sync(0xffffffffu, off_i, lb);
     if (tid == 0)
         trace_event(p, kTrStart);
 
     // ---- union of the served rows' visible ranges; this split's page share
     int lo_u = 0, hi_u = -1;
     {
-        int lo_i = 1, hi_i = 0;
-        if (lane < nr)
-            row_window(p, r0 + lane, lo_i, hi_i);
-        const bool live = lane < nr && hi_i >= lo_i;
-        int lo_m = live ? lo_i : INT_MAX, hi_m = live ? hi_i : INT_MIN;
+        const bool served = lane >= lb && lane < lb + nr && hi_i >= lo_i;
+        int lo_m = served ? lo_i : INT_MAX, hi_m = served ? hi_i : INT_MIN;
 #pragma unroll
         for (int k = 16; k; k >>= 1) {
             lo_m = min(lo_m, __shfl_xor_sync(0xffffffffu, lo_m, k));
@@ -587,8 +617,22 @@ __global__ void __launch_bounds__(Geo<HD>::kThreads, Cfg<HD>::kMinBlocks)
     uint32_t qa[KB][2];
     int lo_a = 1, hi_a = 0;          // visible ranges of query rows 2tig and 2tig+1 (empty if unused)
     int lo_b = 1, hi_b = 0;
+    // windows of query rows 2tig and 2tig+1 (each thread's O^T columns)
+    {
+        const int la = lb + (2 * tig) / nh_sub, lbb = lb + (2 * tig + 1) / nh_sub;
+        const int wla = __shfl_sync(0xffffffffu, lo_i, la & 31), wha = __shfl_sync(0xffffffffu, hi_i, la & 31);
+        const int wlb = __shfl_sync(0xffffffffu, lo_i, lbb & 31), whb = __shfl_sync(0xffffffffu, hi_i, lbb & 31);
+        if (2 * tig < nq) {
+            lo_a = wla;
+            hi_a = wha;
+        }
+        if (2 * tig + 1 < nq) {
+            lo_b = wlb;
+            hi_b = whb;
+        }
+    }
     if (warp == NW) {
-        tbl = p.block_table + __ldg(p.off + r0) + page_begin;
+        tbl = p.block_table + off_r0 + page_begin;
         if (lane < npages_mine) {
             phys_first = __ldg(tbl + lane);
             if (p.page_map)
@@ -610,10 +654,6 @@ __global__ void __launch_bounds__(Geo<HD>::kThreads, Cfg<HD>::kMinBlocks)
                 qa[kb][1] = __ldg(qg + kb * 8 + 4 + tig);      // dims 16kb + 8 + 2tig, +1
             }
         }
-        if (2 * tig < nq)
-            row_window(p, r0 + (2 * tig) / nh_sub, lo_a, hi_a);
-        if (2 * tig + 1 < nq)
-            row_window(p, r0 + (2 * tig + 1) / nh_sub, lo_b, hi_b);
     }
 
     __syncthreads();
@@ -651,10 +691,15 @@ __global__ void __launch_bounds__(Geo<HD>::kThreads, Cfg<HD>::kMinBlocks)
                         const uint32_t dv = dk + SM::kTile;
                         const int tile = ph * p.nkv + kh;
                         mbar_arrive_expect_tx(bar, SM::kStage);
+                        if (p.whole_tile_box) {
+                            tma_load_4d(dk, &tm_k, bar, 0, 0, 0, tile);
+                            tma_load_4d(dv, &tm_v, bar, 0, 0, 0, tile);
+                        } else {
 #pragma unroll
-                        for (int c = 0; c < kChunks; ++c) {
-                            tma_load_3d(dk + c * kBoxBytes, &tm_k, bar, c * kBoxElems, 0, tile);
-                            tma_load_3d(dv + c * kBoxBytes, &tm_v, bar, c * kBoxElems, 0, tile);
+                            for (int c = 0; c < kChunks; ++c) {
+                                tma_load_3d(dk + c * kBoxBytes, &tm_k, bar, c * kBoxElems, 0, tile);
+                                tma_load_3d(dv + c * kBoxBytes, &tm_v, bar, c * kBoxElems, 0, tile);
+                            }
                         }
                         if (i == 0)
                             trace_event(p, kTrFirstTma);
@@ -1060,6 +1105,8 @@ __global__ void __launch_bounds__(combine_threads<HD>()) decode_combine_kernel(c
     __shared__ float wts[kMaxSplits + 1];
     const size_t rh = blockIdx.x;
     const int S = p.splits;
+    grid_dependency_wait();          // the split kernel's partials
+    grid_launch_dependents();
     if (threadIdx.x < 32) {
         const float L = merge_stats_warp(p.part_ml + rh * S, S, wts, threadIdx.x);
         if (threadIdx.x == 0)

@@ -28,30 +28,40 @@ cudaError_t launch_decode(const LaunchArgs &a, bool set_attr)
     }
     const DecodeParams &p = a.p;
     dim3 grid(p.splits, p.nkv * p.hsg, p.rows);
-    cudaError_t e;
+    // Every launch may overlap the tail of the previous kernel in the stream
+    // (programmatic dependent launch); the kernels wait for it before any
+    // memory access.
+    cudaLaunchAttribute attr[2];
+    int na = 0;
+    attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[na].val.programmaticStreamSerializationAllowed = 1;
+    ++na;
     if (p.cluster > 1) {
-        cudaLaunchConfig_t cfg = {};
-        cfg.gridDim = grid;
-        cfg.blockDim = dim3(Geo<HD>::kThreads);
-        cfg.dynamicSmemBytes = Smem<HD>::kAlloc;
-        cfg.stream = a.stream;
-        cudaLaunchAttribute attr[1];
-        attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = p.cluster;
-        attr[0].val.clusterDim.y = 1;
-        attr[0].val.clusterDim.z = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
-        e = cudaLaunchKernelEx(&cfg, decode_split_kernel<HD>, *a.tm_k, *a.tm_v, p);
-    } else {
-        decode_split_kernel<HD><<<grid, Geo<HD>::kThreads, Smem<HD>::kAlloc, a.stream>>>(*a.tm_k, *a.tm_v, p);
-        e = cudaGetLastError();
+        attr[na].id = cudaLaunchAttributeClusterDimension;
+        attr[na].val.clusterDim.x = p.cluster;
+        attr[na].val.clusterDim.y = 1;
+        attr[na].val.clusterDim.z = 1;
+        ++na;
     }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(Geo<HD>::kThreads);
+    cfg.dynamicSmemBytes = Smem<HD>::kAlloc;
+    cfg.stream = a.stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = na;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, decode_split_kernel<HD>, *a.tm_k, *a.tm_v, p);
     if (e != cudaSuccess)
         return e;
     if (p.splits > 1 && p.counters == nullptr) {
-        decode_combine_kernel<HD><<<p.rows * p.nh, combine_threads<HD>(), 0, a.stream>>>(p);
-        e = cudaGetLastError();
+        cudaLaunchConfig_t c2 = {};
+        c2.gridDim = dim3(p.rows * p.nh);
+        c2.blockDim = dim3(combine_threads<HD>());
+        c2.dynamicSmemBytes = 0;
+        c2.stream = a.stream;
+        c2.attrs = attr;
+        c2.numAttrs = 1;
+        e = cudaLaunchKernelEx(&c2, decode_combine_kernel<HD>, p);
     }
     return e;
 }
