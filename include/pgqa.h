@@ -112,11 +112,13 @@ int pgqa_choose_splits_for(int kv_len_eff, int rows, int nkv, int nseq, int num_
 
 /*
  * Bytes of the `part` scratch (`attn::decode_part_bytes` of the test file):
- * rows * nh * splits * (hd + 2) * 4 (f32 O, running max and sum per split).
+ * rows * nh * splits * (hd + 2) * 4 (f32 O, running max and sum per split);
+ * above 8 splits, plus rows * nh * ceil(splits / 8) * (hd + 2) * 4 + 16 for the
+ * merged groups of 8 splits (the merge then runs in two levels).
  */
 size_t pgqa_decode_part_bytes(int rows, int nh, int splits, int hd);
 
-/* uint32 merge-counter slots one call needs: rows * nkv * ceil((nh / nkv) / 8). */
+/* uint32 merge-counter slots one call needs: rows * nkv * ceil((nh / nkv) / 8) * 33. */
 size_t pgqa_decode_counter_count(int rows, int nh, int nkv);
 
 /*

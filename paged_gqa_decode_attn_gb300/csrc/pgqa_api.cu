@@ -224,7 +224,11 @@ size_t pgqa_decode_part_bytes(int rows, int nh, int splits, int hd)
 {
     if (rows <= 0 || nh <= 0 || splits <= 0 || hd <= 0)
         return 0;
-    return static_cast<size_t>(rows) * nh * splits * (static_cast<size_t>(hd) + 2) * 4;
+    size_t partials = static_cast<size_t>(splits);
+    if (splits > pgqa::kGroupSplits)        // plus the merged split groups, 16-byte aligned
+        partials += (splits + pgqa::kGroupSplits - 1) / pgqa::kGroupSplits;
+    return static_cast<size_t>(rows) * nh * partials * (static_cast<size_t>(hd) + 2) * 4 +
+           (splits > pgqa::kGroupSplits ? 16 : 0);
 }
 
 size_t pgqa_decode_counter_count(int rows, int nh, int nkv)
@@ -232,7 +236,7 @@ size_t pgqa_decode_counter_count(int rows, int nh, int nkv)
     if (rows <= 0 || nh <= 0 || nkv <= 0 || nh % nkv != 0)
         return 0;
     const int g = nh / nkv;
-    return static_cast<size_t>(rows) * nkv * ((g + pgqa::kQRows - 1) / pgqa::kQRows);
+    return static_cast<size_t>(rows) * nkv * ((g + pgqa::kQRows - 1) / pgqa::kQRows) * pgqa::kCountersPerTile;
 }
 
 int pgqa_choose_splits_for(int kv_len_eff, int rows, int nkv, int nseq, int num_sms)
@@ -336,6 +340,15 @@ int pgqa_attn_decode(void *o, void *part, const void *q, const void *k_pool, con
     p.part_ml = splits > 1 ? reinterpret_cast<float2 *>(static_cast<char *>(part) +
                                                         static_cast<size_t>(rows) * nh * splits * hd * 4)
                            : nullptr;
+    p.gpart_o = nullptr;
+    p.gpart_ml = nullptr;
+    if (splits > pgqa::kGroupSplits) {
+        const size_t ng = (splits + pgqa::kGroupSplits - 1) / pgqa::kGroupSplits;
+        size_t at = static_cast<size_t>(rows) * nh * splits * (static_cast<size_t>(hd) + 2) * 4;
+        at = (at + 15) / 16 * 16;
+        p.gpart_o = reinterpret_cast<float *>(static_cast<char *>(part) + at);
+        p.gpart_ml = reinterpret_cast<float2 *>(static_cast<char *>(part) + at + static_cast<size_t>(rows) * nh * ng * hd * 4);
+    }
     p.q = static_cast<const __nv_bfloat16 *>(q);
     p.block_table = block_table;
     p.off = off;

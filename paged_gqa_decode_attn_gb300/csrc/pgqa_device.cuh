@@ -44,6 +44,9 @@ constexpr int kBoxElems = 64;             // 128-byte swizzle atom: 64 bf16 per 
 constexpr int kBoxBytes = kPage * kBoxElems * 2;   // one TMA box: 16 rows x 128 B
 constexpr int kMaxSplits = 256;
 constexpr int kMaxCluster = 8;            // largest thread-block cluster for the on-chip merge
+constexpr int kGroupSplits = 8;           // more splits than this merge in two levels of up to 8
+constexpr int kMaxGroups = (kMaxSplits + kGroupSplits - 1) / kGroupSplits;
+constexpr int kCountersPerTile = 1 + kMaxGroups;   // [0] the final merge, [1 + g] split group g
 constexpr long long kWaitLimitCycles = 2000000000ll;   // bounded waits: ~1 s at 2 GHz
 constexpr unsigned int kErrTimeoutFull = 1u;
 constexpr unsigned int kErrTimeoutEmpty = 2u;
@@ -105,7 +108,7 @@ struct Smem {
     static_assert(kStatOff + kQRows * (G::kGroups + 2) * 4 <= kStagesBytes, "group merge scratch");
     // last-CTA merge of the split partials: merge weights [8][kMaxSplits + 1],
     // also in the stage ring
-    static constexpr int kWtsBytes = kQRows * (kMaxSplits + 1) * 4;
+    static constexpr int kWtsBytes = kQRows * (kMaxSplits + 2) * 4;
     static_assert(kWtsBytes <= kStagesBytes, "merge weights");
     // cluster merge, after the group-merge scratch: this CTA's O [8][hd] and
     // (M, L) [8] for its peers to read, then the merge weights [8][kMaxCluster + 1]
@@ -120,6 +123,8 @@ struct DecodeParams {
     __nv_bfloat16 *o;        // [rows][nh][hd]
     float *part_o;           // [rows*nh][splits][hd]
     float2 *part_ml;         // [rows*nh][splits]: (max in log2 units, sum)
+    float *gpart_o;          // splits > 8: [rows*nh][groups][hd] merged split groups
+    float2 *gpart_ml;        // splits > 8: [rows*nh][groups]
     const __nv_bfloat16 *q;  // [rows][nh][hd]
     const int32_t *block_table;
     const int32_t *off;
@@ -273,6 +278,18 @@ __device__ __forceinline__ void grid_launch_dependents()
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
+// 16-byte asynchronous global -> shared copy through L2 (generic proxy).
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src)
+{
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(reinterpret_cast<uint64_t>(src))
+                 : "memory");
+}
+
+__device__ __forceinline__ void cp_async_wait_all()
+{
+    asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
+}
+
 __device__ __forceinline__ void fence_proxy_async_smem()
 {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -349,6 +366,9 @@ __device__ __forceinline__ uint32_t swz(int row, int u)
 // The S split partials (m_s, l_s, O_s) of one (row, head) merge as
 //   M = max_s m_s,  w_s = (m_s == -inf) ? 0 : 2^(m_s - M),  L = sum_s w_s l_s,
 //   o[d] = bf16_rn( (sum_s w_s O_s[d]) / L ), or 0 when L == 0.
+// With more than kGroupSplits splits the merge runs in two levels: splits
+// [8g, 8g+8) merge into an unnormalised group partial (M_g, L_g, O_g), and
+// the group partials merge into o -- the same formula at both levels.
 // The last-CTA merge and the combine kernel run exactly these operations in
 // exactly this order, so they agree bit for bit:
 //  * merge_stats_warp (one warp): lane l takes splits l, l+32, ... in order,
@@ -361,7 +381,8 @@ __device__ __forceinline__ uint32_t swz(int row, int u)
 // The statistics of merge_stats_warp from values already in registers: lane
 // l holds splits l, l+32, ... in v[] ((-inf, 0) beyond S).
 template <int kPer>
-__device__ __forceinline__ float merge_stats_values(float2 (&v)[kPer], int S, float *w, int lane)
+__device__ __forceinline__ float merge_stats_values(float2 (&v)[kPer], int S, float *w, int lane,
+                                                    float *m_out = nullptr)
 {
     float mx = -INFINITY;
 #pragma unroll
@@ -373,6 +394,8 @@ __device__ __forceinline__ float merge_stats_values(float2 (&v)[kPer], int S, fl
 #pragma unroll
     for (int k = 16; k; k >>= 1)
         mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, k));
+    if (m_out)
+        *m_out = mx;
     float L = 0.f;
 #pragma unroll
     for (int j = 0; j < kPer; ++j) {
@@ -389,14 +412,15 @@ __device__ __forceinline__ float merge_stats_values(float2 (&v)[kPer], int S, fl
     return L;
 }
 
-__device__ __forceinline__ float merge_stats_warp(const float2 *ml, int S, float *w, int lane)
+__device__ __forceinline__ float merge_stats_warp(const float2 *ml, int S, float *w, int lane,
+                                                  float *m_out = nullptr)
 {
     constexpr int kPer = kMaxSplits / 32;
     float2 v[kPer];
 #pragma unroll
     for (int j = 0; j < kPer; ++j)
         v[j] = __ldcg(&ml[min(lane + 32 * j, S - 1)]);
-    return merge_stats_values(v, S, w, lane);
+    return merge_stats_values(v, S, w, lane, m_out);
 }
 
 __device__ __forceinline__ void fma4(float4 &acc, float w, const float4 &v)
@@ -997,92 +1021,133 @@ __global__ void __launch_bounds__(Geo<HD>::kThreads, Cfg<HD>::kMinBlocks)
         return;
 
     // ---------------------------------------------------- last-CTA merge
-    // The barrier orders every thread's partial stores before thread 0's
-    // acquire-release ticket; the last CTA's threads see all partials after
-    // the second barrier.
-    named_bar_sync<kAllConsumersBarrier, NT>();
-    const int tile_id = (r0 * p.nkv + kh) * p.hsg + hs;
-    if (tid == 0)
-        s_misc[0] = static_cast<int>(atomic_add_acq_rel(p.counters + tile_id, 1u));
-    named_bar_sync<kAllConsumersBarrier, NT>();
-    if (tid == 0)
-        trace_event(p, kTrTicket, s_misc[0] != S - 1);
-    if (s_misc[0] != S - 1)
-        return;
-
-    // Each thread owns kOwn float4 outputs (query row q, dims 4*d4..+3) and
-    // streams the splits' partial rows through registers: kUnroll splits per
-    // chunk, the next chunk's loads in flight while the current one is
-    // accumulated, fused multiply-adds in split order.  The first chunk's
-    // loads go out before the weights are computed.
+    // A merge pass over `count` partial rows of every served query row:
+    // source row j of (row, head) rh is src_o[(rh * src_rows + first + j) *
+    // hd], with (m, l) at src_ml[rh * src_rows + first + j].  The result goes
+    // to o (final) or, unnormalised with its (M, L), to dst row dst_idx.
+    // The partial rows come into the (now free) stage ring by cp.async, as
+    // many rows at once as fit, while the weights are computed; each thread
+    // then accumulates its kOwn float4 outputs (query row q, dims 4*d4..+3)
+    // in row order.
     constexpr int kVec = HD / 4;                               // float4 per query row
     constexpr int kOwn = kQRows * kVec / NT;                   // float4 outputs per thread
-    constexpr int kUnroll = 8 / kOwn > 0 ? 8 / kOwn : 1;
-    float4 oacc[kOwn];
-    const float4 *src[kOwn];
-    int qown[kOwn];
-#pragma unroll
-    for (int k = 0; k < kOwn; ++k) {
-        const int e = tid + k * NT;
-        const int q = e / kVec, d4 = e - q * kVec;
-        qown[k] = q;
-        oacc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
-        const int qc = min(q, nq - 1);
-        const size_t rh = static_cast<size_t>(r0 + qc / nh_sub) * p.nh + head0 + qc % nh_sub;
-        src[k] = reinterpret_cast<const float4 *>(p.part_o + rh * S * HD) + d4;
-    }
-    float4 va[kUnroll][kOwn], vb[kUnroll][kOwn];
-    auto load_chunk = [&](float4 (&v)[kUnroll][kOwn], int s0) {
-#pragma unroll
-        for (int u = 0; u < kUnroll; ++u)
-#pragma unroll
-            for (int k = 0; k < kOwn; ++k)
-                v[u][k] = (s0 + u < S && qown[k] < nq) ? __ldcg(src[k] + static_cast<size_t>(s0 + u) * kVec)
-                                                       : make_float4(0.f, 0.f, 0.f, 0.f);
+    constexpr int kWStride = kMaxSplits + 2;                   // weights, L, M of one query row
+    constexpr int kStageOff = (SM::kWtsBytes + 15) / 16 * 16;
+    constexpr int kStageRows = (SM::kStagesBytes - kStageOff) / (kQRows * HD * 4);   // rows of all 8 query rows
+    static_assert(kStageRows >= 1, "merge staging");
+    float *wts = reinterpret_cast<float *>(smem);
+    float *stg = reinterpret_cast<float *>(smem + kStageOff);
+    auto rowhead = [&](int q) {
+        return static_cast<size_t>(r0 + q / nh_sub) * p.nh + head0 + q % nh_sub;
     };
-    auto add_chunk = [&](const float4 (&v)[kUnroll][kOwn], int s0, const float *w) {
+    auto merge_pass = [&](const float *src_o, const float2 *src_ml, int src_rows, int first, int count, bool final,
+                          float *dst_o, float2 *dst_ml, int dst_rows, int dst_idx) {
+        float4 oacc[kOwn];
 #pragma unroll
-        for (int u = 0; u < kUnroll; ++u)
-            if (s0 + u < S) {
-#pragma unroll
-                for (int k = 0; k < kOwn; ++k)
-                    if (qown[k] < nq)
-                        fma4(oacc[k], w[qown[k] * (kMaxSplits + 1) + s0 + u], v[u][k]);
+        for (int k = 0; k < kOwn; ++k)
+            oacc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+        auto stage = [&](int j0, int nj) {   // rows [j0, j0 + nj) of every query row -> stg[(j - j0) * nq + q]
+            const int total = nj * nq * kVec;
+            for (int e = tid; e < total; e += NT) {
+                const int jq = e / kVec, d4 = e - jq * kVec;
+                const int j = jq / nq, q = jq - j * nq;
+                cp_async16(smem_u32(stg + static_cast<size_t>(jq) * HD + d4 * 4),
+                           src_o + (rowhead(q) * src_rows + first + j0 + j) * HD + d4 * 4);
             }
-    };
-    load_chunk(va, 0);
-
-    float *wts = reinterpret_cast<float *>(smem);  // [8][kMaxSplits + 1]; entry kMaxSplits = L
-    for (int q = warp; q < nq; q += NW) {
-        const size_t rh = static_cast<size_t>(r0 + q / nh_sub) * p.nh + head0 + q % nh_sub;
-        const float L = merge_stats_warp(p.part_ml + rh * S, S, wts + q * (kMaxSplits + 1), lane);
-        if (lane == 0)
-            wts[q * (kMaxSplits + 1) + kMaxSplits] = L;
-    }
-    named_bar_sync<kAllConsumersBarrier, NT>();      // merge weights visible to every thread
-    if (tid == 0)
-        trace_event(p, kTrStats);
-
-    for (int s0 = 0; s0 < S; s0 += 2 * kUnroll) {
-        if (s0 + kUnroll < S)
-            load_chunk(vb, s0 + kUnroll);
-        add_chunk(va, s0, wts);
-        if (s0 + 2 * kUnroll < S)
-            load_chunk(va, s0 + 2 * kUnroll);
-        if (s0 + kUnroll < S)
-            add_chunk(vb, s0 + kUnroll, wts);
-    }
-#pragma unroll
-    for (int k = 0; k < kOwn; ++k) {
-        const int e = tid + k * NT;
-        const int q = e / kVec, d4 = e - q * kVec;
-        if (q < nq) {
-            const size_t rh = static_cast<size_t>(r0 + q / nh_sub) * p.nh + head0 + q % nh_sub;
-            store_out4(p.o + rh * HD + d4 * 4, oacc[k], wts[q * (kMaxSplits + 1) + kMaxSplits]);
+        };
+        int nj = min(count, kStageRows);
+        stage(0, nj);
+        for (int q = warp; q < nq; q += NW) {
+            float m = 0.f;
+            const float L = merge_stats_warp(src_ml + rowhead(q) * src_rows + first, count, wts + q * kWStride, lane,
+                                             &m);
+            if (lane == 0) {
+                wts[q * kWStride + kMaxSplits] = L;
+                wts[q * kWStride + kMaxSplits + 1] = m;
+            }
         }
+        for (int j0 = 0; j0 < count; j0 += nj) {
+            nj = min(count - j0, kStageRows);
+            if (j0 > 0)
+                stage(j0, nj);
+            cp_async_wait_all();
+            named_bar_sync<kAllConsumersBarrier, NT>();  // staged rows and weights visible to every thread
+            for (int j = 0; j < nj; ++j) {
+#pragma unroll
+                for (int k = 0; k < kOwn; ++k) {
+                    const int e = tid + k * NT;
+                    const int q = e / kVec, d4 = e - q * kVec;
+                    if (q < nq)
+                        fma4(oacc[k], wts[q * kWStride + j0 + j],
+                             *reinterpret_cast<const float4 *>(stg + static_cast<size_t>(j * nq + q) * HD + d4 * 4));
+                }
+            }
+            named_bar_sync<kAllConsumersBarrier, NT>();  // staging area free again
+        }
+#pragma unroll
+        for (int k = 0; k < kOwn; ++k) {
+            const int e = tid + k * NT;
+            const int q = e / kVec, d4 = e - q * kVec;
+            if (q < nq) {
+                const size_t rh = rowhead(q);
+                if (final)
+                    store_out4(p.o + rh * HD + d4 * 4, oacc[k], wts[q * kWStride + kMaxSplits]);
+                else
+                    *reinterpret_cast<float4 *>(dst_o + (rh * dst_rows + dst_idx) * HD + d4 * 4) = oacc[k];
+            }
+        }
+        if (!final && tid < nq)
+            dst_ml[rowhead(tid) * dst_rows + dst_idx] =
+                make_float2(wts[tid * kWStride + kMaxSplits + 1], wts[tid * kWStride + kMaxSplits]);
+    };
+
+    // Tickets: the barrier orders every thread's stores before thread 0's
+    // acquire-release atomic; the winner's threads see all partials after the
+    // second barrier.
+    const int tile_id = (r0 * p.nkv + kh) * p.hsg + hs;
+    unsigned int *cnt = p.counters + static_cast<size_t>(tile_id) * kCountersPerTile;
+    auto take_ticket = [&](unsigned int *c) {
+        named_bar_sync<kAllConsumersBarrier, NT>();
+        if (tid == 0)
+            s_misc[0] = static_cast<int>(atomic_add_acq_rel(c, 1u));
+        named_bar_sync<kAllConsumersBarrier, NT>();
+        return s_misc[0];
+    };
+
+    if (S <= kGroupSplits) {
+        const int t = take_ticket(cnt);
+        if (tid == 0)
+            trace_event(p, kTrTicket, t != S - 1);
+        if (t != S - 1)
+            return;
+        merge_pass(p.part_o, p.part_ml, S, 0, S, true, nullptr, nullptr, 0, 0);
+        if (tid == 0) {
+            cnt[0] = 0u;                   // ready for the next call, which is ordered after this kernel
+            trace_event(p, kTrMerged, true);
+        }
+        return;
     }
+    // two levels: the last CTA of split group g merges it; the last of the
+    // group mergers merges the groups
+    const int ng = (S + kGroupSplits - 1) / kGroupSplits;
+    const int gsp = split / kGroupSplits;
+    const int gsize = min(kGroupSplits, S - gsp * kGroupSplits);
+    const int t1 = take_ticket(cnt + 1 + gsp);
+    if (tid == 0)
+        trace_event(p, kTrTicket, t1 != gsize - 1);
+    if (t1 != gsize - 1)
+        return;
+    merge_pass(p.part_o, p.part_ml, S, gsp * kGroupSplits, gsize, false, p.gpart_o, p.gpart_ml, ng, gsp);
     if (tid == 0) {
-        p.counters[tile_id] = 0u;      // ready for the next call, which is ordered after this kernel
+        cnt[1 + gsp] = 0u;
+        trace_event(p, kTrStats);
+    }
+    const int t2 = take_ticket(cnt);
+    if (t2 != ng - 1)
+        return;
+    merge_pass(p.gpart_o, p.gpart_ml, ng, 0, ng, true, nullptr, nullptr, 0, 0);
+    if (tid == 0) {
+        cnt[0] = 0u;
         trace_event(p, kTrMerged, true);
     }
 }
@@ -1102,24 +1167,56 @@ constexpr int combine_threads()
 template <int HD>
 __global__ void __launch_bounds__(combine_threads<HD>()) decode_combine_kernel(const DecodeParams p)
 {
-    __shared__ float wts[kMaxSplits + 1];
+    __shared__ float wts[kMaxSplits + 2];          // weights of the splits (one level) or of the groups
+    __shared__ float gw[kMaxGroups][kGroupSplits]; // two levels: weights inside each group
+    __shared__ float2 gml[kMaxGroups];             // two levels: (M_g, L_g)
     const size_t rh = blockIdx.x;
     const int S = p.splits;
     grid_dependency_wait();          // the split kernel's partials
     grid_launch_dependents();
+    const int d4 = threadIdx.x;
+    const float4 *po = reinterpret_cast<const float4 *>(p.part_o + rh * S * HD) + d4;
+    if (S <= kGroupSplits) {
+        if (threadIdx.x < 32)
+            wts[kMaxSplits] = merge_stats_warp(p.part_ml + rh * S, S, wts, threadIdx.x);
+        __syncthreads();
+        if (d4 < HD / 4) {
+            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 8
+            for (int s = 0; s < S; ++s)
+                fma4(acc, wts[s], __ldcg(po + static_cast<size_t>(s) * (HD / 4)));
+            store_out4(p.o + rh * HD + d4 * 4, acc, wts[kMaxSplits]);
+        }
+        return;
+    }
+    // two levels, as in the last-CTA path: groups of 8 splits, then the groups
+    const int ng = (S + kGroupSplits - 1) / kGroupSplits;
     if (threadIdx.x < 32) {
-        const float L = merge_stats_warp(p.part_ml + rh * S, S, wts, threadIdx.x);
-        if (threadIdx.x == 0)
-            wts[kMaxSplits] = L;
+        for (int g = 0; g < ng; ++g) {
+            const int n = min(kGroupSplits, S - g * kGroupSplits);
+            float m = 0.f;
+            const float L = merge_stats_warp(p.part_ml + rh * S + g * kGroupSplits, n, gw[g], threadIdx.x, &m);
+            if (threadIdx.x == 0)
+                gml[g] = make_float2(m, L);
+        }
+        __syncwarp();
+        constexpr int kPer = (kMaxGroups + 31) / 32;
+        float2 v[kPer];
+#pragma unroll
+        for (int j = 0; j < kPer; ++j)
+            v[j] = gml[min(static_cast<int>(threadIdx.x) + 32 * j, ng - 1)];
+        wts[kMaxSplits] = merge_stats_values(v, ng, wts, threadIdx.x);
     }
     __syncthreads();
-    const int d4 = threadIdx.x;
     if (d4 < HD / 4) {
-        const float4 *po = reinterpret_cast<const float4 *>(p.part_o + rh * S * HD) + d4;
         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 8
-        for (int s = 0; s < S; ++s)
-            fma4(acc, wts[s], __ldcg(po + static_cast<size_t>(s) * (HD / 4)));
+        for (int g = 0; g < ng; ++g) {
+            const int n = min(kGroupSplits, S - g * kGroupSplits);
+            float4 og = make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int j = 0; j < n; ++j)
+                fma4(og, gw[g][j], __ldcg(po + static_cast<size_t>(g * kGroupSplits + j) * (HD / 4)));
+            fma4(acc, wts[g], og);
+        }
         store_out4(p.o + rh * HD + d4 * 4, acc, wts[kMaxSplits]);
     }
 }
