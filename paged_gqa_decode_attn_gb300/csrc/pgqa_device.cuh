@@ -50,6 +50,7 @@ constexpr int kCountersPerTile = 1 + kMaxGroups;   // [0] the final merge, [1 + 
 constexpr long long kWaitLimitCycles = 2000000000ll;   // bounded waits: ~1 s at 2 GHz
 constexpr unsigned int kErrTimeoutFull = 1u;
 constexpr unsigned int kErrTimeoutEmpty = 2u;
+constexpr unsigned int kErrTimeoutCluster = 4u;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr int kTraceEvents = 32;          // per-CTA slots of a trace build: 16 events x (ns, SM cycles)
 constexpr int kAllConsumersBarrier = 15;  // named barrier of every consumer warp
@@ -95,10 +96,17 @@ struct Smem {
     static constexpr int kXOff = kStagesBytes;                     // S exchange: float4 [groups][2][wpg][32]
     static constexpr int kXBytes = G::kGroups * 2 * G::kWpg * 32 * 16;
     static constexpr int kBarOff = kXOff + kXBytes;
-    static constexpr int kBarBytes = 2 * G::kStages * 8;            // full, empty
+    static constexpr int kBarBytes = (2 * G::kStages + 1) * 8;      // full, empty; cluster receive
     static constexpr int kMiscOff = kBarOff + kBarBytes;
     static constexpr int kTotal = kMiscOff + 16;
     static constexpr int kAlloc = kTotal + 1024;                   // slack for 1024-B alignment
+    // cluster launches only: the slices of the peers' partials that this CTA
+    // merges, O [cluster][8][hd / cluster] f32 (32 hd bytes for any cluster
+    // size), then (M, L) [cluster][8]
+    static constexpr int kRecvOff = (kTotal + 15) / 16 * 16;
+    static constexpr int kRecvMlOff = kRecvOff + kQRows * HD * 4;
+    static constexpr int kRecvBytes = kQRows * HD * 4 + kMaxCluster * kQRows * 8;
+    static constexpr int kAllocCluster = kRecvOff + kRecvBytes + 1024;
     // merge of the page groups' results, in the stage ring once every page is
     // consumed: O [groups][8][hd + 4] f32, (m, l) [groups][8], weights [8][groups + 2]
     static constexpr int kObufStride = HD + 4;
@@ -110,13 +118,10 @@ struct Smem {
     // also in the stage ring
     static constexpr int kWtsBytes = kQRows * (kMaxSplits + 2) * 4;
     static_assert(kWtsBytes <= kStagesBytes, "merge weights");
-    // cluster merge, after the group-merge scratch: this CTA's O [8][hd] and
-    // (M, L) [8] for its peers to read, then the merge weights [8][kMaxCluster + 1]
-    static constexpr int kCpartOff = (kStatOff + kQRows * (G::kGroups + 2) * 4 + 15) / 16 * 16;
-    static constexpr int kCmlOff = kCpartOff + kQRows * HD * 4;
-    static constexpr int kCwOff = kCmlOff + kQRows * 8;
+    // cluster merge weights [8][kMaxCluster + 1], after the group-merge scratch
+    static constexpr int kCwOff = (kStatOff + kQRows * (G::kGroups + 2) * 4 + 15) / 16 * 16;
     static_assert(kCwOff + kQRows * (kMaxCluster + 1) * 4 <= kStagesBytes, "cluster merge scratch");
-    static_assert(kAlloc <= 227 * 1024, "shared memory");
+    static_assert(kAllocCluster <= 227 * 1024, "shared memory");
 };
 
 struct DecodeParams {
@@ -237,10 +242,18 @@ __device__ __forceinline__ unsigned int atomic_add_acq_rel(unsigned int *addr, u
     return old;
 }
 
-// Thread-block cluster helpers (distributed shared memory).
-__device__ __forceinline__ void cluster_sync_all()
+// Thread-block cluster helpers (distributed shared memory).  Every thread
+// of the cluster arrives once, right after the receive barrier is set up
+// (the mbarrier-init fence orders that set-up), and waits before its first
+// access to a peer.
+__device__ __forceinline__ void cluster_arrive_relaxed()
 {
-    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+    asm volatile("barrier.cluster.arrive.relaxed;" ::: "memory");
+}
+
+__device__ __forceinline__ void cluster_wait()
+{
+    asm volatile("barrier.cluster.wait.acquire;" ::: "memory");
 }
 
 // Address of this CTA's shared location `addr` in the shared memory of cluster CTA `rank`.
@@ -251,18 +264,21 @@ __device__ __forceinline__ uint32_t map_to_cta(uint32_t addr, int rank)
     return out;
 }
 
-__device__ __forceinline__ float ld_dsmem_f32(uint32_t addr)
+// Asynchronous store into a peer's shared memory; its bytes count down the
+// transaction count of the peer's mbarrier `bar` (both cluster addresses).
+__device__ __forceinline__ void st_async_f32x4(uint32_t addr, float4 v, uint32_t bar)
 {
-    float v;
-    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
-    return v;
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(
+                     addr),
+                 "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w), "r"(bar)
+                 : "memory");
 }
 
-__device__ __forceinline__ float2 ld_dsmem_f32x2(uint32_t addr)
+__device__ __forceinline__ void st_async_f32x2(uint32_t addr, float2 v, uint32_t bar)
 {
-    float2 v;
-    asm volatile("ld.shared::cluster.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "r"(addr) : "memory");
-    return v;
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v2.f32 [%0], {%1, %2}, [%3];" ::"r"(addr),
+                 "f"(v.x), "f"(v.y), "r"(bar)
+                 : "memory");
 }
 
 // Programmatic dependent launch: wait until the grids this one depends on
@@ -550,14 +566,23 @@ __global__ void __launch_bounds__(Geo<HD>::kThreads, Cfg<HD>::kMinBlocks)
     const int nh_sub = min(kQRows, p.g - hs * kQRows);
     const int S = p.splits;
 
+    const uint32_t s_recv = s_full + 2 * NS * 8;    // cluster launches: peers' slices arrived
     // Barriers first: the init fence then has no earlier load to wait for.
     if (tid == 0) {
         for (int s = 0; s < NS; ++s) {
             mbar_init(s_full + 8 * s, 1);
             mbar_init(s_empty + 8 * s, WPG);
         }
+        if (p.cluster > 1) {
+            // completes once every peer (this CTA included) has pushed its
+            // O slice and (M, L) of all 8 query rows
+            mbar_init(s_recv, 1);
+            mbar_arrive_expect_tx(s_recv, kQRows * HD * 4 + p.cluster * kQRows * 8);
+        }
         mbar_init_fence();
     }
+    if (p.cluster > 1)
+        cluster_arrive_relaxed();
     // Nothing above touched global memory: wait here for the previous kernel
     // in the stream (inputs may be its outputs), then let the next one launch.
     grid_dependency_wait();
@@ -590,8 +615,11 @@ __global__ void __launch_bounds__(Geo<HD>::kThreads, Cfg<HD>::kMinBlocks)
         const bool overlap = max_lo == INT_MIN ||
                              static_cast<long long>(max_lo) <= static_cast<long long>(min_hi) + 1;
         if (same && overlap) {
-            if (rz != g0)
-                return;               // served by the group's first CTA
+            if (rz != g0) {           // served by the group's first CTA
+                if (p.cluster > 1)
+                    cluster_wait();
+                return;
+            }
             r0 = g0;
             nr = gn;
         }
@@ -732,10 +760,9 @@ __global__ void __launch_bounds__(Geo<HD>::kThreads, Cfg<HD>::kMinBlocks)
             }
             ok = __shfl_sync(0xffffffffu, ok, 0);
         }
-        if (p.cluster > 1) {         // the cluster merge's two barriers count every thread
-            cluster_sync_all();
-            cluster_sync_all();
-        }
+        __syncwarp();
+        if (p.cluster > 1)           // each thread that arrived also waits
+            cluster_wait();
         return;
     }
 
@@ -939,62 +966,70 @@ __global__ void __launch_bounds__(Geo<HD>::kThreads, Cfg<HD>::kMinBlocks)
     if (p.cluster > 1) {
         // ------------------------------------------------ on-chip merge of the cluster
         // The S = cluster splits of this tile are the CTAs of one cluster.
-        // Each leaves its (M, L) and O in its own shared memory; CTA r then
-        // merges dims [r*hd/S, (r+1)*hd/S) of every query row from all of
-        // them over distributed shared memory, with the same operations in
-        // the same order as the combine kernel.
-        float *cpart = reinterpret_cast<float *>(smem + SM::kCpartOff);
-        float2 *cml = reinterpret_cast<float2 *>(smem + SM::kCmlOff);
-        float *cw = reinterpret_cast<float *>(smem + SM::kCwOff);
+        // CTA r merges dims [r*hd/S, (r+1)*hd/S) of every query row: each CTA
+        // pushes that slice of its partial O, and its (M, L), into CTA r's
+        // receive buffer with asynchronous stores that complete on CTA r's
+        // receive barrier.  The merge then runs on local shared memory, with
+        // the same operations in the same order as the combine kernel, and
+        // no CTA reads a peer, so none waits for its peers before exiting.
+        const int C = p.cluster;
+        const int slice = HD / C;
+        float *recv_o = reinterpret_cast<float *>(smem + SM::kRecvOff);
+        float2 *recv_ml = reinterpret_cast<float2 *>(smem + SM::kRecvMlOff);
+        cluster_wait();              // every peer's receive barrier is set up
+        constexpr int kVec = HD / 4;
 #pragma unroll
-        for (int q = 0; q < kQRows; ++q) {
+        for (int k = 0; k < kQRows * kVec / NT; ++k) {
+            const int e = tid + k * NT;
+            const int q = e / kVec, d = (e - q * kVec) * 4;
+            float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
             if (q < nq) {
                 const float *st = stat + q * (NG + 2);
+                const float *ob = obuf + q * SM::kObufStride + d;
 #pragma unroll
-                for (int d = tid; d < HD; d += NT) {
-                    float o = 0.f;
-#pragma unroll
-                    for (int g = 0; g < NG; ++g)
-                        o = __fmaf_rn(st[g], obuf[(g * kQRows + q) * SM::kObufStride + d], o);
-                    cpart[q * HD + d] = o;
+                for (int g = 0; g < NG; ++g) {
+                    const float4 v = *reinterpret_cast<const float4 *>(ob + g * kQRows * SM::kObufStride);
+                    o.x = __fmaf_rn(st[g], v.x, o.x);
+                    o.y = __fmaf_rn(st[g], v.y, o.y);
+                    o.z = __fmaf_rn(st[g], v.z, o.z);
+                    o.w = __fmaf_rn(st[g], v.w, o.w);
                 }
             }
+            const int j = d / slice;
+            st_async_f32x4(map_to_cta(smem_u32(recv_o + (split * kQRows + q) * slice + (d - j * slice)), j), o,
+                           map_to_cta(s_recv, j));
         }
-        if (tid < nq)
-            cml[tid] = make_float2(stat[tid * (NG + 2) + NG + 1], stat[tid * (NG + 2) + NG]);
-        cluster_sync_all();          // every CTA's partial is in its shared memory
+        if (tid < C * kQRows) {
+            const int j = tid / kQRows, q = tid - j * kQRows;
+            const float2 ml = q < nq ? make_float2(stat[q * (NG + 2) + NG + 1], stat[q * (NG + 2) + NG])
+                                     : make_float2(-INFINITY, 0.f);
+            st_async_f32x2(map_to_cta(smem_u32(recv_ml + split * kQRows + q), j), ml, map_to_cta(s_recv, j));
+        }
+        if (!mbar_wait_bounded(s_recv, 0, p.err, kErrTimeoutCluster))
+            return;
         if (tid == 0)
             trace_event(p, kTrTicket);
-        const int C = p.cluster;
+        float *cw = reinterpret_cast<float *>(smem + SM::kCwOff);
         for (int q = warp; q < nq; q += NW) {
             float2 v[1];
-            v[0] = lane < C ? ld_dsmem_f32x2(map_to_cta(smem_u32(&cml[q]), lane)) : make_float2(-INFINITY, 0.f);
+            v[0] = lane < C ? recv_ml[lane * kQRows + q] : make_float2(-INFINITY, 0.f);
             const float L = merge_stats_values(v, C, cw + q * (kMaxCluster + 1), lane);
             if (lane == 0)
                 cw[q * (kMaxCluster + 1) + kMaxCluster] = L;
         }
         named_bar_sync<kAllConsumersBarrier, NT>();
-        const int slice = HD / C;
         const int d0 = split * slice;
         for (int e = tid; e < nq * slice; e += NT) {
-            const int q = e / slice, d = d0 + (e - q * slice);
-            const uint32_t la = smem_u32(&cpart[q * HD + d]);
-            float vj[kMaxCluster];
-#pragma unroll
-            for (int j = 0; j < kMaxCluster; ++j)
-                vj[j] = j < C ? ld_dsmem_f32(map_to_cta(la, j)) : 0.f;
+            const int q = e / slice, dd = e - q * slice;
             const float *w = cw + q * (kMaxCluster + 1);
             float acc = 0.f;
-#pragma unroll
-            for (int j = 0; j < kMaxCluster; ++j)
-                if (j < C)
-                    acc = __fmaf_rn(w[j], vj[j], acc);
+            for (int j = 0; j < C; ++j)
+                acc = __fmaf_rn(w[j], recv_o[(j * kQRows + q) * slice + dd], acc);
             const size_t rh = static_cast<size_t>(r0 + q / nh_sub) * p.nh + head0 + q % nh_sub;
-            p.o[rh * HD + d] = merge_finish(acc, w[kMaxCluster]);
+            p.o[rh * HD + d0 + dd] = merge_finish(acc, w[kMaxCluster]);
         }
         if (tid == 0)
             trace_event(p, kTrMerged, true);
-        cluster_sync_all();          // peers may still be reading this CTA's shared memory
         return;
     }
 #pragma unroll

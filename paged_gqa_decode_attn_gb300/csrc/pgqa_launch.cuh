@@ -22,7 +22,8 @@ cudaError_t launch_decode(const LaunchArgs &a, bool set_attr)
 {
     if (set_attr) {
         cudaError_t e = cudaFuncSetAttribute(decode_split_kernel<HD>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, Smem<HD>::kAlloc);
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             Smem<HD>::kAllocCluster);
         if (e != cudaSuccess)
             return e;
     }
@@ -46,7 +47,7 @@ cudaError_t launch_decode(const LaunchArgs &a, bool set_attr)
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
     cfg.blockDim = dim3(Geo<HD>::kThreads);
-    cfg.dynamicSmemBytes = Smem<HD>::kAlloc;
+    cfg.dynamicSmemBytes = p.cluster > 1 ? Smem<HD>::kAllocCluster : Smem<HD>::kAlloc;
     cfg.stream = a.stream;
     cfg.attrs = attr;
     cfg.numAttrs = na;
@@ -72,14 +73,14 @@ template <int HD>
 int cluster_capacity(int cluster)
 {
     if (cudaFuncSetAttribute(decode_split_kernel<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             Smem<HD>::kAlloc) != cudaSuccess)
+                             Smem<HD>::kAllocCluster) != cudaSuccess)
         return 0;
     if (cluster > kMaxCluster)
         return 0;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(cluster, 1, 1);
     cfg.blockDim = dim3(Geo<HD>::kThreads);
-    cfg.dynamicSmemBytes = Smem<HD>::kAlloc;
+    cfg.dynamicSmemBytes = Smem<HD>::kAllocCluster;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = cluster;

@@ -125,6 +125,14 @@ def test_head_dims_and_group_sizes(hd, nh, nkv):
     full_gates(c, splits=3, mapped=False)
 
 
+@pytest.mark.parametrize("hd", [64, 128, 256, 512])
+@pytest.mark.parametrize("splits", [2, 4, 8])
+def test_on_chip_cluster_merge_every_head_dim(hd, splits):
+    """2, 4 and 8 splits merge inside a thread-block cluster when counters are given."""
+    c = wl.page_case(16, 2, hd, 0, 40 * 16 + 5, 2, dist="sym", seed=hd * splits)
+    full_gates(c, splits=splits, mapped=False)
+
+
 @pytest.mark.parametrize("window,ctx,rows", [(1, 50, 3), (5000, 700, 2), (17, 33, 4), (0, 1, 1), (16, 16, 1)])
 def test_window_and_tiny_context_edges(window, ctx, rows):
     c = wl.page_case(16, 4, 128, window, ctx, rows, dist="sym", seed=window + ctx)
