@@ -73,6 +73,9 @@ template <>
 struct Cfg<512> { static constexpr int kStages = 6, kGroups = 2, kWpg = 4, kMinBlocks = 1; };
 
 template <int HD>
+constexpr int kLgHd = HD == 64 ? 6 : HD == 128 ? 7 : HD == 256 ? 8 : 9;
+
+template <int HD>
 struct Geo {
     static constexpr int kStages = Cfg<HD>::kStages;
     static constexpr int kGroups = Cfg<HD>::kGroups;
@@ -396,10 +399,16 @@ __device__ __forceinline__ uint32_t swz(int row, int u)
 // All loads are issued up front (clamped to valid splits, then masked).
 // The statistics of merge_stats_warp from values already in registers: lane
 // l holds splits l, l+32, ... in v[] ((-inf, 0) beyond S).
-template <int kPer>
+//
+// With kLanes < 32 (S <= kLanes, kPer = 1) the butterflies start at
+// kLanes / 2: the skipped steps would only combine lanes < S with lanes
+// holding (-inf, 0) -- an exact max with -inf and an exact sum with +0 --
+// so the result is the same bit for bit, with fewer shuffles.
+template <int kPer, int kLanes = 32>
 __device__ __forceinline__ float merge_stats_values(float2 (&v)[kPer], int S, float *w, int lane,
                                                     float *m_out = nullptr)
 {
+    static_assert(kLanes == 32 || kPer == 1, "narrow butterflies hold one value per lane");
     float mx = -INFINITY;
 #pragma unroll
     for (int j = 0; j < kPer; ++j) {
@@ -408,7 +417,7 @@ __device__ __forceinline__ float merge_stats_values(float2 (&v)[kPer], int S, fl
         mx = fmaxf(mx, v[j].x);
     }
 #pragma unroll
-    for (int k = 16; k; k >>= 1)
+    for (int k = kLanes / 2; k; k >>= 1)
         mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, k));
     if (m_out)
         *m_out = mx;
@@ -423,7 +432,7 @@ __device__ __forceinline__ float merge_stats_values(float2 (&v)[kPer], int S, fl
         }
     }
 #pragma unroll
-    for (int k = 16; k; k >>= 1)
+    for (int k = kLanes / 2; k; k >>= 1)
         L = __fadd_rn(L, __shfl_xor_sync(0xffffffffu, L, k));
     return L;
 }
@@ -492,6 +501,7 @@ enum TraceEvent {
     kTrFence = 9,        // last CTA: after the acquire fence
     kTrGroupO = 10,      // group results in shared memory
     kTrGroupStats = 11,  // group weights ready
+    kTrPushed = 12,      // cluster merge: slices pushed to their owners
 };
 
 // Slots of a CTA's trace record: 0-15 the SM cycle counter at each event;
@@ -711,6 +721,8 @@ __global__ void __launch_bounds__(Geo<HD>::kThreads, Cfg<HD>::kMinBlocks)
     __syncthreads();
     if (tid == 0)
         trace_event(p, kTrReady);
+    if (p.cluster > 1 && warp < NW)
+        cluster_wait();              // consumers: every peer's receive barrier is set up
 
     if (warp == NW) {
         // ------------------------------------------------ producer warp
@@ -972,11 +984,11 @@ __global__ void __launch_bounds__(Geo<HD>::kThreads, Cfg<HD>::kMinBlocks)
         // receive barrier.  The merge then runs on local shared memory, with
         // the same operations in the same order as the combine kernel, and
         // no CTA reads a peer, so none waits for its peers before exiting.
-        const int C = p.cluster;
-        const int slice = HD / C;
+        const int C = p.cluster;                         // 2, 4 or 8
+        const int lg_slice = kLgHd<HD> - (31 - __clz(C));
+        const int slice = 1 << lg_slice;                 // hd / C
         float *recv_o = reinterpret_cast<float *>(smem + SM::kRecvOff);
         float2 *recv_ml = reinterpret_cast<float2 *>(smem + SM::kRecvMlOff);
-        cluster_wait();              // every peer's receive barrier is set up
         constexpr int kVec = HD / 4;
 #pragma unroll
         for (int k = 0; k < kQRows * kVec / NT; ++k) {
@@ -995,9 +1007,9 @@ __global__ void __launch_bounds__(Geo<HD>::kThreads, Cfg<HD>::kMinBlocks)
                     o.w = __fmaf_rn(st[g], v.w, o.w);
                 }
             }
-            const int j = d / slice;
-            st_async_f32x4(map_to_cta(smem_u32(recv_o + (split * kQRows + q) * slice + (d - j * slice)), j), o,
-                           map_to_cta(s_recv, j));
+            const int j = d >> lg_slice;
+            st_async_f32x4(map_to_cta(smem_u32(recv_o + ((split * kQRows + q) << lg_slice) + (d & (slice - 1))), j),
+                           o, map_to_cta(s_recv, j));
         }
         if (tid < C * kQRows) {
             const int j = tid / kQRows, q = tid - j * kQRows;
@@ -1005,6 +1017,8 @@ __global__ void __launch_bounds__(Geo<HD>::kThreads, Cfg<HD>::kMinBlocks)
                                      : make_float2(-INFINITY, 0.f);
             st_async_f32x2(map_to_cta(smem_u32(recv_ml + split * kQRows + q), j), ml, map_to_cta(s_recv, j));
         }
+        if (tid == 0)
+            trace_event(p, kTrPushed);
         if (!mbar_wait_bounded(s_recv, 0, p.err, kErrTimeoutCluster))
             return;
         if (tid == 0)
@@ -1013,18 +1027,28 @@ __global__ void __launch_bounds__(Geo<HD>::kThreads, Cfg<HD>::kMinBlocks)
         for (int q = warp; q < nq; q += NW) {
             float2 v[1];
             v[0] = lane < C ? recv_ml[lane * kQRows + q] : make_float2(-INFINITY, 0.f);
-            const float L = merge_stats_values(v, C, cw + q * (kMaxCluster + 1), lane);
+            const float L = merge_stats_values<1, kMaxCluster>(v, C, cw + q * (kMaxCluster + 1), lane);
             if (lane == 0)
                 cw[q * (kMaxCluster + 1) + kMaxCluster] = L;
         }
+        if (tid == 0)
+            trace_event(p, kTrStats);
         named_bar_sync<kAllConsumersBarrier, NT>();
+        if (tid == 0)
+            trace_event(p, kTrFence);
         const int d0 = split * slice;
-        for (int e = tid; e < nq * slice; e += NT) {
-            const int q = e / slice, dd = e - q * slice;
+        for (int e = tid; e < (nq << lg_slice); e += NT) {
+            const int q = e >> lg_slice, dd = e & (slice - 1);
+            float vj[kMaxCluster];
+#pragma unroll
+            for (int j = 0; j < kMaxCluster; ++j)
+                vj[j] = j < C ? recv_o[((j * kQRows + q) << lg_slice) + dd] : 0.f;
             const float *w = cw + q * (kMaxCluster + 1);
             float acc = 0.f;
-            for (int j = 0; j < C; ++j)
-                acc = __fmaf_rn(w[j], recv_o[(j * kQRows + q) * slice + dd], acc);
+#pragma unroll
+            for (int j = 0; j < kMaxCluster; ++j)
+                if (j < C)
+                    acc = __fmaf_rn(w[j], vj[j], acc);
             const size_t rh = static_cast<size_t>(r0 + q / nh_sub) * p.nh + head0 + q % nh_sub;
             p.o[rh * HD + d0 + dd] = merge_finish(acc, w[kMaxCluster]);
         }
