@@ -239,7 +239,17 @@ size_t pgqa_decode_counter_count(int rows, int nh, int nkv)
     return static_cast<size_t>(rows) * nkv * ((g + pgqa::kQRows - 1) / pgqa::kQRows) * pgqa::kCountersPerTile;
 }
 
-int pgqa_choose_splits_for(int kv_len_eff, int rows, int nkv, int nseq, int num_sms)
+namespace {
+
+// Clusters of 2, 4 and 8 CTAs (index log2) resident at once with one CTA per
+// SM -- the split kernel's shape at head dims 256 and 512 -- measured on a
+// 152-SM GB300.  A cluster must fit in one GPC, so 8-CTA clusters fit only
+// 15 times, not 19.
+constexpr int kClusters152[4] = {152, 76, 36, 15};
+
+// The split-count rule; `clusters` (index log2 of the size) is the device's
+// cluster residency, or null for the 152-SM table scaled to num_sms.
+int choose_splits_rule(int kv_len_eff, int rows, int nkv, int nseq, int num_sms, const int *clusters)
 {
     if (kv_len_eff < 1)
         kv_len_eff = 1;
@@ -263,12 +273,20 @@ int pgqa_choose_splits_for(int kv_len_eff, int rows, int nkv, int nseq, int num_
     if (s > cap)
         s = cap;
     // Up to 24 splits, take a power of two no larger than 8: 2, 4 and 8
-    // splits merge on chip, in one thread-block cluster per tile.
+    // splits merge on chip, in one thread-block cluster per tile.  Prefer the
+    // largest such size whose clusters, one per tile, are all resident at
+    // once; if none is, the largest power of two.
     if (s <= 24) {
         long long p2 = 1;
         while (p2 * 2 <= s && p2 < 8)
             p2 *= 2;
-        s = p2;
+        long long fit = 1;
+        for (int lg = 1; (1LL << lg) <= p2; ++lg) {
+            const long long res = clusters ? clusters[lg] : static_cast<long long>(kClusters152[lg]) * num_sms / 152;
+            if (res >= tiles)
+                fit = 1LL << lg;
+        }
+        s = fit > 1 ? fit : p2;
     }
     if (s > PGQA_MAX_SPLITS)
         s = PGQA_MAX_SPLITS;
@@ -277,16 +295,33 @@ int pgqa_choose_splits_for(int kv_len_eff, int rows, int nkv, int nseq, int num_
     return static_cast<int>(s);
 }
 
+}  // namespace
+
+int pgqa_choose_splits_for(int kv_len_eff, int rows, int nkv, int nseq, int num_sms)
+{
+    return choose_splits_rule(kv_len_eff, rows, nkv, nseq, num_sms, nullptr);
+}
+
 int pgqa_choose_splits(int kv_len_eff, int rows, int nkv, int nseq)
 {
     int sms = 152;
+    int clusters[4] = {};
+    bool have = false;
     {
         std::lock_guard<std::mutex> lock(g_mutex);
         DeviceState *s = nullptr;
-        if (device_state(&s) == PGQA_OK)
+        if (device_state(&s) == PGQA_OK) {
             sms = s->num_sms;
+            have = true;
+            for (int lg = 1; lg <= 3; ++lg) {    // the one-CTA-per-SM shape: head dim 256
+                int &cap = s->cluster_cap[2][lg];
+                if (cap < 0)
+                    cap = pgqa::cluster_capacity_hd256(1 << lg);
+                clusters[lg] = cap;
+            }
+        }
     }
-    return pgqa_choose_splits_for(kv_len_eff, rows, nkv, nseq, sms);
+    return choose_splits_rule(kv_len_eff, rows, nkv, nseq, sms, have ? clusters : nullptr);
 }
 
 int pgqa_device_status(void)

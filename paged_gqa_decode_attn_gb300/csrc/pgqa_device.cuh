@@ -99,7 +99,7 @@ struct Smem {
     static constexpr int kXOff = kStagesBytes;                     // S exchange: float4 [groups][2][wpg][32]
     static constexpr int kXBytes = G::kGroups * 2 * G::kWpg * 32 * 16;
     static constexpr int kBarOff = kXOff + kXBytes;
-    static constexpr int kBarBytes = (2 * G::kStages + 1) * 8;      // full, empty; cluster receive
+    static constexpr int kBarBytes = (2 * G::kStages + 2) * 8;      // full, empty; cluster receive O, (M, L)
     static constexpr int kMiscOff = kBarOff + kBarBytes;
     static constexpr int kTotal = kMiscOff + 16;
     static constexpr int kAlloc = kTotal + 1024;                   // slack for 1024-B alignment
@@ -506,7 +506,8 @@ enum TraceEvent {
 
 // Slots of a CTA's trace record: 0-15 the SM cycle counter at each event;
 // 16 the global timer (ns) at kTrStart, 17 at the CTA's last event, 18 the
-// cycles one global-timer read took, 19 whether whole-tile TMA boxes were used.
+// cycles one global-timer read took, 19 whether whole-tile TMA boxes were used,
+// 20 the SM the CTA ran on, 21 its page count.
 __device__ __forceinline__ void trace_event(const DecodeParams &p, int ev, bool last = false)
 {
 #ifdef PGQA_TRACE
@@ -530,6 +531,22 @@ __device__ __forceinline__ void trace_event(const DecodeParams &p, int ev, bool 
     (void)p;
     (void)ev;
     (void)last;
+#endif
+}
+
+__device__ __forceinline__ void trace_placement(const DecodeParams &p, int npages)
+{
+#ifdef PGQA_TRACE
+    if (p.trace) {
+        const size_t cta = (static_cast<size_t>(blockIdx.z) * gridDim.y + blockIdx.y) * gridDim.x + blockIdx.x;
+        unsigned int sm;
+        asm volatile("mov.u32 %0, %%smid;" : "=r"(sm));
+        p.trace[cta * kTraceEvents + 20] = sm;
+        p.trace[cta * kTraceEvents + 21] = static_cast<unsigned long long>(npages);
+    }
+#else
+    (void)p;
+    (void)npages;
 #endif
 }
 
@@ -576,7 +593,8 @@ __global__ void __launch_bounds__(Geo<HD>::kThreads, Cfg<HD>::kMinBlocks)
     const int nh_sub = min(kQRows, p.g - hs * kQRows);
     const int S = p.splits;
 
-    const uint32_t s_recv = s_full + 2 * NS * 8;    // cluster launches: peers' slices arrived
+    const uint32_t s_recv = s_full + 2 * NS * 8;    // cluster launches: peers' O slices arrived
+    const uint32_t s_recv_ml = s_recv + 8;          // cluster launches: peers' (M, L) arrived
     // Barriers first: the init fence then has no earlier load to wait for.
     if (tid == 0) {
         for (int s = 0; s < NS; ++s) {
@@ -584,10 +602,12 @@ __global__ void __launch_bounds__(Geo<HD>::kThreads, Cfg<HD>::kMinBlocks)
             mbar_init(s_empty + 8 * s, WPG);
         }
         if (p.cluster > 1) {
-            // completes once every peer (this CTA included) has pushed its
-            // O slice and (M, L) of all 8 query rows
+            // complete once every peer (this CTA included) has pushed its O
+            // slice, and its (M, L), of all 8 query rows
             mbar_init(s_recv, 1);
-            mbar_arrive_expect_tx(s_recv, kQRows * HD * 4 + p.cluster * kQRows * 8);
+            mbar_arrive_expect_tx(s_recv, kQRows * HD * 4);
+            mbar_init(s_recv_ml, 1);
+            mbar_arrive_expect_tx(s_recv_ml, p.cluster * kQRows * 8);
         }
         mbar_init_fence();
     }
@@ -667,6 +687,9 @@ __global__ void __launch_bounds__(Geo<HD>::kThreads, Cfg<HD>::kMinBlocks)
             npages_mine = p0 + static_cast<int>((static_cast<long long>(split + 1) * np) / S) - page_begin;
         }
     }
+
+    if (tid == 0)
+        trace_placement(p, npages_mine);
 
     // ---- loads that need no barrier go out before the barrier set-up
     const int32_t *tbl = nullptr;
@@ -953,22 +976,30 @@ __global__ void __launch_bounds__(Geo<HD>::kThreads, Cfg<HD>::kMinBlocks)
     named_bar_sync<kAllConsumersBarrier, NT>();
     if (tid == 0)
         trace_event(p, kTrGroupO);
-    if (tid < nq) {
-        float mx = -INFINITY;
-        for (int g = 0; g < NG; ++g)
-            mx = fmaxf(mx, mlbuf[g * kQRows + tid].x);
-        float L = 0.f;
-        for (int g = 0; g < NG; ++g) {
-            const float2 v = mlbuf[g * kQRows + tid];
-            const float ws = (v.x == -INFINITY) ? 0.f : exp2f(v.x - mx);
-            stat[tid * (NG + 2) + g] = ws;
-            L = __fmaf_rn(ws, v.y, L);
+    if (tid < kQRows) {
+        float mx = -INFINITY, L = 0.f;    // query rows >= nq: an empty partial
+        if (tid < nq) {
+            for (int g = 0; g < NG; ++g)
+                mx = fmaxf(mx, mlbuf[g * kQRows + tid].x);
+            for (int g = 0; g < NG; ++g) {
+                const float2 v = mlbuf[g * kQRows + tid];
+                const float ws = (v.x == -INFINITY) ? 0.f : exp2f(v.x - mx);
+                stat[tid * (NG + 2) + g] = ws;
+                L = __fmaf_rn(ws, v.y, L);
+            }
+            stat[tid * (NG + 2) + NG] = L;
+            stat[tid * (NG + 2) + NG + 1] = mx;
+            if (S > 1 && p.cluster <= 1) {
+                const size_t rh = static_cast<size_t>(r0 + tid / nh_sub) * p.nh + head0 + tid % nh_sub;
+                p.part_ml[rh * S + split] = make_float2(mx, L);
+            }
         }
-        stat[tid * (NG + 2) + NG] = L;
-        stat[tid * (NG + 2) + NG + 1] = mx;
-        if (S > 1 && p.cluster <= 1) {
-            const size_t rh = static_cast<size_t>(r0 + tid / nh_sub) * p.nh + head0 + tid % nh_sub;
-            p.part_ml[rh * S + split] = make_float2(mx, L);
+        if (p.cluster > 1) {
+            // this split's (M, L) to every slice owner, ahead of the O slices,
+            // so the owners' merge weights overlap the O transfer
+            const uint32_t a = smem_u32(reinterpret_cast<float2 *>(smem + SM::kRecvMlOff) + split * kQRows + tid);
+            for (int j = 0; j < p.cluster; ++j)
+                st_async_f32x2(map_to_cta(a, j), make_float2(mx, L), map_to_cta(s_recv_ml, j));
         }
     }
     named_bar_sync<kAllConsumersBarrier, NT>();
@@ -1011,15 +1042,9 @@ __global__ void __launch_bounds__(Geo<HD>::kThreads, Cfg<HD>::kMinBlocks)
             st_async_f32x4(map_to_cta(smem_u32(recv_o + ((split * kQRows + q) << lg_slice) + (d & (slice - 1))), j),
                            o, map_to_cta(s_recv, j));
         }
-        if (tid < C * kQRows) {
-            const int j = tid / kQRows, q = tid - j * kQRows;
-            const float2 ml = q < nq ? make_float2(stat[q * (NG + 2) + NG + 1], stat[q * (NG + 2) + NG])
-                                     : make_float2(-INFINITY, 0.f);
-            st_async_f32x2(map_to_cta(smem_u32(recv_ml + split * kQRows + q), j), ml, map_to_cta(s_recv, j));
-        }
         if (tid == 0)
             trace_event(p, kTrPushed);
-        if (!mbar_wait_bounded(s_recv, 0, p.err, kErrTimeoutCluster))
+        if (!mbar_wait_bounded(s_recv_ml, 0, p.err, kErrTimeoutCluster))
             return;
         if (tid == 0)
             trace_event(p, kTrTicket);
@@ -1033,6 +1058,8 @@ __global__ void __launch_bounds__(Geo<HD>::kThreads, Cfg<HD>::kMinBlocks)
         }
         if (tid == 0)
             trace_event(p, kTrStats);
+        if (!mbar_wait_bounded(s_recv, 0, p.err, kErrTimeoutCluster))
+            return;
         named_bar_sync<kAllConsumersBarrier, NT>();
         if (tid == 0)
             trace_event(p, kTrFence);

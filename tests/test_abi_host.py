@@ -86,6 +86,10 @@ def test_choose_splits_rule(lib):
         for tiles in range(1, 160):
             s = pgqa.choose_splits(kv, tiles, 1, tiles, num_sms=152)
             assert s > 24 or (s in (1, 2, 4, 8))
+            if s in (2, 4, 8) and tiles <= 76:      # GB300 residency: 76 clusters of 2, 36 of 4, 15 of 8
+                assert {2: 76, 4: 36, 8: 15}[s] >= tiles, (kv, tiles, s)
+    assert pgqa.choose_splits(1 << 16, 15, 1, 15, num_sms=152) == 8
+    assert pgqa.choose_splits(1 << 16, 16, 1, 16, num_sms=152) == 4     # 16 clusters of 8 would take 2 waves
     # nseq outside [1, rows] means every row is its own sequence
     assert pgqa.choose_splits(1024, 4, 8, 0, num_sms=152) == pgqa.choose_splits(1024, 4, 8, 4, num_sms=152)
     # without a device the current-device form falls back to 152 SMs
