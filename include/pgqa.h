@@ -43,6 +43,7 @@ extern "C" {
 #define PGQA_ERR_DEVICE_TIMEOUT (-6)     /* a kernel gave up a bounded wait (see pgqa_device_status) */
 #define PGQA_ERR_TOO_MANY_SPLITS (-7)    /* splits > PGQA_MAX_SPLITS */
 #define PGQA_ERR_NOALLOC_TOO_LARGE (-8)  /* call needs more scratch than pgqa_attn_decode_noalloc has */
+#define PGQA_ERR_TILE_TOO_LONG (-9)      /* (device) a prefill tile held more rows than rows_per_tile */
 
 #define PGQA_PAGE_TOKENS 16
 #define PGQA_MAX_SPLITS 256
@@ -169,6 +170,52 @@ int pgqa_attn_decode_noalloc(void *o, const void *q, const void *k_pool, const v
                              const int32_t *block_table, const int32_t *off, const int32_t *qpos,
                              const int32_t *kvpos, int rows, int nh, int nkv, int hd, int window,
                              int splits, const int32_t *page_map, void *stream);
+
+/*
+ * Paged causal prefill: `attn::attn_prefill`, with `attn::make_tiles` and
+ * `attn::prefill_rows_per_tile`, of span-02 engine/crates/kernels/tests/gpu.rs,
+ * `run` ("prefill: all ctx rows causal").
+ *
+ * Every row r of the tiles, for every head h, attends exactly as a decode row
+ * does (pgqa_attn_decode): scale 1.0, kv head h / (nh/nkv), the positions
+ * [lo(r), min(qpos[r], kvpos[r])] with lo(r) = window > 0 ?
+ * max(0, qpos[r] + 1 - window) : 0, read through
+ * block_table[off[r] + pos/16] and the optional page_map.
+ *   o        [rows][nh][hd] bf16, written (round to nearest), never read
+ *   q        [rows][nh][hd] bf16
+ *   k_pool, v_pool, block_table, off, qpos, kvpos, page_map: as for decode
+ *            (kvpos may be NULL, meaning qpos; page_map may be NULL)
+ *   tile_t0, tile_tn  [ntiles] int32, device: tile i is rows
+ *            tile_t0[i] .. tile_t0[i] + tile_tn[i] - 1, all with the same off
+ *            and at most pgqa_prefill_rows_per_tile(hd) of them (pgqa_make_tiles
+ *            builds such tiles); rows not in any tile are not written
+ * All buffers are caller-owned device memory; q, o and the pools must be
+ * 16-byte aligned.  Asynchronous on `stream`; no host synchronisation, no
+ * allocation.  Returns PGQA_OK (also for ntiles == 0) or PGQA_ERR_* for bad
+ * arguments (checked before any CUDA call) or a launch failure.  A tile
+ * longer than rows_per_tile is skipped and reported by pgqa_device_status as
+ * PGQA_ERR_TILE_TOO_LONG.  The result does not depend on the physical page
+ * ids: a permuted pool behind a page map gives the same bits.
+ */
+int pgqa_attn_prefill(void *o, const void *q, const void *k_pool, const void *v_pool,
+                      const int32_t *block_table, const int32_t *off, const int32_t *qpos,
+                      const int32_t *kvpos, const int32_t *tile_t0, const int32_t *tile_tn, int ntiles,
+                      int nh, int nkv, int hd, int window, const int32_t *page_map, void *stream);
+
+/* The longest tile pgqa_attn_prefill takes at head dimension hd (64 rows;
+ * 32 at hd 512), or PGQA_ERR_UNSUPPORTED_HD. */
+int pgqa_prefill_rows_per_tile(int hd);
+
+/*
+ * Host-side tiling of `rows` rows (host int32 `seq[rows]`, any per-row key
+ * whose changes end a tile: the sequence id or its off): consecutive rows
+ * with equal keys, at most rows_per_tile per tile, in row order.  Writes
+ * tile_t0/tile_tn (host arrays of max_tiles) and returns the tile count; with
+ * both NULL only returns the count.  PGQA_ERR_INVALID_ARGUMENT for bad sizes
+ * or too small arrays.
+ */
+int pgqa_make_tiles(const int32_t *seq, int rows, int rows_per_tile, int32_t *tile_t0, int32_t *tile_tn,
+                    int max_tiles);
 
 /* Static, human-readable name of a status code. */
 const char *pgqa_strerror(int status);

@@ -1,14 +1,15 @@
-"""Split-KV paged GQA decode attention for NVIDIA GB300 (sm_103a).
+"""Split-KV paged GQA decode attention, and paged causal prefill, for NVIDIA GB300 (sm_103a).
 
 The compute path is libpgqa.so (hand-written CUDA, C ABI in include/pgqa.h);
 this package only builds it, loads it and marshals arguments.  ``workloads``
 draws the seeded synthetic inputs used by the tests and the benchmark.
 """
-from ._lib import (MAX_SPLITS, PAGE_TOKENS, PgqaError, attn_decode, attn_decode_noalloc, choose_splits,
-                   decode_counter_count, decode_part_bytes, device_status, lib_path, load, strerror, trace_buffer,
-                   version)
+from ._lib import (MAX_SPLITS, PAGE_TOKENS, PgqaError, attn_decode, attn_decode_noalloc, attn_prefill,
+                   choose_splits, decode_counter_count, decode_part_bytes, device_status, lib_path, load, make_tiles,
+                   prefill_rows_per_tile, strerror, trace_buffer, version)
 from .builder import build
 
-__all__ = ["attn_decode", "attn_decode_noalloc", "choose_splits", "decode_part_bytes", "decode_counter_count",
+__all__ = ["attn_decode", "attn_decode_noalloc", "attn_prefill", "make_tiles", "prefill_rows_per_tile",
+           "choose_splits", "decode_part_bytes", "decode_counter_count",
            "device_status", "PgqaError", "build", "load", "lib_path", "strerror", "trace_buffer", "version",
            "PAGE_TOKENS", "MAX_SPLITS"]

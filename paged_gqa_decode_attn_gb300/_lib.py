@@ -1,5 +1,5 @@
 """ctypes binding of libpgqa.so (include/pgqa.h).  Argument marshalling only:
-every step of the decode runs in the library's CUDA kernels.  There is no CPU
+every step of the decode and the prefill runs in the library's CUDA kernels.  There is no CPU
 fallback: without the built library these functions raise."""
 from __future__ import annotations
 
@@ -17,6 +17,7 @@ PGQA_ERR_TENSOR_MAP = -5
 PGQA_ERR_DEVICE_TIMEOUT = -6
 PGQA_ERR_TOO_MANY_SPLITS = -7
 PGQA_ERR_NOALLOC_TOO_LARGE = -8
+PGQA_ERR_TILE_TOO_LONG = -9
 NOALLOC_MAX_COUNTERS = 16384
 NOALLOC_MAX_PART_BYTES = 8 * 1024 * 1024
 PAGE_TOKENS = 16
@@ -35,6 +36,9 @@ SIGNATURES = {
     "pgqa_version": (_I, []),
     "pgqa_trace_buffer": (_I, [_P, ctypes.c_size_t]),
     "pgqa_attn_decode_noalloc": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P]),
+    "pgqa_attn_prefill": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P]),
+    "pgqa_prefill_rows_per_tile": (_I, [_I]),
+    "pgqa_make_tiles": (_I, [_P, _I, _I, _P, _P, _I]),
 }
 
 
@@ -113,6 +117,42 @@ def attn_decode_noalloc(o, q, k_pool, v_pool, block_table, off, qpos, kvpos, row
                                          int(splits), _ptr(page_map), _stream(stream))
     if st != PGQA_OK:
         raise PgqaError(st, "attn_decode_noalloc")
+
+
+def attn_prefill(o, q, k_pool, v_pool, block_table, off, qpos, kvpos, tile_t0, tile_tn, ntiles: int, nh: int,
+                 nkv: int, hd: int, window: int, page_map=None, stream=None) -> None:
+    """Paged causal prefill (``pgqa_attn_prefill``) over the tiles ``tile_t0``/``tile_tn``
+    (device int32 arrays, e.g. from ``make_tiles``), enqueued on ``stream``."""
+    st = load().pgqa_attn_prefill(_ptr(o), _ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(block_table), _ptr(off),
+                                  _ptr(qpos), _ptr(kvpos), _ptr(tile_t0), _ptr(tile_tn), int(ntiles), int(nh),
+                                  int(nkv), int(hd), int(window), _ptr(page_map), _stream(stream))
+    if st != PGQA_OK:
+        raise PgqaError(st, "attn_prefill")
+
+
+def prefill_rows_per_tile(hd: int) -> int:
+    n = int(load().pgqa_prefill_rows_per_tile(int(hd)))
+    if n < 0:
+        raise PgqaError(n, "prefill_rows_per_tile")
+    return n
+
+
+def make_tiles(seq, rows_per_tile: int):
+    """``pgqa_make_tiles`` on a host sequence of per-row keys: (tile_t0, tile_tn) as int32 numpy arrays."""
+    import numpy as np
+    key = np.ascontiguousarray(np.asarray(seq, dtype=np.int32))
+    lib = load()
+    n = int(lib.pgqa_make_tiles(key.ctypes.data if key.size else None, int(key.size), int(rows_per_tile),
+                                None, None, 0))
+    if n < 0:
+        raise PgqaError(n, "make_tiles")
+    t0 = np.zeros(max(n, 1), dtype=np.int32)
+    tn = np.zeros(max(n, 1), dtype=np.int32)
+    m = int(lib.pgqa_make_tiles(key.ctypes.data if key.size else None, int(key.size), int(rows_per_tile),
+                                t0.ctypes.data, tn.ctypes.data, n))
+    if m != n:
+        raise PgqaError(m if m < 0 else PGQA_ERR_INVALID_ARGUMENT, "make_tiles")
+    return t0[:n], tn[:n]
 
 
 def choose_splits(kv_len_eff: int, rows: int, nkv: int, nseq: int, num_sms: int | None = None) -> int:

@@ -13,6 +13,7 @@
 
 #include "pgqa.h"
 #include "pgqa_launch.cuh"
+#include "pgqa_prefill.cuh"
 
 namespace {
 
@@ -26,6 +27,7 @@ struct DeviceState {
     int num_sms = 0;
     unsigned int *err = nullptr;
     bool attr_set[4] = {false, false, false, false};
+    bool prefill_attr_set[4] = {false, false, false, false};
     int cluster_cap[4][5] = {{-1, -1, -1, -1, -1}, {-1, -1, -1, -1, -1}, {-1, -1, -1, -1, -1},
                              {-1, -1, -1, -1, -1}};   // [hd][log2 cluster]: resident clusters, -1 unknown
 };
@@ -216,6 +218,7 @@ const char *pgqa_strerror(int status)
     case PGQA_ERR_DEVICE_TIMEOUT: return "a kernel gave up a bounded wait";
     case PGQA_ERR_TOO_MANY_SPLITS: return "splits above PGQA_MAX_SPLITS";
     case PGQA_ERR_NOALLOC_TOO_LARGE: return "call needs more scratch than the no-allocation entry point holds";
+    case PGQA_ERR_TILE_TOO_LONG: return "a prefill tile held more rows than pgqa_prefill_rows_per_tile";
     default: return "unknown status";
     }
 }
@@ -339,7 +342,7 @@ int pgqa_device_status(void)
         const unsigned int zero = 0;
         if (cudaMemcpy(s->err, &zero, sizeof zero, cudaMemcpyHostToDevice) != cudaSuccess)
             return PGQA_ERR_CUDA;
-        return PGQA_ERR_DEVICE_TIMEOUT;
+        return (word & pgqa::kErrTileRows) ? PGQA_ERR_TILE_TOO_LONG : PGQA_ERR_DEVICE_TIMEOUT;
     }
     return PGQA_OK;
 }
@@ -439,3 +442,115 @@ int pgqa_attn_decode(void *o, void *part, const void *q, const void *k_pool, con
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------- prefill
+
+int pgqa_prefill_rows_per_tile(int hd)
+{
+    switch (hd) {
+    case 64: return pgqa::PfCfg<64>::kRowsPerTile;
+    case 128: return pgqa::PfCfg<128>::kRowsPerTile;
+    case 256: return pgqa::PfCfg<256>::kRowsPerTile;
+    case 512: return pgqa::PfCfg<512>::kRowsPerTile;
+    default: return PGQA_ERR_UNSUPPORTED_HD;
+    }
+}
+
+int pgqa_make_tiles(const int32_t *seq, int rows, int rows_per_tile, int32_t *tile_t0, int32_t *tile_tn,
+                    int max_tiles)
+{
+    if (rows < 0 || rows_per_tile < 1 || (rows > 0 && !seq))
+        return PGQA_ERR_INVALID_ARGUMENT;
+    int n = 0;
+    for (int r = 0, len = 0; r < rows; ++r) {
+        if (r == 0 || seq[r] != seq[r - 1] || len == rows_per_tile) {
+            ++n;
+            len = 0;
+        }
+        ++len;
+    }
+    if (!tile_t0 && !tile_tn)
+        return n;
+    if (!tile_t0 || !tile_tn || max_tiles < n)
+        return PGQA_ERR_INVALID_ARGUMENT;
+    int t = -1;
+    for (int r = 0; r < rows; ++r) {
+        if (r == 0 || seq[r] != seq[r - 1] || tile_tn[t] == rows_per_tile) {
+            ++t;
+            tile_t0[t] = r;
+            tile_tn[t] = 0;
+        }
+        ++tile_tn[t];
+    }
+    return n;
+}
+
+int pgqa_attn_prefill(void *o, const void *q, const void *k_pool, const void *v_pool, const int32_t *block_table,
+                      const int32_t *off, const int32_t *qpos, const int32_t *kvpos, const int32_t *tile_t0,
+                      const int32_t *tile_tn, int ntiles, int nh, int nkv, int hd, int window,
+                      const int32_t *page_map, void *stream)
+{
+    if (ntiles < 0 || nh <= 0 || nkv <= 0 || nh % nkv != 0 || window < 0)
+        return PGQA_ERR_INVALID_ARGUMENT;
+    const int hi = hd_index(hd);
+    if (hi < 0)
+        return PGQA_ERR_UNSUPPORTED_HD;
+    if (ntiles == 0)
+        return PGQA_OK;
+    if (!o || !q || !k_pool || !v_pool || !block_table || !off || !qpos || !tile_t0 || !tile_tn)
+        return PGQA_ERR_INVALID_ARGUMENT;
+    const int g = nh / nkv;
+    const int rpt = pgqa_prefill_rows_per_tile(hd);
+    const int qr = hd == 512 ? pgqa::PfGeo<512>::kQueryRows : pgqa::PfGeo<64>::kQueryRows;
+    if (nkv > 65535 || (static_cast<long long>(rpt) * g + qr - 1) / qr > 65535)
+        return PGQA_ERR_INVALID_ARGUMENT;
+    if (!aligned(k_pool, 16) || !aligned(v_pool, 16) || !aligned(q, 16) || !aligned(o, 16))
+        return PGQA_ERR_MISALIGNED;
+
+    pgqa::PrefillLaunchArgs a;
+    pgqa::PrefillParams &p = a.p;
+    p.o = static_cast<__nv_bfloat16 *>(o);
+    p.q = static_cast<const __nv_bfloat16 *>(q);
+    p.block_table = block_table;
+    p.off = off;
+    p.qpos = qpos;
+    p.kvpos = kvpos;
+    p.page_map = page_map;
+    p.tile_t0 = tile_t0;
+    p.tile_tn = tile_tn;
+    p.nh = nh;
+    p.nkv = nkv;
+    p.g = g;
+    p.window = window;
+    p.rows_per_tile = rpt;
+    a.ntiles = ntiles;
+    a.stream = static_cast<cudaStream_t>(stream);
+
+    std::lock_guard<std::mutex> lock(g_mutex);
+    DeviceState *s = nullptr;
+    int st = device_state(&s);
+    if (st != PGQA_OK)
+        return st;
+    CUtensorMap tk, tv;
+    int whole_k = 0, whole_v = 0;
+    if ((st = pool_map(k_pool, hd, &tk, &whole_k)) != PGQA_OK || (st = pool_map(v_pool, hd, &tv, &whole_v)) != PGQA_OK)
+        return st;
+    if (whole_k != whole_v)
+        return PGQA_ERR_TENSOR_MAP;
+    p.whole_tile_box = whole_k;
+    p.err = s->err;
+    a.tm_k = &tk;
+    a.tm_v = &tv;
+    const bool set_attr = !s->prefill_attr_set[hi];
+    cudaError_t e;
+    switch (hd) {
+    case 64: e = pgqa::launch_prefill_hd64(a, set_attr); break;
+    case 128: e = pgqa::launch_prefill_hd128(a, set_attr); break;
+    case 256: e = pgqa::launch_prefill_hd256(a, set_attr); break;
+    default: e = pgqa::launch_prefill_hd512(a, set_attr); break;
+    }
+    if (e != cudaSuccess)
+        return PGQA_ERR_CUDA;
+    s->prefill_attr_set[hi] = true;
+    return PGQA_OK;
+}

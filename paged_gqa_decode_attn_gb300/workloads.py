@@ -264,6 +264,29 @@ def page_case(nh: int, nkv: int, hd: int, window: int, ctx: int, rows: int,
                 window, rows, q, k, v, bt, off, qpos, ctx=ctx, npg=npg)
 
 
+def prefill_case(nh: int, nkv: int, hd: int, window: int, ctx: int, decode_rows: int = 0,
+                 dist: str = "page", seed: Optional[int] = None, name: str = "") -> Case:
+    """The page's prefill fixture: rows at positions 0..ctx-1, off 0, identity table.
+
+    One LCG stream gives the K pool, the V pool, the decode rows' Q (drawn and
+    dropped when ``decode_rows`` > 0, so the stream matches the page's test,
+    which runs the decode first) and then the ctx rows' Q.
+    """
+    rng = Lcg(12345 + hd if seed is None else seed)
+    npg = (ctx + PAGE - 1) // PAGE + 1
+    n = npg * nkv * PAGE * hd
+    k = draw_bf16(rng, n, dist)
+    v = draw_bf16(rng, n, dist)
+    if decode_rows:
+        draw_bf16(rng, decode_rows * nh * hd, dist)
+    q = draw_bf16(rng, ctx * nh * hd, dist)
+    bt = np.arange((ctx + PAGE - 1) // PAGE, dtype=np.int32)
+    qpos = np.arange(ctx, dtype=np.int32)
+    off = np.zeros(ctx, dtype=np.int32)
+    return Case(name or f"prefill_nh{nh}_nkv{nkv}_hd{hd}_w{window}_ctx{ctx}", nh, nkv, hd, window, ctx, q, k, v,
+                bt, off, qpos, ctx=ctx, npg=npg)
+
+
 def with_mapped_pool(c: Case, fold_into_table: bool = False) -> Case:
     """The same KV behind the permuted / NaN-null-page pool.
 
@@ -318,6 +341,16 @@ SWEEP_HD = (128, 256, 512)
 SWEEP_CTX = (1024, 4096, 16384, 65536)
 SWEEP_ROWS = (1, 4, 16)
 SWEEP_WINDOW = (0, 1024, 4096)
+
+
+def prefill_page() -> Case:
+    """The page's first prefill: nh16 nkv8 hd256, window 1024, 1500 rows (after its 5-row decode)."""
+    return prefill_case(16, 8, 256, 1024, 1500, decode_rows=5, name="prefill_nh16_nkv8_hd256_w1024_ctx1500")
+
+
+def prefill_long() -> Case:
+    """A measured prefill: nh16 nkv8 hd256, window 1024, 8192 rows (the sliding decode's sequence)."""
+    return prefill_case(16, 8, 256, 1024, 8192, dist="sym", name="prefill_nh16_nkv8_hd256_w1024_ctx8192")
 
 
 def sweep_points():

@@ -1,11 +1,36 @@
 """Helpers for the GPU parity tests: upload a workloads.Case and run the library on it.
 
-Only marshalling: the decode itself runs in libpgqa.so's kernels.
+Only marshalling: the decode and the prefill run in libpgqa.so's kernels.
 """
 import numpy as np
 import torch
 
+import oracle
 import paged_gqa_decode_attn_gb300 as pgqa
+from paged_gqa_decode_attn_gb300 import workloads as wl
+
+REL_RMS_GATE = 1e-2
+
+
+def bits_to_f64(b):
+    return wl.bf16_to_f32(b).astype(np.float64)
+
+
+def check_parity(case, got, label=""):
+    """The page's gate (rel-RMS of the bf16 output against the oracle's bf16 output
+    < 1e-2) plus an element bound from the arithmetic (bf16 P and output rounding,
+    f32 accumulation): |o - o_f64| <= 2^-7 (|o_f64| + max|V|)."""
+    ref64, ref16 = oracle.decode_case(case)
+    e = oracle.rel_rms(got, ref16)
+    assert e < REL_RMS_GATE, f"{label} rel_rms {e:.3e}"
+    g = bits_to_f64(got)
+    vv = bits_to_f64(case.v_pool)
+    vmax = float(np.nanmax(np.abs(np.where(np.isfinite(vv), vv, 0))))
+    bound = 2.0 ** -7 * (np.abs(ref64) + vmax)
+    bad = np.abs(g - ref64) > bound
+    assert not bad.any(), f"{label}: {int(bad.sum())} elements beyond bound, first {np.argwhere(bad)[0]}"
+    assert np.all(np.isfinite(g))
+    return e
 
 
 def dev_i16(a: np.ndarray, device="cuda") -> torch.Tensor:
@@ -65,3 +90,36 @@ def first_difference(a: np.ndarray, b: np.ndarray) -> str:
         return "identical"
     i = int(idx[0])
     return f"{idx.size} differ; first at {i}: got 0x{int(fa[i]):04x}, expected 0x{int(fb[i]):04x}"
+
+
+class PrefillDev:
+    """A Case resident on the GPU for pgqa_attn_prefill, tiled by the library's make_tiles
+    over the per-row keys ``seq`` (default: off)."""
+
+    def __init__(self, case, seq=None, device="cuda"):
+        self.c = case
+        self.q = dev_i16(case.q, device)
+        self.k = dev_i16(case.k_pool, device)
+        self.v = dev_i16(case.v_pool, device)
+        self.bt = dev_i32(case.block_table, device)
+        self.off = dev_i32(case.off, device)
+        self.qpos = dev_i32(case.qpos, device)
+        self.kvpos = dev_i32(case.kvpos, device)
+        self.pm = dev_i32(case.page_map, device)
+        t0, tn = pgqa.make_tiles(case.off if seq is None else seq, pgqa.prefill_rows_per_tile(case.hd))
+        self.ntiles = len(t0)
+        self.t0 = dev_i32(t0 if len(t0) else np.zeros(1, np.int32), device)
+        self.tn = dev_i32(tn if len(tn) else np.zeros(1, np.int32), device)
+        self.o = torch.empty(case.rows * case.nh * case.hd, dtype=torch.int16, device=device)
+
+    def run(self, stream=None, fill=0x5555):
+        c = self.c
+        self.o.fill_(fill)
+        pgqa.attn_prefill(self.o, self.q, self.k, self.v, self.bt, self.off, self.qpos, self.kvpos, self.t0,
+                          self.tn, self.ntiles, c.nh, c.nkv, c.hd, c.window, self.pm, stream)
+        return self.o
+
+    def result(self, **kw) -> np.ndarray:
+        out = self.run(**kw)
+        torch.cuda.synchronize()
+        return out.cpu().numpy().view(np.uint16).reshape(self.c.rows, self.c.nh, self.c.hd)

@@ -7,6 +7,8 @@ import os
 import re
 import sys
 
+import numpy as np
+
 import pytest
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
@@ -50,7 +52,8 @@ def test_constants_agree_between_header_kernels_and_binding():
     assert hdr["PGQA_PAGE_TOKENS"] == int(re.search(r"kPage = (\d+);", dev).group(1)) == _lib.PAGE_TOKENS
     assert hdr["PGQA_MAX_SPLITS"] == int(re.search(r"kMaxSplits = (\d+);", dev).group(1)) == _lib.MAX_SPLITS
     for name in ("OK", "ERR_INVALID_ARGUMENT", "ERR_UNSUPPORTED_HD", "ERR_MISALIGNED", "ERR_CUDA",
-                 "ERR_TENSOR_MAP", "ERR_DEVICE_TIMEOUT", "ERR_TOO_MANY_SPLITS"):
+                 "ERR_TENSOR_MAP", "ERR_DEVICE_TIMEOUT", "ERR_TOO_MANY_SPLITS", "ERR_NOALLOC_TOO_LARGE",
+                 "ERR_TILE_TOO_LONG"):
         assert hdr["PGQA_" + name] == getattr(_lib, "PGQA_" + name)
 
 
@@ -97,7 +100,7 @@ def test_choose_splits_rule(lib):
 
 
 def test_strerror_names_every_code(lib):
-    for code in range(-7, 1):
+    for code in range(-9, 1):
         assert pgqa.strerror(code) != "unknown status"
     assert pgqa.strerror(-99) == "unknown status"
 
@@ -132,3 +135,61 @@ def test_python_binding_raises_on_error(lib):
     with pytest.raises(pgqa.PgqaError) as ei:
         pgqa.attn_decode(FAKE, None, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None, 1, 8, 2, 96, 0, 1, stream=0)
     assert ei.value.status == -2
+
+
+# ---------------------------------------------------------------- prefill host side
+
+def test_prefill_rows_per_tile(lib):
+    assert [pgqa.prefill_rows_per_tile(h) for h in (64, 128, 256, 512)] == [64, 64, 64, 32]
+    assert lib.pgqa_prefill_rows_per_tile(96) == -2
+
+
+def brute_tiles(seq, rpt):
+    t0, tn = [], []
+    for r, k in enumerate(seq):
+        if r == 0 or k != seq[r - 1] or tn[-1] == rpt:
+            t0.append(r)
+            tn.append(0)
+        tn[-1] += 1
+    return t0, tn
+
+
+@pytest.mark.parametrize("seq,rpt", [([0] * 130, 64), ([0, 0, 1, 1, 1, 2], 2), ([], 4), ([7], 1),
+                                     ([3] * 64, 64), ([3] * 65, 64), ([0, 1, 0, 1], 8),
+                                     (list(np.repeat([5, 9, 5, 2], [100, 1, 33, 64])), 32)])
+def test_make_tiles_matches_brute_force(lib, seq, rpt):
+    t0, tn = pgqa.make_tiles(seq, rpt)
+    e0, en = brute_tiles(list(seq), rpt)
+    assert list(t0) == e0 and list(tn) == en
+    assert sum(tn) == len(seq) and all(1 <= n <= rpt for n in tn)
+
+
+def test_make_tiles_rejects_bad_arguments(lib):
+    import ctypes
+    seq = (ctypes.c_int32 * 4)(0, 0, 1, 1)
+    t0 = (ctypes.c_int32 * 1)()
+    tn = (ctypes.c_int32 * 1)()
+    assert lib.pgqa_make_tiles(seq, 4, 2, None, None, 0) == 2
+    assert lib.pgqa_make_tiles(seq, 4, 2, t0, tn, 1) == -1          # arrays too small
+    assert lib.pgqa_make_tiles(seq, 4, 0, None, None, 0) == -1       # rows_per_tile < 1
+    assert lib.pgqa_make_tiles(seq, -1, 2, None, None, 0) == -1
+    assert lib.pgqa_make_tiles(None, 3, 2, None, None, 0) == -1
+
+
+def prefill_call(lib, ntiles=1, nh=8, nkv=2, hd=128, window=0, o=FAKE, q=FAKE, k=FAKE, v=FAKE, bt=FAKE,
+                 off=FAKE, qpos=FAKE, t0=FAKE, tn=FAKE):
+    return lib.pgqa_attn_prefill(o, q, k, v, bt, off, qpos, None, t0, tn, ntiles, nh, nkv, hd, window, None, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(ntiles=-1), -1), (dict(nh=0), -1), (dict(nkv=0), -1), (dict(nh=10, nkv=4), -1), (dict(window=-1), -1),
+    (dict(hd=96), -2), (dict(o=None), -1), (dict(q=None), -1), (dict(k=None), -1), (dict(v=None), -1),
+    (dict(bt=None), -1), (dict(off=None), -1), (dict(qpos=None), -1), (dict(t0=None), -1), (dict(tn=None), -1),
+    (dict(k=FAKE + 8), -3), (dict(q=FAKE + 2), -3), (dict(o=FAKE + 4), -3), (dict(nkv=70000, nh=70000), -1),
+])
+def test_prefill_bad_arguments_are_rejected_before_any_cuda_call(lib, kw, code):
+    assert prefill_call(lib, **kw) == code
+
+
+def test_prefill_zero_tiles_is_ok_without_a_device(lib):
+    assert prefill_call(lib, ntiles=0, o=None, q=None) == 0

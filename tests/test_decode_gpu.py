@@ -25,7 +25,7 @@ from paged_gqa_decode_attn_gb300 import workloads as wl  # noqa: E402
 
 pytestmark = pytest.mark.gpu
 
-REL_RMS_GATE = 1e-2
+from gpu_util import REL_RMS_GATE, bits_to_f64, check_parity  # noqa: E402,F401
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -35,23 +35,6 @@ def _lib():
     pgqa.build()
     pgqa.load()
     yield
-
-
-def bits_to_f64(b):
-    return wl.bf16_to_f32(b).astype(np.float64)
-
-
-def check_parity(case, got, label=""):
-    ref64, ref16 = oracle.decode_case(case)
-    e = oracle.rel_rms(got, ref16)
-    assert e < REL_RMS_GATE, f"{label} rel_rms {e:.3e}"
-    g = bits_to_f64(got)
-    vmax = float(np.nanmax(np.abs(np.where(np.isfinite(bits_to_f64(case.v_pool)), bits_to_f64(case.v_pool), 0))))
-    bound = 2.0 ** -7 * (np.abs(ref64) + vmax)
-    bad = np.abs(g - ref64) > bound
-    assert not bad.any(), f"{label}: {int(bad.sum())} elements beyond bound, first {np.argwhere(bad)[0]}"
-    assert np.all(np.isfinite(g))
-    return e
 
 
 def full_gates(case, splits=None, mapped=True):

@@ -1,0 +1,189 @@
+"""GPU parity of libpgqa's paged causal prefill against the f64 oracle.
+
+The gates follow the prefill part of `run` in span-02
+``engine/crates/kernels/tests/gpu.rs``: every row of the sequence, tiled by
+``make_tiles`` with ``prefill_rows_per_tile``, is within rel-RMS 1e-2 of the
+reference, and the permuted pool behind a page map (and the map folded into
+the block table) gives the same bits.  Every element is also held to the
+arithmetic bound of the decode tests.  A prefill row is a decode row at the
+same position, so the oracle is the decode oracle over all rows.
+"""
+import dataclasses
+import os
+import sys
+
+import numpy as np
+import pytest
+
+sys.path.insert(0, os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, os.path.dirname(os.path.dirname(os.path.abspath(__file__))))
+
+from paged_gqa_decode_attn_gb300 import workloads as wl  # noqa: E402
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    import torch  # noqa: F401
+    import paged_gqa_decode_attn_gb300 as pgqa
+    pgqa.build()
+    pgqa.load()
+    yield
+
+
+def prefill_gates(case, mapped=True, seq=None):
+    """Parity, then the page-map gate both ways; returns the identity-pool output."""
+    from gpu_util import PrefillDev, check_parity, first_difference
+    d = PrefillDev(case, seq)
+    a = d.result()
+    check_parity(case, a, case.name)
+    if mapped:
+        for fold in (False, True):
+            m = wl.with_mapped_pool(case, fold_into_table=fold)
+            am = PrefillDev(m, seq).result()
+            assert np.array_equal(am, a), f"page map (fold={fold}) differs: " + first_difference(am, a)
+    return a, d
+
+
+@pytest.mark.parametrize("args", [(16, 8, 256, 1024, 1500, 5), (16, 2, 512, 0, 700, 1)],
+                         ids=["hd256_w1024_T1500", "hd512_w0_T700"])
+def test_page_prefill_cases(args):
+    nh, nkv, hd, window, ctx, rows = args
+    prefill_gates(wl.prefill_case(nh, nkv, hd, window, ctx, decode_rows=rows))
+
+
+@pytest.mark.parametrize("hd", [64, 128, 256, 512])
+@pytest.mark.parametrize("nh,nkv", [(4, 4), (8, 1), (32, 2), (24, 2), (6, 2)])
+def test_head_dims_and_group_sizes(hd, nh, nkv):
+    """g = 1, 8, 16, 12 and 3: chunks of 64 query rows cut rows' heads apart for g = 3 and 12."""
+    c = wl.prefill_case(nh, nkv, hd, 0, 150, dist="sym", seed=hd + nh)
+    prefill_gates(c, mapped=False)
+
+
+@pytest.mark.parametrize("window", [1, 5, 17, 100, 5000])
+def test_windows(window):
+    c = wl.prefill_case(16, 4, 128, window, 300, dist="sym", seed=window)
+    prefill_gates(c)
+
+
+def multi_sequence_case(seed=41, nh=16, nkv=4, hd=128, window=0):
+    """Three sequences in one call, each with its own span of a permuted block table:
+    a 70-row prompt, a 1-row prompt, and a 50-row continuation at positions 80..129
+    whose first 80 positions are already in the cache (chunked prefill)."""
+    rng = wl.Lcg(seed)
+    npages = 40
+    n = npages * nkv * 16 * hd
+    k = wl.draw_bf16(rng, n, "sym")
+    v = wl.draw_bf16(rng, n, "sym")
+    perm = wl.lcg_permutation(npages, seed + 1)
+    bt = np.concatenate([perm[:5], perm[5:6], perm[6:15]]).astype(np.int32)
+    lens = [(0, 70, 0), (5, 1, 0), (6, 50, 80)]          # (off, rows, first position)
+    off = np.concatenate([np.full(r, o, np.int32) for o, r, _ in lens])
+    qpos = np.concatenate([np.arange(p0, p0 + r, dtype=np.int32) for _, r, p0 in lens])
+    rows = len(qpos)
+    q = wl.draw_bf16(rng, rows * nh * hd, "sym")
+    return wl.Case("prefill_multiseq", nh, nkv, hd, window, rows, q, k, v, bt, off, qpos, ctx=130, npg=npages)
+
+
+@pytest.mark.parametrize("window", [0, 33])
+def test_several_sequences_and_a_continuation(window):
+    prefill_gates(multi_sequence_case(window=window), mapped=False)
+
+
+def test_kvpos_below_qpos_and_an_empty_row():
+    """Rows that see only up to kvpos < qpos, and one row whose window holds nothing."""
+    c = wl.prefill_case(8, 2, 256, 20, 90, dist="sym", seed=5)
+    kvpos = c.qpos.copy()
+    kvpos[10:40] -= 3
+    kvpos[50] = c.qpos[50] - 25         # below lo = qpos - 19: nothing visible
+    c = dataclasses.replace(c, kvpos=kvpos)
+    a, _ = prefill_gates(c, mapped=False)
+    assert np.all(a[50] == 0), "a row with no visible position must be zero"
+
+
+def test_nan_outside_the_union_window_never_reaches_output():
+    """Slots before the first row's window and after the last row's position hold NaN."""
+    from gpu_util import PrefillDev, first_difference
+    c = wl.prefill_case(16, 8, 256, 64, 200, dist="sym", seed=3)
+    rows = 150                        # positions 0..149 of a 200-token cache, window 64
+    c = dataclasses.replace(c, rows=rows, q=c.q[:rows * c.nh * c.hd], qpos=c.qpos[:rows], off=c.off[:rows])
+    clean = PrefillDev(c).result()
+    pk = c.k_pool.copy().reshape(c.npg, c.nkv, 16, c.hd)
+    pv = c.v_pool.copy().reshape(c.npg, c.nkv, 16, c.hd)
+    for pos in range(c.npg * 16):
+        if pos > rows - 1:
+            pk[pos // 16, :, pos % 16, :] = wl.BF16_NAN
+            pv[pos // 16, :, pos % 16, :] = wl.BF16_NAN
+    poisoned = dataclasses.replace(c, k_pool=pk.reshape(-1), v_pool=pv.reshape(-1))
+    got = PrefillDev(poisoned).result()
+    assert np.array_equal(got, clean), first_difference(got, clean)
+    # and tiles late in the sequence never read before their window: poison early slots too
+    late = dataclasses.replace(c, rows=20, q=c.q[130 * c.nh * c.hd:150 * c.nh * c.hd], qpos=c.qpos[130:150],
+                               off=c.off[130:150])
+    clean_late = PrefillDev(late).result()
+    pk2, pv2 = pk.copy(), pv.copy()
+    for pos in range(0, 130 + 1 - 64):
+        pk2[pos // 16, :, pos % 16, :] = wl.BF16_NAN
+        pv2[pos // 16, :, pos % 16, :] = wl.BF16_NAN
+    got_late = PrefillDev(dataclasses.replace(late, k_pool=pk2.reshape(-1), v_pool=pv2.reshape(-1))).result()
+    assert np.array_equal(got_late, clean_late), first_difference(got_late, clean_late)
+
+
+def test_prefill_rows_match_decode_rows():
+    """Decode-equals-prefill: the last rows of a prefill, decoded on their own, agree
+    within the gate (the two kernels reduce in different orders, so not bit for bit)."""
+    from gpu_util import DevCase, PrefillDev
+    import oracle
+    c = wl.prefill_case(16, 4, 256, 0, 400, dist="sym", seed=9)
+    pre = PrefillDev(c).result()
+    tail = 8
+    dec_case = dataclasses.replace(c, rows=tail, q=c.q[(400 - tail) * c.nh * c.hd:], qpos=c.qpos[-tail:],
+                                   off=c.off[-tail:])
+    dec = DevCase(dec_case, 4).result(counters=True)
+    assert oracle.rel_rms(pre[-tail:], dec) < 1e-2
+    assert oracle.rel_rms(dec, pre[-tail:]) < 1e-2
+
+
+def test_tile_longer_than_rows_per_tile_is_reported_and_skipped():
+    import torch
+    import paged_gqa_decode_attn_gb300 as pgqa
+    from gpu_util import PrefillDev
+    c = wl.prefill_case(8, 2, 128, 0, 100, dist="sym", seed=2)
+    d = PrefillDev(c)
+    pgqa.device_status()
+    rpt = pgqa.prefill_rows_per_tile(128)
+    d.t0 = torch.tensor([0, rpt + 1], dtype=torch.int32, device="cuda")
+    d.tn = torch.tensor([rpt + 1, 100 - rpt - 1], dtype=torch.int32, device="cuda")
+    d.ntiles = 2
+    out = d.result(fill=0x5555)
+    with pytest.raises(pgqa.PgqaError) as ei:
+        pgqa.device_status()
+    assert ei.value.status == pgqa._lib.PGQA_ERR_TILE_TOO_LONG
+    assert np.all(out[:rpt + 1] == 0x5555), "the over-long tile must be skipped"
+    assert not np.all(out[rpt + 1:] == 0x5555)
+    pgqa.device_status()
+
+
+def test_repeated_calls_and_streams_are_deterministic():
+    import torch
+    from gpu_util import PrefillDev
+    c = wl.prefill_case(32, 4, 512, 0, 130, dist="sym", seed=8)
+    d = PrefillDev(c)
+    first = d.result()
+    for _ in range(3):
+        assert np.array_equal(d.result(), first)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        o = d.run(stream=s)
+    s.synchronize()
+    assert np.array_equal(o.cpu().numpy().view(np.uint16).reshape(first.shape), first)
+
+
+def test_zero_tiles_is_a_no_op():
+    import torch
+    import paged_gqa_decode_attn_gb300 as pgqa
+    x = torch.zeros(16, dtype=torch.int16, device="cuda")
+    pgqa.attn_prefill(x, x, x, x, x, x, x, None, x, x, 0, 8, 2, 128, 0)
+    torch.cuda.synchronize()
+    assert int(x.abs().sum().item()) == 0
