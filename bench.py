@@ -95,6 +95,16 @@ def measured_peaks():
         return 6800.0, "fallback"
 
 
+def measured_bf16_peak():
+    """Dense bf16 tensor peak (TFLOP/s, burst: a kernel timed alone)."""
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["bf16_tflops"]), "measured"
+    except Exception:
+        return 1900.0, "fallback"
+
+
 def kernel_sources_sha() -> str:
     h = hashlib.sha256()
     for rel in KERNEL_SOURCES:
@@ -180,7 +190,18 @@ def build_case(name: str):
         return wl.long_ctx()
     if name == "batched":
         return wl.batched()
+    if name == "prefill_page":
+        return wl.prefill_page()
+    if name == "prefill_long":
+        return wl.prefill_long()
     raise SystemExit(f"unknown workload {name}")
+
+
+def prefill_flops(case) -> int:
+    """Algorithmic FLOPs of one prefill call: 4 nh hd per (row, visible position)."""
+    hi = case.qpos if case.kvpos is None else np.minimum(case.qpos, case.kvpos)
+    lo = np.maximum(0, case.qpos + 1 - case.window) if case.window > 0 else np.zeros_like(case.qpos)
+    return int(np.maximum(0, hi.astype(np.int64) - lo + 1).sum()) * 4 * case.nh * case.hd
 
 
 def nseq_of(case) -> int:
@@ -236,14 +257,18 @@ def oracle_rate(case, budget_s: float, steps: int | None = None, warmup: int = 0
 
 def run_reference(args, case, rank, world):
     gbs, per, sample, cores, k = oracle_rate(case, budget_s=args.ref_budget, steps=args.steps, warmup=args.warmup)
+    metric, unit = METRIC, "GB/s"
+    if args.workload.startswith("prefill"):
+        metric, unit = "paged causal prefill attention TFLOP/s", "TFLOP/s"
+        gbs = prefill_flops(case) * k / (case.rows * case.nh) / per / 1e12
     line = {
-        "impl": "reference", "metric": METRIC, "value": round(gbs, 4), "unit": "GB/s", "n_gpus": args.gpus,
+        "impl": "reference", "metric": metric, "value": round(gbs, 6), "unit": unit, "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": per * 1e3, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": config_of(args, case, None),
-        "cpu_baseline": {"value": round(gbs, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
+        "cpu_baseline": {"value": round(gbs, 6), "unit": unit, "cores": cores, "kind": "oracle",
                          "sample": sample},
-        "e2e": {"value": round(gbs, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "e2e": {"value": round(gbs, 6), "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
         "gpu_launches": 0,
     }
     print(json.dumps(line), flush=True)
@@ -432,6 +457,132 @@ def run_ours(args, case, rank, world, dist):
     return 0
 
 
+def run_prefill(args, case, rank, world, dist):
+    """One step = one pgqa_attn_prefill call over every row of the case (a NEXT-row
+    workload, not the default line): TFLOP/s against the bf16 tensor peak."""
+    import torch
+    import paged_gqa_decode_attn_gb300 as pgqa
+
+    torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
+    dev = torch.device("cuda")
+    if rank == 0:
+        pgqa.build()
+    barrier(dist)
+    pgqa.load()
+    flops = prefill_flops(case)
+    pool_bytes = case.k_pool.nbytes + case.v_pool.nbytes
+    copies = args.copies or max(2, math.ceil(3 * L2_BYTES / pool_bytes))
+    t0_h, tn_h = pgqa.make_tiles(case.off, pgqa.prefill_rows_per_tile(case.hd))
+    ntiles = len(t0_h)
+
+    def i16(a):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16))
+
+    ks = [i16(case.k_pool).to(dev) for _ in range(copies)]
+    vs = [i16(case.v_pool).to(dev) for _ in range(copies)]
+    parts = [np.ascontiguousarray(a).view(np.uint8) for a in
+             (case.q, np.asarray(case.qpos, np.int32), np.asarray(case.off, np.int32),
+              np.asarray(case.block_table, np.int32), t0_h, tn_h)]
+    offs, pos = [], 0
+    for a in parts:
+        offs.append(pos)
+        pos += (a.size + 255) // 256 * 256
+    host_in = torch.zeros(pos, dtype=torch.uint8).pin_memory()
+    for a, o0 in zip(parts, offs):
+        host_in[o0:o0 + a.size] = torch.from_numpy(a)
+    dev_in = host_in.to(dev)
+    views = [dev_in[o0:o0 + a.size] for a, o0 in zip(parts, offs)]
+    q = views[0].view(torch.int16)
+    qpos, off, bt, t0, tn = (v.view(torch.int32) for v in views[1:])
+    o = torch.empty(case.rows * case.nh * case.hd, dtype=torch.int16, device=dev)
+    o_h = torch.empty_like(o, device="cpu").pin_memory()
+
+    def call(i, stream=None):
+        pgqa.attn_prefill(o, q, ks[i % copies], vs[i % copies], bt, off, qpos, None, t0, tn, ntiles, case.nh,
+                          case.nkv, case.hd, case.window, None, stream)
+
+    call(0)
+    torch.cuda.synchronize()
+    spot = None
+    if rank == 0 and not args.no_check:
+        import oracle
+        got = o.cpu().numpy().view(np.uint16).reshape(case.rows, case.nh, case.hd)
+        pairs = [(r, h) for r in range(case.rows) for h in range(case.nh)][:: max(1, case.rows * case.nh // 64)]
+        _, ref = oracle.decode_case(case, pairs=pairs, want_f64=False)
+        spot = oracle.rel_rms(np.stack([got[r, h] for r, h in pairs]), ref)
+        if not spot < 1e-2:
+            raise SystemExit(f"spot check against the oracle failed: rel_rms {spot}")
+    sampler = ClockSampler(torch.cuda.current_device()) if not args.no_clocks else None
+    for i in range(args.warmup):
+        call(i)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for i in range(args.steps):
+            call(i)
+    g.replay()
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(dist)
+    torch.cuda.synchronize()
+    ev0.record(stream)
+    g.replay()
+    ev1.record(stream)
+    ev1.synchronize()
+    barrier(dist)
+    el_ms = ev0.elapsed_time(ev1)
+    clocks = sampler.stop() if sampler else None
+    el_max = max_over_ranks(dist, el_ms)
+    value = sum_over_ranks(dist, float(flops) * args.steps) / (el_max * 1e-3) / 1e12
+    kernel_us = el_ms * 1e3 / args.steps
+
+    e2e_steps = max(1, min(args.steps, args.e2e_steps))
+    barrier(dist)
+    torch.cuda.synchronize()
+    t_0 = time.perf_counter()
+    for i in range(e2e_steps):
+        dev_in.copy_(host_in, non_blocking=True)
+        call(i)
+        o_h.copy_(o, non_blocking=True)
+    torch.cuda.synchronize()
+    e2e_s = max_over_ranks(dist, time.perf_counter() - t_0)
+    e2e_value = sum_over_ranks(dist, float(flops) * e2e_steps) / e2e_s / 1e12
+    if rank != 0:
+        return 0
+    peak, peak_kind = measured_bf16_peak()
+    achieved = flops / (kernel_us * 1e-6) / 1e12
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        gbs, per, sample, cores, k = oracle_rate(case, budget_s=args.cpu_budget, steps=1)
+        tflops_cpu = flops * k / (case.rows * case.nh) / per / 1e12
+        cpu = {"value": round(tflops_cpu, 6), "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+               "sample": sample}
+    cfg = {"workload": case.name, "nh": case.nh, "nkv": case.nkv, "hd": case.hd, "ctx": case.ctx,
+           "rows": case.rows, "window": case.window, "tiles": ntiles,
+           "rows_per_tile": pgqa.prefill_rows_per_tile(case.hd), "flops_per_call": flops,
+           "l2": f"rotating {copies} pool copies ({copies * pool_bytes / 1e9:.2f} GB > 3x L2)",
+           "timing": f"CUDA events around one CUDA graph of {args.steps} back-to-back calls"}
+    if spot is not None:
+        cfg["spot_check_rel_rms"] = spot
+    line = {
+        "metric": "paged causal prefill attention TFLOP/s", "value": round(value, 2), "unit": "TFLOP/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": el_max / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": cfg,
+        "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak, "unit": "TFLOP/s",
+                     "frac": round(achieved / peak, 4), "traffic": None, "peak_kind": peak_kind,
+                     "kernel": "prefill_kernel", "launch_us": round(kernel_us, 3)},
+        "cpu_baseline": cpu,
+        "e2e": {"value": round(e2e_value, 2), "unit": "TFLOP/s", "h2d_bytes_per_step": host_in.numel(),
+                "d2h_bytes_per_step": o_h.numel() * o_h.element_size(), "steps": e2e_steps,
+                "us_per_step": round(e2e_s / e2e_steps * 1e6, 3)},
+        "gpu_launches": args.steps, "clocks": clocks,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
@@ -439,7 +590,7 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="sliding",
-                    choices=["sliding", "sliding_mapped", "tiny", "long", "batched"])
+                    choices=["sliding", "sliding_mapped", "tiny", "long", "batched", "prefill_page", "prefill_long"])
     ap.add_argument("--splits", type=int, default=0, help="override choose_splits")
     ap.add_argument("--merge", choices=["counters", "combine"], default="counters")
     ap.add_argument("--graph-chunk", type=int, default=2000)
@@ -461,6 +612,8 @@ def main(argv=None):
         return run_reference(args, case, rank, world)
     dist = init_dist(world)
     try:
+        if args.workload.startswith("prefill"):
+            return run_prefill(args, case, rank, world, dist)
         return run_ours(args, case, rank, world, dist)
     finally:
         if dist is not None:
