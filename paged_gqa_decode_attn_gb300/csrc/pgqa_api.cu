@@ -122,16 +122,17 @@ int get_encoder()
 struct MapCacheEntry {
     const void *base = nullptr;
     int hd = 0;
+    bool chunked = false;    // built as hd/64 boxes per tile on request (the tcgen05 prefill)
     int whole = 0;
     CUtensorMap map;
 };
 MapCacheEntry g_map_cache[128];
 unsigned g_map_next = 0;
 
-int pool_map(const void *base, int hd, CUtensorMap *out, int *whole)
+int pool_map(const void *base, int hd, CUtensorMap *out, int *whole, bool chunked = false)
 {
     for (auto &e : g_map_cache)
-        if (e.base == base && e.hd == hd) {
+        if (e.base == base && e.hd == hd && e.chunked == chunked) {
             *out = e.map;
             *whole = e.whole;
             return PGQA_OK;
@@ -140,8 +141,8 @@ int pool_map(const void *base, int hd, CUtensorMap *out, int *whole)
     if (st != PGQA_OK)
         return st;
     CUtensorMap m;
-    int w = 1;
-    {
+    int w = chunked ? 0 : 1;
+    if (w) {
         const cuuint64_t dims[4] = {64u, 16u, static_cast<cuuint64_t>(hd / 64), 0x7fffffffull};
         const cuuint64_t strides[3] = {static_cast<cuuint64_t>(hd) * 2u, 128u, static_cast<cuuint64_t>(hd) * 32u};
         const cuuint32_t box[4] = {64u, 16u, static_cast<cuuint32_t>(hd / 64), 1u};
@@ -166,6 +167,7 @@ int pool_map(const void *base, int hd, CUtensorMap *out, int *whole)
     MapCacheEntry &e = g_map_cache[g_map_next++ % 128];
     e.base = base;
     e.hd = hd;
+    e.chunked = chunked;
     e.whole = w;
     e.map = m;
     *out = m;
@@ -501,7 +503,7 @@ int pgqa_attn_prefill(void *o, const void *q, const void *k_pool, const void *v_
         return PGQA_ERR_INVALID_ARGUMENT;
     const int g = nh / nkv;
     const int rpt = pgqa_prefill_rows_per_tile(hd);
-    const int qr = hd == 512 ? pgqa::PfGeo<512>::kQueryRows : pgqa::PfGeo<64>::kQueryRows;
+    const int qr = hd == 512 ? pgqa::PfGeo<512>::kQueryRows : 128;     // query rows per CTA
     if (nkv > 65535 || (static_cast<long long>(rpt) * g + qr - 1) / qr > 65535)
         return PGQA_ERR_INVALID_ARGUMENT;
     if (!aligned(k_pool, 16) || !aligned(v_pool, 16) || !aligned(q, 16) || !aligned(o, 16))
@@ -533,7 +535,9 @@ int pgqa_attn_prefill(void *o, const void *q, const void *k_pool, const void *v_
         return st;
     CUtensorMap tk, tv;
     int whole_k = 0, whole_v = 0;
-    if ((st = pool_map(k_pool, hd, &tk, &whole_k)) != PGQA_OK || (st = pool_map(v_pool, hd, &tv, &whole_v)) != PGQA_OK)
+    const bool chunked = hd <= 256;      // the tcgen05 kernel places each 64-dim box itself
+    if ((st = pool_map(k_pool, hd, &tk, &whole_k, chunked)) != PGQA_OK ||
+        (st = pool_map(v_pool, hd, &tv, &whole_v, chunked)) != PGQA_OK)
         return st;
     if (whole_k != whole_v)
         return PGQA_ERR_TENSOR_MAP;

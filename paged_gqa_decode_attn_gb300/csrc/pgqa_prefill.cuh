@@ -24,14 +24,18 @@ namespace pgqa {
 
 constexpr unsigned int kErrTileRows = 8u;    // a tile longer than rows_per_tile
 
+// Rows per tile: 128 where the tcgen05 kernel (pgqa_prefill_tc.cuh, M = 128
+// query rows) serves the head dim, 32 at hd 512 where this file's mma.sync
+// kernel does.
+
 template <int HD>
 struct PfCfg;
 template <>
-struct PfCfg<64> { static constexpr int kWpg = 1, kBlocks = 4, kStages = 8, kRowsPerTile = 64; };
+struct PfCfg<64> { static constexpr int kWpg = 1, kBlocks = 4, kStages = 8, kRowsPerTile = 128; };
 template <>
-struct PfCfg<128> { static constexpr int kWpg = 1, kBlocks = 4, kStages = 8, kRowsPerTile = 64; };
+struct PfCfg<128> { static constexpr int kWpg = 1, kBlocks = 4, kStages = 8, kRowsPerTile = 128; };
 template <>
-struct PfCfg<256> { static constexpr int kWpg = 2, kBlocks = 4, kStages = 8, kRowsPerTile = 64; };
+struct PfCfg<256> { static constexpr int kWpg = 2, kBlocks = 4, kStages = 8, kRowsPerTile = 128; };
 template <>
 struct PfCfg<512> { static constexpr int kWpg = 4, kBlocks = 2, kStages = 4, kRowsPerTile = 32; };
 

@@ -1,6 +1,6 @@
-// Paged prefill kernel instantiated for head dimension 256.
-#include "pgqa_prefill.cuh"
+// Paged prefill for head dimension 256: the tcgen05 kernel.
+#include "pgqa_prefill_tc.cuh"
 
 namespace pgqa {
-cudaError_t launch_prefill_hd256(const PrefillLaunchArgs &a, bool set_attr) { return launch_prefill<256>(a, set_attr); }
+cudaError_t launch_prefill_hd256(const PrefillLaunchArgs &a, bool set_attr) { return launch_prefill_tc<256>(a, set_attr); }
 }  // namespace pgqa

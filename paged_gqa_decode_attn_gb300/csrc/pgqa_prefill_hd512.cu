@@ -1,4 +1,5 @@
-// Paged prefill kernel instantiated for head dimension 512.
+// Paged prefill for head dimension 512: the mma.sync kernel (O of 128 rows x 512 dims would fill
+// all of tensor memory).
 #include "pgqa_prefill.cuh"
 
 namespace pgqa {

@@ -1,0 +1,483 @@
+// Paged causal prefill on the 5th-generation tensor cores (tcgen05) of GB300,
+// for head dims 64, 128 and 256.  Same result as pgqa_prefill.cuh's kernel
+// (the page's `attn::attn_prefill`: every tile row attends like a decode row
+// at its position), computed as a flash-attention loop with the accumulators
+// in tensor memory:
+//
+//   * one CTA serves 128 query rows (row, head) of one tile and kv head --
+//     the M = 128 of every MMA -- with heads fastest;
+//   * warp 4 streams the chunk's union window in blocks of 4 pages (64
+//     tokens) by TMA: K into a [hd/64][64 tokens][128 B] tile (one N = 64 MMA
+//     per 16 dims), V as 4 page tiles [hd/64][16 tokens][128 B];
+//   * warp 5 issues S_j = Q K_j^T into one of two TMEM buffers (64 columns
+//     each), then O += P_{j-1} V_{j-1} (TMEM, hd columns), one tcgen05.mma per
+//     16 dims or 16 tokens, each batch committed to an mbarrier;
+//   * warps 0-3 own one query row per thread (TMEM lane = row): they read
+//     S_j from TMEM, mask it to the row's window, run the online softmax in
+//     log2 units, rescale O in TMEM only when a row's running max grows by
+//     more than 2^8 (exact in real arithmetic: P then stays below 256), write
+//     P_j as bf16 into shared memory (the A operand of the PV MMA), and at
+//     the end divide O by the row sum and store bf16.
+//
+// Every wait is bounded; a thread that gives up skips its later waits and
+// every role still reaches the final barrier, which frees the tensor memory.
+#pragma once
+
+#include "pgqa_prefill.cuh"
+
+namespace pgqa {
+
+// ---------------------------------------------------------------- tcgen05 helpers
+
+// Shared-memory matrix descriptor: start address, leading and stride byte
+// offsets, the fixed 0b001 at bits 46-48, 128-byte swizzle (mode 2, bits 61-63).
+__device__ __forceinline__ uint64_t umma_sdesc(uint32_t addr, uint32_t lbo, uint32_t sbo)
+{
+    uint64_t d = static_cast<uint64_t>((addr & 0x3FFFFu) >> 4);
+    d |= static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16;
+    d |= static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32;
+    d |= static_cast<uint64_t>(1) << 46;
+    d |= static_cast<uint64_t>(2) << 61;
+    return d;
+}
+
+// Instruction descriptor of kind::f16: f32 accumulate, bf16 A and B, A / B
+// K-major (0) or MN-major (1), N >> 3 at bits 17-22, M >> 4 at bits 24-28.
+__host__ __device__ constexpr uint32_t umma_idesc_bf16(int m, int n, int a_mn, int b_mn)
+{
+    return (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(a_mn) << 15) |
+           (static_cast<uint32_t>(b_mn) << 16) | (static_cast<uint32_t>(n >> 3) << 17) |
+           (static_cast<uint32_t>(m >> 4) << 24);
+}
+
+__device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a), "l"(b), "r"(idesc), "r"(acc)
+        : "memory");
+}
+
+// Arrive once on `bar` when every tcgen05.mma this thread issued so far is complete.
+__device__ __forceinline__ void umma_commit(uint32_t bar)
+{
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+template <int kCols>
+__device__ __forceinline__ void tmem_alloc(uint32_t slot)
+{
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(slot), "n"(kCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+
+template <int kCols>
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr)
+{
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "n"(kCols) : "memory");
+}
+
+// 32 lanes x 16 consecutive 32-bit columns: thread t gets lane (warp's base + t).
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16])
+{
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr)
+        : "memory");
+}
+
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16])
+{
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(
+            taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
+        "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+        : "memory");
+}
+
+__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+__device__ __forceinline__ void fence_async_shared() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
+// ---------------------------------------------------------------- geometry
+
+template <int HD>
+struct TcGeo {
+    static constexpr int kRows = 128;                  // query rows per CTA (MMA M)
+    static constexpr int kBlockPages = 4;
+    static constexpr int kBlockTokens = kBlockPages * kPage;   // 64: S columns per block
+    static constexpr int kChunks = HD / 64;            // 128-byte swizzle rows per head vector
+    static constexpr int kQBytes = kChunks * kRows * 128;      // [chunk][128 rows][128 B]
+    static constexpr int kPBytes = kRows * 128;                // [128 rows][64 tokens]
+    static constexpr int kKBytes = kChunks * kBlockTokens * 128;           // [chunk][64 tokens][128 B]
+    static constexpr int kVPage = kChunks * kPage * 128;                   // [chunk][16 tokens][128 B]
+    static constexpr int kVBytes = kBlockPages * kVPage;
+    static constexpr int kStageBytes = kKBytes + kVBytes;
+    static constexpr int kStages = HD == 256 ? 2 : HD == 128 ? 4 : 8;
+    static constexpr int kQOff = 0;
+    static constexpr int kPOff = kQBytes;
+    static constexpr int kStageOff = kPOff + kPBytes;
+    static constexpr int kBarOff = kStageOff + kStages * kStageBytes;
+    // full[stages], empty[stages], s_full[2], s_free[2], p_full, o_done
+    static constexpr int kBars = 2 * kStages + 6;
+    static constexpr int kSlotOff = kBarOff + kBars * 8;
+    static constexpr int kTotal = kSlotOff + 16;
+    static constexpr int kAlloc = kTotal + 1024;
+    static constexpr int kThreads = 192;               // 4 softmax warps, producer, MMA issuer
+    static constexpr int kTmemCols = HD == 256 ? 512 : 256;   // S0, S1 (64 each), O (hd)
+    static constexpr int kOCol = 2 * kBlockTokens;
+    static_assert(kOCol + HD <= kTmemCols, "tensor memory");
+    static_assert(kAlloc <= 227 * 1024, "shared memory");
+    static_assert(kQBytes % 1024 == 0 && kPBytes % 1024 == 0 && kStageBytes % 1024 == 0, "swizzle atoms");
+};
+
+template <int HD>
+__global__ void __launch_bounds__(TcGeo<HD>::kThreads, 1)
+    prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                      const PrefillParams p)
+{
+    using G = TcGeo<HD>;
+    constexpr int NST = G::kStages;
+    constexpr int NCH = G::kChunks;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t s_base = smem_u32(smem);
+    const uint32_t sQ = s_base + G::kQOff;
+    const uint32_t sP = s_base + G::kPOff;
+    const uint32_t s_bar = s_base + G::kBarOff;
+    const uint32_t b_full = s_bar;                     // [NST]
+    const uint32_t b_empty = s_bar + 8 * NST;          // [NST]
+    const uint32_t b_sfull = s_bar + 16 * NST;         // [2]
+    const uint32_t b_sfree = b_sfull + 16;             // [2]
+    const uint32_t b_pfull = b_sfree + 16;
+    const uint32_t b_odone = b_pfull + 8;
+    uint32_t *tslot = reinterpret_cast<uint32_t *>(smem + G::kSlotOff);
+
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5;
+    const int lane = tid & 31;
+    const int tile = blockIdx.x;
+    const int kh = blockIdx.y;
+    const int chunk = blockIdx.z;
+
+    if (tid == 0) {
+        for (int s = 0; s < NST; ++s) {
+            mbar_init(b_full + 8 * s, 1);
+            mbar_init(b_empty + 8 * s, 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(b_sfull + 8 * b, 1);
+            mbar_init(b_sfree + 8 * b, 4);
+        }
+        mbar_init(b_pfull, 4);
+        mbar_init(b_odone, 1);
+        mbar_init_fence();
+    }
+    grid_dependency_wait();
+    grid_launch_dependents();
+
+    const int t0 = __ldg(p.tile_t0 + tile);
+    const int tn = __ldg(p.tile_tn + tile);
+    if (tn > p.rows_per_tile) {
+        if (tid == 0)
+            atomicOr(p.err, kErrTileRows);
+        return;
+    }
+    const int g = p.g;
+    const int nqr = tn * g;
+    const int qbase = chunk * G::kRows;
+    if (tn <= 0 || qbase >= nqr)
+        return;
+
+    // ---- union window of the served rows (positions pr_first..pr_last)
+    const int pr_first = qbase / g;
+    const int pr_last = min(tn - 1, (qbase + G::kRows - 1) / g);
+    int lo_m = INT_MAX, hi_m = INT_MIN;
+    for (int pr = pr_first + lane; pr <= pr_last; pr += 32) {
+        int lo, hi;
+        prefill_window(p, t0 + pr, lo, hi);
+        if (hi >= lo) {
+            lo_m = min(lo_m, lo);
+            hi_m = max(hi_m, hi);
+        }
+    }
+#pragma unroll
+    for (int k = 16; k; k >>= 1) {
+        lo_m = min(lo_m, __shfl_xor_sync(0xffffffffu, lo_m, k));
+        hi_m = max(hi_m, __shfl_xor_sync(0xffffffffu, hi_m, k));
+    }
+    int lo_u = 0, hi_u = -1;
+    if (hi_m != INT_MIN) {
+        lo_u = lo_m;
+        hi_u = hi_m;
+    }
+    const int p_first = lo_u >> 4;
+    const int npages = hi_u >= lo_u ? (hi_u >> 4) - p_first + 1 : 0;
+    const int nblocks = (npages + G::kBlockPages - 1) / G::kBlockPages;
+    const int off0 = __ldg(p.off + t0);
+
+    // ---- query row of this thread (warps 0-3) and its Q into shared memory
+    bool va = false;
+    int lo_a = 1, hi_a = 0;
+    size_t rh = 0;
+    if (warp < 4) {
+        const int qr = qbase + tid;
+        if (qr < nqr) {
+            const int pr = qr / g, h = qr - pr * g;
+            prefill_window(p, t0 + pr, lo_a, hi_a);
+            rh = static_cast<size_t>(t0 + pr) * p.nh + kh * g + h;
+            va = true;
+        }
+        const uint4 *src = reinterpret_cast<const uint4 *>(p.q + rh * HD);
+#pragma unroll 4
+        for (int u = 0; u < HD / 8; ++u) {
+            const uint4 v = va ? __ldg(src + u) : make_uint4(0u, 0u, 0u, 0u);
+            const int c = u >> 3, w = u & 7;
+            *reinterpret_cast<uint4 *>(smem + G::kQOff + c * (G::kRows * 128) + tid * 128 + ((w ^ (tid & 7)) << 4)) =
+                v;
+        }
+        fence_async_shared();          // Q (generic stores) -> read by the tensor core
+    }
+    if (warp == 0)
+        tmem_alloc<G::kTmemCols>(smem_u32(tslot));
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tbase = *tslot;
+
+    if (warp == 4) {
+        // ------------------------------------------------ producer: blocks of 4 pages
+        if (lane == 0) {
+            tma_prefetch_map(&tm_k);
+            tma_prefetch_map(&tm_v);
+        }
+        const int32_t *tbl = p.block_table + off0 + p_first;
+        bool ok = true;
+        for (int j = 0; j < nblocks; ++j) {
+            const int np = min(G::kBlockPages, npages - j * G::kBlockPages);
+            int phys = 0;
+            if (lane < np) {
+                phys = __ldg(tbl + j * G::kBlockPages + lane);
+                if (p.page_map)
+                    phys = __ldg(p.page_map + phys);
+            }
+            const int st = j % NST;
+            if (lane == 0 && ok && j >= NST)
+                ok = mbar_wait_bounded(b_empty + 8 * st, ((j / NST) - 1) & 1, p.err, kErrTimeoutEmpty);
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            const uint32_t sK = s_base + G::kStageOff + st * G::kStageBytes;
+            const uint32_t sV = sK + G::kKBytes;
+            if (ok && lane == 0)
+                mbar_arrive_expect_tx(b_full + 8 * st, np * 2 * kPage * HD * 2);
+            for (int pp = 0; pp < np; ++pp) {
+                const int ph = __shfl_sync(0xffffffffu, phys, pp);
+                if (ok && lane == 0) {
+                    const int t = ph * p.nkv + kh;
+#pragma unroll
+                    for (int c = 0; c < NCH; ++c) {
+                        tma_load_3d(sK + c * (G::kBlockTokens * 128) + pp * (kPage * 128), &tm_k, b_full + 8 * st,
+                                    c * kBoxElems, 0, t);
+                        tma_load_3d(sV + pp * G::kVPage + c * (kPage * 128), &tm_v, b_full + 8 * st, c * kBoxElems,
+                                    0, t);
+                    }
+                }
+            }
+        }
+    } else if (warp == 5) {
+        // ------------------------------------------------ MMA issuer (one thread)
+        if (lane == 0) {
+            constexpr uint32_t kIdS = umma_idesc_bf16(128, G::kBlockTokens, 0, 0);
+            constexpr uint32_t kIdO = umma_idesc_bf16(128, HD, 0, 1);
+            bool ok = true;
+            for (int j = 0; j <= nblocks; ++j) {
+                if (j < nblocks) {
+                    const int st = j % NST, b = j & 1;
+                    if (ok)
+                        ok = mbar_wait_bounded(b_full + 8 * st, (j / NST) & 1, p.err, kErrTimeoutFull);
+                    if (ok && j >= 2)
+                        ok = mbar_wait_bounded(b_sfree + 8 * b, ((j - 2) >> 1) & 1, p.err, kErrTimeoutFull);
+                    tc_fence_after();
+                    if (ok) {
+                        const uint32_t sK = s_base + G::kStageOff + st * G::kStageBytes;
+#pragma unroll
+                        for (int ks = 0; ks < HD / 16; ++ks) {
+                            const int c = ks >> 2, kk = ks & 3;
+                            umma_bf16(tbase + b * G::kBlockTokens,
+                                      umma_sdesc(sQ + c * (G::kRows * 128) + kk * 32, 16, 1024),
+                                      umma_sdesc(sK + c * (G::kBlockTokens * 128) + kk * 32, 16, 1024), kIdS, ks > 0);
+                        }
+                    }
+                    umma_commit(b_sfull + 8 * b);
+                }
+                if (j >= 1) {
+                    const int jj = j - 1, st = jj % NST;
+                    if (ok)
+                        ok = mbar_wait_bounded(b_pfull, jj & 1, p.err, kErrTimeoutFull);
+                    tc_fence_after();
+                    if (ok) {
+                        const uint32_t sV = s_base + G::kStageOff + st * G::kStageBytes + G::kKBytes;
+                        const int np = min(G::kBlockPages, npages - jj * G::kBlockPages);
+                        for (int pp = 0; pp < np; ++pp)
+                            umma_bf16(tbase + G::kOCol, umma_sdesc(sP + pp * 32, 16, 1024),
+                                      umma_sdesc(sV + pp * G::kVPage, kPage * 128, 1024), kIdO, jj > 0 || pp > 0);
+                    }
+                    umma_commit(b_odone);
+                    umma_commit(b_empty + 8 * st);
+                }
+            }
+        }
+    } else {
+        // ------------------------------------------------ softmax warps: thread = query row
+        const uint32_t trow = tbase + (static_cast<uint32_t>(warp * 32) << 16);
+        float m = -INFINITY, l = 0.f;
+        bool ok = true;
+        for (int j = 0; j < nblocks; ++j) {
+            const int b = j & 1;
+            if (ok)
+                ok = mbar_wait_bounded(b_sfull + 8 * b, (j >> 1) & 1, p.err, kErrTimeoutFull);
+            tc_fence_after();
+            uint32_t sr[G::kBlockTokens];
+#pragma unroll
+            for (int q4 = 0; q4 < G::kBlockTokens / 16; ++q4)
+                tmem_ld16(trow + b * G::kBlockTokens + q4 * 16, *reinterpret_cast<uint32_t(*)[16]>(sr + q4 * 16));
+            tmem_wait_ld();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(b_sfree + 8 * b);
+
+            const int tok0 = (p_first + j * G::kBlockPages) * kPage;
+            float x[G::kBlockTokens];
+            float mx = -INFINITY;
+#pragma unroll
+            for (int c = 0; c < G::kBlockTokens; ++c) {
+                const int t = tok0 + c;
+                x[c] = (t >= lo_a && t <= hi_a) ? __uint_as_float(sr[c]) * kLog2e : -INFINITY;
+                mx = fmaxf(mx, x[c]);
+            }
+            // stale-max rescale: keep m unless the block's max exceeds it by more than 8
+            float m_use = m, alpha = 1.f;
+            if (mx > m + 8.f || (m == -INFINITY && mx != -INFINITY)) {
+                m_use = mx;
+                alpha = (m == -INFINITY) ? 0.f : exp2f(m - mx);
+            }
+            float ls = 0.f;
+            uint32_t pk[G::kBlockTokens / 2];
+#pragma unroll
+            for (int c = 0; c < G::kBlockTokens; c += 2) {
+                const float p0 = m_use == -INFINITY ? 0.f : bf16_round(exp2f(x[c] - m_use));
+                const float p1 = m_use == -INFINITY ? 0.f : bf16_round(exp2f(x[c + 1] - m_use));
+                ls += p0 + p1;
+                pk[c / 2] = pack_bf16x2(p0, p1);
+            }
+            l = __fmaf_rn(l, alpha, ls);
+            m = m_use;
+
+            // O and the P buffer are free once the previous block's PV is done
+            if (j >= 1 && ok)
+                ok = mbar_wait_bounded(b_odone, (j - 1) & 1, p.err, kErrTimeoutFull);
+            tc_fence_after();
+            if (j >= 1 && __any_sync(0xffffffffu, alpha != 1.f)) {
+#pragma unroll 1
+                for (int c0 = 0; c0 < HD; c0 += 16) {
+                    uint32_t r[16];
+                    tmem_ld16(trow + G::kOCol + c0, r);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int k = 0; k < 16; ++k)
+                        r[k] = __float_as_uint(__uint_as_float(r[k]) * alpha);
+                    tmem_st16(trow + G::kOCol + c0, r);
+                }
+                tmem_wait_st();
+            }
+            // P row -> shared memory, 128-byte swizzle
+#pragma unroll
+            for (int w = 0; w < 8; ++w)
+                *reinterpret_cast<uint4 *>(smem + G::kPOff + tid * 128 + ((w ^ (tid & 7)) << 4)) =
+                    make_uint4(pk[4 * w], pk[4 * w + 1], pk[4 * w + 2], pk[4 * w + 3]);
+            // V rows of tokens outside the union window may hold anything (NaN
+            // included) and P is 0 there: zero them before the PV MMA reads them
+            if (tok0 < lo_u || tok0 + G::kBlockTokens - 1 > hi_u) {
+                const int st = j % NST;
+                uint8_t *sV = smem + G::kStageOff + st * G::kStageBytes + G::kKBytes;
+                const int np = min(G::kBlockPages, npages - j * G::kBlockPages);
+                for (int e = tid; e < np * kPage * NCH * 8; e += 128) {
+                    const int u = e & 7, rc = e >> 3;
+                    const int c = rc % NCH, tk = rc / NCH;     // token of the block, chunk
+                    const int t = tok0 + tk;
+                    if (t < lo_u || t > hi_u)
+                        *reinterpret_cast<uint4 *>(sV + (tk >> 4) * G::kVPage + c * (kPage * 128) + (tk & 15) * 128 +
+                                                   u * 16) = make_uint4(0u, 0u, 0u, 0u);
+                }
+            }
+            fence_async_shared();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(b_pfull);
+        }
+        // ---- finish: O / l in bf16
+        if (nblocks > 0 && ok)
+            ok = mbar_wait_bounded(b_odone, (nblocks - 1) & 1, p.err, kErrTimeoutFull);
+        tc_fence_after();
+#pragma unroll 1
+        for (int c0 = 0; c0 < HD; c0 += 16) {
+            uint32_t r[16];
+            tmem_ld16(trow + G::kOCol + c0, r);
+            tmem_wait_ld();
+            if (va) {
+                uint32_t w[8];
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    __nv_bfloat162 v;
+                    v.x = nblocks > 0 ? merge_finish(__uint_as_float(r[2 * k]), l) : __float2bfloat16_rn(0.f);
+                    v.y = nblocks > 0 ? merge_finish(__uint_as_float(r[2 * k + 1]), l) : __float2bfloat16_rn(0.f);
+                    w[k] = *reinterpret_cast<uint32_t *>(&v);
+                }
+                uint4 *dst = reinterpret_cast<uint4 *>(p.o + rh * HD + c0);
+                dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+                dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        tc_fence_after();
+        tmem_dealloc<G::kTmemCols>(tbase);
+    }
+}
+
+template <int HD>
+cudaError_t launch_prefill_tc(const PrefillLaunchArgs &a, bool set_attr)
+{
+    if (set_attr) {
+        cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             TcGeo<HD>::kAlloc);
+        if (e != cudaSuccess)
+            return e;
+    }
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(a.ntiles, a.p.nkv, (a.p.rows_per_tile * a.p.g + TcGeo<HD>::kRows - 1) / TcGeo<HD>::kRows);
+    cfg.blockDim = dim3(TcGeo<HD>::kThreads);
+    cfg.dynamicSmemBytes = TcGeo<HD>::kAlloc;
+    cfg.stream = a.stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, prefill_tc_kernel<HD>, *a.tm_k, *a.tm_v, a.p);
+}
+
+}  // namespace pgqa

@@ -140,7 +140,7 @@ def test_python_binding_raises_on_error(lib):
 # ---------------------------------------------------------------- prefill host side
 
 def test_prefill_rows_per_tile(lib):
-    assert [pgqa.prefill_rows_per_tile(h) for h in (64, 128, 256, 512)] == [64, 64, 64, 32]
+    assert [pgqa.prefill_rows_per_tile(h) for h in (64, 128, 256, 512)] == [128, 128, 128, 32]
     assert lib.pgqa_prefill_rows_per_tile(96) == -2
 
 

@@ -149,12 +149,13 @@ def test_tile_longer_than_rows_per_tile_is_reported_and_skipped():
     import torch
     import paged_gqa_decode_attn_gb300 as pgqa
     from gpu_util import PrefillDev
-    c = wl.prefill_case(8, 2, 128, 0, 100, dist="sym", seed=2)
+    rpt = pgqa.prefill_rows_per_tile(128)
+    rows = rpt + 1 + 40
+    c = wl.prefill_case(8, 2, 128, 0, rows, dist="sym", seed=2)
     d = PrefillDev(c)
     pgqa.device_status()
-    rpt = pgqa.prefill_rows_per_tile(128)
     d.t0 = torch.tensor([0, rpt + 1], dtype=torch.int32, device="cuda")
-    d.tn = torch.tensor([rpt + 1, 100 - rpt - 1], dtype=torch.int32, device="cuda")
+    d.tn = torch.tensor([rpt + 1, rows - rpt - 1], dtype=torch.int32, device="cuda")
     d.ntiles = 2
     out = d.result(fill=0x5555)
     with pytest.raises(pgqa.PgqaError) as ei:
