@@ -6,18 +6,22 @@
 //
 //   * one CTA serves 128 query rows (row, head) of one tile and kv head --
 //     the M = 128 of every MMA -- with heads fastest;
-//   * warp 4 streams the chunk's union window in blocks of 4 pages (64
-//     tokens) by TMA: K into a [hd/64][64 tokens][128 B] tile (one N = 64 MMA
-//     per 16 dims), V as 4 page tiles [hd/64][16 tokens][128 B];
-//   * warp 5 issues S_j = Q K_j^T into one of two TMEM buffers (64 columns
+//   * warp 8 streams the chunk's union window in blocks of 2 pages (32
+//     tokens) by TMA into a ring of 128 KB: K into a [hd/64][32 tokens][128 B]
+//     tile (one N = 32 MMA per 16 dims), V as 2 page tiles [hd/64][16 tokens]
+//     [128 B];
+//   * warp 9 issues S_j = Q K_j^T into one of two TMEM buffers (32 columns
 //     each), then O += P_{j-1} V_{j-1} (TMEM, hd columns), one tcgen05.mma per
 //     16 dims or 16 tokens, each batch committed to an mbarrier;
-//   * warps 0-3 own one query row per thread (TMEM lane = row): they read
-//     S_j from TMEM, mask it to the row's window, run the online softmax in
-//     log2 units, rescale O in TMEM only when a row's running max grows by
-//     more than 2^8 (exact in real arithmetic: P then stays below 256), write
-//     P_j as bf16 into shared memory (the A operand of the PV MMA), and at
-//     the end divide O by the row sum and store bf16.
+//   * warps 0-7 run the softmax, two threads per query row (warps w and w+4
+//     share TMEM lanes 32(w%4)..: lane = row), each over half of the block's
+//     columns: they read S_j from TMEM, mask it to the row's window, agree on
+//     the row max through shared memory, run the online softmax in log2
+//     units, rescale their half of O in TMEM only when the row's running max
+//     grows by more than 2^8 (exact in real arithmetic: P then stays below
+//     256), write their half of P_j as bf16 into shared memory (the A operand
+//     of the PV MMA), and at the end divide their half of O by the row sum and
+//     store bf16.
 //
 // Every wait is bounded; a thread that gives up skips its later waits and
 // every role still reaches the final barrier, which frees the tensor memory.
@@ -109,32 +113,43 @@ __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.
 
 __device__ __forceinline__ void fence_async_shared() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 
+// 2^x by the SFU's approximation (relative error about 2^-22; 2^-inf = +0):
+// one instruction per score, whose result is rounded to bf16 for P anyway.
+__device__ __forceinline__ float ex2_sfu(float x)
+{
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
 // ---------------------------------------------------------------- geometry
 
 template <int HD>
 struct TcGeo {
     static constexpr int kRows = 128;                  // query rows per CTA (MMA M)
-    static constexpr int kBlockPages = 4;
-    static constexpr int kBlockTokens = kBlockPages * kPage;   // 64: S columns per block
+    static constexpr int kBlockPages = 2;
+    static constexpr int kBlockTokens = kBlockPages * kPage;   // 32: S columns per block
     static constexpr int kChunks = HD / 64;            // 128-byte swizzle rows per head vector
     static constexpr int kQBytes = kChunks * kRows * 128;      // [chunk][128 rows][128 B]
-    static constexpr int kPBytes = kRows * 128;                // [128 rows][64 tokens]
-    static constexpr int kKBytes = kChunks * kBlockTokens * 128;           // [chunk][64 tokens][128 B]
+    static constexpr int kPBytes = kRows * 128;                // [128 rows][128 B: 32 tokens used]
+    static constexpr int kKBytes = kChunks * kBlockTokens * 128;           // [chunk][32 tokens][128 B]
     static constexpr int kVPage = kChunks * kPage * 128;                   // [chunk][16 tokens][128 B]
     static constexpr int kVBytes = kBlockPages * kVPage;
     static constexpr int kStageBytes = kKBytes + kVBytes;
-    static constexpr int kStages = HD == 256 ? 2 : HD == 128 ? 4 : 8;
+    static constexpr int kStages = (128 * 1024) / kStageBytes;     // 128 KB of K/V in flight
     static constexpr int kQOff = 0;
     static constexpr int kPOff = kQBytes;
     static constexpr int kStageOff = kPOff + kPBytes;
-    static constexpr int kBarOff = kStageOff + kStages * kStageBytes;
+    static constexpr int kXOff = kStageOff + kStages * kStageBytes;   // row max [2][2 halves][128], row sum [2][128]
+    static constexpr int kBarOff = kXOff + (2 * 2 * kRows + 2 * kRows) * 4;
     // full[stages], empty[stages], s_full[2], s_free[2], p_full, o_done
     static constexpr int kBars = 2 * kStages + 6;
     static constexpr int kSlotOff = kBarOff + kBars * 8;
     static constexpr int kTotal = kSlotOff + 16;
     static constexpr int kAlloc = kTotal + 1024;
-    static constexpr int kThreads = 192;               // 4 softmax warps, producer, MMA issuer
-    static constexpr int kTmemCols = HD == 256 ? 512 : 256;   // S0, S1 (64 each), O (hd)
+    static constexpr int kSoftmaxWarps = 8;            // two threads per query row
+    static constexpr int kThreads = (kSoftmaxWarps + 2) * 32;   // + producer, MMA issuer
+    static constexpr int kTmemCols = HD == 256 ? 512 : HD == 128 ? 256 : 128;   // S0, S1, O (hd)
     static constexpr int kOCol = 2 * kBlockTokens;
     static_assert(kOCol + HD <= kTmemCols, "tensor memory");
     static_assert(kAlloc <= 227 * 1024, "shared memory");
@@ -177,9 +192,9 @@ __global__ void __launch_bounds__(TcGeo<HD>::kThreads, 1)
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(b_sfull + 8 * b, 1);
-            mbar_init(b_sfree + 8 * b, 4);
+            mbar_init(b_sfree + 8 * b, G::kSoftmaxWarps);
         }
-        mbar_init(b_pfull, 4);
+        mbar_init(b_pfull, G::kSoftmaxWarps);
         mbar_init(b_odone, 1);
         mbar_init_fence();
     }
@@ -226,18 +241,23 @@ __global__ void __launch_bounds__(TcGeo<HD>::kThreads, 1)
     const int nblocks = (npages + G::kBlockPages - 1) / G::kBlockPages;
     const int off0 = __ldg(p.off + t0);
 
-    // ---- query row of this thread (warps 0-3) and its Q into shared memory
+    // ---- query row of this thread (softmax warps: row = 32 (warp % 4) + lane,
+    // column half warp / 4) and, by warps 0-3, its Q into shared memory
+    const int row = (warp & 3) * 32 + lane;
+    const int half = warp >> 2;
     bool va = false;
     int lo_a = 1, hi_a = 0;
     size_t rh = 0;
-    if (warp < 4) {
-        const int qr = qbase + tid;
+    if (warp < G::kSoftmaxWarps) {
+        const int qr = qbase + row;
         if (qr < nqr) {
             const int pr = qr / g, h = qr - pr * g;
             prefill_window(p, t0 + pr, lo_a, hi_a);
             rh = static_cast<size_t>(t0 + pr) * p.nh + kh * g + h;
             va = true;
         }
+    }
+    if (warp < 4) {
         const uint4 *src = reinterpret_cast<const uint4 *>(p.q + rh * HD);
 #pragma unroll 4
         for (int u = 0; u < HD / 8; ++u) {
@@ -255,7 +275,7 @@ __global__ void __launch_bounds__(TcGeo<HD>::kThreads, 1)
     tc_fence_after();
     const uint32_t tbase = *tslot;
 
-    if (warp == 4) {
+    if (warp == G::kSoftmaxWarps) {
         // ------------------------------------------------ producer: blocks of 4 pages
         if (lane == 0) {
             tma_prefetch_map(&tm_k);
@@ -293,7 +313,7 @@ __global__ void __launch_bounds__(TcGeo<HD>::kThreads, 1)
                 }
             }
         }
-    } else if (warp == 5) {
+    } else if (warp == G::kSoftmaxWarps + 1) {
         // ------------------------------------------------ MMA issuer (one thread)
         if (lane == 0) {
             constexpr uint32_t kIdS = umma_idesc_bf16(128, G::kBlockTokens, 0, 0);
@@ -337,8 +357,13 @@ __global__ void __launch_bounds__(TcGeo<HD>::kThreads, 1)
             }
         }
     } else {
-        // ------------------------------------------------ softmax warps: thread = query row
-        const uint32_t trow = tbase + (static_cast<uint32_t>(warp * 32) << 16);
+        // ------------------------------------------------ softmax warps: two threads per query row
+        constexpr int HC = G::kBlockTokens / 2;            // columns of S per thread
+        constexpr int HO = HD / 2;                         // columns of O per thread
+        const uint32_t trow = tbase + (static_cast<uint32_t>((warp & 3) * 32) << 16);
+        float *xmax = reinterpret_cast<float *>(smem + G::kXOff);          // [2][2][128]
+        float *xsum = xmax + 2 * 2 * G::kRows;                              // [2][128]
+        const int pair_bar = 1 + (warp & 3);                               // warps w and w + 4
         float m = -INFINITY, l = 0.f;
         bool ok = true;
         for (int j = 0; j < nblocks; ++j) {
@@ -346,41 +371,57 @@ __global__ void __launch_bounds__(TcGeo<HD>::kThreads, 1)
             if (ok)
                 ok = mbar_wait_bounded(b_sfull + 8 * b, (j >> 1) & 1, p.err, kErrTimeoutFull);
             tc_fence_after();
-            uint32_t sr[G::kBlockTokens];
+            uint32_t sr[HC];
 #pragma unroll
-            for (int q4 = 0; q4 < G::kBlockTokens / 16; ++q4)
-                tmem_ld16(trow + b * G::kBlockTokens + q4 * 16, *reinterpret_cast<uint32_t(*)[16]>(sr + q4 * 16));
+            for (int q4 = 0; q4 < HC / 16; ++q4)
+                tmem_ld16(trow + b * G::kBlockTokens + half * HC + q4 * 16,
+                          *reinterpret_cast<uint32_t(*)[16]>(sr + q4 * 16));
             tmem_wait_ld();
             tc_fence_before();
             __syncwarp();
             if (lane == 0)
                 mbar_arrive(b_sfree + 8 * b);
 
-            const int tok0 = (p_first + j * G::kBlockPages) * kPage;
-            float x[G::kBlockTokens];
-            float mx = -INFINITY;
+            const int tok0 = (p_first + j * G::kBlockPages) * kPage + half * HC;
+            // mask to the row's window; this half's max in four chains, then the pair's
+            float x[HC];
+            float mq[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+            if (tok0 >= lo_a && tok0 + HC - 1 <= hi_a) {
 #pragma unroll
-            for (int c = 0; c < G::kBlockTokens; ++c) {
-                const int t = tok0 + c;
-                x[c] = (t >= lo_a && t <= hi_a) ? __uint_as_float(sr[c]) * kLog2e : -INFINITY;
-                mx = fmaxf(mx, x[c]);
+                for (int c = 0; c < HC; ++c) {
+                    x[c] = __uint_as_float(sr[c]);
+                    mq[c & 3] = fmaxf(mq[c & 3], x[c]);
+                }
+            } else {
+#pragma unroll
+                for (int c = 0; c < HC; ++c) {
+                    const int t = tok0 + c;
+                    x[c] = (t >= lo_a && t <= hi_a) ? __uint_as_float(sr[c]) : -INFINITY;
+                    mq[c & 3] = fmaxf(mq[c & 3], x[c]);
+                }
             }
+            const float mh = fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3]));
+            xmax[(b * 2 + half) * G::kRows + row] = mh;
+            group_bar_sync(pair_bar, 64);
+            const float mx = fmaxf(mh, xmax[(b * 2 + (half ^ 1)) * G::kRows + row]) * kLog2e;   // log2 units
             // stale-max rescale: keep m unless the block's max exceeds it by more than 8
             float m_use = m, alpha = 1.f;
             if (mx > m + 8.f || (m == -INFINITY && mx != -INFINITY)) {
                 m_use = mx;
                 alpha = (m == -INFINITY) ? 0.f : exp2f(m - mx);
             }
-            float ls = 0.f;
-            uint32_t pk[G::kBlockTokens / 2];
+            const bool live = m_use != -INFINITY;
+            const float nm = live ? -m_use : 0.f;
+            float lq[4] = {0.f, 0.f, 0.f, 0.f};
+            uint32_t pk[HC / 2];
 #pragma unroll
-            for (int c = 0; c < G::kBlockTokens; c += 2) {
-                const float p0 = m_use == -INFINITY ? 0.f : bf16_round(exp2f(x[c] - m_use));
-                const float p1 = m_use == -INFINITY ? 0.f : bf16_round(exp2f(x[c + 1] - m_use));
-                ls += p0 + p1;
+            for (int c = 0; c < HC; c += 2) {
+                const float p0 = live ? bf16_round(ex2_sfu(__fmaf_rn(x[c], kLog2e, nm))) : 0.f;
+                const float p1 = live ? bf16_round(ex2_sfu(__fmaf_rn(x[c + 1], kLog2e, nm))) : 0.f;
+                lq[(c >> 1) & 3] += p0 + p1;
                 pk[c / 2] = pack_bf16x2(p0, p1);
             }
-            l = __fmaf_rn(l, alpha, ls);
+            l = __fmaf_rn(l, alpha, (lq[0] + lq[1]) + (lq[2] + lq[3]));     // this half's share
             m = m_use;
 
             // O and the P buffer are free once the previous block's PV is done
@@ -389,32 +430,39 @@ __global__ void __launch_bounds__(TcGeo<HD>::kThreads, 1)
             tc_fence_after();
             if (j >= 1 && __any_sync(0xffffffffu, alpha != 1.f)) {
 #pragma unroll 1
-                for (int c0 = 0; c0 < HD; c0 += 16) {
-                    uint32_t r[16];
-                    tmem_ld16(trow + G::kOCol + c0, r);
+                for (int c0 = half * HO; c0 < (half + 1) * HO; c0 += 32) {
+                    uint32_t ra[16], rb[16];
+                    tmem_ld16(trow + G::kOCol + c0, ra);
+                    tmem_ld16(trow + G::kOCol + c0 + 16, rb);
                     tmem_wait_ld();
 #pragma unroll
-                    for (int k = 0; k < 16; ++k)
-                        r[k] = __float_as_uint(__uint_as_float(r[k]) * alpha);
-                    tmem_st16(trow + G::kOCol + c0, r);
+                    for (int k = 0; k < 16; ++k) {
+                        ra[k] = __float_as_uint(__uint_as_float(ra[k]) * alpha);
+                        rb[k] = __float_as_uint(__uint_as_float(rb[k]) * alpha);
+                    }
+                    tmem_st16(trow + G::kOCol + c0, ra);
+                    tmem_st16(trow + G::kOCol + c0 + 16, rb);
                 }
                 tmem_wait_st();
             }
-            // P row -> shared memory, 128-byte swizzle
+            // this half of the P row -> shared memory, 128-byte swizzle
 #pragma unroll
-            for (int w = 0; w < 8; ++w)
-                *reinterpret_cast<uint4 *>(smem + G::kPOff + tid * 128 + ((w ^ (tid & 7)) << 4)) =
+            for (int w = 0; w < HC / 8; ++w) {
+                const int u = half * (HC / 8) + w;
+                *reinterpret_cast<uint4 *>(smem + G::kPOff + row * 128 + ((u ^ (row & 7)) << 4)) =
                     make_uint4(pk[4 * w], pk[4 * w + 1], pk[4 * w + 2], pk[4 * w + 3]);
+            }
             // V rows of tokens outside the union window may hold anything (NaN
             // included) and P is 0 there: zero them before the PV MMA reads them
-            if (tok0 < lo_u || tok0 + G::kBlockTokens - 1 > hi_u) {
+            const int btok0 = (p_first + j * G::kBlockPages) * kPage;
+            if (btok0 < lo_u || btok0 + G::kBlockTokens - 1 > hi_u) {
                 const int st = j % NST;
                 uint8_t *sV = smem + G::kStageOff + st * G::kStageBytes + G::kKBytes;
                 const int np = min(G::kBlockPages, npages - j * G::kBlockPages);
-                for (int e = tid; e < np * kPage * NCH * 8; e += 128) {
+                for (int e = tid; e < np * kPage * NCH * 8; e += G::kSoftmaxWarps * 32) {
                     const int u = e & 7, rc = e >> 3;
                     const int c = rc % NCH, tk = rc / NCH;     // token of the block, chunk
-                    const int t = tok0 + tk;
+                    const int t = btok0 + tk;
                     if (t < lo_u || t > hi_u)
                         *reinterpret_cast<uint4 *>(sV + (tk >> 4) * G::kVPage + c * (kPage * 128) + (tk & 15) * 128 +
                                                    u * 16) = make_uint4(0u, 0u, 0u, 0u);
@@ -426,12 +474,15 @@ __global__ void __launch_bounds__(TcGeo<HD>::kThreads, 1)
             if (lane == 0)
                 mbar_arrive(b_pfull);
         }
-        // ---- finish: O / l in bf16
+        // ---- finish: the row sum over both halves, O / l in bf16 (this half's dims)
+        xsum[half * G::kRows + row] = l;
+        group_bar_sync(pair_bar, 64);
+        const float lt = xsum[row] + xsum[G::kRows + row];
         if (nblocks > 0 && ok)
             ok = mbar_wait_bounded(b_odone, (nblocks - 1) & 1, p.err, kErrTimeoutFull);
         tc_fence_after();
 #pragma unroll 1
-        for (int c0 = 0; c0 < HD; c0 += 16) {
+        for (int c0 = half * HO; c0 < (half + 1) * HO; c0 += 16) {
             uint32_t r[16];
             tmem_ld16(trow + G::kOCol + c0, r);
             tmem_wait_ld();
@@ -440,8 +491,8 @@ __global__ void __launch_bounds__(TcGeo<HD>::kThreads, 1)
 #pragma unroll
                 for (int k = 0; k < 8; ++k) {
                     __nv_bfloat162 v;
-                    v.x = nblocks > 0 ? merge_finish(__uint_as_float(r[2 * k]), l) : __float2bfloat16_rn(0.f);
-                    v.y = nblocks > 0 ? merge_finish(__uint_as_float(r[2 * k + 1]), l) : __float2bfloat16_rn(0.f);
+                    v.x = nblocks > 0 ? merge_finish(__uint_as_float(r[2 * k]), lt) : __float2bfloat16_rn(0.f);
+                    v.y = nblocks > 0 ? merge_finish(__uint_as_float(r[2 * k + 1]), lt) : __float2bfloat16_rn(0.f);
                     w[k] = *reinterpret_cast<uint32_t *>(&v);
                 }
                 uint4 *dst = reinterpret_cast<uint4 *>(p.o + rh * HD + c0);
