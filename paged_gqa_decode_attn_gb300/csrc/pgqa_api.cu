@@ -535,13 +535,16 @@ int pgqa_attn_prefill(void *o, const void *q, const void *k_pool, const void *v_
         return st;
     CUtensorMap tk, tv;
     int whole_k = 0, whole_v = 0;
-    const bool chunked = hd <= 256;      // the tcgen05 kernel places each 64-dim box itself
-    if ((st = pool_map(k_pool, hd, &tk, &whole_k, chunked)) != PGQA_OK ||
-        (st = pool_map(v_pool, hd, &tv, &whole_v, chunked)) != PGQA_OK)
+    // The tcgen05 kernel (hd <= 256) copies K by 64-dim boxes into its
+    // 32-token tile and V by whole-tile boxes where the driver takes them;
+    // the hd-512 kernel takes whole-tile boxes for both where it can.
+    const bool tc = hd <= 256;
+    if ((st = pool_map(k_pool, hd, &tk, &whole_k, tc)) != PGQA_OK ||
+        (st = pool_map(v_pool, hd, &tv, &whole_v, false)) != PGQA_OK)
         return st;
-    if (whole_k != whole_v)
+    if (!tc && whole_k != whole_v)
         return PGQA_ERR_TENSOR_MAP;
-    p.whole_tile_box = whole_k;
+    p.whole_tile_box = whole_v;
     p.err = s->err;
     a.tm_k = &tk;
     a.tm_v = &tv;

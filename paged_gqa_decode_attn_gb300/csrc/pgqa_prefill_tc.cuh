@@ -7,12 +7,13 @@
 //   * one CTA serves 128 query rows (row, head) of one tile and kv head --
 //     the M = 128 of every MMA -- with heads fastest;
 //   * warp 8 streams the chunk's union window in blocks of 2 pages (32
-//     tokens) by TMA into a ring of 128 KB: K into a [hd/64][32 tokens][128 B]
-//     tile (one N = 32 MMA per 16 dims), V as 2 page tiles [hd/64][16 tokens]
-//     [128 B];
+//     tokens) by TMA into a ring of 128 KB, page ids read 32 at a time ahead
+//     of the copies: K by 64-dim boxes into a [hd/64][32 tokens][128 B] tile
+//     (one N = 32 MMA per 16 dims), V by one box per (page, kv head) tile as
+//     [hd/64][16 tokens][128 B];
 //   * warp 9 issues S_j = Q K_j^T into one of two TMEM buffers (32 columns
-//     each), then O += P_{j-1} V_{j-1} (TMEM, hd columns), one tcgen05.mma per
-//     16 dims or 16 tokens, each batch committed to an mbarrier;
+//     each), then O += P_{j-1} V_{j-1} (TMEM, hd columns, one MMA per page),
+//     each batch committed to an mbarrier;
 //   * warps 0-7 run the softmax, two threads per query row (warps w and w+4
 //     share TMEM lanes 32(w%4)..: lane = row), each over half of the block's
 //     columns: they read S_j from TMEM, mask it to the row's window, agree on
@@ -276,39 +277,48 @@ __global__ void __launch_bounds__(TcGeo<HD>::kThreads, 1)
     const uint32_t tbase = *tslot;
 
     if (warp == G::kSoftmaxWarps) {
-        // ------------------------------------------------ producer: blocks of 4 pages
+        // ------------------------------------------------ producer: blocks of 2 pages
         if (lane == 0) {
             tma_prefetch_map(&tm_k);
             tma_prefetch_map(&tm_v);
         }
         const int32_t *tbl = p.block_table + off0 + p_first;
         bool ok = true;
-        for (int j = 0; j < nblocks; ++j) {
-            const int np = min(G::kBlockPages, npages - j * G::kBlockPages);
+        for (int c0 = 0; c0 < npages; c0 += 32) {       // 32 is a multiple of the block's pages
             int phys = 0;
-            if (lane < np) {
-                phys = __ldg(tbl + j * G::kBlockPages + lane);
+            if (c0 + lane < npages) {
+                phys = __ldg(tbl + c0 + lane);
                 if (p.page_map)
                     phys = __ldg(p.page_map + phys);
             }
-            const int st = j % NST;
-            if (lane == 0 && ok && j >= NST)
-                ok = mbar_wait_bounded(b_empty + 8 * st, ((j / NST) - 1) & 1, p.err, kErrTimeoutEmpty);
-            ok = __shfl_sync(0xffffffffu, ok, 0);
-            const uint32_t sK = s_base + G::kStageOff + st * G::kStageBytes;
-            const uint32_t sV = sK + G::kKBytes;
-            if (ok && lane == 0)
-                mbar_arrive_expect_tx(b_full + 8 * st, np * 2 * kPage * HD * 2);
-            for (int pp = 0; pp < np; ++pp) {
-                const int ph = __shfl_sync(0xffffffffu, phys, pp);
-                if (ok && lane == 0) {
-                    const int t = ph * p.nkv + kh;
+            const int nc = min(32, npages - c0);
+            for (int i = 0; i < nc; i += G::kBlockPages) {
+                const int j = (c0 + i) / G::kBlockPages;
+                const int np = min(G::kBlockPages, nc - i);
+                const int st = j % NST;
+                if (lane == 0 && ok && j >= NST)
+                    ok = mbar_wait_bounded(b_empty + 8 * st, ((j / NST) - 1) & 1, p.err, kErrTimeoutEmpty);
+                ok = __shfl_sync(0xffffffffu, ok, 0);
+                const uint32_t sK = s_base + G::kStageOff + st * G::kStageBytes;
+                const uint32_t sV = sK + G::kKBytes;
+                if (ok && lane == 0)
+                    mbar_arrive_expect_tx(b_full + 8 * st, np * 2 * kPage * HD * 2);
+                for (int pp = 0; pp < G::kBlockPages; ++pp) {
+                    const int ph = __shfl_sync(0xffffffffu, phys, (i + pp) & 31);
+                    if (ok && lane == 0 && pp < np) {
+                        const int t = ph * p.nkv + kh;
 #pragma unroll
-                    for (int c = 0; c < NCH; ++c) {
-                        tma_load_3d(sK + c * (G::kBlockTokens * 128) + pp * (kPage * 128), &tm_k, b_full + 8 * st,
-                                    c * kBoxElems, 0, t);
-                        tma_load_3d(sV + pp * G::kVPage + c * (kPage * 128), &tm_v, b_full + 8 * st, c * kBoxElems,
-                                    0, t);
+                        for (int c = 0; c < NCH; ++c)
+                            tma_load_3d(sK + c * (G::kBlockTokens * 128) + pp * (kPage * 128), &tm_k, b_full + 8 * st,
+                                        c * kBoxElems, 0, t);
+                        if (p.whole_tile_box) {
+                            tma_load_4d(sV + pp * G::kVPage, &tm_v, b_full + 8 * st, 0, 0, 0, t);
+                        } else {
+#pragma unroll
+                            for (int c = 0; c < NCH; ++c)
+                                tma_load_3d(sV + pp * G::kVPage + c * (kPage * 128), &tm_v, b_full + 8 * st,
+                                            c * kBoxElems, 0, t);
+                        }
                     }
                 }
             }
