@@ -572,7 +572,7 @@ def run_prefill(args, case, rank, world, dist):
         "config": cfg,
         "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak, "unit": "TFLOP/s",
                      "frac": round(achieved / peak, 4), "traffic": None, "peak_kind": peak_kind,
-                     "kernel": "prefill_kernel", "launch_us": round(kernel_us, 3)},
+                     "kernel": "prefill_tc_kernel (hd <= 256) / prefill_kernel (hd 512)", "launch_us": round(kernel_us, 3)},
         "cpu_baseline": cpu,
         "e2e": {"value": round(e2e_value, 2), "unit": "TFLOP/s", "h2d_bytes_per_step": host_in.numel(),
                 "d2h_bytes_per_step": o_h.numel() * o_h.element_size(), "steps": e2e_steps,
