@@ -56,7 +56,7 @@ def test_page_prefill_cases(args):
 @pytest.mark.parametrize("hd", [64, 128, 256, 512])
 @pytest.mark.parametrize("nh,nkv", [(4, 4), (8, 1), (32, 2), (24, 2), (6, 2)])
 def test_head_dims_and_group_sizes(hd, nh, nkv):
-    """g = 1, 8, 16, 12 and 3: chunks of 64 query rows cut rows' heads apart for g = 3 and 12."""
+    """g = 1, 8, 16, 12 and 3: chunks of 128 (32 at hd 512) query rows cut rows' heads apart for g = 3 and 12."""
     c = wl.prefill_case(nh, nkv, hd, 0, 150, dist="sym", seed=hd + nh)
     prefill_gates(c, mapped=False)
 
