@@ -353,6 +353,70 @@ def prefill_long() -> Case:
     return prefill_case(16, 8, 256, 1024, 8192, dist="sym", name="prefill_nh16_nkv8_hd256_w1024_ctx8192")
 
 
+@dataclasses.dataclass
+class PrepCase:
+    """One QK-RMSNorm / RoPE / paged K-V write problem (bf16 bits, int32 metadata).
+
+    Row t's K and V land in page block_table[off[t] + pos[t]/16] (through
+    page_map when given), slot pos[t] % 16, of [npg][nkv][16][hd] pools.
+    """
+    name: str
+    nh: int
+    nkv: int
+    hd: int
+    rotary_dim: int
+    theta: float
+    eps: float
+    norm_v: bool
+    rows: int
+    q_in: np.ndarray
+    k_in: np.ndarray
+    v_in: np.ndarray
+    q_weight: np.ndarray
+    k_weight: np.ndarray
+    pos: np.ndarray
+    block_table: np.ndarray
+    off: np.ndarray
+    page_map: Optional[np.ndarray] = None
+    npg: int = 0
+
+    def bytes_moved(self) -> int:
+        """Compulsory bytes of one call: the head vectors read and written, weights and metadata aside."""
+        return 2 * self.rows * (self.nh + 2 * self.nkv) * self.hd * 2
+
+
+def prep_case(nh: int, nkv: int, hd: int, rotary_dim: int, rows: int, ctx: int, positions: str = "prefill",
+              theta: float = 10000.0, eps: float = 1e-6, norm_v: bool = True, dist: str = "sym",
+              seed: int = 77, mapped: bool = False, name: str = "") -> PrepCase:
+    """Seeded inputs: Q/K/V rows from one LCG stream, weights around 1, positions
+    0..rows-1 ("prefill"), ctx-rows..ctx-1 ("decode") or a seeded shuffle of
+    distinct positions below ctx ("scattered"), one sequence whose block table
+    is the identity or, with ``mapped``, a seeded permutation of the pool."""
+    rng = Lcg(seed)
+    q_in = draw_bf16(rng, rows * nh * hd, dist)
+    k_in = draw_bf16(rng, rows * nkv * hd, dist)
+    v_in = draw_bf16(rng, rows * nkv * hd, dist)
+    wq = bf16_trunc(np.float32(1.0) + np.float32(0.5) * uniform_sym(rng.states(hd)))
+    wk = bf16_trunc(np.float32(1.0) + np.float32(0.5) * uniform_sym(rng.states(hd)))
+    if positions == "prefill":
+        pos = np.arange(rows, dtype=np.int32)
+    elif positions == "decode":
+        pos = np.arange(ctx - rows, ctx, dtype=np.int32)
+    else:
+        pos = lcg_permutation(ctx, seed + 3)[:rows].astype(np.int32)
+    npages = (ctx + PAGE - 1) // PAGE
+    bt = lcg_permutation(npages, seed + 5).astype(np.int32) if mapped else np.arange(npages, dtype=np.int32)
+    off = np.zeros(rows, dtype=np.int32)
+    return PrepCase(name or f"prep_nh{nh}_nkv{nkv}_hd{hd}_rd{rotary_dim}_r{rows}", nh, nkv, hd, rotary_dim,
+                    float(theta), float(eps), bool(norm_v), rows, q_in, k_in, v_in, wq, wk, pos, bt, off,
+                    npg=npages)
+
+
+def prep_long() -> PrepCase:
+    """A measured prep: the 8192 prompt rows of the sliding sequence, nh16 nkv8 hd256, full rotation."""
+    return prep_case(16, 8, 256, 256, 8192, 8192, positions="prefill", name="prep_nh16_nkv8_hd256_rd256_r8192")
+
+
 def sweep_points():
     """The 108 hybrid-sweep points (hd, ctx, rows, window), in a fixed order."""
     return [(hd, ctx, rows, w) for hd in SWEEP_HD for ctx in SWEEP_CTX
