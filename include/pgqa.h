@@ -217,6 +217,39 @@ int pgqa_prefill_rows_per_tile(int hd);
 int pgqa_make_tiles(const int32_t *seq, int rows, int rows_per_tile, int32_t *tile_t0, int32_t *tile_tn,
                     int max_tiles);
 
+/*
+ * The step before paged attention: QK-RMSNorm, rotary embedding and the paged
+ * K/V write.  pegainfer PR #1002 ("reduce the duplicated CPU operator oracles
+ * in the HD256/HD512 QK-RoPE smokes") describes this step's device gates --
+ * RMSNorm and RoPE of head vectors, rotation over the first rotary_dim dims
+ * ("rope-lo", "rope-hi") with the rest passed through, K and V landing at the
+ * paged-KV layout address -- but prints no formula; this is the plainest
+ * reading.  For every row r and head vector x (hd dims, bf16):
+ *   RMSNorm  y_d = x_d / sqrt(mean(x^2) + eps) * w_d   (Q: q_weight, K: k_weight;
+ *            V: no weight when norm_v, else copied unchanged)
+ *   RoPE     (Q and K) half = rotary_dim / 2, for i < half,
+ *            a = pos[r] * theta^(-2i / rotary_dim):
+ *            y_i <- y_i cos a - y_{i+half} sin a,  y_{i+half} <- y_{i+half} cos a + y_i sin a
+ *   output   q_out[r][h][:]; K and V of kv head kh at element
+ *            ((page * nkv + kh) * 16 + pos[r] % 16) * hd of k_pool / v_pool,
+ *            page = block_table[off[r] + pos[r] / 16] (then page_map[page] when given)
+ * Computed in f32, stored bf16 (round to nearest); the angle is carried in
+ * turns from an f64 frequency, so it stays within ~1e-6 rad at any position.
+ *   q_in [rows][nh][hd], k_in / v_in [rows][nkv][hd], q_weight / k_weight [hd]: bf16
+ *   q_out [rows][nh][hd] bf16, written; k_pool / v_pool: only the rows' slots written
+ *   pos, off [rows], block_table, page_map (may be NULL): int32, device;
+ *            0 <= pos[r] < 2^24 and every looked-up entry in range (not checked)
+ * hd is 64, 128, 256 or 512; rotary_dim in [0, hd], a multiple of hd / 16;
+ * theta > 0, eps >= 0.  Device buffers are caller-owned and 16-byte aligned.
+ * Asynchronous on `stream`; no allocation.  Returns PGQA_OK or PGQA_ERR_* for
+ * bad arguments (checked before any CUDA call) or a launch failure.
+ */
+int pgqa_qk_norm_rope_write(void *q_out, void *k_pool, void *v_pool, const void *q_in, const void *k_in,
+                            const void *v_in, const void *q_weight, const void *k_weight, const int32_t *pos,
+                            const int32_t *block_table, const int32_t *off, const int32_t *page_map, int rows,
+                            int nh, int nkv, int hd, int rotary_dim, float theta, float eps, int norm_v,
+                            void *stream);
+
 /* Static, human-readable name of a status code. */
 const char *pgqa_strerror(int status);
 

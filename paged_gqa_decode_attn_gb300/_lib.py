@@ -39,6 +39,8 @@ SIGNATURES = {
     "pgqa_attn_prefill": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P]),
     "pgqa_prefill_rows_per_tile": (_I, [_I]),
     "pgqa_make_tiles": (_I, [_P, _I, _I, _P, _P, _I]),
+    "pgqa_qk_norm_rope_write": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I,
+                                     ctypes.c_float, ctypes.c_float, _I, _P]),
 }
 
 
@@ -153,6 +155,18 @@ def make_tiles(seq, rows_per_tile: int):
     if m != n:
         raise PgqaError(m if m < 0 else PGQA_ERR_INVALID_ARGUMENT, "make_tiles")
     return t0[:n], tn[:n]
+
+
+def qk_norm_rope_write(q_out, k_pool, v_pool, q_in, k_in, v_in, q_weight, k_weight, pos, block_table, off,
+                       page_map, rows: int, nh: int, nkv: int, hd: int, rotary_dim: int, theta: float, eps: float,
+                       norm_v: bool = True, stream=None) -> None:
+    """QK-RMSNorm, rotary embedding and the paged K/V write (``pgqa_qk_norm_rope_write``)."""
+    st = load().pgqa_qk_norm_rope_write(_ptr(q_out), _ptr(k_pool), _ptr(v_pool), _ptr(q_in), _ptr(k_in), _ptr(v_in),
+                                        _ptr(q_weight), _ptr(k_weight), _ptr(pos), _ptr(block_table), _ptr(off),
+                                        _ptr(page_map), int(rows), int(nh), int(nkv), int(hd), int(rotary_dim),
+                                        float(theta), float(eps), 1 if norm_v else 0, _stream(stream))
+    if st != PGQA_OK:
+        raise PgqaError(st, "qk_norm_rope_write")
 
 
 def choose_splits(kv_len_eff: int, rows: int, nkv: int, nseq: int, num_sms: int | None = None) -> int:

@@ -193,3 +193,27 @@ def test_prefill_bad_arguments_are_rejected_before_any_cuda_call(lib, kw, code):
 
 def test_prefill_zero_tiles_is_ok_without_a_device(lib):
     assert prefill_call(lib, ntiles=0, o=None, q=None) == 0
+
+
+# ---------------------------------------------------------------- QK-RMSNorm / RoPE / paged write host side
+
+def prep_call(lib, rows=1, nh=8, nkv=2, hd=128, rd=128, theta=10000.0, eps=1e-6, qo=FAKE, kp=FAKE, vp=FAKE,
+              qi=FAKE, ki=FAKE, vi=FAKE, wq=FAKE, wk=FAKE, pos=FAKE, bt=FAKE, off=FAKE):
+    return lib.pgqa_qk_norm_rope_write(qo, kp, vp, qi, ki, vi, wq, wk, pos, bt, off, None, rows, nh, nkv, hd, rd,
+                                       theta, eps, 1, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(rows=-1), -1), (dict(nh=0), -1), (dict(nkv=0), -1), (dict(nh=10, nkv=4), -1), (dict(hd=96), -2),
+    (dict(rd=130), -1), (dict(rd=-8), -1), (dict(rd=12), -1), (dict(theta=0.0), -1), (dict(theta=float("inf")), -1),
+    (dict(eps=-1.0), -1), (dict(qo=None), -1), (dict(kp=None), -1), (dict(vp=None), -1), (dict(qi=None), -1),
+    (dict(wk=None), -1), (dict(pos=None), -1), (dict(bt=None), -1), (dict(off=None), -1),
+    (dict(ki=FAKE + 8), -3), (dict(vp=FAKE + 2), -3), (dict(wq=FAKE + 4), -3),
+])
+def test_prep_bad_arguments_are_rejected_before_any_cuda_call(lib, kw, code):
+    assert prep_call(lib, **kw) == code
+
+
+def test_prep_zero_rows_is_ok_without_a_device(lib):
+    assert prep_call(lib, rows=0, qo=None) == 0
+    assert prep_call(lib, rows=0, rd=0) == 0
