@@ -194,6 +194,8 @@ def build_case(name: str):
         return wl.prefill_page()
     if name == "prefill_long":
         return wl.prefill_long()
+    if name == "prep_long":
+        return wl.prep_long()
     raise SystemExit(f"unknown workload {name}")
 
 
@@ -255,7 +257,59 @@ def oracle_rate(case, budget_s: float, steps: int | None = None, warmup: int = 0
             f"{k} of {total_pairs} (row, head) pairs per step, cycling", cores, k)
 
 
+PREP_METRIC = "QK-RMSNorm / RoPE / paged K-V write GB/s"
+
+
+def prep_rows(case, idx):
+    """The oracle's inputs for rows ``idx`` of a prep case (same block table and page map)."""
+    def rows_of(a, width):
+        return np.ascontiguousarray(np.asarray(a).reshape(case.rows, width)[idx]).reshape(-1)
+    return (rows_of(case.q_in, case.nh * case.hd), rows_of(case.k_in, case.nkv * case.hd),
+            rows_of(case.v_in, case.nkv * case.hd), case.q_weight, case.k_weight, np.asarray(case.pos)[idx],
+            case.block_table, np.asarray(case.off)[idx], case.page_map, case.nh, case.nkv, case.hd,
+            case.rotary_dim, case.theta, case.eps, case.norm_v)
+
+
+def prep_oracle_rate(case, budget_s: float, steps: int = 1, warmup: int = 0):
+    """Time the f64 prep oracle (one host thread) on bounded samples of rows sized
+    so the whole run takes about ``budget_s``.  Returns (GB/s, s per step, sample, cores)."""
+    from oracle import prep as op
+    t0 = time.perf_counter()
+    op.prep(*prep_rows(case, np.arange(min(8, case.rows))))
+    t_row = max((time.perf_counter() - t0) / min(8, case.rows), 1e-7)
+    k = int(max(1, min(case.rows, budget_s / max(steps + warmup, 1) / t_row)))
+    cursor = 0
+
+    def one():
+        nonlocal cursor
+        op.prep(*prep_rows(case, (cursor + np.arange(k)) % case.rows))
+        cursor = (cursor + k) % case.rows
+
+    for _ in range(warmup):
+        one()
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        one()
+    per = (time.perf_counter() - t0) / steps
+    return (case.bytes_moved() * k / case.rows / per / 1e9, per,
+            f"{k} of {case.rows} rows per step, cycling", 1)
+
+
 def run_reference(args, case, rank, world):
+    if args.workload.startswith("prep"):
+        gbs, per, sample, cores = prep_oracle_rate(case, args.ref_budget, args.steps, args.warmup)
+        line = {
+            "impl": "reference", "metric": PREP_METRIC, "value": round(gbs, 6), "unit": "GB/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup, "ms_per_step": per * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": prep_config(case),
+            "cpu_baseline": {"value": round(gbs, 6), "unit": "GB/s", "cores": cores, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": round(gbs, 6), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+            "gpu_launches": 0,
+        }
+        print(json.dumps(line), flush=True)
+        return 0
     gbs, per, sample, cores, k = oracle_rate(case, budget_s=args.ref_budget, steps=args.steps, warmup=args.warmup)
     metric, unit = METRIC, "GB/s"
     if args.workload.startswith("prefill"):
@@ -583,6 +637,144 @@ def run_prefill(args, case, rank, world, dist):
     return 0
 
 
+def prep_config(case):
+    return {"workload": case.name, "nh": case.nh, "nkv": case.nkv, "hd": case.hd, "rotary_dim": case.rotary_dim,
+            "theta": case.theta, "norm_v": case.norm_v, "rows": case.rows,
+            "bytes_per_call": case.bytes_moved()}
+
+
+def run_prep(args, case, rank, world, dist):
+    """One step = one pgqa_qk_norm_rope_write call over every row of the case (a
+    NEXT-row workload, not the default line): head-vector bytes read and written
+    over the device time, against the measured HBM copy bandwidth."""
+    import torch
+    import paged_gqa_decode_attn_gb300 as pgqa
+
+    torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
+    dev = torch.device("cuda")
+    if rank == 0:
+        pgqa.build()
+    barrier(dist)
+    pgqa.load()
+    nbytes = case.bytes_moved()
+    copies = args.copies or max(2, math.ceil(3 * L2_BYTES / nbytes))
+    npool = max(int(case.block_table.max()) + 1, case.npg)
+
+    def i16(a):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16))
+
+    parts = [np.ascontiguousarray(a).view(np.uint8) for a in
+             (case.q_in, case.k_in, case.v_in, np.asarray(case.pos, np.int32), np.asarray(case.off, np.int32))]
+    offs, total = [], 0
+    for a in parts:
+        offs.append(total)
+        total += (a.size + 255) // 256 * 256
+    host_in = torch.zeros(total, dtype=torch.uint8).pin_memory()
+    for a, o0 in zip(parts, offs):
+        host_in[o0:o0 + a.size] = torch.from_numpy(a)
+    ins = [host_in.to(dev) for _ in range(copies)]
+    views = [[d[o0:o0 + a.size] for a, o0 in zip(parts, offs)] for d in ins]
+    qw, kw = i16(case.q_weight).to(dev), i16(case.k_weight).to(dev)
+    bt = torch.from_numpy(np.asarray(case.block_table, np.int32)).to(dev)
+    q_out = [torch.empty(case.rows * case.nh * case.hd, dtype=torch.int16, device=dev) for _ in range(copies)]
+    k_pool = [torch.zeros(npool * case.nkv * 16 * case.hd, dtype=torch.int16, device=dev) for _ in range(copies)]
+    v_pool = [torch.zeros_like(k_pool[0]) for _ in range(copies)]
+    q_h = torch.empty(case.rows * case.nh * case.hd, dtype=torch.int16).pin_memory()
+
+    def call(i, stream=None):
+        c = i % copies
+        v = views[c]
+        pgqa.qk_norm_rope_write(q_out[c], k_pool[c], v_pool[c], v[0].view(torch.int16), v[1].view(torch.int16),
+                                v[2].view(torch.int16), qw, kw, v[3].view(torch.int32), bt,
+                                v[4].view(torch.int32), None, case.rows, case.nh, case.nkv, case.hd,
+                                case.rotary_dim, case.theta, case.eps, case.norm_v, stream)
+
+    call(0)
+    torch.cuda.synchronize()
+    spot = None
+    if rank == 0 and not args.no_check:
+        from oracle import prep as op
+        idx = np.arange(0, case.rows, max(1, case.rows // 64))
+        q_ref, k_ref, v_ref, slot = op.prep(*prep_rows(case, idx))
+        got_q = q_out[0].cpu().numpy().view(np.uint16).reshape(case.rows, case.nh, case.hd)[idx]
+        kf = k_pool[0].cpu().numpy().view(np.uint16)
+        vf = v_pool[0].cpu().numpy().view(np.uint16)
+        worst = 0.0
+        for got, ref in [(got_q, q_ref)] + [
+                (f[slot[:, None] + kh * 16 * case.hd + np.arange(case.hd)[None, :]], r[:, kh])
+                for kh in range(case.nkv) for f, r in ((kf, k_ref), (vf, v_ref))]:
+            g = wl.bf16_to_f32(got).astype(np.float64)
+            rms = np.sqrt(np.mean(ref ** 2, axis=-1, keepdims=True))
+            worst = max(worst, float(np.max(np.abs(g - ref) / (np.abs(ref) + rms))))
+        if not worst <= 2.0 ** -8:
+            raise SystemExit(f"spot check against the oracle failed: {worst}")
+        spot = worst
+    sampler = ClockSampler(torch.cuda.current_device()) if not args.no_clocks else None
+    for i in range(args.warmup):
+        call(i)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for i in range(args.steps):
+            call(i)
+    g.replay()
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(dist)
+    torch.cuda.synchronize()
+    ev0.record(stream)
+    g.replay()
+    ev1.record(stream)
+    ev1.synchronize()
+    barrier(dist)
+    el_ms = ev0.elapsed_time(ev1)
+    clocks = sampler.stop() if sampler else None
+    el_max = max_over_ranks(dist, el_ms)
+    value = sum_over_ranks(dist, float(nbytes) * args.steps) / (el_max * 1e-3) / 1e9
+    kernel_us = el_ms * 1e3 / args.steps
+
+    e2e_steps = max(1, min(args.steps, args.e2e_steps))
+    barrier(dist)
+    torch.cuda.synchronize()
+    t_0 = time.perf_counter()
+    for i in range(e2e_steps):
+        ins[i % copies].copy_(host_in, non_blocking=True)
+        call(i)
+        q_h.copy_(q_out[i % copies], non_blocking=True)
+    torch.cuda.synchronize()
+    e2e_s = max_over_ranks(dist, time.perf_counter() - t_0)
+    e2e_value = sum_over_ranks(dist, float(nbytes) * e2e_steps) / e2e_s / 1e9
+    if rank != 0:
+        return 0
+    peak, peak_kind = measured_peaks()
+    achieved = nbytes / (kernel_us * 1e-6) / 1e9
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        gbs, per, sample, cores = prep_oracle_rate(case, args.cpu_budget)
+        cpu = {"value": round(gbs, 6), "unit": "GB/s", "cores": cores, "kind": "oracle", "sample": sample}
+    cfg = prep_config(case)
+    cfg["l2"] = f"rotating {copies} input/output copies ({copies * nbytes / 1e9:.2f} GB moved > 3x L2)"
+    cfg["timing"] = f"CUDA events around one CUDA graph of {args.steps} back-to-back calls"
+    if spot is not None:
+        cfg["spot_check_worst_err_over_abs_plus_rms"] = spot
+    line = {
+        "metric": PREP_METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": el_max / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16 in/out, f32 arithmetic", "data": "synthetic", "config": cfg,
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "traffic": None, "peak_kind": peak_kind,
+                     "kernel": "qk_norm_rope_kernel", "launch_us": round(kernel_us, 3)},
+        "cpu_baseline": cpu,
+        "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": host_in.numel(),
+                "d2h_bytes_per_step": q_h.numel() * q_h.element_size(), "steps": e2e_steps,
+                "us_per_step": round(e2e_s / e2e_steps * 1e6, 3)},
+        "gpu_launches": args.steps, "clocks": clocks,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
@@ -590,7 +782,8 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="sliding",
-                    choices=["sliding", "sliding_mapped", "tiny", "long", "batched", "prefill_page", "prefill_long"])
+                    choices=["sliding", "sliding_mapped", "tiny", "long", "batched", "prefill_page", "prefill_long",
+                             "prep_long"])
     ap.add_argument("--splits", type=int, default=0, help="override choose_splits")
     ap.add_argument("--merge", choices=["counters", "combine"], default="counters")
     ap.add_argument("--graph-chunk", type=int, default=2000)
@@ -614,6 +807,8 @@ def main(argv=None):
     try:
         if args.workload.startswith("prefill"):
             return run_prefill(args, case, rank, world, dist)
+        if args.workload.startswith("prep"):
+            return run_prep(args, case, rank, world, dist)
         return run_ours(args, case, rank, world, dist)
     finally:
         if dist is not None:

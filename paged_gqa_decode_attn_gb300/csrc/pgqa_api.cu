@@ -180,6 +180,20 @@ bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p
 }  // namespace
 
 namespace pgqa {
+// SM count and error-word address of the current device, for the entry
+// points defined in other translation units.
+int device_info(int *num_sms, unsigned int **err)
+{
+    std::lock_guard<std::mutex> lock(g_mutex);
+    DeviceState *s = nullptr;
+    const int st = device_state(&s);
+    if (st != PGQA_OK)
+        return st;
+    *num_sms = s->num_sms;
+    *err = s->err;
+    return PGQA_OK;
+}
+
 int split_kernel_smem_bytes(int hd)
 {
     switch (hd) {

@@ -9,29 +9,48 @@
 // paged decode"); the pages give no formula, so the plainest reading is taken
 // (include/pgqa.h states it).
 //
-// A block takes one row (or a share of its head vectors when rows are few).
-// It first builds the row's rotation table: for each i < rotary_dim / 2 the
-// angle pos * theta^(-2i/rotary_dim) is carried in turns, the frequency over
-// 2 pi given by the host from an f64 pow as a float pair (hi + lo), so the
-// product's whole turns drop out exactly and the remainder keeps ~1e-7 turns
-// at any position below 2^24 -- a plain f32 angle loses ~0.01 rad by
-// position 10^5.  Then one warp per head vector: lane l holds dims
-// [E l, E l + E), E = hd / 32, loaded and stored as one vector; the sum of
-// squares is a warp reduction and each rotation pair meets across lanes
-// half / E apart by one shuffle per element.  Memory-bound: each vector is
-// read once and written once; the next vector's load is issued before the
-// current one is worked.
+// Memory-bound: every head vector is read once and written once.  Persistent
+// CTAs, two per SM, each a producer warp and eight consumer warps around a
+// ring of shared-memory stages.  A work item is a run of up to vpi head
+// vectors of one row (all of a row when they fit).  The producer fetches an
+// item's vectors -- contiguous runs of q_in, k_in, v_in -- with bulk copies
+// that complete on the stage's full barrier, after writing the row's slot
+// (pos, page) and its norm-and-rotation table into the stage.  Consumers work
+// the vectors out of shared memory, each warp a contiguous run of them, one
+// vector at a time with lane l holding dims [E l, E l + E), E = hd / 32,
+// store them and release the stage.
+//
+// Norm and rotation fold into the table: with rs = 1/sqrt(mean x^2 + eps)
+// common to the vector, dim d becomes rs (x_d A_d + x_p B_d), p the partner
+// d +- half, A_d = w_d cos a, B_d = -w_p sin a (low half) or +w_p sin a (high
+// half), and A_d = w_d, B_d = 0 past rotary_dim.  A lane shuffles its
+// partner's raw bf16 words and does two packed f32x2 ops and a scale.  The
+// angle is carried in turns from an f64 frequency split into a float pair, so
+// dropping whole turns is exact and positions up to 2^24 keep ~1e-7 turns.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
 #include <algorithm>
 #include <cmath>
 #include <cstdint>
+#include <mutex>
 
 #include "pgqa.h"
+#include "pgqa_device.cuh"
 
 namespace pgqa {
+
+int device_info(int *num_sms, unsigned int **err);   // pgqa_api.cu
+
 namespace {
+
+constexpr int kPrepConsumerWarps = 8;
+constexpr int kPrepThreads = 32 * (kPrepConsumerWarps + 1);
+constexpr int kPrepCtasPerSm = 2;
+constexpr int kPrepSmemBudget = 110 * 1024;   // per CTA, two beside each other on an SM
+constexpr int kPrepMaxStages = 8;
+constexpr int kPrepItemDataBytes = 16 * 1024;  // head-vector bytes of one item at most
+constexpr int kPrepMetaBytes = 16;
 
 struct PrepParams {
     __nv_bfloat16 *q_out;
@@ -46,163 +65,321 @@ struct PrepParams {
     const int32_t *block_table;
     const int32_t *off;
     const int32_t *page_map;
-    int nh, nkv, rotary_dim, norm_v, vec_per_block;
+    unsigned int *err;
+    int nh, nkv, rotary_dim, norm_v;
+    int vpi;            // head vectors per item
+    int items_per_row;  // ceil((nh + 2 nkv) / vpi)
+    int nitems;         // rows * items_per_row
+    int stages;
+    int stage_bytes;    // table (16 hd) + meta (16) + vpi * hd * 2
     float eps;
     float2 turns[256];  // theta^(-2i/rotary_dim) / (2 pi) = x + y, i < rotary_dim / 2
 };
 
+// E bf16 of one lane, packed two to a word as loaded and stored.
 template <int E>
-struct Vec;
-template <>
-struct Vec<2> { using T = uint32_t; };
-template <>
-struct Vec<4> { using T = uint2; };
-template <>
-struct Vec<8> { using T = uint4; };
+struct Packed {
+    uint32_t w[E / 2];
+};
 
 template <int E>
-__device__ __forceinline__ void load_bf16(const __nv_bfloat16 *src, float (&x)[E])
+__device__ __forceinline__ void load_packed(const __nv_bfloat16 *src, Packed<E> &r)
 {
-    if constexpr (E <= 8) {
-        typename Vec<E>::T raw = *reinterpret_cast<const typename Vec<E>::T *>(src);
-        const __nv_bfloat16 *b = reinterpret_cast<const __nv_bfloat16 *>(&raw);
-#pragma unroll
-        for (int e = 0; e < E; ++e)
-            x[e] = __bfloat162float(b[e]);
+    if constexpr (E == 2) {
+        r.w[0] = *reinterpret_cast<const unsigned int *>(src);
+    } else if constexpr (E == 4) {
+        const uint2 t = *reinterpret_cast<const uint2 *>(src);
+        r.w[0] = t.x;
+        r.w[1] = t.y;
     } else {
-        float (&lo)[8] = *reinterpret_cast<float(*)[8]>(&x[0]);
-        float (&hi)[8] = *reinterpret_cast<float(*)[8]>(&x[8]);
-        load_bf16<8>(src, lo);
-        load_bf16<8>(src + 8, hi);
+#pragma unroll
+        for (int c = 0; c < E / 8; ++c) {
+            const uint4 t = reinterpret_cast<const uint4 *>(src)[c];
+            r.w[4 * c] = t.x;
+            r.w[4 * c + 1] = t.y;
+            r.w[4 * c + 2] = t.z;
+            r.w[4 * c + 3] = t.w;
+        }
     }
 }
 
 template <int E>
-__device__ __forceinline__ void store_bf16(__nv_bfloat16 *dst, const float (&y)[E])
+__device__ __forceinline__ void store_packed(__nv_bfloat16 *dst, const Packed<E> &r)
 {
-    if constexpr (E <= 8) {
-        typename Vec<E>::T raw;
-        __nv_bfloat16 *b = reinterpret_cast<__nv_bfloat16 *>(&raw);
-#pragma unroll
-        for (int e = 0; e < E; ++e)
-            b[e] = __float2bfloat16_rn(y[e]);
-        *reinterpret_cast<typename Vec<E>::T *>(dst) = raw;
+    if constexpr (E == 2) {
+        *reinterpret_cast<unsigned int *>(dst) = r.w[0];
+    } else if constexpr (E == 4) {
+        *reinterpret_cast<uint2 *>(dst) = make_uint2(r.w[0], r.w[1]);
     } else {
-        const float (&lo)[8] = *reinterpret_cast<const float(*)[8]>(&y[0]);
-        const float (&hi)[8] = *reinterpret_cast<const float(*)[8]>(&y[8]);
-        store_bf16<8>(dst, lo);
-        store_bf16<8>(dst + 8, hi);
+#pragma unroll
+        for (int c = 0; c < E / 8; ++c)
+            reinterpret_cast<uint4 *>(dst)[c] = make_uint4(r.w[4 * c], r.w[4 * c + 1], r.w[4 * c + 2], r.w[4 * c + 3]);
     }
 }
 
-template <int HD>
-__device__ __forceinline__ const __nv_bfloat16 *vec_src(const PrepParams &p, int r, int v)
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+// The angle of rotation pair i at position fpos, as (cos, sin): carried in
+// turns, pos * (g.x + g.y) with the product's rounding error recovered
+// exactly, so dropping whole turns loses nothing.
+__device__ __forceinline__ void pair_angle(float fpos, float2 g, float &c, float &s)
 {
-    if (v < p.nh)
-        return p.q_in + (static_cast<size_t>(r) * p.nh + v) * HD;
-    v -= p.nh;
-    const __nv_bfloat16 *base = v < p.nkv ? p.k_in : p.v_in;
-    return base + (static_cast<size_t>(r) * p.nkv + (v < p.nkv ? v : v - p.nkv)) * HD;
+    const float t = fpos * g.x;
+    const float t_err = fmaf(fpos, g.x, -t);
+    const float frac = (t - rintf(t)) + fmaf(fpos, g.y, t_err);
+    sincospif(2.0f * frac, &s, &c);
 }
 
-// grid (rows, ny); block y takes head vectors [vec_per_block y, ..) of row
-// blockIdx.x -- Q heads, then K heads, then V heads -- warp w every 8th from w.
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar)
+{
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+                 "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
+                 : "memory");
+}
+
+// Producer warp: item n of this CTA is global item blockIdx.x + n gridDim.x
+// (row it / items_per_row, run it % items_per_row) in stage n % stages.
 template <int HD>
-__global__ void __launch_bounds__(256) qk_norm_rope_kernel(const __grid_constant__ PrepParams p)
+__device__ void prep_producer(const PrepParams &p, unsigned char *smem, uint32_t bar_full, uint32_t bar_empty,
+                              int my_items)
 {
     constexpr int E = HD / 32;
-    __shared__ float s_cos[HD / 2], s_sin[HD / 2];
-    const int r = blockIdx.x;
-    const int pos = __ldg(p.pos + r);
-    const int half = p.rotary_dim >> 1;
-    const float fpos = static_cast<float>(pos);
-    for (int i = threadIdx.x; i < half; i += blockDim.x) {
-        const float2 g = p.turns[i];
-        const float t = fpos * g.x;
-        const float t_err = fmaf(fpos, g.x, -t);   // exact rounding error of the product
-        const float frac = (t - rintf(t)) + fmaf(fpos, g.y, t_err);
-        float sn, cs;
-        sincospif(2.0f * frac, &sn, &cs);
-        s_cos[i] = cs;
-        s_sin[i] = sn;
-    }
-    __syncthreads();
-
+    constexpr int kPairs = E / 2;
     const int lane = threadIdx.x & 31;
     const int d0 = E * lane;
+    const int half = p.rotary_dim >> 1;
+    const bool low = d0 < half, high = !low && d0 < p.rotary_dim;
+    const int pd0 = low ? d0 + half : (high ? d0 - half : d0);
+    // this lane's weights and its rotation partners' (the table of lane l
+    // serves consumer lane l)
+    Packed<E> wq, wk, pq, pk;
+    load_packed<E>(p.q_weight + d0, wq);
+    load_packed<E>(p.k_weight + d0, wk);
+    load_packed<E>(p.q_weight + pd0, pq);
+    load_packed<E>(p.k_weight + pd0, pk);
+    // this lane's frequencies, read once: a parameter read with a per-lane
+    // index is serialised across the warp
+    float2 g[E];
+#pragma unroll
+    for (int e = 0; e < E; ++e)
+        g[e] = (low || high) ? p.turns[(low ? d0 : pd0) + e] : make_float2(0.f, 0.f);
     const int nvec = p.nh + 2 * p.nkv;
-    const int vend = min(nvec, (blockIdx.y + 1) * p.vec_per_block);
-    int v = blockIdx.y * p.vec_per_block + (threadIdx.x >> 5);
-    if (v >= vend)
-        return;
-    int page = 0;
-    if (p.nkv > 0) {
-        page = __ldg(p.block_table + __ldg(p.off + r) + pos / 16);
-        if (p.page_map)
-            page = __ldg(p.page_map + page);
-    }
-    float x[E];
-    load_bf16<E>(vec_src<HD>(p, r, v) + d0, x);
-    for (; v < vend; v += 8) {
-        float xn[E];
-        if (v + 8 < vend)
-            load_bf16<E>(vec_src<HD>(p, r, v + 8) + d0, xn);
-        const bool is_q = v < p.nh;
-        const bool is_v = v >= p.nh + p.nkv;
-        if (!is_v || p.norm_v) {
-            float ss = 0.f;
-#pragma unroll
-            for (int e = 0; e < E; ++e)
-                ss = fmaf(x[e], x[e], ss);
-#pragma unroll
-            for (int k = 16; k; k >>= 1)
-                ss += __shfl_xor_sync(0xffffffffu, ss, k);
-            const float rs = 1.0f / sqrtf(ss / HD + p.eps);
-            if (is_v) {
-#pragma unroll
-                for (int e = 0; e < E; ++e)
-                    x[e] *= rs;
-            } else {
-                float w[E];
-                load_bf16<E>((is_q ? p.q_weight : p.k_weight) + d0, w);
-#pragma unroll
-                for (int e = 0; e < E; ++e)
-                    x[e] = x[e] * rs * w[e];
-            }
+
+    for (int b = 0; b < my_items; b += 32) {
+        // the slots of 32 items, one per lane
+        int pos_j = 0, page_j = 0;
+        if (b + lane < my_items) {
+            const int r = (blockIdx.x + (b + lane) * gridDim.x) / p.items_per_row;
+            pos_j = __ldg(p.pos + r);
+            page_j = __ldg(p.block_table + __ldg(p.off + r) + pos_j / 16);
+            if (p.page_map)
+                page_j = __ldg(p.page_map + page_j);
         }
-        if (!is_v && half > 0) {
-            // pairs (i, i + half): this lane's dims are all low, all high or all
-            // beyond rotary_dim (rotary_dim is a multiple of 2E)
-            const bool low = d0 < half, high = !low && d0 < p.rotary_dim;
-            const int src_lane = low ? lane + half / E : (high ? lane - half / E : lane);
-            float y[E];
+        const int nb = min(32, my_items - b);
+        for (int k = 0; k < nb; ++k) {
+            const int n = b + k;
+            const int stage = n % p.stages;
+            const int pos = __shfl_sync(0xffffffffu, pos_j, k);
+            const int page = __shfl_sync(0xffffffffu, page_j, k);
+            if (n >= p.stages) {
+                bool ok = true;
+                if (lane == 0)
+                    ok = mbar_wait_bounded(bar_empty + 8 * stage, ((n / p.stages) - 1) & 1, p.err, kErrTimeoutEmpty);
+                if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0))
+                    return;
+                mbar_try_wait(bar_empty + 8 * stage, ((n / p.stages) - 1) & 1);   // every lane acquires
+            }
+            unsigned char *st = smem + static_cast<size_t>(stage) * p.stage_bytes;
+            // table: {A_d, A_d+1, B_d, B_d+1} of lane l's word w (d = E l + 2w)
+            // at [32 w + l], Q then K
+            float4 *tq = reinterpret_cast<float4 *>(st) + lane;
+            float4 *tk = tq + 32 * kPairs;
+            const float fpos = static_cast<float>(pos);
 #pragma unroll
-            for (int e = 0; e < E; ++e)
-                y[e] = __shfl_sync(0xffffffffu, x[e], src_lane);
-            if (low || high) {
-                const int i0 = d0 - (high ? half : 0);
-#pragma unroll
-                for (int e = 0; e < E; ++e) {
-                    const float c = s_cos[i0 + e], sn = s_sin[i0 + e];
-                    x[e] = low ? fmaf(x[e], c, -y[e] * sn) : fmaf(x[e], c, y[e] * sn);
+            for (int w = 0; w < kPairs; ++w) {
+                const float wq0 = bf16_lo(wq.w[w]), wq1 = bf16_hi(wq.w[w]);
+                const float wk0 = bf16_lo(wk.w[w]), wk1 = bf16_hi(wk.w[w]);
+                if (low || high) {
+                    float c0, s0, c1, s1;
+                    pair_angle(fpos, g[2 * w], c0, s0);
+                    pair_angle(fpos, g[2 * w + 1], c1, s1);
+                    if (low) {
+                        s0 = -s0;
+                        s1 = -s1;
+                    }
+                    tq[32 * w] = make_float4(wq0 * c0, wq1 * c1, bf16_lo(pq.w[w]) * s0, bf16_hi(pq.w[w]) * s1);
+                    tk[32 * w] = make_float4(wk0 * c0, wk1 * c1, bf16_lo(pk.w[w]) * s0, bf16_hi(pk.w[w]) * s1);
+                } else {
+                    tq[32 * w] = make_float4(wq0, wq1, 0.f, 0.f);
+                    tk[32 * w] = make_float4(wk0, wk1, 0.f, 0.f);
                 }
             }
+            const int it = blockIdx.x + n * gridDim.x;
+            const int r = it / p.items_per_row;
+            const int va = (it % p.items_per_row) * p.vpi;
+            const int vb = min(nvec, va + p.vpi);
+            const uint32_t bar = bar_full + 8 * stage;
+            if (lane == 0) {
+                *reinterpret_cast<int2 *>(st + 16 * HD) = make_int2(pos, page);
+                mbar_arrive_expect_tx(bar, static_cast<uint32_t>((vb - va) * HD * 2));
+                const uint32_t dst = smem_u32(st) + 16 * HD + kPrepMetaBytes;
+                int a = va, e = min(vb, p.nh);
+                if (a < e)
+                    bulk_g2s(dst + (a - va) * HD * 2, p.q_in + (static_cast<size_t>(r) * p.nh + a) * HD,
+                             (e - a) * HD * 2, bar);
+                a = max(va, p.nh);
+                e = min(vb, p.nh + p.nkv);
+                if (a < e)
+                    bulk_g2s(dst + (a - va) * HD * 2, p.k_in + (static_cast<size_t>(r) * p.nkv + a - p.nh) * HD,
+                             (e - a) * HD * 2, bar);
+                a = max(va, p.nh + p.nkv);
+                if (a < vb)
+                    bulk_g2s(dst + (a - va) * HD * 2,
+                             p.v_in + (static_cast<size_t>(r) * p.nkv + a - p.nh - p.nkv) * HD, (vb - a) * HD * 2,
+                             bar);
+            } else {
+                mbar_arrive(bar);
+            }
         }
-        __nv_bfloat16 *dst;
-        if (is_q) {
-            dst = p.q_out + (static_cast<size_t>(r) * p.nh + v) * HD;
-        } else {
-            const int kh = is_v ? v - p.nh - p.nkv : v - p.nh;
-            dst = (is_v ? p.v_pool : p.k_pool) + ((static_cast<size_t>(page) * p.nkv + kh) * 16 + pos % 16) * HD;
-        }
-        store_bf16<E>(dst + d0, x);
-#pragma unroll
-        for (int e = 0; e < E; ++e)
-            x[e] = xn[e];
     }
+}
+
+template <int HD>
+__device__ void prep_consumer(const PrepParams &p, const unsigned char *smem, uint32_t bar_full,
+                              uint32_t bar_empty, int my_items)
+{
+    constexpr int E = HD / 32;
+    constexpr int kPairs = E / 2;
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int d0 = E * lane;
+    const int half = p.rotary_dim >> 1;
+    const int nl = half / E;
+    // this lane's dims are all low, all high or all beyond rotary_dim
+    // (rotary_dim is a multiple of 2E); past it the partner is the lane itself
+    const int src_lane = d0 < half ? lane + nl : (d0 < p.rotary_dim ? lane - nl : lane);
+    const int nvec = p.nh + 2 * p.nkv;
+
+    for (int n = 0; n < my_items; ++n) {
+        const int stage = n % p.stages;
+        const bool ok = mbar_wait_bounded(bar_full + 8 * stage, (n / p.stages) & 1, p.err, kErrTimeoutFull);
+        if (!__all_sync(0xffffffffu, ok))
+            return;
+        const unsigned char *st = smem + static_cast<size_t>(stage) * p.stage_bytes;
+        const int2 meta = *reinterpret_cast<const int2 *>(st + 16 * HD);
+        const int it = blockIdx.x + n * gridDim.x;
+        const int r = it / p.items_per_row;
+        const int va = (it % p.items_per_row) * p.vpi;
+        const int vb = min(nvec, va + p.vpi);
+        const size_t slot = (static_cast<size_t>(meta.y) * p.nkv * 16 + meta.x % 16) * HD + d0;
+        const unsigned char *data = st + 16 * HD + kPrepMetaBytes;
+
+        // warp w takes a contiguous run of the item's vectors, so Q, K and V
+        // come in long runs and the table of the current kind stays in
+        // registers; V takes A = 1, B = 0 and, without norm_v, rs = 1
+        const int cnt = (vb - va + kPrepConsumerWarps - 1) / kPrepConsumerWarps;
+        const int wa = va + warp * cnt;
+        const int wb = min(vb, wa + cnt);
+        int tab_kind = -1;
+        float4 tab[kPairs];
+        for (int v = wa; v < wb; ++v) {
+            Packed<E> in;
+            load_packed<E>(reinterpret_cast<const __nv_bfloat16 *>(data) + (v - va) * HD + d0, in);
+            const int kind = v < p.nh ? 0 : (v < p.nh + p.nkv ? 1 : 2);
+            if (kind != tab_kind) {
+                const float4 *t = reinterpret_cast<const float4 *>(st) + (kind == 0 ? 0 : 32 * kPairs) + lane;
+#pragma unroll
+                for (int w = 0; w < kPairs; ++w)
+                    tab[w] = kind == 2 ? make_float4(1.f, 1.f, 0.f, 0.f) : t[32 * w];
+                tab_kind = kind;
+            }
+            float2 x[kPairs];
+            float2 acc = make_float2(0.f, 0.f);
+#pragma unroll
+            for (int w = 0; w < kPairs; ++w) {
+                x[w] = make_float2(bf16_lo(in.w[w]), bf16_hi(in.w[w]));
+                acc = __ffma2_rn(x[w], x[w], acc);
+            }
+            float ss = acc.x + acc.y;
+#pragma unroll
+            for (int m = 16; m; m >>= 1)
+                ss += __shfl_xor_sync(0xffffffffu, ss, m);
+            const float rs = (kind == 2 && !p.norm_v) ? 1.0f : rsqrtf(ss * (1.0f / HD) + p.eps);
+            const float2 rs2 = make_float2(rs, rs);
+            Packed<E> out;
+#pragma unroll
+            for (int w = 0; w < kPairs; ++w) {
+                const uint32_t yw = __shfl_sync(0xffffffffu, in.w[w], src_lane);
+                float2 u = __fmul2_rn(x[w], make_float2(tab[w].x, tab[w].y));
+                u = __ffma2_rn(make_float2(bf16_lo(yw), bf16_hi(yw)), make_float2(tab[w].z, tab[w].w), u);
+                u = __fmul2_rn(u, rs2);
+                const __nv_bfloat162 t = __floats2bfloat162_rn(u.x, u.y);
+                out.w[w] = *reinterpret_cast<const uint32_t *>(&t);
+            }
+            __nv_bfloat16 *dst;
+            if (kind == 0)
+                dst = p.q_out + (static_cast<size_t>(r) * p.nh + v) * HD + d0;
+            else if (kind == 2)
+                dst = p.v_pool + slot + static_cast<size_t>(v - p.nh - p.nkv) * 16 * HD;
+            else
+                dst = p.k_pool + slot + static_cast<size_t>(v - p.nh) * 16 * HD;
+            store_packed<E>(dst, out);
+        }
+        __syncwarp();
+        if (lane == 0)
+            mbar_arrive(bar_empty + 8 * stage);
+    }
+}
+
+template <int HD>
+__global__ void __launch_bounds__(kPrepThreads, kPrepCtasPerSm) qk_norm_rope_kernel(const __grid_constant__ PrepParams p)
+{
+    extern __shared__ __align__(128) unsigned char smem[];
+    const uint32_t bar_full = smem_u32(smem) + p.stages * p.stage_bytes;
+    const uint32_t bar_empty = bar_full + 8 * p.stages;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < p.stages; ++s) {
+            mbar_init(bar_full + 8 * s, 32);
+            mbar_init(bar_empty + 8 * s, kPrepConsumerWarps);
+        }
+        mbar_init_fence();
+    }
+    __syncthreads();
+    const int my_items =
+        p.nitems > static_cast<int>(blockIdx.x) ? (p.nitems - 1 - static_cast<int>(blockIdx.x)) / gridDim.x + 1 : 0;
+    if ((threadIdx.x >> 5) == kPrepConsumerWarps)
+        prep_producer<HD>(p, smem, bar_full, bar_empty, my_items);
+    else
+        prep_consumer<HD>(p, smem, bar_full, bar_empty, my_items);
 }
 
 bool aligned16(const void *ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15u) == 0; }
+
+template <int HD>
+cudaError_t launch_prep(const PrepParams &p, int grid, cudaStream_t s)
+{
+    const int bytes = p.stages * p.stage_bytes + 16 * p.stages;
+    static std::mutex mu;
+    static bool set_for_device[64];   // the smem attribute is set on that device
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return e;
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        if (dev < 0 || dev >= 64 || !set_for_device[dev]) {
+            e = cudaFuncSetAttribute(qk_norm_rope_kernel<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     kPrepSmemBudget);
+            if (e != cudaSuccess)
+                return e;
+            if (dev >= 0 && dev < 64)
+                set_for_device[dev] = true;
+        }
+    }
+    qk_norm_rope_kernel<HD><<<grid, kPrepThreads, bytes, s>>>(p);
+    return cudaGetLastError();
+}
 
 }  // namespace
 }  // namespace pgqa
@@ -228,6 +405,15 @@ extern "C" int pgqa_qk_norm_rope_write(void *q_out, void *k_pool, void *v_pool, 
     for (const void *b : bufs)
         if (!pgqa::aligned16(b))
             return PGQA_ERR_MISALIGNED;
+    const long long nvec = static_cast<long long>(nh) + 2ll * nkv;
+    if (nvec * rows > (1ll << 31) - 1)
+        return PGQA_ERR_INVALID_ARGUMENT;
+    int num_sms = 0;
+    unsigned int *err = nullptr;
+    const int st = pgqa::device_info(&num_sms, &err);
+    if (st != PGQA_OK)
+        return st;
+
     pgqa::PrepParams p;
     p.q_out = static_cast<__nv_bfloat16 *>(q_out);
     p.k_pool = static_cast<__nv_bfloat16 *>(k_pool);
@@ -241,6 +427,7 @@ extern "C" int pgqa_qk_norm_rope_write(void *q_out, void *k_pool, void *v_pool, 
     p.block_table = block_table;
     p.off = off;
     p.page_map = page_map;
+    p.err = err;
     p.nh = nh;
     p.nkv = nkv;
     p.rotary_dim = rotary_dim;
@@ -252,18 +439,30 @@ extern "C" int pgqa_qk_norm_rope_write(void *q_out, void *k_pool, void *v_pool, 
         const float hi = static_cast<float>(g);
         p.turns[i] = make_float2(hi, static_cast<float>(g - static_cast<double>(hi)));
     }
-    // one vector per warp while rows are few (about 2048 blocks), else the whole row per block
-    const int nvec = nh + 2 * nkv;
-    const int groups = (nvec + 7) / 8;
-    const int ny = std::min(groups, std::max(1, (2048 + rows - 1) / rows));
-    p.vec_per_block = 8 * ((groups + ny - 1) / ny);
-    const dim3 grid(rows, (nvec + p.vec_per_block - 1) / p.vec_per_block);
+    // Items: a whole row when its vectors fit kPrepItemDataBytes, and finer
+    // runs (down to 8 vectors, one per consumer warp) while there are fewer
+    // items than two per CTA slot.
+    int vpi = static_cast<int>(std::min<long long>(nvec, pgqa::kPrepItemDataBytes / (2 * hd)));
+    const long long slots = static_cast<long long>(num_sms) * pgqa::kPrepCtasPerSm;
+    while (vpi > pgqa::kPrepConsumerWarps && static_cast<long long>(rows) * ((nvec + vpi - 1) / vpi) < 2 * slots)
+        vpi = std::max(pgqa::kPrepConsumerWarps, (vpi + 1) / 2);
+    p.vpi = vpi;
+    p.items_per_row = static_cast<int>((nvec + vpi - 1) / vpi);
+    if (static_cast<long long>(rows) * p.items_per_row > (1ll << 31) - 1)
+        return PGQA_ERR_INVALID_ARGUMENT;
+    p.nitems = rows * p.items_per_row;
+    p.stage_bytes = 16 * hd + pgqa::kPrepMetaBytes + vpi * hd * 2;
+    p.stages = std::min(pgqa::kPrepMaxStages, (pgqa::kPrepSmemBudget - 16 * pgqa::kPrepMaxStages) / p.stage_bytes);
+    if (p.stages < 2)
+        return PGQA_ERR_INVALID_ARGUMENT;
+    const int grid = static_cast<int>(std::min<long long>(p.nitems, slots));
     cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e;
     switch (hd) {
-    case 64: pgqa::qk_norm_rope_kernel<64><<<grid, 256, 0, s>>>(p); break;
-    case 128: pgqa::qk_norm_rope_kernel<128><<<grid, 256, 0, s>>>(p); break;
-    case 256: pgqa::qk_norm_rope_kernel<256><<<grid, 256, 0, s>>>(p); break;
-    default: pgqa::qk_norm_rope_kernel<512><<<grid, 256, 0, s>>>(p); break;
+    case 64: e = pgqa::launch_prep<64>(p, grid, s); break;
+    case 128: e = pgqa::launch_prep<128>(p, grid, s); break;
+    case 256: e = pgqa::launch_prep<256>(p, grid, s); break;
+    default: e = pgqa::launch_prep<512>(p, grid, s); break;
     }
-    return cudaGetLastError() == cudaSuccess ? PGQA_OK : PGQA_ERR_CUDA;
+    return e == cudaSuccess ? PGQA_OK : PGQA_ERR_CUDA;
 }
