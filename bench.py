@@ -41,6 +41,8 @@ L2_BYTES = 129 * 1024 * 1024
 KERNEL_SOURCES = ["paged_gqa_decode_attn_gb300/csrc/pgqa_device.cuh",
                   "paged_gqa_decode_attn_gb300/csrc/pgqa_launch.cuh"]
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "decode_split_kernel_traffic.json")
+PREP_SOURCES = ["paged_gqa_decode_attn_gb300/csrc/pgqa_prep.cu"]
+PREP_TRAFFIC_FILE = os.path.join(ROOT, "profiles", "qk_norm_rope_kernel_traffic.json")
 
 
 # ------------------------------------------------------------------ distributed helpers
@@ -105,23 +107,23 @@ def measured_bf16_peak():
         return 1900.0, "fallback"
 
 
-def kernel_sources_sha() -> str:
+def kernel_sources_sha(sources=KERNEL_SOURCES) -> str:
     h = hashlib.sha256()
-    for rel in KERNEL_SOURCES:
+    for rel in sources:
         with open(os.path.join(ROOT, rel), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
 
 
-def recorded_traffic(workload: str):
+def recorded_traffic(workload: str, path: str = TRAFFIC_FILE, sources=KERNEL_SOURCES):
     """dram bytes per launch from the committed ncu summary, or None if it is stale or absent."""
     try:
-        with open(TRAFFIC_FILE) as f:
+        with open(path) as f:
             d = json.load(f)
     except Exception:
         return None
     e = d.get(workload)
-    if not e or e.get("kernel_sources_sha256_16") != kernel_sources_sha():
+    if not e or e.get("kernel_sources_sha256_16") != kernel_sources_sha(sources):
         return None
     return float(e["dram_bytes_per_launch"])
 
@@ -763,8 +765,9 @@ def run_prep(args, case, rank, world, dist):
         "warmup": args.warmup, "ms_per_step": el_max / args.steps, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16 in/out, f32 arithmetic", "data": "synthetic", "config": cfg,
         "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
-                     "frac": round(achieved / peak, 4), "traffic": None, "peak_kind": peak_kind,
-                     "kernel": "qk_norm_rope_kernel", "launch_us": round(kernel_us, 3)},
+                     "frac": round(achieved / peak, 4),
+                     "traffic": recorded_traffic(case.name, PREP_TRAFFIC_FILE, PREP_SOURCES),
+                     "peak_kind": peak_kind, "kernel": "qk_norm_rope_kernel", "launch_us": round(kernel_us, 3)},
         "cpu_baseline": cpu,
         "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": host_in.numel(),
                 "d2h_bytes_per_step": q_h.numel() * q_h.element_size(), "steps": e2e_steps,
