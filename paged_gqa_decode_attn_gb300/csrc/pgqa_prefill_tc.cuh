@@ -5,13 +5,15 @@
 // in tensor memory:
 //
 //   * one CTA serves 128 query rows (row, head) of one tile and kv head --
-//     the M = 128 of every MMA -- with heads fastest;
-//   * warp 8 streams the chunk's union window in blocks of 2 pages (32
-//     tokens) by TMA into a ring of 128 KB, page ids read 32 at a time ahead
-//     of the copies: K by 64-dim boxes into a [hd/64][32 tokens][128 B] tile
-//     (one N = 32 MMA per 16 dims), V by one box per (page, kv head) tile as
+//     the M = 128 of every MMA -- with heads fastest; their Q sits in tensor
+//     memory (the A operand of S), which leaves 192 KB of shared memory to
+//     the K/V ring;
+//   * warp 8 streams the chunk's union window in blocks of 4 pages (64
+//     tokens) by TMA into that ring, page ids read 32 at a time ahead of the
+//     copies: K by 64-dim boxes into a [hd/64][64 tokens][128 B] tile (one
+//     N = 64 MMA per 16 dims), V by one box per (page, kv head) tile as
 //     [hd/64][16 tokens][128 B];
-//   * warp 9 issues S_j = Q K_j^T into one of two TMEM buffers (32 columns
+//   * warp 9 issues S_j = Q K_j^T into one of two TMEM buffers (64 columns
 //     each), then O += P_{j-1} V_{j-1} (TMEM, hd columns, one MMA per page),
 //     each batch committed to an mbarrier;
 //   * warps 0-7 run the softmax, two threads per query row (warps w and w+4
@@ -61,6 +63,18 @@ __device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t a, uint64_t 
         "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
         "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
         "l"(a), "l"(b), "r"(idesc), "r"(acc)
+        : "memory");
+}
+
+// The same with A in tensor memory: row m in lane m, its K elements two to a
+// 32-bit column (the lower-indexed one in the low half).
+__device__ __forceinline__ void umma_bf16_tmem_a(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t idesc,
+                                                 uint32_t acc)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b), "r"(idesc), "r"(acc)
         : "memory");
 }
 
@@ -128,33 +142,32 @@ __device__ __forceinline__ float ex2_sfu(float x)
 template <int HD>
 struct TcGeo {
     static constexpr int kRows = 128;                  // query rows per CTA (MMA M)
-    static constexpr int kBlockPages = 2;
-    static constexpr int kBlockTokens = kBlockPages * kPage;   // 32: S columns per block
+    static constexpr int kBlockPages = 4;
+    static constexpr int kBlockTokens = kBlockPages * kPage;   // 64: S columns per block
     static constexpr int kChunks = HD / 64;            // 128-byte swizzle rows per head vector
-    static constexpr int kQBytes = kChunks * kRows * 128;      // [chunk][128 rows][128 B]
-    static constexpr int kPBytes = kRows * 128;                // [128 rows][128 B: 32 tokens used]
-    static constexpr int kKBytes = kChunks * kBlockTokens * 128;           // [chunk][32 tokens][128 B]
+    static constexpr int kPBytes = kRows * 128;                // [128 rows][128 B: 64 tokens]
+    static constexpr int kKBytes = kChunks * kBlockTokens * 128;           // [chunk][64 tokens][128 B]
     static constexpr int kVPage = kChunks * kPage * 128;                   // [chunk][16 tokens][128 B]
     static constexpr int kVBytes = kBlockPages * kVPage;
     static constexpr int kStageBytes = kKBytes + kVBytes;
-    static constexpr int kStages = (128 * 1024) / kStageBytes;     // 128 KB of K/V in flight
-    static constexpr int kQOff = 0;
-    static constexpr int kPOff = kQBytes;
+    static constexpr int kStages = (192 * 1024) / kStageBytes;     // 192 KB of K/V in flight
+    static constexpr int kPOff = 0;
     static constexpr int kStageOff = kPOff + kPBytes;
     static constexpr int kXOff = kStageOff + kStages * kStageBytes;   // row max [2][2 halves][128], row sum [2][128]
     static constexpr int kBarOff = kXOff + (2 * 2 * kRows + 2 * kRows) * 4;
-    // full[stages], empty[stages], s_full[2], s_free[2], p_full, o_done
-    static constexpr int kBars = 2 * kStages + 6;
+    // full[stages], empty[stages], s_full[2], s_free[2], p_full, o_done, q_ready
+    static constexpr int kBars = 2 * kStages + 7;
     static constexpr int kSlotOff = kBarOff + kBars * 8;
     static constexpr int kTotal = kSlotOff + 16;
     static constexpr int kAlloc = kTotal + 1024;
     static constexpr int kSoftmaxWarps = 8;            // two threads per query row
     static constexpr int kThreads = (kSoftmaxWarps + 2) * 32;   // + producer, MMA issuer
-    static constexpr int kTmemCols = HD == 256 ? 512 : HD == 128 ? 256 : 128;   // S0, S1, O (hd)
+    static constexpr int kTmemCols = HD == 64 ? 256 : 512;   // S0, S1, O (hd), Q (hd / 2)
     static constexpr int kOCol = 2 * kBlockTokens;
-    static_assert(kOCol + HD <= kTmemCols, "tensor memory");
+    static constexpr int kQCol = kOCol + HD;
+    static_assert(kQCol + HD / 2 <= kTmemCols, "tensor memory");
     static_assert(kAlloc <= 227 * 1024, "shared memory");
-    static_assert(kQBytes % 1024 == 0 && kPBytes % 1024 == 0 && kStageBytes % 1024 == 0, "swizzle atoms");
+    static_assert(kPBytes % 1024 == 0 && kStageBytes % 1024 == 0, "swizzle atoms");
 };
 
 template <int HD>
@@ -168,7 +181,6 @@ __global__ void __launch_bounds__(TcGeo<HD>::kThreads, 1)
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t s_base = smem_u32(smem);
-    const uint32_t sQ = s_base + G::kQOff;
     const uint32_t sP = s_base + G::kPOff;
     const uint32_t s_bar = s_base + G::kBarOff;
     const uint32_t b_full = s_bar;                     // [NST]
@@ -177,6 +189,7 @@ __global__ void __launch_bounds__(TcGeo<HD>::kThreads, 1)
     const uint32_t b_sfree = b_sfull + 16;             // [2]
     const uint32_t b_pfull = b_sfree + 16;
     const uint32_t b_odone = b_pfull + 8;
+    const uint32_t b_qready = b_odone + 8;
     uint32_t *tslot = reinterpret_cast<uint32_t *>(smem + G::kSlotOff);
 
     const int tid = threadIdx.x;
@@ -197,6 +210,7 @@ __global__ void __launch_bounds__(TcGeo<HD>::kThreads, 1)
         }
         mbar_init(b_pfull, G::kSoftmaxWarps);
         mbar_init(b_odone, 1);
+        mbar_init(b_qready, G::kSoftmaxWarps);
         mbar_init_fence();
     }
     grid_dependency_wait();
@@ -243,7 +257,7 @@ __global__ void __launch_bounds__(TcGeo<HD>::kThreads, 1)
     const int off0 = __ldg(p.off + t0);
 
     // ---- query row of this thread (softmax warps: row = 32 (warp % 4) + lane,
-    // column half warp / 4) and, by warps 0-3, its Q into shared memory
+    // column half warp / 4)
     const int row = (warp & 3) * 32 + lane;
     const int half = warp >> 2;
     bool va = false;
@@ -258,23 +272,35 @@ __global__ void __launch_bounds__(TcGeo<HD>::kThreads, 1)
             va = true;
         }
     }
-    if (warp < 4) {
-        const uint4 *src = reinterpret_cast<const uint4 *>(p.q + rh * HD);
-#pragma unroll 4
-        for (int u = 0; u < HD / 8; ++u) {
-            const uint4 v = va ? __ldg(src + u) : make_uint4(0u, 0u, 0u, 0u);
-            const int c = u >> 3, w = u & 7;
-            *reinterpret_cast<uint4 *>(smem + G::kQOff + c * (G::kRows * 128) + tid * 128 + ((w ^ (tid & 7)) << 4)) =
-                v;
-        }
-        fence_async_shared();          // Q (generic stores) -> read by the tensor core
-    }
     if (warp == 0)
         tmem_alloc<G::kTmemCols>(smem_u32(tslot));
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tbase = *tslot;
+    if (warp < G::kSoftmaxWarps) {
+        // this half of the row's Q -> tensor memory columns kQCol + [half hd/4, (half+1) hd/4)
+        const uint4 *src = reinterpret_cast<const uint4 *>(p.q + rh * HD) + half * (HD / 16);
+        const uint32_t tq = tbase + (static_cast<uint32_t>((warp & 3) * 32) << 16) + G::kQCol + half * (HD / 4);
+#pragma unroll 1
+        for (int c0 = 0; c0 < HD / 4; c0 += 16) {
+            uint32_t r[16];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const uint4 v = va ? __ldg(src + c0 / 4 + k) : make_uint4(0u, 0u, 0u, 0u);
+                r[4 * k] = v.x;
+                r[4 * k + 1] = v.y;
+                r[4 * k + 2] = v.z;
+                r[4 * k + 3] = v.w;
+            }
+            tmem_st16(tq + c0, r);
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0)
+            mbar_arrive(b_qready);
+    }
 
     if (warp == G::kSoftmaxWarps) {
         // ------------------------------------------------ producer: blocks of 2 pages
@@ -328,7 +354,8 @@ __global__ void __launch_bounds__(TcGeo<HD>::kThreads, 1)
         if (lane == 0) {
             constexpr uint32_t kIdS = umma_idesc_bf16(128, G::kBlockTokens, 0, 0);
             constexpr uint32_t kIdO = umma_idesc_bf16(128, HD, 0, 1);
-            bool ok = true;
+            bool ok = mbar_wait_bounded(b_qready, 0, p.err, kErrTimeoutFull);
+            tc_fence_after();
             for (int j = 0; j <= nblocks; ++j) {
                 if (j < nblocks) {
                     const int st = j % NST, b = j & 1;
@@ -342,9 +369,9 @@ __global__ void __launch_bounds__(TcGeo<HD>::kThreads, 1)
 #pragma unroll
                         for (int ks = 0; ks < HD / 16; ++ks) {
                             const int c = ks >> 2, kk = ks & 3;
-                            umma_bf16(tbase + b * G::kBlockTokens,
-                                      umma_sdesc(sQ + c * (G::kRows * 128) + kk * 32, 16, 1024),
-                                      umma_sdesc(sK + c * (G::kBlockTokens * 128) + kk * 32, 16, 1024), kIdS, ks > 0);
+                            umma_bf16_tmem_a(tbase + b * G::kBlockTokens, tbase + G::kQCol + ks * 8,
+                                             umma_sdesc(sK + c * (G::kBlockTokens * 128) + kk * 32, 16, 1024), kIdS,
+                                             ks > 0);
                         }
                     }
                     umma_commit(b_sfull + 8 * b);
