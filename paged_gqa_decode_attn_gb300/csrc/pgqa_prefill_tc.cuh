@@ -453,10 +453,13 @@ __global__ void __launch_bounds__(TcGeo<HD>::kThreads, 1)
             uint32_t pk[HC / 2];
 #pragma unroll
             for (int c = 0; c < HC; c += 2) {
-                const float p0 = live ? bf16_round(ex2_sfu(__fmaf_rn(x[c], kLog2e, nm))) : 0.f;
-                const float p1 = live ? bf16_round(ex2_sfu(__fmaf_rn(x[c + 1], kLog2e, nm))) : 0.f;
-                lq[(c >> 1) & 3] += p0 + p1;
-                pk[c / 2] = pack_bf16x2(p0, p1);
+                // P rounded to bf16 once, by the pair conversion; the row sum
+                // takes the rounded values back out of the packed word
+                const float e0 = live ? ex2_sfu(__fmaf_rn(x[c], kLog2e, nm)) : 0.f;
+                const float e1 = live ? ex2_sfu(__fmaf_rn(x[c + 1], kLog2e, nm)) : 0.f;
+                const uint32_t w = pack_bf16x2(e0, e1);
+                pk[c / 2] = w;
+                lq[(c >> 1) & 3] += __uint_as_float(w << 16) + __uint_as_float(w & 0xffff0000u);
             }
             l = __fmaf_rn(l, alpha, (lq[0] + lq[1]) + (lq[2] + lq[3]));     // this half's share
             m = m_use;
