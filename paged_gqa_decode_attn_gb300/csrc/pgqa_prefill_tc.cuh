@@ -8,23 +8,23 @@
 //     the M = 128 of every MMA -- with heads fastest; their Q sits in tensor
 //     memory (the A operand of S), which leaves 192 KB of shared memory to
 //     the K/V ring;
-//   * warp 8 streams the chunk's union window in blocks of 4 pages (64
+//   * warp 16 streams the chunk's union window in blocks of 4 pages (64
 //     tokens) by TMA into that ring, page ids read 32 at a time ahead of the
 //     copies: K by 64-dim boxes into a [hd/64][64 tokens][128 B] tile (one
 //     N = 64 MMA per 16 dims), V by one box per (page, kv head) tile as
 //     [hd/64][16 tokens][128 B];
-//   * warp 9 issues S_j = Q K_j^T into one of two TMEM buffers (64 columns
+//   * warp 17 issues S_j = Q K_j^T into one of two TMEM buffers (64 columns
 //     each), then O += P_{j-1} V_{j-1} (TMEM, hd columns, one MMA per page),
 //     each batch committed to an mbarrier;
-//   * warps 0-7 run the softmax, two threads per query row (warps w and w+4
-//     share TMEM lanes 32(w%4)..: lane = row), each over half of the block's
-//     columns: they read S_j from TMEM, mask it to the row's window, agree on
-//     the row max through shared memory, run the online softmax in log2
-//     units, rescale their half of O in TMEM only when the row's running max
-//     grows by more than 2^8 (exact in real arithmetic: P then stays below
-//     256), write their half of P_j as bf16 into shared memory (the A operand
-//     of the PV MMA), and at the end divide their half of O by the row sum and
-//     store bf16.
+//   * warps 0-15 run the softmax, four threads per query row (warps w, w+4,
+//     w+8, w+12 share TMEM lanes 32(w%4)..: lane = row), each over a quarter
+//     of the block's columns: they read S_j from TMEM, mask it to the row's
+//     window, agree on the row max through shared memory, run the online
+//     softmax in log2 units, rescale their quarter of O in TMEM only when the
+//     row's running max grows by more than 2^8 (exact in real arithmetic: P
+//     then stays below 256), write their quarter of P_j as bf16 into shared
+//     memory (the A operand of the PV MMA), and at the end divide their
+//     quarter of O by the row sum and store bf16.
 //
 // Every wait is bounded; a thread that gives up skips its later waits and
 // every role still reaches the final barrier, which frees the tensor memory.
@@ -153,14 +153,15 @@ struct TcGeo {
     static constexpr int kStages = (192 * 1024) / kStageBytes;     // 192 KB of K/V in flight
     static constexpr int kPOff = 0;
     static constexpr int kStageOff = kPOff + kPBytes;
-    static constexpr int kXOff = kStageOff + kStages * kStageBytes;   // row max [2][2 halves][128], row sum [2][128]
-    static constexpr int kBarOff = kXOff + (2 * 2 * kRows + 2 * kRows) * 4;
+    static constexpr int kSoftmaxWarps = 16;           // four threads per query row
+    static constexpr int kParts = kSoftmaxWarps / 4;   // threads per row, each over 1/kParts of the columns
+    static constexpr int kXOff = kStageOff + kStages * kStageBytes;   // row max [2][parts][128], row sum [parts][128]
+    static constexpr int kBarOff = kXOff + (2 * kParts * kRows + kParts * kRows) * 4;
     // full[stages], empty[stages], s_full[2], s_free[2], p_full, o_done, q_ready
     static constexpr int kBars = 2 * kStages + 7;
     static constexpr int kSlotOff = kBarOff + kBars * 8;
     static constexpr int kTotal = kSlotOff + 16;
     static constexpr int kAlloc = kTotal + 1024;
-    static constexpr int kSoftmaxWarps = 8;            // two threads per query row
     static constexpr int kThreads = (kSoftmaxWarps + 2) * 32;   // + producer, MMA issuer
     static constexpr int kTmemCols = HD == 64 ? 256 : 512;   // S0, S1, O (hd), Q (hd / 2)
     static constexpr int kOCol = 2 * kBlockTokens;
@@ -257,9 +258,9 @@ __global__ void __launch_bounds__(TcGeo<HD>::kThreads, 1)
     const int off0 = __ldg(p.off + t0);
 
     // ---- query row of this thread (softmax warps: row = 32 (warp % 4) + lane,
-    // column half warp / 4)
+    // column part warp / 4 of kParts)
     const int row = (warp & 3) * 32 + lane;
-    const int half = warp >> 2;
+    const int part = warp >> 2;
     bool va = false;
     int lo_a = 1, hi_a = 0;
     size_t rh = 0;
@@ -279,11 +280,12 @@ __global__ void __launch_bounds__(TcGeo<HD>::kThreads, 1)
     tc_fence_after();
     const uint32_t tbase = *tslot;
     if (warp < G::kSoftmaxWarps) {
-        // this half of the row's Q -> tensor memory columns kQCol + [half hd/4, (half+1) hd/4)
-        const uint4 *src = reinterpret_cast<const uint4 *>(p.q + rh * HD) + half * (HD / 16);
-        const uint32_t tq = tbase + (static_cast<uint32_t>((warp & 3) * 32) << 16) + G::kQCol + half * (HD / 4);
+        // the row's Q -> tensor memory columns kQCol + [0, hd/2), 16 columns
+        // (32 elements) at a time, the parts taking turns
+        const uint4 *src = reinterpret_cast<const uint4 *>(p.q + rh * HD);
+        const uint32_t tq = tbase + (static_cast<uint32_t>((warp & 3) * 32) << 16) + G::kQCol;
 #pragma unroll 1
-        for (int c0 = 0; c0 < HD / 4; c0 += 16) {
+        for (int c0 = part * 16; c0 < HD / 2; c0 += 16 * G::kParts) {
             uint32_t r[16];
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
@@ -394,13 +396,15 @@ __global__ void __launch_bounds__(TcGeo<HD>::kThreads, 1)
             }
         }
     } else {
-        // ------------------------------------------------ softmax warps: two threads per query row
-        constexpr int HC = G::kBlockTokens / 2;            // columns of S per thread
-        constexpr int HO = HD / 2;                         // columns of O per thread
+        // ------------------------------------------------ softmax warps: kParts threads per query row
+        constexpr int NP = G::kParts;
+        constexpr int HC = G::kBlockTokens / NP;           // columns of S per thread
+        constexpr int HO = HD / NP;                        // columns of O per thread
+        constexpr int kRs = HO >= 32 ? 32 : 16;            // O columns per rescale step
         const uint32_t trow = tbase + (static_cast<uint32_t>((warp & 3) * 32) << 16);
-        float *xmax = reinterpret_cast<float *>(smem + G::kXOff);          // [2][2][128]
-        float *xsum = xmax + 2 * 2 * G::kRows;                              // [2][128]
-        const int pair_bar = 1 + (warp & 3);                               // warps w and w + 4
+        float *xmax = reinterpret_cast<float *>(smem + G::kXOff);          // [2][NP][128]
+        float *xsum = xmax + 2 * NP * G::kRows;                             // [NP][128]
+        const int pair_bar = 1 + (warp & 3);                               // warps w, w + 4, w + 8, ...
         float m = -INFINITY, l = 0.f;
         bool ok = true;
         for (int j = 0; j < nblocks; ++j) {
@@ -411,7 +415,7 @@ __global__ void __launch_bounds__(TcGeo<HD>::kThreads, 1)
             uint32_t sr[HC];
 #pragma unroll
             for (int q4 = 0; q4 < HC / 16; ++q4)
-                tmem_ld16(trow + b * G::kBlockTokens + half * HC + q4 * 16,
+                tmem_ld16(trow + b * G::kBlockTokens + part * HC + q4 * 16,
                           *reinterpret_cast<uint32_t(*)[16]>(sr + q4 * 16));
             tmem_wait_ld();
             tc_fence_before();
@@ -419,8 +423,8 @@ __global__ void __launch_bounds__(TcGeo<HD>::kThreads, 1)
             if (lane == 0)
                 mbar_arrive(b_sfree + 8 * b);
 
-            const int tok0 = (p_first + j * G::kBlockPages) * kPage + half * HC;
-            // mask to the row's window; this half's max in four chains, then the pair's
+            const int tok0 = (p_first + j * G::kBlockPages) * kPage + part * HC;
+            // mask to the row's window; this part's max in four chains, then the row's
             float x[HC];
             float mq[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
             if (tok0 >= lo_a && tok0 + HC - 1 <= hi_a) {
@@ -438,9 +442,13 @@ __global__ void __launch_bounds__(TcGeo<HD>::kThreads, 1)
                 }
             }
             const float mh = fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3]));
-            xmax[(b * 2 + half) * G::kRows + row] = mh;
-            group_bar_sync(pair_bar, 64);
-            const float mx = fmaxf(mh, xmax[(b * 2 + (half ^ 1)) * G::kRows + row]) * kLog2e;   // log2 units
+            xmax[(b * NP + part) * G::kRows + row] = mh;
+            group_bar_sync(pair_bar, 32 * NP);
+            float mr = mh;
+#pragma unroll
+            for (int k = 0; k < NP; ++k)
+                mr = fmaxf(mr, xmax[(b * NP + k) * G::kRows + row]);
+            const float mx = mr * kLog2e;   // log2 units
             // stale-max rescale: keep m unless the block's max exceeds it by more than 8
             float m_use = m, alpha = 1.f;
             if (mx > m + 8.f || (m == -INFINITY && mx != -INFINITY)) {
@@ -461,7 +469,7 @@ __global__ void __launch_bounds__(TcGeo<HD>::kThreads, 1)
                 pk[c / 2] = w;
                 lq[(c >> 1) & 3] += __uint_as_float(w << 16) + __uint_as_float(w & 0xffff0000u);
             }
-            l = __fmaf_rn(l, alpha, (lq[0] + lq[1]) + (lq[2] + lq[3]));     // this half's share
+            l = __fmaf_rn(l, alpha, (lq[0] + lq[1]) + (lq[2] + lq[3]));     // this part's share
             m = m_use;
 
             // O and the P buffer are free once the previous block's PV is done
@@ -470,25 +478,27 @@ __global__ void __launch_bounds__(TcGeo<HD>::kThreads, 1)
             tc_fence_after();
             if (j >= 1 && __any_sync(0xffffffffu, alpha != 1.f)) {
 #pragma unroll 1
-                for (int c0 = half * HO; c0 < (half + 1) * HO; c0 += 32) {
-                    uint32_t ra[16], rb[16];
-                    tmem_ld16(trow + G::kOCol + c0, ra);
-                    tmem_ld16(trow + G::kOCol + c0 + 16, rb);
+                for (int c0 = part * HO; c0 < (part + 1) * HO; c0 += kRs) {
+                    uint32_t ra[kRs / 16][16];
+#pragma unroll
+                    for (int h = 0; h < kRs / 16; ++h)
+                        tmem_ld16(trow + G::kOCol + c0 + 16 * h, ra[h]);
                     tmem_wait_ld();
 #pragma unroll
-                    for (int k = 0; k < 16; ++k) {
-                        ra[k] = __float_as_uint(__uint_as_float(ra[k]) * alpha);
-                        rb[k] = __float_as_uint(__uint_as_float(rb[k]) * alpha);
-                    }
-                    tmem_st16(trow + G::kOCol + c0, ra);
-                    tmem_st16(trow + G::kOCol + c0 + 16, rb);
+                    for (int h = 0; h < kRs / 16; ++h)
+#pragma unroll
+                        for (int k = 0; k < 16; ++k)
+                            ra[h][k] = __float_as_uint(__uint_as_float(ra[h][k]) * alpha);
+#pragma unroll
+                    for (int h = 0; h < kRs / 16; ++h)
+                        tmem_st16(trow + G::kOCol + c0 + 16 * h, ra[h]);
                 }
                 tmem_wait_st();
             }
-            // this half of the P row -> shared memory, 128-byte swizzle
+            // this part of the P row -> shared memory, 128-byte swizzle
 #pragma unroll
             for (int w = 0; w < HC / 8; ++w) {
-                const int u = half * (HC / 8) + w;
+                const int u = part * (HC / 8) + w;
                 *reinterpret_cast<uint4 *>(smem + G::kPOff + row * 128 + ((u ^ (row & 7)) << 4)) =
                     make_uint4(pk[4 * w], pk[4 * w + 1], pk[4 * w + 2], pk[4 * w + 3]);
             }
@@ -514,15 +524,18 @@ __global__ void __launch_bounds__(TcGeo<HD>::kThreads, 1)
             if (lane == 0)
                 mbar_arrive(b_pfull);
         }
-        // ---- finish: the row sum over both halves, O / l in bf16 (this half's dims)
-        xsum[half * G::kRows + row] = l;
-        group_bar_sync(pair_bar, 64);
-        const float lt = xsum[row] + xsum[G::kRows + row];
+        // ---- finish: the row sum over the parts, O / l in bf16 (this part's dims)
+        xsum[part * G::kRows + row] = l;
+        group_bar_sync(pair_bar, 32 * NP);
+        float lt = xsum[row];
+#pragma unroll
+        for (int k = 1; k < NP; ++k)
+            lt += xsum[k * G::kRows + row];
         if (nblocks > 0 && ok)
             ok = mbar_wait_bounded(b_odone, (nblocks - 1) & 1, p.err, kErrTimeoutFull);
         tc_fence_after();
 #pragma unroll 1
-        for (int c0 = half * HO; c0 < (half + 1) * HO; c0 += 16) {
+        for (int c0 = part * HO; c0 < (part + 1) * HO; c0 += 16) {
             uint32_t r[16];
             tmem_ld16(trow + G::kOCol + c0, r);
             tmem_wait_ld();
