@@ -550,7 +550,7 @@ int pgqa_attn_prefill(void *o, const void *q, const void *k_pool, const void *v_
     CUtensorMap tk, tv;
     int whole_k = 0, whole_v = 0;
     // The tcgen05 kernel (hd <= 256) copies K by 64-dim boxes into its
-    // 32-token tile and V by whole-tile boxes where the driver takes them;
+    // 64-token tile and V by whole-tile boxes where the driver takes them;
     // the hd-512 kernel takes whole-tile boxes for both where it can.
     const bool tc = hd <= 256;
     if ((st = pool_map(k_pool, hd, &tk, &whole_k, tc)) != PGQA_OK ||
@@ -560,6 +560,7 @@ int pgqa_attn_prefill(void *o, const void *q, const void *k_pool, const void *v_
         return PGQA_ERR_TENSOR_MAP;
     p.whole_tile_box = whole_v;
     p.err = s->err;
+    a.num_sms = s->num_sms;
     a.tm_k = &tk;
     a.tm_v = &tv;
     const bool set_attr = !s->prefill_attr_set[hi];

@@ -443,6 +443,7 @@ struct PrefillLaunchArgs {
     const CUtensorMap *tm_k;
     const CUtensorMap *tm_v;
     int ntiles;
+    int num_sms;          // persistent kernels: one CTA per SM
     cudaStream_t stream;
 };
 

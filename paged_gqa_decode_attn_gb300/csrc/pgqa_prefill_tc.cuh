@@ -30,6 +30,9 @@
 // every role still reaches the final barrier, which frees the tensor memory.
 #pragma once
 
+#include <algorithm>
+#include <climits>
+
 #include "pgqa_prefill.cuh"
 
 namespace pgqa {
@@ -157,8 +160,8 @@ struct TcGeo {
     static constexpr int kParts = kSoftmaxWarps / 4;   // threads per row, each over 1/kParts of the columns
     static constexpr int kXOff = kStageOff + kStages * kStageBytes;   // row max [2][parts][128], row sum [parts][128]
     static constexpr int kBarOff = kXOff + (2 * kParts * kRows + kParts * kRows) * 4;
-    // full[stages], empty[stages], s_full[2], s_free[2], p_full, o_done, q_ready
-    static constexpr int kBars = 2 * kStages + 7;
+    // full[stages], empty[stages], s_full[2], s_free[2], p_full, o_done, q_ready, o_free
+    static constexpr int kBars = 2 * kStages + 8;
     static constexpr int kSlotOff = kBarOff + kBars * 8;
     static constexpr int kTotal = kSlotOff + 16;
     static constexpr int kAlloc = kTotal + 1024;
@@ -171,10 +174,80 @@ struct TcGeo {
     static_assert(kPBytes % 1024 == 0 && kStageBytes % 1024 == 0, "swizzle atoms");
 };
 
+// One work item: the 128 query rows of chunk `chunk` of tile `tile` for kv
+// head `kh`, and the union window of their positions.  Every role computes
+// it the same way (a whole warp, one position per lane).
+struct TcItem {
+    int t0, tn, kh, qbase, lo_u, hi_u, p_first, npages, nblocks, off0;
+    bool live;     // the chunk has rows
+};
+
+template <int HD>
+__device__ __forceinline__ TcItem tc_item(const PrefillParams &p, int it, int ntiles, int lane, bool report)
+{
+    using G = TcGeo<HD>;
+    TcItem I;
+    const int tr = it % ntiles;
+    const int rest = it / ntiles;
+    I.kh = rest % p.nkv;
+    const int chunk = rest / p.nkv;
+    const int tile = ntiles - 1 - tr;          // last tiles first: they hold the longest windows
+    I.t0 = __ldg(p.tile_t0 + tile);
+    I.tn = __ldg(p.tile_tn + tile);
+    I.qbase = chunk * G::kRows;
+    I.live = false;
+    I.lo_u = 0;
+    I.hi_u = -1;
+    I.p_first = 0;
+    I.npages = 0;
+    I.nblocks = 0;
+    I.off0 = 0;
+    if (I.tn > p.rows_per_tile) {
+        if (report && lane == 0)
+            atomicOr(p.err, kErrTileRows);
+        return I;
+    }
+    const int g = p.g;
+    const int nqr = I.tn * g;
+    if (I.tn <= 0 || I.qbase >= nqr)
+        return I;
+    I.live = true;
+    const int pr_first = I.qbase / g;
+    const int pr_last = min(I.tn - 1, (I.qbase + G::kRows - 1) / g);
+    int lo_m = INT_MAX, hi_m = INT_MIN;
+    for (int pr = pr_first + lane; pr <= pr_last; pr += 32) {
+        int lo, hi;
+        prefill_window(p, I.t0 + pr, lo, hi);
+        if (hi >= lo) {
+            lo_m = min(lo_m, lo);
+            hi_m = max(hi_m, hi);
+        }
+    }
+#pragma unroll
+    for (int k = 16; k; k >>= 1) {
+        lo_m = min(lo_m, __shfl_xor_sync(0xffffffffu, lo_m, k));
+        hi_m = max(hi_m, __shfl_xor_sync(0xffffffffu, hi_m, k));
+    }
+    if (hi_m != INT_MIN) {
+        I.lo_u = lo_m;
+        I.hi_u = hi_m;
+    }
+    I.p_first = I.lo_u >> 4;
+    I.npages = I.hi_u >= I.lo_u ? (I.hi_u >> 4) - I.p_first + 1 : 0;
+    I.nblocks = (I.npages + G::kBlockPages - 1) / G::kBlockPages;
+    I.off0 = __ldg(p.off + I.t0);
+    return I;
+}
+
+// Persistent: CTA c serves items c, c + gridDim.x, ... of the ntiles * nkv *
+// nchunks items.  The ring, the S buffers and the mbarrier phases run on
+// counters that continue across items, so the next item's K/V stream in
+// while the current one finishes, and its Q goes into tensor memory (after
+// the current item's last S) before the current item's O is read out.
 template <int HD>
 __global__ void __launch_bounds__(TcGeo<HD>::kThreads, 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
-                      const PrefillParams p)
+                      const PrefillParams p, int ntiles, int nchunks)
 {
     using G = TcGeo<HD>;
     constexpr int NST = G::kStages;
@@ -191,14 +264,13 @@ __global__ void __launch_bounds__(TcGeo<HD>::kThreads, 1)
     const uint32_t b_pfull = b_sfree + 16;
     const uint32_t b_odone = b_pfull + 8;
     const uint32_t b_qready = b_odone + 8;
+    const uint32_t b_ofree = b_qready + 8;
     uint32_t *tslot = reinterpret_cast<uint32_t *>(smem + G::kSlotOff);
 
     const int tid = threadIdx.x;
     const int warp = tid >> 5;
     const int lane = tid & 31;
-    const int tile = blockIdx.x;
-    const int kh = blockIdx.y;
-    const int chunk = blockIdx.z;
+    const int nitems = ntiles * p.nkv * nchunks;
 
     if (tid == 0) {
         for (int s = 0; s < NST; ++s) {
@@ -212,140 +284,65 @@ __global__ void __launch_bounds__(TcGeo<HD>::kThreads, 1)
         mbar_init(b_pfull, G::kSoftmaxWarps);
         mbar_init(b_odone, 1);
         mbar_init(b_qready, G::kSoftmaxWarps);
+        mbar_init(b_ofree, G::kSoftmaxWarps);
         mbar_init_fence();
     }
     grid_dependency_wait();
     grid_launch_dependents();
-
-    const int t0 = __ldg(p.tile_t0 + tile);
-    const int tn = __ldg(p.tile_tn + tile);
-    if (tn > p.rows_per_tile) {
-        if (tid == 0)
-            atomicOr(p.err, kErrTileRows);
-        return;
-    }
-    const int g = p.g;
-    const int nqr = tn * g;
-    const int qbase = chunk * G::kRows;
-    if (tn <= 0 || qbase >= nqr)
-        return;
-
-    // ---- union window of the served rows (positions pr_first..pr_last)
-    const int pr_first = qbase / g;
-    const int pr_last = min(tn - 1, (qbase + G::kRows - 1) / g);
-    int lo_m = INT_MAX, hi_m = INT_MIN;
-    for (int pr = pr_first + lane; pr <= pr_last; pr += 32) {
-        int lo, hi;
-        prefill_window(p, t0 + pr, lo, hi);
-        if (hi >= lo) {
-            lo_m = min(lo_m, lo);
-            hi_m = max(hi_m, hi);
-        }
-    }
-#pragma unroll
-    for (int k = 16; k; k >>= 1) {
-        lo_m = min(lo_m, __shfl_xor_sync(0xffffffffu, lo_m, k));
-        hi_m = max(hi_m, __shfl_xor_sync(0xffffffffu, hi_m, k));
-    }
-    int lo_u = 0, hi_u = -1;
-    if (hi_m != INT_MIN) {
-        lo_u = lo_m;
-        hi_u = hi_m;
-    }
-    const int p_first = lo_u >> 4;
-    const int npages = hi_u >= lo_u ? (hi_u >> 4) - p_first + 1 : 0;
-    const int nblocks = (npages + G::kBlockPages - 1) / G::kBlockPages;
-    const int off0 = __ldg(p.off + t0);
-
-    // ---- query row of this thread (softmax warps: row = 32 (warp % 4) + lane,
-    // column part warp / 4 of kParts)
-    const int row = (warp & 3) * 32 + lane;
-    const int part = warp >> 2;
-    bool va = false;
-    int lo_a = 1, hi_a = 0;
-    size_t rh = 0;
-    if (warp < G::kSoftmaxWarps) {
-        const int qr = qbase + row;
-        if (qr < nqr) {
-            const int pr = qr / g, h = qr - pr * g;
-            prefill_window(p, t0 + pr, lo_a, hi_a);
-            rh = static_cast<size_t>(t0 + pr) * p.nh + kh * g + h;
-            va = true;
-        }
-    }
     if (warp == 0)
         tmem_alloc<G::kTmemCols>(smem_u32(tslot));
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tbase = *tslot;
-    if (warp < G::kSoftmaxWarps) {
-        // the row's Q -> tensor memory columns kQCol + [0, hd/2), 16 columns
-        // (32 elements) at a time, the parts taking turns
-        const uint4 *src = reinterpret_cast<const uint4 *>(p.q + rh * HD);
-        const uint32_t tq = tbase + (static_cast<uint32_t>((warp & 3) * 32) << 16) + G::kQCol;
-#pragma unroll 1
-        for (int c0 = part * 16; c0 < HD / 2; c0 += 16 * G::kParts) {
-            uint32_t r[16];
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                const uint4 v = va ? __ldg(src + c0 / 4 + k) : make_uint4(0u, 0u, 0u, 0u);
-                r[4 * k] = v.x;
-                r[4 * k + 1] = v.y;
-                r[4 * k + 2] = v.z;
-                r[4 * k + 3] = v.w;
-            }
-            tmem_st16(tq + c0, r);
-        }
-        tmem_wait_st();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0)
-            mbar_arrive(b_qready);
-    }
 
     if (warp == G::kSoftmaxWarps) {
-        // ------------------------------------------------ producer: blocks of 2 pages
+        // ------------------------------------------------ producer: blocks of 4 pages
         if (lane == 0) {
             tma_prefetch_map(&tm_k);
             tma_prefetch_map(&tm_v);
         }
-        const int32_t *tbl = p.block_table + off0 + p_first;
         bool ok = true;
-        for (int c0 = 0; c0 < npages; c0 += 32) {       // 32 is a multiple of the block's pages
-            int phys = 0;
-            if (c0 + lane < npages) {
-                phys = __ldg(tbl + c0 + lane);
-                if (p.page_map)
-                    phys = __ldg(p.page_map + phys);
-            }
-            const int nc = min(32, npages - c0);
-            for (int i = 0; i < nc; i += G::kBlockPages) {
-                const int j = (c0 + i) / G::kBlockPages;
-                const int np = min(G::kBlockPages, nc - i);
-                const int st = j % NST;
-                if (lane == 0 && ok && j >= NST)
-                    ok = mbar_wait_bounded(b_empty + 8 * st, ((j / NST) - 1) & 1, p.err, kErrTimeoutEmpty);
-                ok = __shfl_sync(0xffffffffu, ok, 0);
-                const uint32_t sK = s_base + G::kStageOff + st * G::kStageBytes;
-                const uint32_t sV = sK + G::kKBytes;
-                if (ok && lane == 0)
-                    mbar_arrive_expect_tx(b_full + 8 * st, np * 2 * kPage * HD * 2);
-                for (int pp = 0; pp < G::kBlockPages; ++pp) {
-                    const int ph = __shfl_sync(0xffffffffu, phys, (i + pp) & 31);
-                    if (ok && lane == 0 && pp < np) {
-                        const int t = ph * p.nkv + kh;
-#pragma unroll
-                        for (int c = 0; c < NCH; ++c)
-                            tma_load_3d(sK + c * (G::kBlockTokens * 128) + pp * (kPage * 128), &tm_k, b_full + 8 * st,
-                                        c * kBoxElems, 0, t);
-                        if (p.whole_tile_box) {
-                            tma_load_4d(sV + pp * G::kVPage, &tm_v, b_full + 8 * st, 0, 0, 0, t);
-                        } else {
+        int jg = 0;                                    // blocks issued, over all items
+        for (int it = blockIdx.x; it < nitems; it += gridDim.x) {
+            const TcItem I = tc_item<HD>(p, it, ntiles, lane, false);
+            if (!I.live || I.nblocks == 0)
+                continue;
+            const int32_t *tbl = p.block_table + I.off0 + I.p_first;
+            for (int c0 = 0; c0 < I.npages; c0 += 32) {       // 32 is a multiple of the block's pages
+                int phys = 0;
+                if (c0 + lane < I.npages) {
+                    phys = __ldg(tbl + c0 + lane);
+                    if (p.page_map)
+                        phys = __ldg(p.page_map + phys);
+                }
+                const int nc = min(32, I.npages - c0);
+                for (int i = 0; i < nc; i += G::kBlockPages, ++jg) {
+                    const int np = min(G::kBlockPages, nc - i);
+                    const int st = jg % NST;
+                    if (lane == 0 && ok && jg >= NST)
+                        ok = mbar_wait_bounded(b_empty + 8 * st, ((jg / NST) - 1) & 1, p.err, kErrTimeoutEmpty);
+                    ok = __shfl_sync(0xffffffffu, ok, 0);
+                    const uint32_t sK = s_base + G::kStageOff + st * G::kStageBytes;
+                    const uint32_t sV = sK + G::kKBytes;
+                    if (ok && lane == 0)
+                        mbar_arrive_expect_tx(b_full + 8 * st, np * 2 * kPage * HD * 2);
+                    for (int pp = 0; pp < G::kBlockPages; ++pp) {
+                        const int ph = __shfl_sync(0xffffffffu, phys, (i + pp) & 31);
+                        if (ok && lane == 0 && pp < np) {
+                            const int t = ph * p.nkv + I.kh;
 #pragma unroll
                             for (int c = 0; c < NCH; ++c)
-                                tma_load_3d(sV + pp * G::kVPage + c * (kPage * 128), &tm_v, b_full + 8 * st,
-                                            c * kBoxElems, 0, t);
+                                tma_load_3d(sK + c * (G::kBlockTokens * 128) + pp * (kPage * 128), &tm_k,
+                                            b_full + 8 * st, c * kBoxElems, 0, t);
+                            if (p.whole_tile_box) {
+                                tma_load_4d(sV + pp * G::kVPage, &tm_v, b_full + 8 * st, 0, 0, 0, t);
+                            } else {
+#pragma unroll
+                                for (int c = 0; c < NCH; ++c)
+                                    tma_load_3d(sV + pp * G::kVPage + c * (kPage * 128), &tm_v, b_full + 8 * st,
+                                                c * kBoxElems, 0, t);
+                            }
                         }
                     }
                 }
@@ -353,47 +350,61 @@ __global__ void __launch_bounds__(TcGeo<HD>::kThreads, 1)
         }
     } else if (warp == G::kSoftmaxWarps + 1) {
         // ------------------------------------------------ MMA issuer (one thread)
-        if (lane == 0) {
-            constexpr uint32_t kIdS = umma_idesc_bf16(128, G::kBlockTokens, 0, 0);
-            constexpr uint32_t kIdO = umma_idesc_bf16(128, HD, 0, 1);
-            bool ok = mbar_wait_bounded(b_qready, 0, p.err, kErrTimeoutFull);
-            tc_fence_after();
-            for (int j = 0; j <= nblocks; ++j) {
-                if (j < nblocks) {
-                    const int st = j % NST, b = j & 1;
-                    if (ok)
-                        ok = mbar_wait_bounded(b_full + 8 * st, (j / NST) & 1, p.err, kErrTimeoutFull);
-                    if (ok && j >= 2)
-                        ok = mbar_wait_bounded(b_sfree + 8 * b, ((j - 2) >> 1) & 1, p.err, kErrTimeoutFull);
-                    tc_fence_after();
-                    if (ok) {
-                        const uint32_t sK = s_base + G::kStageOff + st * G::kStageBytes;
+        constexpr uint32_t kIdS = umma_idesc_bf16(128, G::kBlockTokens, 0, 0);
+        constexpr uint32_t kIdO = umma_idesc_bf16(128, HD, 0, 1);
+        bool ok = true;
+        int jg = 0, kq = 0;                            // blocks and items with blocks, over all items
+        for (int it = blockIdx.x; it < nitems; it += gridDim.x) {
+            const TcItem I = tc_item<HD>(p, it, ntiles, lane, false);
+            if (!I.live || I.nblocks == 0)
+                continue;
+            if (lane == 0) {
+                if (ok)
+                    ok = mbar_wait_bounded(b_qready, kq & 1, p.err, kErrTimeoutFull);
+                tc_fence_after();
+                for (int j = 0; j <= I.nblocks; ++j) {
+                    if (j < I.nblocks) {
+                        const int jj = jg + j;
+                        const int st = jj % NST, b = jj & 1;
+                        if (ok)
+                            ok = mbar_wait_bounded(b_full + 8 * st, (jj / NST) & 1, p.err, kErrTimeoutFull);
+                        if (ok && jj >= 2)
+                            ok = mbar_wait_bounded(b_sfree + 8 * b, ((jj - 2) >> 1) & 1, p.err, kErrTimeoutFull);
+                        tc_fence_after();
+                        if (ok) {
+                            const uint32_t sK = s_base + G::kStageOff + st * G::kStageBytes;
 #pragma unroll
-                        for (int ks = 0; ks < HD / 16; ++ks) {
-                            const int c = ks >> 2, kk = ks & 3;
-                            umma_bf16_tmem_a(tbase + b * G::kBlockTokens, tbase + G::kQCol + ks * 8,
-                                             umma_sdesc(sK + c * (G::kBlockTokens * 128) + kk * 32, 16, 1024), kIdS,
-                                             ks > 0);
+                            for (int ks = 0; ks < HD / 16; ++ks) {
+                                const int c = ks >> 2, kk = ks & 3;
+                                umma_bf16_tmem_a(tbase + b * G::kBlockTokens, tbase + G::kQCol + ks * 8,
+                                                 umma_sdesc(sK + c * (G::kBlockTokens * 128) + kk * 32, 16, 1024),
+                                                 kIdS, ks > 0);
+                            }
                         }
+                        umma_commit(b_sfull + 8 * b);
                     }
-                    umma_commit(b_sfull + 8 * b);
-                }
-                if (j >= 1) {
-                    const int jj = j - 1, st = jj % NST;
-                    if (ok)
-                        ok = mbar_wait_bounded(b_pfull, jj & 1, p.err, kErrTimeoutFull);
-                    tc_fence_after();
-                    if (ok) {
-                        const uint32_t sV = s_base + G::kStageOff + st * G::kStageBytes + G::kKBytes;
-                        const int np = min(G::kBlockPages, npages - jj * G::kBlockPages);
-                        for (int pp = 0; pp < np; ++pp)
-                            umma_bf16(tbase + G::kOCol, umma_sdesc(sP + pp * 32, 16, 1024),
-                                      umma_sdesc(sV + pp * G::kVPage, kPage * 128, 1024), kIdO, jj > 0 || pp > 0);
+                    if (j >= 1) {
+                        const int jb = j - 1, jj = jg + jb, st = jj % NST;
+                        if (ok)
+                            ok = mbar_wait_bounded(b_pfull, jj & 1, p.err, kErrTimeoutFull);
+                        if (ok && jb == 0 && kq >= 1)      // the previous item's O has been read out
+                            ok = mbar_wait_bounded(b_ofree, (kq - 1) & 1, p.err, kErrTimeoutFull);
+                        tc_fence_after();
+                        if (ok) {
+                            const uint32_t sV = s_base + G::kStageOff + st * G::kStageBytes + G::kKBytes;
+                            const int np = min(G::kBlockPages, I.npages - jb * G::kBlockPages);
+                            for (int pp = 0; pp < np; ++pp)
+                                umma_bf16(tbase + G::kOCol, umma_sdesc(sP + pp * 32, 16, 1024),
+                                          umma_sdesc(sV + pp * G::kVPage, kPage * 128, 1024), kIdO, jb > 0 || pp > 0);
+                        }
+                        umma_commit(b_odone);
+                        umma_commit(b_empty + 8 * st);
                     }
-                    umma_commit(b_odone);
-                    umma_commit(b_empty + 8 * st);
                 }
             }
+            __syncwarp();
+            jg += I.nblocks;
+            ++kq;
         }
     } else {
         // ------------------------------------------------ softmax warps: kParts threads per query row
@@ -401,158 +412,236 @@ __global__ void __launch_bounds__(TcGeo<HD>::kThreads, 1)
         constexpr int HC = G::kBlockTokens / NP;           // columns of S per thread
         constexpr int HO = HD / NP;                        // columns of O per thread
         constexpr int kRs = HO >= 32 ? 32 : 16;            // O columns per rescale step
+        const int row = (warp & 3) * 32 + lane;            // query row of the item; TMEM lane
+        const int part = warp >> 2;                        // column part
         const uint32_t trow = tbase + (static_cast<uint32_t>((warp & 3) * 32) << 16);
         float *xmax = reinterpret_cast<float *>(smem + G::kXOff);          // [2][NP][128]
         float *xsum = xmax + 2 * NP * G::kRows;                             // [NP][128]
         const int pair_bar = 1 + (warp & 3);                               // warps w, w + 4, w + 8, ...
-        float m = -INFINITY, l = 0.f;
         bool ok = true;
-        for (int j = 0; j < nblocks; ++j) {
-            const int b = j & 1;
-            if (ok)
-                ok = mbar_wait_bounded(b_sfull + 8 * b, (j >> 1) & 1, p.err, kErrTimeoutFull);
-            tc_fence_after();
-            uint32_t sr[HC];
+        int jg = 0;
+
+        // the finish of an item: the row sum over the parts, O / l in bf16
+        // (this part's dims), then O is free for the next item
+        auto finish = [&](int last_jg, size_t frh, bool fva, float fl) {
+            xsum[part * G::kRows + row] = fl;
+            group_bar_sync(pair_bar, 32 * NP);
+            float lt = xsum[row];
 #pragma unroll
-            for (int q4 = 0; q4 < HC / 16; ++q4)
-                tmem_ld16(trow + b * G::kBlockTokens + part * HC + q4 * 16,
-                          *reinterpret_cast<uint32_t(*)[16]>(sr + q4 * 16));
-            tmem_wait_ld();
+            for (int k = 1; k < NP; ++k)
+                lt += xsum[k * G::kRows + row];
+            if (ok)
+                ok = mbar_wait_bounded(b_odone, last_jg & 1, p.err, kErrTimeoutFull);
+            tc_fence_after();
+#pragma unroll 1
+            for (int c0 = part * HO; c0 < (part + 1) * HO; c0 += 16) {
+                uint32_t r[16];
+                tmem_ld16(trow + G::kOCol + c0, r);
+                tmem_wait_ld();
+                if (fva) {
+                    uint32_t w[8];
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) {
+                        __nv_bfloat162 v;
+                        v.x = merge_finish(__uint_as_float(r[2 * k]), lt);
+                        v.y = merge_finish(__uint_as_float(r[2 * k + 1]), lt);
+                        w[k] = *reinterpret_cast<uint32_t *>(&v);
+                    }
+                    uint4 *dst = reinterpret_cast<uint4 *>(p.o + frh * HD + c0);
+                    dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+                    dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+                }
+            }
             tc_fence_before();
             __syncwarp();
             if (lane == 0)
-                mbar_arrive(b_sfree + 8 * b);
+                mbar_arrive(b_ofree);
+        };
 
-            const int tok0 = (p_first + j * G::kBlockPages) * kPage + part * HC;
-            // mask to the row's window; this part's max in four chains, then the row's
-            float x[HC];
-            float mq[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-            if (tok0 >= lo_a && tok0 + HC - 1 <= hi_a) {
-#pragma unroll
-                for (int c = 0; c < HC; ++c) {
-                    x[c] = __uint_as_float(sr[c]);
-                    mq[c & 3] = fmaxf(mq[c & 3], x[c]);
+        bool pend = false;          // an item whose O has not been read out yet
+        int pend_jg = 0;
+        size_t pend_rh = 0;
+        bool pend_va = false;
+        float pend_l = 0.f;
+        for (int it = blockIdx.x; it < nitems; it += gridDim.x) {
+            const TcItem I = tc_item<HD>(p, it, ntiles, lane, warp == 0);
+            if (!I.live)
+                continue;
+            bool va = false;
+            int lo_a = 1, hi_a = 0;
+            size_t rh = 0;
+            {
+                const int qr = I.qbase + row;
+                if (qr < I.tn * p.g) {
+                    const int pr = qr / p.g, h = qr - pr * p.g;
+                    prefill_window(p, I.t0 + pr, lo_a, hi_a);
+                    rh = static_cast<size_t>(I.t0 + pr) * p.nh + I.kh * p.g + h;
+                    va = true;
                 }
-            } else {
-#pragma unroll
-                for (int c = 0; c < HC; ++c) {
-                    const int t = tok0 + c;
-                    x[c] = (t >= lo_a && t <= hi_a) ? __uint_as_float(sr[c]) : -INFINITY;
-                    mq[c & 3] = fmaxf(mq[c & 3], x[c]);
+            }
+            if (I.nblocks == 0) {           // no position visible to any row: zeros
+                if (va) {
+                    for (int c0 = part * HO; c0 < (part + 1) * HO; c0 += 8)
+                        *reinterpret_cast<uint4 *>(p.o + rh * HD + c0) = make_uint4(0u, 0u, 0u, 0u);
                 }
+                continue;
             }
-            const float mh = fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3]));
-            xmax[(b * NP + part) * G::kRows + row] = mh;
-            group_bar_sync(pair_bar, 32 * NP);
-            float mr = mh;
-#pragma unroll
-            for (int k = 0; k < NP; ++k)
-                mr = fmaxf(mr, xmax[(b * NP + k) * G::kRows + row]);
-            const float mx = mr * kLog2e;   // log2 units
-            // stale-max rescale: keep m unless the block's max exceeds it by more than 8
-            float m_use = m, alpha = 1.f;
-            if (mx > m + 8.f || (m == -INFINITY && mx != -INFINITY)) {
-                m_use = mx;
-                alpha = (m == -INFINITY) ? 0.f : exp2f(m - mx);
-            }
-            const bool live = m_use != -INFINITY;
-            const float nm = live ? -m_use : 0.f;
-            float lq[4] = {0.f, 0.f, 0.f, 0.f};
-            uint32_t pk[HC / 2];
-#pragma unroll
-            for (int c = 0; c < HC; c += 2) {
-                // P rounded to bf16 once, by the pair conversion; the row sum
-                // takes the rounded values back out of the packed word
-                const float e0 = live ? ex2_sfu(__fmaf_rn(x[c], kLog2e, nm)) : 0.f;
-                const float e1 = live ? ex2_sfu(__fmaf_rn(x[c + 1], kLog2e, nm)) : 0.f;
-                const uint32_t w = pack_bf16x2(e0, e1);
-                pk[c / 2] = w;
-                lq[(c >> 1) & 3] += __uint_as_float(w << 16) + __uint_as_float(w & 0xffff0000u);
-            }
-            l = __fmaf_rn(l, alpha, (lq[0] + lq[1]) + (lq[2] + lq[3]));     // this part's share
-            m = m_use;
-
-            // O and the P buffer are free once the previous block's PV is done
-            if (j >= 1 && ok)
-                ok = mbar_wait_bounded(b_odone, (j - 1) & 1, p.err, kErrTimeoutFull);
-            tc_fence_after();
-            if (j >= 1 && __any_sync(0xffffffffu, alpha != 1.f)) {
+            // this item's Q -> tensor memory columns kQCol + [0, hd/2), 16 columns
+            // (32 elements) at a time, the parts taking turns; the previous
+            // item's S MMAs, the only readers of Q, are all complete
+            {
+                const uint4 *src = reinterpret_cast<const uint4 *>(p.q + rh * HD);
+                const uint32_t tq = trow + G::kQCol;
 #pragma unroll 1
-                for (int c0 = part * HO; c0 < (part + 1) * HO; c0 += kRs) {
-                    uint32_t ra[kRs / 16][16];
+                for (int c0 = part * 16; c0 < HD / 2; c0 += 16 * NP) {
+                    uint32_t r[16];
 #pragma unroll
-                    for (int h = 0; h < kRs / 16; ++h)
-                        tmem_ld16(trow + G::kOCol + c0 + 16 * h, ra[h]);
-                    tmem_wait_ld();
-#pragma unroll
-                    for (int h = 0; h < kRs / 16; ++h)
-#pragma unroll
-                        for (int k = 0; k < 16; ++k)
-                            ra[h][k] = __float_as_uint(__uint_as_float(ra[h][k]) * alpha);
-#pragma unroll
-                    for (int h = 0; h < kRs / 16; ++h)
-                        tmem_st16(trow + G::kOCol + c0 + 16 * h, ra[h]);
+                    for (int k = 0; k < 4; ++k) {
+                        const uint4 v = va ? __ldg(src + c0 / 4 + k) : make_uint4(0u, 0u, 0u, 0u);
+                        r[4 * k] = v.x;
+                        r[4 * k + 1] = v.y;
+                        r[4 * k + 2] = v.z;
+                        r[4 * k + 3] = v.w;
+                    }
+                    tmem_st16(tq + c0, r);
                 }
                 tmem_wait_st();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(b_qready);
             }
-            // this part of the P row -> shared memory, 128-byte swizzle
+            if (pend)
+                finish(pend_jg, pend_rh, pend_va, pend_l);
+
+            float m = -INFINITY, l = 0.f;
+            for (int j = 0; j < I.nblocks; ++j) {
+                const int jj = jg + j;
+                const int b = jj & 1;
+                if (ok)
+                    ok = mbar_wait_bounded(b_sfull + 8 * b, (jj >> 1) & 1, p.err, kErrTimeoutFull);
+                tc_fence_after();
+                uint32_t sr[HC];
 #pragma unroll
-            for (int w = 0; w < HC / 8; ++w) {
-                const int u = part * (HC / 8) + w;
-                *reinterpret_cast<uint4 *>(smem + G::kPOff + row * 128 + ((u ^ (row & 7)) << 4)) =
-                    make_uint4(pk[4 * w], pk[4 * w + 1], pk[4 * w + 2], pk[4 * w + 3]);
-            }
-            // V rows of tokens outside the union window may hold anything (NaN
-            // included) and P is 0 there: zero them before the PV MMA reads them
-            const int btok0 = (p_first + j * G::kBlockPages) * kPage;
-            if (btok0 < lo_u || btok0 + G::kBlockTokens - 1 > hi_u) {
-                const int st = j % NST;
-                uint8_t *sV = smem + G::kStageOff + st * G::kStageBytes + G::kKBytes;
-                const int np = min(G::kBlockPages, npages - j * G::kBlockPages);
-                for (int e = tid; e < np * kPage * NCH * 8; e += G::kSoftmaxWarps * 32) {
-                    const int u = e & 7, rc = e >> 3;
-                    const int c = rc % NCH, tk = rc / NCH;     // token of the block, chunk
-                    const int t = btok0 + tk;
-                    if (t < lo_u || t > hi_u)
-                        *reinterpret_cast<uint4 *>(sV + (tk >> 4) * G::kVPage + c * (kPage * 128) + (tk & 15) * 128 +
-                                                   u * 16) = make_uint4(0u, 0u, 0u, 0u);
+                for (int q4 = 0; q4 < HC / 16; ++q4)
+                    tmem_ld16(trow + b * G::kBlockTokens + part * HC + q4 * 16,
+                              *reinterpret_cast<uint32_t(*)[16]>(sr + q4 * 16));
+                tmem_wait_ld();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(b_sfree + 8 * b);
+
+                const int tok0 = (I.p_first + j * G::kBlockPages) * kPage + part * HC;
+                // mask to the row's window; this part's max in four chains, then the row's
+                float x[HC];
+                float mq[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+                if (tok0 >= lo_a && tok0 + HC - 1 <= hi_a) {
+#pragma unroll
+                    for (int c = 0; c < HC; ++c) {
+                        x[c] = __uint_as_float(sr[c]);
+                        mq[c & 3] = fmaxf(mq[c & 3], x[c]);
+                    }
+                } else {
+#pragma unroll
+                    for (int c = 0; c < HC; ++c) {
+                        const int t = tok0 + c;
+                        x[c] = (t >= lo_a && t <= hi_a) ? __uint_as_float(sr[c]) : -INFINITY;
+                        mq[c & 3] = fmaxf(mq[c & 3], x[c]);
+                    }
                 }
-            }
-            fence_async_shared();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0)
-                mbar_arrive(b_pfull);
-        }
-        // ---- finish: the row sum over the parts, O / l in bf16 (this part's dims)
-        xsum[part * G::kRows + row] = l;
-        group_bar_sync(pair_bar, 32 * NP);
-        float lt = xsum[row];
+                const float mh = fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3]));
+                xmax[(b * NP + part) * G::kRows + row] = mh;
+                group_bar_sync(pair_bar, 32 * NP);
+                float mr = mh;
 #pragma unroll
-        for (int k = 1; k < NP; ++k)
-            lt += xsum[k * G::kRows + row];
-        if (nblocks > 0 && ok)
-            ok = mbar_wait_bounded(b_odone, (nblocks - 1) & 1, p.err, kErrTimeoutFull);
-        tc_fence_after();
+                for (int k = 0; k < NP; ++k)
+                    mr = fmaxf(mr, xmax[(b * NP + k) * G::kRows + row]);
+                const float mx = mr * kLog2e;   // log2 units
+                // stale-max rescale: keep m unless the block's max exceeds it by more than 8
+                float m_use = m, alpha = 1.f;
+                if (mx > m + 8.f || (m == -INFINITY && mx != -INFINITY)) {
+                    m_use = mx;
+                    alpha = (m == -INFINITY) ? 0.f : exp2f(m - mx);
+                }
+                const bool live = m_use != -INFINITY;
+                const float nm = live ? -m_use : 0.f;
+                float lq[4] = {0.f, 0.f, 0.f, 0.f};
+                uint32_t pk[HC / 2];
+#pragma unroll
+                for (int c = 0; c < HC; c += 2) {
+                    // P rounded to bf16 once, by the pair conversion; the row sum
+                    // takes the rounded values back out of the packed word
+                    const float e0 = live ? ex2_sfu(__fmaf_rn(x[c], kLog2e, nm)) : 0.f;
+                    const float e1 = live ? ex2_sfu(__fmaf_rn(x[c + 1], kLog2e, nm)) : 0.f;
+                    const uint32_t w = pack_bf16x2(e0, e1);
+                    pk[c / 2] = w;
+                    lq[(c >> 1) & 3] += __uint_as_float(w << 16) + __uint_as_float(w & 0xffff0000u);
+                }
+                l = __fmaf_rn(l, alpha, (lq[0] + lq[1]) + (lq[2] + lq[3]));     // this part's share
+                m = m_use;
+
+                // O and the P buffer are free once the previous block's PV is done
+                if (j >= 1 && ok)
+                    ok = mbar_wait_bounded(b_odone, (jj - 1) & 1, p.err, kErrTimeoutFull);
+                tc_fence_after();
+                if (j >= 1 && __any_sync(0xffffffffu, alpha != 1.f)) {
 #pragma unroll 1
-        for (int c0 = part * HO; c0 < (part + 1) * HO; c0 += 16) {
-            uint32_t r[16];
-            tmem_ld16(trow + G::kOCol + c0, r);
-            tmem_wait_ld();
-            if (va) {
-                uint32_t w[8];
+                    for (int c0 = part * HO; c0 < (part + 1) * HO; c0 += kRs) {
+                        uint32_t ra[kRs / 16][16];
 #pragma unroll
-                for (int k = 0; k < 8; ++k) {
-                    __nv_bfloat162 v;
-                    v.x = nblocks > 0 ? merge_finish(__uint_as_float(r[2 * k]), lt) : __float2bfloat16_rn(0.f);
-                    v.y = nblocks > 0 ? merge_finish(__uint_as_float(r[2 * k + 1]), lt) : __float2bfloat16_rn(0.f);
-                    w[k] = *reinterpret_cast<uint32_t *>(&v);
+                        for (int h = 0; h < kRs / 16; ++h)
+                            tmem_ld16(trow + G::kOCol + c0 + 16 * h, ra[h]);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int h = 0; h < kRs / 16; ++h)
+#pragma unroll
+                            for (int k = 0; k < 16; ++k)
+                                ra[h][k] = __float_as_uint(__uint_as_float(ra[h][k]) * alpha);
+#pragma unroll
+                        for (int h = 0; h < kRs / 16; ++h)
+                            tmem_st16(trow + G::kOCol + c0 + 16 * h, ra[h]);
+                    }
+                    tmem_wait_st();
                 }
-                uint4 *dst = reinterpret_cast<uint4 *>(p.o + rh * HD + c0);
-                dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
-                dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+                // this part of the P row -> shared memory, 128-byte swizzle
+#pragma unroll
+                for (int w = 0; w < HC / 8; ++w) {
+                    const int u = part * (HC / 8) + w;
+                    *reinterpret_cast<uint4 *>(smem + G::kPOff + row * 128 + ((u ^ (row & 7)) << 4)) =
+                        make_uint4(pk[4 * w], pk[4 * w + 1], pk[4 * w + 2], pk[4 * w + 3]);
+                }
+                // V rows of tokens outside the union window may hold anything (NaN
+                // included) and P is 0 there: zero them before the PV MMA reads them
+                const int btok0 = (I.p_first + j * G::kBlockPages) * kPage;
+                if (btok0 < I.lo_u || btok0 + G::kBlockTokens - 1 > I.hi_u) {
+                    const int st = jj % NST;
+                    uint8_t *sV = smem + G::kStageOff + st * G::kStageBytes + G::kKBytes;
+                    const int np = min(G::kBlockPages, I.npages - j * G::kBlockPages);
+                    for (int e = tid; e < np * kPage * NCH * 8; e += G::kSoftmaxWarps * 32) {
+                        const int u = e & 7, rc = e >> 3;
+                        const int c = rc % NCH, tk = rc / NCH;     // token of the block, chunk
+                        const int t = btok0 + tk;
+                        if (t < I.lo_u || t > I.hi_u)
+                            *reinterpret_cast<uint4 *>(sV + (tk >> 4) * G::kVPage + c * (kPage * 128) +
+                                                       (tk & 15) * 128 + u * 16) = make_uint4(0u, 0u, 0u, 0u);
+                    }
+                }
+                fence_async_shared();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(b_pfull);
             }
+            pend = true;
+            pend_jg = jg + I.nblocks - 1;
+            pend_rh = rh;
+            pend_va = va;
+            pend_l = l;
+            jg += I.nblocks;
         }
+        if (pend)
+            finish(pend_jg, pend_rh, pend_va, pend_l);
     }
     tc_fence_before();
     __syncthreads();
@@ -575,13 +664,21 @@ cudaError_t launch_prefill_tc(const PrefillLaunchArgs &a, bool set_attr)
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(a.ntiles, a.p.nkv, (a.p.rows_per_tile * a.p.g + TcGeo<HD>::kRows - 1) / TcGeo<HD>::kRows);
+    const int nchunks = (a.p.rows_per_tile * a.p.g + TcGeo<HD>::kRows - 1) / TcGeo<HD>::kRows;
+    const long long items = static_cast<long long>(a.ntiles) * a.p.nkv * nchunks;
+    if (items > INT_MAX)
+        return cudaErrorInvalidValue;
+    // one CTA per item while they fit in about two waves (the hardware then
+    // hands the second wave to the first SMs free); persistent, one CTA per
+    // SM, beyond that
+    const int sms = a.num_sms > 0 ? a.num_sms : 1;
+    cfg.gridDim = dim3(static_cast<unsigned>(items <= 2ll * sms ? items : sms));
     cfg.blockDim = dim3(TcGeo<HD>::kThreads);
     cfg.dynamicSmemBytes = TcGeo<HD>::kAlloc;
     cfg.stream = a.stream;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, prefill_tc_kernel<HD>, *a.tm_k, *a.tm_v, a.p);
+    return cudaLaunchKernelEx(&cfg, prefill_tc_kernel<HD>, *a.tm_k, *a.tm_v, a.p, a.ntiles, nchunks);
 }
 
 }  // namespace pgqa
