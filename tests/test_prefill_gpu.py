@@ -91,6 +91,54 @@ def test_several_sequences_and_a_continuation(window):
     prefill_gates(multi_sequence_case(window=window), mapped=False)
 
 
+def many_sequence_case(lens, nh, nkv, hd, window, seed):
+    """Sequences given as (rows, first position) in one call, each through its own span
+    of one permuted block table."""
+    rng = wl.Lcg(seed)
+    spans = [(p0 + r + 15) // 16 for r, p0 in lens]
+    npages = sum(spans) + 1
+    n = npages * nkv * 16 * hd
+    k = wl.draw_bf16(rng, n, "sym")
+    v = wl.draw_bf16(rng, n, "sym")
+    bt = wl.lcg_permutation(npages, seed + 1)[:sum(spans)].astype(np.int32)
+    starts = np.cumsum([0] + spans[:-1])
+    off = np.concatenate([np.full(r, o, np.int32) for (r, _), o in zip(lens, starts)])
+    qpos = np.concatenate([np.arange(p0, p0 + r, dtype=np.int32) for r, p0 in lens])
+    rows = len(qpos)
+    q = wl.draw_bf16(rng, rows * nh * hd, "sym")
+    return wl.Case(f"prefill_{len(lens)}seq_nh{nh}_nkv{nkv}_hd{hd}_w{window}", nh, nkv, hd, window, rows, q, k, v,
+                   bt, off, qpos, ctx=int(max(p0 + r for r, p0 in lens)), npg=npages)
+
+
+@pytest.mark.parametrize("hd,nh,nkv,window", [(64, 16, 16, 0), (128, 32, 16, 300), (256, 16, 8, 700)])
+def test_persistent_grid_many_items(hd, nh, nkv, window):
+    """More (tile, kv head, chunk) items than two per SM: each CTA serves several items
+    in turn, its ring, S buffers and barriers running across them.  Four sequences --
+    a 1-row prompt (an empty second chunk) and a continuation at position 300 among
+    them -- give ragged tiles."""
+    import torch
+    from gpu_util import PrefillDev
+    c = many_sequence_case([(1500, 0), (1, 0), (900, 300), (1700, 0)], nh, nkv, hd, window, seed=hd + window)
+    d = PrefillDev(c)
+    chunks = (pgqa_rows_per_tile(hd) * (nh // nkv) + 127) // 128
+    items = d.ntiles * nkv * chunks
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    assert items > 2 * sms, f"{items} items do not reach the persistent grid on {sms} SMs"
+    prefill_gates(c)
+
+
+def pgqa_rows_per_tile(hd):
+    import paged_gqa_decode_attn_gb300 as pgqa
+    return pgqa.prefill_rows_per_tile(hd)
+
+
+def test_prefill_long_full_size():
+    """The benchmark's workload in its launch configuration: 8192 rows, nh16 nkv8 hd256,
+    window 1024 (1024 items on the persistent grid), every element against the oracle,
+    and the page-map gate."""
+    prefill_gates(wl.prefill_long())
+
+
 def test_kvpos_below_qpos_and_an_empty_row():
     """Rows that see only up to kvpos < qpos, and one row whose window holds nothing."""
     c = wl.prefill_case(8, 2, 256, 20, 90, dist="sym", seed=5)

@@ -132,6 +132,12 @@ def test_several_sequences_by_offset():
     check(dataclasses.replace(c, block_table=bt, off=off, npg=2 * c.npg))
 
 
+def test_prep_long_full_size():
+    """The benchmark's workload in its launch configuration: 8192 rows, nh16 nkv8 hd256,
+    full rotation (many items per persistent CTA), every element and every pool slot."""
+    check(wl.prep_long())
+
+
 def test_zero_rows_is_a_no_op():
     import torch
     import paged_gqa_decode_attn_gb300 as pgqa
