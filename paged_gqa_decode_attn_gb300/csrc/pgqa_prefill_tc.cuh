@@ -183,15 +183,18 @@ struct TcItem {
 };
 
 template <int HD>
-__device__ __forceinline__ TcItem tc_item(const PrefillParams &p, int it, int ntiles, int lane, bool report)
+__device__ __forceinline__ TcItem tc_item(const PrefillParams &p, int it, int ntiles, int nchunks, int lane,
+                                          bool report)
 {
     using G = TcGeo<HD>;
     TcItem I;
-    const int tr = it % ntiles;
-    const int rest = it / ntiles;
-    I.kh = rest % p.nkv;
-    const int chunk = rest / p.nkv;
-    const int tile = ntiles - 1 - tr;          // last tiles first: they hold the longest windows
+    // tiles outermost, last tiles first (they hold the longest windows), then
+    // kv head, then chunk
+    const int per_tile = p.nkv * nchunks;
+    const int tile = ntiles - 1 - it / per_tile;
+    const int rest = it - (it / per_tile) * per_tile;
+    I.kh = rest / nchunks;
+    const int chunk = rest - I.kh * nchunks;
     I.t0 = __ldg(p.tile_t0 + tile);
     I.tn = __ldg(p.tile_tn + tile);
     I.qbase = chunk * G::kRows;
@@ -239,8 +242,9 @@ __device__ __forceinline__ TcItem tc_item(const PrefillParams &p, int it, int nt
     return I;
 }
 
-// Persistent: CTA c serves items c, c + gridDim.x, ... of the ntiles * nkv *
-// nchunks items.  The ring, the S buffers and the mbarrier phases run on
+// Persistent: in round k CTA c serves item k G + c (k even) or k G + G - 1 - c
+// (k odd) of the ntiles * nkv * nchunks items, G = gridDim.x: with the items
+// in roughly falling size, the snake pairs long items with short ones.  The ring, the S buffers and the mbarrier phases run on
 // counters that continue across items, so the next item's K/V stream in
 // while the current one finishes, and its Q goes into tensor memory (after
 // the current item's last S) before the current item's O is read out.
@@ -271,6 +275,18 @@ __global__ void __launch_bounds__(TcGeo<HD>::kThreads, 1)
     const int warp = tid >> 5;
     const int lane = tid & 31;
     const int nitems = ntiles * p.nkv * nchunks;
+    const int ncta = gridDim.x;
+    const int cta = blockIdx.x;
+    auto first_item = [&](int) { return cta < nitems ? cta : nitems; };
+    // the item after `it` (round k = it / ncta) for this CTA, or nitems
+    auto next_item = [&](int it) {
+        for (int k = it / ncta + 1; k * ncta < nitems; ++k) {
+            const int n = k * ncta + ((k & 1) ? ncta - 1 - cta : cta);
+            if (n < nitems)
+                return n;
+        }
+        return nitems;
+    };
 
     if (tid == 0) {
         for (int s = 0; s < NST; ++s) {
@@ -304,8 +320,8 @@ __global__ void __launch_bounds__(TcGeo<HD>::kThreads, 1)
         }
         bool ok = true;
         int jg = 0;                                    // blocks issued, over all items
-        for (int it = blockIdx.x; it < nitems; it += gridDim.x) {
-            const TcItem I = tc_item<HD>(p, it, ntiles, lane, false);
+        for (int it = first_item(0); it < nitems; it = next_item(it)) {
+            const TcItem I = tc_item<HD>(p, it, ntiles, nchunks, lane, false);
             if (!I.live || I.nblocks == 0)
                 continue;
             const int32_t *tbl = p.block_table + I.off0 + I.p_first;
@@ -354,8 +370,8 @@ __global__ void __launch_bounds__(TcGeo<HD>::kThreads, 1)
         constexpr uint32_t kIdO = umma_idesc_bf16(128, HD, 0, 1);
         bool ok = true;
         int jg = 0, kq = 0;                            // blocks and items with blocks, over all items
-        for (int it = blockIdx.x; it < nitems; it += gridDim.x) {
-            const TcItem I = tc_item<HD>(p, it, ntiles, lane, false);
+        for (int it = first_item(0); it < nitems; it = next_item(it)) {
+            const TcItem I = tc_item<HD>(p, it, ntiles, nchunks, lane, false);
             if (!I.live || I.nblocks == 0)
                 continue;
             if (lane == 0) {
@@ -463,8 +479,8 @@ __global__ void __launch_bounds__(TcGeo<HD>::kThreads, 1)
         size_t pend_rh = 0;
         bool pend_va = false;
         float pend_l = 0.f;
-        for (int it = blockIdx.x; it < nitems; it += gridDim.x) {
-            const TcItem I = tc_item<HD>(p, it, ntiles, lane, warp == 0);
+        for (int it = first_item(0); it < nitems; it = next_item(it)) {
+            const TcItem I = tc_item<HD>(p, it, ntiles, nchunks, lane, warp == 0);
             if (!I.live)
                 continue;
             bool va = false;
