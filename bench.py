@@ -778,6 +778,117 @@ def run_prep(args, case, rank, world, dist):
     return 0
 
 
+def sweep_bytes(hd, ctx, rows, window, nh=32, nkv=16):
+    """Algorithmic bytes of one sweep call: the union window's K/V once, Q and O."""
+    q0 = ctx - rows
+    lo = max(0, q0 + 1 - window) if window > 0 else 0
+    return (ctx - lo) * nkv * hd * 2 * 2 + 2 * rows * nh * hd * 2
+
+
+def run_sweep(args, rank, world, dist):
+    """Every point of the decode sweep (nh32 nkv16; hd x ctx x rows x window =
+    3 x 4 x 3 x 3 = 108 points): rows at the last positions of one sequence, its
+    pages in a seeded permuted order.  Each point is timed with CUDA events around
+    a graph of back-to-back calls over rotating pool copies; ``value`` is the
+    geometric mean of the points' KV GB/s.  Pools are drawn once per (hd, ctx) on
+    the device from a seeded generator (a timing run: the sweep's parity is the
+    decode tests' business), so this line carries no end-to-end number."""
+    import torch
+    import paged_gqa_decode_attn_gb300 as pgqa
+
+    torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
+    dev = torch.device("cuda")
+    if rank == 0:
+        pgqa.build()
+    barrier(dist)
+    pgqa.load()
+    nh, nkv = 32, 16
+    total_mem = torch.cuda.get_device_properties(dev).total_memory
+    results = []
+    sampler = ClockSampler(torch.cuda.current_device()) if not args.no_clocks else None
+    t_all0 = time.perf_counter()
+    for hd in wl.SWEEP_HD:
+        for ctx in wl.SWEEP_CTX:
+            npages = (ctx + 15) // 16
+            pool_elems = npages * nkv * 16 * hd
+            gen = torch.Generator(device=dev)
+            gen.manual_seed(12345 + hd + ctx)
+            pool_bytes = 2 * pool_elems * 2
+            copies = max(2, math.ceil(3 * L2_BYTES / pool_bytes))
+            copies = min(copies, 16, max(2, int(0.25 * total_mem // pool_bytes)))
+            ks = [torch.randn(pool_elems, generator=gen, device=dev, dtype=torch.float32).to(torch.bfloat16)
+                  for _ in range(copies)]
+            vs = [torch.randn(pool_elems, generator=gen, device=dev, dtype=torch.float32).to(torch.bfloat16)
+                  for _ in range(copies)]
+            bt = torch.from_numpy(wl.lcg_permutation(npages, hd + ctx).astype(np.int32)).to(dev)
+            for rows in wl.SWEEP_ROWS:
+                for window in wl.SWEEP_WINDOW:
+                    q = torch.randn(rows * nh * hd, generator=gen, device=dev).to(torch.bfloat16)
+                    qpos = torch.arange(ctx - rows, ctx, dtype=torch.int32, device=dev)
+                    off = torch.zeros(rows, dtype=torch.int32, device=dev)
+                    kv_eff = min(ctx, window) if window > 0 else ctx
+                    splits = pgqa.choose_splits(kv_eff, rows, nkv, 1)
+                    part = torch.empty(max(1, pgqa.decode_part_bytes(rows, nh, splits, hd)) // 4 + 4,
+                                       dtype=torch.float32, device=dev)
+                    cnt = torch.zeros(max(1, pgqa.decode_counter_count(rows, nh, nkv)), dtype=torch.int32,
+                                      device=dev)
+                    o = torch.empty(rows * nh * hd, dtype=torch.bfloat16, device=dev)
+                    bpc = sweep_bytes(hd, ctx, rows, window, nh, nkv)
+
+                    def call(i):
+                        pgqa.attn_decode(o, part, q, ks[i % copies], vs[i % copies], bt, off, qpos, None, rows, nh,
+                                         nkv, hd, window, splits, cnt, None)
+
+                    for i in range(3):
+                        call(i)
+                    torch.cuda.synchronize()
+                    n = int(min(400, max(20, 2e-3 / max(bpc / 6e12, 5e-6))))
+                    g = torch.cuda.CUDAGraph()
+                    with torch.cuda.graph(g):
+                        for i in range(n):
+                            call(i)
+                    g.replay()
+                    torch.cuda.synchronize()
+                    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                    ev0.record()
+                    g.replay()
+                    ev1.record()
+                    ev1.synchronize()
+                    us = ev0.elapsed_time(ev1) * 1e3 / n
+                    results.append({"hd": hd, "ctx": ctx, "rows": rows, "window": window, "splits": splits,
+                                    "us": round(us, 3), "gbs": round(bpc / (us * 1e-6) / 1e9, 1),
+                                    "bytes": bpc})
+                    del g
+            del ks, vs
+            torch.cuda.empty_cache()
+    clocks = sampler.stop() if sampler else None
+    if rank != 0:
+        return 0
+    peak, peak_kind = measured_peaks()
+    gm = math.exp(sum(math.log(r["gbs"]) for r in results) / len(results))
+    by = sorted(results, key=lambda r: r["gbs"])
+    if args.sweep_out:
+        with open(args.sweep_out, "w") as f:
+            json.dump(results, f, indent=0)
+    line = {
+        "metric": "paged decode attention KV GB/s, geometric mean over the sweep", "value": round(gm, 1),
+        "unit": "GB/s", "n_gpus": world, "steps": len(results), "warmup": 3,
+        "ms_per_step": round(sum(r["us"] for r in results) / len(results) / 1e3, 6), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic (device-drawn Gaussian pools)",
+        "config": {"workload": "sweep_nh32_nkv16", "points": len(results),
+                   "grid": "hd {128,256,512} x ctx {1K,4K,16K,64K} x rows {1,4,16} x window {0,1024,4096}",
+                   "worst": by[:3], "best": by[-3:], "seconds": round(time.perf_counter() - t_all0, 1),
+                   "l2": "rotating pool copies per (hd, ctx)",
+                   "timing": "per point: CUDA events around a graph of 20-400 back-to-back calls"},
+        "roofline": {"bound": "hbm", "achieved": round(gm, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(gm / peak, 4), "traffic": None, "peak_kind": peak_kind,
+                     "kernel": "decode_split_kernel (geometric mean over the points)"},
+        "cpu_baseline": None, "e2e": None, "gpu_launches": sum(1 for _ in results), "clocks": clocks,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
@@ -786,7 +897,7 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="sliding",
                     choices=["sliding", "sliding_mapped", "tiny", "long", "batched", "prefill_page", "prefill_long",
-                             "prep_long"])
+                             "prep_long", "sweep"])
     ap.add_argument("--splits", type=int, default=0, help="override choose_splits")
     ap.add_argument("--merge", choices=["counters", "combine"], default="counters")
     ap.add_argument("--graph-chunk", type=int, default=2000)
@@ -797,12 +908,24 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-check", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
+    ap.add_argument("--sweep-out", default="", help="--workload sweep: write every point's numbers here (JSON)")
     args = ap.parse_args(argv)
     if args.steps < 1 or args.warmup < 0:
         raise SystemExit("--steps >= 1 and --warmup >= 0")
     rank, world, _ = dist_env()
     if args.impl == "reference" and rank != 0:
         return 0            # the reference arm runs on rank 0 alone
+    if args.workload == "sweep":
+        if args.impl == "reference":
+            print(json.dumps({"impl": "reference", "unavailable": "the sweep is a device timing of every point; "
+                              "the oracle baseline is reported on the single workloads"}), flush=True)
+            return 0
+        dist = init_dist(world)
+        try:
+            return run_sweep(args, rank, world, dist)
+        finally:
+            if dist is not None:
+                dist.destroy_process_group()
     case = build_case(args.workload)
     if args.impl == "reference":
         return run_reference(args, case, rank, world)

@@ -33,8 +33,13 @@ struct DeviceState {
 };
 
 // Cluster size for the on-chip merge of `splits` CTAs, or 0 to merge through
-// global memory.  Caller holds g_mutex.
-int on_chip_cluster(DeviceState *s, int hi, int hd, int splits)
+// global memory.  Clusters of 2 and 4 are taken whenever any fit (the short
+// loops that choose them measured faster so than through the last CTA, even
+// with a second wave); clusters of 8 only when all `live` ones (one per tile
+// that does work) are resident at once: the split rule picks 8 beside fewer
+// resident clusters only for long loops, where a waiting cluster would
+// double its tile's time.  Caller holds g_mutex.
+int on_chip_cluster(DeviceState *s, int hi, int hd, int splits, long long live)
 {
     int lg = -1;
     switch (splits) {
@@ -53,7 +58,7 @@ int on_chip_cluster(DeviceState *s, int hi, int hd, int splits)
         default: cap = pgqa::cluster_capacity_hd512(splits); break;
         }
     }
-    return cap >= 1 ? splits : 0;
+    return cap >= 1 && (splits <= 4 || cap >= live) ? splits : 0;
 }
 
 std::mutex g_mutex;
@@ -294,7 +299,11 @@ int choose_splits_rule(int kv_len_eff, int rows, int nkv, int nseq, int num_sms,
     // Up to 24 splits, take a power of two no larger than 8: 2, 4 and 8
     // splits merge on chip, in one thread-block cluster per tile.  Prefer the
     // largest such size whose clusters, one per tile, are all resident at
-    // once; if none is, the largest power of two.
+    // once; if none is, the largest power of two.  When the size that fits is
+    // smaller than wanted and a split's loop is long, the wanted count wins
+    // instead, merged by the last CTA in one level (a few microseconds more
+    // than on chip, about kMergePages pages of one CTA's loop) -- the launch
+    // takes the on-chip merge only where all clusters are resident.
     if (s <= 24) {
         long long p2 = 1;
         while (p2 * 2 <= s && p2 < 8)
@@ -305,7 +314,14 @@ int choose_splits_rule(int kv_len_eff, int rows, int nkv, int nseq, int num_sms,
             if (res >= tiles)
                 fit = 1LL << lg;
         }
-        s = fit > 1 ? fit : p2;
+        // (only while the grid stays one wave even unpacked: how many rows a
+        // CTA packs depends on the group size, which this rule is not given)
+        constexpr long long kMergePages = 16;
+        if (fit > 1 && fit < p2 && pages / fit - pages / p2 > kMergePages &&
+            static_cast<long long>(rows) * nkv * p2 <= num_sms)
+            s = p2;
+        else
+            s = fit > 1 ? fit : p2;
     }
     if (s > PGQA_MAX_SPLITS)
         s = PGQA_MAX_SPLITS;
@@ -438,7 +454,10 @@ int pgqa_attn_decode(void *o, void *part, const void *q, const void *k_pool, con
         return PGQA_ERR_TENSOR_MAP;
     p.whole_tile_box = whole_k;
     p.err = s->err;
-    p.cluster = counters ? on_chip_cluster(s, hi, hd, splits) : 0;
+    // tiles that do work: one per packing group of rows (the rows of a group
+    // that is packed leave at once), kv head and head subgroup
+    const long long live = static_cast<long long>((rows + p.pack - 1) / p.pack) * nkv * hsg;
+    p.cluster = counters ? on_chip_cluster(s, hi, hd, splits, live) : 0;
     if (g_trace && static_cast<size_t>(splits) * nkv * hsg * rows * pgqa::kTraceEvents * 8 <= g_trace_bytes)
         p.trace = g_trace;
     a.tm_k = &tk;

@@ -85,14 +85,25 @@ def test_choose_splits_rule(lib):
     assert pgqa.choose_splits(32768, 1, 4, 1, num_sms=152) == 38
     assert pgqa.choose_splits(4096, 64, 8, 64, num_sms=152) == 2
     # up to 24 the count is a power of two of at most 8 (on-chip merge), above it is not rounded
+    # GB300 residency: 76 clusters of 2, 36 of 4, 15 of 8.  A count whose clusters
+    # are not all resident (merged by the last CTA instead) is taken only when a
+    # smaller resident cluster would leave each CTA more than 16 pages longer.
+    res = {2: 76, 4: 36, 8: 15}
     for kv in (256, 1024, 4096, 1 << 16):
+        pages = (kv + 15) // 16
         for tiles in range(1, 160):
             s = pgqa.choose_splits(kv, tiles, 1, tiles, num_sms=152)
             assert s > 24 or (s in (1, 2, 4, 8))
-            if s in (2, 4, 8) and tiles <= 76:      # GB300 residency: 76 clusters of 2, 36 of 4, 15 of 8
-                assert {2: 76, 4: 36, 8: 15}[s] >= tiles, (kv, tiles, s)
+            if s in (2, 4, 8) and tiles <= 76 and res[s] < tiles:
+                fit = max([c for c in (2, 4) if c < s and res[c] >= tiles], default=0)
+                assert fit and pages // fit - pages // s > 16 and tiles * s <= 152, (kv, tiles, s)
     assert pgqa.choose_splits(1 << 16, 15, 1, 15, num_sms=152) == 8
-    assert pgqa.choose_splits(1 << 16, 16, 1, 16, num_sms=152) == 4     # 16 clusters of 8 would take 2 waves
+    # 16 clusters of 8 would take 2 waves: on chip, 4 splits; the 4096-page loop
+    # makes 8 splits merged by the last CTA worth it (128 CTAs: one wave)
+    assert pgqa.choose_splits(1 << 16, 16, 1, 16, num_sms=152) == 8
+    assert pgqa.choose_splits(1 << 16, 1, 16, 1, num_sms=152) == 8      # one row, 16 kv heads
+    assert pgqa.choose_splits(1024, 16, 1, 16, num_sms=152) == 4       # 64 pages: the short loop stays on chip
+    assert pgqa.choose_splits(1 << 16, 16, 16, 1, num_sms=152) == 4    # 16 rows: unpacked, 8 splits need 13 waves
     # nseq outside [1, rows] means every row is its own sequence
     assert pgqa.choose_splits(1024, 4, 8, 0, num_sms=152) == pgqa.choose_splits(1024, 4, 8, 4, num_sms=152)
     # without a device the current-device form falls back to 152 SMs
