@@ -202,6 +202,29 @@ int pgqa_attn_prefill(void *o, const void *q, const void *k_pool, const void *v_
                       const int32_t *kvpos, const int32_t *tile_t0, const int32_t *tile_tn, int ntiles,
                       int nh, int nkv, int hd, int window, const int32_t *page_map, void *stream);
 
+/*
+ * pgqa_attn_prefill with split-KV, for tiles whose rows share a long context:
+ * chunked prefill, or the multi-token decode of one sequence (speculative
+ * verification), whose rows are many query rows per kv head -- more than the
+ * 8 that pgqa_attn_decode packs into one CTA.  Each (tile chunk, kv head) work
+ * item of the tcgen05 kernel is cut into `splits` page ranges of its window;
+ * each writes an unnormalised partial (as pgqa_attn_decode's scratch holds
+ * them) and the decode combine kernel merges them into o.  The result is the
+ * same attention as pgqa_attn_prefill's (equal within the page's gate: the
+ * sums run in another order).
+ *   part   device scratch of at least pgqa_decode_part_bytes(rows, nh, splits, hd)
+ *          bytes, 16-byte aligned, caller-owned (not read before written)
+ *   rows   the number of rows; every row must be in exactly one tile
+ *   splits 1..PGQA_MAX_SPLITS; 1 is pgqa_attn_prefill (part unused)
+ * Other arguments as for pgqa_attn_prefill.  hd 64, 128 or 256 for splits > 1
+ * (PGQA_ERR_UNSUPPORTED_HD otherwise).  Asynchronous on `stream`; two kernels.
+ */
+int pgqa_attn_prefill_split(void *o, void *part, const void *q, const void *k_pool, const void *v_pool,
+                            const int32_t *block_table, const int32_t *off, const int32_t *qpos,
+                            const int32_t *kvpos, const int32_t *tile_t0, const int32_t *tile_tn, int ntiles,
+                            int rows, int nh, int nkv, int hd, int window, int splits, const int32_t *page_map,
+                            void *stream);
+
 /* The longest tile pgqa_attn_prefill takes at head dimension hd (64 rows;
  * 32 at hd 512), or PGQA_ERR_UNSUPPORTED_HD. */
 int pgqa_prefill_rows_per_tile(int hd);

@@ -37,6 +37,8 @@ SIGNATURES = {
     "pgqa_trace_buffer": (_I, [_P, ctypes.c_size_t]),
     "pgqa_attn_decode_noalloc": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P]),
     "pgqa_attn_prefill": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P]),
+    "pgqa_attn_prefill_split": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I,
+                                     _P, _P]),
     "pgqa_prefill_rows_per_tile": (_I, [_I]),
     "pgqa_make_tiles": (_I, [_P, _I, _I, _P, _P, _I]),
     "pgqa_qk_norm_rope_write": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I,
@@ -130,6 +132,19 @@ def attn_prefill(o, q, k_pool, v_pool, block_table, off, qpos, kvpos, tile_t0, t
                                   int(nkv), int(hd), int(window), _ptr(page_map), _stream(stream))
     if st != PGQA_OK:
         raise PgqaError(st, "attn_prefill")
+
+
+def attn_prefill_split(o, part, q, k_pool, v_pool, block_table, off, qpos, kvpos, tile_t0, tile_tn, ntiles: int,
+                       rows: int, nh: int, nkv: int, hd: int, window: int, splits: int, page_map=None,
+                       stream=None) -> None:
+    """Split-KV tiled attention (``pgqa_attn_prefill_split``): partials in ``part``
+    (``decode_part_bytes(rows, nh, splits, hd)`` bytes), merged into ``o``."""
+    st = load().pgqa_attn_prefill_split(_ptr(o), _ptr(part), _ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(block_table),
+                                        _ptr(off), _ptr(qpos), _ptr(kvpos), _ptr(tile_t0), _ptr(tile_tn),
+                                        int(ntiles), int(rows), int(nh), int(nkv), int(hd), int(window),
+                                        int(splits), _ptr(page_map), _stream(stream))
+    if st != PGQA_OK:
+        raise PgqaError(st, "attn_prefill_split")
 
 
 def prefill_rows_per_tile(hd: int) -> int:

@@ -520,20 +520,30 @@ int pgqa_make_tiles(const int32_t *seq, int rows, int rows_per_tile, int32_t *ti
     return n;
 }
 
-int pgqa_attn_prefill(void *o, const void *q, const void *k_pool, const void *v_pool, const int32_t *block_table,
-                      const int32_t *off, const int32_t *qpos, const int32_t *kvpos, const int32_t *tile_t0,
-                      const int32_t *tile_tn, int ntiles, int nh, int nkv, int hd, int window,
-                      const int32_t *page_map, void *stream)
+namespace {
+
+// pgqa_attn_prefill and, with splits > 1, pgqa_attn_prefill_split: the tiled
+// kernel, then (split) the decode combine kernel over the rows' partials.
+int prefill_call(void *o, void *part, const void *q, const void *k_pool, const void *v_pool,
+                 const int32_t *block_table, const int32_t *off, const int32_t *qpos, const int32_t *kvpos,
+                 const int32_t *tile_t0, const int32_t *tile_tn, int ntiles, int rows, int nh, int nkv, int hd,
+                 int window, int splits, const int32_t *page_map, void *stream)
 {
-    if (ntiles < 0 || nh <= 0 || nkv <= 0 || nh % nkv != 0 || window < 0)
+    if (ntiles < 0 || nh <= 0 || nkv <= 0 || nh % nkv != 0 || window < 0 || splits < 1)
         return PGQA_ERR_INVALID_ARGUMENT;
+    if (splits > PGQA_MAX_SPLITS)
+        return PGQA_ERR_TOO_MANY_SPLITS;
     const int hi = hd_index(hd);
-    if (hi < 0)
+    if (hi < 0 || (splits > 1 && hd > 256))
         return PGQA_ERR_UNSUPPORTED_HD;
     if (ntiles == 0)
         return PGQA_OK;
     if (!o || !q || !k_pool || !v_pool || !block_table || !off || !qpos || !tile_t0 || !tile_tn)
         return PGQA_ERR_INVALID_ARGUMENT;
+    if (splits > 1 && (!part || rows < 1))
+        return PGQA_ERR_INVALID_ARGUMENT;
+    if (splits > 1 && !aligned(part, 16))
+        return PGQA_ERR_MISALIGNED;
     const int g = nh / nkv;
     const int rpt = pgqa_prefill_rows_per_tile(hd);
     const int qr = hd == 512 ? pgqa::PfGeo<512>::kQueryRows : 128;     // query rows per CTA
@@ -558,6 +568,11 @@ int pgqa_attn_prefill(void *o, const void *q, const void *k_pool, const void *v_
     p.g = g;
     p.window = window;
     p.rows_per_tile = rpt;
+    p.splits = splits;
+    p.part_o = splits > 1 ? static_cast<float *>(part) : nullptr;
+    p.part_ml = splits > 1 ? reinterpret_cast<float2 *>(static_cast<char *>(part) +
+                                                        static_cast<size_t>(rows) * nh * splits * hd * 4)
+                           : nullptr;
     a.ntiles = ntiles;
     a.stream = static_cast<cudaStream_t>(stream);
 
@@ -593,5 +608,45 @@ int pgqa_attn_prefill(void *o, const void *q, const void *k_pool, const void *v_
     if (e != cudaSuccess)
         return PGQA_ERR_CUDA;
     s->prefill_attr_set[hi] = true;
+    if (splits > 1) {
+        pgqa::DecodeParams c;
+        std::memset(&c, 0, sizeof c);
+        c.o = p.o;
+        c.part_o = p.part_o;
+        c.part_ml = p.part_ml;
+        c.rows = rows;
+        c.nh = nh;
+        c.nkv = nkv;
+        c.splits = splits;
+        c.err = s->err;
+        switch (hd) {
+        case 64: e = pgqa::launch_combine_hd64(c, a.stream); break;
+        case 128: e = pgqa::launch_combine_hd128(c, a.stream); break;
+        default: e = pgqa::launch_combine_hd256(c, a.stream); break;
+        }
+        if (e != cudaSuccess)
+            return PGQA_ERR_CUDA;
+    }
     return PGQA_OK;
+}
+
+}  // namespace
+
+int pgqa_attn_prefill(void *o, const void *q, const void *k_pool, const void *v_pool, const int32_t *block_table,
+                      const int32_t *off, const int32_t *qpos, const int32_t *kvpos, const int32_t *tile_t0,
+                      const int32_t *tile_tn, int ntiles, int nh, int nkv, int hd, int window,
+                      const int32_t *page_map, void *stream)
+{
+    return prefill_call(o, nullptr, q, k_pool, v_pool, block_table, off, qpos, kvpos, tile_t0, tile_tn, ntiles, 0,
+                        nh, nkv, hd, window, 1, page_map, stream);
+}
+
+int pgqa_attn_prefill_split(void *o, void *part, const void *q, const void *k_pool, const void *v_pool,
+                            const int32_t *block_table, const int32_t *off, const int32_t *qpos,
+                            const int32_t *kvpos, const int32_t *tile_t0, const int32_t *tile_tn, int ntiles,
+                            int rows, int nh, int nkv, int hd, int window, int splits, const int32_t *page_map,
+                            void *stream)
+{
+    return prefill_call(o, part, q, k_pool, v_pool, block_table, off, qpos, kvpos, tile_t0, tile_tn, ntiles, rows,
+                        nh, nkv, hd, window, splits, page_map, stream);
 }

@@ -67,6 +67,24 @@ cudaError_t launch_decode(const LaunchArgs &a, bool set_attr)
     return e;
 }
 
+// The combine kernel alone, over rows * nh (row, head) pairs of p.splits
+// partials in p.part_o / p.part_ml, into p.o.
+template <int HD>
+cudaError_t launch_combine(const DecodeParams &p, cudaStream_t stream)
+{
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t c2 = {};
+    c2.gridDim = dim3(static_cast<unsigned>(p.rows) * p.nh);
+    c2.blockDim = dim3(combine_threads<HD>());
+    c2.dynamicSmemBytes = 0;
+    c2.stream = stream;
+    c2.attrs = attr;
+    c2.numAttrs = 1;
+    return cudaLaunchKernelEx(&c2, decode_combine_kernel<HD>, p);
+}
+
 // How many clusters of `cluster` split CTAs can be resident at once (0: the
 // on-chip merge cannot be used).  Also sets the kernel's attributes.
 template <int HD>
@@ -96,6 +114,9 @@ int cluster_capacity(int cluster)
     return n;
 }
 
+cudaError_t launch_combine_hd64(const DecodeParams &p, cudaStream_t stream);
+cudaError_t launch_combine_hd128(const DecodeParams &p, cudaStream_t stream);
+cudaError_t launch_combine_hd256(const DecodeParams &p, cudaStream_t stream);
 int cluster_capacity_hd64(int cluster);
 int cluster_capacity_hd128(int cluster);
 int cluster_capacity_hd256(int cluster);

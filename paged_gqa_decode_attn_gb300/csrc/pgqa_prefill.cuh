@@ -76,6 +76,13 @@ struct PrefillParams {
     const int32_t *tile_tn;    // [ntiles] rows of each tile
     unsigned int *err;
     int nh, nkv, g, window, rows_per_tile, whole_tile_box;
+    // split-KV (tcgen05 kernel only): with splits > 1 each (row, head) writes
+    // one unnormalised partial per split -- (m, L) in log2 units into
+    // part_ml[rh * splits + s] and O into part_o[(rh * splits + s) * hd] --
+    // for the decode combine kernel, instead of o
+    int splits;
+    float *part_o;
+    float2 *part_ml;
 };
 
 // Visible KV range [lo, hi] of row r (hi < lo: nothing visible).

@@ -178,7 +178,7 @@ struct TcGeo {
 // head `kh`, and the union window of their positions.  Every role computes
 // it the same way (a whole warp, one position per lane).
 struct TcItem {
-    int t0, tn, kh, qbase, lo_u, hi_u, p_first, npages, nblocks, off0;
+    int t0, tn, kh, qbase, lo_u, hi_u, p_first, npages, nblocks, off0, split;
     bool live;     // the chunk has rows
 };
 
@@ -189,7 +189,10 @@ __device__ __forceinline__ TcItem tc_item(const PrefillParams &p, int it, int nt
     using G = TcGeo<HD>;
     TcItem I;
     // tiles outermost, last tiles first (they hold the longest windows), then
-    // kv head, then chunk
+    // kv head, then chunk, then split
+    const int S = p.splits;
+    I.split = it % S;
+    it /= S;
     const int per_tile = p.nkv * nchunks;
     const int tile = ntiles - 1 - it / per_tile;
     const int rest = it - (it / per_tile) * per_tile;
@@ -237,6 +240,13 @@ __device__ __forceinline__ TcItem tc_item(const PrefillParams &p, int it, int nt
     }
     I.p_first = I.lo_u >> 4;
     I.npages = I.hi_u >= I.lo_u ? (I.hi_u >> 4) - I.p_first + 1 : 0;
+    if (S > 1) {       // this split's share of the window's pages, in whole blocks
+        const int nb = (I.npages + G::kBlockPages - 1) / G::kBlockPages;
+        const int per = (nb + S - 1) / S * G::kBlockPages;
+        const int first = I.split * per;
+        I.p_first += first;
+        I.npages = max(0, min(per, I.npages - first));
+    }
     I.nblocks = (I.npages + G::kBlockPages - 1) / G::kBlockPages;
     I.off0 = __ldg(p.off + I.t0);
     return I;
@@ -274,7 +284,7 @@ __global__ void __launch_bounds__(TcGeo<HD>::kThreads, 1)
     const int tid = threadIdx.x;
     const int warp = tid >> 5;
     const int lane = tid & 31;
-    const int nitems = ntiles * p.nkv * nchunks;
+    const int nitems = ntiles * p.nkv * nchunks * p.splits;
     const int ncta = gridDim.x;
     const int cta = blockIdx.x;
     auto first_item = [&](int) { return cta < nitems ? cta : nitems; };
@@ -438,8 +448,9 @@ __global__ void __launch_bounds__(TcGeo<HD>::kThreads, 1)
         int jg = 0;
 
         // the finish of an item: the row sum over the parts, O / l in bf16
-        // (this part's dims), then O is free for the next item
-        auto finish = [&](int last_jg, size_t frh, bool fva, float fl) {
+        // (this part's dims) -- or, split, the unnormalised partial (m, L, O)
+        // -- then O is free for the next item
+        auto finish = [&](int last_jg, size_t frh, bool fva, float fl, float fm, int fsplit) {
             xsum[part * G::kRows + row] = fl;
             group_bar_sync(pair_bar, 32 * NP);
             float lt = xsum[row];
@@ -449,12 +460,22 @@ __global__ void __launch_bounds__(TcGeo<HD>::kThreads, 1)
             if (ok)
                 ok = mbar_wait_bounded(b_odone, last_jg & 1, p.err, kErrTimeoutFull);
             tc_fence_after();
+            const bool split_out = p.splits > 1;
+            const size_t prow = frh * p.splits + fsplit;
+            if (split_out && fva && part == 0)
+                p.part_ml[prow] = make_float2(fm, lt);
 #pragma unroll 1
             for (int c0 = part * HO; c0 < (part + 1) * HO; c0 += 16) {
                 uint32_t r[16];
                 tmem_ld16(trow + G::kOCol + c0, r);
                 tmem_wait_ld();
-                if (fva) {
+                if (fva && split_out) {
+                    float4 *dst = reinterpret_cast<float4 *>(p.part_o + prow * HD + c0);
+#pragma unroll
+                    for (int k = 0; k < 4; ++k)
+                        dst[k] = make_float4(__uint_as_float(r[4 * k]), __uint_as_float(r[4 * k + 1]),
+                                             __uint_as_float(r[4 * k + 2]), __uint_as_float(r[4 * k + 3]));
+                } else if (fva) {
                     uint32_t w[8];
 #pragma unroll
                     for (int k = 0; k < 8; ++k) {
@@ -478,7 +499,8 @@ __global__ void __launch_bounds__(TcGeo<HD>::kThreads, 1)
         int pend_jg = 0;
         size_t pend_rh = 0;
         bool pend_va = false;
-        float pend_l = 0.f;
+        float pend_l = 0.f, pend_m = -INFINITY;
+        int pend_split = 0;
         for (int it = first_item(0); it < nitems; it = next_item(it)) {
             const TcItem I = tc_item<HD>(p, it, ntiles, nchunks, lane, warp == 0);
             if (!I.live)
@@ -495,8 +517,14 @@ __global__ void __launch_bounds__(TcGeo<HD>::kThreads, 1)
                     va = true;
                 }
             }
-            if (I.nblocks == 0) {           // no position visible to any row: zeros
-                if (va) {
+            if (I.nblocks == 0) {           // no position visible to any row: zeros, or an empty partial
+                if (va && p.splits > 1) {
+                    const size_t prow = rh * p.splits + I.split;
+                    if (part == 0)
+                        p.part_ml[prow] = make_float2(-INFINITY, 0.f);
+                    for (int c0 = part * HO; c0 < (part + 1) * HO; c0 += 4)
+                        *reinterpret_cast<float4 *>(p.part_o + prow * HD + c0) = make_float4(0.f, 0.f, 0.f, 0.f);
+                } else if (va) {
                     for (int c0 = part * HO; c0 < (part + 1) * HO; c0 += 8)
                         *reinterpret_cast<uint4 *>(p.o + rh * HD + c0) = make_uint4(0u, 0u, 0u, 0u);
                 }
@@ -528,7 +556,7 @@ __global__ void __launch_bounds__(TcGeo<HD>::kThreads, 1)
                     mbar_arrive(b_qready);
             }
             if (pend)
-                finish(pend_jg, pend_rh, pend_va, pend_l);
+                finish(pend_jg, pend_rh, pend_va, pend_l, pend_m, pend_split);
 
             float m = -INFINITY, l = 0.f;
             for (int j = 0; j < I.nblocks; ++j) {
@@ -654,10 +682,12 @@ __global__ void __launch_bounds__(TcGeo<HD>::kThreads, 1)
             pend_rh = rh;
             pend_va = va;
             pend_l = l;
+            pend_m = m;
+            pend_split = I.split;
             jg += I.nblocks;
         }
         if (pend)
-            finish(pend_jg, pend_rh, pend_va, pend_l);
+            finish(pend_jg, pend_rh, pend_va, pend_l, pend_m, pend_split);
     }
     tc_fence_before();
     __syncthreads();

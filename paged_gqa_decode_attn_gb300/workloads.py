@@ -18,7 +18,9 @@ GPU test file):
   ``qpos = ctx-rows .. ctx-1``; ``off = 0``; seed ``12345 + hd``.
 * ``mapped_pool``: logical page ``p >= first_live`` moves to physical page
   ``npg - p`` of an ``npg + 1``-page pool whose other pages hold the bf16 NaN
-  ``0x7fc0``; pages below ``first_live`` map to the null page 0.
+  ``0x7fc0``; pages below ``first_live`` map to the null page 0.  With a
+  permuted block table or several sequences, the live pages are those some
+  row's window reads (:func:`live_pages`): the same pages for the page's case.
 
 Readings where the page says nothing (each is stated where it is used):
 
@@ -165,20 +167,26 @@ def lcg_permutation(n: int, seed: int) -> np.ndarray:
     return np.asarray(perm, dtype=np.int32)
 
 
-def mapped_pool(k: np.ndarray, v: np.ndarray, npg: int, nkv: int, hd: int, first_live: int):
+def mapped_pool(k: np.ndarray, v: np.ndarray, npg: int, nkv: int, hd: int, first_live):
     """Permuted copy of a ``[npg][nkv][16][hd]`` pool with a NaN null page 0.
 
-    Logical page ``p >= first_live`` sits at physical page ``npg - p``; pages
-    below ``first_live`` map to physical page 0, which (like every unused
-    physical page) holds bf16 NaN.  Returns ``(k_mapped, v_mapped, page_map)``.
+    A live page ``p`` (``first_live``: an int, meaning pages ``>= first_live``,
+    or a boolean mask over the ``npg`` pages) sits at page ``npg - p``; the
+    others map to page 0, which (like every unused page) holds bf16 NaN.
+    Returns ``(k_mapped, v_mapped, page_map)``.
     """
+    if isinstance(first_live, (int, np.integer)):
+        mask = np.arange(npg) >= int(first_live)
+    else:
+        mask = np.asarray(first_live, dtype=bool)
     pe = nkv * PAGE * hd
     mk = np.full((npg + 1) * pe, BF16_NAN, dtype=np.uint16)
     mv = np.full((npg + 1) * pe, BF16_NAN, dtype=np.uint16)
     pmap = np.zeros(npg, dtype=np.int32)
     kf = k.reshape(-1)
     vf = v.reshape(-1)
-    for p in range(first_live, npg):
+    for p in np.flatnonzero(mask):
+        p = int(p)
         s = npg - p
         pmap[p] = s
         mk[s * pe:(s + 1) * pe] = kf[p * pe:(p + 1) * pe]
@@ -287,15 +295,28 @@ def prefill_case(nh: int, nkv: int, hd: int, window: int, ctx: int, decode_rows:
                 bt, off, qpos, ctx=ctx, npg=npg)
 
 
+def live_pages(c: Case) -> np.ndarray:
+    """Mask of the physical pages some row's visible window reads, through the block table."""
+    mask = np.zeros(c.npg, dtype=bool)
+    q = np.asarray(c.qpos, dtype=np.int64)
+    hi = q if c.kvpos is None else np.minimum(q, np.asarray(c.kvpos, dtype=np.int64))
+    lo = np.maximum(0, q + 1 - c.window) if c.window > 0 else np.zeros_like(q)
+    bt = np.asarray(c.block_table)
+    for r in np.flatnonzero(hi >= lo):
+        o = int(c.off[r])
+        mask[bt[o + int(lo[r]) // PAGE:o + int(hi[r]) // PAGE + 1]] = True
+    return mask
+
+
 def with_mapped_pool(c: Case, fold_into_table: bool = False) -> Case:
     """The same KV behind the permuted / NaN-null-page pool.
 
-    ``first_live`` is ``lo(row 0) / 16`` for sliding windows, else 0.  With
-    ``fold_into_table`` the page map is composed into the block table instead
-    of being passed separately.
+    Pages no row's window reads map to the NaN page: for the page's one
+    sequence with an identity table, those below ``lo(row 0) / 16`` (its
+    ``first_live``) and past the last row.  With ``fold_into_table`` the page
+    map is composed into the block table instead of being passed separately.
     """
-    first_live = window_lo(int(c.qpos[0]), c.window) // PAGE if c.window > 0 else 0
-    mk, mv, pmap = mapped_pool(c.k_pool, c.v_pool, c.npg, c.nkv, c.hd, first_live)
+    mk, mv, pmap = mapped_pool(c.k_pool, c.v_pool, c.npg, c.nkv, c.hd, live_pages(c))
     if fold_into_table:
         return dataclasses.replace(c, name=c.name + "_mappedbt", k_pool=mk, v_pool=mv,
                                    block_table=pmap[c.block_table].astype(np.int32), page_map=None)

@@ -139,6 +139,58 @@ def test_prefill_long_full_size():
     prefill_gates(wl.prefill_long())
 
 
+def run_split(case, splits, seq=None):
+    """pgqa_attn_prefill_split over make_tiles' tiles; bf16 bits [rows][nh][hd]."""
+    import torch
+    import paged_gqa_decode_attn_gb300 as pgqa
+    from gpu_util import PrefillDev
+    d = PrefillDev(case, seq)
+    part = torch.empty(pgqa.decode_part_bytes(case.rows, case.nh, splits, case.hd) // 4 + 4, dtype=torch.float32,
+                       device="cuda")
+    d.o.fill_(0x5555)
+    pgqa.attn_prefill_split(d.o, part, d.q, d.k, d.v, d.bt, d.off, d.qpos, d.kvpos, d.t0, d.tn, d.ntiles,
+                            case.rows, case.nh, case.nkv, case.hd, case.window, splits, d.pm)
+    torch.cuda.synchronize()
+    assert pgqa.device_status() is None or pgqa.device_status() == 0
+    return d.o.cpu().numpy().view(np.uint16).reshape(case.rows, case.nh, case.hd)
+
+
+@pytest.mark.parametrize("splits", [1, 2, 5, 16])
+@pytest.mark.parametrize("hd,window", [(64, 0), (128, 1024), (256, 0), (256, 1024)])
+def test_split_kv_multi_row_decode(hd, window, splits):
+    """The tcgen05 large-M path for multi-row decode: 16 rows of one sequence at the
+    end of a 3000-token context (32 query rows per kv head, beyond the decode kernel's
+    8), each work item cut into `splits` page ranges and merged by the combine kernel:
+    against the oracle, and the page-map gate at fixed splits."""
+    from gpu_util import check_parity, first_difference
+    c = many_sequence_case([(16, 2984)], 32, 16, hd, window, seed=hd + splits)
+    a = run_split(c, splits)
+    check_parity(c, a, f"{c.name} splits {splits}")
+    for fold in (False, True):
+        m = wl.with_mapped_pool(c, fold_into_table=fold)
+        am = run_split(m, splits)
+        assert np.array_equal(am, a), f"page map (fold={fold}) differs: " + first_difference(am, a)
+
+
+def test_split_kv_several_sequences_and_empty_splits():
+    """Three sequences (16 rows at the end of 2000 tokens, a 1-row prompt, 40 rows of a
+    continuation) in one call; 13 splits leave the short windows' later splits empty."""
+    from gpu_util import check_parity
+    c = many_sequence_case([(16, 1984), (1, 0), (40, 500)], 16, 8, 256, 0, seed=7)
+    for splits in (4, 13):
+        check_parity(c, run_split(c, splits), f"{c.name} splits {splits}")
+
+
+def test_split_kv_bad_arguments():
+    import torch
+    import paged_gqa_decode_attn_gb300 as pgqa
+    x = torch.zeros(64, dtype=torch.int16, device="cuda")
+    with pytest.raises(pgqa.PgqaError):          # no scratch with splits > 1
+        pgqa.attn_prefill_split(x, None, x, x, x, x, x, x, None, x, x, 1, 1, 8, 2, 128, 0, 2)
+    with pytest.raises(pgqa.PgqaError):          # hd 512 has no split path
+        pgqa.attn_prefill_split(x, x, x, x, x, x, x, x, None, x, x, 1, 1, 8, 2, 512, 0, 2)
+
+
 def test_kvpos_below_qpos_and_an_empty_row():
     """Rows that see only up to kvpos < qpos, and one row whose window holds nothing."""
     c = wl.prefill_case(8, 2, 256, 20, 90, dist="sym", seed=5)
