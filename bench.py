@@ -788,7 +788,9 @@ def sweep_bytes(hd, ctx, rows, window, nh=32, nkv=16):
 def run_sweep(args, rank, world, dist):
     """Every point of the decode sweep (nh32 nkv16; hd x ctx x rows x window =
     3 x 4 x 3 x 3 = 108 points): rows at the last positions of one sequence, its
-    pages in a seeded permuted order.  Each point is timed with CUDA events around
+    pages in a seeded permuted order.  Points with more query rows per kv head
+    than the decode kernel packs (rows x g > 8) go through the tiled tcgen05
+    kernel with split-KV where it serves the head dimension.  Each point is timed with CUDA events around
     a graph of back-to-back calls over rotating pool copies; ``value`` is the
     geometric mean of the points' KV GB/s.  Pools are drawn once per (hd, ctx) on
     the device from a seeded generator (a timing run: the sweep's parity is the
@@ -827,7 +829,17 @@ def run_sweep(args, rank, world, dist):
                     qpos = torch.arange(ctx - rows, ctx, dtype=torch.int32, device=dev)
                     off = torch.zeros(rows, dtype=torch.int32, device=dev)
                     kv_eff = min(ctx, window) if window > 0 else ctx
-                    splits = pgqa.choose_splits(kv_eff, rows, nkv, 1)
+                    # more query rows per kv head than pgqa_attn_decode packs into a
+                    # CTA (8): the rows are one sequence's last positions, served by the
+                    # tiled tcgen05 kernel with split-KV (hd <= 256)
+                    tiled = rows * (nh // nkv) > 8 and hd <= 256
+                    if tiled:
+                        t0_h, tn_h = pgqa.make_tiles(np.zeros(rows, np.int32), pgqa.prefill_rows_per_tile(hd))
+                        t0 = torch.from_numpy(t0_h).to(dev)
+                        tn = torch.from_numpy(tn_h).to(dev)
+                        splits = pgqa.prefill_split_count(kv_eff, rows, len(t0_h), nh, nkv)
+                    else:
+                        splits = pgqa.choose_splits(kv_eff, rows, nkv, 1)
                     part = torch.empty(max(1, pgqa.decode_part_bytes(rows, nh, splits, hd)) // 4 + 4,
                                        dtype=torch.float32, device=dev)
                     cnt = torch.zeros(max(1, pgqa.decode_counter_count(rows, nh, nkv)), dtype=torch.int32,
@@ -836,8 +848,12 @@ def run_sweep(args, rank, world, dist):
                     bpc = sweep_bytes(hd, ctx, rows, window, nh, nkv)
 
                     def call(i):
-                        pgqa.attn_decode(o, part, q, ks[i % copies], vs[i % copies], bt, off, qpos, None, rows, nh,
-                                         nkv, hd, window, splits, cnt, None)
+                        if tiled:
+                            pgqa.attn_prefill_split(o, part, q, ks[i % copies], vs[i % copies], bt, off, qpos, None,
+                                                    t0, tn, len(t0_h), rows, nh, nkv, hd, window, splits, None)
+                        else:
+                            pgqa.attn_decode(o, part, q, ks[i % copies], vs[i % copies], bt, off, qpos, None, rows,
+                                             nh, nkv, hd, window, splits, cnt, None)
 
                     for i in range(3):
                         call(i)
@@ -856,6 +872,7 @@ def run_sweep(args, rank, world, dist):
                     ev1.synchronize()
                     us = ev0.elapsed_time(ev1) * 1e3 / n
                     results.append({"hd": hd, "ctx": ctx, "rows": rows, "window": window, "splits": splits,
+                                    "path": "tiled split-KV" if tiled else "decode",
                                     "us": round(us, 3), "gbs": round(bpc / (us * 1e-6) / 1e9, 1),
                                     "bytes": bpc})
                     del g
@@ -878,6 +895,7 @@ def run_sweep(args, rank, world, dist):
         "config": {"workload": "sweep_nh32_nkv16", "points": len(results),
                    "grid": "hd {128,256,512} x ctx {1K,4K,16K,64K} x rows {1,4,16} x window {0,1024,4096}",
                    "worst": by[:3], "best": by[-3:], "seconds": round(time.perf_counter() - t_all0, 1),
+                   "paths": "pgqa_attn_decode; pgqa_attn_prefill_split for rows x g > 8 at hd <= 256",
                    "l2": "rotating pool copies per (hd, ctx)",
                    "timing": "per point: CUDA events around a graph of 20-400 back-to-back calls"},
         "roofline": {"bound": "hbm", "achieved": round(gm, 1), "peak": peak, "unit": "GB/s",

@@ -225,6 +225,15 @@ int pgqa_attn_prefill_split(void *o, void *part, const void *q, const void *k_po
                             int rows, int nh, int nkv, int hd, int window, int splits, const int32_t *page_map,
                             void *stream);
 
+/*
+ * A split count for pgqa_attn_prefill_split on the current device: enough
+ * splits that the live work items (tiles x kv heads x 128-row chunks of
+ * (row, head) pairs) fill the SMs once, at least two 64-token blocks of the
+ * longest window (kv_len_eff positions) per split; at least 1.
+ * PGQA_ERR_INVALID_ARGUMENT for non-positive sizes or nh % nkv != 0.
+ */
+int pgqa_prefill_split_count(int kv_len_eff, int rows, int ntiles, int nh, int nkv);
+
 /* The longest tile pgqa_attn_prefill takes at head dimension hd (64 rows;
  * 32 at hd 512), or PGQA_ERR_UNSUPPORTED_HD. */
 int pgqa_prefill_rows_per_tile(int hd);

@@ -39,6 +39,7 @@ SIGNATURES = {
     "pgqa_attn_prefill": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P]),
     "pgqa_attn_prefill_split": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I,
                                      _P, _P]),
+    "pgqa_prefill_split_count": (_I, [_I, _I, _I, _I, _I]),
     "pgqa_prefill_rows_per_tile": (_I, [_I]),
     "pgqa_make_tiles": (_I, [_P, _I, _I, _P, _P, _I]),
     "pgqa_qk_norm_rope_write": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I,
@@ -145,6 +146,13 @@ def attn_prefill_split(o, part, q, k_pool, v_pool, block_table, off, qpos, kvpos
                                         int(splits), _ptr(page_map), _stream(stream))
     if st != PGQA_OK:
         raise PgqaError(st, "attn_prefill_split")
+
+
+def prefill_split_count(kv_len_eff: int, rows: int, ntiles: int, nh: int, nkv: int) -> int:
+    n = int(load().pgqa_prefill_split_count(int(kv_len_eff), int(rows), int(ntiles), int(nh), int(nkv)))
+    if n < 0:
+        raise PgqaError(n, "prefill_split_count")
+    return n
 
 
 def prefill_rows_per_tile(hd: int) -> int:

@@ -7,6 +7,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cstdint>
 #include <cstring>
 #include <mutex>
@@ -574,6 +575,7 @@ int prefill_call(void *o, void *part, const void *q, const void *k_pool, const v
                                                         static_cast<size_t>(rows) * nh * splits * hd * 4)
                            : nullptr;
     a.ntiles = ntiles;
+    a.max_tile_rows = rows > 0 ? std::min(rows, rpt) : rpt;
     a.stream = static_cast<cudaStream_t>(stream);
 
     std::lock_guard<std::mutex> lock(g_mutex);
@@ -639,6 +641,28 @@ int pgqa_attn_prefill(void *o, const void *q, const void *k_pool, const void *v_
 {
     return prefill_call(o, nullptr, q, k_pool, v_pool, block_table, off, qpos, kvpos, tile_t0, tile_tn, ntiles, 0,
                         nh, nkv, hd, window, 1, page_map, stream);
+}
+
+int pgqa_prefill_split_count(int kv_len_eff, int rows, int ntiles, int nh, int nkv)
+{
+    if (kv_len_eff < 1 || rows < 1 || ntiles < 1 || nh < 1 || nkv < 1 || nh % nkv != 0)
+        return PGQA_ERR_INVALID_ARGUMENT;
+    int sms = 152;
+    {
+        std::lock_guard<std::mutex> lock(g_mutex);
+        DeviceState *s = nullptr;
+        if (device_state(&s) == PGQA_OK)
+            sms = s->num_sms;
+    }
+    // live work items: tiles x kv heads x 128-row chunks of the average tile
+    const long long tile_rows = std::min<long long>((rows + ntiles - 1) / ntiles, 128);
+    const long long chunks = (tile_rows * (nh / nkv) + 127) / 128;
+    const long long items = static_cast<long long>(ntiles) * nkv * chunks;
+    // one wave: as many splits as fill the SMs, each at least two 64-token blocks
+    long long s = std::max<long long>(1, sms / items);
+    const long long blocks = (kv_len_eff + 63) / 64;
+    s = std::min(s, std::max<long long>(1, blocks / 2));
+    return static_cast<int>(std::min<long long>(s, PGQA_MAX_SPLITS));
 }
 
 int pgqa_attn_prefill_split(void *o, void *part, const void *q, const void *k_pool, const void *v_pool,

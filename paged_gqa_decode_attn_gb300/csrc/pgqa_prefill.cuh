@@ -450,6 +450,7 @@ struct PrefillLaunchArgs {
     const CUtensorMap *tm_k;
     const CUtensorMap *tm_v;
     int ntiles;
+    int max_tile_rows;    // no tile holds more rows (<= rows_per_tile): sets the chunks per tile
     int num_sms;          // persistent kernels: one CTA per SM
     cudaStream_t stream;
 };

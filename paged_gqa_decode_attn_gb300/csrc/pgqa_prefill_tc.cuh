@@ -710,8 +710,9 @@ cudaError_t launch_prefill_tc(const PrefillLaunchArgs &a, bool set_attr)
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cudaLaunchConfig_t cfg = {};
-    const int nchunks = (a.p.rows_per_tile * a.p.g + TcGeo<HD>::kRows - 1) / TcGeo<HD>::kRows;
-    const long long items = static_cast<long long>(a.ntiles) * a.p.nkv * nchunks;
+    const int tile_rows = a.max_tile_rows > 0 ? std::min(a.max_tile_rows, a.p.rows_per_tile) : a.p.rows_per_tile;
+    const int nchunks = (tile_rows * a.p.g + TcGeo<HD>::kRows - 1) / TcGeo<HD>::kRows;
+    const long long items = static_cast<long long>(a.ntiles) * a.p.nkv * nchunks * a.p.splits;
     if (items > INT_MAX)
         return cudaErrorInvalidValue;
     // one CTA per item while they fit in about two waves (the hardware then

@@ -110,6 +110,17 @@ def test_choose_splits_rule(lib):
     assert pgqa.choose_splits(32768, 1, 4, 1) >= 1
 
 
+def test_prefill_split_count(lib):
+    """One wave of live items over the SMs (152 without a device), at least two 64-token blocks a split."""
+    assert pgqa.prefill_split_count(65536, 16, 1, 32, 16) == 152 // 16     # 16 rows of one sequence: 16 items
+    assert pgqa.prefill_split_count(1024, 16, 1, 32, 16) == 8              # 16 blocks: at most 8 splits
+    assert pgqa.prefill_split_count(100, 16, 1, 32, 16) == 1
+    assert pgqa.prefill_split_count(8192, 8192, 64, 16, 8) == 1            # many items already fill the SMs
+    for bad in ((0, 1, 1, 8, 2), (64, 0, 1, 8, 2), (64, 1, 0, 8, 2), (64, 1, 1, 8, 3)):
+        with pytest.raises(pgqa.PgqaError):
+            pgqa.prefill_split_count(*bad)
+
+
 def test_strerror_names_every_code(lib):
     for code in range(-9, 1):
         assert pgqa.strerror(code) != "unknown status"
