@@ -43,6 +43,8 @@ KERNEL_SOURCES = ["paged_gqa_decode_attn_gb300/csrc/pgqa_device.cuh",
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "decode_split_kernel_traffic.json")
 PREP_SOURCES = ["paged_gqa_decode_attn_gb300/csrc/pgqa_prep.cu"]
 PREP_TRAFFIC_FILE = os.path.join(ROOT, "profiles", "qk_norm_rope_kernel_traffic.json")
+TILED_SOURCES = ["paged_gqa_decode_attn_gb300/csrc/pgqa_prefill_tc.cuh"]
+TILED_TRAFFIC_FILE = os.path.join(ROOT, "profiles", "prefill_tc_kernel_traffic.json")
 
 
 # ------------------------------------------------------------------ distributed helpers
@@ -198,6 +200,8 @@ def build_case(name: str):
         return wl.prefill_long()
     if name == "prep_long":
         return wl.prep_long()
+    if name == "multirow":
+        return wl.multirow()
     raise SystemExit(f"unknown workload {name}")
 
 
@@ -314,6 +318,8 @@ def run_reference(args, case, rank, world):
         return 0
     gbs, per, sample, cores, k = oracle_rate(case, budget_s=args.ref_budget, steps=args.steps, warmup=args.warmup)
     metric, unit = METRIC, "GB/s"
+    if args.workload == "multirow":
+        metric = "multi-row decode KV GB/s (tiled split-KV path)"
     if args.workload.startswith("prefill"):
         metric, unit = "paged causal prefill attention TFLOP/s", "TFLOP/s"
         gbs = prefill_flops(case) * k / (case.rows * case.nh) / per / 1e12
@@ -639,6 +645,137 @@ def run_prefill(args, case, rank, world, dist):
     return 0
 
 
+def run_multirow(args, case, rank, world, dist):
+    """One step = one pgqa_attn_prefill_split call (the tcgen05 tiled kernel with
+    split-KV, then the combine kernel) serving a multi-token decode: KV GB/s
+    against the HBM peak, as for the decode workloads."""
+    import torch
+    import paged_gqa_decode_attn_gb300 as pgqa
+
+    torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
+    dev = torch.device("cuda")
+    if rank == 0:
+        pgqa.build()
+    barrier(dist)
+    pgqa.load()
+    bpc = case.algorithmic_bytes()
+    t0_h, tn_h = pgqa.make_tiles(np.asarray(case.off, np.int32), pgqa.prefill_rows_per_tile(case.hd))
+    ntiles = len(t0_h)
+    splits = args.splits or pgqa.prefill_split_count(case.kv_len_eff(), case.rows, ntiles, case.nh, case.nkv)
+    pool_bytes = case.k_pool.nbytes + case.v_pool.nbytes
+    copies = args.copies or max(2, math.ceil(3 * L2_BYTES / max(bpc, 1)))
+    copies = min(copies, max(2, int(0.25 * torch.cuda.get_device_properties(dev).total_memory // pool_bytes)))
+
+    def i16(a):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16))
+
+    ks = [i16(case.k_pool).to(dev) for _ in range(copies)]
+    vs = [i16(case.v_pool).to(dev) for _ in range(copies)]
+    parts = [np.ascontiguousarray(a).view(np.uint8) for a in
+             (case.q, np.asarray(case.qpos, np.int32), np.asarray(case.off, np.int32),
+              np.asarray(case.block_table, np.int32), t0_h, tn_h)]
+    offs, pos = [], 0
+    for a in parts:
+        offs.append(pos)
+        pos += (a.size + 255) // 256 * 256
+    host_in = torch.zeros(pos, dtype=torch.uint8).pin_memory()
+    for a, o0 in zip(parts, offs):
+        host_in[o0:o0 + a.size] = torch.from_numpy(a)
+    dev_in = host_in.to(dev)
+    views = [dev_in[o0:o0 + a.size] for a, o0 in zip(parts, offs)]
+    q = views[0].view(torch.int16)
+    qpos, off, bt, t0, tn = (v.view(torch.int32) for v in views[1:])
+    part = torch.empty(pgqa.decode_part_bytes(case.rows, case.nh, splits, case.hd) // 4 + 4, dtype=torch.float32,
+                       device=dev)
+    o = torch.empty(case.rows * case.nh * case.hd, dtype=torch.int16, device=dev)
+    o_h = torch.empty_like(o, device="cpu").pin_memory()
+
+    def call(i, stream=None):
+        pgqa.attn_prefill_split(o, part, q, ks[i % copies], vs[i % copies], bt, off, qpos, None, t0, tn, ntiles,
+                                case.rows, case.nh, case.nkv, case.hd, case.window, splits, None, stream)
+
+    call(0)
+    torch.cuda.synchronize()
+    spot = None
+    if rank == 0 and not args.no_check:
+        import oracle
+        got = o.cpu().numpy().view(np.uint16).reshape(case.rows, case.nh, case.hd)
+        pairs = [(r, h) for r in range(case.rows) for h in range(case.nh)][:: max(1, case.rows * case.nh // 32)]
+        _, ref = oracle.decode_case(case, pairs=pairs, want_f64=False)
+        spot = oracle.rel_rms(np.stack([got[r, h] for r, h in pairs]), ref)
+        if not spot < 1e-2:
+            raise SystemExit(f"spot check against the oracle failed: rel_rms {spot}")
+    sampler = ClockSampler(torch.cuda.current_device()) if not args.no_clocks else None
+    for i in range(args.warmup):
+        call(i)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for i in range(args.steps):
+            call(i)
+    g.replay()
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(dist)
+    torch.cuda.synchronize()
+    ev0.record(stream)
+    g.replay()
+    ev1.record(stream)
+    ev1.synchronize()
+    barrier(dist)
+    el_ms = ev0.elapsed_time(ev1)
+    clocks = sampler.stop() if sampler else None
+    el_max = max_over_ranks(dist, el_ms)
+    value = sum_over_ranks(dist, float(bpc) * args.steps) / (el_max * 1e-3) / 1e9
+    call_us = el_ms * 1e3 / args.steps
+
+    e2e_steps = max(1, min(args.steps, args.e2e_steps))
+    barrier(dist)
+    torch.cuda.synchronize()
+    t_0 = time.perf_counter()
+    for i in range(e2e_steps):
+        dev_in.copy_(host_in, non_blocking=True)
+        call(i)
+        o_h.copy_(o, non_blocking=True)
+    torch.cuda.synchronize()
+    e2e_s = max_over_ranks(dist, time.perf_counter() - t_0)
+    e2e_value = sum_over_ranks(dist, float(bpc) * e2e_steps) / e2e_s / 1e9
+    if rank != 0:
+        return 0
+    peak, peak_kind = measured_peaks()
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        gbs, per, sample, cores, _ = oracle_rate(case, budget_s=args.cpu_budget)
+        cpu = {"value": round(gbs, 4), "unit": "GB/s", "cores": cores, "kind": "oracle", "sample": sample}
+    cfg = config_of(args, case, None)
+    cfg.update({"splits": splits, "tiles": ntiles, "path": "pgqa_attn_prefill_split (tcgen05 tiled, split-KV) "
+                "+ the decode combine kernel",
+                "l2": f"rotating {copies} pool copies", "timing": f"CUDA events around one CUDA graph of "
+                f"{args.steps} back-to-back calls (two kernels each)"})
+    if spot is not None:
+        cfg["spot_check_rel_rms"] = spot
+    line = {
+        "metric": "multi-row decode KV GB/s (tiled split-KV path)", "value": round(value, 2), "unit": "GB/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": el_max / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": cfg,
+        "roofline": {"bound": "hbm", "achieved": round(value, 2), "peak": peak, "unit": "GB/s",
+                     "frac": round(value / peak, 4),
+                     "traffic": recorded_traffic(case.name, TILED_TRAFFIC_FILE, TILED_SOURCES),
+                     "peak_kind": peak_kind,
+                     "kernel": "prefill_tc_kernel<256> (split) + decode_combine_kernel<256>",
+                     "call_us": round(call_us, 3)},
+        "cpu_baseline": cpu,
+        "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": host_in.numel(),
+                "d2h_bytes_per_step": o_h.numel() * o_h.element_size(), "steps": e2e_steps,
+                "us_per_step": round(e2e_s / e2e_steps * 1e6, 3)},
+        "gpu_launches": 2 * args.steps, "clocks": clocks,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def prep_config(case):
     return {"workload": case.name, "nh": case.nh, "nkv": case.nkv, "hd": case.hd, "rotary_dim": case.rotary_dim,
             "theta": case.theta, "norm_v": case.norm_v, "rows": case.rows,
@@ -915,7 +1052,7 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="sliding",
                     choices=["sliding", "sliding_mapped", "tiny", "long", "batched", "prefill_page", "prefill_long",
-                             "prep_long", "sweep"])
+                             "prep_long", "sweep", "multirow"])
     ap.add_argument("--splits", type=int, default=0, help="override choose_splits")
     ap.add_argument("--merge", choices=["counters", "combine"], default="counters")
     ap.add_argument("--graph-chunk", type=int, default=2000)
@@ -953,6 +1090,8 @@ def main(argv=None):
             return run_prefill(args, case, rank, world, dist)
         if args.workload.startswith("prep"):
             return run_prep(args, case, rank, world, dist)
+        if args.workload == "multirow":
+            return run_multirow(args, case, rank, world, dist)
         return run_ours(args, case, rank, world, dist)
     finally:
         if dist is not None:

@@ -438,6 +438,13 @@ def prep_long() -> PrepCase:
     return prep_case(16, 8, 256, 256, 8192, 8192, positions="prefill", name="prep_nh16_nkv8_hd256_rd256_r8192")
 
 
+def multirow(ctx: int = 32768, rows: int = 16) -> Case:
+    """A multi-token decode: ``rows`` rows of one sequence at its last positions
+    (speculative verification), nh32 nkv16 hd256, full attention over ``ctx``,
+    symmetric uniform; 32 query rows per kv head."""
+    return page_case(32, 16, 256, 0, ctx, rows, dist="sym", name=f"multirow_nh32_nkv16_hd256_ctx{ctx}_r{rows}")
+
+
 def sweep_points():
     """The 108 hybrid-sweep points (hd, ctx, rows, window), in a fixed order."""
     return [(hd, ctx, rows, w) for hd in SWEEP_HD for ctx in SWEEP_CTX
