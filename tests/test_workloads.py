@@ -3,6 +3,8 @@
 import os
 import sys
 
+import dataclasses
+
 import numpy as np
 import pytest
 
@@ -123,3 +125,21 @@ def test_with_mapped_pool_variants(fold):
                                           for j in range(len(c.block_table))]
     else:
         assert m.page_map is not None and m.block_table is c.block_table
+
+
+def test_live_pages_follow_the_rows_windows_through_the_table():
+    """The page's sliding case (identity table): live pages are lo(row 0)/16 .. the last row's page.
+    Behind a permuted table the same logical pages are live, at their permuted physical ids; a row
+    with no visible position adds nothing."""
+    c = wl.page_case(8, 2, 64, 100, 300, 3, dist="sym", seed=5)
+    live = wl.live_pages(c)
+    first = wl.window_lo(int(c.qpos[0]), 100) // 16
+    last = int(c.qpos[-1]) // 16
+    assert np.flatnonzero(live).tolist() == list(range(first, last + 1))
+    perm = wl.lcg_permutation(c.npg, 3).astype(np.int32)
+    pc = dataclasses.replace(c, block_table=perm[:len(c.block_table)])
+    assert sorted(np.flatnonzero(wl.live_pages(pc)).tolist()) == sorted(perm[first:last + 1].tolist())
+    kv = c.qpos.copy()
+    kv[:] = c.qpos - 200                      # below every row's window: nothing visible
+    assert not wl.live_pages(dataclasses.replace(c, kvpos=kv)).any()
+
