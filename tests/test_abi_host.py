@@ -213,6 +213,19 @@ def test_prefill_bad_arguments_are_rejected_before_any_cuda_call(lib, kw, code):
     assert prefill_call(lib, **kw) == code
 
 
+def split_call(lib, splits=2, rows=4, hd=128, part=FAKE, ntiles=1, nh=8, nkv=2):
+    return lib.pgqa_attn_prefill_split(FAKE, part, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None, FAKE, FAKE, ntiles, rows,
+                                       nh, nkv, hd, 0, splits, None, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    ({"splits": 0}, -1), ({"splits": 257}, -7), ({"hd": 512}, -2), ({"hd": 96}, -2), ({"part": None}, -1),
+    ({"rows": 0}, -1), ({"part": FAKE + 4}, -3), ({"nh": 6, "nkv": 4}, -1)])
+def test_prefill_split_bad_arguments_are_rejected_before_any_cuda_call(lib, kw, code):
+    """splits 1..256; hd 512 has no split path; scratch and a row count with splits > 1; 16-byte alignment."""
+    assert split_call(lib, **kw) == code
+
+
 def test_prefill_zero_tiles_is_ok_without_a_device(lib):
     assert prefill_call(lib, ntiles=0, o=None, q=None) == 0
 
