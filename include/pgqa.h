@@ -71,12 +71,14 @@ extern "C" {
  *   counters    merge counters, NULL or at least
  *               pgqa_decode_counter_count(rows, nh, nkv) uint32 slots.  Zero
  *               them once before first use; every successful call leaves them
- *               zero again.  Non-NULL: the split partials merge inside the
- *               kernel -- on chip, through the distributed shared memory of a
- *               thread-block cluster holding a tile's splits, when splits is 2,
- *               4 or 8 and the device can co-schedule such a cluster;
- *               otherwise in the tile's last CTA, found through the counters.
- *               NULL: a separate combine kernel merges them.  All give
+ *               zero again.  Non-NULL with 2 <= splits <= 8: the split
+ *               partials merge inside the kernel -- on chip, through the
+ *               distributed shared memory of a thread-block cluster holding a
+ *               tile's splits, when splits is 2, 4 or 8 and the device can
+ *               co-schedule such a cluster; otherwise in the tile's last CTA,
+ *               found through the counters.  NULL, or more than 8 splits: a
+ *               separate combine kernel merges them (in two levels of up to 8
+ *               splits above 8), and the counters are not touched.  All give
  *               bit-identical o.
  *   page_map    int32 map from block-table entries to physical pages, or NULL.
  *
@@ -113,14 +115,20 @@ int pgqa_choose_splits_for(int kv_len_eff, int rows, int nkv, int nseq, int num_
 
 /*
  * Bytes of the `part` scratch (`attn::decode_part_bytes` of the test file):
- * rows * nh * splits * (hd + 2) * 4 (f32 O, running max and sum per split);
- * above 8 splits, plus rows * nh * ceil(splits / 8) * (hd + 2) * 4 + 16 for the
- * merged groups of 8 splits (the merge then runs in two levels).
+ * rows * nh * splits * (hd + 2) * 4 (f32 O, running max and sum per split).
  */
 size_t pgqa_decode_part_bytes(int rows, int nh, int splits, int hd);
 
-/* uint32 merge-counter slots one call needs: rows * nkv * ceil((nh / nkv) / 8) * 33. */
+/* uint32 merge-counter slots one call needs: rows * nkv * ceil((nh / nkv) / 8), one per tile. */
 size_t pgqa_decode_counter_count(int rows, int nh, int nkv);
+
+/*
+ * Kernels one pgqa_attn_decode call with rows > 0 launches: 1 (the split
+ * kernel, merging in the kernel) when splits == 1, or when counters are given
+ * (with_counters != 0) and splits <= 8; else 2 (plus the combine kernel).
+ * 0 for splits outside [1, PGQA_MAX_SPLITS].  Pure host arithmetic.
+ */
+int pgqa_decode_kernel_count(int splits, int with_counters);
 
 /*
  * Reads and clears the device-side error word of the current device

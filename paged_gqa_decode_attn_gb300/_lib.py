@@ -31,6 +31,7 @@ SIGNATURES = {
     "pgqa_choose_splits_for": (_I, [_I, _I, _I, _I, _I]),
     "pgqa_decode_part_bytes": (ctypes.c_size_t, [_I, _I, _I, _I]),
     "pgqa_decode_counter_count": (ctypes.c_size_t, [_I, _I, _I]),
+    "pgqa_decode_kernel_count": (_I, [_I, _I]),
     "pgqa_device_status": (_I, []),
     "pgqa_strerror": (ctypes.c_char_p, [_I]),
     "pgqa_version": (_I, []),
@@ -204,6 +205,10 @@ def decode_part_bytes(rows: int, nh: int, splits: int, hd: int) -> int:
 
 def decode_counter_count(rows: int, nh: int, nkv: int) -> int:
     return int(load().pgqa_decode_counter_count(int(rows), int(nh), int(nkv)))
+
+
+def decode_kernel_count(splits: int, with_counters: bool) -> int:
+    return int(load().pgqa_decode_kernel_count(int(splits), int(bool(with_counters))))
 
 
 def device_status() -> None:

@@ -249,11 +249,7 @@ size_t pgqa_decode_part_bytes(int rows, int nh, int splits, int hd)
 {
     if (rows <= 0 || nh <= 0 || splits <= 0 || hd <= 0)
         return 0;
-    size_t partials = static_cast<size_t>(splits);
-    if (splits > pgqa::kGroupSplits)        // plus the merged split groups, 16-byte aligned
-        partials += (splits + pgqa::kGroupSplits - 1) / pgqa::kGroupSplits;
-    return static_cast<size_t>(rows) * nh * partials * (static_cast<size_t>(hd) + 2) * 4 +
-           (splits > pgqa::kGroupSplits ? 16 : 0);
+    return static_cast<size_t>(rows) * nh * splits * (static_cast<size_t>(hd) + 2) * 4;
 }
 
 size_t pgqa_decode_counter_count(int rows, int nh, int nkv)
@@ -261,7 +257,14 @@ size_t pgqa_decode_counter_count(int rows, int nh, int nkv)
     if (rows <= 0 || nh <= 0 || nkv <= 0 || nh % nkv != 0)
         return 0;
     const int g = nh / nkv;
-    return static_cast<size_t>(rows) * nkv * ((g + pgqa::kQRows - 1) / pgqa::kQRows) * pgqa::kCountersPerTile;
+    return static_cast<size_t>(rows) * nkv * ((g + pgqa::kQRows - 1) / pgqa::kQRows);
+}
+
+int pgqa_decode_kernel_count(int splits, int with_counters)
+{
+    if (splits < 1 || splits > PGQA_MAX_SPLITS)
+        return 0;
+    return splits == 1 || (with_counters && splits <= pgqa::kGroupSplits) ? 1 : 2;
 }
 
 namespace {
@@ -411,22 +414,15 @@ int pgqa_attn_decode(void *o, void *part, const void *q, const void *k_pool, con
     p.part_ml = splits > 1 ? reinterpret_cast<float2 *>(static_cast<char *>(part) +
                                                         static_cast<size_t>(rows) * nh * splits * hd * 4)
                            : nullptr;
-    p.gpart_o = nullptr;
-    p.gpart_ml = nullptr;
-    if (splits > pgqa::kGroupSplits) {
-        const size_t ng = (splits + pgqa::kGroupSplits - 1) / pgqa::kGroupSplits;
-        size_t at = static_cast<size_t>(rows) * nh * splits * (static_cast<size_t>(hd) + 2) * 4;
-        at = (at + 15) / 16 * 16;
-        p.gpart_o = reinterpret_cast<float *>(static_cast<char *>(part) + at);
-        p.gpart_ml = reinterpret_cast<float2 *>(static_cast<char *>(part) + at + static_cast<size_t>(rows) * nh * ng * hd * 4);
-    }
     p.q = static_cast<const __nv_bfloat16 *>(q);
     p.block_table = block_table;
     p.off = off;
     p.qpos = qpos;
     p.kvpos = kvpos;
     p.page_map = page_map;
-    p.counters = counters;
+    // in-kernel merges take up to kGroupSplits splits; more go to the combine
+    // kernel, whose loads spread over rows * nh * hd / 128 CTAs
+    p.counters = splits <= pgqa::kGroupSplits ? counters : nullptr;
     p.rows = rows;
     p.nh = nh;
     p.nkv = nkv;
@@ -458,7 +454,7 @@ int pgqa_attn_decode(void *o, void *part, const void *q, const void *k_pool, con
     // tiles that do work: one per packing group of rows (the rows of a group
     // that is packed leave at once), kv head and head subgroup
     const long long live = static_cast<long long>((rows + p.pack - 1) / p.pack) * nkv * hsg;
-    p.cluster = counters ? on_chip_cluster(s, hi, hd, splits, live) : 0;
+    p.cluster = p.counters ? on_chip_cluster(s, hi, hd, splits, live) : 0;
     if (g_trace && static_cast<size_t>(splits) * nkv * hsg * rows * pgqa::kTraceEvents * 8 <= g_trace_bytes)
         p.trace = g_trace;
     a.tm_k = &tk;

@@ -44,9 +44,8 @@ constexpr int kBoxElems = 64;             // 128-byte swizzle atom: 64 bf16 per 
 constexpr int kBoxBytes = kPage * kBoxElems * 2;   // one TMA box: 16 rows x 128 B
 constexpr int kMaxSplits = 256;
 constexpr int kMaxCluster = 8;            // largest thread-block cluster for the on-chip merge
-constexpr int kGroupSplits = 8;           // more splits than this merge in two levels of up to 8
+constexpr int kGroupSplits = 8;           // the combine kernel merges more splits than this in two levels
 constexpr int kMaxGroups = (kMaxSplits + kGroupSplits - 1) / kGroupSplits;
-constexpr int kCountersPerTile = 1 + kMaxGroups;   // [0] the final merge, [1 + g] split group g
 constexpr long long kWaitLimitCycles = 2000000000ll;   // bounded waits: ~1 s at 2 GHz
 constexpr unsigned int kErrTimeoutFull = 1u;
 constexpr unsigned int kErrTimeoutEmpty = 2u;
@@ -117,10 +116,6 @@ struct Smem {
     static constexpr int kMlOff = kObufBytes;
     static constexpr int kStatOff = kMlOff + G::kGroups * kQRows * 8;
     static_assert(kStatOff + kQRows * (G::kGroups + 2) * 4 <= kStagesBytes, "group merge scratch");
-    // last-CTA merge of the split partials: merge weights [8][kMaxSplits + 1],
-    // also in the stage ring
-    static constexpr int kWtsBytes = kQRows * (kMaxSplits + 2) * 4;
-    static_assert(kWtsBytes <= kStagesBytes, "merge weights");
     // cluster merge weights [8][kMaxCluster + 1], after the group-merge scratch
     static constexpr int kCwOff = (kStatOff + kQRows * (G::kGroups + 2) * 4 + 15) / 16 * 16;
     static_assert(kCwOff + kQRows * (kMaxCluster + 1) * 4 <= kStagesBytes, "cluster merge scratch");
@@ -131,8 +126,6 @@ struct DecodeParams {
     __nv_bfloat16 *o;        // [rows][nh][hd]
     float *part_o;           // [rows*nh][splits][hd]
     float2 *part_ml;         // [rows*nh][splits]: (max in log2 units, sum)
-    float *gpart_o;          // splits > 8: [rows*nh][groups][hd] merged split groups
-    float2 *gpart_ml;        // splits > 8: [rows*nh][groups]
     const __nv_bfloat16 *q;  // [rows][nh][hd]
     const int32_t *block_table;
     const int32_t *off;
@@ -385,11 +378,11 @@ __device__ __forceinline__ uint32_t swz(int row, int u)
 // The S split partials (m_s, l_s, O_s) of one (row, head) merge as
 //   M = max_s m_s,  w_s = (m_s == -inf) ? 0 : 2^(m_s - M),  L = sum_s w_s l_s,
 //   o[d] = bf16_rn( (sum_s w_s O_s[d]) / L ), or 0 when L == 0.
-// With more than kGroupSplits splits the merge runs in two levels: splits
-// [8g, 8g+8) merge into an unnormalised group partial (M_g, L_g, O_g), and
-// the group partials merge into o -- the same formula at both levels.
-// The last-CTA merge and the combine kernel run exactly these operations in
-// exactly this order, so they agree bit for bit:
+// With more than kGroupSplits splits (combine kernel only) the merge runs in
+// two levels: splits [8g, 8g+8) merge into an unnormalised group partial
+// (M_g, L_g, O_g), and the group partials merge into o -- the same formula at
+// both levels.  The last-CTA merge and the combine kernel run exactly these
+// operations in exactly this order, so they agree bit for bit:
 //  * merge_stats_warp (one warp): lane l takes splits l, l+32, ... in order,
 //    then a fixed xor-butterfly combines the lanes; every lane ends with the
 //    same bits because float max and addition are commutative;
@@ -1107,204 +1100,189 @@ __global__ void __launch_bounds__(Geo<HD>::kThreads, Cfg<HD>::kMinBlocks)
         return;
 
     // ---------------------------------------------------- last-CTA merge
-    // A merge pass over `count` partial rows of every served query row:
-    // source row j of (row, head) rh is src_o[(rh * src_rows + first + j) *
-    // hd], with (m, l) at src_ml[rh * src_rows + first + j].  The result goes
-    // to o (final) or, unnormalised with its (M, L), to dst row dst_idx.
-    // The partial rows come into the (now free) stage ring by cp.async, as
-    // many rows at once as fit, while the weights are computed; each thread
-    // then accumulates its kOwn float4 outputs (query row q, dims 4*d4..+3)
-    // in row order.
+    // Only with counters, which the host passes for S <= kGroupSplits alone
+    // (more splits merge in the combine kernel).  The S partial rows of every
+    // served query row come into the (now free) stage ring by cp.async while
+    // the weights are computed; each thread then accumulates its kOwn float4
+    // outputs (query row q, dims 4*d4..+3) in split order.
     constexpr int kVec = HD / 4;                               // float4 per query row
     constexpr int kOwn = kQRows * kVec / NT;                   // float4 outputs per thread
-    constexpr int kWStride = kMaxSplits + 2;                   // weights, L, M of one query row
-    constexpr int kStageOff = (SM::kWtsBytes + 15) / 16 * 16;
-    constexpr int kStageRows = (SM::kStagesBytes - kStageOff) / (kQRows * HD * 4);   // rows of all 8 query rows
-    static_assert(kStageRows >= 1, "merge staging");
+    constexpr int kWStride = kGroupSplits + 1;                 // weights and L of one query row
+    constexpr int kStageOff = (kQRows * kWStride * 4 + 15) / 16 * 16;
+    static_assert(kStageOff + kGroupSplits * kQRows * HD * 4 <= SM::kStagesBytes, "merge staging");
     float *wts = reinterpret_cast<float *>(smem);
     float *stg = reinterpret_cast<float *>(smem + kStageOff);
     auto rowhead = [&](int q) {
         return static_cast<size_t>(r0 + q / nh_sub) * p.nh + head0 + q % nh_sub;
-    };
-    auto merge_pass = [&](const float *src_o, const float2 *src_ml, int src_rows, int first, int count, bool final,
-                          float *dst_o, float2 *dst_ml, int dst_rows, int dst_idx) {
-        float4 oacc[kOwn];
-#pragma unroll
-        for (int k = 0; k < kOwn; ++k)
-            oacc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
-        auto stage = [&](int j0, int nj) {   // rows [j0, j0 + nj) of every query row -> stg[(j - j0) * nq + q]
-            const int total = nj * nq * kVec;
-            for (int e = tid; e < total; e += NT) {
-                const int jq = e / kVec, d4 = e - jq * kVec;
-                const int j = jq / nq, q = jq - j * nq;
-                cp_async16(smem_u32(stg + static_cast<size_t>(jq) * HD + d4 * 4),
-                           src_o + (rowhead(q) * src_rows + first + j0 + j) * HD + d4 * 4);
-            }
-        };
-        int nj = min(count, kStageRows);
-        stage(0, nj);
-        for (int q = warp; q < nq; q += NW) {
-            float m = 0.f;
-            const float L = merge_stats_warp(src_ml + rowhead(q) * src_rows + first, count, wts + q * kWStride, lane,
-                                             &m);
-            if (lane == 0) {
-                wts[q * kWStride + kMaxSplits] = L;
-                wts[q * kWStride + kMaxSplits + 1] = m;
-            }
-        }
-        for (int j0 = 0; j0 < count; j0 += nj) {
-            nj = min(count - j0, kStageRows);
-            if (j0 > 0)
-                stage(j0, nj);
-            cp_async_wait_all();
-            named_bar_sync<kAllConsumersBarrier, NT>();  // staged rows and weights visible to every thread
-            for (int j = 0; j < nj; ++j) {
-#pragma unroll
-                for (int k = 0; k < kOwn; ++k) {
-                    const int e = tid + k * NT;
-                    const int q = e / kVec, d4 = e - q * kVec;
-                    if (q < nq)
-                        fma4(oacc[k], wts[q * kWStride + j0 + j],
-                             *reinterpret_cast<const float4 *>(stg + static_cast<size_t>(j * nq + q) * HD + d4 * 4));
-                }
-            }
-            named_bar_sync<kAllConsumersBarrier, NT>();  // staging area free again
-        }
-#pragma unroll
-        for (int k = 0; k < kOwn; ++k) {
-            const int e = tid + k * NT;
-            const int q = e / kVec, d4 = e - q * kVec;
-            if (q < nq) {
-                const size_t rh = rowhead(q);
-                if (final)
-                    store_out4(p.o + rh * HD + d4 * 4, oacc[k], wts[q * kWStride + kMaxSplits]);
-                else
-                    *reinterpret_cast<float4 *>(dst_o + (rh * dst_rows + dst_idx) * HD + d4 * 4) = oacc[k];
-            }
-        }
-        if (!final && tid < nq)
-            dst_ml[rowhead(tid) * dst_rows + dst_idx] =
-                make_float2(wts[tid * kWStride + kMaxSplits + 1], wts[tid * kWStride + kMaxSplits]);
     };
 
     // Tickets: the barrier orders every thread's stores before thread 0's
     // acquire-release atomic; the winner's threads see all partials after the
     // second barrier.
     const int tile_id = (r0 * p.nkv + kh) * p.hsg + hs;
-    unsigned int *cnt = p.counters + static_cast<size_t>(tile_id) * kCountersPerTile;
-    auto take_ticket = [&](unsigned int *c) {
-        named_bar_sync<kAllConsumersBarrier, NT>();
-        if (tid == 0)
-            s_misc[0] = static_cast<int>(atomic_add_acq_rel(c, 1u));
-        named_bar_sync<kAllConsumersBarrier, NT>();
-        return s_misc[0];
-    };
-
-    if (S <= kGroupSplits) {
-        const int t = take_ticket(cnt);
-        if (tid == 0)
-            trace_event(p, kTrTicket, t != S - 1);
-        if (t != S - 1)
-            return;
-        merge_pass(p.part_o, p.part_ml, S, 0, S, true, nullptr, nullptr, 0, 0);
-        if (tid == 0) {
-            cnt[0] = 0u;                   // ready for the next call, which is ordered after this kernel
-            trace_event(p, kTrMerged, true);
-        }
-        return;
-    }
-    // two levels: the last CTA of split group g merges it; the last of the
-    // group mergers merges the groups
-    const int ng = (S + kGroupSplits - 1) / kGroupSplits;
-    const int gsp = split / kGroupSplits;
-    const int gsize = min(kGroupSplits, S - gsp * kGroupSplits);
-    const int t1 = take_ticket(cnt + 1 + gsp);
+    unsigned int *cnt = p.counters + tile_id;
+    named_bar_sync<kAllConsumersBarrier, NT>();
     if (tid == 0)
-        trace_event(p, kTrTicket, t1 != gsize - 1);
-    if (t1 != gsize - 1)
+        s_misc[0] = static_cast<int>(atomic_add_acq_rel(cnt, 1u));
+    named_bar_sync<kAllConsumersBarrier, NT>();
+    const int t = s_misc[0];
+    if (tid == 0)
+        trace_event(p, kTrTicket, t != S - 1);
+    if (t != S - 1)
         return;
-    merge_pass(p.part_o, p.part_ml, S, gsp * kGroupSplits, gsize, false, p.gpart_o, p.gpart_ml, ng, gsp);
-    if (tid == 0) {
-        cnt[1 + gsp] = 0u;
-        trace_event(p, kTrStats);
+
+    // rows s of every query row -> stg[(s * nq + q) * HD]
+    for (int e = tid; e < S * nq * kVec; e += NT) {
+        const int sq = e / kVec, d4 = e - sq * kVec;
+        const int sp = sq / nq, q = sq - sp * nq;
+        cp_async16(smem_u32(stg + static_cast<size_t>(sq) * HD + d4 * 4),
+                   p.part_o + (rowhead(q) * S + sp) * HD + d4 * 4);
     }
-    const int t2 = take_ticket(cnt);
-    if (t2 != ng - 1)
-        return;
-    merge_pass(p.gpart_o, p.gpart_ml, ng, 0, ng, true, nullptr, nullptr, 0, 0);
+    for (int q = warp; q < nq; q += NW) {
+        const float L = merge_stats_warp(p.part_ml + rowhead(q) * S, S, wts + q * kWStride, lane);
+        if (lane == 0)
+            wts[q * kWStride + kGroupSplits] = L;
+    }
+    cp_async_wait_all();
+    named_bar_sync<kAllConsumersBarrier, NT>();  // staged rows and weights visible to every thread
+    float4 oacc[kOwn];
+#pragma unroll
+    for (int k = 0; k < kOwn; ++k)
+        oacc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int sp = 0; sp < S; ++sp) {
+#pragma unroll
+        for (int k = 0; k < kOwn; ++k) {
+            const int e = tid + k * NT;
+            const int q = e / kVec, d4 = e - q * kVec;
+            if (q < nq)
+                fma4(oacc[k], wts[q * kWStride + sp],
+                     *reinterpret_cast<const float4 *>(stg + static_cast<size_t>(sp * nq + q) * HD + d4 * 4));
+        }
+    }
+#pragma unroll
+    for (int k = 0; k < kOwn; ++k) {
+        const int e = tid + k * NT;
+        const int q = e / kVec, d4 = e - q * kVec;
+        if (q < nq)
+            store_out4(p.o + rowhead(q) * HD + d4 * 4, oacc[k], wts[q * kWStride + kGroupSplits]);
+    }
     if (tid == 0) {
-        cnt[0] = 0u;
+        cnt[0] = 0u;                   // ready for the next call, which is ordered after this kernel
         trace_event(p, kTrMerged, true);
     }
 }
 
 // ---------------------------------------------------------------- combine kernel
 //
-// One CTA per (row, head), one thread per 4 dims: merges the S partials with
-// the same statistics routine and the same per-element fused multiply-add
-// order as the last-CTA path.  Reads rows*nh*S*(hd+2)*4 bytes, writes
+// One CTA per (row, head) and slice of up to 32 float4 of the head dimension
+// (hd / 128 slices, at least one), one lane per float4.  Warp w merges split
+// groups w, w + kCombineWarps, ...: a group's (m, l) and O loads are all in
+// flight at once, so the merge costs about one L2 round trip per level
+// instead of one per split.  Warp 0 then merges the groups.  The statistics
+// routine and the per-element fused multiply-add order are the in-kernel
+// merges', so up to kGroupSplits splits the two agree bit for bit.  Reads
+// rows*nh*S*(hd+2)*4 bytes (the (m, l) pairs once per slice), writes
 // rows*nh*hd*2.
+constexpr int kCombineWarps = 8;
+
+// float4 of the head dimension per CTA, and CTAs per (row, head)
 template <int HD>
-constexpr int combine_threads()
+__host__ __device__ constexpr int combine_slice()
 {
-    return HD / 4 < 32 ? 32 : HD / 4;
+    return HD / 4 < 32 ? HD / 4 : 32;
 }
 
 template <int HD>
-__global__ void __launch_bounds__(combine_threads<HD>()) decode_combine_kernel(const DecodeParams p)
+__host__ __device__ constexpr int combine_slices()
 {
-    __shared__ float wts[kMaxSplits + 2];          // weights of the splits (one level) or of the groups
-    __shared__ float gw[kMaxGroups][kGroupSplits]; // two levels: weights inside each group
-    __shared__ float2 gml[kMaxGroups];             // two levels: (M_g, L_g)
+    return HD / 4 / combine_slice<HD>();
+}
+
+// Warps of a combine CTA and its dynamic shared memory (the group outputs of
+// two-level merges), for S splits.
+__host__ __device__ constexpr int combine_warps(int S)
+{
+    return S <= kGroupSplits ? 1 : ((S + kGroupSplits - 1) / kGroupSplits < kCombineWarps
+                                         ? (S + kGroupSplits - 1) / kGroupSplits : kCombineWarps);
+}
+__host__ __device__ constexpr int combine_smem_bytes(int S)
+{
+    return S <= kGroupSplits ? 0 : (S + kGroupSplits - 1) / kGroupSplits * 32 * 16;
+}
+
+// The n <= kGroupSplits partial rows at src, src + HD/4, ... (zero beyond n
+// or off this lane's slice), every load issued before any is used.
+template <int HD>
+__device__ __forceinline__ void combine_load_group(float4 (&v)[kGroupSplits], const float4 *src, int n, bool mine)
+{
+#pragma unroll
+    for (int j = 0; j < kGroupSplits; ++j)
+        v[j] = (mine && j < n) ? __ldcg(src + static_cast<size_t>(j) * (HD / 4)) : make_float4(0.f, 0.f, 0.f, 0.f);
+}
+
+template <int HD>
+__global__ void __launch_bounds__(kCombineWarps * 32) decode_combine_kernel(const DecodeParams p)
+{
+    __shared__ float gw[kMaxGroups][kGroupSplits];   // weights inside each group (one level: gw[0])
+    __shared__ float2 gml[kMaxGroups];               // two levels: (M_g, L_g)
+    __shared__ float wts[kMaxGroups];                // two levels: weights of the groups
+    extern __shared__ float4 og[];                   // two levels: [group][32] unnormalised group outputs
     const size_t rh = blockIdx.x;
     const int S = p.splits;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int d4 = blockIdx.y * combine_slice<HD>() + lane;
+    const bool mine = lane < combine_slice<HD>();
     grid_dependency_wait();          // the split kernel's partials
     grid_launch_dependents();
-    const int d4 = threadIdx.x;
     const float4 *po = reinterpret_cast<const float4 *>(p.part_o + rh * S * HD) + d4;
-    if (S <= kGroupSplits) {
-        if (threadIdx.x < 32)
-            wts[kMaxSplits] = merge_stats_warp(p.part_ml + rh * S, S, wts, threadIdx.x);
-        __syncthreads();
-        if (d4 < HD / 4) {
-            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 8
-            for (int s = 0; s < S; ++s)
-                fma4(acc, wts[s], __ldcg(po + static_cast<size_t>(s) * (HD / 4)));
-            store_out4(p.o + rh * HD + d4 * 4, acc, wts[kMaxSplits]);
-        }
+    const float2 *pml = p.part_ml + rh * S;
+    float4 v[kGroupSplits];
+    if (S <= kGroupSplits) {         // one level, one warp
+        combine_load_group<HD>(v, po, S, mine);
+        const float L = merge_stats_warp(pml, S, gw[0], lane);
+        __syncwarp();
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int j = 0; j < kGroupSplits; ++j)
+            if (j < S)
+                fma4(acc, gw[0][j], v[j]);
+        if (mine)
+            store_out4(p.o + rh * HD + d4 * 4, acc, L);
         return;
     }
-    // two levels, as in the last-CTA path: groups of 8 splits, then the groups
+    // two levels: groups of 8 splits, each merged as above into (M_g, L_g, O_g), then the groups
     const int ng = (S + kGroupSplits - 1) / kGroupSplits;
-    if (threadIdx.x < 32) {
-        for (int g = 0; g < ng; ++g) {
-            const int n = min(kGroupSplits, S - g * kGroupSplits);
-            float m = 0.f;
-            const float L = merge_stats_warp(p.part_ml + rh * S + g * kGroupSplits, n, gw[g], threadIdx.x, &m);
-            if (threadIdx.x == 0)
-                gml[g] = make_float2(m, L);
-        }
+    const int nw = blockDim.x >> 5;
+    for (int g = warp; g < ng; g += nw) {
+        const int n = min(kGroupSplits, S - g * kGroupSplits);
+        combine_load_group<HD>(v, po + static_cast<size_t>(g) * kGroupSplits * (HD / 4), n, mine);
+        float m = 0.f;
+        const float L = merge_stats_warp(pml + g * kGroupSplits, n, gw[g], lane, &m);
+        if (lane == 0)
+            gml[g] = make_float2(m, L);
         __syncwarp();
-        constexpr int kPer = (kMaxGroups + 31) / 32;
-        float2 v[kPer];
+        float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-        for (int j = 0; j < kPer; ++j)
-            v[j] = gml[min(static_cast<int>(threadIdx.x) + 32 * j, ng - 1)];
-        wts[kMaxSplits] = merge_stats_values(v, ng, wts, threadIdx.x);
+        for (int j = 0; j < kGroupSplits; ++j)
+            if (j < n)
+                fma4(a, gw[g][j], v[j]);
+        og[g * 32 + lane] = a;
     }
     __syncthreads();
-    if (d4 < HD / 4) {
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        for (int g = 0; g < ng; ++g) {
-            const int n = min(kGroupSplits, S - g * kGroupSplits);
-            float4 og = make_float4(0.f, 0.f, 0.f, 0.f);
-            for (int j = 0; j < n; ++j)
-                fma4(og, gw[g][j], __ldcg(po + static_cast<size_t>(g * kGroupSplits + j) * (HD / 4)));
-            fma4(acc, wts[g], og);
-        }
-        store_out4(p.o + rh * HD + d4 * 4, acc, wts[kMaxSplits]);
-    }
+    if (warp != 0)
+        return;
+    constexpr int kPer = (kMaxGroups + 31) / 32;
+    float2 sv[kPer];
+#pragma unroll
+    for (int j = 0; j < kPer; ++j)
+        sv[j] = gml[min(lane + 32 * j, ng - 1)];
+    const float L = merge_stats_values(sv, ng, wts, lane);
+    __syncwarp();
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int g = 0; g < ng; ++g)
+        fma4(acc, wts[g], og[g * 32 + lane]);
+    if (mine)
+        store_out4(p.o + rh * HD + d4 * 4, acc, L);
 }
 
 }  // namespace pgqa

@@ -17,6 +17,26 @@ struct LaunchArgs {
 // Dynamic shared memory the split kernel of head dimension `hd` asks for.
 int split_kernel_smem_bytes(int hd);
 
+// The combine kernel alone, over rows * nh (row, head) pairs of p.splits
+// partials in p.part_o / p.part_ml, into p.o.  It may overlap the tail of the
+// kernel before it (programmatic dependent launch) and waits for it before
+// reading the partials.
+template <int HD>
+cudaError_t launch_combine(const DecodeParams &p, cudaStream_t stream)
+{
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t c2 = {};
+    c2.gridDim = dim3(static_cast<unsigned>(p.rows) * p.nh, combine_slices<HD>());
+    c2.blockDim = dim3(32 * combine_warps(p.splits));
+    c2.dynamicSmemBytes = combine_smem_bytes(p.splits);
+    c2.stream = stream;
+    c2.attrs = attr;
+    c2.numAttrs = 1;
+    return cudaLaunchKernelEx(&c2, decode_combine_kernel<HD>, p);
+}
+
 template <int HD>
 cudaError_t launch_decode(const LaunchArgs &a, bool set_attr)
 {
@@ -54,35 +74,9 @@ cudaError_t launch_decode(const LaunchArgs &a, bool set_attr)
     cudaError_t e = cudaLaunchKernelEx(&cfg, decode_split_kernel<HD>, *a.tm_k, *a.tm_v, p);
     if (e != cudaSuccess)
         return e;
-    if (p.splits > 1 && p.counters == nullptr) {
-        cudaLaunchConfig_t c2 = {};
-        c2.gridDim = dim3(p.rows * p.nh);
-        c2.blockDim = dim3(combine_threads<HD>());
-        c2.dynamicSmemBytes = 0;
-        c2.stream = a.stream;
-        c2.attrs = attr;
-        c2.numAttrs = 1;
-        e = cudaLaunchKernelEx(&c2, decode_combine_kernel<HD>, p);
-    }
+    if (p.splits > 1 && p.counters == nullptr)
+        e = launch_combine<HD>(p, a.stream);
     return e;
-}
-
-// The combine kernel alone, over rows * nh (row, head) pairs of p.splits
-// partials in p.part_o / p.part_ml, into p.o.
-template <int HD>
-cudaError_t launch_combine(const DecodeParams &p, cudaStream_t stream)
-{
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cudaLaunchConfig_t c2 = {};
-    c2.gridDim = dim3(static_cast<unsigned>(p.rows) * p.nh);
-    c2.blockDim = dim3(combine_threads<HD>());
-    c2.dynamicSmemBytes = 0;
-    c2.stream = stream;
-    c2.attrs = attr;
-    c2.numAttrs = 1;
-    return cudaLaunchKernelEx(&c2, decode_combine_kernel<HD>, p);
 }
 
 // How many clusters of `cluster` split CTAs can be resident at once (0: the

@@ -58,15 +58,27 @@ def test_constants_agree_between_header_kernels_and_binding():
 
 
 def test_part_bytes_and_counter_count(lib):
-    assert pgqa.decode_part_bytes(4, 16, 8, 256) == 4 * 16 * 8 * 258 * 4          # one merge level
-    assert pgqa.decode_part_bytes(4, 16, 9, 256) == 4 * 16 * (9 + 2) * 258 * 4 + 16  # + 2 groups of 8
-    assert pgqa.decode_part_bytes(1, 32, 38, 512) == 32 * (38 + 5) * 514 * 4 + 16
+    assert pgqa.decode_part_bytes(4, 16, 8, 256) == 4 * 16 * 8 * 258 * 4     # f32 O, max and sum per split
+    assert pgqa.decode_part_bytes(4, 16, 9, 256) == 4 * 16 * 9 * 258 * 4
+    assert pgqa.decode_part_bytes(1, 32, 38, 512) == 32 * 38 * 514 * 4
     assert pgqa.decode_part_bytes(1, 32, 1, 512) == 32 * 514 * 4
     assert pgqa.decode_part_bytes(0, 16, 9, 256) == 0
-    assert pgqa.decode_counter_count(4, 16, 8) == 32 * 33     # g = 2: one subgroup per kv head
-    assert pgqa.decode_counter_count(1, 32, 2) == 4 * 33      # g = 16: two subgroups of 8 heads
-    assert pgqa.decode_counter_count(2, 24, 2) == 8 * 33      # g = 12: two subgroups
+    assert pgqa.decode_counter_count(4, 16, 8) == 32          # g = 2: one subgroup per kv head
+    assert pgqa.decode_counter_count(1, 32, 2) == 4           # g = 16: two subgroups of 8 heads
+    assert pgqa.decode_counter_count(2, 24, 2) == 8           # g = 12: two subgroups
     assert pgqa.decode_counter_count(2, 10, 3) == 0           # nh % nkv != 0
+
+
+def test_decode_kernel_count(lib):
+    """The in-kernel merges take up to 8 splits; more, or no counters, add the combine kernel."""
+    assert pgqa.decode_kernel_count(1, False) == 1 and pgqa.decode_kernel_count(1, True) == 1
+    for s in (2, 4, 5, 8):
+        assert pgqa.decode_kernel_count(s, True) == 1
+        assert pgqa.decode_kernel_count(s, False) == 2
+    for s in (9, 38, 256):
+        assert pgqa.decode_kernel_count(s, True) == 2
+        assert pgqa.decode_kernel_count(s, False) == 2
+    assert pgqa.decode_kernel_count(0, True) == 0 and pgqa.decode_kernel_count(257, False) == 0
 
 
 def test_choose_splits_rule(lib):
