@@ -3,7 +3,8 @@
 The three gates follow the `run` function of span-02
 ``engine/crates/kernels/tests/gpu.rs``:
   1. rel-RMS of the bf16 output against the oracle's bf16 output < 1e-2;
-  2. merge counters (last CTA merges) == separate combine kernel, bit for bit;
+  2. merge counters (the split kernel merges, up to 8 splits) == separate combine
+     kernel, bit for bit;
   3. identity pool == permuted pool behind a page map with the NaN null page 0
      for pages outside every row's window, bit for bit (also with the map
      folded into the block table).
@@ -106,6 +107,18 @@ def test_head_dims_and_group_sizes(hd, nh, nkv):
     """g = 1, 8, 16 (two head subgroups per kv head) and 12 (a partial subgroup)."""
     c = wl.page_case(nh, nkv, hd, 0, 200, 2, dist="sym", seed=hd + nh)
     full_gates(c, splits=3, mapped=False)
+
+
+@pytest.mark.parametrize("hd", [64, 128, 256, 512])
+@pytest.mark.parametrize("splits", [9, 13, 70])
+def test_two_level_combine_every_head_dim(hd, splits):
+    """Above 8 splits the combine kernel merges in two levels, with or without counters (which it leaves
+    untouched): ragged last groups (9 = 8 + 1, 13 = 8 + 5, 70 = 8 * 8 + 6), every count of 128-dim slices
+    (hd 64 uses half the lanes), g = 8 so every CTA serves 8 query rows."""
+    import paged_gqa_decode_attn_gb300 as pgqa
+    assert pgqa.decode_kernel_count(splits, True) == 2
+    c = wl.page_case(16, 2, hd, 0, 90 * 16 + 7, 2, dist="sym", seed=hd + splits)
+    full_gates(c, splits=splits, mapped=False)
 
 
 @pytest.mark.parametrize("hd", [64, 128, 256, 512])
