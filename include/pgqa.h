@@ -84,8 +84,10 @@ extern "C" {
  *
  * Host scalars: rows >= 0, nh, nkv > 0 with nh % nkv == 0, hd in
  * {64, 128, 256, 512}, window >= 0 (0 = full causal), 1 <= splits <=
- * PGQA_MAX_SPLITS.  The output for a given (inputs, splits) does not depend on
- * which physical pages hold the data.
+ * PGQA_MAX_SPLITS.  Grid limits: rows <= 65535, nkv * ceil((nh / nkv) / 8)
+ * <= 65535 and, with splits > 1, rows * nh <= INT_MAX; beyond them the call
+ * returns PGQA_ERR_INVALID_ARGUMENT.  The output for a given (inputs, splits)
+ * does not depend on which physical pages hold the data.
  *
  * Row packing: consecutive rows in groups of max(1, 8 / (nh / nkv)) that share
  * their block-table span (equal off) and whose visible ranges pairwise
@@ -222,7 +224,8 @@ int pgqa_attn_prefill(void *o, const void *q, const void *k_pool, const void *v_
  * sums run in another order).
  *   part   device scratch of at least pgqa_decode_part_bytes(rows, nh, splits, hd)
  *          bytes, 16-byte aligned, caller-owned (not read before written)
- *   rows   the number of rows; every row must be in exactly one tile
+ *   rows   the number of rows; every row must be in exactly one tile; with
+ *          splits > 1, rows * nh <= INT_MAX (else PGQA_ERR_INVALID_ARGUMENT)
  *   splits 1..PGQA_MAX_SPLITS; 1 is pgqa_attn_prefill (part unused)
  * Other arguments as for pgqa_attn_prefill.  hd 64, 128 or 256 for splits > 1
  * (PGQA_ERR_UNSUPPORTED_HD otherwise).  Asynchronous on `stream`; two kernels.

@@ -8,6 +8,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <climits>
 #include <cstdint>
 #include <cstring>
 #include <mutex>
@@ -403,6 +404,8 @@ int pgqa_attn_decode(void *o, void *part, const void *q, const void *k_pool, con
     const int hsg = (g + pgqa::kQRows - 1) / pgqa::kQRows;
     if (rows > 65535 || static_cast<long long>(nkv) * hsg > 65535)
         return PGQA_ERR_INVALID_ARGUMENT;
+    if (splits > 1 && static_cast<long long>(rows) * nh > INT_MAX)    // the combine kernel's grid
+        return PGQA_ERR_INVALID_ARGUMENT;
     if (!aligned(k_pool, 16) || !aligned(v_pool, 16) || !aligned(q, 16) || !aligned(o, 16) ||
         (splits > 1 && !aligned(part, 16)))
         return PGQA_ERR_MISALIGNED;
@@ -537,7 +540,7 @@ int prefill_call(void *o, void *part, const void *q, const void *k_pool, const v
         return PGQA_OK;
     if (!o || !q || !k_pool || !v_pool || !block_table || !off || !qpos || !tile_t0 || !tile_tn)
         return PGQA_ERR_INVALID_ARGUMENT;
-    if (splits > 1 && (!part || rows < 1))
+    if (splits > 1 && (!part || rows < 1 || static_cast<long long>(rows) * nh > INT_MAX))
         return PGQA_ERR_INVALID_ARGUMENT;
     if (splits > 1 && !aligned(part, 16))
         return PGQA_ERR_MISALIGNED;

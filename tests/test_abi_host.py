@@ -156,6 +156,7 @@ def call(lib, rows=1, nh=8, nkv=2, hd=128, window=0, splits=1, o=FAKE, part=FAKE
     (dict(splits=2, part=None), -1), (dict(k=FAKE + 8), -3), (dict(v=FAKE + 2), -3),
     (dict(q=FAKE + 4), -3), (dict(o=FAKE + 8), -3), (dict(splits=2, part=FAKE + 4), -3),
     (dict(rows=70000), -1),
+    (dict(rows=65535, nh=65536, nkv=8192, splits=2), -1),   # rows * nh > INT_MAX: the combine grid
 ])
 def test_bad_arguments_are_rejected_before_any_cuda_call(lib, kw, code):
     assert call(lib, **kw) == code
@@ -232,7 +233,8 @@ def split_call(lib, splits=2, rows=4, hd=128, part=FAKE, ntiles=1, nh=8, nkv=2):
 
 @pytest.mark.parametrize("kw,code", [
     ({"splits": 0}, -1), ({"splits": 257}, -7), ({"hd": 512}, -2), ({"hd": 96}, -2), ({"part": None}, -1),
-    ({"rows": 0}, -1), ({"part": FAKE + 4}, -3), ({"nh": 6, "nkv": 4}, -1)])
+    ({"rows": 0}, -1), ({"part": FAKE + 4}, -3), ({"nh": 6, "nkv": 4}, -1),
+    ({"rows": 65535, "nh": 65536, "nkv": 8192}, -1)])
 def test_prefill_split_bad_arguments_are_rejected_before_any_cuda_call(lib, kw, code):
     """splits 1..256; hd 512 has no split path; scratch and a row count with splits > 1; 16-byte alignment."""
     assert split_call(lib, **kw) == code
