@@ -141,6 +141,16 @@ int pgqa_decode_kernel_count(int splits, int with_counters);
 int pgqa_device_status(void);
 
 /*
+ * Self-test of the failure path above: enqueues on `stream` one CTA that
+ * waits, through the kernels' own bounded wait, on an mbarrier that nothing
+ * arrives on.  After about one second of SM clock it gives up and records a
+ * timeout, so the next pgqa_device_status returns PGQA_ERR_DEVICE_TIMEOUT;
+ * nothing faults, traps or hangs, and later calls run normally.  Returns
+ * PGQA_OK once enqueued, or PGQA_ERR_CUDA.
+ */
+int pgqa_selftest_bounded_wait(void *stream);
+
+/*
  * Debug tracing.  In a library built with PGQA_TRACE defined, every split-kernel
  * CTA of later calls writes 32 uint64 slots into device_buffer: the global
  * timer (ns) at up to 16 phase boundaries in slots 0-15 and the SM cycle

@@ -32,6 +32,7 @@ SIGNATURES = {
     "pgqa_decode_part_bytes": (ctypes.c_size_t, [_I, _I, _I, _I]),
     "pgqa_decode_counter_count": (ctypes.c_size_t, [_I, _I, _I]),
     "pgqa_decode_kernel_count": (_I, [_I, _I]),
+    "pgqa_selftest_bounded_wait": (_I, [_P]),
     "pgqa_device_status": (_I, []),
     "pgqa_strerror": (ctypes.c_char_p, [_I]),
     "pgqa_version": (_I, []),
@@ -216,6 +217,13 @@ def device_status() -> None:
     st = load().pgqa_device_status()
     if st != PGQA_OK:
         raise PgqaError(st, "device_status")
+
+
+def selftest_bounded_wait(stream=None) -> None:
+    """Enqueue the bounded-wait self-test; the next device_status() then raises PGQA_ERR_DEVICE_TIMEOUT."""
+    st = load().pgqa_selftest_bounded_wait(_stream(stream))
+    if st != PGQA_OK:
+        raise PgqaError(st, "selftest_bounded_wait")
 
 
 def trace_buffer(buf) -> bool:

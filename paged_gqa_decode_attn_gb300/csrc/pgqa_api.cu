@@ -211,6 +211,8 @@ int split_kernel_smem_bytes(int hd)
     default: return 0;
     }
 }
+
+cudaError_t launch_bounded_wait_probe(unsigned int *err, cudaStream_t stream);   // pgqa_selftest.cu
 }  // namespace pgqa
 
 extern "C" {
@@ -382,6 +384,18 @@ int pgqa_device_status(void)
         return (word & pgqa::kErrTileRows) ? PGQA_ERR_TILE_TOO_LONG : PGQA_ERR_DEVICE_TIMEOUT;
     }
     return PGQA_OK;
+}
+
+int pgqa_selftest_bounded_wait(void *stream)
+{
+    std::lock_guard<std::mutex> lock(g_mutex);
+    DeviceState *s = nullptr;
+    const int st = device_state(&s);
+    if (st != PGQA_OK)
+        return st;
+    return pgqa::launch_bounded_wait_probe(s->err, static_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? PGQA_OK
+               : PGQA_ERR_CUDA;
 }
 
 int pgqa_attn_decode(void *o, void *part, const void *q, const void *k_pool, const void *v_pool,

@@ -245,6 +245,23 @@ def test_zero_rows_is_a_no_op():
     assert int(x.abs().sum().item()) == 0
 
 
+def test_bounded_wait_gives_up_and_the_context_stays_usable():
+    """A wait that nothing ends (the library's self-test kernel, the kernels' own bounded wait) gives up
+    after about a second: device_status reports the timeout once, and the next decode passes the gates."""
+    import torch
+    import paged_gqa_decode_attn_gb300 as pgqa
+    from paged_gqa_decode_attn_gb300 import _lib
+    pgqa.device_status()
+    pgqa.selftest_bounded_wait()
+    torch.cuda.synchronize()
+    with pytest.raises(pgqa.PgqaError) as ei:
+        pgqa.device_status()
+    assert ei.value.status == _lib.PGQA_ERR_DEVICE_TIMEOUT
+    pgqa.device_status()              # read once, then clear
+    full_gates(wl.page_case(8, 2, 128, 0, 300, 3, dist="sym", seed=11), splits=3, mapped=False)
+    pgqa.device_status()
+
+
 def test_device_status_clean_after_runs():
     import paged_gqa_decode_attn_gb300 as pgqa
     from gpu_util import DevCase
