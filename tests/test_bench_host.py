@@ -1,0 +1,99 @@
+"""The benchmark's algorithmic byte and FLOP counts against brute-force enumeration.
+
+Every roofline number divides one of these counts by a measured time, so each
+is checked here on the CPU against a count that enumerates what the call has
+to touch: every (block-table span, position) some row sees, read once per kv
+head for K and V, plus Q in and O out; every (row, visible position) pair for
+prefill; every head vector read and written for the QK-norm / RoPE write.
+"""
+import importlib.util
+import os
+import random
+import sys
+
+import numpy as np
+import pytest
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+ROOT = os.path.dirname(HERE)
+sys.path.insert(0, ROOT)
+
+from paged_gqa_decode_attn_gb300 import workloads as wl  # noqa: E402
+
+
+def _bench():
+    spec = importlib.util.spec_from_file_location("bench_under_test", os.path.join(ROOT, "bench.py"))
+    mod = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(mod)
+    return mod
+
+
+def visible(qp, kv, window):
+    lo = max(0, qp + 1 - window) if window > 0 else 0
+    return range(lo, kv + 1)
+
+
+def brute_decode_bytes(nh, nkv, hd, window, qpos, off, kvpos=None):
+    seen = set()
+    for r, qp in enumerate(qpos):
+        kv = qp if kvpos is None else kvpos[r]
+        for t in visible(qp, kv, window):
+            seen.add((off[r], t))
+    return len(seen) * nkv * hd * 2 * 2 + 2 * len(qpos) * nh * hd * 2
+
+
+@pytest.mark.parametrize("seed", range(40))
+def test_decode_bytes_match_brute_force(seed):
+    rng = random.Random(seed)
+    nkv = rng.choice([1, 2, 4, 8])
+    nh = nkv * rng.choice([1, 2, 3, 8])
+    hd = rng.choice([64, 128, 256, 512])
+    window = rng.choice([0, 0, 1, 5, 17, 64, 300])
+    rows = rng.randint(1, 9)
+    spans = [0, 100, 250][:rng.randint(1, 3)]
+    off = [rng.choice(spans) for _ in range(rows)]
+    qpos = [rng.randint(0, 400) for _ in range(rows)]
+    kvpos = None
+    if rng.random() < 0.4:       # some rows see less than their query position (or nothing)
+        kvpos = [max(-1, q - rng.randint(0, 50)) for q in qpos]
+    got = wl.algorithmic_bytes(nh, nkv, hd, window, qpos, off, kvpos)
+    assert got == brute_decode_bytes(nh, nkv, hd, window, qpos, off, kvpos)
+
+
+def test_sweep_bytes_equal_the_decode_count_at_every_point():
+    b = _bench()
+    for hd, ctx, rows, window in wl.sweep_points():
+        qpos = list(range(ctx - rows, ctx))
+        assert b.sweep_bytes(hd, ctx, rows, window) == wl.algorithmic_bytes(32, 16, hd, window, qpos, [0] * rows)
+
+
+@pytest.mark.parametrize("seed", range(12))
+def test_prefill_flops_match_brute_force(seed):
+    b = _bench()
+    rng = random.Random(100 + seed)
+    nkv = rng.choice([1, 2, 8])
+    nh = nkv * rng.choice([1, 2, 4])
+    hd = rng.choice([64, 128, 256])
+    window = rng.choice([0, 3, 64, 1000])
+    rows = rng.randint(1, 40)
+    qpos = np.array([rng.randint(0, 300) for _ in range(rows)], dtype=np.int32)
+    kvpos = None
+    if seed % 2:
+        kvpos = np.array([q - rng.randint(-5, 20) for q in qpos], dtype=np.int32)
+
+    class C:
+        pass
+    c = C()
+    c.qpos, c.kvpos, c.window, c.nh, c.hd = qpos, kvpos, window, nh, hd
+    pairs = 0
+    for r in range(rows):
+        hi = int(qpos[r]) if kvpos is None else min(int(qpos[r]), int(kvpos[r]))
+        pairs += sum(1 for _ in visible(int(qpos[r]), hi, window))
+    assert b.prefill_flops(c) == pairs * 4 * nh * hd
+
+
+def test_prep_bytes_count_every_head_vector_once_each_way():
+    c = wl.prep_case(8, 2, 128, 64, 33, 200, positions="scattered", seed=1)
+    read = c.q_in.size + c.k_in.size + c.v_in.size          # bf16 elements read
+    written = c.rows * c.nh * c.hd + 2 * c.rows * c.nkv * c.hd   # q_out, and K and V into the pools
+    assert c.bytes_moved() == 2 * (read + written)
