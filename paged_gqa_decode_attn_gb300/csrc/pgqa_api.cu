@@ -35,11 +35,11 @@ struct DeviceState {
 };
 
 // Cluster size for the on-chip merge of `splits` CTAs, or 0 to merge through
-// global memory.  Clusters of 2 and 4 are taken whenever any fit (the short
-// loops that choose them measured faster so than through the last CTA, even
-// with a second wave); clusters of 8 only when all `live` ones (one per tile
-// that does work) are resident at once: the split rule picks 8 beside fewer
-// resident clusters only for long loops, where a waiting cluster would
+// global memory.  Clusters of 2 and 4 are taken whenever any fit (for the
+// short loops that choose them, a second wave of clusters measured faster
+// than the last-CTA merge); clusters of 8 only when all `live` ones (one per
+// tile that does work) are resident at once: the split rule picks 8 beside
+// fewer resident clusters only for long loops, where a waiting cluster would
 // double its tile's time.  Caller holds g_mutex.
 int on_chip_cluster(DeviceState *s, int hi, int hd, int splits, long long live)
 {
@@ -49,7 +49,6 @@ int on_chip_cluster(DeviceState *s, int hi, int hd, int splits, long long live)
     case 4: lg = 2; break;
     case 8: lg = 3; break;
     default: return 0;          // 16-CTA clusters rarely all fit beside each other
-
     }
     int &cap = s->cluster_cap[hi][lg];
     if (cap < 0) {
