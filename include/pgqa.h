@@ -168,8 +168,9 @@ int pgqa_trace_buffer(void *device_buffer, size_t bytes);
  * `part` and `counters` (a plugin inside a host runtime that owns all device
  * allocations, or a caller that must not call cudaMalloc on its path).
  *
- * Same arguments and result as pgqa_attn_decode with the last-CTA merge,
- * minus part and counters: those live in one static device array of this
+ * Same arguments and result as pgqa_attn_decode given merge counters (the
+ * split kernel merges up to 8 splits, the combine kernel more), minus part
+ * and counters: those live in one static device array of this
  * library (PGQA_NOALLOC_MAX_COUNTERS uint32 counters followed by
  * PGQA_NOALLOC_MAX_PART_BYTES of partials, about 8.1 MiB), which every GPU
  * that loads the library holds until the process exits.  Calls needing more

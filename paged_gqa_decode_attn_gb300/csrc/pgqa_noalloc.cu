@@ -12,7 +12,7 @@
 // This entry point allocates nothing: no cudaMalloc, no cudaFree, no
 // allocating library routine.  It clears the merge counters it will use with
 // cudaMemsetAsync on the caller's stream, then enqueues the ordinary
-// pgqa_attn_decode with the last-CTA merge, pointed at the static scratch.
+// pgqa_attn_decode with merge counters, pointed at the static scratch.
 #include <cuda_runtime.h>
 
 #include <cstdint>

@@ -39,6 +39,31 @@ def test_header_declares_the_entry_points():
     assert set(names) <= set(_lib.SIGNATURES), "binding lacks a declared function"
 
 
+def test_every_declaration_has_its_own_doc_comment():
+    """Each function of the boundary is documented where it is declared: the nearest non-blank,
+    non-#define line above the declaration closes a comment."""
+    lines = open(HEADER).read().splitlines()
+    in_comment = False
+    checked = []
+    for i, ln in enumerate(lines):
+        s = ln.strip()
+        if in_comment:
+            in_comment = "*/" not in s
+            continue
+        if s.startswith("/*"):
+            in_comment = "*/" not in s
+            continue
+        m = re.match(r"(?:const\s+)?[\w ]+?\*?\s*(pgqa_\w+)\s*\(", s)
+        if not m or s.startswith("#"):
+            continue
+        j = i - 1
+        while j >= 0 and (not lines[j].strip() or lines[j].strip().startswith("#define")):
+            j -= 1
+        assert j >= 0 and lines[j].strip().endswith("*/"), f"{m.group(1)} has no doc comment above it"
+        checked.append(m.group(1))
+    assert set(checked) == set(declared_functions())
+
+
 def test_library_exports_every_declared_symbol(lib):
     for n in declared_functions():
         assert hasattr(lib, n), n
