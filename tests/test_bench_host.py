@@ -5,6 +5,7 @@ is checked here on the CPU against a count that enumerates what the call has
 to touch: every (block-table span, position) some row sees, read once per kv
 head for K and V, plus Q in and O out; every (row, visible position) pair for
 prefill; every head vector read and written for the QK-norm / RoPE write.
+The reference arm, which needs no GPU, is run here too, for the keys of its line.
 """
 import importlib.util
 import os
@@ -97,3 +98,25 @@ def test_prep_bytes_count_every_head_vector_once_each_way():
     read = c.q_in.size + c.k_in.size + c.v_in.size          # bf16 elements read
     written = c.rows * c.nh * c.hd + 2 * c.rows * c.nkv * c.hd   # q_out, and K and V into the pools
     assert c.bytes_moved() == 2 * (read + written)
+
+
+def test_reference_arm_prints_the_contract_line():
+    """`bench.py --impl reference` runs the oracle on the host cores alone and prints one JSON line with the
+    contract's keys; its cpu_baseline and e2e repeat the line's own value, with no host-device bytes."""
+    import json
+    import subprocess
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--workload", "tiny",
+                        "--steps", "2", "--warmup", "1", "--ref-budget", "1"],
+                       capture_output=True, text=True, timeout=600, cwd=ROOT)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [ln for ln in r.stdout.splitlines() if ln.strip()]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    for k in ("impl", "metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better",
+              "scaling", "vs_baseline", "dtype", "data", "config", "cpu_baseline", "e2e"):
+        assert k in d, k
+    assert d["impl"] == "reference" and d["steps"] == 2 and d["warmup"] == 1 and d["n_gpus"] == 1
+    assert d["value"] > 0 and d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["value"] == d["value"]
+    assert d["cpu_baseline"]["cores"] >= 1
+    assert d["e2e"]["value"] == d["value"] and d["e2e"]["h2d_bytes_per_step"] == 0
+    assert d["e2e"]["d2h_bytes_per_step"] == 0 and d["config"]["workload"].startswith("tiny")
