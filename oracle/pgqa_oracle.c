@@ -21,8 +21,11 @@
  *
  * Readings where the page is silent:
  *  - `kvpos` (the second position array the page passes, always equal to
- *    qpos there) is the last visible KV position of the row: the row attends
- *    over [lo, kvpos[t]], lo still taken from qpos.  NULL means kvpos = qpos.
+ *    qpos there) is the last KV position written for the row.  The `reference`
+ *    range ends at the query's own position (`lo..=qp`: the attention is
+ *    causal), so the second array can only shorten it: the row attends over
+ *    [lo, min(qpos[t], kvpos[t])], lo still taken from qpos.  NULL means
+ *    kvpos = qpos.
  *  - The page map composes after the block table: page_map[block_table[.]].
  *  - A row with no visible position (kvpos < lo) yields zeros.
  *
@@ -79,7 +82,9 @@ static void row_head(const job_t *j, int t, int h, double *o, double *s)
 {
     int hd = j->hd;
     int qp = j->qpos[t];
-    int hi = j->kvpos ? j->kvpos[t] : qp;
+    int hi = qp;                      /* causal: no position past the query's own */
+    if (j->kvpos && j->kvpos[t] < hi)
+        hi = j->kvpos[t];             /* the second position array only shortens the range */
     int lo = 0;
     if (j->window > 0) {
         lo = qp + 1 - j->window;
@@ -126,7 +131,7 @@ static int max_len(const job_t *j)
     int best = 1;
     for (int t = 0; t < j->rows; t++) {
         int qp = j->qpos[t];
-        int hi = j->kvpos ? j->kvpos[t] : qp;
+        int hi = j->kvpos && j->kvpos[t] < qp ? j->kvpos[t] : qp;
         int lo = j->window > 0 ? qp + 1 - j->window : 0;
         if (lo < 0)
             lo = 0;

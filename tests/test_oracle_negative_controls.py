@@ -25,8 +25,8 @@ MUTATIONS = {
     "score_sign": ("acc += bf16_value(qv[d]) * bf16_value(kv[d]);",
                    "acc -= bf16_value(qv[d]) * bf16_value(kv[d]);"),
     "offset_ignored": ("j->block_table[(int64_t)j->off[t] + p / 16]", "j->block_table[p / 16]"),
-    "kvpos_ignored": ("int hi = j->kvpos ? j->kvpos[t] : qp;\n    int lo = 0;",
-                      "int hi = qp;\n    int lo = 0;"),
+    "kvpos_ignored": ("if (j->kvpos && j->kvpos[t] < hi)", "if (0)"),
+    "kvpos_clamp_dropped": ("if (j->kvpos && j->kvpos[t] < hi)", "if (j->kvpos)"),
 }
 
 

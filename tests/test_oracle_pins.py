@@ -181,8 +181,10 @@ def test_large_scores_stay_finite():
 
 def _brute_force_mp(qv, dense_k, dense_v, qpos, kvpos, window, kh, mp):
     """Softmax without max-subtraction, in 50-digit arithmetic, over the set
-    {p : p <= kvpos and (window == 0 or qpos - p < window)}."""
-    vis = [p for p in range(0, kvpos + 1) if window == 0 or qpos - p < window]
+    {p : p <= qpos (causal), p <= kvpos, and (window == 0 or qpos - p < window)},
+    each condition tested on its own for every position of the dense context."""
+    vis = [p for p in range(dense_k.shape[0])
+           if p <= qpos and p <= kvpos and (window == 0 or qpos - p < window)]
     if not vis:
         return [mp.mpf(0)] * len(qv)
     s = [mp.fsum(mp.mpf(float(a)) * mp.mpf(float(b)) for a, b in zip(qv, dense_k[p, kh]))
@@ -219,7 +221,8 @@ def test_brute_force_tiny_cases():
         for r in range(rows):
             bt[offs[r]:offs[r] + npg] = table
         qpos = rng.integers(0, ctx, size=rows).astype(np.int32)
-        kvpos = np.minimum(qpos + rng.integers(0, 3, size=rows), ctx - 1).astype(np.int32)
+        # the second position array both below and past qpos (past it, causality must win)
+        kvpos = np.minimum(qpos + rng.integers(-3, 4, size=rows), ctx - 1).astype(np.int32)
         q = wl.bf16_trunc(rng.standard_normal(rows * nh * hd).astype(np.float32))
         o64, _ = run_oracle(q, kp, vp, bt, offs, qpos, nh, nkv, hd, window, kvpos=kvpos)
         dkv = wl.bf16_to_f32(dk).astype(np.float64)
@@ -339,6 +342,46 @@ def test_row_with_no_visible_position_is_zero():
     # window 4 at qpos 30 starts at 27; kvpos 20 < 27 leaves nothing visible
     o64, o16 = run_oracle(q, kp, vp, bt, np.zeros(1, np.int32), [30], nh, nkv, hd, 4, kvpos=[20])
     assert np.all(o64 == 0.0) and np.all(o16 == 0)
+
+
+def test_kvpos_past_qpos_is_causal():
+    """The page's ``reference`` attends over ``lo..=qp``: the attention is causal, so a second
+    position array past qpos must give exactly the result of kvpos = qpos, and a distinct V at the
+    positions past qpos must not leak into the output."""
+    rng = np.random.default_rng(11)
+    nh, nkv, hd, ctx = 4, 2, 8, 64
+    dk = wl.bf16_trunc(rng.standard_normal((ctx, nkv, hd)).astype(np.float32))
+    dv = wl.bf16_trunc(rng.standard_normal((ctx, nkv, hd)).astype(np.float32))
+    dv[41:] = bf(np.full((ctx - 41, nkv, hd), 1000.0, np.float32))      # loud V past every qpos
+    dk[41:] = bf(np.full((ctx - 41, nkv, hd), 4.0, np.float32))         # and keys that would win
+    kp, vp, bt = build_pool(dk, dv)
+    qpos = [40, 33, 7]
+    q = bf(np.abs(wl.bf16_to_f32(wl.bf16_trunc(rng.standard_normal(3 * nh * hd).astype(np.float32)))))
+    for window in (0, 5):
+        a64, a16 = run_oracle(q, kp, vp, bt, np.zeros(3, np.int32), qpos, nh, nkv, hd, window,
+                              kvpos=qpos)
+        b64, b16 = run_oracle(q, kp, vp, bt, np.zeros(3, np.int32), qpos, nh, nkv, hd, window,
+                              kvpos=[63, 40, 9])
+        assert np.array_equal(a64, b64) and np.array_equal(a16, b16)
+        assert np.all(np.abs(b64) < 10.0)          # nothing of the loud V past qpos
+        n64, _ = run_oracle(q, kp, vp, bt, np.zeros(3, np.int32), qpos, nh, nkv, hd, window)
+        assert np.array_equal(a64, n64)            # NULL kvpos means kvpos = qpos
+
+
+def test_kvpos_below_qpos_shortens_the_range():
+    """kvpos < qpos: the row sees [lo, kvpos] only; with Q = 0 the output is that range's mean of V."""
+    rng = np.random.default_rng(12)
+    nh, nkv, hd, ctx = 2, 1, 8, 50
+    dk = wl.bf16_trunc(rng.standard_normal((ctx, nkv, hd)).astype(np.float32))
+    dv = wl.bf16_trunc(rng.standard_normal((ctx, nkv, hd)).astype(np.float32))
+    kp, vp, bt = build_pool(dk, dv)
+    q = np.zeros(nh * hd, dtype=np.uint16)
+    for window, qp, kv in ((0, 45, 30), (20, 45, 30), (20, 45, 26)):
+        o64, _ = run_oracle(q, kp, vp, bt, np.zeros(1, np.int32), [qp], nh, nkv, hd, window, kvpos=[kv])
+        first = 0 if window == 0 else qp + 1 - window
+        vis = wl.bf16_to_f32(dv[first:kv + 1, 0]).astype(np.float64)
+        for d in range(hd):
+            assert o64[0, 0, d] == pytest.approx(math.fsum(vis[:, d]) / vis.shape[0], rel=1e-14, abs=1e-15)
 
 
 def test_pairs_and_threads_do_not_change_results():
