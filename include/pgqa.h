@@ -12,7 +12,7 @@
  *
  *   for every query row r and head h, kv head kh = h / (nh / nkv):
  *     lo   = window > 0 ? max(0, qpos[r] + 1 - window) : 0
- *     hi   = kvpos ? kvpos[r] : qpos[r]
+ *     hi   = kvpos ? min(qpos[r], kvpos[r]) : qpos[r]     (causal)
  *     o[r,h,:] = softmax_p( q[r,h,:] . K[p,kh,:] ) @ V[p,kh,:],  p in [lo, hi]
  *
  * with scale 1.0 (no 1/sqrt(hd)).  KV position p of row r is slot p % 16 of
@@ -67,7 +67,9 @@ extern "C" {
  *   block_table int32; row r's logical page j is block_table[off[r] + j].
  *   off         [rows] int32, per-row start in block_table.
  *   qpos        [rows] int32, query position of each row (>= 0).
- *   kvpos       [rows] int32 last visible KV position, or NULL for kvpos = qpos.
+ *   kvpos       [rows] int32 last KV position written for each row, or NULL
+ *               for kvpos = qpos.  The attention is causal, so a value past
+ *               qpos[r] changes nothing; a smaller one ends the range early.
  *   counters    merge counters, NULL or at least
  *               pgqa_decode_counter_count(rows, nh, nkv) uint32 slots.  Zero
  *               them once before first use; every successful call leaves them
@@ -175,12 +177,15 @@ int pgqa_trace_buffer(void *device_buffer, size_t bytes);
  * PGQA_NOALLOC_MAX_PART_BYTES of partials, about 8.1 MiB), which every GPU
  * that loads the library holds until the process exits.  Calls needing more
  * (pgqa_decode_part_bytes or pgqa_decode_counter_count above those limits)
- * return PGQA_ERR_NOALLOC_TOO_LARGE and enqueue nothing.
+ * return PGQA_ERR_NOALLOC_TOO_LARGE.  Every argument check of
+ * pgqa_attn_decode runs first too, and a rejected call enqueues nothing.
  *
  * It allocates nothing.  Each call clears the counters it uses with
  * cudaMemsetAsync on `stream`, then enqueues the decode there.  The first
  * call on a device looks up the array's device address (cudaGetSymbolAddress,
  * with that device current); make that first call before any stream capture.
+ * After a device reset (cudaDeviceReset) the next call sees a new context and
+ * looks the address up again, so that call, too, belongs outside a capture.
  * Every call on a device shares the one array and finds it as the previous
  * call left it, so calls that may overlap on the GPU (different streams
  * without ordering between them) race and must not be issued.

@@ -12,19 +12,32 @@
 //
 // GB300 design:
 //  * one producer warp streams whole (page, kv head) tiles of K and V into a
-//    ring of shared-memory stages with 3-D TMA (cp.async.bulk.tensor) and the
-//    128-byte swizzle, completion counted on mbarriers;
-//  * four consumer warps work on every page together, each owning a quarter
-//    of the head dimension: partial S = Q K^T over its quarter on the tensor
-//    cores (mma.sync m16n8k16 bf16 -> f32, all query heads of the kv head in
-//    the MMA rows so each KV byte leaves HBM once), partial sums exchanged
-//    through a small double-buffered shared array (one barrier per page),
-//    then the same online softmax in every warp and O^T += V^T P^T for its
-//    quarter.  The S accumulator fragment is, register for register, the B
-//    fragment of the PV product, so P never touches shared memory.  Pages
-//    are consumed in order, so the producer keeps the whole ring in flight;
+//    ring of shared-memory stages with TMA (cp.async.bulk.tensor, one 4-D box
+//    per tile where the driver takes it) and the 128-byte swizzle, completion
+//    counted on mbarriers;
+//  * the consumer warps form Cfg<HD>::kGroups page groups of Cfg<HD>::kWpg
+//    warps each (four groups of one warp at hd 64/128, four of two at hd 256,
+//    two of four at hd 512).  Pages go round-robin to the groups, and a group
+//    owns the ring stages s with s % kGroups == its index.  The warps of a
+//    group split the head dimension: each computes S^T = K Q^T over its dims
+//    on the tensor cores (mma.sync m16n8k16 bf16 -> f32, the page's 16 tokens
+//    as MMA rows and up to 8 query rows -- all query heads of the kv head, or
+//    packed rows -- as columns, so each KV byte leaves HBM once), the group
+//    sums the partial scores through a small double-buffered shared array
+//    (one named barrier per page), and every warp of the group runs the same
+//    online softmax and O^T += V^T P^T for its dims, with P moved from the S
+//    accumulators to the PV operand by movmatrix, never through shared
+//    memory.  When every page is consumed the groups' (m, l, O) merge in
+//    shared memory;
 //  * online softmax in the log2 domain with quad shuffles; the O rescale is
 //    skipped when no running max moved;
+//  * the splits of a tile then merge in one of three ways, all with the same
+//    arithmetic in the same order, so they agree bit for bit: inside a
+//    thread-block cluster (2, 4 or 8 splits with merge counters), each CTA
+//    pushing its (M, L) and a slice of its O into the slice owner's shared
+//    memory with st.async; in the tile's last CTA, found through the merge
+//    counters (other counts up to 8); or in the sliced combine kernel (no
+//    counters, or more than 8 splits);
 //  * every wait is bounded (about one second) and reports through a device
 //    error word instead of hanging.
 #pragma once
@@ -472,7 +485,7 @@ __device__ __forceinline__ void store_out4(__nv_bfloat16 *dst, const float4 &acc
 __device__ __forceinline__ void row_window(const DecodeParams &p, int r, int &lo, int &hi)
 {
     const int qp = __ldg(p.qpos + r);
-    hi = p.kvpos ? __ldg(p.kvpos + r) : qp;
+    hi = p.kvpos ? min(qp, __ldg(p.kvpos + r)) : qp;    // causal: never past the query's own position
     lo = p.window > 0 ? max(0, qp + 1 - p.window) : 0;
 }
 

@@ -89,7 +89,7 @@ struct PrefillParams {
 __device__ __forceinline__ void prefill_window(const PrefillParams &p, int r, int &lo, int &hi)
 {
     const int qp = __ldg(p.qpos + r);
-    hi = p.kvpos ? __ldg(p.kvpos + r) : qp;
+    hi = p.kvpos ? min(qp, __ldg(p.kvpos + r)) : qp;    // causal: never past the query's own position
     lo = p.window > 0 ? max(0, qp + 1 - p.window) : 0;
 }
 

@@ -237,7 +237,7 @@ def algorithmic_bytes(nh: int, nkv: int, hd: int, window: int, qpos, off, kvpos=
     spans = {}
     for r in range(rows):
         qp = int(qpos[r])
-        hi = int(kvpos[r]) if kvpos is not None else qp
+        hi = min(qp, int(kvpos[r])) if kvpos is not None else qp     # causal
         lo = window_lo(qp, window)
         if hi < lo:
             continue

@@ -39,6 +39,8 @@ def brute_decode_bytes(nh, nkv, hd, window, qpos, off, kvpos=None):
     for r, qp in enumerate(qpos):
         kv = qp if kvpos is None else kvpos[r]
         for t in visible(qp, kv, window):
+            if t > qp:               # causal: a second position past qpos adds nothing
+                continue
             seen.add((off[r], t))
     return len(seen) * nkv * hd * 2 * 2 + 2 * len(qpos) * nh * hd * 2
 
@@ -55,8 +57,8 @@ def test_decode_bytes_match_brute_force(seed):
     off = [rng.choice(spans) for _ in range(rows)]
     qpos = [rng.randint(0, 400) for _ in range(rows)]
     kvpos = None
-    if rng.random() < 0.4:       # some rows see less than their query position (or nothing)
-        kvpos = [max(-1, q - rng.randint(0, 50)) for q in qpos]
+    if rng.random() < 0.4:       # some rows see less than their query position (or nothing), some more
+        kvpos = [max(-1, q - rng.randint(-5, 50)) for q in qpos]
     got = wl.algorithmic_bytes(nh, nkv, hd, window, qpos, off, kvpos)
     assert got == brute_decode_bytes(nh, nkv, hd, window, qpos, off, kvpos)
 
@@ -120,3 +122,8 @@ def test_reference_arm_prints_the_contract_line():
     assert d["cpu_baseline"]["cores"] >= 1
     assert d["e2e"]["value"] == d["value"] and d["e2e"]["h2d_bytes_per_step"] == 0
     assert d["e2e"]["d2h_bytes_per_step"] == 0 and d["config"]["workload"].startswith("tiny")
+    # the config describes the workload alone, with the keys and values the GPU arm prints for it
+    # (run details such as splits and timing go under "run"), so the two lines match
+    b = _bench()
+    assert d["config"] == json.loads(json.dumps(b.config_of(b.build_case("tiny"))))
+    assert not {"splits", "merge", "l2", "timing"} & set(d["config"])

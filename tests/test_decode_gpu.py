@@ -148,7 +148,8 @@ def ragged_case(seed=21, nh=16, nkv=4, hd=128, window=40):
     bt = np.concatenate([perm[:20], perm[20:44], perm[44:64]]).astype(np.int32)
     off = np.array([0, 20, 44, 20, 5], dtype=np.int32)
     qpos = np.array([300, 383, 250, 17, 100], dtype=np.int32)
-    kvpos = np.array([300, 383, 250, 19, 30], dtype=np.int32)    # row 3 sees ahead; row 4 is empty
+    # row 3's kvpos lies past its qpos (causal: that changes nothing); row 4 is empty
+    kvpos = np.array([300, 383, 250, 19, 30], dtype=np.int32)
     return wl.Case("ragged", nh, nkv, hd, window, rows, q, k, v, bt, off, qpos, kvpos=kvpos,
                    ctx=384, npg=npages)
 
@@ -164,6 +165,28 @@ def test_ragged_rows_offsets_kvpos_and_empty_row(window):
         assert np.array_equal(a, d.result(counters=False))
         if window:
             assert np.all(a[4] == 0), "row with no visible position must be zero"
+
+
+@pytest.mark.parametrize("splits", [1, 4, 13])
+def test_kvpos_past_qpos_changes_nothing(splits):
+    """The attention is causal: a second position array past qpos gives the bits of kvpos = qpos,
+    even with NaN in every slot past the rows' query positions (they are never read into o)."""
+    import dataclasses
+    from gpu_util import DevCase, first_difference
+    c = wl.page_case(16, 4, 128, 0, 700, 4, dist="sym", seed=19)
+    c = dataclasses.replace(c, qpos=np.array([650, 651, 652, 653], np.int32))
+    ref = DevCase(c, splits).result()
+    pk = c.k_pool.copy().reshape(c.npg, c.nkv, 16, c.hd)
+    pv = c.v_pool.copy().reshape(c.npg, c.nkv, 16, c.hd)
+    for pos in range(654, c.npg * 16):
+        pk[pos // 16, :, pos % 16, :] = wl.BF16_NAN
+        pv[pos // 16, :, pos % 16, :] = wl.BF16_NAN
+    ahead = dataclasses.replace(c, k_pool=pk.reshape(-1), v_pool=pv.reshape(-1),
+                                kvpos=c.qpos + np.array([1, 5, 16, 40], np.int32))
+    d = DevCase(ahead, splits)
+    for counters in (True, False):
+        got = d.result(counters=counters)
+        assert np.array_equal(got, ref), first_difference(got, ref)
 
 
 def packing_case(kind, seed=31, nh=16, nkv=8, hd=256, window=300):

@@ -202,6 +202,27 @@ def test_kvpos_below_qpos_and_an_empty_row():
     assert np.all(a[50] == 0), "a row with no visible position must be zero"
 
 
+def test_kvpos_past_qpos_changes_nothing():
+    """Causal prefill: kvpos past qpos gives the bits of kvpos = qpos, on the tiled kernel
+    (hd 128, 256), the hd-512 kernel and the split-KV path, with NaN in every slot past the
+    last row's position."""
+    from gpu_util import PrefillDev, first_difference
+    for hd, splits in ((128, 1), (256, 1), (512, 1), (256, 3)):
+        c = wl.prefill_case(16, 8, hd, 0, 200, dist="sym", seed=hd)
+        rows = 150
+        c = dataclasses.replace(c, rows=rows, q=c.q[:rows * c.nh * c.hd], qpos=c.qpos[:rows], off=c.off[:rows])
+        ref = PrefillDev(c).result() if splits == 1 else run_split(c, splits)
+        pk = c.k_pool.copy().reshape(c.npg, c.nkv, 16, c.hd)
+        pv = c.v_pool.copy().reshape(c.npg, c.nkv, 16, c.hd)
+        for pos in range(rows, c.npg * 16):
+            pk[pos // 16, :, pos % 16, :] = wl.BF16_NAN
+            pv[pos // 16, :, pos % 16, :] = wl.BF16_NAN
+        ahead = dataclasses.replace(c, k_pool=pk.reshape(-1), v_pool=pv.reshape(-1),
+                                    kvpos=c.qpos + 1 + (np.arange(rows, dtype=np.int32) % 30))
+        got = PrefillDev(ahead).result() if splits == 1 else run_split(ahead, splits)
+        assert np.array_equal(got, ref), f"hd {hd} splits {splits}: " + first_difference(got, ref)
+
+
 def test_nan_outside_the_union_window_never_reaches_output():
     """Slots before the first row's window and after the last row's position hold NaN."""
     from gpu_util import PrefillDev, first_difference
