@@ -17,6 +17,10 @@
 #include "pgqa_launch.cuh"
 #include "pgqa_prefill.cuh"
 
+namespace pgqa {
+int current_context_id(unsigned long long *id);
+}
+
 namespace {
 
 // Device-side error word: bounded waits OR their code into it.
@@ -26,6 +30,7 @@ constexpr int kMaxDevices = 64;
 
 struct DeviceState {
     bool ready = false;
+    unsigned long long ctx_id = 0;   // the context everything below belongs to
     int num_sms = 0;
     unsigned int *err = nullptr;
     bool attr_set[4] = {false, false, false, false};
@@ -67,6 +72,11 @@ DeviceState g_dev[kMaxDevices];
 unsigned long long *g_trace = nullptr;    // trace builds: per-CTA timestamps
 size_t g_trace_bytes = 0;
 
+using CtxGetCurrentFn = CUresult (*)(CUcontext *);
+using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long *);
+CtxGetCurrentFn g_ctx_current = nullptr;
+CtxGetIdFn g_ctx_id = nullptr;
+
 using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
                                    const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
                                    CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
@@ -84,13 +94,23 @@ int hd_index(int hd)
 }
 
 // Per-device set-up (SM count, error-word address).  Caller holds g_mutex.
+// Everything cached here belongs to one CUDA context: a device reset
+// (cudaDeviceReset) destroys the context, and the next one may place the
+// module's device symbols elsewhere and has none of the kernel attributes, so
+// the state is rebuilt whenever the current context's id changes.
 int device_state(DeviceState **out)
 {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
         return PGQA_ERR_CUDA;
+    unsigned long long ctx = 0;
+    if (pgqa::current_context_id(&ctx) != PGQA_OK)
+        return PGQA_ERR_CUDA;
     DeviceState &s = g_dev[dev];
+    if (s.ready && s.ctx_id != ctx)
+        s = DeviceState();
     if (!s.ready) {
+        s.ctx_id = ctx;
         if (cudaDeviceGetAttribute(&s.num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
             return PGQA_ERR_CUDA;
         void *p = nullptr;
@@ -186,6 +206,38 @@ bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p
 }  // namespace
 
 namespace pgqa {
+// Unique id of the CUDA context current on this thread (the runtime's primary
+// context of the current device unless the caller made another current).  A
+// thread with no current context gets the current device's primary context
+// first: cudaSetDevice initialises it, and allocates nothing.
+int current_context_id(unsigned long long *id)
+{
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &fn, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_ctx_current = reinterpret_cast<CtxGetCurrentFn>(fn);
+        fn = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &fn, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_ctx_id = reinterpret_cast<CtxGetIdFn>(fn);
+    });
+    if (!g_ctx_current || !g_ctx_id)
+        return PGQA_ERR_CUDA;
+    CUcontext ctx = nullptr;
+    if (g_ctx_current(&ctx) != CUDA_SUCCESS)
+        return PGQA_ERR_CUDA;
+    if (ctx == nullptr) {
+        int dev = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess || cudaSetDevice(dev) != cudaSuccess ||
+            g_ctx_current(&ctx) != CUDA_SUCCESS || ctx == nullptr)
+            return PGQA_ERR_CUDA;
+    }
+    return g_ctx_id(ctx, id) == CUDA_SUCCESS ? PGQA_OK : PGQA_ERR_CUDA;
+}
+
 // SM count and error-word address of the current device, for the entry
 // points defined in other translation units.
 int device_info(int *num_sms, unsigned int **err)
@@ -397,15 +449,18 @@ int pgqa_selftest_bounded_wait(void *stream)
                : PGQA_ERR_CUDA;
 }
 
-int pgqa_attn_decode(void *o, void *part, const void *q, const void *k_pool, const void *v_pool,
-                     const int32_t *block_table, const int32_t *off, const int32_t *qpos, const int32_t *kvpos,
-                     int rows, int nh, int nkv, int hd, int window, int splits, uint32_t *counters,
-                     const int32_t *page_map, void *stream)
+}  // extern "C"
+
+namespace pgqa {
+// Every host-side check of pgqa_attn_decode's arguments, in its order; no CUDA
+// call.  PGQA_OK for rows == 0 too (the call then does nothing).
+int check_decode_args(const void *o, const void *part, const void *q, const void *k_pool, const void *v_pool,
+                      const int32_t *block_table, const int32_t *off, const int32_t *qpos, int rows, int nh,
+                      int nkv, int hd, int window, int splits)
 {
     if (rows < 0 || nh <= 0 || nkv <= 0 || nh % nkv != 0 || window < 0 || splits < 1)
         return PGQA_ERR_INVALID_ARGUMENT;
-    const int hi = hd_index(hd);
-    if (hi < 0)
+    if (hd_index(hd) < 0)
         return PGQA_ERR_UNSUPPORTED_HD;
     if (splits > PGQA_MAX_SPLITS)
         return PGQA_ERR_TOO_MANY_SPLITS;
@@ -414,7 +469,7 @@ int pgqa_attn_decode(void *o, void *part, const void *q, const void *k_pool, con
     if (!o || !q || !k_pool || !v_pool || !block_table || !off || !qpos || (splits > 1 && !part))
         return PGQA_ERR_INVALID_ARGUMENT;
     const int g = nh / nkv;
-    const int hsg = (g + pgqa::kQRows - 1) / pgqa::kQRows;
+    const int hsg = (g + kQRows - 1) / kQRows;
     if (rows > 65535 || static_cast<long long>(nkv) * hsg > 65535)
         return PGQA_ERR_INVALID_ARGUMENT;
     if (splits > 1 && static_cast<long long>(rows) * nh > INT_MAX)    // the combine kernel's grid
@@ -422,6 +477,24 @@ int pgqa_attn_decode(void *o, void *part, const void *q, const void *k_pool, con
     if (!aligned(k_pool, 16) || !aligned(v_pool, 16) || !aligned(q, 16) || !aligned(o, 16) ||
         (splits > 1 && !aligned(part, 16)))
         return PGQA_ERR_MISALIGNED;
+    return PGQA_OK;
+}
+}  // namespace pgqa
+
+extern "C" {
+
+int pgqa_attn_decode(void *o, void *part, const void *q, const void *k_pool, const void *v_pool,
+                     const int32_t *block_table, const int32_t *off, const int32_t *qpos, const int32_t *kvpos,
+                     int rows, int nh, int nkv, int hd, int window, int splits, uint32_t *counters,
+                     const int32_t *page_map, void *stream)
+{
+    const int cs = pgqa::check_decode_args(o, part, q, k_pool, v_pool, block_table, off, qpos, rows, nh, nkv, hd,
+                                           window, splits);
+    if (cs != PGQA_OK || rows == 0)
+        return cs;
+    const int hi = hd_index(hd);
+    const int g = nh / nkv;
+    const int hsg = (g + pgqa::kQRows - 1) / pgqa::kQRows;
 
     pgqa::LaunchArgs a;
     pgqa::DecodeParams &p = a.p;

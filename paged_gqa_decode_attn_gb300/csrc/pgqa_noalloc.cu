@@ -10,15 +10,23 @@
 // provides all inputs and the output.
 //
 // This entry point allocates nothing: no cudaMalloc, no cudaFree, no
-// allocating library routine.  It clears the merge counters it will use with
-// cudaMemsetAsync on the caller's stream, then enqueues the ordinary
-// pgqa_attn_decode with merge counters, pointed at the static scratch.
+// allocating library routine.  It checks its arguments as pgqa_attn_decode
+// does, clears the merge counters it will use with cudaMemsetAsync on the
+// caller's stream, then enqueues the ordinary pgqa_attn_decode with merge
+// counters, pointed at the static scratch.
 #include <cuda_runtime.h>
 
 #include <cstdint>
 #include <mutex>
 
 #include "pgqa.h"
+
+namespace pgqa {
+int current_context_id(unsigned long long *id);    // pgqa_api.cu
+int check_decode_args(const void *o, const void *part, const void *q, const void *k_pool, const void *v_pool,
+                      const int32_t *block_table, const int32_t *off, const int32_t *qpos, int rows, int nh,
+                      int nkv, int hd, int window, int splits);
+}  // namespace pgqa
 
 namespace {
 
@@ -33,20 +41,27 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[kScratchBytes];
 constexpr int kMaxDevices = 64;
 std::mutex g_noalloc_mutex;
 unsigned char *g_scratch_ptr[kMaxDevices] = {};
+unsigned long long g_scratch_ctx[kMaxDevices] = {};   // the context each address belongs to
 
-// Device address of the scratch on the current device; looked up once per
-// device (the first call on each device does this, with that device current).
+// Device address of the scratch on the current device; looked up by the first
+// call on each device, with that device current, and again after the device's
+// context has been replaced (cudaDeviceReset destroys it, and the module may
+// then load at another address).
 int scratch_address(unsigned char **out)
 {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
         return PGQA_ERR_CUDA;
+    unsigned long long ctx = 0;
+    if (pgqa::current_context_id(&ctx) != PGQA_OK)
+        return PGQA_ERR_CUDA;
     std::lock_guard<std::mutex> lock(g_noalloc_mutex);
-    if (g_scratch_ptr[dev] == nullptr) {
+    if (g_scratch_ptr[dev] == nullptr || g_scratch_ctx[dev] != ctx) {
         void *ptr = nullptr;
         if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || ptr == nullptr)
             return PGQA_ERR_CUDA;
         g_scratch_ptr[dev] = static_cast<unsigned char *>(ptr);
+        g_scratch_ctx[dev] = ctx;
     }
     *out = g_scratch_ptr[dev];
     return PGQA_OK;
@@ -69,8 +84,15 @@ extern "C" int pgqa_attn_decode_noalloc(void *o, const void *q, const void *k_po
         counters > static_cast<size_t>(PGQA_NOALLOC_MAX_COUNTERS))
         return PGQA_ERR_NOALLOC_TOO_LARGE;
 
+    // every other check of pgqa_attn_decode, before any CUDA call (part: an
+    // aligned host stand-in for the static scratch, which is 256-byte aligned)
+    alignas(16) static const unsigned char part_stand_in[16] = {};
+    int st = pgqa::check_decode_args(o, part_stand_in, q, k_pool, v_pool, block_table, off, qpos, rows, nh, nkv, hd,
+                                     window, splits);
+    if (st != PGQA_OK)
+        return st;
     unsigned char *scratch = nullptr;
-    int st = scratch_address(&scratch);
+    st = scratch_address(&scratch);
     if (st != PGQA_OK)
         return st;
     uint32_t *cnt = reinterpret_cast<uint32_t *>(scratch);

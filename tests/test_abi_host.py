@@ -191,6 +191,24 @@ def test_zero_rows_is_ok_without_a_device(lib):
     assert call(lib, rows=0, o=None, q=None) == 0
 
 
+@pytest.mark.parametrize("kw,code", [
+    (dict(rows=-1), -1), (dict(nh=10, nkv=4), -1), (dict(window=-1), -1), (dict(splits=0), -1),
+    (dict(hd=96), -2), (dict(splits=257), -7), (dict(o=None), -1), (dict(q=None), -1), (dict(k=None), -1),
+    (dict(v=None), -1), (dict(bt=None), -1), (dict(off=None), -1), (dict(qpos=None), -1),
+    (dict(k=FAKE + 8), -3), (dict(v=FAKE + 2), -3), (dict(q=FAKE + 4), -3), (dict(o=FAKE + 8), -3),
+    (dict(rows=70000), -8),
+])
+def test_noalloc_rejects_bad_arguments_before_any_cuda_call(lib, kw, code):
+    """The no-allocation entry point runs pgqa_attn_decode's checks before it clears its counters, so a
+    rejected call enqueues nothing (here: no device at all, and no CUDA call is reached)."""
+    a = dict(rows=1, nh=8, nkv=2, hd=128, window=0, splits=1, o=FAKE, q=FAKE, k=FAKE, v=FAKE, bt=FAKE, off=FAKE,
+             qpos=FAKE)
+    a.update(kw)
+    st = lib.pgqa_attn_decode_noalloc(a["o"], a["q"], a["k"], a["v"], a["bt"], a["off"], a["qpos"], None,
+                                      a["rows"], a["nh"], a["nkv"], a["hd"], a["window"], a["splits"], None, None)
+    assert st == code
+
+
 def test_python_binding_raises_on_error(lib):
     with pytest.raises(pgqa.PgqaError) as ei:
         pgqa.attn_decode(FAKE, None, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None, 1, 8, 2, 96, 0, 1, stream=0)

@@ -43,10 +43,14 @@ def _run_both(case, splits):
 
 
 @pytest.mark.parametrize("make,splits", [
-    (lambda: wl.page_case(16, 8, 256, 1024, 1500, 5), 6),       # the page's first decode case
-    (lambda: wl.sliding(mapped=True), 19),                       # sliding window, page map + NaN null page
-    (lambda: wl.long_ctx(), 38),                                 # 32K context, hd 512
-], ids=["page_case_hd256", "sliding_mapped", "long_32k"])
+    (lambda: wl.page_case(16, 8, 256, 1024, 1500, 5), 6),       # the page's first decode case: last-CTA merge
+    (lambda: wl.page_case(16, 8, 256, 1024, 1500, 5), 4),       # the same, merged on chip (4-CTA clusters)
+    (lambda: wl.sliding(mapped=True), 8),                        # sliding window, page map: 8-CTA clusters
+    (lambda: wl.tiny(), 2),                                      # 2-CTA clusters
+    (lambda: wl.sliding(mapped=True), 19),                       # the combine kernel
+    (lambda: wl.long_ctx(), 38),                                 # 32K context, hd 512, two-level combine
+], ids=["page_case_hd256_s6", "page_case_hd256_s4", "sliding_mapped_s8", "tiny_s2", "sliding_mapped_s19",
+        "long_32k_s38"])
 def test_noalloc_matches_allocating_entry_point_twice(make, splits):
     case = make()
     ref, outs = _run_both(case, splits)
