@@ -9,8 +9,8 @@ The three gates follow the `run` function of span-02
      for pages outside every row's window, bit for bit (also with the map
      folded into the block table).
 On top of the page's gate every element is held to a bound derived from the
-arithmetic (bf16 P and output rounding, f32 score accumulation):
-|o - o_f64| <= 2^-7 (|o_f64| + max|V|).
+arithmetic (bf16 P and output rounding; ``parity.py``):
+|o - o_f64| <= 2^-8 |o_f64| + 2^-7 rms_h(o_f64), per (row, head).
 """
 import os
 import sys

@@ -5,7 +5,8 @@ The gates follow the prefill part of `run` in span-02
 ``make_tiles`` with ``prefill_rows_per_tile``, is within rel-RMS 1e-2 of the
 reference, and the permuted pool behind a page map (and the map folded into
 the block table) gives the same bits.  Every element is also held to the
-arithmetic bound of the decode tests.  A prefill row is a decode row at the
+arithmetic bound of ``parity.py`` (c = 2^-6 on the tcgen05 kernels, which let P
+grow to 2^8 before rescaling).  A prefill row is a decode row at the
 same position, so the oracle is the decode oracle over all rows.
 """
 import dataclasses
@@ -37,7 +38,7 @@ def prefill_gates(case, mapped=True, seq=None):
     from gpu_util import PrefillDev, check_parity, first_difference
     d = PrefillDev(case, seq)
     a = d.result()
-    check_parity(case, a, case.name)
+    check_parity(case, a, case.name, tiled=case.hd <= 256)
     if mapped:
         for fold in (False, True):
             m = wl.with_mapped_pool(case, fold_into_table=fold)
@@ -165,11 +166,32 @@ def test_split_kv_multi_row_decode(hd, window, splits):
     from gpu_util import check_parity, first_difference
     c = many_sequence_case([(16, 2984)], 32, 16, hd, window, seed=hd + splits)
     a = run_split(c, splits)
-    check_parity(c, a, f"{c.name} splits {splits}")
+    check_parity(c, a, f"{c.name} splits {splits}", tiled=True)
     for fold in (False, True):
         m = wl.with_mapped_pool(c, fold_into_table=fold)
         am = run_split(m, splits)
         assert np.array_equal(am, a), f"page map (fold={fold}) differs: " + first_difference(am, a)
+
+
+SWEEP_TILED = [(128, 16384, 16, 4096), (128, 65536, 16, 0), (128, 65536, 16, 1024), (256, 4096, 16, 1024),
+               (256, 16384, 16, 0), (256, 65536, 16, 4096)]
+
+
+@pytest.mark.parametrize("pt", SWEEP_TILED, ids=lambda p: "hd%d_ctx%d_r%d_w%d" % p)
+def test_sweep_rows16_points_on_the_tiled_split_path(pt):
+    """The sweep's 16-row points that the benchmark sends down the tiled tcgen05 path (rows x g > 8,
+    hd <= 256), routed exactly as it routes them -- make_tiles over one sequence, splits from
+    prefill_split_count, the combine kernel merging -- on the sweep's inputs: Gaussian Q/K/V with 5% of
+    keys x8, served from the permuted pool with the NaN null page, at 4K to 64K positions."""
+    import paged_gqa_decode_attn_gb300 as pgqa
+    from gpu_util import check_parity
+    hd, ctx, rows, window = pt
+    c = wl.sweep(*pt, mapped=True)
+    assert rows * (c.nh // c.nkv) > 8 and hd <= 256
+    t0, _ = pgqa.make_tiles(np.zeros(rows, np.int32), pgqa.prefill_rows_per_tile(hd))
+    splits = pgqa.prefill_split_count(c.kv_len_eff(), rows, len(t0), c.nh, c.nkv)
+    assert splits > 1
+    check_parity(c, run_split(c, splits), f"{c.name} splits {splits}", tiled=True)
 
 
 def test_split_kv_several_sequences_and_empty_splits():
@@ -178,7 +200,7 @@ def test_split_kv_several_sequences_and_empty_splits():
     from gpu_util import check_parity
     c = many_sequence_case([(16, 1984), (1, 0), (40, 500)], 16, 8, 256, 0, seed=7)
     for splits in (4, 13):
-        check_parity(c, run_split(c, splits), f"{c.name} splits {splits}")
+        check_parity(c, run_split(c, splits), f"{c.name} splits {splits}", tiled=True)
 
 
 def test_split_kv_bad_arguments():
