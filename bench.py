@@ -323,11 +323,12 @@ def run_reference(args, case, rank, world):
     if args.workload.startswith("prefill"):
         metric, unit = "paged causal prefill attention TFLOP/s", "TFLOP/s"
         gbs = prefill_flops(case) * k / (case.rows * case.nh) / per / 1e12
+    cfg = prefill_config(case) if args.workload.startswith("prefill") else config_of(case)
     line = {
         "impl": "reference", "metric": metric, "value": round(gbs, 6), "unit": unit, "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": per * 1e3, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": config_of(args, case, None),
+        "config": cfg,
         "cpu_baseline": {"value": round(gbs, 6), "unit": unit, "cores": cores, "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": round(gbs, 6), "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -337,22 +338,225 @@ def run_reference(args, case, rank, world):
     return 0
 
 
-def config_of(args, case, splits):
-    c = {"workload": case.name, "nh": case.nh, "nkv": case.nkv, "hd": case.hd, "ctx": case.ctx,
-         "rows": case.rows, "window": case.window, "pool": "page map + NaN null page" if case.page_map is not None
-         else "identity", "algorithmic_bytes_per_call": case.algorithmic_bytes()}
-    if splits is not None:
-        c["splits"] = splits
-        if splits == 1:
-            c["merge"] = "none (one split)"
-        elif args.merge == "counters" and splits <= 8:
-            c["merge"] = "in the split kernel (thread-block cluster or last CTA, through merge counters)"
-        else:
-            c["merge"] = "combine kernel" + (" (more than 8 splits)" if args.merge == "counters" else "")
+def config_of(case):
+    """The workload alone: the same keys and values in both arms' lines."""
+    return {"workload": case.name, "nh": case.nh, "nkv": case.nkv, "hd": case.hd, "ctx": case.ctx,
+            "rows": case.rows, "window": case.window,
+            "pool": "page map + NaN null page" if case.page_map is not None else "identity",
+            "algorithmic_bytes_per_call": case.algorithmic_bytes()}
+
+
+def prefill_config(case):
+    c = config_of(case)
+    del c["algorithmic_bytes_per_call"]
+    c["flops_per_call"] = prefill_flops(case)
     return c
 
 
+def run_of(args, case, splits):
+    """How this arm ran the workload (split count and merge path)."""
+    r = {"splits": splits}
+    if splits == 1:
+        r["merge"] = "none (one split)"
+    elif args.merge == "counters" and splits <= 8:
+        r["merge"] = "in the split kernel (thread-block cluster or last CTA, through merge counters)"
+    else:
+        r["merge"] = "combine kernel" + (" (more than 8 splits)" if args.merge == "counters" else "")
+    return r
+
+
 # ------------------------------------------------------------------ our arm
+
+class DecodeRig:
+    """One decode workload resident on the device, ready to call: rotating pool
+    copies (each copy's reads > 3x L2 apart, so every call reads KV from HBM),
+    the per-step inputs in one pinned host buffer and one device buffer, scratch
+    and counters."""
+
+    def __init__(self, args, case, dev, splits=None, copies=None):
+        import torch
+        import paged_gqa_decode_attn_gb300 as pgqa
+        self.case = case
+        self.bpc = case.algorithmic_bytes()
+        self.splits = splits or args.splits or pgqa.choose_splits(case.kv_len_eff(), case.rows, case.nkv,
+                                                                   nseq_of(case))
+        self.pool_bytes = case.k_pool.nbytes + case.v_pool.nbytes
+        n = max(2, math.ceil(3 * L2_BYTES / max(self.bpc, 1)))
+        n = min(n, max(2, int(0.25 * torch.cuda.get_device_properties(dev).total_memory // self.pool_bytes)))
+        self.copies = copies or args.copies or n
+
+        def i16(a):
+            return torch.from_numpy(np.ascontiguousarray(a).view(np.int16))
+
+        def i32(a):
+            return None if a is None else torch.from_numpy(np.ascontiguousarray(a, dtype=np.int32))
+
+        k_host, v_host = i16(case.k_pool), i16(case.v_pool)
+        self.ks = [k_host.to(dev) for _ in range(self.copies)]
+        self.vs = [v_host.to(dev) for _ in range(self.copies)]
+        # q, qpos, off and the block table share one pinned host buffer and one
+        # device buffer, so a step moves them with a single copy
+        parts = [np.ascontiguousarray(case.q).view(np.uint8),
+                 np.ascontiguousarray(case.qpos, np.int32).view(np.uint8),
+                 np.ascontiguousarray(case.off, np.int32).view(np.uint8),
+                 np.ascontiguousarray(case.block_table, np.int32).view(np.uint8)]
+        offs, pos = [], 0
+        for a in parts:
+            offs.append(pos)
+            pos += (a.size + 255) // 256 * 256
+        self.host_in = torch.zeros(pos, dtype=torch.uint8).pin_memory()
+        for a, o0 in zip(parts, offs):
+            self.host_in[o0:o0 + a.size] = torch.from_numpy(a)
+        self.dev_in = self.host_in.to(dev)
+        self.q = self.dev_in[offs[0]:offs[0] + parts[0].size].view(torch.int16)
+        self.qpos = self.dev_in[offs[1]:offs[1] + parts[1].size].view(torch.int32)
+        self.off = self.dev_in[offs[2]:offs[2] + parts[2].size].view(torch.int32)
+        self.bt = self.dev_in[offs[3]:offs[3] + parts[3].size].view(torch.int32)
+        self.kvpos = None if case.kvpos is None else i32(case.kvpos).to(dev)
+        self.pm = None if case.page_map is None else i32(case.page_map).to(dev)
+        self.part = torch.empty(max(1, pgqa.decode_part_bytes(case.rows, case.nh, self.splits, case.hd)) // 4 + 4,
+                                dtype=torch.float32, device=dev)
+        self.cnt = torch.zeros(max(1, pgqa.decode_counter_count(case.rows, case.nh, case.nkv)), dtype=torch.int32,
+                               device=dev)
+        self.o = torch.empty(case.rows * case.nh * case.hd, dtype=torch.int16, device=dev)
+        self.o_h = torch.empty_like(self.o, device="cpu").pin_memory()
+        self.counters = self.cnt if args.merge == "counters" else None
+        self.launches_per_call = pgqa.decode_kernel_count(self.splits, self.counters is not None)
+        self.graphs = {}
+
+    def call(self, i, stream=None):
+        import paged_gqa_decode_attn_gb300 as pgqa
+        c = self.case
+        pgqa.attn_decode(self.o, self.part, self.q, self.ks[i % self.copies], self.vs[i % self.copies], self.bt,
+                         self.off, self.qpos, self.kvpos, c.rows, c.nh, c.nkv, c.hd, c.window, self.splits,
+                         self.counters, self.pm, stream)
+
+    def spot_check(self, npairs=16):
+        """rel-RMS of a sample of (row, head) outputs against the oracle (raises above the page's 1e-2)."""
+        import torch
+        import oracle
+        c = self.case
+        self.call(0)
+        torch.cuda.synchronize()
+        got = self.o.cpu().numpy().view(np.uint16).reshape(c.rows, c.nh, c.hd)
+        pairs = [(r, h) for r in range(c.rows) for h in range(c.nh)][:: max(1, c.rows * c.nh // npairs)]
+        _, ref = oracle.decode_case(c, pairs=pairs, want_f64=False)
+        e = oracle.rel_rms(np.stack([got[r, h] for r, h in pairs]), ref)
+        if not e < 1e-2:
+            raise SystemExit(f"{c.name}: spot check against the oracle failed: rel_rms {e}")
+        return e
+
+    def graph(self, n):
+        import torch
+        if n not in self.graphs:
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                for i in range(n):
+                    self.call(i)
+            self.graphs[n] = g
+        return self.graphs[n]
+
+    def time_steps(self, steps, warmup, chunk, dist=None, load_s=0.0):
+        """Device time (ms) of exactly ``steps`` back-to-back calls: CUDA events on the
+        launching stream around graph replays, after ``warmup`` eager calls.  A short
+        GPU sleep is queued ahead of the start event, so the replays are already
+        queued when the GPU reaches it: the region holds the calls, not the host's
+        launch latency.  With ``load_s`` the graphs also replay for about that long
+        before and after the region (the clock samples' window)."""
+        import torch
+        for i in range(warmup):
+            self.call(i)
+        torch.cuda.synchronize()
+        chunk = max(1, min(steps, chunk))
+        full, rem = divmod(steps, chunk)
+        g_full = self.graph(chunk) if full else None
+        g_rem = self.graph(rem) if rem else None
+        (g_full or g_rem).replay()       # settles the graphs' first-launch cost
+        torch.cuda.synchronize()
+        self._load(g_full or g_rem, load_s)
+        stream = torch.cuda.current_stream()
+        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        barrier(dist)
+        torch.cuda.synchronize()
+        torch.cuda._sleep(200000)        # ~0.1 ms: the replays below queue behind it
+        ev0.record(stream)
+        for _ in range(full):
+            g_full.replay()
+        if rem:
+            g_rem.replay()
+        ev1.record(stream)
+        ev1.synchronize()
+        torch.cuda.synchronize()
+        barrier(dist)
+        self._load(g_full or g_rem, load_s / 3)
+        return ev0.elapsed_time(ev1), chunk
+
+    @staticmethod
+    def _load(g, seconds):
+        import torch
+        t0 = time.perf_counter()
+        while time.perf_counter() - t0 < seconds:
+            for _ in range(8):
+                g.replay()
+            torch.cuda.synchronize()
+
+    def time_e2e(self, steps, dist=None):
+        """End to end through the public API from pinned host memory: per step one
+        host->device copy of the step's inputs, the call, one device->host copy of o.
+        Also the host cost of each part, enqueued alone."""
+        import torch
+        barrier(dist)
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for i in range(steps):
+            self.dev_in.copy_(self.host_in, non_blocking=True)
+            self.call(i)
+            self.o_h.copy_(self.o, non_blocking=True)
+        torch.cuda.synchronize()
+        e2e_s = max_over_ranks(dist, time.perf_counter() - t0)
+        n = min(steps, 200)
+        parts = {}
+        for name, fn in (("h2d_copy", lambda i: self.dev_in.copy_(self.host_in, non_blocking=True)),
+                         ("attn_decode_call", self.call),
+                         ("d2h_copy", lambda i: self.o_h.copy_(self.o, non_blocking=True))):
+            torch.cuda.synchronize()
+            t0 = time.perf_counter()
+            for i in range(n):
+                fn(i)
+            parts[name] = round((time.perf_counter() - t0) / n * 1e6, 2)
+            torch.cuda.synchronize()
+        # the same step captured in a CUDA graph (copies and call), replayed per step
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            self.dev_in.copy_(self.host_in, non_blocking=True)
+            self.call(0)
+            self.o_h.copy_(self.o, non_blocking=True)
+        g.replay()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for _ in range(steps):
+            g.replay()
+        torch.cuda.synchronize()
+        graph_us = (time.perf_counter() - t0) / steps * 1e6
+        return e2e_s, parts, graph_us
+
+
+def decode_summary(rig, el_ms, steps, spot, peak):
+    """Per-workload record: device time per call, GB/s, roofline fraction, splits, parity, traffic."""
+    c = rig.case
+    us = el_ms * 1e3 / steps
+    gbs = rig.bpc / (us * 1e-6) / 1e9
+    return {"workload": c.name, "us_per_call": round(us, 3), "value": round(gbs, 2), "unit": "GB/s",
+            "frac": round(gbs / peak, 4), "splits": rig.splits, "kernels_per_call": rig.launches_per_call,
+            "algorithmic_bytes_per_call": rig.bpc, "spot_check_rel_rms": spot,
+            "traffic": recorded_traffic(c.name), "steps": steps}
+
+
+# The other decode configurations timed in the default run beside the headline
+# (sliding): the 32K-context target, the batched shared-table case and the tiny
+# latency case.  Each is timed with the headline's protocol.
+EXTRA_DECODE = ["long", "batched", "tiny"]
+
 
 def run_ours(args, case, rank, world, dist):
     import torch
@@ -364,166 +568,74 @@ def run_ours(args, case, rank, world, dist):
         pgqa.build()
     barrier(dist)
     pgqa.load()
-
-    bpc = case.algorithmic_bytes()
-    splits = args.splits or pgqa.choose_splits(case.kv_len_eff(), case.rows, case.nkv, nseq_of(case))
-    # enough pool copies that consecutive reads of one copy are > 3x L2 apart
-    pool_bytes = case.k_pool.nbytes + case.v_pool.nbytes
-    copies = max(2, math.ceil(3 * L2_BYTES / max(bpc, 1)))
-    copies = min(copies, max(2, int(0.25 * torch.cuda.get_device_properties(dev).total_memory // pool_bytes)))
-    if args.copies:
-        copies = args.copies
-
-    def i16(a):
-        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16))
-
-    def i32(a):
-        return None if a is None else torch.from_numpy(np.ascontiguousarray(a, dtype=np.int32))
-
-    k_host, v_host = i16(case.k_pool), i16(case.v_pool)
-    ks = [k_host.to(dev) for _ in range(copies)]
-    vs = [v_host.to(dev) for _ in range(copies)]
-    # The per-step inputs (q, qpos, off, block table) share one pinned host
-    # buffer and one device buffer, so a step moves them with a single copy.
-    parts = [np.ascontiguousarray(case.q).view(np.uint8), np.ascontiguousarray(case.qpos, np.int32).view(np.uint8),
-             np.ascontiguousarray(case.off, np.int32).view(np.uint8),
-             np.ascontiguousarray(case.block_table, np.int32).view(np.uint8)]
-    offs, pos = [], 0
-    for a in parts:
-        offs.append(pos)
-        pos += (a.size + 255) // 256 * 256
-    host_in = torch.zeros(pos, dtype=torch.uint8).pin_memory()
-    for a, o0 in zip(parts, offs):
-        host_in[o0:o0 + a.size] = torch.from_numpy(a)
-    dev_in = host_in.to(dev)
-    q = dev_in[offs[0]:offs[0] + parts[0].size].view(torch.int16)
-    qpos = dev_in[offs[1]:offs[1] + parts[1].size].view(torch.int32)
-    off = dev_in[offs[2]:offs[2] + parts[2].size].view(torch.int32)
-    bt = dev_in[offs[3]:offs[3] + parts[3].size].view(torch.int32)
-    kvpos = None if case.kvpos is None else i32(case.kvpos).to(dev)
-    pm = None if case.page_map is None else i32(case.page_map).to(dev)
-    part = torch.empty(max(1, pgqa.decode_part_bytes(case.rows, case.nh, splits, case.hd)) // 4 + 4,
-                       dtype=torch.float32, device=dev)
-    cnt = torch.zeros(max(1, pgqa.decode_counter_count(case.rows, case.nh, case.nkv)), dtype=torch.int32,
-                      device=dev)
-    o = torch.empty(case.rows * case.nh * case.hd, dtype=torch.int16, device=dev)
-    o_h = torch.empty_like(o, device="cpu").pin_memory()
-    counters = cnt if args.merge == "counters" else None
-    launches_per_call = pgqa.decode_kernel_count(splits, counters is not None)
-
-    def call(i, stream=None):
-        pgqa.attn_decode(o, part, q, ks[i % copies], vs[i % copies], bt, off, qpos, kvpos, case.rows, case.nh,
-                         case.nkv, case.hd, case.window, splits, counters, pm, stream)
-
-    # spot check against the oracle on rank 0 (a few (row, head) pairs)
-    call(0)
-    torch.cuda.synchronize()
-    spot = None
-    if rank == 0 and not args.no_check:
-        import oracle
-        got = o.cpu().numpy().view(np.uint16).reshape(case.rows, case.nh, case.hd)
-        pairs = [(r, h) for r in range(case.rows) for h in range(case.nh)][:: max(1, case.rows * case.nh // 16)]
-        _, ref = oracle.decode_case(case, pairs=pairs, want_f64=False)
-        spot = oracle.rel_rms(np.stack([got[r, h] for r, h in pairs]), ref)
-        if not spot < 1e-2:
-            raise SystemExit(f"spot check against the oracle failed: rel_rms {spot}")
-
     sampler = ClockSampler(torch.cuda.current_device()) if not args.no_clocks else None
 
-    # warm-up (eager), then graphs of back-to-back calls for the timed steps
-    for i in range(args.warmup):
-        call(i)
-    torch.cuda.synchronize()
-    chunk = max(1, min(args.steps, args.graph_chunk))
-    graphs = {}
-
-    def graph_for(n):
-        if n not in graphs:
-            g = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(g):
-                for i in range(n):
-                    call(i)
-            graphs[n] = g
-        return graphs[n]
-
-    full, rem = divmod(args.steps, chunk)
-    g_full = graph_for(chunk) if full else None
-    g_rem = graph_for(rem) if rem else None
-    # a graph replay before timing settles the graphs' first-launch cost
-    (g_full or g_rem).replay()
-    torch.cuda.synchronize()
-
-    stream = torch.cuda.current_stream()
-    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    barrier(dist)
-    torch.cuda.synchronize()
-    ev0.record(stream)
-    for _ in range(full):
-        g_full.replay()
-    if rem:
-        g_rem.replay()
-    ev1.record(stream)
-    ev1.synchronize()
-    torch.cuda.synchronize()
-    barrier(dist)
-    el_ms = ev0.elapsed_time(ev1)
+    rig = DecodeRig(args, case, dev)
+    spot = rig.spot_check() if rank == 0 and not args.no_check else None
+    el_ms, chunk = rig.time_steps(args.steps, args.warmup, args.graph_chunk, dist,
+                                  load_s=0.0 if args.no_clocks else args.clock_window)
     clocks = sampler.stop() if sampler else None
     el_max = max_over_ranks(dist, el_ms)
     ms_per_step = el_max / args.steps
-    total_bytes = sum_over_ranks(dist, float(bpc) * args.steps)
-    value = total_bytes / (el_max * 1e-3) / 1e9
+    value = sum_over_ranks(dist, float(rig.bpc) * args.steps) / (el_max * 1e-3) / 1e9
     # the step's device time: with two launches the combine kernel overlaps the
     # split kernel's tail (programmatic dependent launch), so they are timed together
     kernel_us = el_ms * 1e3 / args.steps
-
-    # end to end through the public API from pinned host memory: per step one
-    # H2D of q, qpos, off and the block table, the call, one D2H of o
     e2e_steps = max(1, min(args.steps, args.e2e_steps))
-    h2d = host_in.numel()
-    d2h = o_h.numel() * o_h.element_size()
-    barrier(dist)
-    torch.cuda.synchronize()
-    t0 = time.perf_counter()
-    for i in range(e2e_steps):
-        dev_in.copy_(host_in, non_blocking=True)
-        call(i)
-        o_h.copy_(o, non_blocking=True)
-    torch.cuda.synchronize()
-    e2e_s = max_over_ranks(dist, time.perf_counter() - t0)
-    e2e_value = sum_over_ranks(dist, float(bpc) * e2e_steps) / e2e_s / 1e9
+    e2e_s, host_parts, graph_us = rig.time_e2e(e2e_steps, dist)
+    e2e_value = sum_over_ranks(dist, float(rig.bpc) * e2e_steps) / e2e_s / 1e9
+
+    # the other decode configurations, same protocol, reported inside the one line
+    peak, peak_kind = measured_peaks()
+    extra = []
+    if args.workload == "sliding" and not args.no_extra:
+        for name in EXTRA_DECODE:
+            c2 = build_case(name)
+            r2 = DecodeRig(args, c2, dev)
+            sp2 = r2.spot_check() if rank == 0 and not args.no_check else None
+            ms2, _ = r2.time_steps(args.steps, args.warmup, args.graph_chunk, dist)
+            ms2 = max_over_ranks(dist, ms2)
+            extra.append(decode_summary(r2, ms2, args.steps, sp2, peak))
+            del r2
+            torch.cuda.empty_cache()
 
     if rank != 0:
         return 0
-    peak, peak_kind = measured_peaks()
-    achieved = bpc / (kernel_us * 1e-6) / 1e9
+    achieved = rig.bpc / (kernel_us * 1e-6) / 1e9
     traffic = recorded_traffic(case.name)
-    kernel = "decode_split_kernel" if launches_per_call == 1 else \
+    kernel = "decode_split_kernel" if rig.launches_per_call == 1 else \
         "decode_split_kernel with decode_combine_kernel (timed together: the combine overlaps the split's tail)"
     roofline = {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak,
                 "unit": "GB/s", "frac": round(achieved / peak, 4),
                 "traffic": traffic, "peak_kind": peak_kind, "kernel": kernel,
-                "algorithmic_bytes_per_launch": bpc, "launch_us": round(kernel_us, 3)}
+                "algorithmic_bytes_per_launch": rig.bpc, "launch_us": round(kernel_us, 3)}
     cpu = None
     if world == 1 and not args.no_cpu_baseline:
         gbs, per, sample, cores, _ = oracle_rate(case, budget_s=args.cpu_budget)
         cpu = {"value": round(gbs, 4), "unit": "GB/s", "cores": cores, "kind": "oracle", "sample": sample}
-    cfg = config_of(args, case, splits)
-    cfg["l2"] = (f"rotating {copies} pool copies ({copies * pool_bytes / 1e9:.2f} GB, "
-                 f"{copies * bpc / 1e6:.0f} MB of reads per rotation > 3x L2): every step reads KV from HBM")
-    cfg["timing"] = f"CUDA events around CUDA graphs of {chunk} back-to-back calls"
+    run = run_of(args, case, rig.splits)
+    run["l2"] = (f"rotating {rig.copies} pool copies ({rig.copies * rig.pool_bytes / 1e9:.2f} GB, "
+                 f"{rig.copies * rig.bpc / 1e6:.0f} MB of reads per rotation > 3x L2): every step reads KV from HBM")
+    run["timing"] = (f"CUDA events around CUDA graphs of {chunk} back-to-back calls, queued behind a short "
+                     f"GPU sleep so the region holds only the calls")
     if spot is not None:
-        cfg["spot_check_rel_rms"] = spot
+        run["spot_check_rel_rms"] = spot
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "us_per_call": round(ms_per_step * 1e3, 3),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": cfg, "roofline": roofline, "cpu_baseline": cpu,
-        "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+        "config": config_of(case), "run": run, "roofline": roofline, "cpu_baseline": cpu,
+        "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": rig.host_in.numel(),
+                "d2h_bytes_per_step": rig.o_h.numel() * rig.o_h.element_size(),
                 "steps": e2e_steps, "us_per_step": round(e2e_s / e2e_steps * 1e6, 3),
+                "host_us_per_part": host_parts, "graph_us_per_step": round(graph_us, 3),
                 "resident": "k_pool and v_pool stay in HBM (the KV cache); q, qpos, off and the block table come "
                             "from pinned host memory (one copy) and o goes back (one copy) every step"},
-        "gpu_launches": args.steps * launches_per_call, "clocks": clocks,
+        "gpu_launches": args.steps * rig.launches_per_call
+        + sum(e["steps"] * e["kernels_per_call"] for e in extra), "clocks": clocks,
     }
+    if extra:
+        line["workloads"] = extra
     print(json.dumps(line), flush=True)
     return 0
 
@@ -629,18 +741,17 @@ def run_prefill(args, case, rank, world, dist):
         tflops_cpu = flops * k / (case.rows * case.nh) / per / 1e12
         cpu = {"value": round(tflops_cpu, 6), "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
                "sample": sample}
-    cfg = {"workload": case.name, "nh": case.nh, "nkv": case.nkv, "hd": case.hd, "ctx": case.ctx,
-           "rows": case.rows, "window": case.window, "tiles": ntiles,
-           "rows_per_tile": pgqa.prefill_rows_per_tile(case.hd), "flops_per_call": flops,
+    cfg = prefill_config(case)
+    run = {"tiles": ntiles, "rows_per_tile": pgqa.prefill_rows_per_tile(case.hd),
            "l2": f"rotating {copies} pool copies ({copies * pool_bytes / 1e9:.2f} GB > 3x L2)",
            "timing": f"CUDA events around one CUDA graph of {args.steps} back-to-back calls"}
     if spot is not None:
-        cfg["spot_check_rel_rms"] = spot
+        run["spot_check_rel_rms"] = spot
     line = {
         "metric": "paged causal prefill attention TFLOP/s", "value": round(value, 2), "unit": "TFLOP/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": el_max / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": cfg,
+        "config": cfg, "run": run,
         "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak, "unit": "TFLOP/s",
                      "frac": round(achieved / peak, 4), "traffic": None, "peak_kind": peak_kind,
                      "kernel": "prefill_tc_kernel (hd <= 256) / prefill_kernel (hd 512)", "launch_us": round(kernel_us, 3)},
@@ -757,18 +868,18 @@ def run_multirow(args, case, rank, world, dist):
     if world == 1 and not args.no_cpu_baseline:
         gbs, per, sample, cores, _ = oracle_rate(case, budget_s=args.cpu_budget)
         cpu = {"value": round(gbs, 4), "unit": "GB/s", "cores": cores, "kind": "oracle", "sample": sample}
-    cfg = config_of(args, case, None)
-    cfg.update({"splits": splits, "tiles": ntiles, "path": "pgqa_attn_prefill_split (tcgen05 tiled, split-KV) "
-                "+ the decode combine kernel",
-                "l2": f"rotating {copies} pool copies", "timing": f"CUDA events around one CUDA graph of "
-                f"{args.steps} back-to-back calls (two kernels each)"})
+    cfg = config_of(case)
+    run = {"splits": splits, "tiles": ntiles, "path": "pgqa_attn_prefill_split (tcgen05 tiled, split-KV) "
+           "+ the decode combine kernel",
+           "l2": f"rotating {copies} pool copies", "timing": f"CUDA events around one CUDA graph of "
+           f"{args.steps} back-to-back calls (two kernels each)"}
     if spot is not None:
-        cfg["spot_check_rel_rms"] = spot
+        run["spot_check_rel_rms"] = spot
     line = {
         "metric": "multi-row decode KV GB/s (tiled split-KV path)", "value": round(value, 2), "unit": "GB/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": el_max / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": cfg,
+        "config": cfg, "run": run,
         "roofline": {"bound": "hbm", "achieved": round(value, 2), "peak": peak, "unit": "GB/s",
                      "frac": round(value / peak, 4),
                      "traffic": recorded_traffic(case.name, TILED_TRAFFIC_FILE, TILED_SOURCES),
@@ -902,14 +1013,15 @@ def run_prep(args, case, rank, world, dist):
         gbs, per, sample, cores = prep_oracle_rate(case, args.cpu_budget)
         cpu = {"value": round(gbs, 6), "unit": "GB/s", "cores": cores, "kind": "oracle", "sample": sample}
     cfg = prep_config(case)
-    cfg["l2"] = f"rotating {copies} input/output copies ({copies * nbytes / 1e9:.2f} GB moved > 3x L2)"
-    cfg["timing"] = f"CUDA events around one CUDA graph of {args.steps} back-to-back calls"
+    run = {"l2": f"rotating {copies} input/output copies ({copies * nbytes / 1e9:.2f} GB moved > 3x L2)",
+           "timing": f"CUDA events around one CUDA graph of {args.steps} back-to-back calls"}
     if spot is not None:
-        cfg["spot_check_worst_err_over_abs_plus_rms"] = spot
+        run["spot_check_worst_err_over_abs_plus_rms"] = spot
     line = {
         "metric": PREP_METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": el_max / args.steps, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16 in/out, f32 arithmetic", "data": "synthetic", "config": cfg,
+        "run": run,
         "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4),
                      "traffic": recorded_traffic(case.name, PREP_TRAFFIC_FILE, PREP_SOURCES),
@@ -1074,6 +1186,10 @@ def main(argv=None):
     ap.add_argument("--no-check", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
     ap.add_argument("--sweep-out", default="", help="--workload sweep: write every point's numbers here (JSON)")
+    ap.add_argument("--no-extra", action="store_true",
+                    help="sliding: skip timing the long, batched and tiny configurations beside it")
+    ap.add_argument("--clock-window", type=float, default=1.0,
+                    help="seconds of graph replays around the timed region while clocks are sampled")
     args = ap.parse_args(argv)
     if args.steps < 1 or args.warmup < 0:
         raise SystemExit("--steps >= 1 and --warmup >= 0")
