@@ -129,9 +129,6 @@ struct Smem {
     static constexpr int kMlOff = kObufBytes;
     static constexpr int kStatOff = kMlOff + G::kGroups * kQRows * 8;
     static_assert(kStatOff + kQRows * (G::kGroups + 2) * 4 <= kStagesBytes, "group merge scratch");
-    // cluster merge weights [8][kMaxCluster + 1], after the group-merge scratch
-    static constexpr int kCwOff = (kStatOff + kQRows * (G::kGroups + 2) * 4 + 15) / 16 * 16;
-    static_assert(kCwOff + kQRows * (kMaxCluster + 1) * 4 <= kStagesBytes, "cluster merge scratch");
     static_assert(kAllocCluster <= 227 * 1024, "shared memory");
 };
 
@@ -443,6 +440,33 @@ __device__ __forceinline__ float merge_stats_values(float2 (&v)[kPer], int S, fl
     return L;
 }
 
+// The statistics of merge_stats_values<1, kMaxCluster> for C <= kMaxCluster
+// splits, computed by one thread: pair j at ml[j * stride], weights into w[],
+// returns L.  The sum follows the butterfly as lane 0 sees it -- pairs 0 and
+// 4, 2 and 6, 1 and 5, 3 and 7 first, then those sums over 2, then over 1 --
+// with +0 for pairs past C, so the bits are those of the warp version (and of
+// merge_stats_warp, whose wider butterfly only adds exact zeros first).
+__device__ __forceinline__ float cluster_merge_weights(const float2 *ml, int stride, int C, float (&w)[kMaxCluster])
+{
+    static_assert(kMaxCluster == 8, "the butterfly below is written for 8 lanes");
+    float2 v[kMaxCluster];
+    float mx = -INFINITY;
+#pragma unroll
+    for (int j = 0; j < kMaxCluster; ++j) {
+        v[j] = j < C ? ml[j * stride] : make_float2(-INFINITY, 0.f);
+        mx = fmaxf(mx, v[j].x);
+    }
+    float l[kMaxCluster];
+#pragma unroll
+    for (int j = 0; j < kMaxCluster; ++j) {
+        w[j] = (j >= C || v[j].x == -INFINITY) ? 0.f : exp2f(v[j].x - mx);
+        l[j] = j < C ? __fmaf_rn(w[j], v[j].y, 0.f) : 0.f;
+    }
+    const float a0 = __fadd_rn(l[0], l[4]), a1 = __fadd_rn(l[1], l[5]);
+    const float a2 = __fadd_rn(l[2], l[6]), a3 = __fadd_rn(l[3], l[7]);
+    return __fadd_rn(__fadd_rn(a0, a2), __fadd_rn(a1, a3));
+}
+
 __device__ __forceinline__ float merge_stats_warp(const float2 *ml, int S, float *w, int lane,
                                                   float *m_out = nullptr)
 {
@@ -556,6 +580,104 @@ __device__ __forceinline__ void trace_placement(const DecodeParams &p, int npage
 #endif
 }
 
+// ---------------------------------------------------------------- merges of more than 8 splits
+//
+// The combine kernel runs one CTA per (row, head) and slice of up to 32 float4 of the head dimension
+// (hd / 128 slices, at least one), one lane per float4.  Warp w merges split
+// groups w, w + kCombineWarps, ...: a group's (m, l) and O loads are all in
+// flight at once, so the merge costs about one L2 round trip per level
+// instead of one per split.  Warp 0 then merges the groups.  The statistics
+// routine and the per-element fused multiply-add order are the in-kernel
+// merges', so up to kGroupSplits splits the two agree bit for bit.  Reads
+// rows*nh*S*(hd+2)*4 bytes (the (m, l) pairs once per slice), writes
+// rows*nh*hd*2.
+constexpr int kCombineWarps = 8;
+
+// float4 of the head dimension per CTA, and CTAs per (row, head)
+template <int HD>
+__host__ __device__ constexpr int combine_slice()
+{
+    return HD / 4 < 32 ? HD / 4 : 32;
+}
+
+template <int HD>
+__host__ __device__ constexpr int combine_slices()
+{
+    return HD / 4 / combine_slice<HD>();
+}
+
+// Warps of a combine CTA and its dynamic shared memory (the group outputs of
+// two-level merges), for S splits.
+__host__ __device__ constexpr int combine_warps(int S)
+{
+    return S <= kGroupSplits ? 1 : ((S + kGroupSplits - 1) / kGroupSplits < kCombineWarps
+                                         ? (S + kGroupSplits - 1) / kGroupSplits : kCombineWarps);
+}
+__host__ __device__ constexpr int combine_smem_bytes(int S)
+{
+    return S <= kGroupSplits ? 0 : (S + kGroupSplits - 1) / kGroupSplits * 32 * 16;
+}
+
+// The n <= kGroupSplits partial rows at src, src + HD/4, ... (zero beyond n
+// or off this lane's slice), every load issued before any is used.
+template <int HD>
+__device__ __forceinline__ void combine_load_group(float4 (&v)[kGroupSplits], const float4 *src, int n, bool mine)
+{
+#pragma unroll
+    for (int j = 0; j < kGroupSplits; ++j)
+        v[j] = (mine && j < n) ? __ldcg(src + static_cast<size_t>(j) * (HD / 4)) : make_float4(0.f, 0.f, 0.f, 0.f);
+}
+
+// The merge of the S > kGroupSplits partials of one (row, head) over float4
+// slice c of its head dimension (lanes past the slice idle), by warps
+// warp0 .. warp0 + nw - 1 of the calling CTA: warp w merges split groups
+// w, w + nw, ... (up to kGroupSplits splits each) into og, then the first of
+// them merges the groups and writes o.  `sync` is a barrier over those warps.
+// The combine kernel runs this for every (row, head) and slice.
+template <int HD, typename Sync>
+__device__ __forceinline__ void merge_two_level(const DecodeParams &p, size_t rh, int c, int w, int nw, int lane,
+                                                float (*gw)[kGroupSplits], float2 *gml, float *wts, float4 *og,
+                                                Sync sync)
+{
+    const int S = p.splits;
+    const int d4 = c * combine_slice<HD>() + lane;
+    const bool mine = lane < combine_slice<HD>();
+    const float4 *po = reinterpret_cast<const float4 *>(p.part_o + rh * S * HD) + d4;
+    const float2 *pml = p.part_ml + rh * S;
+    const int ng = (S + kGroupSplits - 1) / kGroupSplits;
+    float4 v[kGroupSplits];
+    for (int g = w; g < ng; g += nw) {
+        const int n = min(kGroupSplits, S - g * kGroupSplits);
+        combine_load_group<HD>(v, po + static_cast<size_t>(g) * kGroupSplits * (HD / 4), n, mine);
+        float m = 0.f;
+        const float L = merge_stats_warp(pml + g * kGroupSplits, n, gw[g], lane, &m);
+        if (lane == 0)
+            gml[g] = make_float2(m, L);
+        __syncwarp();
+        float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int j = 0; j < kGroupSplits; ++j)
+            if (j < n)
+                fma4(a, gw[g][j], v[j]);
+        og[g * 32 + lane] = a;
+    }
+    sync();
+    if (w != 0)
+        return;
+    constexpr int kPer = (kMaxGroups + 31) / 32;
+    float2 sv[kPer];
+#pragma unroll
+    for (int j = 0; j < kPer; ++j)
+        sv[j] = gml[min(lane + 32 * j, ng - 1)];
+    const float L = merge_stats_values(sv, ng, wts, lane);
+    __syncwarp();
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int g = 0; g < ng; ++g)
+        fma4(acc, wts[g], og[g * 32 + lane]);
+    if (mine)
+        store_out4(p.o + rh * HD + d4 * 4, acc, L);
+}
+
 // ---------------------------------------------------------------- main kernel
 //
 // Grid (splits, nkv * hsg, rows); block = the consumer warps of Cfg<HD> + one
@@ -619,6 +741,12 @@ __global__ void __launch_bounds__(Geo<HD>::kThreads, Cfg<HD>::kMinBlocks)
     }
     if (p.cluster > 1)
         cluster_arrive_relaxed();
+    // The tensor maps are kernel parameters, which no earlier kernel writes:
+    // fetching them now hides the descriptor latency of the first copies.
+    if (warp == NW && lane == 0) {
+        tma_prefetch_map(&tm_k);
+        tma_prefetch_map(&tm_v);
+    }
     // Nothing above touched global memory: wait here for the previous kernel
     // in the stream (inputs may be its outputs), then let the next one launch.
     grid_dependency_wait();
@@ -755,10 +883,6 @@ __global__ void __launch_bounds__(Geo<HD>::kThreads, Cfg<HD>::kMinBlocks)
 
     if (warp == NW) {
         // ------------------------------------------------ producer warp
-        if (lane == 0) {
-            tma_prefetch_map(&tm_k);
-            tma_prefetch_map(&tm_v);
-        }
         bool ok = true;
         for (int c0 = 0; c0 < npages_mine && ok; c0 += 32) {
             int phys = phys_first;
@@ -982,35 +1106,33 @@ __global__ void __launch_bounds__(Geo<HD>::kThreads, Cfg<HD>::kMinBlocks)
     named_bar_sync<kAllConsumersBarrier, NT>();
     if (tid == 0)
         trace_event(p, kTrGroupO);
-    if (tid < kQRows) {
-        float mx = -INFINITY, L = 0.f;    // query rows >= nq: an empty partial
-        if (tid < nq) {
+    // weights of the page groups for query row q, w_g = 2^(m_g - max_g m_g)
+    // (0 for a group that saw nothing); every thread that needs them computes
+    // them the same way, so all copies agree bit for bit
+    auto group_weights = [&](int q, float (&w)[NG]) {
+        float mx = -INFINITY;
+#pragma unroll
+        for (int g = 0; g < NG; ++g)
+            mx = fmaxf(mx, mlbuf[g * kQRows + q].x);
+#pragma unroll
+        for (int g = 0; g < NG; ++g) {
+            const float m = mlbuf[g * kQRows + q].x;
+            w[g] = (m == -INFINITY) ? 0.f : exp2f(m - mx);
+        }
+        return mx;
+    };
+    // this split's (M, L) of query row q (an empty partial past the served rows)
+    auto split_stats = [&](int q) {
+        float mx = -INFINITY, L = 0.f;
+        if (q < nq) {
+            float w[NG];
+            mx = group_weights(q, w);
+#pragma unroll
             for (int g = 0; g < NG; ++g)
-                mx = fmaxf(mx, mlbuf[g * kQRows + tid].x);
-            for (int g = 0; g < NG; ++g) {
-                const float2 v = mlbuf[g * kQRows + tid];
-                const float ws = (v.x == -INFINITY) ? 0.f : exp2f(v.x - mx);
-                stat[tid * (NG + 2) + g] = ws;
-                L = __fmaf_rn(ws, v.y, L);
-            }
-            stat[tid * (NG + 2) + NG] = L;
-            stat[tid * (NG + 2) + NG + 1] = mx;
-            if (S > 1 && p.cluster <= 1) {
-                const size_t rh = static_cast<size_t>(r0 + tid / nh_sub) * p.nh + head0 + tid % nh_sub;
-                p.part_ml[rh * S + split] = make_float2(mx, L);
-            }
+                L = __fmaf_rn(w[g], mlbuf[g * kQRows + q].y, L);
         }
-        if (p.cluster > 1) {
-            // this split's (M, L) to every slice owner, ahead of the O slices,
-            // so the owners' merge weights overlap the O transfer
-            const uint32_t a = smem_u32(reinterpret_cast<float2 *>(smem + SM::kRecvMlOff) + split * kQRows + tid);
-            for (int j = 0; j < p.cluster; ++j)
-                st_async_f32x2(map_to_cta(a, j), make_float2(mx, L), map_to_cta(s_recv_ml, j));
-        }
-    }
-    named_bar_sync<kAllConsumersBarrier, NT>();
-    if (tid == 0)
-        trace_event(p, kTrGroupStats);
+        return make_float2(mx, L);
+    };
 
     if (p.cluster > 1) {
         // ------------------------------------------------ on-chip merge of the cluster
@@ -1021,11 +1143,21 @@ __global__ void __launch_bounds__(Geo<HD>::kThreads, Cfg<HD>::kMinBlocks)
         // receive barrier.  The merge then runs on local shared memory, with
         // the same operations in the same order as the combine kernel, and
         // no CTA reads a peer, so none waits for its peers before exiting.
+        // Every thread derives the weights it needs itself: no barrier
+        // between the group merge, the pushes and the final merge.
         const int C = p.cluster;                         // 2, 4 or 8
         const int lg_slice = kLgHd<HD> - (31 - __clz(C));
         const int slice = 1 << lg_slice;                 // hd / C
         float *recv_o = reinterpret_cast<float *>(smem + SM::kRecvOff);
         float2 *recv_ml = reinterpret_cast<float2 *>(smem + SM::kRecvMlOff);
+        if (tid < kQRows) {
+            // this split's (M, L) to every slice owner, ahead of the O slices,
+            // so the owners' merge weights overlap the O transfer
+            const float2 ml = split_stats(tid);
+            const uint32_t a = smem_u32(recv_ml + split * kQRows + tid);
+            for (int j = 0; j < C; ++j)
+                st_async_f32x2(map_to_cta(a, j), ml, map_to_cta(s_recv_ml, j));
+        }
         constexpr int kVec = HD / 4;
 #pragma unroll
         for (int k = 0; k < kQRows * kVec / NT; ++k) {
@@ -1033,15 +1165,16 @@ __global__ void __launch_bounds__(Geo<HD>::kThreads, Cfg<HD>::kMinBlocks)
             const int q = e / kVec, d = (e - q * kVec) * 4;
             float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
             if (q < nq) {
-                const float *st = stat + q * (NG + 2);
+                float w[NG];
+                group_weights(q, w);
                 const float *ob = obuf + q * SM::kObufStride + d;
 #pragma unroll
                 for (int g = 0; g < NG; ++g) {
                     const float4 v = *reinterpret_cast<const float4 *>(ob + g * kQRows * SM::kObufStride);
-                    o.x = __fmaf_rn(st[g], v.x, o.x);
-                    o.y = __fmaf_rn(st[g], v.y, o.y);
-                    o.z = __fmaf_rn(st[g], v.z, o.z);
-                    o.w = __fmaf_rn(st[g], v.w, o.w);
+                    o.x = __fmaf_rn(w[g], v.x, o.x);
+                    o.y = __fmaf_rn(w[g], v.y, o.y);
+                    o.z = __fmaf_rn(w[g], v.z, o.z);
+                    o.w = __fmaf_rn(w[g], v.w, o.w);
                 }
             }
             const int j = d >> lg_slice;
@@ -1054,41 +1187,50 @@ __global__ void __launch_bounds__(Geo<HD>::kThreads, Cfg<HD>::kMinBlocks)
             return;
         if (tid == 0)
             trace_event(p, kTrTicket);
-        float *cw = reinterpret_cast<float *>(smem + SM::kCwOff);
-        for (int q = warp; q < nq; q += NW) {
-            float2 v[1];
-            v[0] = lane < C ? recv_ml[lane * kQRows + q] : make_float2(-INFINITY, 0.f);
-            const float L = merge_stats_values<1, kMaxCluster>(v, C, cw + q * (kMaxCluster + 1), lane);
-            if (lane == 0)
-                cw[q * (kMaxCluster + 1) + kMaxCluster] = L;
-        }
-        if (tid == 0)
-            trace_event(p, kTrStats);
-        if (!mbar_wait_bounded(s_recv, 0, p.err, kErrTimeoutCluster))
-            return;
-        named_bar_sync<kAllConsumersBarrier, NT>();
-        if (tid == 0)
-            trace_event(p, kTrFence);
         const int d0 = split * slice;
+        bool have = false;
         for (int e = tid; e < (nq << lg_slice); e += NT) {
             const int q = e >> lg_slice, dd = e & (slice - 1);
-            float vj[kMaxCluster];
-#pragma unroll
-            for (int j = 0; j < kMaxCluster; ++j)
-                vj[j] = j < C ? recv_o[((j * kQRows + q) << lg_slice) + dd] : 0.f;
-            const float *w = cw + q * (kMaxCluster + 1);
+            float w[kMaxCluster];
+            const float L = cluster_merge_weights(recv_ml + q, kQRows, C, w);
+            if (!have) {
+                if (tid == 0)
+                    trace_event(p, kTrStats);
+                if (!mbar_wait_bounded(s_recv, 0, p.err, kErrTimeoutCluster))
+                    return;
+                have = true;
+            }
             float acc = 0.f;
 #pragma unroll
             for (int j = 0; j < kMaxCluster; ++j)
                 if (j < C)
-                    acc = __fmaf_rn(w[j], vj[j], acc);
+                    acc = __fmaf_rn(w[j], recv_o[((j * kQRows + q) << lg_slice) + dd], acc);
             const size_t rh = static_cast<size_t>(r0 + q / nh_sub) * p.nh + head0 + q % nh_sub;
-            p.o[rh * HD + d0 + dd] = merge_finish(acc, w[kMaxCluster]);
+            p.o[rh * HD + d0 + dd] = merge_finish(acc, L);
         }
         if (tid == 0)
             trace_event(p, kTrMerged, true);
         return;
     }
+
+    if (tid < kQRows) {
+        const float2 ml = split_stats(tid);
+        float w[NG];
+        if (tid < nq)
+            group_weights(tid, w);
+#pragma unroll
+        for (int g = 0; g < NG; ++g)
+            stat[tid * (NG + 2) + g] = tid < nq ? w[g] : 0.f;
+        stat[tid * (NG + 2) + NG] = ml.y;
+        stat[tid * (NG + 2) + NG + 1] = ml.x;
+        if (S > 1 && tid < nq) {
+            const size_t rh = static_cast<size_t>(r0 + tid / nh_sub) * p.nh + head0 + tid % nh_sub;
+            p.part_ml[rh * S + split] = ml;
+        }
+    }
+    named_bar_sync<kAllConsumersBarrier, NT>();
+    if (tid == 0)
+        trace_event(p, kTrGroupStats);
 #pragma unroll
     for (int q = 0; q < kQRows; ++q) {
         if (q < nq) {
@@ -1187,52 +1329,7 @@ __global__ void __launch_bounds__(Geo<HD>::kThreads, Cfg<HD>::kMinBlocks)
 
 // ---------------------------------------------------------------- combine kernel
 //
-// One CTA per (row, head) and slice of up to 32 float4 of the head dimension
-// (hd / 128 slices, at least one), one lane per float4.  Warp w merges split
-// groups w, w + kCombineWarps, ...: a group's (m, l) and O loads are all in
-// flight at once, so the merge costs about one L2 round trip per level
-// instead of one per split.  Warp 0 then merges the groups.  The statistics
-// routine and the per-element fused multiply-add order are the in-kernel
-// merges', so up to kGroupSplits splits the two agree bit for bit.  Reads
-// rows*nh*S*(hd+2)*4 bytes (the (m, l) pairs once per slice), writes
-// rows*nh*hd*2.
-constexpr int kCombineWarps = 8;
-
-// float4 of the head dimension per CTA, and CTAs per (row, head)
-template <int HD>
-__host__ __device__ constexpr int combine_slice()
-{
-    return HD / 4 < 32 ? HD / 4 : 32;
-}
-
-template <int HD>
-__host__ __device__ constexpr int combine_slices()
-{
-    return HD / 4 / combine_slice<HD>();
-}
-
-// Warps of a combine CTA and its dynamic shared memory (the group outputs of
-// two-level merges), for S splits.
-__host__ __device__ constexpr int combine_warps(int S)
-{
-    return S <= kGroupSplits ? 1 : ((S + kGroupSplits - 1) / kGroupSplits < kCombineWarps
-                                         ? (S + kGroupSplits - 1) / kGroupSplits : kCombineWarps);
-}
-__host__ __device__ constexpr int combine_smem_bytes(int S)
-{
-    return S <= kGroupSplits ? 0 : (S + kGroupSplits - 1) / kGroupSplits * 32 * 16;
-}
-
-// The n <= kGroupSplits partial rows at src, src + HD/4, ... (zero beyond n
-// or off this lane's slice), every load issued before any is used.
-template <int HD>
-__device__ __forceinline__ void combine_load_group(float4 (&v)[kGroupSplits], const float4 *src, int n, bool mine)
-{
-#pragma unroll
-    for (int j = 0; j < kGroupSplits; ++j)
-        v[j] = (mine && j < n) ? __ldcg(src + static_cast<size_t>(j) * (HD / 4)) : make_float4(0.f, 0.f, 0.f, 0.f);
-}
-
+// The merge of the split partials as a kernel of its own (see above).
 template <int HD>
 __global__ void __launch_bounds__(kCombineWarps * 32) decode_combine_kernel(const DecodeParams p)
 {
@@ -1243,16 +1340,15 @@ __global__ void __launch_bounds__(kCombineWarps * 32) decode_combine_kernel(cons
     const size_t rh = blockIdx.x;
     const int S = p.splits;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int d4 = blockIdx.y * combine_slice<HD>() + lane;
-    const bool mine = lane < combine_slice<HD>();
     grid_dependency_wait();          // the split kernel's partials
     grid_launch_dependents();
-    const float4 *po = reinterpret_cast<const float4 *>(p.part_o + rh * S * HD) + d4;
-    const float2 *pml = p.part_ml + rh * S;
-    float4 v[kGroupSplits];
     if (S <= kGroupSplits) {         // one level, one warp
+        const int d4 = blockIdx.y * combine_slice<HD>() + lane;
+        const bool mine = lane < combine_slice<HD>();
+        const float4 *po = reinterpret_cast<const float4 *>(p.part_o + rh * S * HD) + d4;
+        float4 v[kGroupSplits];
         combine_load_group<HD>(v, po, S, mine);
-        const float L = merge_stats_warp(pml, S, gw[0], lane);
+        const float L = merge_stats_warp(p.part_ml + rh * S, S, gw[0], lane);
         __syncwarp();
         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
@@ -1264,38 +1360,7 @@ __global__ void __launch_bounds__(kCombineWarps * 32) decode_combine_kernel(cons
         return;
     }
     // two levels: groups of 8 splits, each merged as above into (M_g, L_g, O_g), then the groups
-    const int ng = (S + kGroupSplits - 1) / kGroupSplits;
-    const int nw = blockDim.x >> 5;
-    for (int g = warp; g < ng; g += nw) {
-        const int n = min(kGroupSplits, S - g * kGroupSplits);
-        combine_load_group<HD>(v, po + static_cast<size_t>(g) * kGroupSplits * (HD / 4), n, mine);
-        float m = 0.f;
-        const float L = merge_stats_warp(pml + g * kGroupSplits, n, gw[g], lane, &m);
-        if (lane == 0)
-            gml[g] = make_float2(m, L);
-        __syncwarp();
-        float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-        for (int j = 0; j < kGroupSplits; ++j)
-            if (j < n)
-                fma4(a, gw[g][j], v[j]);
-        og[g * 32 + lane] = a;
-    }
-    __syncthreads();
-    if (warp != 0)
-        return;
-    constexpr int kPer = (kMaxGroups + 31) / 32;
-    float2 sv[kPer];
-#pragma unroll
-    for (int j = 0; j < kPer; ++j)
-        sv[j] = gml[min(lane + 32 * j, ng - 1)];
-    const float L = merge_stats_values(sv, ng, wts, lane);
-    __syncwarp();
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int g = 0; g < ng; ++g)
-        fma4(acc, wts[g], og[g * 32 + lane]);
-    if (mine)
-        store_out4(p.o + rh * HD + d4 * 4, acc, L);
+    merge_two_level<HD>(p, rh, blockIdx.y, warp, blockDim.x >> 5, lane, gw, gml, wts, og, [] { __syncthreads(); });
 }
 
 }  // namespace pgqa
