@@ -140,6 +140,45 @@ __device__ __forceinline__ float ex2_sfu(float x)
     return y;
 }
 
+// L2 prefetches (hints: nothing is written, nothing waits): a contiguous
+// range of `bytes` (16-byte aligned and sized), and one TMA box of a tensor map.
+__device__ __forceinline__ void l2_prefetch_bytes(const void *src, uint32_t bytes)
+{
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(src)), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void l2_prefetch_box_3d(const CUtensorMap *map, int x, int y, int z)
+{
+    asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(x), "r"(y), "r"(z)
+                 : "memory");
+}
+
+__device__ __forceinline__ void l2_prefetch_box_4d(const CUtensorMap *map, int x, int y, int z, int w)
+{
+    asm volatile("cp.async.bulk.prefetch.tensor.4d.L2.global.tile [%0, {%1, %2, %3, %4}];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(x), "r"(y), "r"(z), "r"(w)
+                 : "memory");
+}
+
+// Non-blocking test of an mbarrier phase (try_wait may suspend the thread for
+// a while before it answers, which would hold up a poller watching two barriers).
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
 // ---------------------------------------------------------------- geometry
 
 template <int HD>
@@ -159,13 +198,21 @@ struct TcGeo {
     static constexpr int kSoftmaxWarps = 16;           // four threads per query row
     static constexpr int kParts = kSoftmaxWarps / 4;   // threads per row, each over 1/kParts of the columns
     static constexpr int kXOff = kStageOff + kStages * kStageBytes;   // row max [2][parts][128], row sum [parts][128]
-    static constexpr int kBarOff = kXOff + (2 * kParts * kRows + kParts * kRows) * 4;
-    // full[stages], empty[stages], s_full[2], s_free[2], p_full, o_done, q_ready, o_free
-    static constexpr int kBars = 2 * kStages + 8;
+    // the scheduler's published items: [2] TcItem, then [2][kRows] int2 row windows
+    static constexpr int kInfoOff = kXOff + (2 * kParts * kRows + kParts * kRows) * 4;
+    static constexpr int kInfoBytes = 2 * 64;          // two slots of kItemSlot bytes
+    static constexpr int kWinOff = kInfoOff + kInfoBytes;
+    static constexpr int kBarOff = kWinOff + 2 * kRows * 8;
+    // full[stages], empty[stages], s_full[2], s_free[2], p_full, o_done, q_ready, o_free,
+    // info_full[2], info_empty[2]
+    static constexpr int kBars = 2 * kStages + 12;
     static constexpr int kSlotOff = kBarOff + kBars * 8;
     static constexpr int kTotal = kSlotOff + 16;
     static constexpr int kAlloc = kTotal + 1024;
-    static constexpr int kThreads = (kSoftmaxWarps + 2) * 32;   // + producer, MMA issuer
+    static constexpr int kProducerWarp = kSoftmaxWarps;
+    static constexpr int kMmaWarp = kSoftmaxWarps + 1;
+    static constexpr int kSchedWarp = kSoftmaxWarps + 2;
+    static constexpr int kThreads = (kSoftmaxWarps + 3) * 32;   // + producer, MMA issuer, scheduler
     static constexpr int kTmemCols = HD == 64 ? 256 : 512;   // S0, S1, O (hd), Q (hd / 2)
     static constexpr int kOCol = 2 * kBlockTokens;
     static constexpr int kQCol = kOCol + HD;
@@ -175,16 +222,21 @@ struct TcGeo {
 };
 
 // One work item: the 128 query rows of chunk `chunk` of tile `tile` for kv
-// head `kh`, and the union window of their positions.  Every role computes
-// it the same way (a whole warp, one position per lane).
+// head `kh`, and the union window of their positions.  The scheduler warp
+// computes each item once and publishes it, with every query row's window,
+// through shared memory.
 struct TcItem {
     int t0, tn, kh, qbase, lo_u, hi_u, p_first, npages, nblocks, off0, split;
     bool live;     // the chunk has rows
 };
+constexpr int kItemSlot = 64;     // bytes of one published item in shared memory
+static_assert(sizeof(TcItem) <= kItemSlot && kItemSlot % 16 == 0, "published item slot");
 
+// Item `it` (by one whole warp, four query rows per lane), and the visible
+// range (lo, hi) of each of its 128 query rows into win[] ((1, 0): no row).
 template <int HD>
-__device__ __forceinline__ TcItem tc_item(const PrefillParams &p, int it, int ntiles, int nchunks, int lane,
-                                          bool report)
+__device__ __forceinline__ TcItem tc_item_rows(const PrefillParams &p, int it, int ntiles, int nchunks, int lane,
+                                               int2 *win)
 {
     using G = TcGeo<HD>;
     TcItem I;
@@ -208,27 +260,28 @@ __device__ __forceinline__ TcItem tc_item(const PrefillParams &p, int it, int nt
     I.npages = 0;
     I.nblocks = 0;
     I.off0 = 0;
-    if (I.tn > p.rows_per_tile) {
-        if (report && lane == 0)
-            atomicOr(p.err, kErrTileRows);
-        return I;
-    }
+    const bool too_long = I.tn > p.rows_per_tile;
+    if (too_long && lane == 0)
+        atomicOr(p.err, kErrTileRows);
     const int g = p.g;
-    const int nqr = I.tn * g;
-    if (I.tn <= 0 || I.qbase >= nqr)
-        return I;
-    I.live = true;
-    const int pr_first = I.qbase / g;
-    const int pr_last = min(I.tn - 1, (I.qbase + G::kRows - 1) / g);
+    const int nqr = too_long ? 0 : I.tn * g;
     int lo_m = INT_MAX, hi_m = INT_MIN;
-    for (int pr = pr_first + lane; pr <= pr_last; pr += 32) {
-        int lo, hi;
-        prefill_window(p, I.t0 + pr, lo, hi);
+#pragma unroll
+    for (int k = 0; k < G::kRows / 32; ++k) {
+        const int r = lane + 32 * k;
+        const int qr = I.qbase + r;
+        int lo = 1, hi = 0;
+        if (qr < nqr)
+            prefill_window(p, I.t0 + qr / g, lo, hi);
+        win[r] = make_int2(lo, hi);
         if (hi >= lo) {
             lo_m = min(lo_m, lo);
             hi_m = max(hi_m, hi);
         }
     }
+    if (I.tn <= 0 || I.qbase >= nqr)
+        return I;
+    I.live = true;
 #pragma unroll
     for (int k = 16; k; k >>= 1) {
         lo_m = min(lo_m, __shfl_xor_sync(0xffffffffu, lo_m, k));
@@ -250,6 +303,41 @@ __device__ __forceinline__ TcItem tc_item(const PrefillParams &p, int it, int nt
     I.nblocks = (I.npages + G::kBlockPages - 1) / G::kBlockPages;
     I.off0 = __ldg(p.off + I.t0);
     return I;
+}
+
+// L2 prefetch, by one warp, of an item's Q rows (every head of its kv head, a
+// superset of the chunk's) and of the K and V tiles of its first
+// kPrefetchPages pages.
+template <int HD>
+__device__ __forceinline__ void tc_prefetch_item(const PrefillParams &p, const TcItem &I, const CUtensorMap *tm_k,
+                                                 const CUtensorMap *tm_v, int lane)
+{
+    using G = TcGeo<HD>;
+    constexpr int kPrefetchPages = 2 * G::kBlockPages;
+    if (!I.live || I.nblocks == 0)
+        return;
+    const int g = p.g;
+    const int pr_first = I.qbase / g;
+    const int pr_last = min(I.tn - 1, (I.qbase + G::kRows - 1) / g);
+    for (int pr = pr_first + lane; pr <= pr_last; pr += 32)
+        l2_prefetch_bytes(p.q + (static_cast<size_t>(I.t0 + pr) * p.nh + I.kh * g) * HD,
+                          static_cast<uint32_t>(g * HD * 2));
+    if (lane < min(kPrefetchPages, I.npages)) {
+        int phys = __ldg(p.block_table + I.off0 + I.p_first + lane);
+        if (p.page_map)
+            phys = __ldg(p.page_map + phys);
+        const int t = phys * p.nkv + I.kh;
+#pragma unroll
+        for (int c = 0; c < G::kChunks; ++c)
+            l2_prefetch_box_3d(tm_k, c * kBoxElems, 0, t);
+        if (p.whole_tile_box) {
+            l2_prefetch_box_4d(tm_v, 0, 0, 0, t);
+        } else {
+#pragma unroll
+            for (int c = 0; c < G::kChunks; ++c)
+                l2_prefetch_box_3d(tm_v, c * kBoxElems, 0, t);
+        }
+    }
 }
 
 // Persistent: in round k CTA c serves item k G + c (k even) or k G + G - 1 - c
@@ -279,6 +367,9 @@ __global__ void __launch_bounds__(TcGeo<HD>::kThreads, 1)
     const uint32_t b_odone = b_pfull + 8;
     const uint32_t b_qready = b_odone + 8;
     const uint32_t b_ofree = b_qready + 8;
+    const uint32_t b_ifull = b_ofree + 8;              // [2] a published item is in its slot
+    const uint32_t b_iempty = b_ifull + 16;            // [2] every role has read it
+    const int2 *win = reinterpret_cast<const int2 *>(smem + G::kWinOff);
     uint32_t *tslot = reinterpret_cast<uint32_t *>(smem + G::kSlotOff);
 
     const int tid = threadIdx.x;
@@ -311,6 +402,10 @@ __global__ void __launch_bounds__(TcGeo<HD>::kThreads, 1)
         mbar_init(b_odone, 1);
         mbar_init(b_qready, G::kSoftmaxWarps);
         mbar_init(b_ofree, G::kSoftmaxWarps);
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(b_ifull + 8 * b, 1);
+            mbar_init(b_iempty + 8 * b, G::kSoftmaxWarps + 2);   // softmax warps, producer, MMA issuer
+        }
         mbar_init_fence();
     }
     grid_dependency_wait();
@@ -321,8 +416,45 @@ __global__ void __launch_bounds__(TcGeo<HD>::kThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tbase = *tslot;
+    // The k-th item of this CTA, published by the scheduler in slot k % 2;
+    // the reading warp takes a copy and frees the slot (one arrival per warp).
+    bool iok = true;
+    auto take_item = [&](int k) {
+        const int sl = k & 1;
+        if (iok)
+            iok = mbar_wait_bounded(b_ifull + 8 * sl, (k >> 1) & 1, p.err, kErrTimeoutFull);
+        const TcItem I = *reinterpret_cast<const TcItem *>(smem + G::kInfoOff + sl * kItemSlot);
+        return I;
+    };
+    auto release_item = [&](int k) {
+        __syncwarp();
+        if (lane == 0)
+            mbar_arrive(b_iempty + 8 * (k & 1));
+    };
 
-    if (warp == G::kSoftmaxWarps) {
+    if (warp == G::kSchedWarp) {
+        // ------------------------------------------------ scheduler: items ahead of time
+        // Each item's metadata and row windows take a few dependent global
+        // loads; computed here, up to two items ahead, no other role waits for
+        // them at an item's start.  Each published item's Q rows and first
+        // K/V pages are also prefetched into L2: items of all CTAs end about
+        // together, and their first loads would otherwise meet in one burst.
+        int kit = 0;
+        for (int it = first_item(0); it < nitems; it = next_item(it), ++kit) {
+            const int sl = kit & 1;
+            if (kit >= 2 && lane == 0 && iok)
+                iok = mbar_wait_bounded(b_iempty + 8 * sl, ((kit >> 1) - 1) & 1, p.err, kErrTimeoutEmpty);
+            __syncwarp();
+            int2 *w = reinterpret_cast<int2 *>(smem + G::kWinOff) + sl * G::kRows;
+            const TcItem I = tc_item_rows<HD>(p, it, ntiles, nchunks, lane, w);
+            if (lane == 0)
+                *reinterpret_cast<TcItem *>(smem + G::kInfoOff + sl * kItemSlot) = I;
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(b_ifull + 8 * sl);
+            tc_prefetch_item<HD>(p, I, &tm_k, &tm_v, lane);
+        }
+    } else if (warp == G::kProducerWarp) {
         // ------------------------------------------------ producer: blocks of 4 pages
         if (lane == 0) {
             tma_prefetch_map(&tm_k);
@@ -330,8 +462,10 @@ __global__ void __launch_bounds__(TcGeo<HD>::kThreads, 1)
         }
         bool ok = true;
         int jg = 0;                                    // blocks issued, over all items
-        for (int it = first_item(0); it < nitems; it = next_item(it)) {
-            const TcItem I = tc_item<HD>(p, it, ntiles, nchunks, lane, false);
+        int kit = 0;
+        for (int it = first_item(0); it < nitems; it = next_item(it), ++kit) {
+            const TcItem I = take_item(kit);
+            release_item(kit);
             if (!I.live || I.nblocks == 0)
                 continue;
             const int32_t *tbl = p.block_table + I.off0 + I.p_first;
@@ -374,30 +508,37 @@ __global__ void __launch_bounds__(TcGeo<HD>::kThreads, 1)
                 }
             }
         }
-    } else if (warp == G::kSoftmaxWarps + 1) {
+    } else if (warp == G::kMmaWarp) {
         // ------------------------------------------------ MMA issuer (one thread)
         constexpr uint32_t kIdS = umma_idesc_bf16(128, G::kBlockTokens, 0, 0);
         constexpr uint32_t kIdO = umma_idesc_bf16(128, HD, 0, 1);
         bool ok = true;
         int jg = 0, kq = 0;                            // blocks and items with blocks, over all items
-        for (int it = first_item(0); it < nitems; it = next_item(it)) {
-            const TcItem I = tc_item<HD>(p, it, ntiles, nchunks, lane, false);
+        int kit = 0;
+        for (int it = first_item(0); it < nitems; it = next_item(it), ++kit) {
+            const TcItem I = take_item(kit);
+            release_item(kit);
             if (!I.live || I.nblocks == 0)
                 continue;
             if (lane == 0) {
                 if (ok)
                     ok = mbar_wait_bounded(b_qready, kq & 1, p.err, kErrTimeoutFull);
                 tc_fence_after();
-                for (int j = 0; j <= I.nblocks; ++j) {
-                    if (j < I.nblocks) {
-                        const int jj = jg + j;
+                // Issue S_j and PV_j each as soon as its inputs are ready, S
+                // first when both are: PV_j waits only for P_j, not for the K
+                // of block j + 1 behind it, so a late copy does not hold back
+                // the softmax of block j + 1 (which waits for PV_j).  The
+                // barriers are polled with test_wait, which never suspends.
+                int jS = 0, jP = 0;
+                long long t_last = clock64();
+                while (ok && jP < I.nblocks) {
+                    bool did = false;
+                    if (jS < I.nblocks) {
+                        const int jj = jg + jS;
                         const int st = jj % NST, b = jj & 1;
-                        if (ok)
-                            ok = mbar_wait_bounded(b_full + 8 * st, (jj / NST) & 1, p.err, kErrTimeoutFull);
-                        if (ok && jj >= 2)
-                            ok = mbar_wait_bounded(b_sfree + 8 * b, ((jj - 2) >> 1) & 1, p.err, kErrTimeoutFull);
-                        tc_fence_after();
-                        if (ok) {
+                        if (mbar_test_wait(b_full + 8 * st, (jj / NST) & 1) &&
+                            (jj < 2 || mbar_test_wait(b_sfree + 8 * b, ((jj - 2) >> 1) & 1))) {
+                            tc_fence_after();
                             const uint32_t sK = s_base + G::kStageOff + st * G::kStageBytes;
 #pragma unroll
                             for (int ks = 0; ks < HD / 16; ++ks) {
@@ -406,25 +547,33 @@ __global__ void __launch_bounds__(TcGeo<HD>::kThreads, 1)
                                                  umma_sdesc(sK + c * (G::kBlockTokens * 128) + kk * 32, 16, 1024),
                                                  kIdS, ks > 0);
                             }
+                            umma_commit(b_sfull + 8 * b);
+                            ++jS;
+                            did = true;
                         }
-                        umma_commit(b_sfull + 8 * b);
                     }
-                    if (j >= 1) {
-                        const int jb = j - 1, jj = jg + jb, st = jj % NST;
-                        if (ok)
-                            ok = mbar_wait_bounded(b_pfull, jj & 1, p.err, kErrTimeoutFull);
-                        if (ok && jb == 0 && kq >= 1)      // the previous item's O has been read out
-                            ok = mbar_wait_bounded(b_ofree, (kq - 1) & 1, p.err, kErrTimeoutFull);
-                        tc_fence_after();
-                        if (ok) {
+                    if (jP < jS) {
+                        const int jj = jg + jP, st = jj % NST;
+                        if (mbar_test_wait(b_pfull, jj & 1) &&
+                            (jP != 0 || kq == 0 || mbar_test_wait(b_ofree, (kq - 1) & 1))) {   // previous O read out
+                            tc_fence_after();
                             const uint32_t sV = s_base + G::kStageOff + st * G::kStageBytes + G::kKBytes;
-                            const int np = min(G::kBlockPages, I.npages - jb * G::kBlockPages);
+                            const int np = min(G::kBlockPages, I.npages - jP * G::kBlockPages);
                             for (int pp = 0; pp < np; ++pp)
                                 umma_bf16(tbase + G::kOCol, umma_sdesc(sP + pp * 32, 16, 1024),
-                                          umma_sdesc(sV + pp * G::kVPage, kPage * 128, 1024), kIdO, jb > 0 || pp > 0);
+                                          umma_sdesc(sV + pp * G::kVPage, kPage * 128, 1024), kIdO,
+                                          jP > 0 || pp > 0);
+                            umma_commit(b_odone);
+                            umma_commit(b_empty + 8 * st);
+                            ++jP;
+                            did = true;
                         }
-                        umma_commit(b_odone);
-                        umma_commit(b_empty + 8 * st);
+                    }
+                    if (did) {
+                        t_last = clock64();
+                    } else if (clock64() - t_last > kWaitLimitCycles) {
+                        atomicOr(p.err, kErrTimeoutFull);
+                        ok = false;
                     }
                 }
             }
@@ -501,8 +650,11 @@ __global__ void __launch_bounds__(TcGeo<HD>::kThreads, 1)
         bool pend_va = false;
         float pend_l = 0.f, pend_m = -INFINITY;
         int pend_split = 0;
-        for (int it = first_item(0); it < nitems; it = next_item(it)) {
-            const TcItem I = tc_item<HD>(p, it, ntiles, nchunks, lane, warp == 0);
+        int kit = 0;
+        for (int it = first_item(0); it < nitems; it = next_item(it), ++kit) {
+            const TcItem I = take_item(kit);
+            const int2 wr = win[(kit & 1) * G::kRows + row];     // this query row's visible range
+            release_item(kit);
             if (!I.live)
                 continue;
             bool va = false;
@@ -512,7 +664,8 @@ __global__ void __launch_bounds__(TcGeo<HD>::kThreads, 1)
                 const int qr = I.qbase + row;
                 if (qr < I.tn * p.g) {
                     const int pr = qr / p.g, h = qr - pr * p.g;
-                    prefill_window(p, I.t0 + pr, lo_a, hi_a);
+                    lo_a = wr.x;
+                    hi_a = wr.y;
                     rh = static_cast<size_t>(I.t0 + pr) * p.nh + I.kh * p.g + h;
                     va = true;
                 }
