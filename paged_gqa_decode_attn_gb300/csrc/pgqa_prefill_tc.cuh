@@ -613,6 +613,9 @@ __global__ void __launch_bounds__(TcGeo<HD>::kThreads, 1)
             const size_t prow = frh * p.splits + fsplit;
             if (split_out && fva && part == 0)
                 p.part_ml[prow] = make_float2(fm, lt);
+            // one division per row, then a multiply per element (64 IEEE
+            // divisions per thread took about 4 us per item)
+            const float inv = lt > 0.f ? __frcp_rn(lt) : 0.f;
 #pragma unroll 1
             for (int c0 = part * HO; c0 < (part + 1) * HO; c0 += 16) {
                 uint32_t r[16];
@@ -629,8 +632,8 @@ __global__ void __launch_bounds__(TcGeo<HD>::kThreads, 1)
 #pragma unroll
                     for (int k = 0; k < 8; ++k) {
                         __nv_bfloat162 v;
-                        v.x = merge_finish(__uint_as_float(r[2 * k]), lt);
-                        v.y = merge_finish(__uint_as_float(r[2 * k + 1]), lt);
+                        v.x = __float2bfloat16_rn(__fmul_rn(__uint_as_float(r[2 * k]), inv));
+                        v.y = __float2bfloat16_rn(__fmul_rn(__uint_as_float(r[2 * k + 1]), inv));
                         w[k] = *reinterpret_cast<uint32_t *>(&v);
                     }
                     uint4 *dst = reinterpret_cast<uint4 *>(p.o + frh * HD + c0);
@@ -687,20 +690,32 @@ __global__ void __launch_bounds__(TcGeo<HD>::kThreads, 1)
             // (32 elements) at a time, the parts taking turns; the previous
             // item's S MMAs, the only readers of Q, are all complete
             {
+                // every load of this thread's part goes out before the first store
+                constexpr int kQIt = (HD / 2 + 16 * NP - 1) / (16 * NP);   // 16-column pieces per thread
                 const uint4 *src = reinterpret_cast<const uint4 *>(p.q + rh * HD);
                 const uint32_t tq = trow + G::kQCol;
-#pragma unroll 1
-                for (int c0 = part * 16; c0 < HD / 2; c0 += 16 * NP) {
-                    uint32_t r[16];
+                uint4 qv[kQIt][4];
 #pragma unroll
-                    for (int k = 0; k < 4; ++k) {
-                        const uint4 v = va ? __ldg(src + c0 / 4 + k) : make_uint4(0u, 0u, 0u, 0u);
-                        r[4 * k] = v.x;
-                        r[4 * k + 1] = v.y;
-                        r[4 * k + 2] = v.z;
-                        r[4 * k + 3] = v.w;
+                for (int i = 0; i < kQIt; ++i) {
+                    const int c0 = part * 16 + i * 16 * NP;
+#pragma unroll
+                    for (int k = 0; k < 4; ++k)
+                        qv[i][k] = va && c0 < HD / 2 ? __ldg(src + c0 / 4 + k) : make_uint4(0u, 0u, 0u, 0u);
+                }
+#pragma unroll
+                for (int i = 0; i < kQIt; ++i) {
+                    const int c0 = part * 16 + i * 16 * NP;
+                    if (c0 < HD / 2) {
+                        uint32_t r[16];
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) {
+                            r[4 * k] = qv[i][k].x;
+                            r[4 * k + 1] = qv[i][k].y;
+                            r[4 * k + 2] = qv[i][k].z;
+                            r[4 * k + 3] = qv[i][k].w;
+                        }
+                        tmem_st16(tq + c0, r);
                     }
-                    tmem_st16(tq + c0, r);
                 }
                 tmem_wait_st();
                 tc_fence_before();
