@@ -179,6 +179,15 @@ __device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity)
     return ok != 0;
 }
 
+// 32 bytes to global memory in one instruction (a whole L2 sector); dst must be
+// 32-byte aligned.
+__device__ __forceinline__ void st_global_32B(void *dst, const uint32_t (&w)[8])
+{
+    asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(reinterpret_cast<uint64_t>(dst)),
+                 "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
+                 : "memory");
+}
+
 // ---------------------------------------------------------------- geometry
 
 template <int HD>
@@ -616,17 +625,36 @@ __global__ void __launch_bounds__(TcGeo<HD>::kThreads, 1)
             // one division per row, then a multiply per element (64 IEEE
             // divisions per thread took about 4 us per item)
             const float inv = lt > 0.f ? __frcp_rn(lt) : 0.f;
+            const bool o_sector_aligned = (reinterpret_cast<uintptr_t>(p.o) & 31) == 0;
+            const bool part_sector_aligned = (reinterpret_cast<uintptr_t>(p.part_o) & 31) == 0;
+            // the row's O in pieces of kFinLd x 16 columns: the loads of a piece
+            // are in flight together, then converted and stored
+            constexpr int kFinLd = HO / 16 >= 2 ? 2 : 1;
 #pragma unroll 1
-            for (int c0 = part * HO; c0 < (part + 1) * HO; c0 += 16) {
-                uint32_t r[16];
-                tmem_ld16(trow + G::kOCol + c0, r);
-                tmem_wait_ld();
-                if (fva && split_out) {
-                    float4 *dst = reinterpret_cast<float4 *>(p.part_o + prow * HD + c0);
+            for (int c1 = part * HO; c1 < (part + 1) * HO; c1 += 16 * kFinLd) {
+              uint32_t rr[kFinLd][16];
 #pragma unroll
-                    for (int k = 0; k < 4; ++k)
-                        dst[k] = make_float4(__uint_as_float(r[4 * k]), __uint_as_float(r[4 * k + 1]),
-                                             __uint_as_float(r[4 * k + 2]), __uint_as_float(r[4 * k + 3]));
+              for (int h = 0; h < kFinLd; ++h)
+                  tmem_ld16(trow + G::kOCol + c1 + 16 * h, rr[h]);
+              tmem_wait_ld();
+#pragma unroll
+              for (int h = 0; h < kFinLd; ++h) {
+                const int c0 = c1 + 16 * h;
+                const uint32_t (&r)[16] = rr[h];
+                if (fva && split_out) {
+                    float *dst = p.part_o + prow * HD + c0;
+                    if (part_sector_aligned) {          // two whole sectors
+                        const uint32_t (&lo)[8] = *reinterpret_cast<const uint32_t (*)[8]>(&r[0]);
+                        const uint32_t (&hi)[8] = *reinterpret_cast<const uint32_t (*)[8]>(&r[8]);
+                        st_global_32B(dst, lo);
+                        st_global_32B(dst + 8, hi);
+                    } else {
+#pragma unroll
+                        for (int k = 0; k < 4; ++k)
+                            reinterpret_cast<float4 *>(dst)[k] =
+                                make_float4(__uint_as_float(r[4 * k]), __uint_as_float(r[4 * k + 1]),
+                                            __uint_as_float(r[4 * k + 2]), __uint_as_float(r[4 * k + 3]));
+                    }
                 } else if (fva) {
                     uint32_t w[8];
 #pragma unroll
@@ -636,10 +664,18 @@ __global__ void __launch_bounds__(TcGeo<HD>::kThreads, 1)
                         v.y = __float2bfloat16_rn(__fmul_rn(__uint_as_float(r[2 * k + 1]), inv));
                         w[k] = *reinterpret_cast<uint32_t *>(&v);
                     }
-                    uint4 *dst = reinterpret_cast<uint4 *>(p.o + frh * HD + c0);
-                    dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
-                    dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+                    // one whole sector per lane where o allows it: the 32 lanes
+                    // write 32 rows, so two 16-byte halves would each cost a
+                    // partial-sector write
+                    __nv_bfloat16 *dst = p.o + frh * HD + c0;
+                    if (o_sector_aligned) {
+                        st_global_32B(dst, w);
+                    } else {
+                        reinterpret_cast<uint4 *>(dst)[0] = make_uint4(w[0], w[1], w[2], w[3]);
+                        reinterpret_cast<uint4 *>(dst)[1] = make_uint4(w[4], w[5], w[6], w[7]);
+                    }
                 }
+              }
             }
             tc_fence_before();
             __syncwarp();

@@ -224,6 +224,48 @@ def test_kvpos_below_qpos_and_an_empty_row():
     assert np.all(a[50] == 0), "a row with no visible position must be zero"
 
 
+def test_output_16_byte_aligned_gives_the_same_bits():
+    """o needs only 16-byte alignment; the epilogue's whole-sector stores take 32-byte-aligned outputs, and a
+    16-byte-aligned one takes the two-store path: the bits must not depend on which."""
+    import torch
+    import paged_gqa_decode_attn_gb300 as pgqa
+    from gpu_util import PrefillDev, first_difference
+    c = wl.prefill_case(16, 8, 256, 1024, 300, dist="sym", seed=9)
+    d = PrefillDev(c)
+    ref = d.result()
+    n = c.rows * c.nh * c.hd
+    big = torch.full((n + 16,), 0x5555, dtype=torch.int16, device="cuda")
+    o16 = big[8:8 + n]                       # 16 bytes past a 32-byte boundary
+    assert o16.data_ptr() % 32 == 16
+    pgqa.attn_prefill(o16, d.q, d.k, d.v, d.bt, d.off, d.qpos, d.kvpos, d.t0, d.tn, d.ntiles, c.nh, c.nkv, c.hd,
+                      c.window, d.pm)
+    torch.cuda.synchronize()
+    got = o16.cpu().numpy().view(np.uint16).reshape(ref.shape)
+    assert np.array_equal(got, ref), first_difference(got, ref)
+
+
+def test_split_scratch_16_byte_aligned_gives_the_same_bits():
+    """The split path's partials go out as whole sectors when part is 32-byte aligned, else in 16-byte
+    pieces (the API asks for 16): the merged output must not depend on which."""
+    import torch
+    import paged_gqa_decode_attn_gb300 as pgqa
+    from gpu_util import PrefillDev, first_difference
+    c = many_sequence_case([(16, 2984)], 32, 16, 128, 0, seed=5)
+    splits = 5
+    ref = run_split(c, splits)
+    d = PrefillDev(c)
+    nf = pgqa.decode_part_bytes(c.rows, c.nh, splits, c.hd) // 4
+    big = torch.empty(nf + 8, dtype=torch.float32, device="cuda")
+    part = big[4:4 + nf]                     # 16 bytes past a 32-byte boundary
+    assert part.data_ptr() % 32 == 16
+    d.o.fill_(0x5555)
+    pgqa.attn_prefill_split(d.o, part, d.q, d.k, d.v, d.bt, d.off, d.qpos, d.kvpos, d.t0, d.tn, d.ntiles, c.rows,
+                            c.nh, c.nkv, c.hd, c.window, splits, d.pm)
+    torch.cuda.synchronize()
+    got = d.o.cpu().numpy().view(np.uint16).reshape(ref.shape)
+    assert np.array_equal(got, ref), first_difference(got, ref)
+
+
 def test_kvpos_past_qpos_changes_nothing():
     """Causal prefill: kvpos past qpos gives the bits of kvpos = qpos, on the tiled kernel
     (hd 128, 256), the hd-512 kernel and the split-KV path, with NaN in every slot past the
