@@ -1231,21 +1231,25 @@ __global__ void __launch_bounds__(Geo<HD>::kThreads, Cfg<HD>::kMinBlocks)
     named_bar_sync<kAllConsumersBarrier, NT>();
     if (tid == 0)
         trace_event(p, kTrGroupStats);
+    // this split's O (or, with one split, the output): four consecutive dims
+    // per thread and step, so loads and stores go out 16 (8) bytes wide
+    {
+        constexpr int kVec4 = HD / 4;
 #pragma unroll
-    for (int q = 0; q < kQRows; ++q) {
-        if (q < nq) {
-            const float *st = stat + q * (NG + 2);
-            const size_t rh = static_cast<size_t>(r0 + q / nh_sub) * p.nh + head0 + q % nh_sub;
-#pragma unroll
-            for (int d = tid; d < HD; d += NT) {
-                float o = 0.f;
+        for (int k = 0; k < kQRows * kVec4 / NT; ++k) {
+            const int e = tid + k * NT;
+            const int q = e / kVec4, d = (e - q * kVec4) * 4;
+            if (q < nq) {
+                const float *st = stat + q * (NG + 2);
+                const size_t rh = static_cast<size_t>(r0 + q / nh_sub) * p.nh + head0 + q % nh_sub;
+                float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
                 for (int g = 0; g < NG; ++g)
-                    o = __fmaf_rn(st[g], obuf[(g * kQRows + q) * SM::kObufStride + d], o);
+                    fma4(o, st[g], *reinterpret_cast<const float4 *>(obuf + (g * kQRows + q) * SM::kObufStride + d));
                 if (S == 1)
-                    p.o[rh * HD + d] = merge_finish(o, st[NG]);
+                    store_out4(p.o + rh * HD + d, o, st[NG]);
                 else
-                    p.part_o[(rh * S + split) * HD + d] = o;
+                    *reinterpret_cast<float4 *>(p.part_o + (rh * S + split) * HD + d) = o;
             }
         }
     }
