@@ -804,7 +804,9 @@ def run_prefill(args, case, rank, world, dist):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": cfg, "run": run,
         "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak, "unit": "TFLOP/s",
-                     "frac": round(achieved / peak, 4), "traffic": None, "peak_kind": peak_kind,
+                     "frac": round(achieved / peak, 4),
+                     "traffic": recorded_traffic(case.name, TILED_TRAFFIC_FILE, TILED_SOURCES) if case.hd <= 256
+                     else None, "peak_kind": peak_kind,
                      "kernel": "prefill_tc_kernel (hd <= 256) / prefill_kernel (hd 512)", "launch_us": round(kernel_us, 3)},
         "cpu_baseline": cpu,
         "e2e": {"value": round(e2e_value, 2), "unit": "TFLOP/s", "h2d_bytes_per_step": host_in.numel(),
