@@ -221,7 +221,8 @@ struct TcGeo {
     static constexpr int kProducerWarp = kSoftmaxWarps;
     static constexpr int kMmaWarp = kSoftmaxWarps + 1;
     static constexpr int kSchedWarp = kSoftmaxWarps + 2;
-    static constexpr int kThreads = (kSoftmaxWarps + 3) * 32;   // + producer, MMA issuer, scheduler
+    static constexpr int kPvWarp = kSoftmaxWarps + 3;
+    static constexpr int kThreads = (kSoftmaxWarps + 4) * 32;   // + producer, S issuer, scheduler, PV issuer
     static constexpr int kTmemCols = HD == 64 ? 256 : 512;   // S0, S1, O (hd), Q (hd / 2)
     static constexpr int kOCol = 2 * kBlockTokens;
     static constexpr int kQCol = kOCol + HD;
@@ -413,7 +414,7 @@ __global__ void __launch_bounds__(TcGeo<HD>::kThreads, 1)
         mbar_init(b_ofree, G::kSoftmaxWarps);
         for (int b = 0; b < 2; ++b) {
             mbar_init(b_ifull + 8 * b, 1);
-            mbar_init(b_iempty + 8 * b, G::kSoftmaxWarps + 2);   // softmax warps, producer, MMA issuer
+            mbar_init(b_iempty + 8 * b, G::kSoftmaxWarps + 3);   // softmax warps, producer, S and PV issuers
         }
         mbar_init_fence();
     }
@@ -518,9 +519,13 @@ __global__ void __launch_bounds__(TcGeo<HD>::kThreads, 1)
             }
         }
     } else if (warp == G::kMmaWarp) {
-        // ------------------------------------------------ MMA issuer (one thread)
+        // ------------------------------------------------ S issuer (one thread)
+        // The S and PV batches come from two threads of two warps: issuing an
+        // MMA batch takes the issuing thread a good fraction of a microsecond,
+        // and with one thread PV_j waited for the S batch in its way.  Their
+        // MMAs touch disjoint tensor memory (S buffers, O) and meet only
+        // through the barriers below.
         constexpr uint32_t kIdS = umma_idesc_bf16(128, G::kBlockTokens, 0, 0);
-        constexpr uint32_t kIdO = umma_idesc_bf16(128, HD, 0, 1);
         bool ok = true;
         int jg = 0, kq = 0;                            // blocks and items with blocks, over all items
         int kit = 0;
@@ -533,57 +538,63 @@ __global__ void __launch_bounds__(TcGeo<HD>::kThreads, 1)
                 if (ok)
                     ok = mbar_wait_bounded(b_qready, kq & 1, p.err, kErrTimeoutFull);
                 tc_fence_after();
-                // Issue S_j and PV_j each as soon as its inputs are ready, S
-                // first when both are: PV_j waits only for P_j, not for the K
-                // of block j + 1 behind it, so a late copy does not hold back
-                // the softmax of block j + 1 (which waits for PV_j).  The
-                // barriers are polled with test_wait, which never suspends.
-                int jS = 0, jP = 0;
-                long long t_last = clock64();
-                while (ok && jP < I.nblocks) {
-                    bool did = false;
-                    if (jS < I.nblocks) {
-                        const int jj = jg + jS;
-                        const int st = jj % NST, b = jj & 1;
-                        if (mbar_test_wait(b_full + 8 * st, (jj / NST) & 1) &&
-                            (jj < 2 || mbar_test_wait(b_sfree + 8 * b, ((jj - 2) >> 1) & 1))) {
-                            tc_fence_after();
-                            const uint32_t sK = s_base + G::kStageOff + st * G::kStageBytes;
+                for (int j = 0; j < I.nblocks; ++j) {
+                    const int jj = jg + j;
+                    const int st = jj % NST, b = jj & 1;
+                    if (ok)
+                        ok = mbar_wait_bounded(b_full + 8 * st, (jj / NST) & 1, p.err, kErrTimeoutFull);
+                    if (ok && jj >= 2)
+                        ok = mbar_wait_bounded(b_sfree + 8 * b, ((jj - 2) >> 1) & 1, p.err, kErrTimeoutFull);
+                    tc_fence_after();
+                    if (ok) {
+                        const uint32_t sK = s_base + G::kStageOff + st * G::kStageBytes;
 #pragma unroll
-                            for (int ks = 0; ks < HD / 16; ++ks) {
-                                const int c = ks >> 2, kk = ks & 3;
-                                umma_bf16_tmem_a(tbase + b * G::kBlockTokens, tbase + G::kQCol + ks * 8,
-                                                 umma_sdesc(sK + c * (G::kBlockTokens * 128) + kk * 32, 16, 1024),
-                                                 kIdS, ks > 0);
-                            }
-                            umma_commit(b_sfull + 8 * b);
-                            ++jS;
-                            did = true;
+                        for (int ks = 0; ks < HD / 16; ++ks) {
+                            const int c = ks >> 2, kk = ks & 3;
+                            umma_bf16_tmem_a(tbase + b * G::kBlockTokens, tbase + G::kQCol + ks * 8,
+                                             umma_sdesc(sK + c * (G::kBlockTokens * 128) + kk * 32, 16, 1024),
+                                             kIdS, ks > 0);
                         }
                     }
-                    if (jP < jS) {
-                        const int jj = jg + jP, st = jj % NST;
-                        if (mbar_test_wait(b_pfull, jj & 1) &&
-                            (jP != 0 || kq == 0 || mbar_test_wait(b_ofree, (kq - 1) & 1))) {   // previous O read out
-                            tc_fence_after();
-                            const uint32_t sV = s_base + G::kStageOff + st * G::kStageBytes + G::kKBytes;
-                            const int np = min(G::kBlockPages, I.npages - jP * G::kBlockPages);
-                            for (int pp = 0; pp < np; ++pp)
-                                umma_bf16(tbase + G::kOCol, umma_sdesc(sP + pp * 32, 16, 1024),
-                                          umma_sdesc(sV + pp * G::kVPage, kPage * 128, 1024), kIdO,
-                                          jP > 0 || pp > 0);
-                            umma_commit(b_odone);
-                            umma_commit(b_empty + 8 * st);
-                            ++jP;
-                            did = true;
-                        }
+                    umma_commit(b_sfull + 8 * b);
+                }
+            }
+            __syncwarp();
+            jg += I.nblocks;
+            ++kq;
+        }
+    } else if (warp == G::kPvWarp) {
+        // ------------------------------------------------ PV issuer (one thread)
+        constexpr uint32_t kIdO = umma_idesc_bf16(128, HD, 0, 1);
+        bool ok = true;
+        int jg = 0, kq = 0;
+        int kit = 0;
+        for (int it = first_item(0); it < nitems; it = next_item(it), ++kit) {
+            const TcItem I = take_item(kit);
+            release_item(kit);
+            if (!I.live || I.nblocks == 0)
+                continue;
+            if (lane == 0) {
+                for (int j = 0; j < I.nblocks; ++j) {
+                    const int jj = jg + j, st = jj % NST;
+                    if (ok)
+                        ok = mbar_wait_bounded(b_pfull, jj & 1, p.err, kErrTimeoutFull);
+                    if (ok && j == 0 && kq >= 1)            // the previous item's O has been read out
+                        ok = mbar_wait_bounded(b_ofree, (kq - 1) & 1, p.err, kErrTimeoutFull);
+                    // V_j landed with K_j: the S issuer saw the stage full before S_j, and P_j
+                    // follows S_j; the test is free and makes this thread see it too
+                    if (ok)
+                        ok = mbar_wait_bounded(b_full + 8 * st, (jj / NST) & 1, p.err, kErrTimeoutFull);
+                    tc_fence_after();
+                    if (ok) {
+                        const uint32_t sV = s_base + G::kStageOff + st * G::kStageBytes + G::kKBytes;
+                        const int np = min(G::kBlockPages, I.npages - j * G::kBlockPages);
+                        for (int pp = 0; pp < np; ++pp)
+                            umma_bf16(tbase + G::kOCol, umma_sdesc(sP + pp * 32, 16, 1024),
+                                      umma_sdesc(sV + pp * G::kVPage, kPage * 128, 1024), kIdO, j > 0 || pp > 0);
                     }
-                    if (did) {
-                        t_last = clock64();
-                    } else if (clock64() - t_last > kWaitLimitCycles) {
-                        atomicOr(p.err, kErrTimeoutFull);
-                        ok = false;
-                    }
+                    umma_commit(b_odone);
+                    umma_commit(b_empty + 8 * st);
                 }
             }
             __syncwarp();
