@@ -139,36 +139,44 @@ int get_encoder()
 
 // TMA descriptors of a [pages][nkv][16][hd] bf16 pool.  The pool's page
 // count is not known here, so the tile dimension spans the int32 coordinate
-// range; only tiles the block table names are ever addressed.  Preferred is
-// a 4-D view (64 dims, 16 slots, hd/64 dim chunks, tile = phys*nkv + kh)
-// whose single box is a whole (page, kv head) tile -- one TMA per tile, laid
-// out in shared memory as [chunk][slot][64] under the 128-byte swizzle.  If
-// the driver refuses that stride order, a 3-D view (dims, slots, tiles) with
-// 64-dim boxes gives the same shared-memory layout in hd/64 copies.
+// range; only tiles the block table names are ever addressed.  Three views,
+// all under the 128-byte swizzle:
+//   kMapWhole  -- 4-D (64 dims, 16 slots, hd/64 dim chunks, tile = phys*nkv + kh):
+//                 one box per (page, kv head) tile, in shared memory as
+//                 [chunk][slot][64];
+//   kMapHalves -- 5-D (64 dims, 8 slots, hd/64 chunks, 2 slot halves, tile):
+//                 one box per tile, in shared memory as [half][chunk][8 slots][64],
+//                 so that the 8-slot swizzle atoms of one chunk sit hd * 16
+//                 bytes apart across consecutive tiles (the tcgen05 prefill's
+//                 K operand);
+//   kMapChunks -- 3-D (dims, slots, tiles) with 64-dim boxes: hd/64 copies per
+//                 tile, and the fallback where the driver refuses the others.
+enum MapKind { kMapWhole = 1, kMapHalves = 2, kMapChunks = 0 };
+
 struct MapCacheEntry {
     const void *base = nullptr;
     int hd = 0;
-    bool chunked = false;    // built as hd/64 boxes per tile on request (the tcgen05 prefill)
-    int whole = 0;
+    int want = -1;           // the view asked for
+    int kind = 0;            // the view built
     CUtensorMap map;
 };
 MapCacheEntry g_map_cache[128];
 unsigned g_map_next = 0;
 
-int pool_map(const void *base, int hd, CUtensorMap *out, int *whole, bool chunked = false)
+int pool_map(const void *base, int hd, CUtensorMap *out, int *kind, int want = kMapWhole)
 {
     for (auto &e : g_map_cache)
-        if (e.base == base && e.hd == hd && e.chunked == chunked) {
+        if (e.base == base && e.hd == hd && e.want == want) {
             *out = e.map;
-            *whole = e.whole;
+            *kind = e.kind;
             return PGQA_OK;
         }
     int st = get_encoder();
     if (st != PGQA_OK)
         return st;
     CUtensorMap m;
-    int w = chunked ? 0 : 1;
-    if (w) {
+    int w = want;
+    if (w == kMapWhole) {
         const cuuint64_t dims[4] = {64u, 16u, static_cast<cuuint64_t>(hd / 64), 0x7fffffffull};
         const cuuint64_t strides[3] = {static_cast<cuuint64_t>(hd) * 2u, 128u, static_cast<cuuint64_t>(hd) * 32u};
         const cuuint32_t box[4] = {64u, 16u, static_cast<cuuint32_t>(hd / 64), 1u};
@@ -177,9 +185,20 @@ int pool_map(const void *base, int hd, CUtensorMap *out, int *whole, bool chunke
                               estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
         if (r != CUDA_SUCCESS)
-            w = 0;
+            w = kMapChunks;
+    } else if (w == kMapHalves) {
+        const cuuint64_t dims[5] = {64u, 8u, static_cast<cuuint64_t>(hd / 64), 2u, 0x7fffffffull};
+        const cuuint64_t strides[4] = {static_cast<cuuint64_t>(hd) * 2u, 128u, static_cast<cuuint64_t>(hd) * 16u,
+                                       static_cast<cuuint64_t>(hd) * 32u};
+        const cuuint32_t box[5] = {64u, 8u, static_cast<cuuint32_t>(hd / 64), 2u, 1u};
+        const cuuint32_t estride[5] = {1u, 1u, 1u, 1u, 1u};
+        CUresult r = g_encode(&m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void *>(base), dims, strides, box,
+                              estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        if (r != CUDA_SUCCESS)
+            w = kMapChunks;
     }
-    if (!w) {
+    if (w == kMapChunks) {
         const cuuint64_t dims[3] = {static_cast<cuuint64_t>(hd), 16u, 0x7fffffffull};
         const cuuint64_t strides[2] = {static_cast<cuuint64_t>(hd) * 2u, static_cast<cuuint64_t>(hd) * 32u};
         const cuuint32_t box[3] = {64u, 16u, 1u};
@@ -193,11 +212,11 @@ int pool_map(const void *base, int hd, CUtensorMap *out, int *whole, bool chunke
     MapCacheEntry &e = g_map_cache[g_map_next++ % 128];
     e.base = base;
     e.hd = hd;
-    e.chunked = chunked;
-    e.whole = w;
+    e.want = want;
+    e.kind = w;
     e.map = m;
     *out = m;
-    *whole = w;
+    *kind = w;
     return PGQA_OK;
 }
 
@@ -669,17 +688,19 @@ int prefill_call(void *o, void *part, const void *q, const void *k_pool, const v
     if (st != PGQA_OK)
         return st;
     CUtensorMap tk, tv;
-    int whole_k = 0, whole_v = 0;
-    // The tcgen05 kernel (hd <= 256) copies K by 64-dim boxes into its
-    // 64-token tile and V by whole-tile boxes where the driver takes them;
-    // the hd-512 kernel takes whole-tile boxes for both where it can.
+    int kind_k = 0, kind_v = 0;
+    // The tcgen05 kernel (hd <= 256) copies K by one box per tile in the
+    // halves view (64-dim boxes where the driver refuses it) and V by
+    // whole-tile boxes where the driver takes them; the hd-512 kernel takes
+    // whole-tile boxes for both where it can.
     const bool tc = hd <= 256;
-    if ((st = pool_map(k_pool, hd, &tk, &whole_k, tc)) != PGQA_OK ||
-        (st = pool_map(v_pool, hd, &tv, &whole_v, false)) != PGQA_OK)
+    if ((st = pool_map(k_pool, hd, &tk, &kind_k, tc ? kMapHalves : kMapWhole)) != PGQA_OK ||
+        (st = pool_map(v_pool, hd, &tv, &kind_v)) != PGQA_OK)
         return st;
-    if (!tc && whole_k != whole_v)
+    if (!tc && kind_k != kind_v)
         return PGQA_ERR_TENSOR_MAP;
-    p.whole_tile_box = whole_v;
+    p.whole_tile_box = kind_v == kMapWhole;
+    p.k_halves = kind_k == kMapHalves;
     p.err = s->err;
     a.num_sms = s->num_sms;
     a.tm_k = &tk;

@@ -76,6 +76,7 @@ struct PrefillParams {
     const int32_t *tile_tn;    // [ntiles] rows of each tile
     unsigned int *err;
     int nh, nkv, g, window, rows_per_tile, whole_tile_box;
+    int k_halves;              // tcgen05 kernel: K by one 5-D box per tile ([half][chunk][8][64]), else hd/64 boxes
     // split-KV (tcgen05 kernel only): with splits > 1 each (row, head) writes
     // one unnormalised partial per split -- (m, L) in log2 units into
     // part_ml[rh * splits + s] and O into part_o[(rh * splits + s) * hd] --

@@ -10,12 +10,17 @@
 //     the K/V ring;
 //   * warp 16 streams the chunk's union window in blocks of 4 pages (64
 //     tokens) by TMA into that ring, page ids read 32 at a time ahead of the
-//     copies: K by 64-dim boxes into a [hd/64][64 tokens][128 B] tile (one
-//     N = 64 MMA per 16 dims), V by one box per (page, kv head) tile as
-//     [hd/64][16 tokens][128 B];
+//     copies, one box per (page, kv head) tile each: K in a 5-D view that
+//     lands as [2 halves][hd/64][8 tokens][128 B], so one chunk's 8-token
+//     swizzle atoms sit hd * 16 bytes apart over the block's 4 pages and one
+//     N = 64 MMA per 16 dims reads them (per-page 64-dim boxes, four times as
+//     many copies, where the driver refuses the view); V as
+//     [hd/64][16 tokens][128 B]; a stage's K and V have barriers of their
+//     own, so K_{j+NST} streams in as soon as S_j is done;
 //   * warp 17 issues S_j = Q K_j^T into one of two TMEM buffers (64 columns
-//     each), then O += P_{j-1} V_{j-1} (TMEM, hd columns, one MMA per page),
-//     each batch committed to an mbarrier;
+//     each) and warp 19 O += P_j V_j (TMEM, hd columns, one MMA per page),
+//     each batch committed to mbarriers;
+//   * warp 18 computes the work items ahead and publishes them;
 //   * warps 0-15 run the softmax, four threads per query row (warps w, w+4,
 //     w+8, w+12 share TMEM lanes 32(w%4)..: lane = row), each over a quarter
 //     of the block's columns: they read S_j from TMEM, mask it to the row's
@@ -164,6 +169,25 @@ __device__ __forceinline__ void l2_prefetch_box_4d(const CUtensorMap *map, int x
                  : "memory");
 }
 
+__device__ __forceinline__ void l2_prefetch_box_5d(const CUtensorMap *map, int t)
+{
+    asm volatile("cp.async.bulk.prefetch.tensor.5d.L2.global.tile [%0, {%1, %1, %1, %1, %2}];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(0), "r"(t)
+                 : "memory");
+}
+
+// One TMA box of a 5-D tensor map at (0, 0, 0, 0, t): a whole (page, kv head)
+// tile in the halves view.
+__device__ __forceinline__ void tma_load_5d_tile(uint32_t dst, const CUtensorMap *map, uint32_t bar, int t)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.5d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %3, %3, %3, %4}], [%2];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(0), "r"(t)
+        : "memory");
+}
+
 // Non-blocking test of an mbarrier phase (try_wait may suspend the thread for
 // a while before it answers, which would hold up a poller watching two barriers).
 __device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity)
@@ -212,9 +236,9 @@ struct TcGeo {
     static constexpr int kInfoBytes = 2 * 64;          // two slots of kItemSlot bytes
     static constexpr int kWinOff = kInfoOff + kInfoBytes;
     static constexpr int kBarOff = kWinOff + 2 * kRows * 8;
-    // full[stages], empty[stages], s_full[2], s_free[2], p_full, o_done, q_ready, o_free,
-    // info_full[2], info_empty[2]
-    static constexpr int kBars = 2 * kStages + 12;
+    // k_full[stages], k_empty[stages], v_full[stages], v_empty[stages], s_full[2], s_free[2],
+    // p_full, o_done, q_ready, o_free, info_full[2], info_empty[2]
+    static constexpr int kBars = 4 * kStages + 12;
     static constexpr int kSlotOff = kBarOff + kBars * 8;
     static constexpr int kTotal = kSlotOff + 16;
     static constexpr int kAlloc = kTotal + 1024;
@@ -337,9 +361,13 @@ __device__ __forceinline__ void tc_prefetch_item(const PrefillParams &p, const T
         if (p.page_map)
             phys = __ldg(p.page_map + phys);
         const int t = phys * p.nkv + I.kh;
+        if (p.k_halves) {
+            l2_prefetch_box_5d(tm_k, t);
+        } else {
 #pragma unroll
-        for (int c = 0; c < G::kChunks; ++c)
-            l2_prefetch_box_3d(tm_k, c * kBoxElems, 0, t);
+            for (int c = 0; c < G::kChunks; ++c)
+                l2_prefetch_box_3d(tm_k, c * kBoxElems, 0, t);
+        }
         if (p.whole_tile_box) {
             l2_prefetch_box_4d(tm_v, 0, 0, 0, t);
         } else {
@@ -369,9 +397,13 @@ __global__ void __launch_bounds__(TcGeo<HD>::kThreads, 1)
     const uint32_t s_base = smem_u32(smem);
     const uint32_t sP = s_base + G::kPOff;
     const uint32_t s_bar = s_base + G::kBarOff;
-    const uint32_t b_full = s_bar;                     // [NST]
-    const uint32_t b_empty = s_bar + 8 * NST;          // [NST]
-    const uint32_t b_sfull = s_bar + 16 * NST;         // [2]
+    // a stage's K and V halves fill and free apart: K is free once its S
+    // batch is done, about a block before the PV batch frees V
+    const uint32_t b_kfull = s_bar;                    // [NST]
+    const uint32_t b_kempty = s_bar + 8 * NST;         // [NST]
+    const uint32_t b_vfull = s_bar + 16 * NST;         // [NST]
+    const uint32_t b_vempty = s_bar + 24 * NST;        // [NST]
+    const uint32_t b_sfull = s_bar + 32 * NST;         // [2]
     const uint32_t b_sfree = b_sfull + 16;             // [2]
     const uint32_t b_pfull = b_sfree + 16;
     const uint32_t b_odone = b_pfull + 8;
@@ -401,8 +433,10 @@ __global__ void __launch_bounds__(TcGeo<HD>::kThreads, 1)
 
     if (tid == 0) {
         for (int s = 0; s < NST; ++s) {
-            mbar_init(b_full + 8 * s, 1);
-            mbar_init(b_empty + 8 * s, 1);
+            mbar_init(b_kfull + 8 * s, 1);
+            mbar_init(b_kempty + 8 * s, 1);
+            mbar_init(b_vfull + 8 * s, 1);
+            mbar_init(b_vempty + 8 * s, 1);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(b_sfull + 8 * b, 1);
@@ -490,27 +524,45 @@ __global__ void __launch_bounds__(TcGeo<HD>::kThreads, 1)
                 for (int i = 0; i < nc; i += G::kBlockPages, ++jg) {
                     const int np = min(G::kBlockPages, nc - i);
                     const int st = jg % NST;
-                    if (lane == 0 && ok && jg >= NST)
-                        ok = mbar_wait_bounded(b_empty + 8 * st, ((jg / NST) - 1) & 1, p.err, kErrTimeoutEmpty);
-                    ok = __shfl_sync(0xffffffffu, ok, 0);
                     const uint32_t sK = s_base + G::kStageOff + st * G::kStageBytes;
                     const uint32_t sV = sK + G::kKBytes;
+                    const uint32_t half_tx = np * kPage * HD * 2;
+                    // K of block jg, once S of block jg - NST is done
+                    if (lane == 0 && ok && jg >= NST)
+                        ok = mbar_wait_bounded(b_kempty + 8 * st, ((jg / NST) - 1) & 1, p.err, kErrTimeoutEmpty);
+                    ok = __shfl_sync(0xffffffffu, ok, 0);
                     if (ok && lane == 0)
-                        mbar_arrive_expect_tx(b_full + 8 * st, np * 2 * kPage * HD * 2);
+                        mbar_arrive_expect_tx(b_kfull + 8 * st, half_tx);
                     for (int pp = 0; pp < G::kBlockPages; ++pp) {
                         const int ph = __shfl_sync(0xffffffffu, phys, (i + pp) & 31);
                         if (ok && lane == 0 && pp < np) {
                             const int t = ph * p.nkv + I.kh;
+                            if (p.k_halves) {      // one box: [half][chunk][8 slots][128 B] per page
+                                tma_load_5d_tile(sK + pp * G::kVPage, &tm_k, b_kfull + 8 * st, t);
+                            } else {               // [chunk][64 tokens][128 B]
 #pragma unroll
-                            for (int c = 0; c < NCH; ++c)
-                                tma_load_3d(sK + c * (G::kBlockTokens * 128) + pp * (kPage * 128), &tm_k,
-                                            b_full + 8 * st, c * kBoxElems, 0, t);
+                                for (int c = 0; c < NCH; ++c)
+                                    tma_load_3d(sK + c * (G::kBlockTokens * 128) + pp * (kPage * 128), &tm_k,
+                                                b_kfull + 8 * st, c * kBoxElems, 0, t);
+                            }
+                        }
+                    }
+                    // V of block jg, once PV of block jg - NST is done
+                    if (lane == 0 && ok && jg >= NST)
+                        ok = mbar_wait_bounded(b_vempty + 8 * st, ((jg / NST) - 1) & 1, p.err, kErrTimeoutEmpty);
+                    ok = __shfl_sync(0xffffffffu, ok, 0);
+                    if (ok && lane == 0)
+                        mbar_arrive_expect_tx(b_vfull + 8 * st, half_tx);
+                    for (int pp = 0; pp < G::kBlockPages; ++pp) {
+                        const int ph = __shfl_sync(0xffffffffu, phys, (i + pp) & 31);
+                        if (ok && lane == 0 && pp < np) {
+                            const int t = ph * p.nkv + I.kh;
                             if (p.whole_tile_box) {
-                                tma_load_4d(sV + pp * G::kVPage, &tm_v, b_full + 8 * st, 0, 0, 0, t);
+                                tma_load_4d(sV + pp * G::kVPage, &tm_v, b_vfull + 8 * st, 0, 0, 0, t);
                             } else {
 #pragma unroll
                                 for (int c = 0; c < NCH; ++c)
-                                    tma_load_3d(sV + pp * G::kVPage + c * (kPage * 128), &tm_v, b_full + 8 * st,
+                                    tma_load_3d(sV + pp * G::kVPage + c * (kPage * 128), &tm_v, b_vfull + 8 * st,
                                                 c * kBoxElems, 0, t);
                             }
                         }
@@ -526,6 +578,12 @@ __global__ void __launch_bounds__(TcGeo<HD>::kThreads, 1)
         // MMAs touch disjoint tensor memory (S buffers, O) and meet only
         // through the barriers below.
         constexpr uint32_t kIdS = umma_idesc_bf16(128, G::kBlockTokens, 0, 0);
+        // K of a block as the B operand (64 token rows, K-major): in the
+        // halves layout a chunk's 8-row swizzle atoms are 1 KB into each
+        // (page, half) and hd * 16 bytes apart; in the chunk layout they are
+        // contiguous, 1 KB apart, within the chunk's 8 KB
+        const uint32_t k_chunk = p.k_halves ? 1024u : static_cast<uint32_t>(G::kBlockTokens * 128);
+        const uint32_t k_sbo = p.k_halves ? static_cast<uint32_t>(NCH * 1024) : 1024u;
         bool ok = true;
         int jg = 0, kq = 0;                            // blocks and items with blocks, over all items
         int kit = 0;
@@ -542,7 +600,7 @@ __global__ void __launch_bounds__(TcGeo<HD>::kThreads, 1)
                     const int jj = jg + j;
                     const int st = jj % NST, b = jj & 1;
                     if (ok)
-                        ok = mbar_wait_bounded(b_full + 8 * st, (jj / NST) & 1, p.err, kErrTimeoutFull);
+                        ok = mbar_wait_bounded(b_kfull + 8 * st, (jj / NST) & 1, p.err, kErrTimeoutFull);
                     if (ok && jj >= 2)
                         ok = mbar_wait_bounded(b_sfree + 8 * b, ((jj - 2) >> 1) & 1, p.err, kErrTimeoutFull);
                     tc_fence_after();
@@ -552,11 +610,11 @@ __global__ void __launch_bounds__(TcGeo<HD>::kThreads, 1)
                         for (int ks = 0; ks < HD / 16; ++ks) {
                             const int c = ks >> 2, kk = ks & 3;
                             umma_bf16_tmem_a(tbase + b * G::kBlockTokens, tbase + G::kQCol + ks * 8,
-                                             umma_sdesc(sK + c * (G::kBlockTokens * 128) + kk * 32, 16, 1024),
-                                             kIdS, ks > 0);
+                                             umma_sdesc(sK + c * k_chunk + kk * 32, 16, k_sbo), kIdS, ks > 0);
                         }
                     }
                     umma_commit(b_sfull + 8 * b);
+                    umma_commit(b_kempty + 8 * st);
                 }
             }
             __syncwarp();
@@ -581,10 +639,10 @@ __global__ void __launch_bounds__(TcGeo<HD>::kThreads, 1)
                         ok = mbar_wait_bounded(b_pfull, jj & 1, p.err, kErrTimeoutFull);
                     if (ok && j == 0 && kq >= 1)            // the previous item's O has been read out
                         ok = mbar_wait_bounded(b_ofree, (kq - 1) & 1, p.err, kErrTimeoutFull);
-                    // V_j landed with K_j: the S issuer saw the stage full before S_j, and P_j
-                    // follows S_j; the test is free and makes this thread see it too
+                    // V_j has landed: the softmax waited for it before P_j (it zeroes edge
+                    // rows of V_j); the test is free and makes this thread see it too
                     if (ok)
-                        ok = mbar_wait_bounded(b_full + 8 * st, (jj / NST) & 1, p.err, kErrTimeoutFull);
+                        ok = mbar_wait_bounded(b_vfull + 8 * st, (jj / NST) & 1, p.err, kErrTimeoutFull);
                     tc_fence_after();
                     if (ok) {
                         const uint32_t sV = s_base + G::kStageOff + st * G::kStageBytes + G::kKBytes;
@@ -594,7 +652,7 @@ __global__ void __launch_bounds__(TcGeo<HD>::kThreads, 1)
                                       umma_sdesc(sV + pp * G::kVPage, kPage * 128, 1024), kIdO, j > 0 || pp > 0);
                     }
                     umma_commit(b_odone);
-                    umma_commit(b_empty + 8 * st);
+                    umma_commit(b_vempty + 8 * st);
                 }
             }
             __syncwarp();
@@ -875,6 +933,8 @@ __global__ void __launch_bounds__(TcGeo<HD>::kThreads, 1)
                 const int btok0 = (I.p_first + j * G::kBlockPages) * kPage;
                 if (btok0 < I.lo_u || btok0 + G::kBlockTokens - 1 > I.hi_u) {
                     const int st = jj % NST;
+                    if (ok)           // V_j lands apart from K_j: zero nothing before the copy has
+                        ok = mbar_wait_bounded(b_vfull + 8 * st, (jj / NST) & 1, p.err, kErrTimeoutFull);
                     uint8_t *sV = smem + G::kStageOff + st * G::kStageBytes + G::kKBytes;
                     const int np = min(G::kBlockPages, I.npages - j * G::kBlockPages);
                     for (int e = tid; e < np * kPage * NCH * 8; e += G::kSoftmaxWarps * 32) {
