@@ -43,7 +43,8 @@ KERNEL_SOURCES = ["paged_gqa_decode_attn_gb300/csrc/pgqa_device.cuh",
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "decode_split_kernel_traffic.json")
 PREP_SOURCES = ["paged_gqa_decode_attn_gb300/csrc/pgqa_prep.cu"]
 PREP_TRAFFIC_FILE = os.path.join(ROOT, "profiles", "qk_norm_rope_kernel_traffic.json")
-TILED_SOURCES = ["paged_gqa_decode_attn_gb300/csrc/pgqa_prefill_tc.cuh"]
+TILED_SOURCES = ["paged_gqa_decode_attn_gb300/csrc/pgqa_prefill_tc.cuh",
+                 "paged_gqa_decode_attn_gb300/csrc/pgqa_prefill.cuh"]
 TILED_TRAFFIC_FILE = os.path.join(ROOT, "profiles", "prefill_tc_kernel_traffic.json")
 
 
@@ -198,6 +199,8 @@ def build_case(name: str):
         return wl.prefill_page()
     if name == "prefill_long":
         return wl.prefill_long()
+    if name == "prefill_hd512":
+        return wl.prefill_hd512()
     if name == "prep_long":
         return wl.prep_long()
     if name == "multirow":
@@ -805,9 +808,10 @@ def run_prefill(args, case, rank, world, dist):
         "config": cfg, "run": run,
         "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak, "unit": "TFLOP/s",
                      "frac": round(achieved / peak, 4),
-                     "traffic": recorded_traffic(case.name, TILED_TRAFFIC_FILE, TILED_SOURCES) if case.hd <= 256
-                     else None, "peak_kind": peak_kind,
-                     "kernel": "prefill_tc_kernel (hd <= 256) / prefill_kernel (hd 512)", "launch_us": round(kernel_us, 3)},
+                     "traffic": recorded_traffic(case.name, TILED_TRAFFIC_FILE, TILED_SOURCES),
+                     "peak_kind": peak_kind,
+                     "kernel": "prefill_tc_kernel<%d>%s" % (case.hd, " (CTA pairs)" if case.hd > 256 else ""),
+                     "launch_us": round(kernel_us, 3)},
         "cpu_baseline": cpu,
         "e2e": {"value": round(e2e_value, 2), "unit": "TFLOP/s", "h2d_bytes_per_step": host_in.numel(),
                 "d2h_bytes_per_step": o_h.numel() * o_h.element_size(), "steps": e2e_steps,
@@ -1227,7 +1231,7 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="sliding",
                     choices=["sliding", "sliding_mapped", "tiny", "long", "batched", "prefill_page", "prefill_long",
-                             "prep_long", "sweep", "multirow"])
+                             "prefill_hd512", "prep_long", "sweep", "multirow"])
     ap.add_argument("--splits", type=int, default=0, help="override choose_splits")
     ap.add_argument("--merge", choices=["counters", "combine"], default="counters")
     ap.add_argument("--graph-chunk", type=int, default=2000)

@@ -243,8 +243,8 @@ int pgqa_attn_prefill(void *o, const void *q, const void *k_pool, const void *v_
  *   rows   the number of rows; every row must be in exactly one tile; with
  *          splits > 1, rows * nh <= INT_MAX (else PGQA_ERR_INVALID_ARGUMENT)
  *   splits 1..PGQA_MAX_SPLITS; 1 is pgqa_attn_prefill (part unused)
- * Other arguments as for pgqa_attn_prefill.  hd 64, 128 or 256 for splits > 1
- * (PGQA_ERR_UNSUPPORTED_HD otherwise).  Asynchronous on `stream`; two kernels.
+ * Other arguments as for pgqa_attn_prefill.  Asynchronous on `stream`; two
+ * kernels.
  */
 int pgqa_attn_prefill_split(void *o, void *part, const void *q, const void *k_pool, const void *v_pool,
                             const int32_t *block_table, const int32_t *off, const int32_t *qpos,
@@ -261,8 +261,8 @@ int pgqa_attn_prefill_split(void *o, void *part, const void *q, const void *k_po
  */
 int pgqa_prefill_split_count(int kv_len_eff, int rows, int ntiles, int nh, int nkv);
 
-/* The longest tile pgqa_attn_prefill takes at head dimension hd (64 rows;
- * 32 at hd 512), or PGQA_ERR_UNSUPPORTED_HD. */
+/* The longest tile pgqa_attn_prefill takes at head dimension hd (128 rows at
+ * every supported hd), or PGQA_ERR_UNSUPPORTED_HD. */
 int pgqa_prefill_rows_per_tile(int hd);
 
 /*

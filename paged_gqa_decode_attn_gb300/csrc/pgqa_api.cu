@@ -157,16 +157,22 @@ struct MapCacheEntry {
     const void *base = nullptr;
     int hd = 0;
     int want = -1;           // the view asked for
+    int box_chunks = 0;      // 64-dim chunks per box (the whole and halves views)
     int kind = 0;            // the view built
     CUtensorMap map;
 };
 MapCacheEntry g_map_cache[128];
 unsigned g_map_next = 0;
 
-int pool_map(const void *base, int hd, CUtensorMap *out, int *kind, int want = kMapWhole)
+// `box_chunks` (0: hd / 64) sets how many 64-dim chunks of a tile one box of
+// the whole or halves view takes: half of them serves one CTA of the hd-512
+// prefill's pairs.
+int pool_map(const void *base, int hd, CUtensorMap *out, int *kind, int want = kMapWhole, int box_chunks = 0)
 {
+    if (box_chunks <= 0)
+        box_chunks = hd / 64;
     for (auto &e : g_map_cache)
-        if (e.base == base && e.hd == hd && e.want == want) {
+        if (e.base == base && e.hd == hd && e.want == want && e.box_chunks == box_chunks) {
             *out = e.map;
             *kind = e.kind;
             return PGQA_OK;
@@ -179,7 +185,7 @@ int pool_map(const void *base, int hd, CUtensorMap *out, int *kind, int want = k
     if (w == kMapWhole) {
         const cuuint64_t dims[4] = {64u, 16u, static_cast<cuuint64_t>(hd / 64), 0x7fffffffull};
         const cuuint64_t strides[3] = {static_cast<cuuint64_t>(hd) * 2u, 128u, static_cast<cuuint64_t>(hd) * 32u};
-        const cuuint32_t box[4] = {64u, 16u, static_cast<cuuint32_t>(hd / 64), 1u};
+        const cuuint32_t box[4] = {64u, 16u, static_cast<cuuint32_t>(box_chunks), 1u};
         const cuuint32_t estride[4] = {1u, 1u, 1u, 1u};
         CUresult r = g_encode(&m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(base), dims, strides, box,
                               estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -190,7 +196,7 @@ int pool_map(const void *base, int hd, CUtensorMap *out, int *kind, int want = k
         const cuuint64_t dims[5] = {64u, 8u, static_cast<cuuint64_t>(hd / 64), 2u, 0x7fffffffull};
         const cuuint64_t strides[4] = {static_cast<cuuint64_t>(hd) * 2u, 128u, static_cast<cuuint64_t>(hd) * 16u,
                                        static_cast<cuuint64_t>(hd) * 32u};
-        const cuuint32_t box[5] = {64u, 8u, static_cast<cuuint32_t>(hd / 64), 2u, 1u};
+        const cuuint32_t box[5] = {64u, 8u, static_cast<cuuint32_t>(box_chunks), 2u, 1u};
         const cuuint32_t estride[5] = {1u, 1u, 1u, 1u, 1u};
         CUresult r = g_encode(&m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void *>(base), dims, strides, box,
                               estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -213,6 +219,7 @@ int pool_map(const void *base, int hd, CUtensorMap *out, int *kind, int want = k
     e.base = base;
     e.hd = hd;
     e.want = want;
+    e.box_chunks = box_chunks;
     e.kind = w;
     e.map = m;
     *out = m;
@@ -588,10 +595,10 @@ int pgqa_attn_decode(void *o, void *part, const void *q, const void *k_pool, con
 int pgqa_prefill_rows_per_tile(int hd)
 {
     switch (hd) {
-    case 64: return pgqa::PfCfg<64>::kRowsPerTile;
-    case 128: return pgqa::PfCfg<128>::kRowsPerTile;
-    case 256: return pgqa::PfCfg<256>::kRowsPerTile;
-    case 512: return pgqa::PfCfg<512>::kRowsPerTile;
+    case 64:
+    case 128:
+    case 256:
+    case 512: return pgqa::kPrefillRowsPerTile;
     default: return PGQA_ERR_UNSUPPORTED_HD;
     }
 }
@@ -639,7 +646,7 @@ int prefill_call(void *o, void *part, const void *q, const void *k_pool, const v
     if (splits > PGQA_MAX_SPLITS)
         return PGQA_ERR_TOO_MANY_SPLITS;
     const int hi = hd_index(hd);
-    if (hi < 0 || (splits > 1 && hd > 256))
+    if (hi < 0)
         return PGQA_ERR_UNSUPPORTED_HD;
     if (ntiles == 0)
         return PGQA_OK;
@@ -651,7 +658,7 @@ int prefill_call(void *o, void *part, const void *q, const void *k_pool, const v
         return PGQA_ERR_MISALIGNED;
     const int g = nh / nkv;
     const int rpt = pgqa_prefill_rows_per_tile(hd);
-    const int qr = hd == 512 ? pgqa::PfGeo<512>::kQueryRows : 128;     // query rows per CTA
+    const int qr = 128;     // query rows per CTA (pair, at hd 512)
     if (nkv > 65535 || (static_cast<long long>(rpt) * g + qr - 1) / qr > 65535)
         return PGQA_ERR_INVALID_ARGUMENT;
     if (!aligned(k_pool, 16) || !aligned(v_pool, 16) || !aligned(q, 16) || !aligned(o, 16))
@@ -689,16 +696,13 @@ int prefill_call(void *o, void *part, const void *q, const void *k_pool, const v
         return st;
     CUtensorMap tk, tv;
     int kind_k = 0, kind_v = 0;
-    // The tcgen05 kernel (hd <= 256) copies K by one box per tile in the
-    // halves view (64-dim boxes where the driver refuses it) and V by
-    // whole-tile boxes where the driver takes them; the hd-512 kernel takes
-    // whole-tile boxes for both where it can.
-    const bool tc = hd <= 256;
-    if ((st = pool_map(k_pool, hd, &tk, &kind_k, tc ? kMapHalves : kMapWhole)) != PGQA_OK ||
-        (st = pool_map(v_pool, hd, &tv, &kind_v)) != PGQA_OK)
+    // The tcgen05 kernel copies K by one box per tile in the halves view and
+    // V by one whole-tile box, each of this CTA's dims (all of them, or half at
+    // hd 512), or by 64-dim boxes where the driver refuses those views.
+    const int box_chunks = hd > 256 ? hd / 128 : hd / 64;
+    if ((st = pool_map(k_pool, hd, &tk, &kind_k, kMapHalves, box_chunks)) != PGQA_OK ||
+        (st = pool_map(v_pool, hd, &tv, &kind_v, kMapWhole, box_chunks)) != PGQA_OK)
         return st;
-    if (!tc && kind_k != kind_v)
-        return PGQA_ERR_TENSOR_MAP;
     p.whole_tile_box = kind_v == kMapWhole;
     p.k_halves = kind_k == kMapHalves;
     p.err = s->err;
@@ -730,7 +734,8 @@ int prefill_call(void *o, void *part, const void *q, const void *k_pool, const v
         switch (hd) {
         case 64: e = pgqa::launch_combine_hd64(c, a.stream); break;
         case 128: e = pgqa::launch_combine_hd128(c, a.stream); break;
-        default: e = pgqa::launch_combine_hd256(c, a.stream); break;
+        case 256: e = pgqa::launch_combine_hd256(c, a.stream); break;
+        default: e = pgqa::launch_combine_hd512(c, a.stream); break;
         }
         if (e != cudaSuccess)
             return PGQA_ERR_CUDA;

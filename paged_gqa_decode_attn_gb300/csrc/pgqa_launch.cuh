@@ -111,6 +111,7 @@ int cluster_capacity(int cluster)
 cudaError_t launch_combine_hd64(const DecodeParams &p, cudaStream_t stream);
 cudaError_t launch_combine_hd128(const DecodeParams &p, cudaStream_t stream);
 cudaError_t launch_combine_hd256(const DecodeParams &p, cudaStream_t stream);
+cudaError_t launch_combine_hd512(const DecodeParams &p, cudaStream_t stream);
 int cluster_capacity_hd64(int cluster);
 int cluster_capacity_hd128(int cluster);
 int cluster_capacity_hd256(int cluster);

@@ -1,8 +1,7 @@
 // Paged causal prefill on the 5th-generation tensor cores (tcgen05) of GB300,
-// for head dims 64, 128 and 256.  Same result as pgqa_prefill.cuh's kernel
-// (the page's `attn::attn_prefill`: every tile row attends like a decode row
-// at its position), computed as a flash-attention loop with the accumulators
-// in tensor memory:
+// for head dims 64, 128, 256 and 512 (the page's `attn::attn_prefill`: every
+// tile row attends like a decode row at its position), computed as a
+// flash-attention loop with the accumulators in tensor memory:
 //
 //   * one CTA serves 128 query rows (row, head) of one tile and kv head --
 //     the M = 128 of every MMA -- with heads fastest; their Q sits in tensor
@@ -21,6 +20,11 @@
 //     each) and warp 19 O += P_j V_j (TMEM, hd columns, one MMA per page),
 //     each batch committed to mbarriers;
 //   * warp 18 computes the work items ahead and publishes them;
+//   * at hd 512, where O of 128 rows would fill all of tensor memory, a pair
+//     of CTAs (a cluster of two) serves each item, each CTA over half of the
+//     head dims of Q, K, V and O: both compute their half of S_j, swap the
+//     halves through distributed shared memory (st.async, one mbarrier per
+//     buffer) and add them, so both run the same softmax on the same S_j;
 //   * warps 0-15 run the softmax, four threads per query row (warps w, w+4,
 //     w+8, w+12 share TMEM lanes 32(w%4)..: lane = row), each over a quarter
 //     of the block's columns: they read S_j from TMEM, mask it to the row's
@@ -169,24 +173,35 @@ __device__ __forceinline__ void l2_prefetch_box_4d(const CUtensorMap *map, int x
                  : "memory");
 }
 
-__device__ __forceinline__ void l2_prefetch_box_5d(const CUtensorMap *map, int t)
+__device__ __forceinline__ void l2_prefetch_box_5d(const CUtensorMap *map, int c, int t)
 {
-    asm volatile("cp.async.bulk.prefetch.tensor.5d.L2.global.tile [%0, {%1, %1, %1, %1, %2}];" ::"l"(
+    asm volatile("cp.async.bulk.prefetch.tensor.5d.L2.global.tile [%0, {%1, %1, %2, %1, %3}];" ::"l"(
                      reinterpret_cast<uint64_t>(map)),
-                 "r"(0), "r"(t)
+                 "r"(0), "r"(c), "r"(t)
                  : "memory");
 }
 
-// One TMA box of a 5-D tensor map at (0, 0, 0, 0, t): a whole (page, kv head)
-// tile in the halves view.
-__device__ __forceinline__ void tma_load_5d_tile(uint32_t dst, const CUtensorMap *map, uint32_t bar, int t)
+// One TMA box of a 5-D tensor map at (0, 0, c, 0, t): the (page, kv head)
+// tile t in the halves view, from 64-dim chunk c on (the box's chunk count).
+__device__ __forceinline__ void tma_load_5d_tile(uint32_t dst, const CUtensorMap *map, uint32_t bar, int c, int t)
 {
     asm volatile(
         "cp.async.bulk.tensor.5d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-        " [%0], [%1, {%3, %3, %3, %3, %4}], [%2];" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(0), "r"(t)
+        " [%0], [%1, {%3, %3, %4, %3, %5}], [%2];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(0), "r"(c), "r"(t)
         : "memory");
 }
+
+// A CTA pair: this CTA's rank in its cluster, and the cluster barrier's
+// arrive with release semantics.
+__device__ __forceinline__ int cluster_ctarank()
+{
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return static_cast<int>(r);
+}
+
+__device__ __forceinline__ void cluster_arrive_release() { asm volatile("barrier.cluster.arrive.release;" ::: "memory"); }
 
 // Non-blocking test of an mbarrier phase (try_wait may suspend the thread for
 // a while before it answers, which would hold up a poller watching two barriers).
@@ -216,16 +231,22 @@ __device__ __forceinline__ void st_global_32B(void *dst, const uint32_t (&w)[8])
 
 template <int HD>
 struct TcGeo {
+    // hd 512: O of 128 rows would fill all of tensor memory, so a pair of CTAs
+    // (a cluster of two) serves each item, each CTA over half of the head
+    // dims, and they add their halves of S through distributed shared memory
+    static constexpr bool kSplitDims = HD > 256;
+    static constexpr int kHdc = kSplitDims ? HD / 2 : HD;     // head dims per CTA
     static constexpr int kRows = 128;                  // query rows per CTA (MMA M)
     static constexpr int kBlockPages = 4;
     static constexpr int kBlockTokens = kBlockPages * kPage;   // 64: S columns per block
-    static constexpr int kChunks = HD / 64;            // 128-byte swizzle rows per head vector
+    static constexpr int kChunks = kHdc / 64;          // 128-byte swizzle rows per head vector (this CTA's dims)
     static constexpr int kPBytes = kRows * 128;                // [128 rows][128 B: 64 tokens]
     static constexpr int kKBytes = kChunks * kBlockTokens * 128;           // [chunk][64 tokens][128 B]
     static constexpr int kVPage = kChunks * kPage * 128;                   // [chunk][16 tokens][128 B]
     static constexpr int kVBytes = kBlockPages * kVPage;
     static constexpr int kStageBytes = kKBytes + kVBytes;
-    static constexpr int kStages = (192 * 1024) / kStageBytes;     // 192 KB of K/V in flight
+    // 192 KB of K/V in flight; 128 KB beside the S exchange buffers of a pair
+    static constexpr int kStages = ((kSplitDims ? 128 : 192) * 1024) / kStageBytes;
     static constexpr int kPOff = 0;
     static constexpr int kStageOff = kPOff + kPBytes;
     static constexpr int kSoftmaxWarps = 16;           // four threads per query row
@@ -235,10 +256,14 @@ struct TcGeo {
     static constexpr int kInfoOff = kXOff + (2 * kParts * kRows + kParts * kRows) * 4;
     static constexpr int kInfoBytes = 2 * 64;          // two slots of kItemSlot bytes
     static constexpr int kWinOff = kInfoOff + kInfoBytes;
-    static constexpr int kBarOff = kWinOff + 2 * kRows * 8;
+    // split dims: the peer's half of S_j, [2 buffers][parts][4][kRows] float4
+    // (a thread's 16 columns as 4 float4, rows adjacent)
+    static constexpr int kSxOff = kWinOff + 2 * kRows * 8;
+    static constexpr int kSxBytes = kSplitDims ? 2 * kRows * kBlockTokens * 4 : 0;
+    static constexpr int kBarOff = kSxOff + kSxBytes;
     // k_full[stages], k_empty[stages], v_full[stages], v_empty[stages], s_full[2], s_free[2],
-    // p_full, o_done, q_ready, o_free, info_full[2], info_empty[2]
-    static constexpr int kBars = 4 * kStages + 12;
+    // p_full, o_done, q_ready, o_free, info_full[2], info_empty[2], then (split dims) x_full[2]
+    static constexpr int kBars = 4 * kStages + 12 + (kSplitDims ? 2 : 0);
     static constexpr int kSlotOff = kBarOff + kBars * 8;
     static constexpr int kTotal = kSlotOff + 16;
     static constexpr int kAlloc = kTotal + 1024;
@@ -247,10 +272,10 @@ struct TcGeo {
     static constexpr int kSchedWarp = kSoftmaxWarps + 2;
     static constexpr int kPvWarp = kSoftmaxWarps + 3;
     static constexpr int kThreads = (kSoftmaxWarps + 4) * 32;   // + producer, S issuer, scheduler, PV issuer
-    static constexpr int kTmemCols = HD == 64 ? 256 : 512;   // S0, S1, O (hd), Q (hd / 2)
+    static constexpr int kTmemCols = kHdc == 64 ? 256 : 512;   // S0, S1, O (dims), Q (dims / 2)
     static constexpr int kOCol = 2 * kBlockTokens;
-    static constexpr int kQCol = kOCol + HD;
-    static_assert(kQCol + HD / 2 <= kTmemCols, "tensor memory");
+    static constexpr int kQCol = kOCol + kHdc;
+    static_assert(kQCol + kHdc / 2 <= kTmemCols, "tensor memory");
     static_assert(kAlloc <= 227 * 1024, "shared memory");
     static_assert(kPBytes % 1024 == 0 && kStageBytes % 1024 == 0, "swizzle atoms");
 };
@@ -344,7 +369,7 @@ __device__ __forceinline__ TcItem tc_item_rows(const PrefillParams &p, int it, i
 // kPrefetchPages pages.
 template <int HD>
 __device__ __forceinline__ void tc_prefetch_item(const PrefillParams &p, const TcItem &I, const CUtensorMap *tm_k,
-                                                 const CUtensorMap *tm_v, int lane)
+                                                 const CUtensorMap *tm_v, int dofs, int lane)
 {
     using G = TcGeo<HD>;
     constexpr int kPrefetchPages = 2 * G::kBlockPages;
@@ -362,18 +387,18 @@ __device__ __forceinline__ void tc_prefetch_item(const PrefillParams &p, const T
             phys = __ldg(p.page_map + phys);
         const int t = phys * p.nkv + I.kh;
         if (p.k_halves) {
-            l2_prefetch_box_5d(tm_k, t);
+            l2_prefetch_box_5d(tm_k, dofs / kBoxElems, t);
         } else {
 #pragma unroll
             for (int c = 0; c < G::kChunks; ++c)
-                l2_prefetch_box_3d(tm_k, c * kBoxElems, 0, t);
+                l2_prefetch_box_3d(tm_k, dofs + c * kBoxElems, 0, t);
         }
         if (p.whole_tile_box) {
-            l2_prefetch_box_4d(tm_v, 0, 0, 0, t);
+            l2_prefetch_box_4d(tm_v, 0, 0, dofs / kBoxElems, t);
         } else {
 #pragma unroll
             for (int c = 0; c < G::kChunks; ++c)
-                l2_prefetch_box_3d(tm_v, c * kBoxElems, 0, t);
+                l2_prefetch_box_3d(tm_v, dofs + c * kBoxElems, 0, t);
         }
     }
 }
@@ -392,6 +417,8 @@ __global__ void __launch_bounds__(TcGeo<HD>::kThreads, 1)
     using G = TcGeo<HD>;
     constexpr int NST = G::kStages;
     constexpr int NCH = G::kChunks;
+    constexpr int HDC = G::kHdc;                       // head dims of this CTA
+    constexpr bool kSplit = G::kSplitDims;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t s_base = smem_u32(smem);
@@ -411,15 +438,19 @@ __global__ void __launch_bounds__(TcGeo<HD>::kThreads, 1)
     const uint32_t b_ofree = b_qready + 8;
     const uint32_t b_ifull = b_ofree + 8;              // [2] a published item is in its slot
     const uint32_t b_iempty = b_ifull + 16;            // [2] every role has read it
+    const uint32_t b_xfull = b_iempty + 16;            // [2] split dims: the peer's half of S_j is here
     const int2 *win = reinterpret_cast<const int2 *>(smem + G::kWinOff);
     uint32_t *tslot = reinterpret_cast<uint32_t *>(smem + G::kSlotOff);
 
     const int tid = threadIdx.x;
     const int warp = tid >> 5;
     const int lane = tid & 31;
+    // split dims: the pair is one scheduling unit; rank r takes dims [r HDC, (r + 1) HDC)
+    const int crank = kSplit ? cluster_ctarank() : 0;
+    const int dofs = crank * HDC;
     const int nitems = ntiles * p.nkv * nchunks * p.splits;
-    const int ncta = gridDim.x;
-    const int cta = blockIdx.x;
+    const int ncta = kSplit ? gridDim.x / 2 : gridDim.x;
+    const int cta = kSplit ? blockIdx.x / 2 : blockIdx.x;
     auto first_item = [&](int) { return cta < nitems ? cta : nitems; };
     // the item after `it` (round k = it / ncta) for this CTA, or nitems
     auto next_item = [&](int it) {
@@ -450,8 +481,19 @@ __global__ void __launch_bounds__(TcGeo<HD>::kThreads, 1)
             mbar_init(b_ifull + 8 * b, 1);
             mbar_init(b_iempty + 8 * b, G::kSoftmaxWarps + 3);   // softmax warps, producer, S and PV issuers
         }
+        if (kSplit) {
+            // each phase: the peer's 128 x 64 f32 half of one S block; the next
+            // phase is armed by thread 0 as soon as it has seen this one
+            for (int b = 0; b < 2; ++b) {
+                mbar_init(b_xfull + 8 * b, 1);
+                mbar_arrive_expect_tx(b_xfull + 8 * b, G::kRows * G::kBlockTokens * 4);
+            }
+        }
         mbar_init_fence();
     }
+    // split dims: the peer's barriers are set up before anything is sent to them
+    if (kSplit)
+        cluster_arrive_relaxed();
     grid_dependency_wait();
     grid_launch_dependents();
     if (warp == 0)
@@ -459,6 +501,8 @@ __global__ void __launch_bounds__(TcGeo<HD>::kThreads, 1)
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    if (kSplit)
+        cluster_wait();
     const uint32_t tbase = *tslot;
     // The k-th item of this CTA, published by the scheduler in slot k % 2;
     // the reading warp takes a copy and frees the slot (one arrival per warp).
@@ -496,7 +540,7 @@ __global__ void __launch_bounds__(TcGeo<HD>::kThreads, 1)
             __syncwarp();
             if (lane == 0)
                 mbar_arrive(b_ifull + 8 * sl);
-            tc_prefetch_item<HD>(p, I, &tm_k, &tm_v, lane);
+            tc_prefetch_item<HD>(p, I, &tm_k, &tm_v, dofs, lane);
         }
     } else if (warp == G::kProducerWarp) {
         // ------------------------------------------------ producer: blocks of 4 pages
@@ -526,7 +570,7 @@ __global__ void __launch_bounds__(TcGeo<HD>::kThreads, 1)
                     const int st = jg % NST;
                     const uint32_t sK = s_base + G::kStageOff + st * G::kStageBytes;
                     const uint32_t sV = sK + G::kKBytes;
-                    const uint32_t half_tx = np * kPage * HD * 2;
+                    const uint32_t half_tx = np * kPage * HDC * 2;
                     // K of block jg, once S of block jg - NST is done
                     if (lane == 0 && ok && jg >= NST)
                         ok = mbar_wait_bounded(b_kempty + 8 * st, ((jg / NST) - 1) & 1, p.err, kErrTimeoutEmpty);
@@ -538,12 +582,12 @@ __global__ void __launch_bounds__(TcGeo<HD>::kThreads, 1)
                         if (ok && lane == 0 && pp < np) {
                             const int t = ph * p.nkv + I.kh;
                             if (p.k_halves) {      // one box: [half][chunk][8 slots][128 B] per page
-                                tma_load_5d_tile(sK + pp * G::kVPage, &tm_k, b_kfull + 8 * st, t);
+                                tma_load_5d_tile(sK + pp * G::kVPage, &tm_k, b_kfull + 8 * st, dofs / kBoxElems, t);
                             } else {               // [chunk][64 tokens][128 B]
 #pragma unroll
                                 for (int c = 0; c < NCH; ++c)
                                     tma_load_3d(sK + c * (G::kBlockTokens * 128) + pp * (kPage * 128), &tm_k,
-                                                b_kfull + 8 * st, c * kBoxElems, 0, t);
+                                                b_kfull + 8 * st, dofs + c * kBoxElems, 0, t);
                             }
                         }
                     }
@@ -558,12 +602,12 @@ __global__ void __launch_bounds__(TcGeo<HD>::kThreads, 1)
                         if (ok && lane == 0 && pp < np) {
                             const int t = ph * p.nkv + I.kh;
                             if (p.whole_tile_box) {
-                                tma_load_4d(sV + pp * G::kVPage, &tm_v, b_vfull + 8 * st, 0, 0, 0, t);
+                                tma_load_4d(sV + pp * G::kVPage, &tm_v, b_vfull + 8 * st, 0, 0, dofs / kBoxElems, t);
                             } else {
 #pragma unroll
                                 for (int c = 0; c < NCH; ++c)
                                     tma_load_3d(sV + pp * G::kVPage + c * (kPage * 128), &tm_v, b_vfull + 8 * st,
-                                                c * kBoxElems, 0, t);
+                                                dofs + c * kBoxElems, 0, t);
                             }
                         }
                     }
@@ -607,7 +651,7 @@ __global__ void __launch_bounds__(TcGeo<HD>::kThreads, 1)
                     if (ok) {
                         const uint32_t sK = s_base + G::kStageOff + st * G::kStageBytes;
 #pragma unroll
-                        for (int ks = 0; ks < HD / 16; ++ks) {
+                        for (int ks = 0; ks < HDC / 16; ++ks) {
                             const int c = ks >> 2, kk = ks & 3;
                             umma_bf16_tmem_a(tbase + b * G::kBlockTokens, tbase + G::kQCol + ks * 8,
                                              umma_sdesc(sK + c * k_chunk + kk * 32, 16, k_sbo), kIdS, ks > 0);
@@ -623,7 +667,7 @@ __global__ void __launch_bounds__(TcGeo<HD>::kThreads, 1)
         }
     } else if (warp == G::kPvWarp) {
         // ------------------------------------------------ PV issuer (one thread)
-        constexpr uint32_t kIdO = umma_idesc_bf16(128, HD, 0, 1);
+        constexpr uint32_t kIdO = umma_idesc_bf16(128, HDC, 0, 1);
         bool ok = true;
         int jg = 0, kq = 0;
         int kit = 0;
@@ -663,7 +707,7 @@ __global__ void __launch_bounds__(TcGeo<HD>::kThreads, 1)
         // ------------------------------------------------ softmax warps: kParts threads per query row
         constexpr int NP = G::kParts;
         constexpr int HC = G::kBlockTokens / NP;           // columns of S per thread
-        constexpr int HO = HD / NP;                        // columns of O per thread
+        constexpr int HO = HDC / NP;                       // columns of O per thread
         constexpr int kRs = HO >= 32 ? 32 : 16;            // O columns per rescale step
         const int row = (warp & 3) * 32 + lane;            // query row of the item; TMEM lane
         const int part = warp >> 2;                        // column part
@@ -689,7 +733,7 @@ __global__ void __launch_bounds__(TcGeo<HD>::kThreads, 1)
             tc_fence_after();
             const bool split_out = p.splits > 1;
             const size_t prow = frh * p.splits + fsplit;
-            if (split_out && fva && part == 0)
+            if (split_out && fva && part == 0 && crank == 0)     // a pair's two (m, L) are equal
                 p.part_ml[prow] = make_float2(fm, lt);
             // one division per row, then a multiply per element (64 IEEE
             // divisions per thread took about 4 us per item)
@@ -711,7 +755,7 @@ __global__ void __launch_bounds__(TcGeo<HD>::kThreads, 1)
                 const int c0 = c1 + 16 * h;
                 const uint32_t (&r)[16] = rr[h];
                 if (fva && split_out) {
-                    float *dst = p.part_o + prow * HD + c0;
+                    float *dst = p.part_o + prow * HD + dofs + c0;
                     if (part_sector_aligned) {          // two whole sectors
                         const uint32_t (&lo)[8] = *reinterpret_cast<const uint32_t (*)[8]>(&r[0]);
                         const uint32_t (&hi)[8] = *reinterpret_cast<const uint32_t (*)[8]>(&r[8]);
@@ -736,7 +780,7 @@ __global__ void __launch_bounds__(TcGeo<HD>::kThreads, 1)
                     // one whole sector per lane where o allows it: the 32 lanes
                     // write 32 rows, so two 16-byte halves would each cost a
                     // partial-sector write
-                    __nv_bfloat16 *dst = p.o + frh * HD + c0;
+                    __nv_bfloat16 *dst = p.o + frh * HD + dofs + c0;
                     if (o_sector_aligned) {
                         st_global_32B(dst, w);
                     } else {
@@ -781,13 +825,14 @@ __global__ void __launch_bounds__(TcGeo<HD>::kThreads, 1)
             if (I.nblocks == 0) {           // no position visible to any row: zeros, or an empty partial
                 if (va && p.splits > 1) {
                     const size_t prow = rh * p.splits + I.split;
-                    if (part == 0)
+                    if (part == 0 && crank == 0)
                         p.part_ml[prow] = make_float2(-INFINITY, 0.f);
                     for (int c0 = part * HO; c0 < (part + 1) * HO; c0 += 4)
-                        *reinterpret_cast<float4 *>(p.part_o + prow * HD + c0) = make_float4(0.f, 0.f, 0.f, 0.f);
+                        *reinterpret_cast<float4 *>(p.part_o + prow * HD + dofs + c0) =
+                            make_float4(0.f, 0.f, 0.f, 0.f);
                 } else if (va) {
                     for (int c0 = part * HO; c0 < (part + 1) * HO; c0 += 8)
-                        *reinterpret_cast<uint4 *>(p.o + rh * HD + c0) = make_uint4(0u, 0u, 0u, 0u);
+                        *reinterpret_cast<uint4 *>(p.o + rh * HD + dofs + c0) = make_uint4(0u, 0u, 0u, 0u);
                 }
                 continue;
             }
@@ -796,8 +841,8 @@ __global__ void __launch_bounds__(TcGeo<HD>::kThreads, 1)
             // item's S MMAs, the only readers of Q, are all complete
             {
                 // every load of this thread's part goes out before the first store
-                constexpr int kQIt = (HD / 2 + 16 * NP - 1) / (16 * NP);   // 16-column pieces per thread
-                const uint4 *src = reinterpret_cast<const uint4 *>(p.q + rh * HD);
+                constexpr int kQIt = (HDC / 2 + 16 * NP - 1) / (16 * NP);   // 16-column pieces per thread
+                const uint4 *src = reinterpret_cast<const uint4 *>(p.q + rh * HD + dofs);
                 const uint32_t tq = trow + G::kQCol;
                 uint4 qv[kQIt][4];
 #pragma unroll
@@ -805,12 +850,12 @@ __global__ void __launch_bounds__(TcGeo<HD>::kThreads, 1)
                     const int c0 = part * 16 + i * 16 * NP;
 #pragma unroll
                     for (int k = 0; k < 4; ++k)
-                        qv[i][k] = va && c0 < HD / 2 ? __ldg(src + c0 / 4 + k) : make_uint4(0u, 0u, 0u, 0u);
+                        qv[i][k] = va && c0 < HDC / 2 ? __ldg(src + c0 / 4 + k) : make_uint4(0u, 0u, 0u, 0u);
                 }
 #pragma unroll
                 for (int i = 0; i < kQIt; ++i) {
                     const int c0 = part * 16 + i * 16 * NP;
-                    if (c0 < HD / 2) {
+                    if (c0 < HDC / 2) {
                         uint32_t r[16];
 #pragma unroll
                         for (int k = 0; k < 4; ++k) {
@@ -848,6 +893,36 @@ __global__ void __launch_bounds__(TcGeo<HD>::kThreads, 1)
                 __syncwarp();
                 if (lane == 0)
                     mbar_arrive(b_sfree + 8 * b);
+                if constexpr (kSplit) {
+                    // The pair's halves of S_j: this thread's 16 columns go to the
+                    // peer, the peer's come here, and the two are added.  a + b is
+                    // b + a bit for bit, so both CTAs hold the same S_j and run the
+                    // same softmax.  The peer writes buffer b again (block jj + 2)
+                    // only after it has every thread's half of block jj + 1 from
+                    // here, which each thread sends after reading block jj's.
+                    static_assert(HC == 16, "exchange layout: four float4 per thread");
+                    const uint32_t xoff = G::kSxOff + static_cast<uint32_t>(((b * NP + part) * 4 * G::kRows + row) * 16);
+                    const int peer = crank ^ 1;
+                    const uint32_t rbar = map_to_cta(b_xfull + 8 * b, peer);
+#pragma unroll
+                    for (int k = 0; k < 4; ++k)
+                        st_async_f32x4(map_to_cta(s_base + xoff + k * G::kRows * 16, peer),
+                                       make_float4(__uint_as_float(sr[4 * k]), __uint_as_float(sr[4 * k + 1]),
+                                                   __uint_as_float(sr[4 * k + 2]), __uint_as_float(sr[4 * k + 3])),
+                                       rbar);
+                    if (ok)
+                        ok = mbar_wait_bounded(b_xfull + 8 * b, (jj >> 1) & 1, p.err, kErrTimeoutFull);
+                    if (tid == 0 && ok)    // arm the buffer's next phase (block jj + 2)
+                        mbar_arrive_expect_tx(b_xfull + 8 * b, G::kRows * G::kBlockTokens * 4);
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        const float4 v = *reinterpret_cast<const float4 *>(smem + xoff + k * G::kRows * 16);
+                        sr[4 * k] = __float_as_uint(__uint_as_float(sr[4 * k]) + v.x);
+                        sr[4 * k + 1] = __float_as_uint(__uint_as_float(sr[4 * k + 1]) + v.y);
+                        sr[4 * k + 2] = __float_as_uint(__uint_as_float(sr[4 * k + 2]) + v.z);
+                        sr[4 * k + 3] = __float_as_uint(__uint_as_float(sr[4 * k + 3]) + v.w);
+                    }
+                }
 
                 const int tok0 = (I.p_first + j * G::kBlockPages) * kPage + part * HC;
                 // mask to the row's window; this part's max in four chains, then the row's
@@ -964,6 +1039,12 @@ __global__ void __launch_bounds__(TcGeo<HD>::kThreads, 1)
         if (pend)
             finish(pend_jg, pend_rh, pend_va, pend_l, pend_m, pend_split);
     }
+    // split dims: neither CTA of the pair leaves while the other may still
+    // write into its shared memory
+    if (kSplit) {
+        cluster_arrive_release();
+        cluster_wait();
+    }
     tc_fence_before();
     __syncthreads();
     if (warp == 0) {
@@ -972,34 +1053,83 @@ __global__ void __launch_bounds__(TcGeo<HD>::kThreads, 1)
     }
 }
 
+// Clusters of two CTAs of the split-dims kernel that can be resident at once
+// on the current device (0: none), asked once per device after the kernel's
+// shared-memory attribute is set.
+template <int HD>
+int prefill_tc_pair_capacity()
+{
+    static int cap[64];
+    static bool known[64];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)
+        return 0;
+    if (known[dev])
+        return cap[dev];
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2);
+    cfg.blockDim = dim3(TcGeo<HD>::kThreads);
+    cfg.dynamicSmemBytes = TcGeo<HD>::kAlloc;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, prefill_tc_kernel<HD>, &cfg) != cudaSuccess) {
+        cudaGetLastError();
+        n = 0;
+    }
+    cap[dev] = n;
+    known[dev] = true;
+    return n;
+}
+
 template <int HD>
 cudaError_t launch_prefill_tc(const PrefillLaunchArgs &a, bool set_attr)
 {
+    using G = TcGeo<HD>;
     if (set_attr) {
         cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             TcGeo<HD>::kAlloc);
+                                             G::kAlloc);
         if (e != cudaSuccess)
             return e;
     }
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cudaLaunchConfig_t cfg = {};
     const int tile_rows = a.max_tile_rows > 0 ? std::min(a.max_tile_rows, a.p.rows_per_tile) : a.p.rows_per_tile;
-    const int nchunks = (tile_rows * a.p.g + TcGeo<HD>::kRows - 1) / TcGeo<HD>::kRows;
+    const int nchunks = (tile_rows * a.p.g + G::kRows - 1) / G::kRows;
     const long long items = static_cast<long long>(a.ntiles) * a.p.nkv * nchunks * a.p.splits;
     if (items > INT_MAX)
         return cudaErrorInvalidValue;
-    // one CTA per item while they fit in about two waves (the hardware then
-    // hands the second wave to the first SMs free); persistent, one CTA per
-    // SM, beyond that
-    const int sms = a.num_sms > 0 ? a.num_sms : 1;
-    cfg.gridDim = dim3(static_cast<unsigned>(items <= 2ll * sms ? items : sms));
-    cfg.blockDim = dim3(TcGeo<HD>::kThreads);
-    cfg.dynamicSmemBytes = TcGeo<HD>::kAlloc;
+    // one unit (a CTA, or at hd 512 a pair) per item while they fit in about
+    // two waves (the hardware then hands the second wave to the first units
+    // free); persistent, as many units as are resident at once, beyond that
+    long long resident = a.num_sms > 0 ? a.num_sms : 1;
+    if (G::kSplitDims) {
+        resident = prefill_tc_pair_capacity<HD>();
+        if (resident < 1)
+            return cudaErrorInvalidConfiguration;
+    }
+    const long long units = items <= 2 * resident ? items : resident;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    int na = 1;
+    if (G::kSplitDims) {
+        attr[1].id = cudaLaunchAttributeClusterDimension;
+        attr[1].val.clusterDim.x = 2;
+        attr[1].val.clusterDim.y = 1;
+        attr[1].val.clusterDim.z = 1;
+        na = 2;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(G::kSplitDims ? 2 * units : units));
+    cfg.blockDim = dim3(G::kThreads);
+    cfg.dynamicSmemBytes = G::kAlloc;
     cfg.stream = a.stream;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = na;
     return cudaLaunchKernelEx(&cfg, prefill_tc_kernel<HD>, *a.tm_k, *a.tm_v, a.p, a.ntiles, nchunks);
 }
 

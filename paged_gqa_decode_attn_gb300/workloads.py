@@ -374,6 +374,11 @@ def prefill_long() -> Case:
     return prefill_case(16, 8, 256, 1024, 8192, dist="sym", name="prefill_nh16_nkv8_hd256_w1024_ctx8192")
 
 
+def prefill_hd512() -> Case:
+    """A measured prefill in the page's second case shape: nh16 nkv2 hd512, full causal, 4096 rows."""
+    return prefill_case(16, 2, 512, 0, 4096, dist="sym", name="prefill_nh16_nkv2_hd512_w0_ctx4096")
+
+
 @dataclasses.dataclass
 class PrepCase:
     """One QK-RMSNorm / RoPE / paged K-V write problem (bf16 bits, int32 metadata).

@@ -218,7 +218,7 @@ def test_python_binding_raises_on_error(lib):
 # ---------------------------------------------------------------- prefill host side
 
 def test_prefill_rows_per_tile(lib):
-    assert [pgqa.prefill_rows_per_tile(h) for h in (64, 128, 256, 512)] == [128, 128, 128, 32]
+    assert [pgqa.prefill_rows_per_tile(h) for h in (64, 128, 256, 512)] == [128, 128, 128, 128]
     assert lib.pgqa_prefill_rows_per_tile(96) == -2
 
 
@@ -275,11 +275,11 @@ def split_call(lib, splits=2, rows=4, hd=128, part=FAKE, ntiles=1, nh=8, nkv=2):
 
 
 @pytest.mark.parametrize("kw,code", [
-    ({"splits": 0}, -1), ({"splits": 257}, -7), ({"hd": 512}, -2), ({"hd": 96}, -2), ({"part": None}, -1),
+    ({"splits": 0}, -1), ({"splits": 257}, -7), ({"hd": 32}, -2), ({"hd": 96}, -2), ({"part": None}, -1),
     ({"rows": 0}, -1), ({"part": FAKE + 4}, -3), ({"nh": 6, "nkv": 4}, -1),
     ({"rows": 65535, "nh": 65536, "nkv": 8192}, -1)])
 def test_prefill_split_bad_arguments_are_rejected_before_any_cuda_call(lib, kw, code):
-    """splits 1..256; hd 512 has no split path; scratch and a row count with splits > 1; 16-byte alignment."""
+    """splits 1..256; head dims 64..512 only; scratch and a row count with splits > 1; 16-byte alignment."""
     assert split_call(lib, **kw) == code
 
 

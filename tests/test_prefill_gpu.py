@@ -5,8 +5,8 @@ The gates follow the prefill part of `run` in span-02
 ``make_tiles`` with ``prefill_rows_per_tile``, is within rel-RMS 1e-2 of the
 reference, and the permuted pool behind a page map (and the map folded into
 the block table) gives the same bits.  Every element is also held to the
-arithmetic bound of ``parity.py`` (c = 2^-6 on the tcgen05 kernels, which let P
-grow to 2^8 before rescaling).  A prefill row is a decode row at the
+arithmetic bound of ``parity.py`` (c = 2^-6: the tcgen05 kernel, at every head
+dim, lets P grow to 2^8 before rescaling).  A prefill row is a decode row at the
 same position, so the oracle is the decode oracle over all rows.
 """
 import dataclasses
@@ -38,7 +38,7 @@ def prefill_gates(case, mapped=True, seq=None):
     from gpu_util import PrefillDev, check_parity, first_difference
     d = PrefillDev(case, seq)
     a = d.result()
-    check_parity(case, a, case.name, tiled=case.hd <= 256)
+    check_parity(case, a, case.name, tiled=True)
     if mapped:
         for fold in (False, True):
             m = wl.with_mapped_pool(case, fold_into_table=fold)
@@ -57,7 +57,8 @@ def test_page_prefill_cases(args):
 @pytest.mark.parametrize("hd", [64, 128, 256, 512])
 @pytest.mark.parametrize("nh,nkv", [(4, 4), (8, 1), (32, 2), (24, 2), (6, 2)])
 def test_head_dims_and_group_sizes(hd, nh, nkv):
-    """g = 1, 8, 16, 12 and 3: chunks of 128 (32 at hd 512) query rows cut rows' heads apart for g = 3 and 12."""
+    """g = 1, 8, 16, 12 and 3: chunks of 128 query rows cut rows' heads apart for g = 3 and 12; at hd 512
+    each chunk runs on a CTA pair, each CTA over half of the head dims."""
     c = wl.prefill_case(nh, nkv, hd, 0, 150, dist="sym", seed=hd + nh)
     prefill_gates(c, mapped=False)
 
@@ -111,12 +112,14 @@ def many_sequence_case(lens, nh, nkv, hd, window, seed):
                    bt, off, qpos, ctx=int(max(p0 + r for r, p0 in lens)), npg=npages)
 
 
-@pytest.mark.parametrize("hd,nh,nkv,window", [(64, 16, 16, 0), (128, 32, 16, 300), (256, 16, 8, 700)])
+@pytest.mark.parametrize("hd,nh,nkv,window", [(64, 16, 16, 0), (128, 32, 16, 300), (256, 16, 8, 700),
+                                              (512, 16, 4, 300)])
 def test_persistent_grid_many_items(hd, nh, nkv, window):
-    """More (tile, kv head, chunk) items than two per SM: each CTA serves several items
-    in turn, its ring, S buffers and barriers running across them.  Four sequences --
-    a 1-row prompt (an empty second chunk) and a continuation at position 300 among
-    them -- give ragged tiles."""
+    """More (tile, kv head, chunk) items than two per SM: each CTA (CTA pair at hd 512)
+    serves several items in turn, its ring, S buffers and barriers -- at hd 512 also
+    the S exchange buffers -- running across them.  Four sequences -- a 1-row prompt
+    (an empty second chunk) and a continuation at position 300 among them -- give
+    ragged tiles."""
     import torch
     from gpu_util import PrefillDev
     c = many_sequence_case([(1500, 0), (1, 0), (900, 300), (1700, 0)], nh, nkv, hd, window, seed=hd + window)
@@ -157,7 +160,7 @@ def run_split(case, splits, seq=None):
 
 
 @pytest.mark.parametrize("splits", [1, 2, 5, 16])
-@pytest.mark.parametrize("hd,window", [(64, 0), (128, 1024), (256, 0), (256, 1024)])
+@pytest.mark.parametrize("hd,window", [(64, 0), (128, 1024), (256, 0), (256, 1024), (512, 0), (512, 1024)])
 def test_split_kv_multi_row_decode(hd, window, splits):
     """The tcgen05 large-M path for multi-row decode: 16 rows of one sequence at the
     end of a 3000-token context (32 query rows per kv head, beyond the decode kernel's
@@ -209,8 +212,8 @@ def test_split_kv_bad_arguments():
     x = torch.zeros(64, dtype=torch.int16, device="cuda")
     with pytest.raises(pgqa.PgqaError):          # no scratch with splits > 1
         pgqa.attn_prefill_split(x, None, x, x, x, x, x, x, None, x, x, 1, 1, 8, 2, 128, 0, 2)
-    with pytest.raises(pgqa.PgqaError):          # hd 512 has no split path
-        pgqa.attn_prefill_split(x, x, x, x, x, x, x, x, None, x, x, 1, 1, 8, 2, 512, 0, 2)
+    with pytest.raises(pgqa.PgqaError):          # a head dim the kernels do not take
+        pgqa.attn_prefill_split(x, x, x, x, x, x, x, x, None, x, x, 1, 1, 8, 2, 96, 0, 2)
 
 
 def test_kvpos_below_qpos_and_an_empty_row():
@@ -268,10 +271,10 @@ def test_split_scratch_16_byte_aligned_gives_the_same_bits():
 
 def test_kvpos_past_qpos_changes_nothing():
     """Causal prefill: kvpos past qpos gives the bits of kvpos = qpos, on the tiled kernel
-    (hd 128, 256), the hd-512 kernel and the split-KV path, with NaN in every slot past the
-    last row's position."""
+    (hd 128, 256; hd 512 on CTA pairs) and the split-KV path, with NaN in every slot past
+    the last row's position."""
     from gpu_util import PrefillDev, first_difference
-    for hd, splits in ((128, 1), (256, 1), (512, 1), (256, 3)):
+    for hd, splits in ((128, 1), (256, 1), (512, 1), (256, 3), (512, 3)):
         c = wl.prefill_case(16, 8, hd, 0, 200, dist="sym", seed=hd)
         rows = 150
         c = dataclasses.replace(c, rows=rows, q=c.q[:rows * c.nh * c.hd], qpos=c.qpos[:rows], off=c.off[:rows])
