@@ -1146,8 +1146,8 @@ def run_sweep(args, rank, world, dist):
                     kv_eff = min(ctx, window) if window > 0 else ctx
                     # more query rows per kv head than pgqa_attn_decode packs into a
                     # CTA (8): the rows are one sequence's last positions, served by the
-                    # tiled tcgen05 kernel with split-KV (hd <= 256)
-                    tiled = rows * (nh // nkv) > 8 and hd <= 256
+                    # tiled tcgen05 kernel with split-KV
+                    tiled = rows * (nh // nkv) > 8
                     if tiled:
                         t0_h, tn_h = pgqa.make_tiles(np.zeros(rows, np.int32), pgqa.prefill_rows_per_tile(hd))
                         t0 = torch.from_numpy(t0_h).to(dev)
@@ -1211,7 +1211,7 @@ def run_sweep(args, rank, world, dist):
         "config": {"workload": "sweep_nh32_nkv16", "points": len(results),
                    "grid": "hd {128,256,512} x ctx {1K,4K,16K,64K} x rows {1,4,16} x window {0,1024,4096}",
                    "worst": by[:3], "best": by[-3:], "seconds": round(time.perf_counter() - t_all0, 1),
-                   "paths": "pgqa_attn_decode; pgqa_attn_prefill_split for rows x g > 8 at hd <= 256",
+                   "paths": "pgqa_attn_decode; pgqa_attn_prefill_split for rows x g > 8",
                    "l2": "rotating pool copies per (hd, ctx)",
                    "timing": "per point: CUDA events around a graph of 20-400 back-to-back calls"},
         "roofline": {"bound": "hbm", "achieved": round(gm, 1), "peak": peak, "unit": "GB/s",

@@ -177,20 +177,20 @@ def test_split_kv_multi_row_decode(hd, window, splits):
 
 
 SWEEP_TILED = [(128, 16384, 16, 4096), (128, 65536, 16, 0), (128, 65536, 16, 1024), (256, 4096, 16, 1024),
-               (256, 16384, 16, 0), (256, 65536, 16, 4096)]
+               (256, 16384, 16, 0), (256, 65536, 16, 4096), (512, 16384, 16, 0), (512, 65536, 16, 4096)]
 
 
 @pytest.mark.parametrize("pt", SWEEP_TILED, ids=lambda p: "hd%d_ctx%d_r%d_w%d" % p)
 def test_sweep_rows16_points_on_the_tiled_split_path(pt):
-    """The sweep's 16-row points that the benchmark sends down the tiled tcgen05 path (rows x g > 8,
-    hd <= 256), routed exactly as it routes them -- make_tiles over one sequence, splits from
+    """The sweep's 16-row points that the benchmark sends down the tiled tcgen05 path (rows x g > 8;
+    CTA pairs at hd 512), routed exactly as it routes them -- make_tiles over one sequence, splits from
     prefill_split_count, the combine kernel merging -- on the sweep's inputs: Gaussian Q/K/V with 5% of
     keys x8, served from the permuted pool with the NaN null page, at 4K to 64K positions."""
     import paged_gqa_decode_attn_gb300 as pgqa
     from gpu_util import check_parity
     hd, ctx, rows, window = pt
     c = wl.sweep(*pt, mapped=True)
-    assert rows * (c.nh // c.nkv) > 8 and hd <= 256
+    assert rows * (c.nh // c.nkv) > 8
     t0, _ = pgqa.make_tiles(np.zeros(rows, np.int32), pgqa.prefill_rows_per_tile(hd))
     splits = pgqa.prefill_split_count(c.kv_len_eff(), rows, len(t0), c.nh, c.nkv)
     assert splits > 1
