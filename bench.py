@@ -608,6 +608,20 @@ def decode_summary(rig, el_ms, steps, spot, peak):
 # (sliding): the 32K-context target, the batched shared-table case and the tiny
 # latency case.  Each is timed with the headline's protocol.
 EXTRA_DECODE = ["long", "batched", "tiny"]
+# The tiled tcgen05 paths and the K/V write, timed in the default run too, each
+# by its own workload's protocol (no CPU baseline there, two end-to-end steps).
+EXTRA_OTHER = ["prefill_long", "prefill_hd512", "multirow", "prep_long"]
+
+
+def line_summary(line):
+    """The per-workload record of another workload's full line."""
+    ro = line["roofline"]
+    return {"workload": line["config"]["workload"], "metric": line["metric"],
+            "us_per_call": round(line["ms_per_step"] * 1e3, 3), "value": line["value"], "unit": line["unit"],
+            "frac": ro["frac"], "bound": ro["bound"], "kernel": ro["kernel"],
+            "spot_check": {k: v for k, v in line["run"].items() if k.startswith("spot_check")} or None,
+            "traffic": ro["traffic"],
+            "steps": line["steps"], "kernels_per_call": line["gpu_launches"] // max(1, line["steps"])}
 
 
 def run_ours(args, case, rank, world, dist):
@@ -649,6 +663,14 @@ def run_ours(args, case, rank, world, dist):
             ms2 = max_over_ranks(dist, ms2)
             extra.append(decode_summary(r2, ms2, args.steps, sp2, peak))
             del r2
+            torch.cuda.empty_cache()
+        for name in EXTRA_OTHER:
+            a2 = argparse.Namespace(**vars(args))
+            a2.workload, a2.no_cpu_baseline, a2.no_clocks, a2.e2e_steps, a2.copies = name, True, True, 2, 0
+            run = run_multirow if name == "multirow" else (run_prep if name.startswith("prep") else run_prefill)
+            l2 = run(a2, build_case(name), rank, world, dist)
+            if isinstance(l2, dict):
+                extra.append(line_summary(l2))
             torch.cuda.empty_cache()
 
     if rank != 0:
@@ -695,8 +717,8 @@ def run_ours(args, case, rank, world, dist):
 
 
 def run_prefill(args, case, rank, world, dist):
-    """One step = one pgqa_attn_prefill call over every row of the case (a NEXT-row
-    workload, not the default line): TFLOP/s against the bf16 tensor peak."""
+    """One step = one pgqa_attn_prefill call over every row of the case: TFLOP/s
+    against the bf16 tensor peak.  Returns the line (rank 0) or 0."""
     import torch
     import paged_gqa_decode_attn_gb300 as pgqa
 
@@ -818,14 +840,13 @@ def run_prefill(args, case, rank, world, dist):
                 "us_per_step": round(e2e_s / e2e_steps * 1e6, 3)},
         "gpu_launches": args.steps, "clocks": clocks,
     }
-    print(json.dumps(line), flush=True)
-    return 0
+    return line
 
 
 def run_multirow(args, case, rank, world, dist):
     """One step = one pgqa_attn_prefill_split call (the tcgen05 tiled kernel with
     split-KV, then the combine kernel) serving a multi-token decode: KV GB/s
-    against the HBM peak, as for the decode workloads."""
+    against the HBM peak, as for the decode workloads.  Returns the line (rank 0) or 0."""
     import torch
     import paged_gqa_decode_attn_gb300 as pgqa
 
@@ -949,8 +970,7 @@ def run_multirow(args, case, rank, world, dist):
                 "us_per_step": round(e2e_s / e2e_steps * 1e6, 3)},
         "gpu_launches": 2 * args.steps, "clocks": clocks,
     }
-    print(json.dumps(line), flush=True)
-    return 0
+    return line
 
 
 def prep_config(case):
@@ -960,9 +980,9 @@ def prep_config(case):
 
 
 def run_prep(args, case, rank, world, dist):
-    """One step = one pgqa_qk_norm_rope_write call over every row of the case (a
-    NEXT-row workload, not the default line): head-vector bytes read and written
-    over the device time, against the measured HBM copy bandwidth."""
+    """One step = one pgqa_qk_norm_rope_write call over every row of the case:
+    head-vector bytes read and written over the device time, against the measured
+    HBM copy bandwidth.  Returns the line (rank 0) or 0."""
     import torch
     import paged_gqa_decode_attn_gb300 as pgqa
 
@@ -1089,8 +1109,7 @@ def run_prep(args, case, rank, world, dist):
                 "us_per_step": round(e2e_s / e2e_steps * 1e6, 3)},
         "gpu_launches": args.steps, "clocks": clocks,
     }
-    print(json.dumps(line), flush=True)
-    return 0
+    return line
 
 
 def sweep_bytes(hd, ctx, rows, window, nh=32, nkv=16):
@@ -1244,7 +1263,8 @@ def main(argv=None):
     ap.add_argument("--no-clocks", action="store_true")
     ap.add_argument("--sweep-out", default="", help="--workload sweep: write every point's numbers here (JSON)")
     ap.add_argument("--no-extra", action="store_true",
-                    help="sliding: skip timing the long, batched and tiny configurations beside it")
+                    help="sliding: skip timing the other workloads (long, batched, tiny, the tiled paths, the "
+                         "K/V write) beside it")
     ap.add_argument("--clock-window", type=float, default=1.0,
                     help="seconds of graph replays around the timed region while clocks are sampled")
     args = ap.parse_args(argv)
@@ -1270,12 +1290,16 @@ def main(argv=None):
     dist = init_dist(world)
     try:
         if args.workload.startswith("prefill"):
-            return run_prefill(args, case, rank, world, dist)
-        if args.workload.startswith("prep"):
-            return run_prep(args, case, rank, world, dist)
-        if args.workload == "multirow":
-            return run_multirow(args, case, rank, world, dist)
-        return run_ours(args, case, rank, world, dist)
+            line = run_prefill(args, case, rank, world, dist)
+        elif args.workload.startswith("prep"):
+            line = run_prep(args, case, rank, world, dist)
+        elif args.workload == "multirow":
+            line = run_multirow(args, case, rank, world, dist)
+        else:
+            return run_ours(args, case, rank, world, dist)
+        if isinstance(line, dict):
+            print(json.dumps(line), flush=True)
+        return 0
     finally:
         if dist is not None:
             dist.destroy_process_group()
