@@ -41,6 +41,7 @@
 namespace pgqa {
 
 int device_info(int *num_sms, unsigned int **err);   // pgqa_api.cu
+int current_context_id(unsigned long long *id);      // pgqa_api.cu
 
 namespace {
 
@@ -360,21 +361,26 @@ template <int HD>
 cudaError_t launch_prep(const PrepParams &p, int grid, cudaStream_t s)
 {
     const int bytes = p.stages * p.stage_bytes + 16 * p.stages;
+    // the smem attribute belongs to a CUDA context: set once per context
+    // (a device reset makes a new one) on each device
     static std::mutex mu;
-    static bool set_for_device[64];   // the smem attribute is set on that device
+    static unsigned long long set_for_ctx[64];   // 0: not set in any context yet
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess)
         return e;
+    unsigned long long ctx = 0;
+    if (current_context_id(&ctx) != PGQA_OK)
+        ctx = 0;
     {
         std::lock_guard<std::mutex> lock(mu);
-        if (dev < 0 || dev >= 64 || !set_for_device[dev]) {
+        if (dev < 0 || dev >= 64 || ctx == 0 || set_for_ctx[dev] != ctx) {
             e = cudaFuncSetAttribute(qk_norm_rope_kernel<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      kPrepSmemBudget);
             if (e != cudaSuccess)
                 return e;
             if (dev >= 0 && dev < 64)
-                set_for_device[dev] = true;
+                set_for_ctx[dev] = ctx;
         }
     }
     qk_norm_rope_kernel<HD><<<grid, kPrepThreads, bytes, s>>>(p);
