@@ -6,7 +6,7 @@
 //   * one CTA serves 128 query rows (row, head) of one tile and kv head --
 //     the M = 128 of every MMA -- with heads fastest; their Q sits in tensor
 //     memory (the A operand of S), which leaves 192 KB of shared memory to
-//     the K/V ring;
+//     the K/V ring (128 KB beside the S exchange buffers at hd 512);
 //   * warp 16 streams the chunk's union window in blocks of 4 pages (64
 //     tokens) by TMA into that ring, page ids read 32 at a time ahead of the
 //     copies, one box per (page, kv head) tile each: K in a 5-D view that
@@ -17,8 +17,8 @@
 //     [hd/64][16 tokens][128 B]; a stage's K and V have barriers of their
 //     own, so K_{j+NST} streams in as soon as S_j is done;
 //   * warp 17 issues S_j = Q K_j^T into one of two TMEM buffers (64 columns
-//     each) and warp 19 O += P_j V_j (TMEM, hd columns, one MMA per page),
-//     each batch committed to mbarriers;
+//     each) and warp 19 O += P_j V_j (TMEM, a column per head dim of the CTA,
+//     one MMA per page), each batch committed to mbarriers;
 //   * warp 18 computes the work items ahead and publishes them;
 //   * at hd 512, where O of 128 rows would fill all of tensor memory, a pair
 //     of CTAs (a cluster of two) serves each item, each CTA over half of the
