@@ -227,6 +227,51 @@ int pool_map(const void *base, int hd, CUtensorMap *out, int *kind, int want = k
     return PGQA_OK;
 }
 
+// A TMA descriptor of a [rows][nh][hd] bf16 Q whose box is one tcgen05 prefill
+// chunk's 64 dims: 64 dims x g heads (one kv head's) x 128 / g rows, under the
+// 128-byte swizzle.  The row count is not known here, so the row dimension
+// spans the int32 range; the kernel loads only chunks whose rows all lie in a
+// tile.  Needs g to divide 128.
+struct QMapEntry {
+    const void *base = nullptr;
+    int nh = 0, hd = 0, g = 0;
+    CUtensorMap map;
+};
+QMapEntry g_qmap_cache[32];
+unsigned g_qmap_next = 0;
+
+int q_map(const void *base, int nh, int hd, int g, CUtensorMap *out)
+{
+    if (g < 1 || g > 128 || 128 % g != 0)
+        return PGQA_ERR_INVALID_ARGUMENT;
+    for (auto &e : g_qmap_cache)
+        if (e.base == base && e.nh == nh && e.hd == hd && e.g == g) {
+            *out = e.map;
+            return PGQA_OK;
+        }
+    int st = get_encoder();
+    if (st != PGQA_OK)
+        return st;
+    CUtensorMap m;
+    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(hd), static_cast<cuuint64_t>(nh), 0x7fffffffull};
+    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(hd) * 2u, static_cast<cuuint64_t>(nh) * hd * 2u};
+    const cuuint32_t box[3] = {64u, static_cast<cuuint32_t>(g), static_cast<cuuint32_t>(128 / g)};
+    const cuuint32_t estride[3] = {1u, 1u, 1u};
+    CUresult r = g_encode(&m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box,
+                          estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS)
+        return PGQA_ERR_TENSOR_MAP;
+    QMapEntry &e = g_qmap_cache[g_qmap_next++ % 32];
+    e.base = base;
+    e.nh = nh;
+    e.hd = hd;
+    e.g = g;
+    e.map = m;
+    *out = m;
+    return PGQA_OK;
+}
+
 bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
 }  // namespace
@@ -705,6 +750,14 @@ int prefill_call(void *o, void *part, const void *q, const void *k_pool, const v
         return st;
     p.whole_tile_box = kind_v == kMapWhole;
     p.k_halves = kind_k == kMapHalves;
+    // Q by TMA where g divides the 128-row chunk and a tile can fill a chunk
+    // (else, or if the driver refuses the map, by loads from the softmax
+    // threads, in the kernel built without that path)
+    CUtensorMap tq;
+    a.tm_q = (128 % g == 0 && static_cast<long long>(a.max_tile_rows) * g >= 128 &&
+              q_map(q, nh, hd, g, &tq) == PGQA_OK)
+                 ? &tq
+                 : nullptr;
     p.err = s->err;
     a.num_sms = s->num_sms;
     a.tm_k = &tk;

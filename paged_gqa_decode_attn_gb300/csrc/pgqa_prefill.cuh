@@ -57,6 +57,7 @@ struct PrefillLaunchArgs {
     PrefillParams p;
     const CUtensorMap *tm_k;
     const CUtensorMap *tm_v;
+    const CUtensorMap *tm_q;    // Q as [rows][nh][hd], boxes of 64 dims x g heads x 128/g rows; null: no Q by TMA
     int ntiles;
     int max_tile_rows;    // no tile holds more rows (<= rows_per_tile): sets the chunks per tile
     int num_sms;          // persistent grids: one CTA per SM (pairs: as many as are resident)

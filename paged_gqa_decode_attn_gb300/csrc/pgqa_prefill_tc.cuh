@@ -287,13 +287,14 @@ struct TcGeo {
 struct TcItem {
     int t0, tn, kh, qbase, lo_u, hi_u, p_first, npages, nblocks, off0, split;
     bool live;     // the chunk has rows
+    bool qslot;    // the chunk's Q comes by TMA through a ring stage ahead of its blocks
 };
 constexpr int kItemSlot = 64;     // bytes of one published item in shared memory
 static_assert(sizeof(TcItem) <= kItemSlot && kItemSlot % 16 == 0, "published item slot");
 
 // Item `it` (by one whole warp, four query rows per lane), and the visible
 // range (lo, hi) of each of its 128 query rows into win[] ((1, 0): no row).
-template <int HD>
+template <int HD, bool kQTma>
 __device__ __forceinline__ TcItem tc_item_rows(const PrefillParams &p, int it, int ntiles, int nchunks, int lane,
                                                int2 *win)
 {
@@ -319,6 +320,7 @@ __device__ __forceinline__ TcItem tc_item_rows(const PrefillParams &p, int it, i
     I.npages = 0;
     I.nblocks = 0;
     I.off0 = 0;
+    I.qslot = false;
     const bool too_long = I.tn > p.rows_per_tile;
     if (too_long && lane == 0)
         atomicOr(p.err, kErrTileRows);
@@ -361,6 +363,10 @@ __device__ __forceinline__ TcItem tc_item_rows(const PrefillParams &p, int it, i
     }
     I.nblocks = (I.npages + G::kBlockPages - 1) / G::kBlockPages;
     I.off0 = __ldg(p.off + I.t0);
+    // Q through the ring: its 128 rows are whole positions of the tile (g
+    // divides 128 wherever the kernel takes this path), so one box per 64
+    // dims reads nothing past the tile
+    I.qslot = kQTma && I.nblocks > 0 && I.qbase + G::kRows <= nqr;
     return I;
 }
 
@@ -409,10 +415,14 @@ __device__ __forceinline__ void tc_prefetch_item(const PrefillParams &p, const T
 // counters that continue across items, so the next item's K/V stream in
 // while the current one finishes, and its Q goes into tensor memory (after
 // the current item's last S) before the current item's O is read out.
-template <int HD>
+// kQTma: a chunk whose 128 rows are whole positions of its tile takes its Q
+// by TMA (tm_q: a [rows][nh][hd] view with boxes of 64 dims x g heads x
+// 128 / g positions) into a ring stage ahead of its blocks, instead of by
+// loads from every softmax thread when the item starts.
+template <int HD, bool kQTma>
 __global__ void __launch_bounds__(TcGeo<HD>::kThreads, 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
-                      const PrefillParams p, int ntiles, int nchunks)
+                      const __grid_constant__ CUtensorMap tm_q, const PrefillParams p, int ntiles, int nchunks)
 {
     using G = TcGeo<HD>;
     constexpr int NST = G::kStages;
@@ -534,7 +544,7 @@ __global__ void __launch_bounds__(TcGeo<HD>::kThreads, 1)
                 iok = mbar_wait_bounded(b_iempty + 8 * sl, ((kit >> 1) - 1) & 1, p.err, kErrTimeoutEmpty);
             __syncwarp();
             int2 *w = reinterpret_cast<int2 *>(smem + G::kWinOff) + sl * G::kRows;
-            const TcItem I = tc_item_rows<HD>(p, it, ntiles, nchunks, lane, w);
+            const TcItem I = tc_item_rows<HD, kQTma>(p, it, ntiles, nchunks, lane, w);
             if (lane == 0)
                 *reinterpret_cast<TcItem *>(smem + G::kInfoOff + sl * kItemSlot) = I;
             __syncwarp();
@@ -547,15 +557,39 @@ __global__ void __launch_bounds__(TcGeo<HD>::kThreads, 1)
         if (lane == 0) {
             tma_prefetch_map(&tm_k);
             tma_prefetch_map(&tm_v);
+            if (kQTma)
+                tma_prefetch_map(&tm_q);
         }
         bool ok = true;
-        int jg = 0;                                    // blocks issued, over all items
+        int js = 0;                                    // ring slots filled (Q tiles and blocks), over all items
         int kit = 0;
         for (int it = first_item(0); it < nitems; it = next_item(it), ++kit) {
             const TcItem I = take_item(kit);
             release_item(kit);
             if (!I.live || I.nblocks == 0)
                 continue;
+            if (kQTma && I.qslot) {
+                // the chunk's Q, [hd/64][128 rows][128 B] under the 128-byte
+                // swizzle, takes a whole stage ahead of its blocks; V's barrier
+                // passes the slot with a bare arrival
+                const int st = js % NST;
+                if (lane == 0 && ok && js >= NST) {
+                    ok = mbar_wait_bounded(b_kempty + 8 * st, ((js / NST) - 1) & 1, p.err, kErrTimeoutEmpty);
+                    if (ok)
+                        ok = mbar_wait_bounded(b_vempty + 8 * st, ((js / NST) - 1) & 1, p.err, kErrTimeoutEmpty);
+                }
+                ok = __shfl_sync(0xffffffffu, ok, 0);
+                if (ok && lane == 0) {
+                    const uint32_t sQ = s_base + G::kStageOff + st * G::kStageBytes;
+                    mbar_arrive_expect_tx(b_kfull + 8 * st, G::kStageBytes);
+#pragma unroll
+                    for (int c = 0; c < NCH; ++c)
+                        tma_load_3d(sQ + c * (G::kRows * 128), &tm_q, b_kfull + 8 * st, dofs + c * kBoxElems,
+                                    I.kh * p.g, I.t0 + I.qbase / p.g);
+                    mbar_arrive(b_vfull + 8 * st);
+                }
+                ++js;
+            }
             const int32_t *tbl = p.block_table + I.off0 + I.p_first;
             for (int c0 = 0; c0 < I.npages; c0 += 32) {       // 32 is a multiple of the block's pages
                 int phys = 0;
@@ -565,15 +599,15 @@ __global__ void __launch_bounds__(TcGeo<HD>::kThreads, 1)
                         phys = __ldg(p.page_map + phys);
                 }
                 const int nc = min(32, I.npages - c0);
-                for (int i = 0; i < nc; i += G::kBlockPages, ++jg) {
+                for (int i = 0; i < nc; i += G::kBlockPages, ++js) {
                     const int np = min(G::kBlockPages, nc - i);
-                    const int st = jg % NST;
+                    const int st = js % NST;
                     const uint32_t sK = s_base + G::kStageOff + st * G::kStageBytes;
                     const uint32_t sV = sK + G::kKBytes;
                     const uint32_t half_tx = np * kPage * HDC * 2;
-                    // K of block jg, once S of block jg - NST is done
-                    if (lane == 0 && ok && jg >= NST)
-                        ok = mbar_wait_bounded(b_kempty + 8 * st, ((jg / NST) - 1) & 1, p.err, kErrTimeoutEmpty);
+                    // K of this block, once the slot's last use is released (its S batch)
+                    if (lane == 0 && ok && js >= NST)
+                        ok = mbar_wait_bounded(b_kempty + 8 * st, ((js / NST) - 1) & 1, p.err, kErrTimeoutEmpty);
                     ok = __shfl_sync(0xffffffffu, ok, 0);
                     if (ok && lane == 0)
                         mbar_arrive_expect_tx(b_kfull + 8 * st, half_tx);
@@ -591,9 +625,9 @@ __global__ void __launch_bounds__(TcGeo<HD>::kThreads, 1)
                             }
                         }
                     }
-                    // V of block jg, once PV of block jg - NST is done
-                    if (lane == 0 && ok && jg >= NST)
-                        ok = mbar_wait_bounded(b_vempty + 8 * st, ((jg / NST) - 1) & 1, p.err, kErrTimeoutEmpty);
+                    // V of this block, once the slot's last use is released (its PV batch)
+                    if (lane == 0 && ok && js >= NST)
+                        ok = mbar_wait_bounded(b_vempty + 8 * st, ((js / NST) - 1) & 1, p.err, kErrTimeoutEmpty);
                     ok = __shfl_sync(0xffffffffu, ok, 0);
                     if (ok && lane == 0)
                         mbar_arrive_expect_tx(b_vfull + 8 * st, half_tx);
@@ -630,21 +664,24 @@ __global__ void __launch_bounds__(TcGeo<HD>::kThreads, 1)
         const uint32_t k_sbo = p.k_halves ? static_cast<uint32_t>(NCH * 1024) : 1024u;
         bool ok = true;
         int jg = 0, kq = 0;                            // blocks and items with blocks, over all items
+        int qs = 0;                                    // Q tiles that came through the ring
         int kit = 0;
         for (int it = first_item(0); it < nitems; it = next_item(it), ++kit) {
             const TcItem I = take_item(kit);
             release_item(kit);
             if (!I.live || I.nblocks == 0)
                 continue;
+            if (kQTma && I.qslot)
+                ++qs;
             if (lane == 0) {
                 if (ok)
                     ok = mbar_wait_bounded(b_qready, kq & 1, p.err, kErrTimeoutFull);
                 tc_fence_after();
                 for (int j = 0; j < I.nblocks; ++j) {
-                    const int jj = jg + j;
-                    const int st = jj % NST, b = jj & 1;
+                    const int jj = jg + j, js = jj + qs;    // block and ring slot
+                    const int st = js % NST, b = jj & 1;
                     if (ok)
-                        ok = mbar_wait_bounded(b_kfull + 8 * st, (jj / NST) & 1, p.err, kErrTimeoutFull);
+                        ok = mbar_wait_bounded(b_kfull + 8 * st, (js / NST) & 1, p.err, kErrTimeoutFull);
                     if (ok && jj >= 2)
                         ok = mbar_wait_bounded(b_sfree + 8 * b, ((jj - 2) >> 1) & 1, p.err, kErrTimeoutFull);
                     tc_fence_after();
@@ -669,24 +706,26 @@ __global__ void __launch_bounds__(TcGeo<HD>::kThreads, 1)
         // ------------------------------------------------ PV issuer (one thread)
         constexpr uint32_t kIdO = umma_idesc_bf16(128, HDC, 0, 1);
         bool ok = true;
-        int jg = 0, kq = 0;
+        int jg = 0, kq = 0, qs = 0;
         int kit = 0;
         for (int it = first_item(0); it < nitems; it = next_item(it), ++kit) {
             const TcItem I = take_item(kit);
             release_item(kit);
             if (!I.live || I.nblocks == 0)
                 continue;
+            if (kQTma && I.qslot)
+                ++qs;
             if (lane == 0) {
                 for (int j = 0; j < I.nblocks; ++j) {
-                    const int jj = jg + j, st = jj % NST;
+                    const int jj = jg + j, js = jj + qs, st = js % NST;
                     if (ok)
                         ok = mbar_wait_bounded(b_pfull, jj & 1, p.err, kErrTimeoutFull);
                     if (ok && j == 0 && kq >= 1)            // the previous item's O has been read out
                         ok = mbar_wait_bounded(b_ofree, (kq - 1) & 1, p.err, kErrTimeoutFull);
-                    // V_j has landed: the softmax waited for it before P_j (it zeroes edge
-                    // rows of V_j); the test is free and makes this thread see it too
+                    // V_j has landed (the softmax has waited for it already where it
+                    // zeroes V_j's edge rows)
                     if (ok)
-                        ok = mbar_wait_bounded(b_vfull + 8 * st, (jj / NST) & 1, p.err, kErrTimeoutFull);
+                        ok = mbar_wait_bounded(b_vfull + 8 * st, (js / NST) & 1, p.err, kErrTimeoutFull);
                     tc_fence_after();
                     if (ok) {
                         const uint32_t sV = s_base + G::kStageOff + st * G::kStageBytes + G::kKBytes;
@@ -717,6 +756,7 @@ __global__ void __launch_bounds__(TcGeo<HD>::kThreads, 1)
         const int pair_bar = 1 + (warp & 3);                               // warps w, w + 4, w + 8, ...
         bool ok = true;
         int jg = 0;
+        int qs = 0;                 // Q tiles that came through the ring
 
         // the finish of an item: the row sum over the parts, O / l in bf16
         // (this part's dims) -- or, split, the unnormalised partial (m, L, O)
@@ -839,7 +879,43 @@ __global__ void __launch_bounds__(TcGeo<HD>::kThreads, 1)
             // this item's Q -> tensor memory columns kQCol + [0, hd/2), 16 columns
             // (32 elements) at a time, the parts taking turns; the previous
             // item's S MMAs, the only readers of Q, are all complete
-            {
+            if (kQTma && I.qslot) {
+                // from its ring stage: row r's 64-dim chunk c at c * 16 KB + 128 r,
+                // 16-byte unit u at u ^ (r % 8)
+                const int js = jg + qs;
+                ++qs;
+                const int st = js % NST;
+                if (ok)
+                    ok = mbar_wait_bounded(b_kfull + 8 * st, (js / NST) & 1, p.err, kErrTimeoutFull);
+                const uint8_t *sq = smem + G::kStageOff + st * G::kStageBytes + row * 128;
+                const uint32_t tq = trow + G::kQCol;
+#pragma unroll
+                for (int c0 = part * 16; c0 < HDC / 2; c0 += 16 * NP) {
+                    const int e0 = 2 * c0;                          // first element of the piece
+                    const uint8_t *src = sq + (e0 >> 6) * (G::kRows * 128);
+                    const int u0 = (e0 & 63) >> 3;
+                    uint32_t r[16];
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        const uint4 v = *reinterpret_cast<const uint4 *>(src + (((u0 + k) ^ (row & 7)) << 4));
+                        r[4 * k] = v.x;
+                        r[4 * k + 1] = v.y;
+                        r[4 * k + 2] = v.z;
+                        r[4 * k + 3] = v.w;
+                    }
+                    tmem_st16(tq + c0, r);
+                }
+                tmem_wait_st();
+                tc_fence_before();
+                group_bar_sync(5, 32 * G::kSoftmaxWarps);          // every softmax thread has read the tile
+                if (tid == 0) {
+                    mbar_arrive(b_kempty + 8 * st);
+                    mbar_arrive(b_vempty + 8 * st);
+                }
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(b_qready);
+            } else {
                 // every load of this thread's part goes out before the first store
                 constexpr int kQIt = (HDC / 2 + 16 * NP - 1) / (16 * NP);   // 16-column pieces per thread
                 const uint4 *src = reinterpret_cast<const uint4 *>(p.q + rh * HD + dofs);
@@ -1007,9 +1083,9 @@ __global__ void __launch_bounds__(TcGeo<HD>::kThreads, 1)
                 // included) and P is 0 there: zero them before the PV MMA reads them
                 const int btok0 = (I.p_first + j * G::kBlockPages) * kPage;
                 if (btok0 < I.lo_u || btok0 + G::kBlockTokens - 1 > I.hi_u) {
-                    const int st = jj % NST;
+                    const int js = jj + qs, st = js % NST;
                     if (ok)           // V_j lands apart from K_j: zero nothing before the copy has
-                        ok = mbar_wait_bounded(b_vfull + 8 * st, (jj / NST) & 1, p.err, kErrTimeoutFull);
+                        ok = mbar_wait_bounded(b_vfull + 8 * st, (js / NST) & 1, p.err, kErrTimeoutFull);
                     uint8_t *sV = smem + G::kStageOff + st * G::kStageBytes + G::kKBytes;
                     const int np = min(G::kBlockPages, I.npages - j * G::kBlockPages);
                     for (int e = tid; e < np * kPage * NCH * 8; e += G::kSoftmaxWarps * 32) {
@@ -1078,7 +1154,7 @@ int prefill_tc_pair_capacity()
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, prefill_tc_kernel<HD>, &cfg) != cudaSuccess) {
+    if (cudaOccupancyMaxActiveClusters(&n, prefill_tc_kernel<HD, false>, &cfg) != cudaSuccess) {
         cudaGetLastError();
         n = 0;
     }
@@ -1092,8 +1168,11 @@ cudaError_t launch_prefill_tc(const PrefillLaunchArgs &a, bool set_attr)
 {
     using G = TcGeo<HD>;
     if (set_attr) {
-        cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             G::kAlloc);
+        cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel<HD, false>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, G::kAlloc);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(prefill_tc_kernel<HD, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     G::kAlloc);
         if (e != cudaSuccess)
             return e;
     }
@@ -1130,7 +1209,12 @@ cudaError_t launch_prefill_tc(const PrefillLaunchArgs &a, bool set_attr)
     cfg.stream = a.stream;
     cfg.attrs = attr;
     cfg.numAttrs = na;
-    return cudaLaunchKernelEx(&cfg, prefill_tc_kernel<HD>, *a.tm_k, *a.tm_v, a.p, a.ntiles, nchunks);
+    // without a Q map the kernel never reads tm_q: K's map fills the parameter
+    if (a.tm_q)
+        return cudaLaunchKernelEx(&cfg, prefill_tc_kernel<HD, true>, *a.tm_k, *a.tm_v, *a.tm_q, a.p, a.ntiles,
+                                  nchunks);
+    return cudaLaunchKernelEx(&cfg, prefill_tc_kernel<HD, false>, *a.tm_k, *a.tm_v, *a.tm_k, a.p, a.ntiles,
+                              nchunks);
 }
 
 }  // namespace pgqa
