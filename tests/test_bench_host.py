@@ -127,3 +127,25 @@ def test_reference_arm_prints_the_contract_line():
     b = _bench()
     assert d["config"] == json.loads(json.dumps(b.config_of(b.build_case("tiny"))))
     assert not {"splits", "merge", "l2", "timing"} & set(d["config"])
+
+
+def test_the_default_line_summarises_each_other_workload():
+    """The default run times the tiled paths and the K/V write beside the decode workloads: each of their
+    workloads builds on the host, and a full line of theirs reduces to the record the default line lists
+    (its metric, rate, roofline fraction, launches per call and every spot-check key)."""
+    b = _bench()
+    assert set(b.EXTRA_OTHER) <= {"prefill_long", "prefill_hd512", "multirow", "prep_long", "prefill_page"}
+    for name in b.EXTRA_OTHER:
+        assert b.build_case(name).name
+    line = {"metric": "paged causal prefill attention TFLOP/s", "value": 700.0, "unit": "TFLOP/s", "steps": 20,
+            "ms_per_step": 0.1845, "gpu_launches": 40,
+            "config": {"workload": "prefill_nh16_nkv8_hd256_w1024_ctx8192"},
+            "run": {"tiles": 64, "spot_check_rel_rms": 0.004, "spot_check_worst": 0.1},
+            "roofline": {"bound": "tensor", "frac": 0.37, "kernel": "prefill_tc_kernel<256>", "traffic": 1.0e8}}
+    s = b.line_summary(line)
+    assert s["workload"] == "prefill_nh16_nkv8_hd256_w1024_ctx8192" and s["us_per_call"] == 184.5
+    assert s["value"] == 700.0 and s["unit"] == "TFLOP/s" and s["frac"] == 0.37 and s["bound"] == "tensor"
+    assert s["kernels_per_call"] == 2 and s["steps"] == 20 and s["traffic"] == 1.0e8
+    assert s["spot_check"] == {"spot_check_rel_rms": 0.004, "spot_check_worst": 0.1}
+    line["run"] = {"tiles": 64}
+    assert b.line_summary(line)["spot_check"] is None
