@@ -99,6 +99,17 @@ extern "C" {
  * stream: a cudaStream_t (NULL = the legacy default stream).  The call only
  * enqueues work: it never synchronises and never allocates.  Calls sharing
  * `part` or `counters` must be ordered on the GPU (same stream or events).
+ *
+ * Ordering with the kernel before it in the stream: the kernels may start
+ * while that kernel ends (programmatic dependent launch) and wait for it to
+ * complete before they use any input.  A call that merges in the combine
+ * kernel also reads off, qpos, kvpos, block_table and page_map before that
+ * wait, through L2 only, to prefetch its first K/V pages into L2.  Those
+ * reads may see values the earlier kernel is still writing; they only steer
+ * the prefetch, and every index they produce is checked against the extent
+ * of the allocation it points into (cuMemGetAddressRange), so nothing
+ * outside the caller's allocations is touched.  Where the driver cannot size
+ * an allocation (virtual-memory mappings, for example) the prefetch is off.
  */
 int pgqa_attn_decode(void *o, void *part, const void *q, const void *k_pool, const void *v_pool,
                      const int32_t *block_table, const int32_t *off, const int32_t *qpos,

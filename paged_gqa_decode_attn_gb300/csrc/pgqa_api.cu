@@ -77,6 +77,9 @@ using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long *);
 CtxGetCurrentFn g_ctx_current = nullptr;
 CtxGetIdFn g_ctx_id = nullptr;
 
+using MemGetAddressRangeFn = CUresult (*)(CUdeviceptr *, size_t *, CUdeviceptr);
+MemGetAddressRangeFn g_mem_range = nullptr;
+
 using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
                                    const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
                                    CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
@@ -121,6 +124,45 @@ int device_state(DeviceState **out)
     }
     *out = &s;
     return PGQA_OK;
+}
+
+// Bytes from `ptr` to the end of the device allocation that holds it, or 0
+// when the driver cannot tell (memory it did not allocate with cuMemAlloc or
+// cudaMalloc, such as virtual-memory mappings, or a null pointer).
+long long bytes_to_allocation_end(const void *ptr)
+{
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuMemGetAddressRange", &fn, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_mem_range = reinterpret_cast<MemGetAddressRangeFn>(fn);
+    });
+    if (!g_mem_range || !ptr)
+        return 0;
+    CUdeviceptr base = 0;
+    size_t size = 0;
+    const CUdeviceptr d = reinterpret_cast<CUdeviceptr>(ptr);
+    if (g_mem_range(&base, &size, d) != CUDA_SUCCESS || d < base || d - base >= size)
+        return 0;
+    return static_cast<long long>(base + size - d);
+}
+
+// The speculative prefetch's extents for a decode launch (pgqa_device.cuh):
+// every field stays 0, and the prefetch off, unless all allocations are known.
+void set_speculation(pgqa::DecodeParams &p, const void *k_pool, const void *v_pool, int hd)
+{
+    const long long tile_bytes = static_cast<long long>(pgqa::kPage) * hd * 2;
+    const long long kb = bytes_to_allocation_end(k_pool), vb = bytes_to_allocation_end(v_pool);
+    const long long bb = bytes_to_allocation_end(p.block_table);
+    const long long mb = p.page_map ? bytes_to_allocation_end(p.page_map) : 0;
+    if (kb < tile_bytes || vb < tile_bytes || bb < 4 || (p.page_map && mb < 4))
+        return;
+    p.spec_tiles = std::min(kb, vb) / tile_bytes;
+    p.spec_bt_len = bb / 4;
+    p.spec_pm_len = mb / 4;
 }
 
 int get_encoder()
@@ -594,6 +636,9 @@ int pgqa_attn_decode(void *o, void *part, const void *q, const void *k_pool, con
     p.trace = nullptr;
     p.cluster = 0;
     p.whole_tile_box = 0;
+    p.spec_tiles = p.spec_bt_len = p.spec_pm_len = 0;
+    p.k_pool = static_cast<const __nv_bfloat16 *>(k_pool);
+    p.v_pool = static_cast<const __nv_bfloat16 *>(v_pool);
     a.stream = static_cast<cudaStream_t>(stream);
 
     // The lock covers set-up and the (asynchronous) launch itself, so the
@@ -615,6 +660,15 @@ int pgqa_attn_decode(void *o, void *part, const void *q, const void *k_pool, con
     // that is packed leave at once), kv head and head subgroup
     const long long live = static_cast<long long>((rows + p.pack - 1) / p.pack) * nkv * hsg;
     p.cluster = p.counters ? on_chip_cluster(s, hi, hd, splits, live) : 0;
+    // Launches that merge in the combine kernel (more than 8 splits, or no
+    // counters) are long ones.  Their split CTAs prefetch their first pages
+    // while the kernel ahead of them in the stream ends: in a loop of calls,
+    // the previous call's combine kernel, during which they take the SMs its
+    // split CTAs leave.  When nothing ahead is still running, the guess costs
+    // a few dependent loads.  One wave of split CTAs at most: later waves
+    // start after the wait anyway.
+    if (splits > 1 && p.counters == nullptr && live * splits <= 2LL * s->num_sms)
+        set_speculation(p, k_pool, v_pool, hd);
     if (g_trace && static_cast<size_t>(splits) * nkv * hsg * rows * pgqa::kTraceEvents * 8 <= g_trace_bytes)
         p.trace = g_trace;
     a.tm_k = &tk;

@@ -150,6 +150,15 @@ struct DecodeParams {
     int cluster;             // > 1: the splits of a tile are one cluster of this size, merged on chip
     int whole_tile_box;      // 1: one 4-D TMA box per (page, kv head) tile; 0: hd/64 3-D boxes
     unsigned long long *trace;   // per-CTA timestamps (trace builds only), or null
+    // Speculative L2 prefetch before the dependency wait (0: none).  The
+    // extents of the caller's allocations, from each pointer to its
+    // allocation's end: block-table and page-map entries, and (page, kv head)
+    // tiles of both pools.
+    long long spec_tiles;
+    long long spec_bt_len;
+    long long spec_pm_len;
+    const __nv_bfloat16 *k_pool;
+    const __nv_bfloat16 *v_pool;
 };
 
 // ---------------------------------------------------------------- PTX helpers
@@ -513,6 +522,86 @@ __device__ __forceinline__ void row_window(const DecodeParams &p, int r, int &lo
     lo = p.window > 0 ? max(0, qp + 1 - p.window) : 0;
 }
 
+// ---------------------------------------------------------------- speculative prefetch
+//
+// A split CTA may be resident well before the kernel ahead of it in the stream
+// completes: when the combine kernel of the previous call runs, this call's
+// CTAs take the SMs its split CTAs leave.  Until its dependency wait returns,
+// such a CTA may read nothing that the previous kernel could still be writing
+// and rely on it.  It may, though, guess: it reads off, qpos, kvpos, the block
+// table and the page map as they stand and prefetches the first pages of its
+// range into L2, which the wait leaves idle.  The guess is only a hint:
+//  * every read goes through L2 alone (ld.global.cg), so no line it brings in
+//    can be read stale from the L1 after the wait;
+//  * every index is checked against the extent of the allocation it points
+//    into (measured on the host), so a stale or never-written entry cannot
+//    make an access outside the caller's memory;
+//  * a wrong guess costs bandwidth, not correctness: the loads after the wait
+//    read the inputs as they then are.
+// Budget: up to 512 KB of K and V per CTA, at most 32 pages.
+template <int HD>
+__device__ __forceinline__ void speculative_prefetch(const DecodeParams &p, int lane, int kh)
+{
+    constexpr int kPages = 8192 / HD < 32 ? 8192 / HD : 32;
+    const int rz = blockIdx.z;
+    const int g0 = p.pack > 1 ? rz - rz % p.pack : rz;
+    const int gn = p.pack > 1 ? min(p.pack, p.rows - g0) : 1;
+    int off_i = 0, lo_i = 1, hi_i = 0;
+    if (lane < gn) {
+        off_i = __ldcg(p.off + g0 + lane);
+        const int qp = __ldcg(p.qpos + g0 + lane);
+        hi_i = p.kvpos ? min(qp, __ldcg(p.kvpos + g0 + lane)) : qp;
+        lo_i = p.window > 0 ? max(0, qp + 1 - p.window) : 0;
+    }
+    // the packing verdict and the union range, as after the wait
+    const int off0 = __shfl_sync(0xffffffffu, off_i, 0);
+    const bool live = lane < gn && hi_i >= lo_i;
+    const bool same = __all_sync(0xffffffffu, lane >= gn || off_i == off0);
+    int max_lo = live ? lo_i : INT_MIN, min_hi = live ? hi_i : INT_MAX;
+    int lo_u = live ? lo_i : INT_MAX, hi_u = live ? hi_i : INT_MIN;
+#pragma unroll
+    for (int k = 16; k; k >>= 1) {
+        max_lo = max(max_lo, __shfl_xor_sync(0xffffffffu, max_lo, k));
+        min_hi = min(min_hi, __shfl_xor_sync(0xffffffffu, min_hi, k));
+        lo_u = min(lo_u, __shfl_xor_sync(0xffffffffu, lo_u, k));
+        hi_u = max(hi_u, __shfl_xor_sync(0xffffffffu, hi_u, k));
+    }
+    const bool packed = gn > 1 && same &&
+                        (max_lo == INT_MIN || static_cast<long long>(max_lo) <= static_cast<long long>(min_hi) + 1);
+    int off_r = off0;
+    if (packed) {
+        if (rz != g0)
+            return;                  // the group's first CTA prefetches for it
+    } else {
+        const int l = rz - g0;       // this CTA's own row
+        off_r = __shfl_sync(0xffffffffu, off_i, l & 31);
+        lo_u = __shfl_sync(0xffffffffu, lo_i, l & 31);
+        hi_u = __shfl_sync(0xffffffffu, hi_i, l & 31);
+    }
+    if (hi_u < lo_u)
+        return;
+    const long long p0 = lo_u >> 4, np = (hi_u >> 4) - p0 + 1;
+    const long long pb = p0 + (static_cast<long long>(blockIdx.x) * np) / p.splits;
+    const long long pn = p0 + (static_cast<long long>(blockIdx.x + 1) * np) / p.splits - pb;
+    if (lane >= pn || lane >= kPages)
+        return;
+    const long long idx = static_cast<long long>(off_r) + pb + lane;
+    if (idx < 0 || idx >= p.spec_bt_len)
+        return;
+    long long ph = __ldcg(p.block_table + idx);
+    if (p.page_map) {
+        if (ph < 0 || ph >= p.spec_pm_len)
+            return;
+        ph = __ldcg(p.page_map + ph);
+    }
+    const long long tile = ph * p.nkv + kh;
+    if (ph < 0 || tile >= p.spec_tiles)
+        return;
+    const size_t e = static_cast<size_t>(tile) * (kPage * HD);
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p.k_pool + e), "r"(kPage * HD * 2) : "memory");
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p.v_pool + e), "r"(kPage * HD * 2) : "memory");
+}
+
 // ---------------------------------------------------------------- tracing
 //
 // A library built with PGQA_TRACE records, per CTA, the global timer (ns) at a
@@ -747,8 +836,11 @@ __global__ void __launch_bounds__(Geo<HD>::kThreads, Cfg<HD>::kMinBlocks)
         tma_prefetch_map(&tm_k);
         tma_prefetch_map(&tm_v);
     }
-    // Nothing above touched global memory: wait here for the previous kernel
-    // in the stream (inputs may be its outputs), then let the next one launch.
+    if (p.spec_tiles > 0 && warp == NW)
+        speculative_prefetch<HD>(p, lane, kh);
+    // Nothing above relies on a value read from global memory: wait here for
+    // the previous kernel in the stream (inputs may be its outputs), then let
+    // the next one launch.
     grid_dependency_wait();
     grid_launch_dependents();
 
@@ -1344,8 +1436,12 @@ __global__ void __launch_bounds__(kCombineWarps * 32) decode_combine_kernel(cons
     const size_t rh = blockIdx.x;
     const int S = p.splits;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    grid_dependency_wait();          // the split kernel's partials
+    // The next kernel may launch at once: its own dependency wait still waits
+    // for this grid to complete, and this grid completes only after the split
+    // kernel it waits for here.  Its CTAs then take the SMs the split CTAs
+    // leave, ready (and prefetching) by the time this merge ends.
     grid_launch_dependents();
+    grid_dependency_wait();          // the split kernel's partials
     if (S <= kGroupSplits) {         // one level, one warp
         const int d4 = blockIdx.y * combine_slice<HD>() + lane;
         const bool mine = lane < combine_slice<HD>();
