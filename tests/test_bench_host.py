@@ -149,3 +149,15 @@ def test_the_default_line_summarises_each_other_workload():
     assert s["spot_check"] == {"spot_check_rel_rms": 0.004, "spot_check_worst": 0.1}
     line["run"] = {"tiles": 64}
     assert b.line_summary(line)["spot_check"] is None
+
+
+def test_l2_note_claims_hbm_only_past_three_l2():
+    """A run's L2 note says its reads come from HBM only when one rotation of its copies moves at least
+    3x L2 (129 MB); a smaller rotation (``--copies 1`` on the sliding workload) is marked a diagnostic."""
+    b = _bench()
+    big = b.l2_note(48, "pool copies", 48 * 8478720, "every step reads KV from HBM")
+    assert big.endswith("every step reads KV from HBM") and "> 3x L2" in big
+    small = b.l2_note(1, "pool copies", 8478720, "every step reads KV from HBM")
+    assert "HBM" not in small and "<= 3x L2" in small and "diagnostic" in small
+    edge = b.l2_note(3, "pool copies", 3 * b.L2_BYTES, "from HBM")
+    assert edge.endswith("from HBM")
