@@ -503,6 +503,50 @@ class DecodeRig:
         self._load(g_full or g_rem, load_s / 3)
         return ev0.elapsed_time(ev1), chunk
 
+    def time_single(self, n=30):
+        """Latency of one call alone: CUDA events around a single eager call on an idle
+        GPU (synchronised before and after), median over ``n`` calls on rotating pool
+        copies, in us.  A short GPU sleep ahead of the start event lets the host
+        enqueue the call first, so the region holds the call, not its host launch.
+        The per-call period of back-to-back calls is what the line's value reports;
+        this is the time one call takes from its first kernel's start to its last
+        kernel's end."""
+        import torch
+        stream = torch.cuda.current_stream()
+        ts = []
+        for i in range(n):
+            ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            torch.cuda.synchronize()
+            torch.cuda._sleep(100000)    # ~50 us
+            ev0.record(stream)
+            self.call(i)
+            ev1.record(stream)
+            ev1.synchronize()
+            ts.append(ev0.elapsed_time(ev1) * 1e3)
+        return statistics.median(ts)
+
+    def time_repeats(self, steps, chunk, reps=5):
+        """us per call of ``reps`` more timed regions of ``steps`` calls each (the
+        graphs of time_steps, already captured): their median and each value."""
+        import torch
+        chunk = max(1, min(steps, chunk))
+        full, rem = divmod(steps, chunk)
+        stream = torch.cuda.current_stream()
+        out = []
+        for _ in range(reps):
+            ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            torch.cuda.synchronize()
+            torch.cuda._sleep(200000)
+            ev0.record(stream)
+            for _ in range(full):
+                self.graph(chunk).replay()
+            if rem:
+                self.graph(rem).replay()
+            ev1.record(stream)
+            ev1.synchronize()
+            out.append(round(ev0.elapsed_time(ev1) * 1e3 / steps, 3))
+        return {"median": statistics.median(out), "each": out}
+
     @staticmethod
     def _load(g, seconds):
         import torch
@@ -601,15 +645,21 @@ class DecodeRig:
         return e2e_s, parts, eager_us
 
 
-def decode_summary(rig, el_ms, steps, spot, peak):
-    """Per-workload record: device time per call, GB/s, roofline fraction, splits, parity, traffic."""
+def decode_summary(rig, el_ms, steps, spot, peak, single_us=None, repeats=None):
+    """Per-workload record: device time per call, GB/s, roofline fraction, splits, parity, traffic; with
+    them, the latency of one call alone and the per-call time of repeated timed regions."""
     c = rig.case
     us = el_ms * 1e3 / steps
     gbs = rig.bpc / (us * 1e-6) / 1e9
-    return {"workload": c.name, "us_per_call": round(us, 3), "value": round(gbs, 2), "unit": "GB/s",
-            "frac": round(gbs / peak, 4), "splits": rig.splits, "kernels_per_call": rig.launches_per_call,
-            "algorithmic_bytes_per_call": rig.bpc, "spot_check_rel_rms": spot,
-            "traffic": recorded_traffic(c.name), "steps": steps}
+    r = {"workload": c.name, "us_per_call": round(us, 3), "value": round(gbs, 2), "unit": "GB/s",
+         "frac": round(gbs / peak, 4), "splits": rig.splits, "kernels_per_call": rig.launches_per_call,
+         "algorithmic_bytes_per_call": rig.bpc, "spot_check_rel_rms": spot,
+         "traffic": recorded_traffic(c.name), "steps": steps}
+    if single_us is not None:
+        r["single_call_us"] = round(single_us, 3)
+    if repeats is not None:
+        r["us_per_call_repeats"] = repeats
+    return r
 
 
 # The other decode configurations timed in the default run beside the headline
@@ -649,6 +699,8 @@ def run_ours(args, case, rank, world, dist):
     el_ms, chunk = rig.time_steps(args.steps, args.warmup, args.graph_chunk, dist,
                                   load_s=0.0 if args.no_clocks else args.clock_window)
     clocks = sampler.stop() if sampler else None
+    single_us = rig.time_single()
+    repeats = rig.time_repeats(args.steps, chunk)
     el_max = max_over_ranks(dist, el_ms)
     ms_per_step = el_max / args.steps
     value = sum_over_ranks(dist, float(rig.bpc) * args.steps) / (el_max * 1e-3) / 1e9
@@ -667,9 +719,10 @@ def run_ours(args, case, rank, world, dist):
             c2 = build_case(name)
             r2 = DecodeRig(args, c2, dev)
             sp2 = r2.spot_check() if rank == 0 and not args.no_check else None
-            ms2, _ = r2.time_steps(args.steps, args.warmup, args.graph_chunk, dist)
+            ms2, ch2 = r2.time_steps(args.steps, args.warmup, args.graph_chunk, dist)
             ms2 = max_over_ranks(dist, ms2)
-            extra.append(decode_summary(r2, ms2, args.steps, sp2, peak))
+            extra.append(decode_summary(r2, ms2, args.steps, sp2, peak, r2.time_single(),
+                                        r2.time_repeats(args.steps, ch2)))
             del r2
             torch.cuda.empty_cache()
         for name in EXTRA_OTHER:
@@ -700,6 +753,9 @@ def run_ours(args, case, rank, world, dist):
                         rig.copies * rig.bpc, "every step reads KV from HBM")
     run["timing"] = (f"CUDA events around CUDA graphs of {chunk} back-to-back calls, queued behind a short "
                      f"GPU sleep so the region holds only the calls")
+    run["single_call_us"] = round(single_us, 3)
+    run["single_call"] = "one call alone on an idle GPU, CUDA events around it, median of 30"
+    run["us_per_call_repeats"] = repeats
     if spot is not None:
         run["spot_check_rel_rms"] = spot
     line = {

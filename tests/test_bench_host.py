@@ -161,3 +161,17 @@ def test_l2_note_claims_hbm_only_past_three_l2():
     assert "HBM" not in small and "<= 3x L2" in small and "diagnostic" in small
     edge = b.l2_note(3, "pool copies", 3 * b.L2_BYTES, "from HBM")
     assert edge.endswith("from HBM")
+
+
+def test_decode_summary_carries_single_call_latency_and_repeats():
+    """Each extra decode workload's record keeps the protocol's other two numbers beside the per-call period:
+    the latency of one call alone, and the per-call time of repeated timed regions (median and each)."""
+    import types
+    b = _bench()
+    case = b.build_case("tiny")
+    rig = types.SimpleNamespace(case=case, bpc=case.algorithmic_bytes(), splits=8, launches_per_call=1)
+    rec = b.decode_summary(rig, 0.08, 20, 0.004, 6788.3, single_us=3.21,
+                           repeats={"median": 3.95, "each": [3.95, 3.94, 3.96]})
+    assert rec["us_per_call"] == 4.0 and rec["single_call_us"] == 3.21
+    assert rec["us_per_call_repeats"]["median"] == 3.95 and len(rec["us_per_call_repeats"]["each"]) == 3
+    assert "single_call_us" not in b.decode_summary(rig, 0.08, 20, None, 6788.3)
