@@ -390,7 +390,7 @@ class DecodeRig:
         self.case = case
         self.bpc = case.algorithmic_bytes()
         self.splits = splits or args.splits or pgqa.choose_splits(case.kv_len_eff(), case.rows, case.nkv,
-                                                                   nseq_of(case))
+                                                                   nseq_of(case), nh=case.nh, hd=case.hd)
         self.pool_bytes = case.k_pool.nbytes + case.v_pool.nbytes
         n = max(2, math.ceil(3 * L2_BYTES / max(self.bpc, 1)))
         n = min(n, max(2, int(0.25 * torch.cuda.get_device_properties(dev).total_memory // self.pool_bytes)))
@@ -1238,7 +1238,7 @@ def run_sweep(args, rank, world, dist):
                         tn = torch.from_numpy(tn_h).to(dev)
                         splits = pgqa.prefill_split_count(kv_eff, rows, len(t0_h), nh, nkv)
                     else:
-                        splits = pgqa.choose_splits(kv_eff, rows, nkv, 1)
+                        splits = pgqa.choose_splits(kv_eff, rows, nkv, 1, nh=nh, hd=hd)
                     part = torch.empty(max(1, pgqa.decode_part_bytes(rows, nh, splits, hd)) // 4 + 4,
                                        dtype=torch.float32, device=dev)
                     cnt = torch.zeros(max(1, pgqa.decode_counter_count(rows, nh, nkv)), dtype=torch.int32,

@@ -129,6 +129,33 @@ int pgqa_choose_splits(int kv_len_eff, int rows, int nkv, int nseq);
 int pgqa_choose_splits_for(int kv_len_eff, int rows, int nkv, int nseq, int num_sms);
 
 /*
+ * Splits per tile when the caller also knows the head count nh and head
+ * dimension hd: not in the pages, whose `choose_splits` takes neither.  It
+ * knows how many rows of a sequence share a CTA (max(1, 8 / (nh / nkv))), so
+ * how many CTAs one split launches, and, from the current device, how many of
+ * the hd kernel's CTAs and clusters can be resident at once.  With fewer tiles
+ * than SMs it fills the GPU in one wave -- one CTA per SM at hd 256 and 512,
+ * about 2.5 per SM at hd 64 and 128, whose CTAs are a third of an SM -- unless
+ * each CTA's share of K and V stays within 128 KB per two query rows it serves
+ * (q = min(8, rows packed per CTA x nh / nkv); 128 KB x max(1, q / 2)) with
+ * the largest cluster size (2, 4 or 8) whose clusters all fit, which then
+ * merges on chip: the combine kernel's cost grows with the rows it merges.  With at
+ * least one tile per SM it returns pgqa_choose_splits's count.  The rule was
+ * fitted to measured decode times over hd, kv heads and context lengths.
+ * Returns >= 1, PGQA_ERR_UNSUPPORTED_HD for another hd, or
+ * PGQA_ERR_INVALID_ARGUMENT unless nh and nkv are positive with nh % nkv == 0.
+ */
+int pgqa_choose_splits_ex(int kv_len_eff, int rows, int nkv, int nseq, int nh, int hd);
+
+/*
+ * pgqa_choose_splits_ex for an explicit device (pure host arithmetic): its SM
+ * count, the split kernel's resident CTAs per SM at hd, and how many clusters
+ * of 2, 4 and 8 of them can be resident at once.
+ */
+int pgqa_choose_splits_ex_for(int kv_len_eff, int rows, int nkv, int nseq, int nh, int hd, int num_sms,
+                              int ctas_per_sm, int clusters2, int clusters4, int clusters8);
+
+/*
  * Bytes of the `part` scratch (`attn::decode_part_bytes` of the test file):
  * rows * nh * splits * (hd + 2) * 4 (f32 O, running max and sum per split).
  */

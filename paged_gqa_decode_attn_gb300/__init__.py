@@ -5,7 +5,7 @@ this package only builds it, loads it and marshals arguments.  ``workloads``
 draws the seeded synthetic inputs used by the tests and the benchmark.
 """
 from ._lib import (MAX_SPLITS, PAGE_TOKENS, PgqaError, attn_decode, attn_decode_noalloc, attn_prefill,
-                   attn_prefill_split, choose_splits, decode_counter_count, decode_kernel_count, decode_part_bytes,
+                   attn_prefill_split, choose_splits, choose_splits_ex_for, decode_counter_count, decode_kernel_count, decode_part_bytes,
                    device_status, lib_path, load, make_tiles, prefill_rows_per_tile, prefill_split_count,
                    qk_norm_rope_write, selftest_bounded_wait, strerror, trace_buffer, version)
 from .builder import build
@@ -13,6 +13,6 @@ from .builder import build
 __all__ = ["attn_decode", "attn_decode_noalloc", "attn_prefill", "attn_prefill_split", "make_tiles", "prefill_rows_per_tile",
            "prefill_split_count",
            "qk_norm_rope_write",
-           "choose_splits", "decode_part_bytes", "decode_counter_count", "decode_kernel_count",
+           "choose_splits", "choose_splits_ex_for", "decode_part_bytes", "decode_counter_count", "decode_kernel_count",
            "device_status", "selftest_bounded_wait", "PgqaError", "build", "load", "lib_path", "strerror", "trace_buffer", "version",
            "PAGE_TOKENS", "MAX_SPLITS"]

@@ -29,6 +29,8 @@ SIGNATURES = {
     "pgqa_attn_decode": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P, _P]),
     "pgqa_choose_splits": (_I, [_I, _I, _I, _I]),
     "pgqa_choose_splits_for": (_I, [_I, _I, _I, _I, _I]),
+    "pgqa_choose_splits_ex": (_I, [_I, _I, _I, _I, _I, _I]),
+    "pgqa_choose_splits_ex_for": (_I, [_I, _I, _I, _I, _I, _I, _I, _I, _I, _I, _I]),
     "pgqa_decode_part_bytes": (ctypes.c_size_t, [_I, _I, _I, _I]),
     "pgqa_decode_counter_count": (ctypes.c_size_t, [_I, _I, _I]),
     "pgqa_decode_kernel_count": (_I, [_I, _I]),
@@ -194,10 +196,26 @@ def qk_norm_rope_write(q_out, k_pool, v_pool, q_in, k_in, v_in, q_weight, k_weig
         raise PgqaError(st, "qk_norm_rope_write")
 
 
-def choose_splits(kv_len_eff: int, rows: int, nkv: int, nseq: int, num_sms: int | None = None) -> int:
+def choose_splits(kv_len_eff: int, rows: int, nkv: int, nseq: int, num_sms: int | None = None,
+                  nh: int | None = None, hd: int | None = None) -> int:
+    """Splits per tile: ``pgqa_choose_splits`` (the page's arguments), or, given ``nh`` and ``hd``,
+    ``pgqa_choose_splits_ex`` (which knows how rows pack and the hd kernel's residency)."""
+    if nh is not None and hd is not None:
+        st = int(load().pgqa_choose_splits_ex(int(kv_len_eff), int(rows), int(nkv), int(nseq), int(nh), int(hd)))
+        if st < 1:
+            raise PgqaError(st, "choose_splits_ex")
+        return st
     if num_sms is None:
         return int(load().pgqa_choose_splits(int(kv_len_eff), int(rows), int(nkv), int(nseq)))
     return int(load().pgqa_choose_splits_for(int(kv_len_eff), int(rows), int(nkv), int(nseq), int(num_sms)))
+
+
+def choose_splits_ex_for(kv_len_eff: int, rows: int, nkv: int, nseq: int, nh: int, hd: int, num_sms: int,
+                         ctas_per_sm: int, clusters2: int, clusters4: int, clusters8: int) -> int:
+    """``pgqa_choose_splits_ex_for``: the same rule for an explicit device (host arithmetic only)."""
+    return int(load().pgqa_choose_splits_ex_for(int(kv_len_eff), int(rows), int(nkv), int(nseq), int(nh), int(hd),
+                                                int(num_sms), int(ctas_per_sm), int(clusters2), int(clusters4),
+                                                int(clusters8)))
 
 
 def decode_part_bytes(rows: int, nh: int, splits: int, hd: int) -> int:

@@ -37,6 +37,7 @@ struct DeviceState {
     bool prefill_attr_set[4] = {false, false, false, false};
     int cluster_cap[4][5] = {{-1, -1, -1, -1, -1}, {-1, -1, -1, -1, -1}, {-1, -1, -1, -1, -1},
                              {-1, -1, -1, -1, -1}};   // [hd][log2 cluster]: resident clusters, -1 unknown
+    int cps[4] = {-1, -1, -1, -1};   // [hd]: split CTAs resident per SM, -1 unknown
 };
 
 // Cluster size for the on-chip merge of `splits` CTAs, or 0 to merge through
@@ -501,7 +502,118 @@ int choose_splits_rule(int kv_len_eff, int rows, int nkv, int nseq, int num_sms,
     return static_cast<int>(s);
 }
 
+// The split rule with the kernel's shape known (pgqa_choose_splits_ex).  Every
+// sequence's rows pack into CTAs of max(1, 8 / g) rows (g = nh / nkv), so a
+// split has `tiles` CTAs.  With at least one tile per SM the grid is many
+// waves and the page-signature rule above stands.  With fewer, the count was
+// fitted to decode timings over hd {128, 256, 512} x nkv {2..32} x context
+// {1K..64K} on a GB300:
+//  * fill the GPU in one wave: one CTA per SM where one fits per SM (hd 256,
+//    512), about 2.5 per SM where three fit (hd 64, 128: each CTA's ring is
+//    then half an SM's, and more CTAs keep more bytes in flight);
+//  * but while a CTA's loop stays short -- at most kShortLoopBytes of K and V
+//    per two query rows the CTA serves, with the largest cluster size whose
+//    clusters all fit -- take that cluster size: its on-chip merge costs less
+//    than the combine kernel's second launch saves, and the combine kernel's
+//    share grows with the (row, head) pairs it merges (4 packed rows at g = 2
+//    took 11.6 us through it against 8.8 on chip, where one row was even).
+constexpr long long kShortLoopBytes = 128 * 1024;
+
+int choose_splits_ex_rule(int kv_len_eff, int rows, int nkv, int nseq, int nh, int hd, int num_sms, int cps,
+                          const int *clusters)
+{
+    if (kv_len_eff < 1)
+        kv_len_eff = 1;
+    if (rows < 1)
+        rows = 1;
+    if (nseq < 1 || nseq > rows)
+        nseq = rows;
+    if (num_sms < 1)
+        num_sms = 1;
+    if (cps < 1)
+        cps = 1;
+    const int g = nh / nkv;
+    const long long pack = g <= pgqa::kQRows ? pgqa::kQRows / g : 1;
+    const long long hsg = (g + pgqa::kQRows - 1) / pgqa::kQRows;
+    const long long per_seq = (rows + nseq - 1) / nseq;
+    const long long tiles = static_cast<long long>(nseq) * ((per_seq + pack - 1) / pack) * nkv * hsg;
+    if (tiles >= num_sms)
+        return choose_splits_rule(kv_len_eff, rows, nkv, nseq, num_sms, clusters);
+    const long long pages = (kv_len_eff + PGQA_PAGE_TOKENS - 1) / PGQA_PAGE_TOKENS;
+    const long long target = cps > 1 ? 5LL * num_sms / 2 : num_sms;
+    long long fill = target / tiles;
+    fill = std::min<long long>(fill, std::max<long long>(1, pages / 2));    // at least two pages per split
+    fill = std::max<long long>(1, std::min<long long>(fill, PGQA_MAX_SPLITS));
+    long long c = 1;                                                      // on-chip merge that fits
+    for (int lg = 1; lg <= 3; ++lg)
+        if ((1LL << lg) <= fill && clusters[lg] >= tiles)
+            c = 1LL << lg;
+    const long long qrows = std::min<long long>(pgqa::kQRows, std::min(per_seq, pack) * g);   // per CTA
+    long long s;
+    if (fill <= 8)
+        s = c > 1 ? c : fill;
+    else if (c > 1 && (pages + c - 1) / c * 64LL * hd <= kShortLoopBytes * std::max<long long>(1, qrows / 2))
+        s = c;
+    else
+        s = fill;
+    return static_cast<int>(s);
+}
+
+bool ex_args_ok(int nh, int nkv, int hd)
+{
+    return nh > 0 && nkv > 0 && nh % nkv == 0 && hd_index(hd) >= 0;
+}
+
 }  // namespace
+
+int pgqa_choose_splits_ex_for(int kv_len_eff, int rows, int nkv, int nseq, int nh, int hd, int num_sms,
+                              int ctas_per_sm, int clusters2, int clusters4, int clusters8)
+{
+    if (!ex_args_ok(nh, nkv, hd))
+        return hd_index(hd) < 0 ? PGQA_ERR_UNSUPPORTED_HD : PGQA_ERR_INVALID_ARGUMENT;
+    const int clusters[4] = {num_sms, clusters2, clusters4, clusters8};
+    return choose_splits_ex_rule(kv_len_eff, rows, nkv, nseq, nh, hd, num_sms, ctas_per_sm, clusters);
+}
+
+int pgqa_choose_splits_ex(int kv_len_eff, int rows, int nkv, int nseq, int nh, int hd)
+{
+    if (!ex_args_ok(nh, nkv, hd))
+        return hd_index(hd) < 0 ? PGQA_ERR_UNSUPPORTED_HD : PGQA_ERR_INVALID_ARGUMENT;
+    const int hi = hd_index(hd);
+    int sms = 0, cps = 0;
+    int clusters[4] = {};
+    {
+        std::lock_guard<std::mutex> lock(g_mutex);
+        DeviceState *s = nullptr;
+        const int st = device_state(&s);
+        if (st != PGQA_OK)
+            return st;
+        sms = s->num_sms;
+        if (s->cps[hi] < 0) {
+            switch (hd) {
+            case 64: s->cps[hi] = pgqa::ctas_per_sm_hd64(); break;
+            case 128: s->cps[hi] = pgqa::ctas_per_sm_hd128(); break;
+            case 256: s->cps[hi] = pgqa::ctas_per_sm_hd256(); break;
+            default: s->cps[hi] = pgqa::ctas_per_sm_hd512(); break;
+            }
+        }
+        cps = s->cps[hi];
+        clusters[0] = sms;
+        for (int lg = 1; lg <= 3; ++lg) {
+            int &cap = s->cluster_cap[hi][lg];
+            if (cap < 0) {
+                switch (hd) {
+                case 64: cap = pgqa::cluster_capacity_hd64(1 << lg); break;
+                case 128: cap = pgqa::cluster_capacity_hd128(1 << lg); break;
+                case 256: cap = pgqa::cluster_capacity_hd256(1 << lg); break;
+                default: cap = pgqa::cluster_capacity_hd512(1 << lg); break;
+                }
+            }
+            clusters[lg] = cap;
+        }
+    }
+    return choose_splits_ex_rule(kv_len_eff, rows, nkv, nseq, nh, hd, sms, cps, clusters);
+}
 
 int pgqa_choose_splits_for(int kv_len_eff, int rows, int nkv, int nseq, int num_sms)
 {

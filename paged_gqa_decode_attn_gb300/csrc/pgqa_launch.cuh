@@ -108,6 +108,23 @@ int cluster_capacity(int cluster)
     return n;
 }
 
+// Split CTAs (of the cluster-launch shape, the larger shared memory) that can
+// be resident on one SM at once.  Also sets the kernel's attributes.
+template <int HD>
+int ctas_per_sm()
+{
+    if (cudaFuncSetAttribute(decode_split_kernel<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             Smem<HD>::kAllocCluster) != cudaSuccess)
+        return 0;
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_split_kernel<HD>, Geo<HD>::kThreads,
+                                                      Smem<HD>::kAllocCluster) != cudaSuccess) {
+        cudaGetLastError();
+        return 0;
+    }
+    return n;
+}
+
 cudaError_t launch_combine_hd64(const DecodeParams &p, cudaStream_t stream);
 cudaError_t launch_combine_hd128(const DecodeParams &p, cudaStream_t stream);
 cudaError_t launch_combine_hd256(const DecodeParams &p, cudaStream_t stream);
@@ -116,6 +133,10 @@ int cluster_capacity_hd64(int cluster);
 int cluster_capacity_hd128(int cluster);
 int cluster_capacity_hd256(int cluster);
 int cluster_capacity_hd512(int cluster);
+int ctas_per_sm_hd64();
+int ctas_per_sm_hd128();
+int ctas_per_sm_hd256();
+int ctas_per_sm_hd512();
 
 cudaError_t launch_decode_hd64(const LaunchArgs &a, bool set_attr);
 cudaError_t launch_decode_hd128(const LaunchArgs &a, bool set_attr);

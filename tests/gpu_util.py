@@ -99,7 +99,7 @@ class DevCase:
         if splits is None:
             rows = case.rows
             nseq = len(set(int(x) for x in case.off))
-            splits = pgqa.choose_splits(case.kv_len_eff(), rows, case.nkv, nseq)
+            splits = pgqa.choose_splits(case.kv_len_eff(), rows, case.nkv, nseq, nh=case.nh, hd=case.hd)
         self.splits = splits
         self.part = torch.zeros(max(1, pgqa.decode_part_bytes(case.rows, case.nh, splits, case.hd)) // 4 + 4,
                                 dtype=torch.float32, device=device)

@@ -147,6 +147,50 @@ def test_choose_splits_rule(lib):
     assert pgqa.choose_splits(32768, 1, 4, 1) >= 1
 
 
+def test_choose_splits_ex_rule(lib):
+    """The head-aware rule on a 152-SM GB300 (one CTA per SM and 76/36/15 clusters of 2/4/8 at hd 256 and
+    512; three per SM at hd 64 and 128, with three times the clusters), against its statement in pgqa.h."""
+    d1 = dict(num_sms=152, ctas_per_sm=1, clusters2=76, clusters4=36, clusters8=15)
+    d3 = dict(num_sms=152, ctas_per_sm=3, clusters2=228, clusters4=108, clusters8=45)
+    f = pgqa.choose_splits_ex_for
+    # the named workloads keep their counts
+    assert f(1024, 4, 8, 1, 16, 256, **d1) == 8          # sliding: 8 pages a CTA, on chip
+    assert f(32768, 1, 4, 1, 32, 512, **d1) == 38        # long: fills 152 SMs, combine kernel
+    assert f(256, 1, 2, 1, 8, 128, **d3) == 8            # tiny: capped at two pages per split
+    assert f(4096, 64, 8, 64, 32, 128, **d3) == 2        # batched: many tiles, the page-signature rule
+    assert f(4096, 64, 8, 64, 32, 128, **d3) == pgqa.choose_splits(4096, 64, 8, 64, num_sms=152)
+    # rows of one sequence pack: 4 rows at g = 2 launch the CTAs one row does (and long loops take the same count)
+    for hd, d in ((128, d3), (256, d1), (512, d1)):
+        assert f(65536, 4, 16, 1, 32, hd, **d) == f(65536, 1, 16, 1, 32, hd, **d)
+    # long loops fill the GPU in one wave: one CTA per SM at hd 256 and 512, ~2.5 per SM at hd 128
+    for nkv in (2, 4, 8, 16, 32):
+        assert f(65536, 1, nkv, 1, 2 * nkv, 256, **d1) == 152 // nkv
+        assert f(65536, 1, nkv, 1, 2 * nkv, 512, **d1) == 152 // nkv
+        assert f(65536, 1, nkv, 1, 2 * nkv, 128, **d3) == min(380 // nkv, 256)
+    # a short loop (each CTA <= 128 KB of K and V with the largest cluster that fits) merges on chip
+    assert f(1024, 1, 8, 1, 16, 256, **d1) == 8           # 8 pages x 16 KB
+    assert f(1024, 1, 16, 1, 32, 128, **d3) == 8          # 8 pages x 8 KB; 16 clusters of 8 fit at 3 per SM
+    assert f(1024, 1, 16, 1, 32, 256, **d1) == 9          # 16 clusters of 8 do not fit; 4 leaves 256 KB
+    assert f(4096, 1, 8, 1, 16, 256, **d1) == 19          # 32 pages x 16 KB > 128 KB
+    # the budget grows with the query rows a CTA serves: 4 packed rows x g = 2 -> 8 rows -> 512 KB
+    assert f(1024, 4, 16, 1, 32, 256, **d1) == 4          # 16 pages x 16 KB on chip, not 9 through the combine
+    assert f(1024, 4, 16, 1, 32, 512, **d1) == 4          # 16 pages x 32 KB
+    assert f(4096, 4, 16, 1, 32, 256, **d1) == 9          # 64 pages x 16 KB = 1 MB > 512 KB
+    # bounds: >= 1, at least two pages per split, at most PGQA_MAX_SPLITS; every g and group size
+    for hd, d in ((64, d3), (128, d3), (256, d1), (512, d1)):
+        for kv in (1, 16, 100, 1024, 1 << 20):
+            for rows, nseq in ((1, 1), (4, 1), (16, 1), (16, 16), (64, 64)):
+                for nkv, nh in ((1, 1), (2, 16), (8, 8), (4, 96), (16, 32)):
+                    s = f(kv, rows, nkv, nseq, nh, hd, **d)
+                    pages = (kv + 15) // 16
+                    assert 1 <= s <= pgqa.MAX_SPLITS and (s == 1 or s <= pages // 2), (hd, kv, rows, nkv, nh, s)
+    # arguments the rule cannot take
+    from paged_gqa_decode_attn_gb300 import _lib
+    assert f(1024, 1, 2, 1, 8, 96, **d1) == _lib.PGQA_ERR_UNSUPPORTED_HD
+    assert f(1024, 1, 3, 1, 8, 128, **d1) == _lib.PGQA_ERR_INVALID_ARGUMENT
+    assert f(1024, 1, 0, 1, 8, 128, **d1) == _lib.PGQA_ERR_INVALID_ARGUMENT
+
+
 def test_prefill_split_count(lib):
     """One wave of live items over the SMs (152 without a device), at least two 64-token blocks a split."""
     assert pgqa.prefill_split_count(65536, 16, 1, 32, 16) == 152 // 16     # 16 rows of one sequence: 16 items
