@@ -923,7 +923,8 @@ def run_multirow(args, case, rank, world, dist):
     bpc = case.algorithmic_bytes()
     t0_h, tn_h = pgqa.make_tiles(np.asarray(case.off, np.int32), pgqa.prefill_rows_per_tile(case.hd))
     ntiles = len(t0_h)
-    splits = args.splits or pgqa.prefill_split_count(case.kv_len_eff(), case.rows, ntiles, case.nh, case.nkv)
+    splits = args.splits or pgqa.prefill_split_count(case.kv_len_eff(), case.rows, ntiles, case.nh, case.nkv,
+                                                     hd=case.hd)
     pool_bytes = case.k_pool.nbytes + case.v_pool.nbytes
     copies = args.copies or max(2, math.ceil(3 * L2_BYTES / max(bpc, 1)))
     copies = min(copies, max(2, int(0.25 * torch.cuda.get_device_properties(dev).total_memory // pool_bytes)))
@@ -1236,7 +1237,7 @@ def run_sweep(args, rank, world, dist):
                         t0_h, tn_h = pgqa.make_tiles(np.zeros(rows, np.int32), pgqa.prefill_rows_per_tile(hd))
                         t0 = torch.from_numpy(t0_h).to(dev)
                         tn = torch.from_numpy(tn_h).to(dev)
-                        splits = pgqa.prefill_split_count(kv_eff, rows, len(t0_h), nh, nkv)
+                        splits = pgqa.prefill_split_count(kv_eff, rows, len(t0_h), nh, nkv, hd=hd)
                     else:
                         splits = pgqa.choose_splits(kv_eff, rows, nkv, 1, nh=nh, hd=hd)
                     part = torch.empty(max(1, pgqa.decode_part_bytes(rows, nh, splits, hd)) // 4 + 4,

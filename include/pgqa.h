@@ -299,6 +299,17 @@ int pgqa_attn_prefill_split(void *o, void *part, const void *q, const void *k_po
  */
 int pgqa_prefill_split_count(int kv_len_eff, int rows, int ntiles, int nh, int nkv);
 
+/*
+ * pgqa_prefill_split_count with the head dimension known (no counterpart in the
+ * pages).  At hd 512 a work item runs on a CTA pair, and fewer pairs than SMs
+ * are resident at once: while each split keeps at most 32 64-token blocks, the
+ * count is the one wave of resident pairs allows (a second wave doubled short
+ * calls); otherwise, and at every other hd, it is pgqa_prefill_split_count's.
+ * PGQA_ERR_UNSUPPORTED_HD for another hd, and pgqa_prefill_split_count's
+ * errors.
+ */
+int pgqa_prefill_split_count_ex(int kv_len_eff, int rows, int ntiles, int nh, int nkv, int hd);
+
 /* The longest tile pgqa_attn_prefill takes at head dimension hd (128 rows at
  * every supported hd), or PGQA_ERR_UNSUPPORTED_HD. */
 int pgqa_prefill_rows_per_tile(int hd);

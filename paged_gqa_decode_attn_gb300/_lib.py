@@ -44,6 +44,7 @@ SIGNATURES = {
     "pgqa_attn_prefill_split": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I,
                                      _P, _P]),
     "pgqa_prefill_split_count": (_I, [_I, _I, _I, _I, _I]),
+    "pgqa_prefill_split_count_ex": (_I, [_I, _I, _I, _I, _I, _I]),
     "pgqa_prefill_rows_per_tile": (_I, [_I]),
     "pgqa_make_tiles": (_I, [_P, _I, _I, _P, _P, _I]),
     "pgqa_qk_norm_rope_write": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I,
@@ -152,8 +153,13 @@ def attn_prefill_split(o, part, q, k_pool, v_pool, block_table, off, qpos, kvpos
         raise PgqaError(st, "attn_prefill_split")
 
 
-def prefill_split_count(kv_len_eff: int, rows: int, ntiles: int, nh: int, nkv: int) -> int:
-    n = int(load().pgqa_prefill_split_count(int(kv_len_eff), int(rows), int(ntiles), int(nh), int(nkv)))
+def prefill_split_count(kv_len_eff: int, rows: int, ntiles: int, nh: int, nkv: int, hd: int | None = None) -> int:
+    """``pgqa_prefill_split_count``, or with ``hd`` given ``pgqa_prefill_split_count_ex``."""
+    if hd is None:
+        n = int(load().pgqa_prefill_split_count(int(kv_len_eff), int(rows), int(ntiles), int(nh), int(nkv)))
+    else:
+        n = int(load().pgqa_prefill_split_count_ex(int(kv_len_eff), int(rows), int(ntiles), int(nh), int(nkv),
+                                                   int(hd)))
     if n < 0:
         raise PgqaError(n, "prefill_split_count")
     return n

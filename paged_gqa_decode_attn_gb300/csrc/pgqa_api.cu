@@ -995,6 +995,30 @@ int pgqa_prefill_split_count(int kv_len_eff, int rows, int ntiles, int nh, int n
     return static_cast<int>(std::min<long long>(s, PGQA_MAX_SPLITS));
 }
 
+int pgqa_prefill_split_count_ex(int kv_len_eff, int rows, int ntiles, int nh, int nkv, int hd)
+{
+    const int base = pgqa_prefill_split_count(kv_len_eff, rows, ntiles, nh, nkv);
+    if (base < 1 || hd != 512)
+        return base < 1 ? base : (hd_index(hd) < 0 ? PGQA_ERR_UNSUPPORTED_HD : base);
+    // At hd 512 a work item takes a CTA pair, and only so many pairs are
+    // resident: beyond one wave of them a second wave doubles a short call.
+    // While each split keeps at most 32 blocks, size the splits to one wave.
+    int pairs = 0;
+    {
+        std::lock_guard<std::mutex> lock(g_mutex);
+        DeviceState *s = nullptr;
+        if (device_state(&s) == PGQA_OK)
+            pairs = pgqa::prefill_pair_capacity_hd512();
+    }
+    const long long tile_rows = std::min<long long>((rows + ntiles - 1) / ntiles, 128);
+    const long long items = static_cast<long long>(ntiles) * nkv * ((tile_rows * (nh / nkv) + 127) / 128);
+    const long long one_wave = std::max<long long>(1, pairs / items);
+    const long long blocks = (kv_len_eff + 63) / 64;
+    if (pairs > 0 && one_wave < base && (blocks + one_wave - 1) / one_wave <= 32)
+        return static_cast<int>(one_wave);
+    return base;
+}
+
 int pgqa_attn_prefill_split(void *o, void *part, const void *q, const void *k_pool, const void *v_pool,
                             const int32_t *block_table, const int32_t *off, const int32_t *qpos,
                             const int32_t *kvpos, const int32_t *tile_t0, const int32_t *tile_tn, int ntiles,

@@ -69,5 +69,7 @@ cudaError_t launch_prefill_hd64(const PrefillLaunchArgs &a, bool set_attr);
 cudaError_t launch_prefill_hd128(const PrefillLaunchArgs &a, bool set_attr);
 cudaError_t launch_prefill_hd256(const PrefillLaunchArgs &a, bool set_attr);
 cudaError_t launch_prefill_hd512(const PrefillLaunchArgs &a, bool set_attr);
+// CTA pairs of the hd-512 kernel that can be resident at once on the current device (0: none).
+int prefill_pair_capacity_hd512();
 
 }  // namespace pgqa

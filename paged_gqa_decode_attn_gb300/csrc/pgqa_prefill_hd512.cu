@@ -5,4 +5,11 @@
 
 namespace pgqa {
 cudaError_t launch_prefill_hd512(const PrefillLaunchArgs &a, bool set_attr) { return launch_prefill_tc<512>(a, set_attr); }
+int prefill_pair_capacity_hd512()
+{
+    if (cudaFuncSetAttribute(prefill_tc_kernel<512, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             TcGeo<512>::kAlloc) != cudaSuccess)
+        return 0;
+    return prefill_tc_pair_capacity<512>();
+}
 }  // namespace pgqa

@@ -191,6 +191,19 @@ def test_choose_splits_ex_rule(lib):
     assert f(1024, 1, 0, 1, 8, 128, **d1) == _lib.PGQA_ERR_INVALID_ARGUMENT
 
 
+def test_prefill_split_count_ex_errors_and_other_head_dims(lib):
+    """The hd form is the base count at hd 64, 128 and 256 (it asks the device only at hd 512), and rejects
+    other head dims and the base count's bad sizes."""
+    from paged_gqa_decode_attn_gb300 import _lib
+    for hd in (64, 128, 256):
+        for kv in (100, 1024, 65536):
+            assert pgqa.prefill_split_count(kv, 16, 1, 32, 16, hd=hd) == pgqa.prefill_split_count(kv, 16, 1, 32, 16)
+    with pytest.raises(pgqa.PgqaError):
+        pgqa.prefill_split_count(1024, 16, 1, 32, 16, hd=96)
+    assert pgqa.load().pgqa_prefill_split_count_ex(1024, 16, 1, 32, 16, 96) == _lib.PGQA_ERR_UNSUPPORTED_HD
+    assert pgqa.load().pgqa_prefill_split_count_ex(1024, 16, 1, 32, 5, 128) == _lib.PGQA_ERR_INVALID_ARGUMENT
+
+
 def test_prefill_split_count(lib):
     """One wave of live items over the SMs (152 without a device), at least two 64-token blocks a split."""
     assert pgqa.prefill_split_count(65536, 16, 1, 32, 16) == 152 // 16     # 16 rows of one sequence: 16 items

@@ -192,7 +192,7 @@ def test_sweep_rows16_points_on_the_tiled_split_path(pt):
     c = wl.sweep(*pt, mapped=True)
     assert rows * (c.nh // c.nkv) > 8
     t0, _ = pgqa.make_tiles(np.zeros(rows, np.int32), pgqa.prefill_rows_per_tile(hd))
-    splits = pgqa.prefill_split_count(c.kv_len_eff(), rows, len(t0), c.nh, c.nkv)
+    splits = pgqa.prefill_split_count(c.kv_len_eff(), rows, len(t0), c.nh, c.nkv, hd=c.hd)
     assert splits > 1
     check_parity(c, run_split(c, splits), f"{c.name} splits {splits}", tiled=True)
 
