@@ -136,8 +136,9 @@ int pgqa_choose_splits_for(int kv_len_eff, int rows, int nkv, int nseq, int num_
  * the hd kernel's CTAs and clusters can be resident at once.  With fewer tiles
  * than SMs it fills the GPU in one wave -- one CTA per SM at hd 256 and 512,
  * about 2.5 per SM at hd 64 and 128, whose CTAs are a third of an SM -- unless
- * each CTA's share of K and V stays within 128 KB per two query rows it serves
- * (q = min(8, rows packed per CTA x nh / nkv); 128 KB x max(1, q / 2)) with
+ * each CTA's share of K and V stays within 16 pages and 128 KB per two query
+ * rows it serves (q = min(8, rows packed per CTA x nh / nkv); 128 KB x
+ * max(1, q / 2)) with
  * the largest cluster size (2, 4 or 8) whose clusters all fit, which then
  * merges on chip: the combine kernel's cost grows with the rows it merges.  With at
  * least one tile per SM it returns pgqa_choose_splits's count.  The rule was

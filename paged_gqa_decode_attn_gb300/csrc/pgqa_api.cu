@@ -518,6 +518,10 @@ int choose_splits_rule(int kv_len_eff, int rows, int nkv, int nseq, int num_sms,
 //    share grows with the (row, head) pairs it merges (4 packed rows at g = 2
 //    took 11.6 us through it against 8.8 on chip, where one row was even).
 constexpr long long kShortLoopBytes = 128 * 1024;
+// ... and at most 16 pages: at hd 128 a one-CTA-per-SM cluster grid keeps
+// fewer bytes in flight per SM than the fill (4 rows over 256 pages: 12.9 us
+// on chip against 11.8 through the combine kernel).
+constexpr long long kShortLoopPages = 16;
 
 int choose_splits_ex_rule(int kv_len_eff, int rows, int nkv, int nseq, int nh, int hd, int num_sms, int cps,
                           const int *clusters)
@@ -552,7 +556,8 @@ int choose_splits_ex_rule(int kv_len_eff, int rows, int nkv, int nseq, int nh, i
     long long s;
     if (fill <= 8)
         s = c > 1 ? c : fill;
-    else if (c > 1 && (pages + c - 1) / c * 64LL * hd <= kShortLoopBytes * std::max<long long>(1, qrows / 2))
+    else if (c > 1 && (pages + c - 1) / c <= kShortLoopPages &&
+             (pages + c - 1) / c * 64LL * hd <= kShortLoopBytes * std::max<long long>(1, qrows / 2))
         s = c;
     else
         s = fill;

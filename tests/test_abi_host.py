@@ -176,6 +176,8 @@ def test_choose_splits_ex_rule(lib):
     assert f(1024, 4, 16, 1, 32, 256, **d1) == 4          # 16 pages x 16 KB on chip, not 9 through the combine
     assert f(1024, 4, 16, 1, 32, 512, **d1) == 4          # 16 pages x 32 KB
     assert f(4096, 4, 16, 1, 32, 256, **d1) == 9          # 64 pages x 16 KB = 1 MB > 512 KB
+    assert f(4096, 4, 16, 1, 32, 128, **d3) == 23         # 32 pages: more than 16 a CTA, though 256 KB
+    assert f(1024, 4, 16, 1, 32, 128, **d3) == 8          # 8 pages
     # bounds: >= 1, at least two pages per split, at most PGQA_MAX_SPLITS; every g and group size
     for hd, d in ((64, d3), (128, d3), (256, d1), (512, d1)):
         for kv in (1, 16, 100, 1024, 1 << 20):
