@@ -16,9 +16,10 @@
 // item's vectors -- contiguous runs of q_in, k_in, v_in -- with bulk copies
 // that complete on the stage's full barrier, after writing the row's slot
 // (pos, page) and its norm-and-rotation table into the stage.  Consumers work
-// the vectors out of shared memory, each warp a contiguous run of them, one
-// vector at a time with lane l holding dims [E l, E l + E), E = hd / 32,
-// store them and release the stage.
+// the vectors out of shared memory, each warp a contiguous run of them, up to
+// four of one kind side by side (so that their shuffle chains overlap) with
+// lane l holding dims [E l, E l + E), E = hd / 32, store them and release the
+// stage.
 //
 // Norm and rotation fold into the table: with rs = 1/sqrt(mean x^2 + eps)
 // common to the vector, dim d becomes rs (x_d A_d + x_p B_d), p the partner
@@ -246,12 +247,71 @@ __device__ void prep_producer(const PrepParams &p, unsigned char *smem, uint32_t
     }
 }
 
+// NV head vectors of one kind, consecutive in the stage, worked side by side
+// so that their dependent chains (the sum-of-squares shuffles, rsqrt, the
+// partner shuffles) overlap.  Vector j goes to dst + j * dst_stride.  Each
+// vector's arithmetic and its order are those of a vector worked alone.
+template <int HD, int NV>
+__device__ __forceinline__ void norm_rotate(const __nv_bfloat16 *src, __nv_bfloat16 *dst, size_t dst_stride,
+                                            const float4 (&tab)[HD / 64], bool scale, float eps, int src_lane)
+{
+    constexpr int E = HD / 32;
+    constexpr int kPairs = E / 2;
+    Packed<E> in[NV];
+#pragma unroll
+    for (int j = 0; j < NV; ++j)
+        load_packed<E>(src + j * HD, in[j]);
+    // the f32 values are re-derived from the packed words where they are
+    // used (a shift or a mask): keeping them would double the registers
+    float ss[NV];
+#pragma unroll
+    for (int j = 0; j < NV; ++j) {
+        float2 acc = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int w = 0; w < kPairs; ++w) {
+            const float2 x = make_float2(bf16_lo(in[j].w[w]), bf16_hi(in[j].w[w]));
+            acc = __ffma2_rn(x, x, acc);
+        }
+        ss[j] = acc.x + acc.y;
+    }
+    uint32_t yw[NV][kPairs];
+#pragma unroll
+    for (int j = 0; j < NV; ++j)
+#pragma unroll
+        for (int w = 0; w < kPairs; ++w)
+            yw[j][w] = __shfl_sync(0xffffffffu, in[j].w[w], src_lane);
+#pragma unroll
+    for (int m = 16; m; m >>= 1)
+#pragma unroll
+        for (int j = 0; j < NV; ++j)
+            ss[j] += __shfl_xor_sync(0xffffffffu, ss[j], m);
+#pragma unroll
+    for (int j = 0; j < NV; ++j) {
+        const float rs = scale ? rsqrtf(ss[j] * (1.0f / HD) + eps) : 1.0f;
+        const float2 rs2 = make_float2(rs, rs);
+        Packed<E> out;
+#pragma unroll
+        for (int w = 0; w < kPairs; ++w) {
+            const float2 x = make_float2(bf16_lo(in[j].w[w]), bf16_hi(in[j].w[w]));
+            float2 u = __fmul2_rn(x, make_float2(tab[w].x, tab[w].y));
+            u = __ffma2_rn(make_float2(bf16_lo(yw[j][w]), bf16_hi(yw[j][w])), make_float2(tab[w].z, tab[w].w), u);
+            u = __fmul2_rn(u, rs2);
+            const __nv_bfloat162 t = __floats2bfloat162_rn(u.x, u.y);
+            out.w[w] = *reinterpret_cast<const uint32_t *>(&t);
+        }
+        store_packed<E>(dst + j * dst_stride, out);
+    }
+}
+
 template <int HD>
 __device__ void prep_consumer(const PrepParams &p, const unsigned char *smem, uint32_t bar_full,
                               uint32_t bar_empty, int my_items)
 {
     constexpr int E = HD / 32;
     constexpr int kPairs = E / 2;
+    // vectors worked side by side at most (hd 512 keeps one: more would not
+    // fit the registers of two CTAs per SM)
+    constexpr int kNv = HD <= 256 ? 4 : 1;
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int d0 = E * lane;
@@ -284,9 +344,7 @@ __device__ void prep_consumer(const PrepParams &p, const unsigned char *smem, ui
         const int wb = min(vb, wa + cnt);
         int tab_kind = -1;
         float4 tab[kPairs];
-        for (int v = wa; v < wb; ++v) {
-            Packed<E> in;
-            load_packed<E>(reinterpret_cast<const __nv_bfloat16 *>(data) + (v - va) * HD + d0, in);
+        for (int v = wa; v < wb;) {
             const int kind = v < p.nh ? 0 : (v < p.nh + p.nkv ? 1 : 2);
             if (kind != tab_kind) {
                 const float4 *t = reinterpret_cast<const float4 *>(st) + (kind == 0 ? 0 : 32 * kPairs) + lane;
@@ -295,37 +353,30 @@ __device__ void prep_consumer(const PrepParams &p, const unsigned char *smem, ui
                     tab[w] = kind == 2 ? make_float4(1.f, 1.f, 0.f, 0.f) : t[32 * w];
                 tab_kind = kind;
             }
-            float2 x[kPairs];
-            float2 acc = make_float2(0.f, 0.f);
-#pragma unroll
-            for (int w = 0; w < kPairs; ++w) {
-                x[w] = make_float2(bf16_lo(in.w[w]), bf16_hi(in.w[w]));
-                acc = __ffma2_rn(x[w], x[w], acc);
-            }
-            float ss = acc.x + acc.y;
-#pragma unroll
-            for (int m = 16; m; m >>= 1)
-                ss += __shfl_xor_sync(0xffffffffu, ss, m);
-            const float rs = (kind == 2 && !p.norm_v) ? 1.0f : rsqrtf(ss * (1.0f / HD) + p.eps);
-            const float2 rs2 = make_float2(rs, rs);
-            Packed<E> out;
-#pragma unroll
-            for (int w = 0; w < kPairs; ++w) {
-                const uint32_t yw = __shfl_sync(0xffffffffu, in.w[w], src_lane);
-                float2 u = __fmul2_rn(x[w], make_float2(tab[w].x, tab[w].y));
-                u = __ffma2_rn(make_float2(bf16_lo(yw), bf16_hi(yw)), make_float2(tab[w].z, tab[w].w), u);
-                u = __fmul2_rn(u, rs2);
-                const __nv_bfloat162 t = __floats2bfloat162_rn(u.x, u.y);
-                out.w[w] = *reinterpret_cast<const uint32_t *>(&t);
-            }
+            // the run of this kind left to the warp
+            const int kind_end = min(wb, kind == 0 ? p.nh : (kind == 1 ? p.nh + p.nkv : nvec));
+            const __nv_bfloat16 *src = reinterpret_cast<const __nv_bfloat16 *>(data) + (v - va) * HD + d0;
+            const bool scale = !(kind == 2 && !p.norm_v);
             __nv_bfloat16 *dst;
-            if (kind == 0)
+            size_t stride = static_cast<size_t>(16) * HD;
+            if (kind == 0) {
                 dst = p.q_out + (static_cast<size_t>(r) * p.nh + v) * HD + d0;
-            else if (kind == 2)
+                stride = HD;
+            } else if (kind == 2) {
                 dst = p.v_pool + slot + static_cast<size_t>(v - p.nh - p.nkv) * 16 * HD;
-            else
+            } else {
                 dst = p.k_pool + slot + static_cast<size_t>(v - p.nh) * 16 * HD;
-            store_packed<E>(dst, out);
+            }
+            if (kNv >= 4 && v + 4 <= kind_end) {
+                norm_rotate<HD, (kNv >= 4 ? 4 : 1)>(src, dst, stride, tab, scale, p.eps, src_lane);
+                v += 4;
+            } else if (kNv >= 2 && v + 2 <= kind_end) {
+                norm_rotate<HD, (kNv >= 2 ? 2 : 1)>(src, dst, stride, tab, scale, p.eps, src_lane);
+                v += 2;
+            } else {
+                norm_rotate<HD, 1>(src, dst, stride, tab, scale, p.eps, src_lane);
+                v += 1;
+            }
         }
         __syncwarp();
         if (lane == 0)
