@@ -154,12 +154,19 @@ __device__ void prep_producer(const PrepParams &p, unsigned char *smem, uint32_t
     const bool low = d0 < half, high = !low && d0 < p.rotary_dim;
     const int pd0 = low ? d0 + half : (high ? d0 - half : d0);
     // this lane's weights and its rotation partners' (the table of lane l
-    // serves consumer lane l)
+    // serves consumer lane l); at hd 512 they are read again for every item
+    // (from L1), since holding them beside the frequencies would not fit the
+    // registers of two CTAs per SM
+    constexpr bool kHoldWeights = HD <= 256;
     Packed<E> wq, wk, pq, pk;
-    load_packed<E>(p.q_weight + d0, wq);
-    load_packed<E>(p.k_weight + d0, wk);
-    load_packed<E>(p.q_weight + pd0, pq);
-    load_packed<E>(p.k_weight + pd0, pk);
+    auto load_weights = [&]() {
+        load_packed<E>(p.q_weight + d0, wq);
+        load_packed<E>(p.k_weight + d0, wk);
+        load_packed<E>(p.q_weight + pd0, pq);
+        load_packed<E>(p.k_weight + pd0, pk);
+    };
+    if constexpr (kHoldWeights)
+        load_weights();
     // this lane's frequencies, read once: a parameter read with a per-lane
     // index is serialised across the warp
     float2 g[E];
@@ -198,6 +205,8 @@ __device__ void prep_producer(const PrepParams &p, unsigned char *smem, uint32_t
             float4 *tq = reinterpret_cast<float4 *>(st) + lane;
             float4 *tk = tq + 32 * kPairs;
             const float fpos = static_cast<float>(pos);
+            if constexpr (!kHoldWeights)
+                load_weights();
 #pragma unroll
             for (int w = 0; w < kPairs; ++w) {
                 const float wq0 = bf16_lo(wq.w[w]), wq1 = bf16_hi(wq.w[w]);
