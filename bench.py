@@ -380,9 +380,10 @@ def run_of(args, case, splits):
 
 class DecodeRig:
     """One decode workload resident on the device, ready to call: rotating pool
-    copies (each copy's reads > 3x L2 apart, so every call reads KV from HBM),
-    the per-step inputs in one pinned host buffer and one device buffer, scratch
-    and counters."""
+    copies (each copy's reads > 3x L2 apart, so every call reads KV from HBM; and
+    more copies than the streams of the concurrent and end-to-end runs, so calls
+    in flight at once read different copies), the per-step inputs in one pinned
+    host buffer and one device buffer, scratch and counters."""
 
     def __init__(self, args, case, dev, splits=None, copies=None):
         import torch
@@ -392,7 +393,7 @@ class DecodeRig:
         self.splits = splits or args.splits or pgqa.choose_splits(case.kv_len_eff(), case.rows, case.nkv,
                                                                    nseq_of(case), nh=case.nh, hd=case.hd)
         self.pool_bytes = case.k_pool.nbytes + case.v_pool.nbytes
-        n = max(2, math.ceil(3 * L2_BYTES / max(self.bpc, 1)))
+        n = max(2, math.ceil(3 * L2_BYTES / max(self.bpc, 1)), getattr(args, "e2e_streams", 1) + 2)
         n = min(n, max(2, int(0.25 * torch.cuda.get_device_properties(dev).total_memory // self.pool_bytes)))
         self.copies = copies or args.copies or n
 
@@ -525,6 +526,55 @@ class DecodeRig:
             ts.append(ev0.elapsed_time(ev1) * 1e3)
         return statistics.median(ts)
 
+    def time_streams(self, steps, nstreams, reps=3):
+        """us per call of ``steps`` independent calls taken in turn by ``nstreams``
+        streams, each with its own output, scratch and counters (inputs resident, the
+        pool copies rotating as in time_steps): one CUDA graph forked from and joined
+        back to the timing stream, CUDA events around its replay on that stream, the
+        median of ``reps`` regions.  Calls on different streams do not wait for each
+        other, so several run at once; the line's value is the one-stream period."""
+        import torch
+        sets = [(self.o, self.part, self.cnt)] + [
+            (torch.empty_like(self.o), torch.empty_like(self.part), torch.zeros_like(self.cnt))
+            for _ in range(nstreams - 1)]
+        streams = [torch.cuda.Stream() for _ in range(nstreams)]
+        c = self.case
+
+        def call_on(i, b, s):
+            import paged_gqa_decode_attn_gb300 as pgqa
+            o, part, cnt = b
+            pgqa.attn_decode(o, part, self.q, self.ks[i % self.copies], self.vs[i % self.copies], self.bt,
+                             self.off, self.qpos, self.kvpos, c.rows, c.nh, c.nkv, c.hd, c.window, self.splits,
+                             cnt if self.counters is not None else None, self.pm, s)
+
+        cap = torch.cuda.Stream()
+        for k, b in enumerate(sets):
+            call_on(k, b, cap)
+        cap.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=cap):
+            for st in streams:
+                st.wait_stream(cap)
+            for i in range(steps):
+                call_on(i, sets[i % nstreams], streams[i % nstreams])
+            for st in streams:
+                cap.wait_stream(st)
+        g.replay()
+        torch.cuda.synchronize()
+        out = []
+        for _ in range(reps):
+            ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            torch.cuda.synchronize()
+            with torch.cuda.stream(cap):
+                torch.cuda._sleep(200000)
+                ev0.record(cap)
+                g.replay()
+                ev1.record(cap)
+            ev1.synchronize()
+            out.append(ev0.elapsed_time(ev1) * 1e3 / steps)
+        del g
+        return statistics.median(out)
+
     def time_repeats(self, steps, chunk, reps=5):
         """us per call of ``reps`` more timed regions of ``steps`` calls each (the
         graphs of time_steps, already captured): their median and each value."""
@@ -582,30 +632,31 @@ class DecodeRig:
                          b["off"], b["qpos"], self.kvpos, c.rows, c.nh, c.nkv, c.hd, c.window, self.splits,
                          b["cnt"] if self.counters is not None else None, self.pm, stream)
 
-    def time_e2e(self, steps, dist=None):
+    def time_e2e(self, steps, dist=None, nstreams=2):
         """End to end through the public API from pinned host memory: per step one
         host->device copy of the step's inputs, the call, and one device->host copy of
-        o.  The timed run is one CUDA graph of `steps` such steps, alternating between
-        two streams and two sets of buffers, so one step's copies overlap the other's
-        kernel (the steps are independent batches).  Also reported: the same steps
-        issued eagerly one after another on one stream, and the host cost of each
-        part enqueued alone."""
+        o.  The timed run is one CUDA graph of `steps` such steps, taken in turn by
+        `nstreams` streams, each with its own set of buffers, so one step's copies
+        overlap other steps' kernels (the steps are independent batches).  Also
+        reported: the same steps issued eagerly one after another on one stream, and
+        the host cost of each part enqueued alone."""
         import torch
         mine = {"dev_in": self.dev_in, "part": self.part, "cnt": self.cnt, "o": self.o, "o_h": self.o_h,
                 "q": self.q, "qpos": self.qpos, "off": self.off, "bt": self.bt}
-        sets = [mine, self._step_buffers()]
-        streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+        sets = [mine] + [self._step_buffers() for _ in range(nstreams - 1)]
+        streams = [torch.cuda.Stream() for _ in range(nstreams)]
         g = torch.cuda.CUDAGraph()
         cap = torch.cuda.Stream()
         with torch.cuda.stream(cap):
-            sets[1]["dev_in"].copy_(self.host_in)       # warm the second set once, outside the graph
-            self._call_on(sets[1], 0, cap)
+            for b in sets[1:]:
+                b["dev_in"].copy_(self.host_in)         # warm the other sets once, outside the graph
+                self._call_on(b, 0, cap)
         cap.synchronize()
         with torch.cuda.graph(g, stream=cap):
             for s in streams:
                 s.wait_stream(cap)
             for i in range(steps):
-                s, b = streams[i % 2], sets[i % 2]
+                s, b = streams[i % nstreams], sets[i % nstreams]
                 with torch.cuda.stream(s):
                     b["dev_in"].copy_(self.host_in, non_blocking=True)
                     self._call_on(b, i, s)
@@ -645,9 +696,24 @@ class DecodeRig:
         return e2e_s, parts, eager_us
 
 
-def decode_summary(rig, el_ms, steps, spot, peak, single_us=None, repeats=None):
+# independent calls per timed region of DecodeRig.time_streams
+CONCURRENT_CALLS = 400
+
+
+def concurrent(rig, us, nstreams, peak):
+    """The record of DecodeRig.time_streams: independent calls on several streams, inputs resident."""
+    gbs = rig.bpc / (us * 1e-6) / 1e9
+    return {"streams": nstreams, "calls": CONCURRENT_CALLS, "us_per_call": round(us, 3), "value": round(gbs, 2),
+            "frac": round(gbs / peak, 4),
+            "what": "independent calls taken in turn by the streams, each stream with its own output and scratch, "
+                    "inputs resident; calls on different streams run at once, so this is throughput, not one "
+                    "call's duration; the line's value and roofline are the one-stream period"}
+
+
+def decode_summary(rig, el_ms, steps, spot, peak, single_us=None, repeats=None, conc=None):
     """Per-workload record: device time per call, GB/s, roofline fraction, splits, parity, traffic; with
-    them, the latency of one call alone and the per-call time of repeated timed regions."""
+    them, the latency of one call alone, the per-call time of repeated timed regions and the throughput
+    of independent calls on several streams."""
     c = rig.case
     us = el_ms * 1e3 / steps
     gbs = rig.bpc / (us * 1e-6) / 1e9
@@ -659,6 +725,8 @@ def decode_summary(rig, el_ms, steps, spot, peak, single_us=None, repeats=None):
         r["single_call_us"] = round(single_us, 3)
     if repeats is not None:
         r["us_per_call_repeats"] = repeats
+    if conc is not None:
+        r["concurrent_streams"] = conc
     return r
 
 
@@ -701,6 +769,7 @@ def run_ours(args, case, rank, world, dist):
     clocks = sampler.stop() if sampler else None
     single_us = rig.time_single()
     repeats = rig.time_repeats(args.steps, chunk)
+    conc_us = rig.time_streams(CONCURRENT_CALLS, args.e2e_streams)
     el_max = max_over_ranks(dist, el_ms)
     ms_per_step = el_max / args.steps
     value = sum_over_ranks(dist, float(rig.bpc) * args.steps) / (el_max * 1e-3) / 1e9
@@ -708,7 +777,7 @@ def run_ours(args, case, rank, world, dist):
     # split kernel's tail (programmatic dependent launch), so they are timed together
     kernel_us = el_ms * 1e3 / args.steps
     e2e_steps = max(1, args.e2e_steps)
-    e2e_s, host_parts, eager_us = rig.time_e2e(e2e_steps, dist)
+    e2e_s, host_parts, eager_us = rig.time_e2e(e2e_steps, dist, args.e2e_streams)
     e2e_value = sum_over_ranks(dist, float(rig.bpc) * e2e_steps) / e2e_s / 1e9
 
     # the other decode configurations, same protocol, reported inside the one line
@@ -722,7 +791,9 @@ def run_ours(args, case, rank, world, dist):
             ms2, ch2 = r2.time_steps(args.steps, args.warmup, args.graph_chunk, dist)
             ms2 = max_over_ranks(dist, ms2)
             extra.append(decode_summary(r2, ms2, args.steps, sp2, peak, r2.time_single(),
-                                        r2.time_repeats(args.steps, ch2)))
+                                        r2.time_repeats(args.steps, ch2),
+                                        concurrent(r2, r2.time_streams(CONCURRENT_CALLS, args.e2e_streams),
+                                                   args.e2e_streams, peak)))
             del r2
             torch.cuda.empty_cache()
         for name in EXTRA_OTHER:
@@ -756,6 +827,7 @@ def run_ours(args, case, rank, world, dist):
     run["single_call_us"] = round(single_us, 3)
     run["single_call"] = "one call alone on an idle GPU, CUDA events around it, median of 30"
     run["us_per_call_repeats"] = repeats
+    run["concurrent_streams"] = concurrent(rig, conc_us, args.e2e_streams, peak)
     if spot is not None:
         run["spot_check_rel_rms"] = spot
     line = {
@@ -766,8 +838,10 @@ def run_ours(args, case, rank, world, dist):
         "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": rig.host_in.numel(),
                 "d2h_bytes_per_step": rig.o_h.numel() * rig.o_h.element_size(),
                 "steps": e2e_steps, "us_per_step": round(e2e_s / e2e_steps * 1e6, 3),
-                "mode": "one CUDA graph of the steps on two streams with two buffer sets: each step copies its "
-                        "inputs in, calls attn_decode and copies o out; one step's copies overlap the other's kernel",
+                "mode": f"one CUDA graph of the steps taken in turn by {args.e2e_streams} streams, each with its "
+                        "own buffer set: each step copies its inputs in, calls attn_decode and copies o out; one "
+                        "step's copies overlap other steps' kernels",
+                "streams": args.e2e_streams,
                 "eager_us_per_step": round(eager_us, 3), "host_us_per_part": host_parts,
                 "resident": "k_pool and v_pool stay in HBM (the KV cache); q, qpos, off and the block table come "
                             "from pinned host memory (one copy) and o goes back (one copy) every step"},
@@ -1322,6 +1396,8 @@ def main(argv=None):
     ap.add_argument("--graph-chunk", type=int, default=2000)
     ap.add_argument("--copies", type=int, default=0, help="override the number of rotated pool copies")
     ap.add_argument("--e2e-steps", type=int, default=2000)
+    ap.add_argument("--e2e-streams", type=int, default=6,
+                    help="decode e2e: streams (each with its own buffers) that take the steps in turn")
     ap.add_argument("--cpu-budget", type=float, default=10.0, help="seconds of oracle work for cpu_baseline")
     ap.add_argument("--ref-budget", type=float, default=60.0, help="seconds of oracle work for --impl reference")
     ap.add_argument("--no-cpu-baseline", action="store_true")
