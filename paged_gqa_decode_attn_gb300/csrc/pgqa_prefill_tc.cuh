@@ -31,9 +31,12 @@
 //     window, agree on the row max through shared memory, run the online
 //     softmax in log2 units, rescale their quarter of O in TMEM only when the
 //     row's running max grows by more than 2^8 (exact in real arithmetic: P
-//     then stays below 256), write their quarter of P_j as bf16 into shared
-//     memory (the A operand of the PV MMA), and at the end divide their
-//     quarter of O by the row sum and store bf16.
+//     then stays below 256), write their quarter of P_j as bf16 (the A
+//     operand of the PV MMA), and at the end divide their quarter of O by the
+//     row sum and store bf16 -- or, split-KV, the unnormalised partial;
+//   * P_j goes into the first half of S_j's own TMEM buffer, the PV MMA's A
+//     operand: the buffer takes S_{j+2} once PV_j is done, and P_j waits for
+//     no PV (a single shared-memory P buffer had to wait for PV_{j-1}).
 //
 // Every wait is bounded; a thread that gives up skips its later waits and
 // every role still reaches the final barrier, which frees the tensor memory.
@@ -133,6 +136,13 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16
         "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
         "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
         : "memory");
+}
+
+__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&r)[8])
+{
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(taddr), "r"(r[0]),
+                 "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
+                 : "memory");
 }
 
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
@@ -240,15 +250,13 @@ struct TcGeo {
     static constexpr int kBlockPages = 4;
     static constexpr int kBlockTokens = kBlockPages * kPage;   // 64: S columns per block
     static constexpr int kChunks = kHdc / 64;          // 128-byte swizzle rows per head vector (this CTA's dims)
-    static constexpr int kPBytes = kRows * 128;                // [128 rows][128 B: 64 tokens]
     static constexpr int kKBytes = kChunks * kBlockTokens * 128;           // [chunk][64 tokens][128 B]
     static constexpr int kVPage = kChunks * kPage * 128;                   // [chunk][16 tokens][128 B]
     static constexpr int kVBytes = kBlockPages * kVPage;
     static constexpr int kStageBytes = kKBytes + kVBytes;
     // 192 KB of K/V in flight; 128 KB beside the S exchange buffers of a pair
     static constexpr int kStages = ((kSplitDims ? 128 : 192) * 1024) / kStageBytes;
-    static constexpr int kPOff = 0;
-    static constexpr int kStageOff = kPOff + kPBytes;
+    static constexpr int kStageOff = 0;
     static constexpr int kSoftmaxWarps = 16;           // four threads per query row
     static constexpr int kParts = kSoftmaxWarps / 4;   // threads per row, each over 1/kParts of the columns
     static constexpr int kXOff = kStageOff + kStages * kStageBytes;   // row max [2][parts][128], row sum [parts][128]
@@ -262,8 +270,8 @@ struct TcGeo {
     static constexpr int kSxBytes = kSplitDims ? 2 * kRows * kBlockTokens * 4 : 0;
     static constexpr int kBarOff = kSxOff + kSxBytes;
     // k_full[stages], k_empty[stages], v_full[stages], v_empty[stages], s_full[2], s_free[2],
-    // p_full, o_done, q_ready, o_free, info_full[2], info_empty[2], then (split dims) x_full[2]
-    static constexpr int kBars = 4 * kStages + 12 + (kSplitDims ? 2 : 0);
+    // p_full[2], o_done, q_ready, o_free, info_full[2], info_empty[2], o_item, then (split dims) x_full[2]
+    static constexpr int kBars = 4 * kStages + 14 + (kSplitDims ? 2 : 0);
     static constexpr int kSlotOff = kBarOff + kBars * 8;
     static constexpr int kTotal = kSlotOff + 16;
     static constexpr int kAlloc = kTotal + 1024;
@@ -277,7 +285,7 @@ struct TcGeo {
     static constexpr int kQCol = kOCol + kHdc;
     static_assert(kQCol + kHdc / 2 <= kTmemCols, "tensor memory");
     static_assert(kAlloc <= 227 * 1024, "shared memory");
-    static_assert(kPBytes % 1024 == 0 && kStageBytes % 1024 == 0, "swizzle atoms");
+    static_assert(kStageBytes % 1024 == 0, "swizzle atoms");
 };
 
 // One work item: the 128 query rows of chunk `chunk` of tile `tile` for kv
@@ -432,7 +440,6 @@ __global__ void __launch_bounds__(TcGeo<HD>::kThreads, 1)
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t s_base = smem_u32(smem);
-    const uint32_t sP = s_base + G::kPOff;
     const uint32_t s_bar = s_base + G::kBarOff;
     // a stage's K and V halves fill and free apart: K is free once its S
     // batch is done, about a block before the PV batch frees V
@@ -442,13 +449,21 @@ __global__ void __launch_bounds__(TcGeo<HD>::kThreads, 1)
     const uint32_t b_vempty = s_bar + 24 * NST;        // [NST]
     const uint32_t b_sfull = s_bar + 32 * NST;         // [2]
     const uint32_t b_sfree = b_sfull + 16;             // [2]
-    const uint32_t b_pfull = b_sfree + 16;
-    const uint32_t b_odone = b_pfull + 8;
+    // P_j is in S_j's buffer: one p_full per buffer.  A softmax warp that runs a
+    // block ahead of the others (nothing holds it to PV_{j-1}) then arrives on
+    // the other buffer's barrier; it reaches this one again (block j + 2) only
+    // after S_{j+2}, so after PV_j has taken this phase.
+    const uint32_t b_pfull = b_sfree + 16;             // [2]
+    const uint32_t b_odone = b_pfull + 16;
     const uint32_t b_qready = b_odone + 8;
     const uint32_t b_ofree = b_qready + 8;
     const uint32_t b_ifull = b_ofree + 8;              // [2] a published item is in its slot
     const uint32_t b_iempty = b_ifull + 16;            // [2] every role has read it
-    const uint32_t b_xfull = b_iempty + 16;            // [2] split dims: the peer's half of S_j is here
+    // an item's last PV batch is done (one phase per item with blocks): the
+    // read-out of O waits on it.  o_done, a phase per block, cannot serve: by
+    // then it may be one phase past the item, and a parity wait would alias.
+    const uint32_t b_oitem = b_iempty + 16;
+    const uint32_t b_xfull = b_oitem + 8;              // [2] split dims: the peer's half of S_j is here
     const int2 *win = reinterpret_cast<const int2 *>(smem + G::kWinOff);
     uint32_t *tslot = reinterpret_cast<uint32_t *>(smem + G::kSlotOff);
 
@@ -481,10 +496,12 @@ __global__ void __launch_bounds__(TcGeo<HD>::kThreads, 1)
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(b_sfull + 8 * b, 1);
-            mbar_init(b_sfree + 8 * b, G::kSoftmaxWarps);
+            mbar_init(b_sfree + 8 * b, 1);          // PV_j's commit: S_j and P_j read
         }
-        mbar_init(b_pfull, G::kSoftmaxWarps);
+        for (int b = 0; b < 2; ++b)
+            mbar_init(b_pfull + 8 * b, G::kSoftmaxWarps);
         mbar_init(b_odone, 1);
+        mbar_init(b_oitem, 1);
         mbar_init(b_qready, G::kSoftmaxWarps);
         mbar_init(b_ofree, G::kSoftmaxWarps);
         for (int b = 0; b < 2; ++b) {
@@ -719,7 +736,7 @@ __global__ void __launch_bounds__(TcGeo<HD>::kThreads, 1)
                 for (int j = 0; j < I.nblocks; ++j) {
                     const int jj = jg + j, js = jj + qs, st = js % NST;
                     if (ok)
-                        ok = mbar_wait_bounded(b_pfull, jj & 1, p.err, kErrTimeoutFull);
+                        ok = mbar_wait_bounded(b_pfull + 8 * (jj & 1), (jj >> 1) & 1, p.err, kErrTimeoutFull);
                     if (ok && j == 0 && kq >= 1)            // the previous item's O has been read out
                         ok = mbar_wait_bounded(b_ofree, (kq - 1) & 1, p.err, kErrTimeoutFull);
                     // V_j has landed (the softmax has waited for it already where it
@@ -730,12 +747,18 @@ __global__ void __launch_bounds__(TcGeo<HD>::kThreads, 1)
                     if (ok) {
                         const uint32_t sV = s_base + G::kStageOff + st * G::kStageBytes + G::kKBytes;
                         const int np = min(G::kBlockPages, I.npages - j * G::kBlockPages);
+                        // P_j: 16 tokens of page pp are 8 columns of S_j's buffer
+                        const uint32_t tP = tbase + (jj & 1) * G::kBlockTokens;
                         for (int pp = 0; pp < np; ++pp)
-                            umma_bf16(tbase + G::kOCol, umma_sdesc(sP + pp * 32, 16, 1024),
-                                      umma_sdesc(sV + pp * G::kVPage, kPage * 128, 1024), kIdO, j > 0 || pp > 0);
+                            umma_bf16_tmem_a(tbase + G::kOCol, tP + pp * 8,
+                                             umma_sdesc(sV + pp * G::kVPage, kPage * 128, 1024), kIdO,
+                                             j > 0 || pp > 0);
                     }
                     umma_commit(b_odone);
                     umma_commit(b_vempty + 8 * st);
+                    umma_commit(b_sfree + 8 * (jj & 1));    // S_j's buffer, P_j with it, is free
+                    if (j == I.nblocks - 1)
+                        umma_commit(b_oitem);
                 }
             }
             __syncwarp();
@@ -761,15 +784,19 @@ __global__ void __launch_bounds__(TcGeo<HD>::kThreads, 1)
         // the finish of an item: the row sum over the parts, O / l in bf16
         // (this part's dims) -- or, split, the unnormalised partial (m, L, O)
         // -- then O is free for the next item
-        auto finish = [&](int last_jg, size_t frh, bool fva, float fl, float fm, int fsplit) {
+        int kfin = 0;               // items whose O has been read out
+        auto finish = [&](size_t frh, bool fva, float fl, float fm, int fsplit) {
             xsum[part * G::kRows + row] = fl;
             group_bar_sync(pair_bar, 32 * NP);
             float lt = xsum[row];
 #pragma unroll
             for (int k = 1; k < NP; ++k)
                 lt += xsum[k * G::kRows + row];
+            // every PV of the item is done (phase kfin of o_item: the items with
+            // blocks in order; the next item's cannot end before this read-out)
             if (ok)
-                ok = mbar_wait_bounded(b_odone, last_jg & 1, p.err, kErrTimeoutFull);
+                ok = mbar_wait_bounded(b_oitem, kfin & 1, p.err, kErrTimeoutFull);
+            ++kfin;
             tc_fence_after();
             const bool split_out = p.splits > 1;
             const size_t prow = frh * p.splits + fsplit;
@@ -837,7 +864,6 @@ __global__ void __launch_bounds__(TcGeo<HD>::kThreads, 1)
         };
 
         bool pend = false;          // an item whose O has not been read out yet
-        int pend_jg = 0;
         size_t pend_rh = 0;
         bool pend_va = false;
         float pend_l = 0.f, pend_m = -INFINITY;
@@ -950,7 +976,7 @@ __global__ void __launch_bounds__(TcGeo<HD>::kThreads, 1)
                     mbar_arrive(b_qready);
             }
             if (pend)
-                finish(pend_jg, pend_rh, pend_va, pend_l, pend_m, pend_split);
+                finish(pend_rh, pend_va, pend_l, pend_m, pend_split);
 
             float m = -INFINITY, l = 0.f;
             for (int j = 0; j < I.nblocks; ++j) {
@@ -966,9 +992,6 @@ __global__ void __launch_bounds__(TcGeo<HD>::kThreads, 1)
                               *reinterpret_cast<uint32_t(*)[16]>(sr + q4 * 16));
                 tmem_wait_ld();
                 tc_fence_before();
-                __syncwarp();
-                if (lane == 0)
-                    mbar_arrive(b_sfree + 8 * b);
                 if constexpr (kSplit) {
                     // The pair's halves of S_j: this thread's 16 columns go to the
                     // peer, the peer's come here, and the two are added.  a + b is
@@ -1049,11 +1072,16 @@ __global__ void __launch_bounds__(TcGeo<HD>::kThreads, 1)
                 l = __fmaf_rn(l, alpha, (lq[0] + lq[1]) + (lq[2] + lq[3]));     // this part's share
                 m = m_use;
 
-                // O and the P buffer are free once the previous block's PV is done
-                if (j >= 1 && ok)
+                // O may be rescaled once the previous block's PV is done.  P_j goes
+                // where S_j was, so it waits for nothing more: PV_{j-2}, the
+                // buffer's last reader, was done before S_j was issued into it, and
+                // every part of the row has read S_j (the row-max barrier above).
+                // PV_j needs P_j, so b_odone has not passed PV_{j-1} here.
+                const bool rescale = j >= 1 && __any_sync(0xffffffffu, alpha != 1.f);
+                if (rescale && ok)
                     ok = mbar_wait_bounded(b_odone, (jj - 1) & 1, p.err, kErrTimeoutFull);
                 tc_fence_after();
-                if (j >= 1 && __any_sync(0xffffffffu, alpha != 1.f)) {
+                if (rescale) {
 #pragma unroll 1
                     for (int c0 = part * HO; c0 < (part + 1) * HO; c0 += kRs) {
                         uint32_t ra[kRs / 16][16];
@@ -1072,13 +1100,11 @@ __global__ void __launch_bounds__(TcGeo<HD>::kThreads, 1)
                     }
                     tmem_wait_st();
                 }
-                // this part of the P row -> shared memory, 128-byte swizzle
-#pragma unroll
-                for (int w = 0; w < HC / 8; ++w) {
-                    const int u = part * (HC / 8) + w;
-                    *reinterpret_cast<uint4 *>(smem + G::kPOff + row * 128 + ((u ^ (row & 7)) << 4)) =
-                        make_uint4(pk[4 * w], pk[4 * w + 1], pk[4 * w + 2], pk[4 * w + 3]);
-                }
+                // this part of the P row -> tensor memory, tokens (2c, 2c + 1) of the
+                // block in column c of S_j's buffer (the low half the lower token)
+                static_assert(HC == 16, "P: eight columns per part");
+                tmem_st8(trow + b * G::kBlockTokens + part * (HC / 2), pk);
+                tmem_wait_st();
                 // V rows of tokens outside the union window may hold anything (NaN
                 // included) and P is 0 there: zero them before the PV MMA reads them
                 const int btok0 = (I.p_first + j * G::kBlockPages) * kPage;
@@ -1101,10 +1127,9 @@ __global__ void __launch_bounds__(TcGeo<HD>::kThreads, 1)
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0)
-                    mbar_arrive(b_pfull);
+                    mbar_arrive(b_pfull + 8 * b);
             }
             pend = true;
-            pend_jg = jg + I.nblocks - 1;
             pend_rh = rh;
             pend_va = va;
             pend_l = l;
@@ -1113,7 +1138,7 @@ __global__ void __launch_bounds__(TcGeo<HD>::kThreads, 1)
             jg += I.nblocks;
         }
         if (pend)
-            finish(pend_jg, pend_rh, pend_va, pend_l, pend_m, pend_split);
+            finish(pend_rh, pend_va, pend_l, pend_m, pend_split);
     }
     // split dims: neither CTA of the pair leaves while the other may still
     // write into its shared memory
@@ -1168,11 +1193,10 @@ cudaError_t launch_prefill_tc(const PrefillLaunchArgs &a, bool set_attr)
 {
     using G = TcGeo<HD>;
     if (set_attr) {
-        cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel<HD, false>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, G::kAlloc);
-        if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(prefill_tc_kernel<HD, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     G::kAlloc);
+        cudaError_t e = cudaSuccess;
+        for (auto kern : {prefill_tc_kernel<HD, false>, prefill_tc_kernel<HD, true>})
+            if (e == cudaSuccess)
+                e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, G::kAlloc);
         if (e != cudaSuccess)
             return e;
     }
@@ -1210,11 +1234,9 @@ cudaError_t launch_prefill_tc(const PrefillLaunchArgs &a, bool set_attr)
     cfg.attrs = attr;
     cfg.numAttrs = na;
     // without a Q map the kernel never reads tm_q: K's map fills the parameter
-    if (a.tm_q)
-        return cudaLaunchKernelEx(&cfg, prefill_tc_kernel<HD, true>, *a.tm_k, *a.tm_v, *a.tm_q, a.p, a.ntiles,
-                                  nchunks);
-    return cudaLaunchKernelEx(&cfg, prefill_tc_kernel<HD, false>, *a.tm_k, *a.tm_v, *a.tm_k, a.p, a.ntiles,
-                              nchunks);
+    const CUtensorMap &tq = a.tm_q ? *a.tm_q : *a.tm_k;
+    auto kern = a.tm_q ? prefill_tc_kernel<HD, true> : prefill_tc_kernel<HD, false>;
+    return cudaLaunchKernelEx(&cfg, kern, *a.tm_k, *a.tm_v, tq, a.p, a.ntiles, nchunks);
 }
 
 }  // namespace pgqa
