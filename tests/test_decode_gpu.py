@@ -259,6 +259,38 @@ def test_repeated_calls_and_streams_are_deterministic():
     assert int(d.cnt.abs().sum().item()) == 0
 
 
+@pytest.mark.parametrize("make,splits,counters", [
+    (lambda: wl.sliding(), 8, True),                                            # cluster merge
+    (lambda: wl.page_case(32, 4, 512, 0, 3000, 1, dist="sym", seed=9), 19, False),   # combine kernel
+    (lambda: wl.page_case(32, 4, 512, 0, 3000, 1, dist="sym", seed=9), 6, True),     # last-CTA merge
+], ids=["cluster8", "combine19", "lastcta6"])
+def test_independent_calls_on_several_streams_match_one_stream(make, splits, counters):
+    """Independent calls taken in turn by four streams, each stream with its own output, scratch and
+    counters and nothing between the launches (as the bench's concurrent and end-to-end runs issue
+    them), give the bits of one call on one stream; every stream's counters end at zero."""
+    import torch
+    import paged_gqa_decode_attn_gb300 as pgqa
+    from gpu_util import DevCase, first_difference
+    c = make()
+    d = DevCase(c, splits)
+    ref = d.result(counters=counters)
+    streams = [torch.cuda.Stream() for _ in range(4)]
+    sets = [(torch.empty_like(d.o), torch.zeros_like(d.part), torch.zeros_like(d.cnt)) for _ in streams]
+    torch.cuda.synchronize()
+    for i in range(12):
+        s = streams[i % 4]
+        o, part, cnt = sets[i % 4]
+        with torch.cuda.stream(s):
+            pgqa.attn_decode(o, part, d.q, d.k, d.v, d.bt, d.off, d.qpos, d.kvpos, c.rows, c.nh, c.nkv, c.hd,
+                             c.window, splits, cnt if counters else None, d.pm, s)
+    torch.cuda.synchronize()
+    pgqa.device_status()
+    for o, _, cnt in sets:
+        got = o.cpu().numpy().view(np.uint16).reshape(ref.shape)
+        assert np.array_equal(got, ref), first_difference(got, ref)
+        assert int(cnt.abs().sum().item()) == 0
+
+
 def test_zero_rows_is_a_no_op():
     import torch
     import paged_gqa_decode_attn_gb300 as pgqa
